@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Benchmark: tokens/s and ms per gdr_chunk_fwd call on one GB300, with the
+roofline fraction of the dominant kernel.
+
+One step is one gdr_chunk_fwd call (the whole forward path: chunk indexing,
+gate cumsum, Gram / inverse / WY factors, state scan, output) over one batch
+of the wide varlen workload (32 packed sequences of 128..512 tokens, H=16,
+K=V=128, BF16 q/k/v), inputs resident in HBM.  L2 is flushed (a 256 MiB
+write) between timed steps, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdr|reference]
+
+--impl reference times the FP64 CPU oracle (the slow reference program) on a
+bounded sample of the same workload.  Under torchrun every rank runs an
+independent replica (the path needs no exchange between GPUs); rank 0
+prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s and ms per gdr_chunk_fwd call on 1 GB300; % of roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "wide_varlen_bf16"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gdr", "reference"], default="gdr")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--segments", type=int, default=0)
+    ap.add_argument("--force-path", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# environment: ranks, peaks, clocks
+# ----------------------------------------------------------------------------
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    p = dict(FALLBACK_PEAKS)
+    p["source"] = "fallback"
+    return p
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.gpu_index is not None:
+                cmd += ["-i", str(self.gpu_index)]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def gpu_index_for_smi():
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local < len(ids):
+            return ids[local]
+    return local
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes per kernel launch (units: token-heads, chunk-heads,
+# sequence-heads; figures stated in DESIGN.md "Measurement")
+# ----------------------------------------------------------------------------
+def counts(x):
+    import torch
+    H = x["H"]
+    if x["cu_seqlens"] is not None:
+        lens = (x["cu_seqlens"][1:] - x["cu_seqlens"][:-1]).tolist()
+    else:
+        lens = [x["T"]] * x["B"]
+    chunks = sum((L + 63) // 64 for L in lens)
+    return dict(tokens=sum(lens), token_heads=sum(lens) * H, chunk_heads=chunks * H,
+                seq_heads=len(lens) * H, n_seqs=len(lens), chunks=chunks)
+
+
+def algorithmic_bytes(kernel, x, c):
+    K, V = x["K"], x["V"]
+    es = 2 if x["dtype"] == "bf16" else 4
+    delta = x["beta"] is not None
+    th, ch, sh = c["token_heads"], c["chunk_heads"], c["seq_heads"]
+    states = sh * K * V * 4 * ((1 if x["h0"] is not None else 0) + 1)
+    if kernel == "call":  # whole forward pass: inputs once, outputs once
+        return th * ((2 * K + V) * es + 4 + (4 if delta else 0) + V * es) + states
+    if kernel == "simt_prep":
+        b = th * 4 + ch * 64 * 4
+        if delta:
+            b += th * ((K + V) * es + 4) + ch * 64 * (K + V) * 4
+        return b
+    if kernel in ("simt_scan_serial", "simt_scan_segment_out"):
+        b = th * K * es + ch * 64 * 4 + ch * K * V * 4
+        b += (ch * 64 * (K + V) * 4 + ch * 64 * V * 4) if delta else th * V * es
+        return b + (states if kernel == "simt_scan_serial" else sh * K * V * 4)
+    if kernel == "simt_output":
+        return (th * 2 * K * es + ch * K * V * 4 + ch * 64 * 4 + th * V * es
+                + (ch * 64 * V * 4 if delta else th * V * es))
+    return None
+
+
+def traffic_record(kernel, workload):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = source_hash()
+    for line in open(path):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if (f.get("kernel") == kernel and f.get("workload") == workload
+                and f.get("source_sha") == src):
+            return float(f["dram_bytes_per_launch"])
+    return None
+
+
+def source_hash():
+    import glob
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "chunked_gated_delta_rule_gb300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (reported baseline / reference arm)
+# ----------------------------------------------------------------------------
+def oracle_inputs(x):
+    import numpy as np
+    import oracle
+    return {k: (oracle._f64(v) if k in ("q", "k", "v", "g", "beta", "h0") else v)
+            for k, v in x.items()}
+
+
+def time_oracle_on(xo, seqs):
+    """Runs the oracle on the (sequence, head) pairs of `seqs` (all heads);
+    returns (seconds, tokens, threads)."""
+    import numpy as np
+    import oracle
+    N, H = xo["N"], xo["H"]
+    mask = np.zeros(N * H, dtype=bool)
+    for n in seqs:
+        mask[n * H:(n + 1) * H] = True
+    if xo["cu_seqlens"] is not None:
+        cu = xo["cu_seqlens"].tolist()
+        tokens = sum(cu[n + 1] - cu[n] for n in seqs)
+    else:
+        tokens = xo["T"] * len(seqs)
+    t0 = time.perf_counter()
+    _, _, threads = oracle.forward(xo["q"], xo["k"], xo["v"], xo["g"], xo["beta"],
+                                   cu_seqlens=xo["cu_seqlens"], h0=xo["h0"],
+                                   pair_mask=mask, want_ht=True)
+    return time.perf_counter() - t0, tokens, threads
+
+
+def cpu_baseline(x, budget_s):
+    """Times the oracle over groups of 4 sequences (all heads), cycling
+    through the batch, until about `budget_s` seconds of CPU work (at most
+    8 passes over the batch)."""
+    xo = oracle_inputs(x)
+    N = xo["N"]
+    secs, toks, threads, groups = 0.0, 0, 1, 0
+    n = 0
+    while secs < budget_s and n < 8 * N:
+        group = [(n + j) % N for j in range(min(4, N))]
+        dt, tk, threads = time_oracle_on(xo, group)
+        secs += dt
+        toks += tk
+        groups += 1
+        n += len(group)
+    return {"value": toks / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{groups} groups of 4 sequences x all {xo['H']} heads cycling over "
+                      f"the {N}-sequence batch ({toks} tokens), FP64 token recurrence, "
+                      f"{secs:.1f} s"}
+
+
+def run_reference(args):
+    from chunked_gated_delta_rule_gb300 import synthetic
+    rank, _, world = int(os.environ.get("RANK", "0")), 0, int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    w = synthetic.WORKLOADS[args.workload]
+    x = synthetic.make_inputs(w)
+    xo = oracle_inputs(x)
+    N = xo["N"]
+    per_step = 1 if N >= 1 else 0
+    times, toks, threads = [], [], 1
+    for i in range(args.warmup + args.steps):
+        seqs = [(i * per_step + j) % N for j in range(per_step)]
+        dt, tk, threads = time_oracle_on(xo, seqs)
+        if i >= args.warmup:
+            times.append(dt)
+            toks.append(tk)
+    value = sum(toks) / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(args, x, None),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"each step one sequence x all {xo['H']} heads of the "
+                                       "workload (cycling), FP64 token recurrence"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(args, x, plan):
+    c = {"workload": args.workload, "tokens": None, "n_seqs": x["N"], "H": x["H"],
+         "K": x["K"], "V": x["V"], "input_dtype": x["dtype"],
+         "beta_free": x["beta"] is None, "h0": x["h0"] is not None,
+         "l2": "flushed between timed steps (256 MiB write, untimed)"}
+    c["tokens"] = counts(x)["tokens"]
+    if plan is not None:
+        c["plan"] = plan
+    return c
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_gdr(args):
+    import torch
+    import chunked_gated_delta_rule_gb300 as pkg
+    from chunked_gated_delta_rule_gb300 import synthetic
+
+    rank, local, world = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synthetic.WORKLOADS[args.workload]
+    x = synthetic.make_inputs(w)
+    c = counts(x)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+    o = torch.empty_like(d["v"])
+    ht = torch.empty(c["n_seqs"], x["H"], x["K"], x["V"], dtype=torch.float32, device=dev)
+    kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], o=o, ht=ht, n_segments=args.segments,
+              force_path=args.force_path)
+    args_t = (d["q"], d["k"], d["v"], d["g"], d["beta"])
+    plan = pkg.gdr_plan_query(x["B"], x["T"], x["H"], x["K"], x["V"], N=x["N"] if
+                              x["cu_seqlens"] is not None else 0,
+                              dtype=0 if x["dtype"] == "f32" else 1,
+                              beta_free=x["beta"] is None, n_segments=args.segments)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(max(3, args.warmup)):
+        pkg.gdr_chunk_fwd(*args_t, **kw)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    timers = [pkg.LaunchTimer(16) for _ in range(K)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_index_for_smi()) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        pkg.gdr_chunk_fwd(*args_t, timer=timers[i], **kw)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = statistics.mean(step_ms)
+    ms = max_over_ranks(ms_local, world)
+    per_kernel = {}
+    launches = 0
+    for t in timers:
+        launches += t.count
+        for i, kid in enumerate(t.ids):
+            name = pkg.gdr_kernel_name(kid)
+            per_kernel.setdefault(name, []).append(t.elapsed_ms(i))
+    kernels = {n: {"launches": len(v), "avg_ms": statistics.mean(v),
+                   "share": sum(v) / sum(step_ms)} for n, v in per_kernel.items()}
+    dom = max(per_kernel, key=lambda n: sum(per_kernel[n]))
+    peaks = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    ab = algorithmic_bytes(dom, x, c)
+    dom_ms = statistics.mean(per_kernel[dom])
+    achieved = ab / (dom_ms * 1e-3) / 1e9 if ab else None
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm if achieved else None,
+                "traffic": traffic_record(dom, args.workload),
+                "algorithmic_bytes_per_launch": ab, "avg_launch_ms": dom_ms,
+                "peak_source": peaks["source"] + " (hbm_gbs, copy bandwidth)"}
+    call_bytes = algorithmic_bytes("call", x, c)
+    call_roofline = {"achieved": call_bytes / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": call_bytes / (ms * 1e-3) / 1e9 / hbm,
+                     "algorithmic_bytes": call_bytes}
+
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()}
+        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        ht_h = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
+        hargs = (pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"])
+        hkw = dict(cu_seqlens=pin["cu_seqlens"], h0=pin["h0"], o=o_h, ht=ht_h,
+                   n_segments=args.segments)
+        for _ in range(3):
+            pkg.gdr_chunk_fwd_host(*hargs, **hkw)
+        ke = max(3, min(K, 50))
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            pkg.gdr_chunk_fwd_host(*hargs, **hkw)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world)
+        h2d = sum(t.numel() * t.element_size() for t in
+                  [pin[k] for k in ("q", "k", "v", "g", "beta", "cu_seqlens", "h0")]
+                  if t is not None)
+        d2h = o_h.numel() * o_h.element_size() + ht_h.numel() * ht_h.element_size()
+        e2e = {"value": world * c["tokens"] / (e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "steps": ke, "api": "gdr_chunk_fwd_host (pinned host buffers)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": world * c["tokens"] / (ms * 1e-3), "unit": UNIT,
+                "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None,
+                "dtype": "f32" if plan["path"] == 1 else "bf16",
+                "data": "synthetic (seeded; shapes and distributions of the workload)",
+                "config": config_of(args, x, plan),
+                "roofline": roofline, "call_roofline": call_roofline,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "kernels": kernels, "clocks": clocks,
+                "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
+                            "p10": sorted(step_ms)[len(step_ms) // 10],
+                            "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]}}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gdr(args)
+
+
+if __name__ == "__main__":
+    main()

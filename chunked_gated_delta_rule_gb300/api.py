@@ -1,0 +1,264 @@
+"""ctypes binding of ``include/gdr.h``: argument marshalling only.
+
+Every step of the forward pass runs in the CUDA library; these functions pass
+tensor pointers, sizes and the current CUDA stream across the C ABI.  If the
+library has not been built (``__graft_entry__.build()``), every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+GDR_F32, GDR_BF16 = 0, 1
+
+
+class gdr_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("V", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class gdr_plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("bv", ctypes.c_int32),
+                ("n_segments", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class gdr_options(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("force_path", ctypes.c_int32),
+                ("force_bv", ctypes.c_int32), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("status", ctypes.c_void_p),
+                ("events", ctypes.c_void_p), ("max_launches", ctypes.c_int32),
+                ("launch_ids", ctypes.c_void_p), ("n_launches", ctypes.c_void_p)]
+
+
+# Every symbol include/gdr.h declares.
+EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_host",
+           "gdr_workspace_size", "gdr_plan_query", "gdr_kernel_name", "gdr_error_string",
+           "gdr_version")
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library():
+    """Open ``libgdr.so``.  Raises if it has not been built: there is no
+    fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        vp, i32p = ctypes.c_void_p, ctypes.c_void_p
+        dims_p = ctypes.POINTER(gdr_dims)
+        fwd_args = [dims_p, vp, vp, vp, vp, vp, i32p, vp, vp, vp, ctypes.c_int]
+        lib.gdr_chunk_fwd.argtypes = fwd_args + [vp]
+        lib.gdr_chunk_fwd.restype = ctypes.c_int
+        lib.gdr_chunk_fwd_ex.argtypes = fwd_args + [ctypes.POINTER(gdr_options), vp]
+        lib.gdr_chunk_fwd_ex.restype = ctypes.c_int
+        lib.gdr_chunk_fwd_host.argtypes = fwd_args + [vp]
+        lib.gdr_chunk_fwd_host.restype = ctypes.c_int
+        lib.gdr_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.c_int]
+        lib.gdr_workspace_size.restype = ctypes.c_size_t
+        lib.gdr_plan_query.argtypes = [dims_p, ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(gdr_plan)]
+        lib.gdr_plan_query.restype = ctypes.c_int
+        lib.gdr_kernel_name.argtypes = [ctypes.c_int]
+        lib.gdr_kernel_name.restype = ctypes.c_char_p
+        lib.gdr_error_string.argtypes = [ctypes.c_int]
+        lib.gdr_error_string.restype = ctypes.c_char_p
+        lib.gdr_version.argtypes = []
+        lib.gdr_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+class GdrError(RuntimeError):
+    def __init__(self, code: int):
+        msg = load_library().gdr_error_string(code).decode()
+        super().__init__(f"gdr error {code}: {msg}")
+        self.code = code
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return GDR_F32
+    if t == torch.bfloat16:
+        return GDR_BF16
+    raise TypeError(f"unsupported dtype {t}: q, k, v must be float32 or bfloat16")
+
+
+def make_dims(B, T, H, K, V, N=0, dtype=GDR_BF16) -> gdr_dims:
+    return gdr_dims(B, T, H, K, V, N, dtype, 0)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dims_of(q, v, cu_seqlens) -> gdr_dims:
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    return make_dims(B, T, H, K, V, N, _dtype_code(q.dtype))
+
+
+def _check(name, t, dtype, device=None):
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+class LaunchTimer:
+    """Caller-side CUDA events for the per-launch timing hook of
+    gdr_chunk_fwd_ex (benchmarks).  After a call, ``ids[:count]`` are the
+    kernel ids launched and ``elapsed_ms(i)`` the duration of launch i once
+    the stream has been synchronised."""
+
+    def __init__(self, max_launches=16):
+        self.max = max_launches
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_launches)]
+        for e in self.events:  # torch creates the CUDA event on first record
+            e.record()
+        torch.cuda.current_stream().synchronize()
+        self._handles = (ctypes.c_void_p * (2 * max_launches))(
+            *[ctypes.c_void_p(e.cuda_event) for e in self.events])
+        self._ids = (ctypes.c_int32 * max_launches)()
+        self._count = ctypes.c_int32(0)
+
+    @property
+    def count(self):
+        return int(self._count.value)
+
+    @property
+    def ids(self):
+        return [int(self._ids[i]) for i in range(min(self.count, self.max))]
+
+    def elapsed_ms(self, i):
+        return self.events[2 * i].elapsed_time(self.events[2 * i + 1])
+
+
+def gdr_chunk_fwd(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments=0,
+                  output_final_state=True, o=None, ht=None, scale=0.0, force_path=0,
+                  force_bv=0, workspace=None, status=None, stream=None, timer=None):
+    """Forward pass on CUDA tensors (layouts of include/gdr.h).  Returns
+    ``(o, ht)``; ``ht`` is None unless ``output_final_state``.  Work is
+    enqueued on ``stream`` (default: torch's current stream) and not
+    synchronised.  ``timer`` (a :class:`LaunchTimer`) records events around
+    every kernel launch."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr_chunk_fwd takes CUDA tensors; use gdr_chunk_fwd_host for host buffers")
+    _check("q", q, None, dev)
+    for name, t in (("k", k), ("v", v)):
+        _check(name, t, q.dtype, dev)
+    _check("g", g, torch.float32, dev)
+    _check("beta", beta, torch.float32, dev)
+    _check("cu_seqlens", cu_seqlens, torch.int32, dev)
+    _check("h0", h0, torch.float32, dev)
+    dims = _dims_of(q, v, cu_seqlens)
+    nseq = dims.N if dims.N else dims.B
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    if ht is None and output_final_state:
+        ht = torch.empty(nseq, dims.H, dims.K, dims.V, dtype=torch.float32, device=dev)
+    _check("o", o, q.dtype, dev)
+    _check("ht", ht, torch.float32, dev)
+    opt = gdr_options(float(scale), int(force_path), int(force_bv),
+                      None if workspace is None else workspace.data_ptr(),
+                      0 if workspace is None else workspace.numel() * workspace.element_size(),
+                      None if status is None else status.data_ptr())
+    if timer is not None:
+        opt.events = ctypes.cast(timer._handles, ctypes.c_void_p)
+        opt.max_launches = timer.max
+        opt.launch_ids = ctypes.cast(timer._ids, ctypes.c_void_p)
+        opt.n_launches = ctypes.cast(ctypes.pointer(timer._count), ctypes.c_void_p)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdr_chunk_fwd_ex(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                  _ptr(beta), _ptr(cu_seqlens), _ptr(h0), _ptr(o), _ptr(ht),
+                                  int(n_segments), ctypes.byref(opt),
+                                  ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise GdrError(rc)
+    return o, ht
+
+
+def gdr_chunk_fwd_host(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments=0,
+                       output_final_state=True, o=None, ht=None, stream=None):
+    """Forward pass on HOST (CPU) tensors through ``gdr_chunk_fwd_host``: the
+    library copies inputs in, runs, copies o / ht out and synchronises.
+    Pinned tensors give asynchronous copies."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta),
+                    ("cu_seqlens", cu_seqlens), ("h0", h0)):
+        if t is not None and t.device.type != "cpu":
+            raise ValueError(f"{name} must be a host tensor")
+    _check("k", k, q.dtype)
+    _check("v", v, q.dtype)
+    _check("g", g, torch.float32)
+    _check("beta", beta, torch.float32)
+    _check("cu_seqlens", cu_seqlens, torch.int32)
+    _check("h0", h0, torch.float32)
+    dims = _dims_of(q, v, cu_seqlens)
+    nseq = dims.N if dims.N else dims.B
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype)
+    if ht is None and output_final_state:
+        ht = torch.empty(nseq, dims.H, dims.K, dims.V, dtype=torch.float32)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    rc = lib.gdr_chunk_fwd_host(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                _ptr(beta), _ptr(cu_seqlens), _ptr(h0), _ptr(o), _ptr(ht),
+                                int(n_segments), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise GdrError(rc)
+    return o, ht
+
+
+def gdr_workspace_size(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, n_segments=0) -> int:
+    return int(load_library().gdr_workspace_size(
+        ctypes.byref(make_dims(B, T, H, K, V, N, dtype)), int(bool(beta_free)), int(n_segments)))
+
+
+def gdr_plan_query(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, n_segments=0) -> dict:
+    plan = gdr_plan()
+    rc = load_library().gdr_plan_query(ctypes.byref(make_dims(B, T, H, K, V, N, dtype)),
+                                       int(bool(beta_free)), int(n_segments), ctypes.byref(plan))
+    if rc != 0:
+        raise GdrError(rc)
+    return dict(path=plan.path, bv=plan.bv, n_segments=plan.n_segments)
+
+
+def gdr_kernel_name(kid: int) -> str:
+    return load_library().gdr_kernel_name(int(kid)).decode()
+
+
+def gdr_error_string(code: int) -> str:
+    return load_library().gdr_error_string(int(code)).decode()
+
+
+def gdr_version() -> int:
+    return int(load_library().gdr_version())

@@ -1,0 +1,335 @@
+// gdr_api.cu -- host runtime behind include/gdr.h: argument validation, launch
+// plan (A13), workspace layout, and the launch sequence of the forward pass.
+#include <cmath>
+#include <cstring>
+
+#include "gdr_internal.cuh"
+
+namespace gdr {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kNumSMs = 152;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool is_varlen(const gdr_dims &d) { return d.N > 0; }
+int64_t n_seqs(const gdr_dims &d) { return is_varlen(d) ? d.N : d.B; }
+
+// Upper bound on the number of 64-token chunks: the chunk table is sized on
+// the host, before cu_seqlens (device data) is read.  Each sequence adds at
+// most one partial chunk.
+int64_t max_chunks_of(const gdr_dims &d) {
+    if (is_varlen(d)) return d.T / kChunk + d.N + 1;
+    return d.B * ((d.T + kChunk - 1) / kChunk);
+}
+
+int validate_dims(const gdr_dims *d) {
+    if (!d) return GDR_ERR_INVALID;
+    if (d->B < 1 || d->T < 0 || d->H < 1 || d->K < 1 || d->V < 1 || d->N < 0)
+        return GDR_ERR_INVALID;
+    if (d->dtype != GDR_F32 && d->dtype != GDR_BF16) return GDR_ERR_INVALID;
+    if (is_varlen(*d) && d->B != 1) return GDR_ERR_INVALID;
+    if (d->K % 16 || d->V % 16) return GDR_ERR_UNSUPPORTED;
+    if (d->K > kMaxK || d->V > kMaxV) return GDR_ERR_UNSUPPORTED;
+    if (d->H > 65535) return GDR_ERR_UNSUPPORTED;
+    if (d->B * d->T >= (int64_t)INT32_MAX) return GDR_ERR_UNSUPPORTED;
+    return GDR_OK;
+}
+
+// Value columns per scan CTA: the widest of 64/32/16 that divides both V and
+// K (the transition tiles of the segment pre-scan cover K columns) and keeps
+// the scan's shared memory within 227 KB.
+int pick_bv(const gdr_dims &d) {
+    for (int bv : {64, 32, 16}) {
+        if (d.V % bv || d.K % bv) continue;
+        const size_t smem = sizeof(float) * ((size_t)d.K * (bv + 1) +
+                                             2 * (size_t)kChunk * (d.K + 1) +
+                                             (size_t)kChunk * (bv + 1) + kChunk);
+        if (smem <= 227 * 1024) return bv;
+    }
+    return 16;
+}
+
+// Segment count when the caller passes 0: split long sequences until the
+// scan has about two CTAs per SM, at most 16 segments, and only while every
+// segment keeps at least 8 chunks.
+int auto_segments(const gdr_dims &d, int bv) {
+    const int64_t nseq = n_seqs(d);
+    const int64_t chunks_per_seq =
+        is_varlen(d) ? (d.N ? (d.T / d.N) / kChunk : 0) : (d.T + kChunk - 1) / kChunk;
+    const int64_t chains = nseq * d.H * (d.V / bv);
+    int S = 1;
+    while (S < 16 && chains * S < 2 * kNumSMs && chunks_per_seq / (2 * S) >= 8) S *= 2;
+    return S;
+}
+
+int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_options *opt,
+              gdr_plan *plan) {
+    (void)beta_free;
+    gdr_plan p{};
+    p.path = 1;
+    p.bv = pick_bv(d);
+    if (opt && opt->force_bv) {
+        const int bv = opt->force_bv;
+        if (bv != 16 && bv != 32 && bv != 64) return GDR_ERR_INVALID;
+        if (d.V % bv || d.K % bv) return GDR_ERR_UNSUPPORTED;
+        p.bv = bv;
+    }
+    if (opt && opt->force_path) {
+        if (opt->force_path != 1) return GDR_ERR_UNSUPPORTED;
+        p.path = opt->force_path;
+    }
+    if (n_segments < 0) return GDR_ERR_INVALID;
+    if (n_segments > kMaxSegments) return GDR_ERR_UNSUPPORTED;
+    p.n_segments = n_segments == 0 ? auto_segments(d, p.bv) : n_segments;
+    *plan = p;
+    return GDR_OK;
+}
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S) {
+    const bool delta = !beta_free;
+    const int64_t mc = max_chunks_of(d);
+    const int64_t ns = n_seqs(d);
+    const size_t H = (size_t)d.H, K = (size_t)d.K, V = (size_t)d.V;
+    WorkspaceLayout L{};
+    L.max_chunks = mc;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes);
+        return at;
+    };
+    L.off_tab = take(sizeof(int32_t) * 4 * (size_t)mc);
+    L.off_seq0 = take(sizeof(int32_t) * (size_t)(ns + 1));
+    L.off_nchunks = take(sizeof(int32_t));
+    L.off_G = take(sizeof(float) * (size_t)mc * H * kChunk);
+    L.off_W = take(delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
+    L.off_U = take(delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
+    L.off_hpre = take(sizeof(float) * (size_t)mc * H * K * V);
+    L.off_vnew = take(delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
+    const size_t segs = S > 1 ? (size_t)ns * H * (size_t)S : 0;
+    L.off_segM = take(delta ? sizeof(float) * segs * K * K : 0);
+    L.off_segC = take(sizeof(float) * segs * K * V);
+    L.off_segH = take(sizeof(float) * segs * K * V);
+    L.off_segD = take(delta ? 0 : sizeof(float) * segs);
+    L.total = off;
+    return L;
+}
+
+Workspace carve_workspace(void *base, const WorkspaceLayout &L, int S) {
+    char *b = static_cast<char *>(base);
+    Workspace w{};
+    w.chunk_tab = reinterpret_cast<int32_t *>(b + L.off_tab);
+    w.seq_chunk0 = reinterpret_cast<int32_t *>(b + L.off_seq0);
+    w.n_chunks = reinterpret_cast<int32_t *>(b + L.off_nchunks);
+    w.G = reinterpret_cast<float *>(b + L.off_G);
+    w.W = reinterpret_cast<float *>(b + L.off_W);
+    w.U = reinterpret_cast<float *>(b + L.off_U);
+    w.hpre = reinterpret_cast<float *>(b + L.off_hpre);
+    w.vnew = reinterpret_cast<float *>(b + L.off_vnew);
+    w.segM = reinterpret_cast<float *>(b + L.off_segM);
+    w.segC = reinterpret_cast<float *>(b + L.off_segC);
+    w.segH = reinterpret_cast<float *>(b + L.off_segH);
+    w.segD = reinterpret_cast<float *>(b + L.off_segD);
+    w.max_chunks = L.max_chunks;
+    w.n_segments = S;
+    return w;
+}
+
+namespace {
+
+#define GDR_TRY(expr)                                                  \
+    do {                                                               \
+        cudaError_t e_ = (expr);                                       \
+        if (e_ != cudaSuccess) return GDR_ERR_CUDA;                    \
+    } while (0)
+
+#define GDR_LAUNCH(rec, id, expr)                                      \
+    do {                                                               \
+        GDR_TRY((rec).begin(id));                                      \
+        GDR_TRY(expr);                                                 \
+        GDR_TRY((rec).end());                                          \
+    } while (0)
+
+int run_simt(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStream_t st,
+             LaunchRecorder &rec) {
+    GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
+    GDR_LAUNCH(rec, kKPrep, simt_prep(p, ws, st));
+    if (plan.n_segments <= 1) {
+        GDR_LAUNCH(rec, kKScanSerial, simt_scan(p, ws, 0, plan.bv, st));
+    } else {
+        GDR_LAUNCH(rec, kKScanPre, simt_scan(p, ws, 1, plan.bv, st));
+        GDR_LAUNCH(rec, kKCompose, simt_compose(p, ws, plan.bv, st));
+        GDR_LAUNCH(rec, kKScanSegOut, simt_scan(p, ws, 2, plan.bv, st));
+    }
+    GDR_LAUNCH(rec, kKOutput, simt_output(p, ws, st));
+    return GDR_OK;
+}
+
+}  // namespace
+}  // namespace gdr
+
+using namespace gdr;
+
+extern "C" {
+
+int gdr_version(void) { return 100; }
+
+const char *gdr_kernel_name(int id) {
+    switch (id) {
+    case kKChunkTable: return "simt_chunk_table";
+    case kKPrep: return "simt_prep";
+    case kKScanSerial: return "simt_scan_serial";
+    case kKScanPre: return "simt_scan_prescan";
+    case kKCompose: return "simt_compose";
+    case kKScanSegOut: return "simt_scan_segment_out";
+    case kKOutput: return "simt_output";
+    default: return "?";
+    }
+}
+
+const char *gdr_error_string(int code) {
+    switch (code) {
+    case GDR_OK: return "ok";
+    case GDR_ERR_INVALID: return "invalid argument";
+    case GDR_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case GDR_ERR_CUDA: return "CUDA runtime or launch error";
+    case GDR_ERR_TIMEOUT: return "device-side bounded wait expired";
+    case GDR_ERR_SEQLENS: return "malformed cu_seqlens";
+    case GDR_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown error code";
+    }
+}
+
+int gdr_plan_query(const gdr_dims *dims, int beta_free, int n_segments, gdr_plan *out) {
+    int rc = validate_dims(dims);
+    if (rc != GDR_OK) return rc;
+    if (!out) return GDR_ERR_INVALID;
+    return make_plan(*dims, beta_free != 0, n_segments, nullptr, out);
+}
+
+size_t gdr_workspace_size(const gdr_dims *dims, int beta_free, int n_segments) {
+    if (validate_dims(dims) != GDR_OK) return 0;
+    gdr_plan plan;
+    if (make_plan(*dims, beta_free != 0, n_segments, nullptr, &plan) != GDR_OK) return 0;
+    return workspace_layout(*dims, beta_free != 0, plan.n_segments).total;
+}
+
+int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const void *v,
+                     const float *g, const float *beta, const int32_t *cu_seqlens,
+                     const float *h0, void *o, float *ht, int n_segments,
+                     const gdr_options *opt, gdr_stream_t stream) {
+    int rc = validate_dims(dims);
+    if (rc != GDR_OK) return rc;
+    if (!q || !k || !v || !g || !o) return GDR_ERR_INVALID;
+    if ((cu_seqlens != nullptr) != is_varlen(*dims)) return GDR_ERR_INVALID;
+    const bool beta_free = beta == nullptr;
+    gdr_plan plan;
+    rc = make_plan(*dims, beta_free, n_segments, opt, &plan);
+    if (rc != GDR_OK) return rc;
+    if (opt && !(opt->scale >= 0.f)) return GDR_ERR_INVALID;  // rejects NaN too
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Problem p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.cu = cu_seqlens;
+    p.h0 = h0; p.o = o; p.ht = ht;
+    p.B = dims->B; p.T = dims->T; p.H = dims->H; p.K = dims->K; p.V = dims->V;
+    p.N = n_seqs(*dims);
+    p.dtype = dims->dtype;
+    p.scale = (opt && opt->scale > 0.f) ? opt->scale : 1.0f / std::sqrt((float)dims->K);
+    p.status = opt ? opt->status : nullptr;
+    if (p.N == 0) return GDR_OK;
+
+    const WorkspaceLayout L = workspace_layout(*dims, beta_free, plan.n_segments);
+    void *base = nullptr;
+    bool owned = false;
+    if (opt && opt->workspace) {
+        if (opt->workspace_bytes < L.total) return GDR_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(opt->workspace) % kAlign) return GDR_ERR_INVALID;
+        base = opt->workspace;
+    } else {
+        if (cudaMallocAsync(&base, L.total, st) != cudaSuccess) return GDR_ERR_CUDA;
+        owned = true;
+    }
+    const Workspace ws = carve_workspace(base, L, plan.n_segments);
+    LaunchRecorder rec;
+    rec.st = st;
+    if (opt) {
+        rec.events = reinterpret_cast<cudaEvent_t *>(opt->events);
+        rec.max_launches = opt->events ? opt->max_launches : 0;
+        rec.ids = opt->launch_ids;
+        if (!opt->events && opt->launch_ids) rec.max_launches = opt->max_launches;
+    }
+    rc = run_simt(p, ws, plan, st, rec);
+    if (opt && opt->n_launches) *opt->n_launches = rec.count;
+    if (owned) {
+        if (cudaFreeAsync(base, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;
+    }
+    return rc;
+}
+
+int gdr_chunk_fwd(const gdr_dims *dims, const void *q, const void *k, const void *v,
+                  const float *g, const float *beta, const int32_t *cu_seqlens,
+                  const float *h0, void *o, float *ht, int n_segments,
+                  gdr_stream_t stream) {
+    return gdr_chunk_fwd_ex(dims, q, k, v, g, beta, cu_seqlens, h0, o, ht, n_segments,
+                            nullptr, stream);
+}
+
+int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const int32_t *cu_seqlens,
+                       const float *h0, void *o, float *ht, int n_segments,
+                       gdr_stream_t stream) {
+    int rc = validate_dims(dims);
+    if (rc != GDR_OK) return rc;
+    if (!q || !k || !v || !g || !o) return GDR_ERR_INVALID;
+    if ((cu_seqlens != nullptr) != is_varlen(*dims)) return GDR_ERR_INVALID;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t es = dims->dtype == GDR_BF16 ? 2 : 4;
+    const size_t ntok = (size_t)dims->B * (size_t)dims->T * (size_t)dims->H;
+    const size_t ns = (size_t)n_seqs(*dims);
+    const size_t bq = ntok * dims->K * es, bv = ntok * dims->V * es, bg = ntok * 4;
+    const size_t bcu = cu_seqlens ? (ns + 1) * 4 : 0;
+    const size_t bh = ns * dims->H * dims->K * dims->V * 4;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes); return at; };
+    const size_t oq = take(bq), ok = take(bq), ov = take(bv), og = take(bg);
+    const size_t ob = take(beta ? bg : 0), ocu = take(bcu), oh0 = take(h0 ? bh : 0);
+    const size_t oo = take(bv), oht = take(ht ? bh : 0);
+    char *d = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&d), off ? off : kAlign, st) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    auto h2d = [&](size_t at, const void *src, size_t bytes) {
+        return bytes ? cudaMemcpyAsync(d + at, src, bytes, cudaMemcpyHostToDevice, st)
+                     : cudaSuccess;
+    };
+    rc = GDR_OK;
+    if (h2d(oq, q, bq) != cudaSuccess || h2d(ok, k, bq) != cudaSuccess ||
+        h2d(ov, v, bv) != cudaSuccess || h2d(og, g, bg) != cudaSuccess ||
+        (beta && h2d(ob, beta, bg) != cudaSuccess) ||
+        (cu_seqlens && h2d(ocu, cu_seqlens, bcu) != cudaSuccess) ||
+        (h0 && h2d(oh0, h0, bh) != cudaSuccess))
+        rc = GDR_ERR_CUDA;
+    if (rc == GDR_OK)
+        rc = gdr_chunk_fwd(dims, d + oq, d + ok, d + ov, reinterpret_cast<float *>(d + og),
+                           beta ? reinterpret_cast<float *>(d + ob) : nullptr,
+                           cu_seqlens ? reinterpret_cast<int32_t *>(d + ocu) : nullptr,
+                           h0 ? reinterpret_cast<float *>(d + oh0) : nullptr, d + oo,
+                           ht ? reinterpret_cast<float *>(d + oht) : nullptr, n_segments,
+                           stream);
+    if (rc == GDR_OK && bv &&
+        cudaMemcpyAsync(o, d + oo, bv, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        rc = GDR_ERR_CUDA;
+    if (rc == GDR_OK && ht &&
+        cudaMemcpyAsync(ht, d + oht, bh, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        rc = GDR_ERR_CUDA;
+    if (cudaFreeAsync(d, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;
+    return rc;
+}
+
+}  // extern "C"

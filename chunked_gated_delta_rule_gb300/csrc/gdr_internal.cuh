@@ -1,0 +1,106 @@
+// gdr_internal.cuh -- structures shared by the host runtime and the kernels
+// of the chunked gated-delta-rule forward pass (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "gdr.h"
+
+namespace gdr {
+
+constexpr int kChunk = 64;       // tokens per chunk
+constexpr int kMaxK = 256;       // largest key dim supported
+constexpr int kMaxV = 1024;      // largest value dim supported
+constexpr int kMaxSegments = 64; // largest segment count
+
+// Everything a kernel needs to address the caller's tensors.
+struct Problem {
+    const void *q, *k, *v;      // [B,T,H,K] / [B,T,H,V], dtype
+    const float *g, *beta;      // [B,T,H]; beta == nullptr => beta-free
+    const int32_t *cu;          // [N+1] or nullptr (dense)
+    const float *h0;            // [N,H,K,V] or nullptr
+    void *o;                    // [B,T,H,V], dtype
+    float *ht;                  // [N,H,K,V] or nullptr
+    int64_t B, T, H, K, V, N;   // N = B when dense
+    int dtype;                  // GDR_F32 | GDR_BF16
+    float scale;
+    int32_t *status;            // device status word or nullptr
+};
+
+// Scratch carved out of one device allocation (offsets fixed by the host).
+struct Workspace {
+    int32_t *chunk_tab;   // [max_chunks][4]: seq, first flat token, len, chunk-in-seq
+    int32_t *seq_chunk0;  // [N+1]: first global chunk of each sequence
+    int32_t *n_chunks;    // [1]: total chunks
+    float *G;             // [max_chunks][H][64]: chunk-local gate cumsum
+    float *W;             // [max_chunks][H][64][K]   (delta mode)
+    float *U;             // [max_chunks][H][64][V]   (delta mode)
+    float *hpre;          // [max_chunks][H][K][V]: state before each chunk
+    float *vnew;          // [max_chunks][H][64][V]   (delta mode)
+    float *segM;          // [N][H][S][K][K] transition per segment (delta)
+    float *segC;          // [N][H][S][K][V] local state per segment
+    float *segH;          // [N][H][S][K][V] composed initial state per segment
+    float *segD;          // [N][H][S] scalar transition (beta-free)
+    int64_t max_chunks;
+    int n_segments;       // S (1 = serial)
+};
+
+// Byte layout of the workspace for one problem.
+struct WorkspaceLayout {
+    size_t off_tab, off_seq0, off_nchunks, off_G, off_W, off_U, off_hpre,
+        off_vnew, off_segM, off_segC, off_segH, off_segD, total;
+    int64_t max_chunks;
+};
+
+WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int n_segments);
+Workspace carve_workspace(void *base, const WorkspaceLayout &L, int n_segments);
+
+// Kernel ids reported through gdr_options.launch_ids.
+enum KernelId {
+    kKChunkTable = 0,
+    kKPrep = 1,
+    kKScanSerial = 2,
+    kKScanPre = 3,
+    kKCompose = 4,
+    kKScanSegOut = 5,
+    kKOutput = 6,
+    kKNumIds
+};
+
+// Records caller-provided events around each launch (benchmark hook).
+struct LaunchRecorder {
+    cudaEvent_t *events = nullptr;
+    int max_launches = 0;
+    int32_t *ids = nullptr;
+    int count = 0;
+    cudaStream_t st = nullptr;
+    cudaError_t begin(int id) {
+        if (ids && count < max_launches) ids[count] = id;
+        if (events && count < max_launches) return cudaEventRecord(events[2 * count], st);
+        return cudaSuccess;
+    }
+    cudaError_t end() {
+        cudaError_t e = cudaSuccess;
+        if (events && count < max_launches) e = cudaEventRecord(events[2 * count + 1], st);
+        ++count;
+        return e;
+    }
+};
+
+// ---- CUDA-core FP32 path (any supported shape; arithmetic in FP32) --------
+cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool check,
+                             cudaStream_t st);
+cudaError_t simt_prep(const Problem &p, const Workspace &ws, cudaStream_t st);
+// mode 0: serial scan (h0 -> ht), stores hpre / vnew
+// mode 1: segment pre-scan (zero / identity start), stores segC / segM / segD
+// mode 2: segment output pass (start from segH), stores hpre / vnew
+cudaError_t simt_scan(const Problem &p, const Workspace &ws, int mode, int bv,
+                      cudaStream_t st);
+cudaError_t simt_compose(const Problem &p, const Workspace &ws, int bv,
+                         cudaStream_t st);
+cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st);
+
+}  // namespace gdr

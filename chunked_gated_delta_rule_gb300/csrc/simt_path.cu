@@ -1,0 +1,583 @@
+// simt_path.cu -- CUDA-core FP32 path of the chunked gated-delta-rule forward
+// pass.  Used for FP32 inputs (where the 1e-5 accuracy bound rules out
+// BF16/TF32 tensor-core operands) and for any shape the tensor-core path does
+// not cover.  BF16 inputs are widened to FP32 on load; all arithmetic and
+// the state are FP32.
+//
+// Every output element is produced by one thread with a fixed, sequential
+// accumulation order, so results do not depend on the value-tile width or on
+// the grid: all launch plans give bit-identical results.
+//
+// Chunked form (project statement; the state scan of fla's
+// chunk_gated_delta_rule_fwd_kernel_h_blockdim64, Kev PR #259 intro):
+//   G = chunk-local inclusive cumsum of the log gate g
+//   A_ij = beta_i e^{G_i - G_j} (k_i . k_j)  for i > j, else 0
+//   T = (I + A)^-1;  W = T diag(beta e^G) K;  U = T diag(beta) V
+//   v_new = U - W h;  h <- e^{G_last} h + K^T (v_new e^{G_last - G})
+//   o = scale [(Q e^G) h + (Q K^T * e^{G_i - G_j}, j <= i) v_new]
+// Segment split (cuLA PR #127 "Root cause and implementation"): per segment
+// a local state c_s (scan from 0) and a K x K transition M_s (the same scan
+// on identity columns with U = 0), then h_{s+1} = M_s h_s + c_s.
+#include "gdr_internal.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float ld_in(const float *p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_in(const __nv_bfloat16 *p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_out(float *p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_out(__nv_bfloat16 *p, int64_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void report(int32_t *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// A1: chunk indexing.  One block.  Builds the (sequence, first token, length,
+// chunk-in-sequence) table for every 64-token chunk and the first global
+// chunk of every sequence.  Malformed cu_seqlens (not non-decreasing, not
+// starting at 0, not ending at T, or more chunks than the table holds) make
+// the call compute nothing and set GDR_ERR_SEQLENS in the status word.
+__global__ void k_chunk_table(const int32_t *__restrict__ cu, int64_t N, int64_t T,
+                              int64_t max_chunks, int32_t *__restrict__ tab,
+                              int32_t *__restrict__ seq_chunk0,
+                              int32_t *__restrict__ n_chunks, int32_t *status) {
+    __shared__ int s_bad;
+    if (threadIdx.x == 0) {
+        int64_t acc = 0;
+        int bad = 0;
+        if (cu && (cu[0] != 0 || cu[N] != T)) bad = 1;
+        for (int64_t n = 0; n < N && !bad; ++n) {
+            const int64_t a = cu ? cu[n] : n * T;
+            const int64_t b = cu ? cu[n + 1] : (n + 1) * T;
+            const int64_t len = b - a;
+            if (len < 0) { bad = 1; break; }
+            const int64_t c = (len + kChunk - 1) / kChunk;
+            seq_chunk0[n] = (int32_t)acc;
+            acc += c;
+            if (acc > max_chunks) { bad = 1; break; }
+        }
+        s_bad = bad;
+        *n_chunks = bad ? 0 : (int32_t)acc;
+        if (!bad) seq_chunk0[N] = (int32_t)acc;
+        if (bad) report(status, GDR_ERR_SEQLENS);
+    }
+    __syncthreads();
+    if (s_bad) {
+        for (int64_t n = threadIdx.x; n <= N; n += blockDim.x) seq_chunk0[n] = 0;
+        return;
+    }
+    for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
+        const int64_t a = cu ? cu[n] : n * T;
+        const int64_t len = (cu ? cu[n + 1] : (n + 1) * T) - a;
+        const int32_t c0 = seq_chunk0[n];
+        const int32_t cnt = seq_chunk0[n + 1] - c0;
+        for (int32_t c = 0; c < cnt; ++c) {
+            int32_t *e = tab + 4 * (int64_t)(c0 + c);
+            const int64_t rem = len - (int64_t)c * kChunk;
+            e[0] = (int32_t)n;
+            e[1] = (int32_t)(a + (int64_t)c * kChunk);
+            e[2] = (int32_t)(rem < kChunk ? rem : kChunk);
+            e[3] = c;
+        }
+    }
+}
+
+// A2-A5: per (chunk, head) gate cumsum; in delta mode also the Gram matrix
+// A, the unit-lower-triangular inverse T = (I + A)^-1 and the WY factors W, U.
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+k_prep(Problem p, Workspace ws) {
+    const int64_t chunk = blockIdx.x;
+    const int h = blockIdx.y;
+    if (chunk >= *ws.n_chunks) return;
+    const int4 e = reinterpret_cast<const int4 *>(ws.chunk_tab)[chunk];
+    const int64_t t0 = e.y;
+    const int len = e.z;
+    const int H = (int)p.H, K = (int)p.K, V = (int)p.V;
+    const int tid = threadIdx.x;
+    const int ldk = K + 1;
+    const int VB = V < 128 ? V : 128;
+    const int ldv = VB + 1;
+
+    extern __shared__ float sm[];
+    float *sG = sm;
+    float *sB = sG + kChunk;
+    float *sBG = sB + kChunk;
+    float *sK = sBG + kChunk;
+    float *sA = sK + kChunk * ldk;
+    float *sT = sA + kChunk * 65;
+    float *sV = sT + kChunk * 65;
+
+    const bool delta = p.beta != nullptr;
+    if (tid < kChunk) {
+        sG[tid] = tid < len ? p.g[(t0 + tid) * H + h] : 0.f;
+        sB[tid] = (delta && tid < len) ? p.beta[(t0 + tid) * H + h] : 0.f;
+    }
+    __syncthreads();
+    if (tid == 0) {  // fixed left-to-right order
+        float acc = 0.f;
+        for (int i = 0; i < kChunk; ++i) {
+            acc += sG[i];
+            sG[i] = acc;
+        }
+    }
+    __syncthreads();
+    if (tid < kChunk) ws.G[(chunk * H + h) * kChunk + tid] = sG[tid];
+    if (!delta) return;
+    if (tid < kChunk) sBG[tid] = sB[tid] * expf(sG[tid]);
+
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+        const int i = idx / K, c = idx - i * K;
+        sK[i * ldk + c] = i < len ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
+    }
+    __syncthreads();
+    // A3: A_ij = beta_i e^{G_i - G_j} (k_i . k_j), strictly lower (the mask is
+    // applied before exp, so e^{G_i - G_j} is only formed for i > j).
+    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+        const int i = idx >> 6, j = idx & 63;
+        float a = 0.f;
+        if (j < i && i < len) {
+            float d = 0.f;
+            for (int c = 0; c < K; ++c) d = fmaf(sK[i * ldk + c], sK[j * ldk + c], d);
+            a = sB[i] * expf(sG[i] - sG[j]) * d;
+        }
+        sA[i * 65 + j] = a;
+    }
+    __syncthreads();
+    // A4: T = (I + A)^-1.  Column m solves (I + A) x = e_m by forward
+    // substitution; columns are independent, one thread each.
+    if (tid < kChunk) {
+        const int m = tid;
+        for (int i = 0; i < kChunk; ++i) {
+            float x;
+            if (i < m) {
+                x = 0.f;
+            } else if (i == m) {
+                x = 1.f;
+            } else {
+                float s = 0.f;
+                for (int j = m; j < i; ++j) s = fmaf(sA[i * 65 + j], sT[j * 65 + m], s);
+                x = -s;
+            }
+            sT[i * 65 + m] = x;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+        const int i = idx / K, c = idx - i * K;
+        sK[i * ldk + c] *= sBG[i];
+    }
+    __syncthreads();
+    // A5: W = T diag(beta e^G) K
+    float *Wg = ws.W + (chunk * H + h) * (int64_t)kChunk * K;
+    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+        const int i = idx / K, c = idx - i * K;
+        float s = 0.f;
+        for (int j = 0; j <= i; ++j) s = fmaf(sT[i * 65 + j], sK[j * ldk + c], s);
+        Wg[idx] = s;
+    }
+    // A5: U = T diag(beta) V, in column blocks of VB
+    float *Ug = ws.U + (chunk * H + h) * (int64_t)kChunk * V;
+    for (int v0 = 0; v0 < V; v0 += VB) {
+        __syncthreads();
+        for (int idx = tid; idx < kChunk * VB; idx += kThreads) {
+            const int i = idx / VB, c = idx - i * VB;
+            sV[i * ldv + c] =
+                i < len ? sB[i] * ld_in(v, ((t0 + i) * H + h) * (int64_t)V + v0 + c) : 0.f;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kChunk * VB; idx += kThreads) {
+            const int i = idx / VB, c = idx - i * VB;
+            float s = 0.f;
+            for (int j = 0; j <= i; ++j) s = fmaf(sT[i * 65 + j], sV[j * ldv + c], s);
+            Ug[(int64_t)i * V + v0 + c] = s;
+        }
+    }
+}
+
+// A6 / A8 / A10: the serial state scan over the chunks of one (sequence,
+// segment, head, column tile).  mode 0: whole sequence from h0, writes ht;
+// mode 1: segment pre-scan from zero (value columns -> c_s) or identity
+// (transition columns, U = 0 -> M_s); mode 2: segment output pass from the
+// composed segment state.  Modes 0 and 2 store h_pre and v_new for the
+// output kernel.
+template <typename Tin, int BV>
+__global__ void __launch_bounds__(kThreads)
+k_scan(Problem p, Workspace ws, int mode) {
+    const int H = (int)p.H, K = (int)p.K, V = (int)p.V;
+    const int S = mode == 0 ? 1 : ws.n_segments;
+    const bool delta = p.beta != nullptr;
+    const int n_vtiles = V / BV;
+    const int ntiles = (mode == 1 && delta) ? (V + K) / BV : n_vtiles;
+    int64_t bid = blockIdx.x;
+    const int tile = (int)(bid % ntiles);
+    bid /= ntiles;
+    const int s = (int)(bid % S);
+    const int64_t n = bid / S;
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x;
+
+    const int c_begin = ws.seq_chunk0[n];
+    const int nc = ws.seq_chunk0[n + 1] - c_begin;
+    int s0 = 0, s1 = nc;
+    if (mode != 0) {
+        const int per = (nc + S - 1) / S;
+        s0 = s * per;
+        s1 = min(nc, s0 + per);
+        if (s0 >= s1) return;
+    }
+    const bool trans = tile >= n_vtiles;
+    const int col0 = trans ? (tile - n_vtiles) * BV : tile * BV;
+    const int ldk = K + 1;
+    constexpr int ldh = BV + 1;
+
+    extern __shared__ float sm[];
+    float *hs = sm;                   // [K][BV+1] state tile
+    float *sK = hs + K * ldh;         // [64][K+1]
+    float *sW = sK + kChunk * ldk;    // [64][K+1] (delta)
+    float *vn = sW + (delta ? kChunk * ldk : 0);  // [64][BV+1]
+    float *sG = vn + kChunk * ldh;    // [64]
+
+    const int64_t seg_base = ((n * H + h) * (int64_t)S + s);
+    for (int idx = tid; idx < K * BV; idx += kThreads) {
+        const int key = idx / BV, c = idx - key * BV;
+        float x = 0.f;
+        if (mode == 0) {
+            if (p.h0) x = p.h0[((n * H + h) * K + key) * (int64_t)V + col0 + c];
+        } else if (mode == 2) {
+            x = ws.segH[(seg_base * K + key) * V + col0 + c];
+        } else if (trans) {
+            x = (key == col0 + c) ? 1.f : 0.f;
+        }
+        hs[key * ldh + c] = x;
+    }
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    float dprod = 1.f;
+
+    for (int cc = s0; cc < s1; ++cc) {
+        const int64_t gc = c_begin + cc;
+        const int4 e = reinterpret_cast<const int4 *>(ws.chunk_tab)[gc];
+        const int64_t t0 = e.y;
+        const int len = e.z;
+        __syncthreads();
+        if (tid < kChunk) sG[tid] = ws.G[(gc * H + h) * kChunk + tid];
+        for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+            const int i = idx / K, c = idx - i * K;
+            sK[i * ldk + c] = i < len ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
+            if (delta) sW[i * ldk + c] = ws.W[((gc * H + h) * kChunk + i) * (int64_t)K + c];
+        }
+        if (mode != 1) {
+            float *hp = ws.hpre + (gc * H + h) * (int64_t)K * V;
+            for (int idx = tid; idx < K * BV; idx += kThreads) {
+                const int key = idx / BV, c = idx - key * BV;
+                hp[(int64_t)key * V + col0 + c] = hs[key * ldh + c];
+            }
+        }
+        __syncthreads();
+        const float gl = sG[len - 1];
+        const float gam = expf(gl);
+        // v_new = U - W h (delta) or V (beta-free), then scaled by e^{G_last - G}
+        for (int idx = tid; idx < kChunk * BV; idx += kThreads) {
+            const int i = idx / BV, c = idx - i * BV;
+            float x = 0.f;
+            if (i < len) {
+                if (delta) {
+                    float acc = 0.f;
+                    for (int key = 0; key < K; ++key)
+                        acc = fmaf(sW[i * ldk + key], hs[key * ldh + c], acc);
+                    const float u = trans ? 0.f
+                        : ws.U[((gc * H + h) * kChunk + i) * (int64_t)V + col0 + c];
+                    x = u - acc;
+                    if (mode != 1)
+                        ws.vnew[((gc * H + h) * kChunk + i) * (int64_t)V + col0 + c] = x;
+                } else {
+                    x = ld_in(v, ((t0 + i) * H + h) * (int64_t)V + col0 + c);
+                }
+                x *= expf(gl - sG[i]);
+            }
+            vn[i * ldh + c] = x;
+        }
+        __syncthreads();
+        // h <- e^{G_last} h + K^T (v_new e^{G_last - G})
+        for (int idx = tid; idx < K * BV; idx += kThreads) {
+            const int key = idx / BV, c = idx - key * BV;
+            float acc = 0.f;
+            for (int i = 0; i < len; ++i) acc = fmaf(sK[i * ldk + key], vn[i * ldh + c], acc);
+            hs[key * ldh + c] = fmaf(gam, hs[key * ldh + c], acc);
+        }
+        dprod *= gam;
+    }
+    __syncthreads();
+    if (mode == 0) {
+        if (p.ht) {
+            for (int idx = tid; idx < K * BV; idx += kThreads) {
+                const int key = idx / BV, c = idx - key * BV;
+                p.ht[((n * H + h) * K + key) * (int64_t)V + col0 + c] = hs[key * ldh + c];
+            }
+        }
+    } else if (mode == 1) {
+        for (int idx = tid; idx < K * BV; idx += kThreads) {
+            const int key = idx / BV, c = idx - key * BV;
+            if (trans)
+                ws.segM[(seg_base * K + key) * K + col0 + c] = hs[key * ldh + c];
+            else
+                ws.segC[(seg_base * K + key) * V + col0 + c] = hs[key * ldh + c];
+        }
+        if (!delta && tile == 0 && tid == 0) ws.segD[seg_base] = dprod;
+    }
+}
+
+// A9: ordered composition over the segments of one (sequence, head, value
+// tile): records each segment's initial state and h_{s+1} = M_s h_s + c_s
+// (beta-free: d_s h_s + c_s); the last state is ht.
+template <int BV>
+__global__ void __launch_bounds__(kThreads)
+k_compose(Problem p, Workspace ws) {
+    const int H = (int)p.H, K = (int)p.K, V = (int)p.V;
+    const int S = ws.n_segments;
+    const int n_vtiles = V / BV;
+    const int tile = blockIdx.x % n_vtiles;
+    const int64_t n = blockIdx.x / n_vtiles;
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int col0 = tile * BV;
+    const bool delta = p.beta != nullptr;
+    constexpr int ldh = BV + 1;
+    extern __shared__ float sm[];
+    float *hs = sm;
+    float *hn = sm + K * ldh;
+
+    const int nc = ws.seq_chunk0[n + 1] - ws.seq_chunk0[n];
+    const int per = (nc + S - 1) / S;
+    const int nseg = per ? (nc + per - 1) / per : 0;
+    for (int idx = tid; idx < K * BV; idx += kThreads) {
+        const int key = idx / BV, c = idx - key * BV;
+        hs[key * ldh + c] = p.h0 ? p.h0[((n * H + h) * K + key) * (int64_t)V + col0 + c] : 0.f;
+    }
+    __syncthreads();
+    for (int s = 0; s < nseg; ++s) {
+        const int64_t seg_base = ((n * H + h) * (int64_t)S + s);
+        const float *M = ws.segM + seg_base * K * K;
+        const float *C = ws.segC + seg_base * K * V;
+        const float d = delta ? 0.f : ws.segD[seg_base];
+        for (int idx = tid; idx < K * BV; idx += kThreads) {
+            const int key = idx / BV, c = idx - key * BV;
+            ws.segH[(seg_base * K + key) * V + col0 + c] = hs[key * ldh + c];
+            float acc;
+            if (delta) {
+                acc = 0.f;
+                for (int m = 0; m < K; ++m) acc = fmaf(M[(int64_t)key * K + m], hs[m * ldh + c], acc);
+                acc += C[(int64_t)key * V + col0 + c];
+            } else {
+                acc = fmaf(d, hs[key * ldh + c], C[(int64_t)key * V + col0 + c]);
+            }
+            hn[key * ldh + c] = acc;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < K * BV; idx += kThreads) {
+            const int key = idx / BV, c = idx - key * BV;
+            hs[key * ldh + c] = hn[key * ldh + c];
+        }
+        __syncthreads();
+    }
+    if (p.ht) {
+        for (int idx = tid; idx < K * BV; idx += kThreads) {
+            const int key = idx / BV, c = idx - key * BV;
+            p.ht[((n * H + h) * K + key) * (int64_t)V + col0 + c] = hs[key * ldh + c];
+        }
+    }
+}
+
+// A7: o = scale [(Q e^G) h_pre + (Q K^T * e^{G_i - G_j}, j <= i) v_new]
+// per (chunk, head, value block).  The causal mask includes the diagonal:
+// o_t reads the state after token t's own write.
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+k_output(Problem p, Workspace ws, int bvo) {
+    const int64_t chunk = blockIdx.x;
+    const int h = blockIdx.y;
+    if (chunk >= *ws.n_chunks) return;
+    const int4 e = reinterpret_cast<const int4 *>(ws.chunk_tab)[chunk];
+    const int64_t t0 = e.y;
+    const int len = e.z;
+    const int H = (int)p.H, K = (int)p.K, V = (int)p.V;
+    const int col0 = blockIdx.z * bvo;
+    const int tid = threadIdx.x;
+    const int ldk = K + 1, ldo = bvo + 1;
+    const bool delta = p.beta != nullptr;
+
+    extern __shared__ float sm[];
+    float *sQ = sm;
+    float *sK = sQ + kChunk * ldk;
+    float *sP = sK + kChunk * ldk;
+    float *sHp = sP + kChunk * 65;
+    float *sVn = sHp + K * ldo;
+    float *sG = sVn + kChunk * ldo;
+
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    if (tid < kChunk) sG[tid] = ws.G[(chunk * H + h) * kChunk + tid];
+    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
+        const int i = idx / K, c = idx - i * K;
+        const int64_t off = ((t0 + i) * H + h) * (int64_t)K + c;
+        sQ[i * ldk + c] = i < len ? ld_in(q, off) : 0.f;
+        sK[i * ldk + c] = i < len ? ld_in(k, off) : 0.f;
+    }
+    const float *hp = ws.hpre + (chunk * H + h) * (int64_t)K * V;
+    for (int idx = tid; idx < K * bvo; idx += kThreads) {
+        const int key = idx / bvo, c = idx - key * bvo;
+        sHp[key * ldo + c] = hp[(int64_t)key * V + col0 + c];
+    }
+    for (int idx = tid; idx < kChunk * bvo; idx += kThreads) {
+        const int i = idx / bvo, c = idx - i * bvo;
+        float x = 0.f;
+        if (i < len) {
+            x = delta ? ws.vnew[((chunk * H + h) * kChunk + i) * (int64_t)V + col0 + c]
+                      : ld_in(v, ((t0 + i) * H + h) * (int64_t)V + col0 + c);
+        }
+        sVn[i * ldo + c] = x;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
+        const int i = idx >> 6, j = idx & 63;
+        float a = 0.f;
+        if (j <= i && i < len) {
+            float d = 0.f;
+            for (int c = 0; c < K; ++c) d = fmaf(sQ[i * ldk + c], sK[j * ldk + c], d);
+            a = d * expf(sG[i] - sG[j]);
+        }
+        sP[i * 65 + j] = a;
+    }
+    __syncthreads();
+    Tin *o = static_cast<Tin *>(p.o);
+    for (int idx = tid; idx < kChunk * bvo; idx += kThreads) {
+        const int i = idx / bvo, c = idx - i * bvo;
+        if (i >= len) continue;
+        float a1 = 0.f;
+        for (int key = 0; key < K; ++key) a1 = fmaf(sQ[i * ldk + key], sHp[key * ldo + c], a1);
+        float a2 = 0.f;
+        for (int j = 0; j <= i; ++j) a2 = fmaf(sP[i * 65 + j], sVn[j * ldo + c], a2);
+        const float y = p.scale * fmaf(expf(sG[i]), a1, a2);
+        st_out(o, ((t0 + i) * H + h) * (int64_t)V + col0 + c, y);
+    }
+}
+
+template <typename F>
+cudaError_t set_smem(F *f, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(f),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool /*check*/,
+                             cudaStream_t st) {
+    k_chunk_table<<<1, kThreads, 0, st>>>(p.cu, p.N, p.T, ws.max_chunks, ws.chunk_tab,
+                                          ws.seq_chunk0, ws.n_chunks, p.status);
+    return cudaGetLastError();
+}
+
+cudaError_t simt_prep(const Problem &p, const Workspace &ws, cudaStream_t st) {
+    if (ws.max_chunks == 0) return cudaSuccess;
+    const int K = (int)p.K, V = (int)p.V;
+    const int VB = V < 128 ? V : 128;
+    const size_t smem = sizeof(float) *
+        (3 * kChunk + kChunk * (K + 1) + 2 * kChunk * 65 + kChunk * (VB + 1));
+    dim3 grid((unsigned)ws.max_chunks, (unsigned)p.H);
+    cudaError_t err;
+    if (p.dtype == GDR_BF16) {
+        if ((err = set_smem(k_prep<__nv_bfloat16>, smem)) != cudaSuccess) return err;
+        k_prep<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p, ws);
+    } else {
+        if ((err = set_smem(k_prep<float>, smem)) != cudaSuccess) return err;
+        k_prep<float><<<grid, kThreads, smem, st>>>(p, ws);
+    }
+    return cudaGetLastError();
+}
+
+template <typename Tin, int BV>
+static cudaError_t launch_scan(const Problem &p, const Workspace &ws, int mode,
+                               cudaStream_t st) {
+    const int K = (int)p.K, V = (int)p.V;
+    const bool delta = p.beta != nullptr;
+    const int S = mode == 0 ? 1 : ws.n_segments;
+    const int ntiles = (mode == 1 && delta) ? (V + K) / BV : V / BV;
+    const size_t smem = sizeof(float) *
+        ((size_t)K * (BV + 1) + (size_t)kChunk * (K + 1) * (delta ? 2 : 1) +
+         (size_t)kChunk * (BV + 1) + kChunk);
+    cudaError_t err = set_smem(k_scan<Tin, BV>, smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((unsigned)((int64_t)ntiles * p.N * S), (unsigned)p.H);
+    k_scan<Tin, BV><<<grid, kThreads, smem, st>>>(p, ws, mode);
+    return cudaGetLastError();
+}
+
+cudaError_t simt_scan(const Problem &p, const Workspace &ws, int mode, int bv,
+                      cudaStream_t st) {
+    if (p.dtype == GDR_BF16) {
+        switch (bv) {
+        case 16: return launch_scan<__nv_bfloat16, 16>(p, ws, mode, st);
+        case 32: return launch_scan<__nv_bfloat16, 32>(p, ws, mode, st);
+        case 64: return launch_scan<__nv_bfloat16, 64>(p, ws, mode, st);
+        }
+    } else {
+        switch (bv) {
+        case 16: return launch_scan<float, 16>(p, ws, mode, st);
+        case 32: return launch_scan<float, 32>(p, ws, mode, st);
+        case 64: return launch_scan<float, 64>(p, ws, mode, st);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int BV>
+static cudaError_t launch_compose(const Problem &p, const Workspace &ws, cudaStream_t st) {
+    const size_t smem = sizeof(float) * 2 * (size_t)p.K * (BV + 1);
+    cudaError_t err = set_smem(k_compose<BV>, smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((unsigned)((p.V / BV) * p.N), (unsigned)p.H);
+    k_compose<BV><<<grid, kThreads, smem, st>>>(p, ws);
+    return cudaGetLastError();
+}
+
+cudaError_t simt_compose(const Problem &p, const Workspace &ws, int bv, cudaStream_t st) {
+    switch (bv) {
+    case 16: return launch_compose<16>(p, ws, st);
+    case 32: return launch_compose<32>(p, ws, st);
+    case 64: return launch_compose<64>(p, ws, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st) {
+    if (ws.max_chunks == 0) return cudaSuccess;
+    const int K = (int)p.K, V = (int)p.V;
+    int bvo = K <= 128 ? 64 : 32;
+    while (V % bvo) bvo >>= 1;
+    const size_t smem = sizeof(float) *
+        (2 * (size_t)kChunk * (K + 1) + kChunk * 65 + (size_t)K * (bvo + 1) +
+         (size_t)kChunk * (bvo + 1) + kChunk);
+    dim3 grid((unsigned)ws.max_chunks, (unsigned)p.H, (unsigned)(V / bvo));
+    cudaError_t err;
+    if (p.dtype == GDR_BF16) {
+        if ((err = set_smem(k_output<__nv_bfloat16>, smem)) != cudaSuccess) return err;
+        k_output<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p, ws, bvo);
+    } else {
+        if ((err = set_smem(k_output<float>, smem)) != cudaSuccess) return err;
+        k_output<float><<<grid, kThreads, smem, st>>>(p, ws, bvo);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

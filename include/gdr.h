@@ -1,0 +1,177 @@
+/*
+ * gdr.h -- C ABI of the GB300 chunked gated-delta-rule forward pass.
+ *
+ * One call computes, for every sequence n and head h, the forward pass of
+ * gated delta-rule linear attention over 64-token chunks:
+ *
+ *   per token   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *               o_t = scale * S_t q_t,   alpha_t = exp(g_t),  scale = 1/sqrt(K)
+ *
+ *   per chunk   (the state scan of fla's chunk_gated_delta_rule_fwd_kernel_h,
+ *               Kev PR #259 intro; the serial recurrence of cuLA PR #127
+ *               "Summary"): chunk-local cumsum G of the log gate g;
+ *               A = strictly-lower(diag(beta) * decay-masked K K^T);
+ *               T = (I + A)^-1;  W = T diag(beta e^G) K;  U = T diag(beta) V;
+ *               then serially over chunks, with h = S^T (K x V, FP32):
+ *               v_new = U - W h;   o = scale [(Q e^G) h + causal(Q K^T * decay) v_new]
+ *               h <- e^{G_last} h + K^T (v_new * e^{G_last - G}).
+ *
+ *   segment split (cuLA PR #127 "Summary", "Root cause and implementation":
+ *               intra-card context parallelism): each run of whole chunks
+ *               emits a local state c_s and a K x K affine transition M_s in
+ *               FP32; an ordered pass h_{s+1} = M_s h_s + c_s chains them;
+ *               then every segment produces its outputs in parallel.
+ *
+ *   beta-free   (beta == NULL; the diagonal affine chunk transform of
+ *               flash-linear-attention issue #23 "Proposed Dataflow"):
+ *               S_t = alpha_t S_{t-1} + v_t k_t^T, the transition is a scalar.
+ *
+ * Layouts (all row-major and contiguous, element strides implied):
+ *   q, k        [B, T, H, K]   dtype GDR_BF16 or GDR_F32 (same for q, k, v, o)
+ *   v, o        [B, T, H, V]
+ *   g, beta     [B, T, H]      float32; g is the per-token LOG gate (<= 0)
+ *   cu_seqlens  [N + 1]        int32 prefix offsets of N packed sequences
+ *                              (varlen: dims.N = N > 0, B == 1, T = total)
+ *   h0, ht      [Nseq, H, K, V] float32 state h = S^T, Nseq = N (varlen)
+ *                              or B (dense)
+ *
+ * Ownership: every pointer is caller-owned.  gdr_chunk_fwd* take DEVICE
+ * pointers, enqueue work on `stream` and return without synchronising; the
+ * library keeps no pointer after the call returns.  Scratch is taken
+ * stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`) unless the
+ * caller passes a workspace through gdr_chunk_fwd_ex.
+ *
+ * Errors: every entry point returns 0 on success or a negative GDR_ERR_*
+ * code; arguments are checked before any work is enqueued, so a rejected
+ * call leaves the outputs untouched.  cu_seqlens is device data and is not
+ * read on the host: it must be non-decreasing with cu[0] = 0 and cu[N] = T.
+ * The device checks this before any other work; a malformed table makes the
+ * call compute nothing and, if a status word is given (gdr_chunk_fwd_ex),
+ * sets it to GDR_ERR_SEQLENS.
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *gdr_stream_t;
+
+/* Element type of q, k, v and o. */
+enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1 };
+
+/* Return codes. */
+enum gdr_status {
+    GDR_OK = 0,
+    GDR_ERR_INVALID = -1,      /* null pointer, bad size, misaligned row   */
+    GDR_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. K > 256) */
+    GDR_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed      */
+    GDR_ERR_TIMEOUT = -4,      /* device status: a bounded wait expired     */
+    GDR_ERR_SEQLENS = -5,      /* device status: cu_seqlens malformed       */
+    GDR_ERR_WORKSPACE = -6     /* caller workspace too small                */
+};
+
+/* Problem size.  Dense layout: N = 0 (there are B sequences of T tokens).
+ * Varlen layout: N > 0 sequences packed along T (the total length), B == 1,
+ * cu_seqlens required. */
+typedef struct gdr_dims {
+    int64_t B, T, H, K, V, N;
+    int32_t dtype; /* enum gdr_dtype */
+    int32_t reserved;
+} gdr_dims;
+
+/* Launch plan (A13): chosen per shape from measured timings; every plan of
+ * one path gives bit-identical results for a fixed segment count. */
+typedef struct gdr_plan {
+    int32_t path;       /* 1 = CUDA-core FP32 path, 2 = tensor-core path    */
+    int32_t bv;         /* value columns per scan CTA                      */
+    int32_t n_segments; /* 1 = serial scan, S > 1 = segment split           */
+    int32_t reserved;
+} gdr_plan;
+
+/* Options of gdr_chunk_fwd_ex.  Zero-initialise, then set what you need. */
+typedef struct gdr_options {
+    float scale;            /* readout scale; 0 => 1/sqrt(K)                */
+    int32_t force_path;     /* 0 => plan; 1 CUDA-core path; 2 tensor cores  */
+    int32_t force_bv;       /* 0 => plan; else value columns per scan CTA   */
+    void *workspace;        /* device scratch, NULL => stream-ordered alloc */
+    size_t workspace_bytes; /* size of `workspace`                          */
+    int32_t *status;        /* device int32 status word or NULL; kernels
+                               write a GDR_ERR_* code there on a device-side
+                               failure (never trap); caller zeroes it        */
+    /* Per-launch timing for benchmarks.  If `events` is non-NULL it holds
+     * 2 * max_launches cudaEvent_t handles created by the caller; the
+     * library records events[2i] just before and events[2i+1] just after its
+     * i-th kernel launch on `stream` (launches past max_launches are not
+     * recorded), stores the kernel id of launch i in launch_ids[i] (host
+     * array, may be NULL; see gdr_kernel_name) and the number of kernel
+     * launches of the call in *n_launches (host, may be NULL). */
+    void **events;
+    int32_t max_launches;
+    int32_t *launch_ids;
+    int32_t *n_launches;
+} gdr_options;
+
+/*
+ * gdr_chunk_fwd -- the forward pass on device buffers (see top of file).
+ *   beta        NULL selects the beta-free mode.
+ *   cu_seqlens  NULL selects the dense layout.
+ *   h0          NULL: zero initial state.   ht  NULL: final state not written.
+ *   n_segments  0: plan chooses; 1: serial scan; S > 1: split every sequence
+ *               into runs of ceil(chunks / S) whole chunks.
+ * Returns GDR_OK or GDR_ERR_*.
+ */
+int gdr_chunk_fwd(const gdr_dims *dims, const void *q, const void *k,
+                  const void *v, const float *g, const float *beta,
+                  const int32_t *cu_seqlens, const float *h0, void *o,
+                  float *ht, int n_segments, gdr_stream_t stream);
+
+/* As gdr_chunk_fwd, with options (scale override, forced plan for tests,
+ * caller workspace, device status word).  opt == NULL equals gdr_chunk_fwd. */
+int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k,
+                     const void *v, const float *g, const float *beta,
+                     const int32_t *cu_seqlens, const float *h0, void *o,
+                     float *ht, int n_segments, const gdr_options *opt,
+                     gdr_stream_t stream);
+
+/*
+ * gdr_chunk_fwd_host -- the same pass on HOST buffers (same layouts).  The
+ * call copies the inputs to the device, runs gdr_chunk_fwd on `stream`,
+ * copies o (and ht) back and synchronises `stream` before returning.  Pinned
+ * host memory gives asynchronous copies; pageable memory works but copies
+ * synchronously.  Device buffers are stream-ordered allocations.
+ */
+int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k,
+                       const void *v, const float *g, const float *beta,
+                       const int32_t *cu_seqlens, const float *h0, void *o,
+                       float *ht, int n_segments, gdr_stream_t stream);
+
+/* Bytes of device scratch gdr_chunk_fwd_ex needs for this problem
+ * (beta_free != 0 for the beta-free mode).  0 on invalid arguments. */
+size_t gdr_workspace_size(const gdr_dims *dims, int beta_free,
+                          int n_segments);
+
+/* The plan gdr_chunk_fwd would use (host-only lookup, no GPU needed). */
+int gdr_plan_query(const gdr_dims *dims, int beta_free, int n_segments,
+                   gdr_plan *out);
+
+/* Name of a kernel id reported through gdr_options.launch_ids ("?" if
+ * unknown). */
+const char *gdr_kernel_name(int id);
+
+/* Static description of a return code. */
+const char *gdr_error_string(int code);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int gdr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H_ */

@@ -1,0 +1,100 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol the header
+declares, and its host-only logic (argument checks, plan, workspace size,
+error strings) works without a GPU.  No compute call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_gated_delta_rule_gb300 as pkg
+from chunked_gated_delta_rule_gb300 import api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from chunked_gated_delta_rule_gb300 import build
+    build.build()
+    return pkg.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdr_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    assert declared_functions() == sorted(api.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert callable(getattr(lib, name))
+
+
+def test_version_and_error_strings(lib):
+    assert pkg.gdr_version() == 100
+    assert pkg.gdr_error_string(0) == "ok"
+    assert pkg.gdr_error_string(-5) == "malformed cu_seqlens"
+    assert pkg.gdr_error_string(12345) == "unknown error code"
+
+
+def _fwd(lib, dims, q=1, k=1, v=1, g=1, o=1, cu=None, n_segments=0, opt=None):
+    p = lambda x: None if x is None else ctypes.c_void_p(0x1000 * x)
+    if opt is None:
+        return lib.gdr_chunk_fwd(ctypes.byref(dims), p(q), p(k), p(v), p(g), None, p(cu),
+                                 None, p(o), None, n_segments, None)
+    return lib.gdr_chunk_fwd_ex(ctypes.byref(dims), p(q), p(k), p(v), p(g), None, p(cu),
+                                None, p(o), None, n_segments, ctypes.byref(opt), None)
+
+
+def test_argument_checks_reject_before_any_gpu_work(lib):
+    ok = api.make_dims(1, 128, 2, 64, 64)
+    assert _fwd(lib, ok, q=None) == -1
+    assert _fwd(lib, ok, o=None) == -1
+    assert _fwd(lib, api.make_dims(1, 128, 2, 64, 64, dtype=7)) == -1
+    assert _fwd(lib, api.make_dims(0, 128, 2, 64, 64)) == -1
+    assert _fwd(lib, api.make_dims(1, -1, 2, 64, 64)) == -1
+    assert _fwd(lib, api.make_dims(1, 128, 2, 60, 64)) == -2      # K % 16
+    assert _fwd(lib, api.make_dims(1, 128, 2, 512, 64)) == -2     # K > 256
+    assert _fwd(lib, api.make_dims(1, 128, 2, 64, 2048)) == -2    # V > 1024
+    assert _fwd(lib, api.make_dims(2, 128, 2, 64, 64, N=3), cu=5) == -1  # varlen needs B == 1
+    assert _fwd(lib, api.make_dims(1, 128, 2, 64, 64, N=3), cu=None) == -1  # N>0 needs cu
+    assert _fwd(lib, ok, cu=5) == -1                                # cu given, N == 0
+    assert _fwd(lib, ok, n_segments=-1) == -1
+    assert _fwd(lib, ok, n_segments=1000) == -2
+    bad_bv = api.gdr_options(0.0, 0, 48, None, 0, None)
+    assert _fwd(lib, ok, opt=bad_bv) == -1
+    bad_scale = api.gdr_options(float("nan"), 0, 0, None, 0, None)
+    assert _fwd(lib, ok, opt=bad_scale) == -1
+
+
+def test_plan_query_is_deterministic_and_valid():
+    for dims in [(1, 256, 2, 64, 64, 0, 0), (1, 10456, 16, 128, 128, 32, 1),
+                 (1, 16384, 16, 128, 128, 0, 1), (1, 65536, 1, 128, 128, 0, 1),
+                 (2, 8192, 4, 256, 512, 0, 1)]:
+        a = pkg.gdr_plan_query(*dims)
+        b = pkg.gdr_plan_query(*dims)
+        assert a == b
+        B, T, H, K, V = dims[:5]
+        assert V % a["bv"] == 0 and K % a["bv"] == 0
+        assert 1 <= a["n_segments"] <= 16
+    # an explicit segment count is taken as given
+    assert pkg.gdr_plan_query(1, 16384, 16, 128, 128, n_segments=8)["n_segments"] == 8
+    # a long single sequence with few heads is split; a wide batch is not
+    assert pkg.gdr_plan_query(1, 65536, 1, 128, 128)["n_segments"] > 1
+    assert pkg.gdr_plan_query(1, 10456, 16, 128, 128, N=32)["n_segments"] == 1
+
+
+def test_workspace_size_scales_with_problem():
+    small = pkg.gdr_workspace_size(1, 256, 2, 64, 64, dtype=0)
+    big = pkg.gdr_workspace_size(1, 16384, 16, 128, 128, n_segments=1)
+    seg = pkg.gdr_workspace_size(1, 16384, 16, 128, 128, n_segments=16)
+    assert 0 < small < big < seg
+    assert pkg.gdr_workspace_size(1, 256, 2, 60, 64) == 0  # unsupported -> 0
+    assert pkg.gdr_workspace_size(1, 16384, 16, 128, 128, beta_free=True, n_segments=1) < big

@@ -1,0 +1,181 @@
+"""GPU parity of the CUDA path against the FP64 oracle, element by element,
+at sizes the oracle finishes in seconds (several chunks, ragged tails, empty
+sequences), plus the launch-plan and run-to-run bit identity, graph capture,
+NaN-poisoned outputs, the device status word, the host-buffer entry point
+and caller-provided workspace.  All calls go through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_delta_rule_gb300 import synthetic
+from gpu_util import (TOL_BF16, TOL_F32, rel_l2_masked, run_gpu, run_oracle, to_dev,
+                      tol_of)
+
+pytestmark = pytest.mark.gpu
+
+W = synthetic.WORKLOADS
+
+
+def check(x, tol=None, **kw):
+    tol = tol or tol_of(x)
+    o, ht = run_gpu(x, **kw)
+    ro, rht = run_oracle(x)
+    eo, eh = rel_l2_masked(o, ro), rel_l2_masked(ht, rht)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
+    assert eo <= tol and eh <= tol, (eo, eh, tol)
+    return eo, eh
+
+
+@pytest.mark.parametrize("S", [1, 2, 4])
+def test_tiny_dense_f32(S):
+    """FP32 tiny dense workload (B=1, T=256, H=2, K=V=64, h0 in, ht out)."""
+    check(synthetic.make_inputs(W["tiny_dense_f32"]), n_segments=S)
+
+
+@pytest.mark.parametrize("K,V", [(16, 16), (32, 64), (128, 32), (256, 128)])
+def test_f32_shapes(K, V):
+    w = synthetic.small(W["tiny_dense_f32"], K=K, V=V, T=200, H=2, B=2)
+    check(synthetic.make_inputs(w))
+
+
+RAGGED = [1, 63, 64, 65, 127, 128, 257, 7, 300]
+
+
+@pytest.mark.parametrize("S", [1, 2, 4, 16])
+def test_bf16_ragged_varlen(S):
+    w = synthetic.small(W["wide_varlen_bf16"], H=3)
+    check(synthetic.make_inputs(w, lengths=RAGGED), n_segments=S)
+
+
+def test_bf16_varlen_with_empty_sequences_and_h0():
+    w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True)
+    x = synthetic.make_inputs(w, lengths=[0, 70, 0, 129, 0])
+    o, ht = run_gpu(x)
+    ro, rht = run_oracle(x)
+    assert rel_l2_masked(o, ro) <= TOL_BF16
+    assert rel_l2_masked(ht, rht) <= TOL_BF16
+    # an empty sequence hands back its initial state exactly
+    assert torch.equal(ht[0].cpu(), x["h0"][0])
+    assert torch.equal(ht[4].cpu(), x["h0"][4])
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 4, 8, 16])
+def test_bf16_dense_h0_segments(S):
+    w = synthetic.small(W["long_16k_bf16"], B=2, T=1000, H=2, with_h0=True)
+    check(synthetic.make_inputs(w), n_segments=S)
+
+
+@pytest.mark.parametrize("S", [1, 4])
+def test_beta_free_k256_v512(S):
+    w = synthetic.small(W["gla_k256_v512_bf16"], T=300, H=2)
+    check(synthetic.make_inputs(w), n_segments=S)
+
+
+def test_literal_beta_zero():
+    """An all-zero beta tensor freezes the state: o_t = e^{G_t} h0^T q_t / sqrt(K)."""
+    w = synthetic.small(W["long_16k_bf16"], T=200, H=2, with_h0=True)
+    x = synthetic.make_inputs(w, beta_zero=True)
+    check(x)
+    check(x, n_segments=2)
+
+
+def test_scale_override():
+    x = synthetic.make_inputs(synthetic.small(W["tiny_dense_f32"], T=130))
+    o1, _ = run_gpu(x)
+    o2, _ = run_gpu(x, scale=0.5)
+    s = 1 / math.sqrt(x["K"])
+    torch.testing.assert_close(o2, o1 * (0.5 / s), rtol=1e-5, atol=1e-6)
+
+
+# --------------------------------------------------------------------------
+# bit identity, graph capture, poisoning, status, host entry, workspace
+# --------------------------------------------------------------------------
+def _bits(t):
+    return t.detach().contiguous().view(torch.uint8).cpu()
+
+
+@pytest.mark.parametrize("S", [1, 4])
+def test_bit_identical_across_plans_and_repeats(S):
+    w = synthetic.small(W["wide_varlen_bf16"], H=2)
+    x = synthetic.make_inputs(w, lengths=RAGGED)
+    ref_o, ref_h = run_gpu(x, n_segments=S, force_bv=64)
+    for bv in (16, 32, 64, 64):
+        o, ht = run_gpu(x, n_segments=S, force_bv=bv)
+        assert torch.equal(_bits(o), _bits(ref_o)), bv
+        assert torch.equal(_bits(ht), _bits(ref_h)), bv
+
+
+def test_graph_capture_matches_eager():
+    import chunked_gated_delta_rule_gb300 as pkg
+    x = to_dev(synthetic.make_inputs(synthetic.small(W["wide_varlen_bf16"], H=2),
+                                     lengths=RAGGED))
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"])
+    o_e, ht_e = pkg.gdr_chunk_fwd(*args, cu_seqlens=x["cu_seqlens"])
+    o = torch.full_like(o_e, float("nan"))
+    ht = torch.full_like(ht_e, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        pkg.gdr_chunk_fwd(*args, cu_seqlens=x["cu_seqlens"], o=o, ht=ht)  # warm-up
+        torch.cuda.synchronize()
+        o.fill_(float("nan"))
+        with torch.cuda.graph(graph, stream=s):
+            pkg.gdr_chunk_fwd(*args, cu_seqlens=x["cu_seqlens"], o=o, ht=ht)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(o), _bits(o_e))
+    assert torch.equal(_bits(ht), _bits(ht_e))
+
+
+def test_nan_poisoned_outputs_are_fully_written():
+    import chunked_gated_delta_rule_gb300 as pkg
+    x = to_dev(synthetic.make_inputs(synthetic.small(W["wide_varlen_bf16"], H=2),
+                                     lengths=RAGGED))
+    o = torch.full(x["v"].shape, float("nan"), dtype=x["v"].dtype, device="cuda")
+    ht = torch.full((len(RAGGED), 2, 128, 128), float("nan"), device="cuda")
+    pkg.gdr_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu_seqlens=x["cu_seqlens"],
+                      o=o, ht=ht)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all()
+    assert torch.isfinite(ht).all()
+
+
+def test_status_word_reports_malformed_cu_seqlens():
+    import chunked_gated_delta_rule_gb300 as pkg
+    x = to_dev(synthetic.make_inputs(synthetic.small(W["wide_varlen_bf16"], H=1),
+                                     lengths=[64, 64, 64]))
+    cu = torch.tensor([0, 100, 50, 192], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = torch.full(x["v"].shape, 7.0, dtype=x["v"].dtype, device="cuda")
+    pkg.gdr_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu_seqlens=cu, o=o,
+                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -5
+    assert bool((o == 7.0).all())  # nothing computed
+
+
+def test_host_entry_matches_device_entry():
+    import chunked_gated_delta_rule_gb300 as pkg
+    x = synthetic.make_inputs(synthetic.small(W["wide_varlen_bf16"], H=2), lengths=RAGGED)
+    o_d, ht_d = run_gpu(x)
+    pin = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()}
+    o_h, ht_h = pkg.gdr_chunk_fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"],
+                                       cu_seqlens=pin["cu_seqlens"])
+    assert torch.equal(_bits(o_h), _bits(o_d))
+    assert torch.equal(_bits(ht_h), _bits(ht_d))
+
+
+def test_caller_workspace_matches_internal_allocation():
+    import chunked_gated_delta_rule_gb300 as pkg
+    x = synthetic.make_inputs(synthetic.small(W["wide_varlen_bf16"], H=2), lengths=RAGGED)
+    o_a, ht_a = run_gpu(x, n_segments=2)
+    nbytes = pkg.gdr_workspace_size(1, x["T"], 2, 128, 128, N=len(RAGGED), n_segments=2)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    o_b, ht_b = run_gpu(x, n_segments=2, workspace=ws)
+    assert torch.equal(_bits(o_a), _bits(o_b))
+    assert torch.equal(_bits(ht_a), _bits(ht_b))
+    with pytest.raises(pkg.GdrError):
+        run_gpu(x, n_segments=2, workspace=ws[: nbytes // 2])

@@ -1,0 +1,56 @@
+"""GPU parity at the full workload sizes, in the plan the benchmark times
+(n_segments=0) and at forced segment counts.  Where the FP64 oracle over
+every (sequence, head) pair would take too long, a fixed sample of pairs is
+checked element by element (the oracle computes pairs independently)."""
+import numpy as np
+import pytest
+
+from chunked_gated_delta_rule_gb300 import synthetic
+from gpu_util import TOL_BF16, rel_l2_masked, run_gpu, run_oracle, sample_mask
+
+pytestmark = pytest.mark.gpu
+
+W = synthetic.WORKLOADS
+
+_cache = {}
+
+
+def reference(name, pairs=None):
+    key = (name, tuple(pairs) if pairs else None)
+    if key not in _cache:
+        x = synthetic.make_inputs(W[name])
+        mask = None if pairs is None else sample_mask(x["N"], x["H"], pairs)
+        _cache[key] = (x, run_oracle(x, pair_mask=mask))
+    return _cache[key]
+
+
+def check(name, pairs=None, **kw):
+    x, (ro, rht) = reference(name, pairs)
+    o, ht = run_gpu(x, **kw)
+    eo, eh = rel_l2_masked(o, ro), rel_l2_masked(ht, rht)
+    print(f"{name} {kw}: rel_l2 o={eo:.3e} ht={eh:.3e}")
+    assert eo <= TOL_BF16 and eh <= TOL_BF16, (eo, eh)
+
+
+def test_wide_varlen_all_pairs():
+    check("wide_varlen_bf16", n_segments=0)
+
+
+@pytest.mark.parametrize("S", [0, 1, 2, 4, 8, 16])
+def test_long_16k(S):
+    check("long_16k_bf16", pairs=[(0, 0), (0, 5), (0, 10), (0, 15)], n_segments=S)
+
+
+@pytest.mark.parametrize("S", [0, 1, 16])
+def test_stress_64k_h8(S):
+    check("stress_64k_h8_bf16", pairs=[(0, 0), (0, 7)], n_segments=S)
+
+
+@pytest.mark.parametrize("S", [0, 1, 16])
+def test_stress_64k_h1(S):
+    check("stress_64k_h1_bf16", n_segments=S)
+
+
+@pytest.mark.parametrize("S", [0, 1, 8])
+def test_gla_k256_v512(S):
+    check("gla_k256_v512_bf16", pairs=[(0, 0), (1, 3)], n_segments=S)
