@@ -39,7 +39,7 @@ class gdr_options(ctypes.Structure):
 
 
 # Every symbol include/gdr.h declares.
-EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_host",
+EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_host", "gdr_chunk_fwd_noalloc",
            "gdr_workspace_size", "gdr_plan_query", "gdr_kernel_name", "gdr_error_string",
            "gdr_version")
 
@@ -73,6 +73,8 @@ def load_library():
         lib.gdr_chunk_fwd_ex.restype = ctypes.c_int
         lib.gdr_chunk_fwd_host.argtypes = fwd_args + [vp]
         lib.gdr_chunk_fwd_host.restype = ctypes.c_int
+        lib.gdr_chunk_fwd_noalloc.argtypes = fwd_args + [vp]
+        lib.gdr_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.gdr_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.c_int]
         lib.gdr_workspace_size.restype = ctypes.c_size_t
         lib.gdr_plan_query.argtypes = [dims_p, ctypes.c_int, ctypes.c_int,
@@ -233,6 +235,48 @@ def gdr_chunk_fwd_host(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_seg
     rc = lib.gdr_chunk_fwd_host(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                 _ptr(beta), _ptr(cu_seqlens), _ptr(h0), _ptr(o), _ptr(ht),
                                 int(n_segments), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise GdrError(rc)
+    return o, ht
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def gdr_chunk_fwd_noalloc(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments=0,
+                          output_final_state=True, o=None, ht=None, stream=None):
+    """Forward pass through ``gdr_chunk_fwd_noalloc``: the library uses a
+    fixed 64 MiB device array as scratch and allocates nothing, for callers
+    that must not allocate device memory during the call.  ``o`` and ``ht``
+    should be passed in by such callers (this wrapper creates them with
+    torch only when they are omitted).  Calls that overlap on the GPU share
+    the one scratch array and must be ordered by the caller; the first call
+    on a device should happen outside CUDA graph capture."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr_chunk_fwd_noalloc takes CUDA tensors")
+    _check("q", q, None, dev)
+    for name, t in (("k", k), ("v", v)):
+        _check(name, t, q.dtype, dev)
+    _check("g", g, torch.float32, dev)
+    _check("beta", beta, torch.float32, dev)
+    _check("cu_seqlens", cu_seqlens, torch.int32, dev)
+    _check("h0", h0, torch.float32, dev)
+    dims = _dims_of(q, v, cu_seqlens)
+    nseq = dims.N if dims.N else dims.B
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    if ht is None and output_final_state:
+        ht = torch.empty(nseq, dims.H, dims.K, dims.V, dtype=torch.float32, device=dev)
+    _check("o", o, q.dtype, dev)
+    _check("ht", ht, torch.float32, dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdr_chunk_fwd_noalloc(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                       _ptr(beta), _ptr(cu_seqlens), _ptr(h0), _ptr(o), _ptr(ht),
+                                       int(n_segments), ctypes.c_void_p(stream.cuda_stream))
     if rc != 0:
         raise GdrError(rc)
     return o, ht

@@ -151,6 +151,29 @@ int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k,
                        const int32_t *cu_seqlens, const float *h0, void *o,
                        float *ht, int n_segments, gdr_stream_t stream);
 
+/*
+ * gdr_chunk_fwd_noalloc -- gdr_chunk_fwd that allocates nothing.  The pages
+ * describe no counterpart; this entry point exists for callers that cannot
+ * let a library allocate device memory while they run (engines that reserve
+ * nearly all HBM up front and treat a later allocation as a failure,
+ * frameworks that own the allocator, code where an allocation call is not
+ * allowed or would block).  Its scratch is a 64 MiB array inside the library,
+ * held on every GPU that loads the library until the process exits.
+ *   - Same arguments, layouts and results as gdr_chunk_fwd; device buffers,
+ *     work enqueued on `stream`, no synchronisation.
+ *   - Returns GDR_ERR_WORKSPACE, computing nothing, when the problem needs
+ *     more than 64 MiB of scratch (gdr_workspace_size tells in advance).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call outside stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (several
+ *     streams or host threads) race on it; order them.  No part of the
+ *     scratch has to start at zero.
+ */
+int gdr_chunk_fwd_noalloc(const gdr_dims *dims, const void *q, const void *k,
+                          const void *v, const float *g, const float *beta,
+                          const int32_t *cu_seqlens, const float *h0, void *o,
+                          float *ht, int n_segments, gdr_stream_t stream);
+
 /* Bytes of device scratch gdr_chunk_fwd_ex needs for this problem
  * (beta_free != 0 for the beta-free mode).  0 on invalid arguments. */
 size_t gdr_workspace_size(const gdr_dims *dims, int beta_free,
