@@ -38,6 +38,9 @@ class gdr_options(ctypes.Structure):
                 ("launch_ids", ctypes.c_void_p), ("n_launches", ctypes.c_void_p)]
 
 
+# Diagnostic entry points declared in include/gdr_selftest.h.
+SELFTEST_EXPORTS = ("gdr_selftest_umma", "gdr_selftest_tma")
+
 # Every symbol include/gdr.h declares.
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_host", "gdr_chunk_fwd_noalloc",
            "gdr_workspace_size", "gdr_plan_query", "gdr_kernel_name", "gdr_error_string",
@@ -84,6 +87,12 @@ def load_library():
         lib.gdr_kernel_name.restype = ctypes.c_char_p
         lib.gdr_error_string.argtypes = [ctypes.c_int]
         lib.gdr_error_string.restype = ctypes.c_char_p
+        lib.gdr_selftest_umma.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, vp, vp]
+        lib.gdr_selftest_umma.restype = ctypes.c_int
+        lib.gdr_selftest_tma.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+        lib.gdr_selftest_tma.restype = ctypes.c_int
         lib.gdr_version.argtypes = []
         lib.gdr_version.restype = ctypes.c_int
         _lib = lib
@@ -294,6 +303,32 @@ def gdr_plan_query(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, n_segmen
     if rc != 0:
         raise GdrError(rc)
     return dict(path=plan.path, bv=plan.bv, n_segments=plan.n_segments)
+
+
+def gdr_selftest_umma(A, B, a_mn, b_mn, status=None):
+    """D = A @ B^T (A [128, Kd], B [N, Kd] BF16 CUDA tensors) computed by one
+    tcgen05 MMA chain with the given operand layouts; returns D (FP32)."""
+    N, Kd = B.shape
+    D = torch.full((A.shape[0], N), float("nan"), dtype=torch.float32, device=A.device)
+    rc = load_library().gdr_selftest_umma(_ptr(A), _ptr(B), _ptr(D), N, Kd, int(a_mn), int(b_mn),
+                                          _ptr(status),
+                                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if rc != 0:
+        raise GdrError(rc)
+    return D
+
+
+def gdr_selftest_tma(src, t0, h, k0, status=None):
+    """One 64x64 box of src [T, H, K] (BF16 CUDA) through TMA + the swizzle
+    address map; returns the [64, 64] box."""
+    T, H, K = src.shape
+    out = torch.full((64, 64), float("nan"), dtype=torch.bfloat16, device=src.device)
+    rc = load_library().gdr_selftest_tma(_ptr(src), T, H, K, int(t0), int(h), int(k0), _ptr(out),
+                                         _ptr(status),
+                                         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if rc != 0:
+        raise GdrError(rc)
+    return out
 
 
 def gdr_kernel_name(kid: int) -> str:

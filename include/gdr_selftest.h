@@ -1,0 +1,40 @@
+/*
+ * gdr_selftest.h -- diagnostic entry points of libgdr.so.  They exercise, on
+ * the GPU, the tensor-core building blocks the fused forward path uses, so a
+ * test can compare them with a library matmul before trusting the fused
+ * kernels.  The pages describe no counterpart (they are tests of this
+ * implementation's own operand layouts).  Device pointers; work enqueued on
+ * `stream`; `status` (device int32, may be NULL) receives GDR_ERR_TIMEOUT if
+ * a bounded wait expires.  Return GDR_OK or a GDR_ERR_* code (gdr.h).
+ */
+#ifndef GDR_SELFTEST_H_
+#define GDR_SELFTEST_H_
+
+#include <stdint.h>
+
+#include "gdr.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* D[128][N] (FP32, row-major) = A[128][Kd] * B[N][Kd]^T with A, B BF16
+ * row-major, computed by tcgen05.mma (kind::f16) with A staged K-major
+ * (a_mn = 0) or MN-major (a_mn = 1), and B likewise (b_mn), both with the
+ * 128-byte swizzle.  N in {64, 128}, Kd in {64, 128}. */
+int gdr_selftest_umma(const void *A, const void *B, float *D, int N, int Kd,
+                      int a_mn, int b_mn, int32_t *status, gdr_stream_t stream);
+
+/* out[64][64] (BF16) = src[t0 + r][h][k0 + c] for r, c < 64 (zero past T),
+ * src a BF16 [T][H][K] tensor, loaded as one TMA box with the 128-byte
+ * swizzle and read back through the library's swizzle address map.
+ * k0 a multiple of 8 with k0 + 64 <= K. */
+int gdr_selftest_tma(const void *src, int64_t T, int64_t H, int64_t K, int t0,
+                     int h, int k0, void *out, int32_t *status,
+                     gdr_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_SELFTEST_H_ */

@@ -12,6 +12,8 @@ from chunked_gated_delta_rule_gb300 import api
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdr.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -21,14 +23,17 @@ def lib():
     return pkg.load_library()
 
 
-def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gdr_[a-z_0-9]+)\s*\(", text)))
+def declared_functions(paths=None):
+    names = set()
+    for path in paths or HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names |= set(re.findall(r"\b(gdr_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_expected_entry_points():
-    assert declared_functions() == sorted(api.EXPORTS)
+    assert declared_functions([HEADER]) == sorted(api.EXPORTS)
+    assert declared_functions() == sorted(api.EXPORTS + api.SELFTEST_EXPORTS)
 
 
 def test_library_exports_every_declared_symbol(lib):
