@@ -169,16 +169,20 @@ def gpu_index_for_smi():
 # algorithmic bytes per kernel launch (units: token-heads, chunk-heads,
 # sequence-heads; figures stated in DESIGN.md "Measurement")
 # ----------------------------------------------------------------------------
-def counts(x):
-    import torch
+def counts(x, n_segments=1):
     H = x["H"]
     if x["cu_seqlens"] is not None:
         lens = (x["cu_seqlens"][1:] - x["cu_seqlens"][:-1]).tolist()
     else:
         lens = [x["T"]] * x["B"]
     chunks = sum((L + 63) // 64 for L in lens)
+    segs = 0
+    for L in lens:  # runs of ceil(chunks / S) whole chunks per sequence
+        nc = (L + 63) // 64
+        per = -(-nc // max(1, n_segments)) if nc else 0
+        segs += -(-nc // per) if per else 0
     return dict(tokens=sum(lens), token_heads=sum(lens) * H, chunk_heads=chunks * H,
-                seq_heads=len(lens) * H, n_seqs=len(lens), chunks=chunks)
+                seq_heads=len(lens) * H, n_seqs=len(lens), chunks=chunks, segments=segs * H)
 
 
 def algorithmic_bytes(kernel, x, c):
@@ -187,8 +191,14 @@ def algorithmic_bytes(kernel, x, c):
     delta = x["beta"] is not None
     th, ch, sh = c["token_heads"], c["chunk_heads"], c["seq_heads"]
     states = sh * K * V * 4 * ((1 if x["h0"] is not None else 0) + 1)
-    if kernel == "call":  # whole forward pass: inputs once, outputs once
+    if kernel in ("call", "tc_chain_serial"):
+        # whole forward pass (the fused serial chain kernel does all of it):
+        # q, k, v, g, beta read once, o written once, h0 / ht once
         return th * ((2 * K + V) * es + 4 + (4 if delta else 0) + V * es) + states
+    if kernel == "tc_chain_prescan":  # k, v, g, beta read; c_s and M_s written
+        return th * ((K + V) * es + 8) + c["segments"] * K * (K + V) * 4
+    if kernel == "tc_chain_segment_out":  # q, k, v, g, beta read, o written, h_s read
+        return th * ((2 * K + V) * es + 8 + V * es) + c["segments"] * K * V * 4
     if kernel == "simt_prep":
         b = th * 4 + ch * 64 * 4
         if delta:
@@ -335,10 +345,9 @@ def run_gdr(args):
     torch.cuda.set_device(dev)
     w = synthetic.WORKLOADS[args.workload]
     x = synthetic.make_inputs(w)
-    c = counts(x)
     d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
     o = torch.empty_like(d["v"])
-    ht = torch.empty(c["n_seqs"], x["H"], x["K"], x["V"], dtype=torch.float32, device=dev)
+    ht = torch.empty(x["N"], x["H"], x["K"], x["V"], dtype=torch.float32, device=dev)
     kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], o=o, ht=ht, n_segments=args.segments,
               force_path=args.force_path)
     args_t = (d["q"], d["k"], d["v"], d["g"], d["beta"])
@@ -346,6 +355,9 @@ def run_gdr(args):
                               x["cu_seqlens"] is not None else 0,
                               dtype=0 if x["dtype"] == "f32" else 1,
                               beta_free=x["beta"] is None, n_segments=args.segments)
+    if args.force_path:
+        plan["path"] = args.force_path
+    c = counts(x, plan["n_segments"])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 

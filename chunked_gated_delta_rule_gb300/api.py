@@ -39,7 +39,7 @@ class gdr_options(ctypes.Structure):
 
 
 # Diagnostic entry points declared in include/gdr_selftest.h.
-SELFTEST_EXPORTS = ("gdr_selftest_umma", "gdr_selftest_tma")
+SELFTEST_EXPORTS = ("gdr_selftest_umma", "gdr_selftest_tma", "gdr_selftest_inverse")
 
 # Every symbol include/gdr.h declares.
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_host", "gdr_chunk_fwd_noalloc",
@@ -93,6 +93,8 @@ def load_library():
         lib.gdr_selftest_tma.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
         lib.gdr_selftest_tma.restype = ctypes.c_int
+        lib.gdr_selftest_inverse.argtypes = [vp, vp, vp]
+        lib.gdr_selftest_inverse.restype = ctypes.c_int
         lib.gdr_version.argtypes = []
         lib.gdr_version.restype = ctypes.c_int
         _lib = lib
@@ -329,6 +331,18 @@ def gdr_selftest_tma(src, t0, h, k0, status=None):
     if rc != 0:
         raise GdrError(rc)
     return out
+
+
+def gdr_selftest_inverse(A):
+    """(I + tril(A, -1))^-1 for a 64x64 FP32 CUDA tensor, by the device routine
+    of the tensor-core path."""
+    A = A.contiguous()
+    T = torch.full_like(A, float("nan"))
+    rc = load_library().gdr_selftest_inverse(_ptr(A), _ptr(T),
+                                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if rc != 0:
+        raise GdrError(rc)
+    return T
 
 
 def gdr_kernel_name(kid: int) -> str:

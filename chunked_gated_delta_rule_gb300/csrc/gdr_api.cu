@@ -65,21 +65,28 @@ int auto_segments(const gdr_dims &d, int bv) {
     return S;
 }
 
+// Shapes the tensor-core path covers (pointer alignment is checked per call).
+bool tc_shape(const gdr_dims &d, bool beta_free) {
+    return d.dtype == GDR_BF16 && d.K == 128 && d.V == 128 && !beta_free;
+}
+
 int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_options *opt,
               gdr_plan *plan) {
-    (void)beta_free;
     gdr_plan p{};
-    p.path = 1;
-    p.bv = pick_bv(d);
+    p.path = tc_shape(d, beta_free) ? 2 : 1;
+    p.bv = p.path == 2 ? 128 : pick_bv(d);
+    if (opt && opt->force_path) {
+        if (opt->force_path != 1 && opt->force_path != 2) return GDR_ERR_INVALID;
+        if (opt->force_path == 2 && !tc_shape(d, beta_free)) return GDR_ERR_UNSUPPORTED;
+        p.path = opt->force_path;
+        p.bv = p.path == 2 ? 128 : pick_bv(d);
+    }
     if (opt && opt->force_bv) {
         const int bv = opt->force_bv;
-        if (bv != 16 && bv != 32 && bv != 64) return GDR_ERR_INVALID;
-        if (d.V % bv || d.K % bv) return GDR_ERR_UNSUPPORTED;
+        if (bv != 16 && bv != 32 && bv != 64 && bv != 128) return GDR_ERR_INVALID;
+        if (p.path == 1 && (bv == 128 || d.V % bv || d.K % bv)) return GDR_ERR_UNSUPPORTED;
+        if (p.path == 2 && bv != 128) return GDR_ERR_UNSUPPORTED;
         p.bv = bv;
-    }
-    if (opt && opt->force_path) {
-        if (opt->force_path != 1) return GDR_ERR_UNSUPPORTED;
-        p.path = opt->force_path;
     }
     if (n_segments < 0) return GDR_ERR_INVALID;
     if (n_segments > kMaxSegments) return GDR_ERR_UNSUPPORTED;
@@ -90,8 +97,9 @@ int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_optio
 
 }  // namespace
 
-WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S) {
+WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int path) {
     const bool delta = !beta_free;
+    const bool simt = path == 1;
     const int64_t mc = max_chunks_of(d);
     const int64_t ns = n_seqs(d);
     const size_t H = (size_t)d.H, K = (size_t)d.K, V = (size_t)d.V;
@@ -106,11 +114,11 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S) {
     L.off_tab = take(sizeof(int32_t) * 4 * (size_t)mc);
     L.off_seq0 = take(sizeof(int32_t) * (size_t)(ns + 1));
     L.off_nchunks = take(sizeof(int32_t));
-    L.off_G = take(sizeof(float) * (size_t)mc * H * kChunk);
-    L.off_W = take(delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
-    L.off_U = take(delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
-    L.off_hpre = take(sizeof(float) * (size_t)mc * H * K * V);
-    L.off_vnew = take(delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
+    L.off_G = take(simt ? sizeof(float) * (size_t)mc * H * kChunk : 0);
+    L.off_W = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
+    L.off_U = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
+    L.off_hpre = take(simt ? sizeof(float) * (size_t)mc * H * K * V : 0);
+    L.off_vnew = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
     const size_t segs = S > 1 ? (size_t)ns * H * (size_t)S : 0;
     L.off_segM = take(delta ? sizeof(float) * segs * K * K : 0);
     L.off_segC = take(sizeof(float) * segs * K * V);
@@ -163,10 +171,26 @@ int run_simt(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaSt
         GDR_LAUNCH(rec, kKScanSerial, simt_scan(p, ws, 0, plan.bv, st));
     } else {
         GDR_LAUNCH(rec, kKScanPre, simt_scan(p, ws, 1, plan.bv, st));
-        GDR_LAUNCH(rec, kKCompose, simt_compose(p, ws, plan.bv, st));
+        if (compose_mt_supported(p))
+            GDR_LAUNCH(rec, kKCompose, compose_mt(p, ws, st));
+        else
+            GDR_LAUNCH(rec, kKCompose, simt_compose(p, ws, plan.bv, st));
         GDR_LAUNCH(rec, kKScanSegOut, simt_scan(p, ws, 2, plan.bv, st));
     }
     GDR_LAUNCH(rec, kKOutput, simt_output(p, ws, st));
+    return GDR_OK;
+}
+
+int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStream_t st,
+           LaunchRecorder &rec) {
+    GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
+    if (plan.n_segments <= 1) {
+        GDR_LAUNCH(rec, kKTcSerial, tc_chain(p, ws, 0, st));
+    } else {
+        GDR_LAUNCH(rec, kKTcPre, tc_chain(p, ws, 1, st));
+        GDR_LAUNCH(rec, kKCompose, compose_mt(p, ws, st));
+        GDR_LAUNCH(rec, kKTcSegOut, tc_chain(p, ws, 2, st));
+    }
     return GDR_OK;
 }
 
@@ -188,6 +212,9 @@ const char *gdr_kernel_name(int id) {
     case kKCompose: return "simt_compose";
     case kKScanSegOut: return "simt_scan_segment_out";
     case kKOutput: return "simt_output";
+    case kKTcSerial: return "tc_chain_serial";
+    case kKTcPre: return "tc_chain_prescan";
+    case kKTcSegOut: return "tc_chain_segment_out";
     default: return "?";
     }
 }
@@ -216,7 +243,7 @@ size_t gdr_workspace_size(const gdr_dims *dims, int beta_free, int n_segments) {
     if (validate_dims(dims) != GDR_OK) return 0;
     gdr_plan plan;
     if (make_plan(*dims, beta_free != 0, n_segments, nullptr, &plan) != GDR_OK) return 0;
-    return workspace_layout(*dims, beta_free != 0, plan.n_segments).total;
+    return workspace_layout(*dims, beta_free != 0, plan.n_segments, plan.path).total;
 }
 
 int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const void *v,
@@ -243,8 +270,13 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
     p.scale = (opt && opt->scale > 0.f) ? opt->scale : 1.0f / std::sqrt((float)dims->K);
     p.status = opt ? opt->status : nullptr;
     if (p.N == 0) return GDR_OK;
+    if (plan.path == 2 && !tc_supported(p)) {
+        if (opt && opt->force_path == 2) return GDR_ERR_INVALID;  // misaligned pointers
+        plan.path = 1;
+        plan.bv = pick_bv(*dims);
+    }
 
-    const WorkspaceLayout L = workspace_layout(*dims, beta_free, plan.n_segments);
+    const WorkspaceLayout L = workspace_layout(*dims, beta_free, plan.n_segments, plan.path);
     void *base = nullptr;
     bool owned = false;
     if (opt && opt->workspace) {
@@ -264,7 +296,7 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
         rec.ids = opt->launch_ids;
         if (!opt->events && opt->launch_ids) rec.max_launches = opt->max_launches;
     }
-    rc = run_simt(p, ws, plan, st, rec);
+    rc = plan.path == 2 ? run_tc(p, ws, plan, st, rec) : run_simt(p, ws, plan, st, rec);
     if (opt && opt->n_launches) *opt->n_launches = rec.count;
     if (owned) {
         if (cudaFreeAsync(base, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;

@@ -40,7 +40,7 @@ struct Workspace {
     float *U;             // [max_chunks][H][64][V]   (delta mode)
     float *hpre;          // [max_chunks][H][K][V]: state before each chunk
     float *vnew;          // [max_chunks][H][64][V]   (delta mode)
-    float *segM;          // [N][H][S][K][K] transition per segment (delta)
+    float *segM;          // [N][H][S][K][K] transition per segment (delta), transposed
     float *segC;          // [N][H][S][K][V] local state per segment
     float *segH;          // [N][H][S][K][V] composed initial state per segment
     float *segD;          // [N][H][S] scalar transition (beta-free)
@@ -55,7 +55,9 @@ struct WorkspaceLayout {
     int64_t max_chunks;
 };
 
-WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int n_segments);
+// path 1: CUDA-core path (chunk table, G, W, U, h_pre, v_new, segments);
+// path 2: tensor-core path (chunk table and segment summaries only).
+WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int n_segments, int path);
 Workspace carve_workspace(void *base, const WorkspaceLayout &L, int n_segments);
 
 // Kernel ids reported through gdr_options.launch_ids.
@@ -67,6 +69,9 @@ enum KernelId {
     kKCompose = 4,
     kKScanSegOut = 5,
     kKOutput = 6,
+    kKTcSerial = 7,
+    kKTcPre = 8,
+    kKTcSegOut = 9,
     kKNumIds
 };
 
@@ -102,5 +107,16 @@ cudaError_t simt_scan(const Problem &p, const Workspace &ws, int mode, int bv,
 cudaError_t simt_compose(const Problem &p, const Workspace &ws, int bv,
                          cudaStream_t st);
 cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st);
+// Composition for the delta rule with K <= 128 and V % 32 == 0 (both paths):
+// bulk-copied transposed transitions, 32 value columns per CTA.
+bool compose_mt_supported(const Problem &p);
+cudaError_t compose_mt(const Problem &p, const Workspace &ws, cudaStream_t st);
+
+// ---- tensor-core path (BF16, K = V = 128, delta rule) ---------------------
+// Shapes and pointer alignment the fused chain kernel takes.
+bool tc_supported(const Problem &p);
+// mode 0: serial scan + output (h0 -> ht); 1: segment pre-scan (c_s and M_s
+// chains); 2: segment output pass from the composed segment states.
+cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream_t st);
 
 }  // namespace gdr

@@ -6,6 +6,7 @@
 #include "gdr_internal.cuh"
 #include "gdr_selftest.h"
 #include "tc_common.cuh"
+#include "tc_inverse.cuh"
 #include "tma_host.cuh"
 
 namespace gdr {
@@ -110,10 +111,36 @@ k_selftest_tma(const __grid_constant__ CUtensorMap map, __nv_bfloat16 *__restric
     }
 }
 
+// T = (I + A)^-1 for one strictly lower 64 x 64 FP32 matrix, through the same
+// device routine the tensor-core chain kernel uses.
+__global__ void __launch_bounds__(256) k_selftest_inverse(const float *__restrict__ A,
+                                                          float *__restrict__ T) {
+    __shared__ float sA[64 * kInvLd];
+    __shared__ float sT[64 * kInvLd];
+    __shared__ float sX[3 * 16 * kInvXLd];
+    const int tid = threadIdx.x;
+    for (int idx = tid; idx < 64 * 64; idx += 256) {
+        const int i = idx >> 6, j = idx & 63;
+        sA[i * kInvLd + j] = j < i ? A[idx] : 0.f;
+    }
+    __syncthreads();
+    invert_unit_lower64(sA, sT, sX, tid);
+    for (int idx = tid; idx < 64 * 64; idx += 256) {
+        const int i = idx >> 6, j = idx & 63;
+        T[idx] = j <= i ? sT[i * kInvLd + j] : 0.f;
+    }
+}
+
 }  // namespace
 }  // namespace gdr
 
 using namespace gdr;
+
+extern "C" int gdr_selftest_inverse(const float *A, float *T, gdr_stream_t stream) {
+    if (!A || !T) return GDR_ERR_INVALID;
+    k_selftest_inverse<<<1, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(A, T);
+    return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
 
 extern "C" int gdr_selftest_umma(const void *A, const void *B, float *D, int N, int Kd,
                                  int a_mn, int b_mn, int32_t *status, gdr_stream_t stream) {

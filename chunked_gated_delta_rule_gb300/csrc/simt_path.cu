@@ -327,8 +327,8 @@ k_scan(Problem p, Workspace ws, int mode) {
     } else if (mode == 1) {
         for (int idx = tid; idx < K * BV; idx += kThreads) {
             const int key = idx / BV, c = idx - key * BV;
-            if (trans)
-                ws.segM[(seg_base * K + key) * K + col0 + c] = hs[key * ldh + c];
+            if (trans)  // stored transposed: row m of M^T is column m of M
+                ws.segM[(seg_base * K + col0 + c) * K + key] = hs[key * ldh + c];
             else
                 ws.segC[(seg_base * K + key) * V + col0 + c] = hs[key * ldh + c];
         }
@@ -338,7 +338,9 @@ k_scan(Problem p, Workspace ws, int mode) {
 
 // A9: ordered composition over the segments of one (sequence, head, value
 // tile): records each segment's initial state and h_{s+1} = M_s h_s + c_s
-// (beta-free: d_s h_s + c_s); the last state is ht.
+// (beta-free: d_s h_s + c_s); the last state is ht.  M_s is stored
+// transposed.  Used for the beta-free mode and for K > 128 (the delta rule
+// with K <= 128 uses k_compose_mt in compose.cu).
 template <int BV>
 __global__ void __launch_bounds__(kThreads)
 k_compose(Problem p, Workspace ws) {
@@ -375,7 +377,7 @@ k_compose(Problem p, Workspace ws) {
             float acc;
             if (delta) {
                 acc = 0.f;
-                for (int m = 0; m < K; ++m) acc = fmaf(M[(int64_t)key * K + m], hs[m * ldh + c], acc);
+                for (int m = 0; m < K; ++m) acc = fmaf(M[(int64_t)m * K + key], hs[m * ldh + c], acc);
                 acc += C[(int64_t)key * V + col0 + c];
             } else {
                 acc = fmaf(d, hs[key * ldh + c], C[(int64_t)key * V + col0 + c]);

@@ -87,6 +87,17 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// 1-D bulk copy global -> shared (16-B aligned addresses, size a multiple of
+// 16), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -141,6 +152,87 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
                    "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                  :
                  : "memory");
+}
+
+// 32 data-path lanes x 32-bit, 32 consecutive columns, waited.
+__device__ __forceinline__ void tmem_load32f(uint32_t taddr, float (&f)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),
+                   "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
+                   "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------- warp MMA
+// Round-to-nearest TF32 value of x (kept in a 32-bit register).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// D(16x8) += A(16x8, row) * B(8x8, col) with TF32 operands, FP32 accumulate.
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4],
+                                                const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// acc(16x16) += A(16x16) * B(16x16), both row-major FP32 in shared memory
+// with leading dimensions lda / ldb, as three TF32 products per step
+// (a_lo b_hi + a_hi b_lo + a_hi b_hi with x = hi + lo), which keeps close to
+// FP32 accuracy.  acc[nt] holds the 16x8 output column block nt in the
+// mma accumulator layout: rows (lane/4, lane/4 + 8), columns 2(lane%4) + {0,1}.
+__device__ __forceinline__ void warp_gemm16_3xtf32(float (&acc)[2][4], const float *A, int lda,
+                                                   const float *B, int ldb, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const float av[4] = {A[g * lda + 8 * ks + t], A[(g + 8) * lda + 8 * ks + t],
+                             A[g * lda + 8 * ks + t + 4], A[(g + 8) * lda + 8 * ks + t + 4]};
+        uint32_t ahi[4], alo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ahi[i] = to_tf32(av[i]);
+            alo[i] = to_tf32(av[i] - __uint_as_float(ahi[i]));
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float bv[2] = {B[(8 * ks + t) * ldb + 8 * nt + g],
+                                 B[(8 * ks + t + 4) * ldb + 8 * nt + g]};
+            uint32_t bhi[2], blo[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                bhi[i] = to_tf32(bv[i]);
+                blo[i] = to_tf32(bv[i] - __uint_as_float(bhi[i]));
+            }
+            mma_tf32_16x8x8(acc[nt], alo, bhi);
+            mma_tf32_16x8x8(acc[nt], ahi, blo);
+            mma_tf32_16x8x8(acc[nt], ahi, bhi);
+        }
+    }
 }
 
 // Loads 16 FP32 columns of this thread's TMEM row.

@@ -33,6 +33,13 @@ int gdr_selftest_tma(const void *src, int64_t T, int64_t H, int64_t K, int t0,
                      int h, int k0, void *out, int32_t *status,
                      gdr_stream_t stream);
 
+/* T[64][64] (FP32, row-major) = (I + A)^-1 for the strictly lower part of
+ * A[64][64] (FP32, row-major; entries on and above the diagonal are
+ * ignored), by the blocked triangular inverse the tensor-core path uses (FP32
+ * diagonal blocks, warp-level 3xTF32 products off the diagonal).  Entries
+ * above the diagonal of T are written as 0. */
+int gdr_selftest_inverse(const float *A, float *T, gdr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -41,18 +41,22 @@ def test_f32_shapes(K, V):
 
 
 RAGGED = [1, 63, 64, 65, 127, 128, 257, 7, 300]
+# 1: CUDA-core FP32 path; 2: tensor-core path (BF16, K = V = 128, delta rule)
+PATHS = [1, 2]
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("S", [1, 2, 4, 16])
-def test_bf16_ragged_varlen(S):
+def test_bf16_ragged_varlen(S, path):
     w = synthetic.small(W["wide_varlen_bf16"], H=3)
-    check(synthetic.make_inputs(w, lengths=RAGGED), n_segments=S)
+    check(synthetic.make_inputs(w, lengths=RAGGED), n_segments=S, force_path=path)
 
 
-def test_bf16_varlen_with_empty_sequences_and_h0():
+@pytest.mark.parametrize("path", PATHS)
+def test_bf16_varlen_with_empty_sequences_and_h0(path):
     w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True)
     x = synthetic.make_inputs(w, lengths=[0, 70, 0, 129, 0])
-    o, ht = run_gpu(x)
+    o, ht = run_gpu(x, force_path=path)
     ro, rht = run_oracle(x)
     assert rel_l2_masked(o, ro) <= TOL_BF16
     assert rel_l2_masked(ht, rht) <= TOL_BF16
@@ -61,10 +65,11 @@ def test_bf16_varlen_with_empty_sequences_and_h0():
     assert torch.equal(ht[4].cpu(), x["h0"][4])
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("S", [1, 2, 3, 4, 8, 16])
-def test_bf16_dense_h0_segments(S):
+def test_bf16_dense_h0_segments(S, path):
     w = synthetic.small(W["long_16k_bf16"], B=2, T=1000, H=2, with_h0=True)
-    check(synthetic.make_inputs(w), n_segments=S)
+    check(synthetic.make_inputs(w), n_segments=S, force_path=path)
 
 
 @pytest.mark.parametrize("S", [1, 4])
@@ -73,12 +78,13 @@ def test_beta_free_k256_v512(S):
     check(synthetic.make_inputs(w), n_segments=S)
 
 
-def test_literal_beta_zero():
+@pytest.mark.parametrize("path", PATHS)
+def test_literal_beta_zero(path):
     """An all-zero beta tensor freezes the state: o_t = e^{G_t} h0^T q_t / sqrt(K)."""
     w = synthetic.small(W["long_16k_bf16"], T=200, H=2, with_h0=True)
     x = synthetic.make_inputs(w, beta_zero=True)
-    check(x)
-    check(x, n_segments=2)
+    check(x, force_path=path)
+    check(x, n_segments=2, force_path=path)
 
 
 def test_scale_override():
@@ -98,13 +104,20 @@ def _bits(t):
 
 @pytest.mark.parametrize("S", [1, 4])
 def test_bit_identical_across_plans_and_repeats(S):
+    """CUDA-core path: every value-tile width gives the same bits; the
+    tensor-core path (one plan per shape) gives the same bits run to run."""
     w = synthetic.small(W["wide_varlen_bf16"], H=2)
     x = synthetic.make_inputs(w, lengths=RAGGED)
-    ref_o, ref_h = run_gpu(x, n_segments=S, force_bv=64)
+    ref_o, ref_h = run_gpu(x, n_segments=S, force_path=1, force_bv=64)
     for bv in (16, 32, 64, 64):
-        o, ht = run_gpu(x, n_segments=S, force_bv=bv)
+        o, ht = run_gpu(x, n_segments=S, force_path=1, force_bv=bv)
         assert torch.equal(_bits(o), _bits(ref_o)), bv
         assert torch.equal(_bits(ht), _bits(ref_h)), bv
+    tc_o, tc_h = run_gpu(x, n_segments=S, force_path=2)
+    for _ in range(3):
+        o, ht = run_gpu(x, n_segments=S, force_path=2)
+        assert torch.equal(_bits(o), _bits(tc_o))
+        assert torch.equal(_bits(ht), _bits(tc_h))
 
 
 def test_graph_capture_matches_eager():
@@ -166,6 +179,13 @@ def test_host_entry_matches_device_entry():
                                        cu_seqlens=pin["cu_seqlens"])
     assert torch.equal(_bits(o_h), _bits(o_d))
     assert torch.equal(_bits(ht_h), _bits(ht_d))
+
+
+def test_default_plan_uses_tensor_core_path_for_bf16_k128():
+    import chunked_gated_delta_rule_gb300 as pkg
+    assert pkg.gdr_plan_query(1, 10456, 16, 128, 128, N=32)["path"] == 2
+    assert pkg.gdr_plan_query(1, 256, 2, 64, 64, dtype=0)["path"] == 1
+    assert pkg.gdr_plan_query(2, 8192, 4, 256, 512, beta_free=True)["path"] == 1
 
 
 def test_caller_workspace_matches_internal_allocation():

@@ -40,3 +40,23 @@ def test_tma_swizzled_box(t0, h, k0):
     rows = min(64, T - t0)
     want[:rows] = src[t0:t0 + rows, h, k0:k0 + 64]
     assert torch.equal(out, want)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_blocked_triangular_inverse(seed):
+    """The chain kernel's (I + A)^-1 (FP32 diagonal blocks, 3xTF32 warp MMAs
+    off the diagonal) against a float64 library inverse, on A shaped like the
+    chunk Gram matrix: beta_i e^{G_i - G_j} (k_i . k_j) with unit keys."""
+    pkg.load_library()
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn(64, 128, generator=g, dtype=torch.float64)
+    k = k / k.norm(dim=1, keepdim=True)
+    beta = torch.sigmoid(torch.randn(64, generator=g, dtype=torch.float64))
+    G = torch.cumsum(torch.nn.functional.logsigmoid(torch.randn(64, generator=g,
+                                                                dtype=torch.float64) + 3), 0)
+    A = torch.tril(beta[:, None] * torch.exp(G[:, None] - G[None, :]) * (k @ k.T), -1)
+    T = api.gdr_selftest_inverse(A.float().cuda())
+    torch.cuda.synchronize()
+    ref = torch.linalg.inv(torch.eye(64, dtype=torch.float64) + A.float().double())
+    err = ((T.double().cpu() - ref).norm() / ref.norm()).item()
+    assert err < 2e-6, err

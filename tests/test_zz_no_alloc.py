@@ -49,8 +49,11 @@ def test_noalloc_matches_allocating_entry_on_two_calls_in_a_row():
 def test_noalloc_refuses_problems_larger_than_its_scratch():
     """Refused on the host before any CUDA call (runs without a GPU)."""
     lib = pkg.load_library()
-    dims = api.make_dims(1, 16384, 16, 128, 128)  # needs far more than 64 MiB
-    assert pkg.gdr_workspace_size(1, 16384, 16, 128, 128) > api.NOALLOC_SCRATCH_BYTES
+    # FP32 inputs run on the CUDA-core path, which keeps per-chunk W, U,
+    # h_pre and v_new in scratch: this size needs far more than 64 MiB
+    dims = api.make_dims(1, 16384, 16, 64, 64, dtype=api.GDR_F32)
+    assert (pkg.gdr_workspace_size(1, 16384, 16, 64, 64, dtype=api.GDR_F32)
+            > api.NOALLOC_SCRATCH_BYTES)
     p = ctypes.c_void_p(0x1000)
     rc = lib.gdr_chunk_fwd_noalloc(ctypes.byref(dims), p, p, p, p, p, None, None, p, p, 0, None)
     assert rc == -6
