@@ -113,7 +113,8 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     };
     L.off_tab = take(sizeof(int32_t) * 4 * (size_t)mc);
     L.off_seq0 = take(sizeof(int32_t) * (size_t)(ns + 1));
-    L.off_nchunks = take(sizeof(int32_t));
+    L.off_nchunks = take(sizeof(int32_t) * 4);
+    L.off_order = take(sizeof(int32_t) * (size_t)ns);
     L.off_G = take(simt ? sizeof(float) * (size_t)mc * H * kChunk : 0);
     L.off_W = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
     L.off_U = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
@@ -134,6 +135,7 @@ Workspace carve_workspace(void *base, const WorkspaceLayout &L, int S) {
     w.chunk_tab = reinterpret_cast<int32_t *>(b + L.off_tab);
     w.seq_chunk0 = reinterpret_cast<int32_t *>(b + L.off_seq0);
     w.n_chunks = reinterpret_cast<int32_t *>(b + L.off_nchunks);
+    w.seq_order = reinterpret_cast<int32_t *>(b + L.off_order);
     w.G = reinterpret_cast<float *>(b + L.off_G);
     w.W = reinterpret_cast<float *>(b + L.off_W);
     w.U = reinterpret_cast<float *>(b + L.off_U);

@@ -34,7 +34,9 @@ struct Problem {
 struct Workspace {
     int32_t *chunk_tab;   // [max_chunks][4]: seq, first flat token, len, chunk-in-seq
     int32_t *seq_chunk0;  // [N+1]: first global chunk of each sequence
-    int32_t *n_chunks;    // [1]: total chunks
+    int32_t *n_chunks;    // [4]: total chunks, then the chain counters of the
+                          // persistent tensor-core kernels (zeroed per call)
+    int32_t *seq_order;   // [N]: sequences by descending chunk count
     float *G;             // [max_chunks][H][64]: chunk-local gate cumsum
     float *W;             // [max_chunks][H][64][K]   (delta mode)
     float *U;             // [max_chunks][H][64][V]   (delta mode)
@@ -50,7 +52,7 @@ struct Workspace {
 
 // Byte layout of the workspace for one problem.
 struct WorkspaceLayout {
-    size_t off_tab, off_seq0, off_nchunks, off_G, off_W, off_U, off_hpre,
+    size_t off_tab, off_seq0, off_nchunks, off_order, off_G, off_W, off_U, off_hpre,
         off_vnew, off_segM, off_segC, off_segH, off_segD, total;
     int64_t max_chunks;
 };

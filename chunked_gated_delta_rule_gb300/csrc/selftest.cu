@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(256) k_selftest_inverse(const float *__restric
                                                           float *__restrict__ T) {
     __shared__ float sA[64 * kInvLd];
     __shared__ float sT[64 * kInvLd];
-    __shared__ float sX[3 * 16 * kInvXLd];
+    __shared__ float sX[kInvScratchFloats];
     const int tid = threadIdx.x;
     for (int idx = tid; idx < 64 * 64; idx += 256) {
         const int i = idx >> 6, j = idx & 63;

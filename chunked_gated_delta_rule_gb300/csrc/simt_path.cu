@@ -43,42 +43,79 @@ __device__ __forceinline__ void report(int32_t *status, int code) {
 // chunk of every sequence.  Malformed cu_seqlens (not non-decreasing, not
 // starting at 0, not ending at T, or more chunks than the table holds) make
 // the call compute nothing and set GDR_ERR_SEQLENS in the status word.
+// Also writes the sequences in descending order of chunk count (a stable
+// counting sort; counts above 127 share the top bucket) for the persistent
+// tensor-core kernels, which take the longest chains first, and zeroes their
+// chain counters.  Up to kSmemSeqs sequences the serial passes run on shared
+// memory; beyond that on global memory.
+constexpr int kSmemSeqs = 8192;
+constexpr int kBuckets = 128;
+
 __global__ void k_chunk_table(const int32_t *__restrict__ cu, int64_t N, int64_t T,
                               int64_t max_chunks, int32_t *__restrict__ tab,
                               int32_t *__restrict__ seq_chunk0,
-                              int32_t *__restrict__ n_chunks, int32_t *status) {
+                              int32_t *__restrict__ n_chunks, int32_t *__restrict__ seq_order,
+                              int32_t *status) {
     __shared__ int s_bad;
-    if (threadIdx.x == 0) {
+    __shared__ int s_hist[kBuckets];
+    __shared__ int s_c0[kSmemSeqs + 1];
+    const bool in_smem = N <= kSmemSeqs;
+    int32_t *c0 = in_smem ? s_c0 : seq_chunk0;  // chunk counts, then prefix offsets
+    for (int b = threadIdx.x; b < kBuckets; b += blockDim.x) s_hist[b] = 0;
+    if (threadIdx.x < 3) n_chunks[1 + threadIdx.x] = 0;
+    if (threadIdx.x == 0) s_bad = (cu && (cu[0] != 0 || cu[N] != T)) ? 1 : 0;
+    __syncthreads();
+    for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
+        const int64_t a = cu ? cu[n] : n * T;
+        const int64_t len = (cu ? cu[n + 1] : (n + 1) * T) - a;
+        if (len < 0) s_bad = 1;
+        const int64_t c = len < 0 ? 0 : (len + kChunk - 1) / kChunk;
+        c0[n] = (int32_t)(c <= max_chunks ? c : max_chunks + 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !s_bad) {
         int64_t acc = 0;
-        int bad = 0;
-        if (cu && (cu[0] != 0 || cu[N] != T)) bad = 1;
-        for (int64_t n = 0; n < N && !bad; ++n) {
-            const int64_t a = cu ? cu[n] : n * T;
-            const int64_t b = cu ? cu[n + 1] : (n + 1) * T;
-            const int64_t len = b - a;
-            if (len < 0) { bad = 1; break; }
-            const int64_t c = (len + kChunk - 1) / kChunk;
-            seq_chunk0[n] = (int32_t)acc;
+        for (int64_t n = 0; n < N; ++n) {
+            const int c = c0[n];
+            ++s_hist[c < kBuckets - 1 ? c : kBuckets - 1];
+            c0[n] = (int32_t)acc;
             acc += c;
-            if (acc > max_chunks) { bad = 1; break; }
+            if (acc > max_chunks) { s_bad = 1; break; }
         }
-        s_bad = bad;
-        *n_chunks = bad ? 0 : (int32_t)acc;
-        if (!bad) seq_chunk0[N] = (int32_t)acc;
-        if (bad) report(status, GDR_ERR_SEQLENS);
+        if (!s_bad) {
+            c0[N] = (int32_t)acc;
+            int run = 0;  // bucket b starts after every longer bucket
+            for (int b = kBuckets - 1; b >= 0; --b) {
+                const int c = s_hist[b];
+                s_hist[b] = run;
+                run += c;
+            }
+            for (int64_t n = 0; n < N; ++n) {
+                const int c = c0[n + 1] - c0[n];
+                seq_order[s_hist[c < kBuckets - 1 ? c : kBuckets - 1]++] = (int32_t)n;
+            }
+        }
+        *n_chunks = s_bad ? 0 : (int32_t)acc;
+        if (s_bad) report(status, GDR_ERR_SEQLENS);
+    } else if (threadIdx.x == 0) {
+        *n_chunks = 0;
+        report(status, GDR_ERR_SEQLENS);
     }
     __syncthreads();
     if (s_bad) {
         for (int64_t n = threadIdx.x; n <= N; n += blockDim.x) seq_chunk0[n] = 0;
+        for (int64_t n = threadIdx.x; n < N; n += blockDim.x) seq_order[n] = (int32_t)n;
         return;
     }
+    if (in_smem)
+        for (int64_t n = threadIdx.x; n <= N; n += blockDim.x) seq_chunk0[n] = c0[n];
     for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
         const int64_t a = cu ? cu[n] : n * T;
         const int64_t len = (cu ? cu[n + 1] : (n + 1) * T) - a;
-        const int32_t c0 = seq_chunk0[n];
-        const int32_t cnt = seq_chunk0[n + 1] - c0;
+        const int32_t first = c0[n];
+        const int32_t cnt = c0[n + 1] - first;
         for (int32_t c = 0; c < cnt; ++c) {
-            int32_t *e = tab + 4 * (int64_t)(c0 + c);
+            int32_t *e = tab + 4 * (int64_t)(first + c);
             const int64_t rem = len - (int64_t)c * kChunk;
             e[0] = (int32_t)n;
             e[1] = (int32_t)(a + (int64_t)c * kChunk);
@@ -486,7 +523,7 @@ cudaError_t set_smem(F *f, size_t bytes) {
 cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool /*check*/,
                              cudaStream_t st) {
     k_chunk_table<<<1, kThreads, 0, st>>>(p.cu, p.N, p.T, ws.max_chunks, ws.chunk_tab,
-                                          ws.seq_chunk0, ws.n_chunks, p.status);
+                                          ws.seq_chunk0, ws.n_chunks, ws.seq_order, p.status);
     return cudaGetLastError();
 }
 

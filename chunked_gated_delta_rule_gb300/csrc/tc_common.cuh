@@ -182,6 +182,23 @@ __device__ __forceinline__ void tmem_load32f(uint32_t taddr, float (&f)[32]) {
     for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
 }
 
+// Stores 32 FP32 columns of this thread's TMEM row (32 data-path lanes x
+// 32-bit, 32 consecutive columns) and waits for the store to complete.
+__device__ __forceinline__ void tmem_store32f(uint32_t taddr, const float (&f)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]),
+        "f"(f[8]), "f"(f[9]), "f"(f[10]), "f"(f[11]), "f"(f[12]), "f"(f[13]), "f"(f[14]),
+        "f"(f[15]), "f"(f[16]), "f"(f[17]), "f"(f[18]), "f"(f[19]), "f"(f[20]), "f"(f[21]),
+        "f"(f[22]), "f"(f[23]), "f"(f[24]), "f"(f[25]), "f"(f[26]), "f"(f[27]), "f"(f[28]),
+        "f"(f[29]), "f"(f[30]), "f"(f[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- warp MMA
 // Round-to-nearest TF32 value of x (kept in a 32-bit register).
 __device__ __forceinline__ uint32_t to_tf32(float x) {
@@ -198,41 +215,6 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// acc(16x16) += A(16x16) * B(16x16), both row-major FP32 in shared memory
-// with leading dimensions lda / ldb, as three TF32 products per step
-// (a_lo b_hi + a_hi b_lo + a_hi b_hi with x = hi + lo), which keeps close to
-// FP32 accuracy.  acc[nt] holds the 16x8 output column block nt in the
-// mma accumulator layout: rows (lane/4, lane/4 + 8), columns 2(lane%4) + {0,1}.
-__device__ __forceinline__ void warp_gemm16_3xtf32(float (&acc)[2][4], const float *A, int lda,
-                                                   const float *B, int ldb, int lane) {
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        const float av[4] = {A[g * lda + 8 * ks + t], A[(g + 8) * lda + 8 * ks + t],
-                             A[g * lda + 8 * ks + t + 4], A[(g + 8) * lda + 8 * ks + t + 4]};
-        uint32_t ahi[4], alo[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ahi[i] = to_tf32(av[i]);
-            alo[i] = to_tf32(av[i] - __uint_as_float(ahi[i]));
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const float bv[2] = {B[(8 * ks + t) * ldb + 8 * nt + g],
-                                 B[(8 * ks + t + 4) * ldb + 8 * nt + g]};
-            uint32_t bhi[2], blo[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                bhi[i] = to_tf32(bv[i]);
-                blo[i] = to_tf32(bv[i] - __uint_as_float(bhi[i]));
-            }
-            mma_tf32_16x8x8(acc[nt], alo, bhi);
-            mma_tf32_16x8x8(acc[nt], ahi, blo);
-            mma_tf32_16x8x8(acc[nt], ahi, bhi);
-        }
-    }
 }
 
 // Loads 16 FP32 columns of this thread's TMEM row.
