@@ -125,6 +125,7 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     L.off_segC = take(sizeof(float) * segs * K * V);
     L.off_segH = take(sizeof(float) * segs * K * V);
     L.off_segD = take(delta ? 0 : sizeof(float) * segs);
+    L.off_rec = take(simt ? 0 : (size_t)mc * H * 41984u);
     L.total = off;
     return L;
 }
@@ -145,6 +146,7 @@ Workspace carve_workspace(void *base, const WorkspaceLayout &L, int S) {
     w.segC = reinterpret_cast<float *>(b + L.off_segC);
     w.segH = reinterpret_cast<float *>(b + L.off_segH);
     w.segD = reinterpret_cast<float *>(b + L.off_segD);
+    w.rec = reinterpret_cast<uint8_t *>(b + L.off_rec);
     w.max_chunks = L.max_chunks;
     w.n_segments = S;
     return w;
@@ -186,6 +188,7 @@ int run_simt(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaSt
 int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStream_t st,
            LaunchRecorder &rec) {
     GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
+    GDR_LAUNCH(rec, kKTcPrep, tc_prep(p, ws, st));
     if (plan.n_segments <= 1) {
         GDR_LAUNCH(rec, kKTcSerial, tc_chain(p, ws, 0, st));
     } else {
@@ -217,6 +220,7 @@ const char *gdr_kernel_name(int id) {
     case kKTcSerial: return "tc_chain_serial";
     case kKTcPre: return "tc_chain_prescan";
     case kKTcSegOut: return "tc_chain_segment_out";
+    case kKTcPrep: return "tc_prep";
     default: return "?";
     }
 }
@@ -272,7 +276,10 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
     p.scale = (opt && opt->scale > 0.f) ? opt->scale : 1.0f / std::sqrt((float)dims->K);
     p.status = opt ? opt->status : nullptr;
     if (p.N == 0) return GDR_OK;
-    if (plan.path == 2 && !tc_supported(p)) {
+    // The tensor-core path addresses its per-chunk records with 32-bit TMA
+    // row coordinates (328 rows per chunk and head).
+    const bool rec_fits = max_chunks_of(*dims) * dims->H * 328 < (int64_t)INT32_MAX;
+    if (plan.path == 2 && (!tc_supported(p) || !rec_fits)) {
         if (opt && opt->force_path == 2) return GDR_ERR_INVALID;  // misaligned pointers
         plan.path = 1;
         plan.bv = pick_bv(*dims);

@@ -46,6 +46,8 @@ struct Workspace {
     float *segC;          // [N][H][S][K][V] local state per segment
     float *segH;          // [N][H][S][K][V] composed initial state per segment
     float *segD;          // [N][H][S] scalar transition (beta-free)
+    uint8_t *rec;         // [max_chunks][H] per-chunk records of the
+                          // tensor-core path (tc_chunk.cuh)
     int64_t max_chunks;
     int n_segments;       // S (1 = serial)
 };
@@ -53,7 +55,7 @@ struct Workspace {
 // Byte layout of the workspace for one problem.
 struct WorkspaceLayout {
     size_t off_tab, off_seq0, off_nchunks, off_order, off_G, off_W, off_U, off_hpre,
-        off_vnew, off_segM, off_segC, off_segH, off_segD, total;
+        off_vnew, off_segM, off_segC, off_segH, off_segD, off_rec, total;
     int64_t max_chunks;
 };
 
@@ -74,6 +76,7 @@ enum KernelId {
     kKTcSerial = 7,
     kKTcPre = 8,
     kKTcSegOut = 9,
+    kKTcPrep = 10,
     kKNumIds
 };
 
@@ -115,8 +118,10 @@ bool compose_mt_supported(const Problem &p);
 cudaError_t compose_mt(const Problem &p, const Workspace &ws, cudaStream_t st);
 
 // ---- tensor-core path (BF16, K = V = 128, delta rule) ---------------------
-// Shapes and pointer alignment the fused chain kernel takes.
+// Shapes and pointer alignment the tensor-core kernels take.
 bool tc_supported(const Problem &p);
+// A2-A5 for every (chunk, head) in parallel -> per-chunk records.
+cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st);
 // mode 0: serial scan + output (h0 -> ht); 1: segment pre-scan (c_s and M_s
 // chains); 2: segment output pass from the composed segment states.
 cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream_t st);

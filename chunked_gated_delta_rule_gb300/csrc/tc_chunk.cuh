@@ -1,0 +1,107 @@
+// tc_chunk.cuh -- pieces shared by the tensor-core prep and scan kernels:
+// the per-chunk record the prep kernel leaves for the scan kernel, BF16
+// packing, and the per-chunk gate vectors.
+#pragma once
+
+#include "tc_common.cuh"
+
+namespace gdr {
+namespace tc {
+
+constexpr int kD = 128;  // K = V = 128 on the tensor-core path
+
+// One record per (chunk, head), BF16 rows of 64 elements (128 bytes):
+//   rows   0..127  W, MN-major: row `key` holds W[t][key] for t = 0..63
+//   rows 128..255  U^T: row `v` holds U[t][v] for t = 0..63
+//   rows 256..319  P: row i holds (Q K^T * e^{G_i - G_j}, j <= i)[i][j]
+//   rows 320..327  FP32 vectors: e^{G_last - G_t} (64), e^{G_t} (64),
+//                  e^{G_last} (1), padding
+// Padded tokens (past a sequence end) have zero W rows' entries, zero U and
+// P entries: every later product with them adds exact zeros.
+constexpr int kRecRows = 328;
+constexpr uint32_t kRecBytes = kRecRows * 128;  // 41984, also sized in gdr_api.cu
+constexpr int kRecW = 0, kRecU = 128, kRecP = 256, kRecVec = 320;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint8_t *p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
+}
+
+// Eight FP32 values -> one 16-byte chunk of BF16 at `p` (shared or global).
+__device__ __forceinline__ void st_bf16x8(void *p, const float *x) {
+    *reinterpret_cast<uint4 *>(p) =
+        make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                   pack_bf16x2(x[6], x[7]));
+}
+
+// Eight BF16 of a 16-byte chunk -> FP32.
+__device__ __forceinline__ void ld_bf16x8(const void *p, float *x) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+        const float2 f = __bfloat1622float2(b);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+// Per-chunk gate vectors (A2) from one warp: lane l holds the log gates and
+// betas of tokens 2l and 2l + 1 (zero past `len`).  Fixed-order scan: pair
+// sums scanned across lanes.  Layout of v (kGateFloats floats):
+//   [0,64) G   [64,128) beta   [128,192) beta e^G   [192,256) e^{G_last - G}
+//   [256,320) e^G   [320,384) e^{G - G_last}
+//   [384] G_last  [385] e^{G_last}  [386] 1 if every |G_t - G_last| < 80
+//   (then e^{G_i - G_j} = e^{G_i - G_last} e^{G_last - G_j} neither
+//   overflows nor underflows), else 0.
+constexpr int kGateFloats = 392;
+
+__device__ __forceinline__ void gate_vectors(float *v, const float (&g2)[2], const float (&b2)[2],
+                                             int len, int lane_id) {
+    float *sG = v, *sBeta = v + 64, *sBG = v + 128, *sDec = v + 192, *sGam = v + 256,
+          *sEP = v + 320, *sScal = v + 384;
+    float x = g2[0] + g2[1];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane_id >= off) x += y;
+    }
+    float excl = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane_id == 0) excl = 0.f;
+    const float G0 = excl + g2[0], G1 = G0 + g2[1];
+    sG[2 * lane_id] = G0;
+    sG[2 * lane_id + 1] = G1;
+    sBeta[2 * lane_id] = b2[0];
+    sBeta[2 * lane_id + 1] = b2[1];
+    __syncwarp();
+    const float glast = sG[len - 1];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int tok = 2 * lane_id + u;
+        const float Gt = u ? G1 : G0;
+        const float gm = __expf(Gt);
+        sGam[tok] = gm;
+        sBG[tok] = b2[u] * gm;
+        sDec[tok] = __expf(glast - Gt);
+        sEP[tok] = __expf(Gt - glast);
+    }
+    float spread = fmaxf(fabsf(G0 - glast), fabsf(G1 - glast));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        spread = fmaxf(spread, __shfl_xor_sync(0xffffffffu, spread, off));
+    if (lane_id == 0) {
+        sScal[0] = glast;
+        sScal[1] = __expf(glast);
+        sScal[2] = spread < 80.f ? 1.f : 0.f;
+    }
+    __syncwarp();
+}
+
+}  // namespace tc
+}  // namespace gdr

@@ -87,6 +87,16 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// 2-D tiled load into shared memory, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map,
+                                            uint64_t *bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 // 1-D bulk copy global -> shared (16-B aligned addresses, size a multiple of
 // 16), completion counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,

@@ -1,0 +1,252 @@
+// tc_prep.cu -- A2-A5 on the tensor-core path (BF16, K = V = 128, delta rule):
+// everything of the chunked form that does not depend on the state, for
+// every (chunk, head) in parallel (one CTA each, two CTAs per SM):
+//
+//   G (gate cumsum), D1 = [K; Q] K^T on tcgen05 (rows 0-63 K K^T, rows 64-127
+//   Q K^T), A_ij = beta_i e^{G_i - G_j} (k_i . k_j) for i > j, T = (I + A)^-1
+//   (tc_inverse.cuh), W^T = K^T (T diag(beta e^G))^T and U^T = V^T
+//   (T diag(beta))^T on tcgen05, P = (Q K^T) * e^{G_i - G_j} for j <= i.
+//
+// The results go to one record per (chunk, head) (layout in tc_chunk.cuh),
+// which the scan kernel (tc_chain.cu) streams back by TMA, so the serial
+// chain only does the state-dependent products.  Chunked form: the project
+// statement; the WY/UT preparation ahead of fla's state-scan kernel
+// chunk_gated_delta_rule_fwd_kernel_h_blockdim64 (Kev PR #259 intro).
+#include "gdr_internal.cuh"
+#include "tc_chunk.cuh"
+#include "tc_inverse.cuh"
+#include "tma_host.cuh"
+
+namespace gdr {
+namespace {
+
+using namespace tc;
+
+struct PrepArgs {
+    Problem p;
+    Workspace ws;
+    CUtensorMap tq, tk, tv;
+};
+
+constexpr int kThreads = 256;
+
+// Shared memory (bytes from a 1024-aligned base).
+// [0, 48 KB): the K, Q, V tiles [Kb0|Qb0|Kb1|Qb1|Vb0|Vb1]
+constexpr uint32_t kOffAT = 49152;                      // sA, sT (FP32, ld kInvLd)
+constexpr uint32_t kOffT = kOffAT + 64 * kInvLd * 4;
+constexpr uint32_t kOffBW = kOffAT;                     // B_W, B_U over sA afterwards
+constexpr uint32_t kOffBU = kOffAT + 8192;
+constexpr uint32_t kOffX = kOffAT + 34816;              // inverse scratch
+constexpr uint32_t kOffVec = kOffX + 3072;              // gate vectors
+constexpr uint32_t kOffBar = kOffVec + 1600;
+constexpr uint32_t kSmemLaunch = kOffBar + 64 + 1024;
+
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColD1 = 0, kColW = 64, kColU = 128;
+
+constexpr uint32_t kIdescKK64 = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t kIdescMK64 = idesc_bf16(128, 64, 1, 0);
+
+__global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__ PrepArgs args) {
+    const Problem &p = args.p;
+    const Workspace &ws = args.ws;
+    const int64_t chunk = blockIdx.x;
+    const int h = blockIdx.y;
+    if (chunk >= *ws.n_chunks) return;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    float *vec = reinterpret_cast<float *>(sm + kOffVec);
+    const float *sG = vec, *sBeta = vec + 64, *sBG = vec + 128, *sDec = vec + 192,
+                *sGam = vec + 256, *sEP = vec + 320, *sScal = vec + 384;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);  // tma, mma
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffBar + 16);
+    float *sA = reinterpret_cast<float *>(sm + kOffAT);
+    float *sT = reinterpret_cast<float *>(sm + kOffT);
+    float *sX = reinterpret_cast<float *>(sm + kOffX);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = 32 * quad + lane_id;  // TMEM lane = matrix row
+    const int H = (int)p.H;
+    const int4 e = reinterpret_cast<const int4 *>(ws.chunk_tab)[chunk];
+    const int64_t t0 = e.y;
+    const int len = e.z;
+    uint8_t *rec = ws.rec + (chunk * H + h) * (int64_t)kRecBytes;
+
+    if (warp == 0) {
+        tmem_alloc(s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init_fence();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const uint32_t lane = (uint32_t)(32 * quad) << 16;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bars[0], 49152u);
+        tma_load_3d(sm + 0, &args.tk, &bars[0], 0, h, (int)t0);
+        tma_load_3d(sm + 16384, &args.tk, &bars[0], 64, h, (int)t0);
+        tma_load_3d(sm + 8192, &args.tq, &bars[0], 0, h, (int)t0);
+        tma_load_3d(sm + 24576, &args.tq, &bars[0], 64, h, (int)t0);
+        tma_load_3d(sm + 32768, &args.tv, &bars[0], 0, h, (int)t0);
+        tma_load_3d(sm + 40960, &args.tv, &bars[0], 64, h, (int)t0);
+    }
+    if (warp == 0) {  // A2: gates of this chunk (padded tokens: g = beta = 0)
+        float g2[2], b2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int tok = 2 * lane_id + u;
+            g2[u] = tok < len ? p.g[(t0 + tok) * H + h] : 0.f;
+            b2[u] = tok < len ? p.beta[(t0 + tok) * H + h] : 0.f;
+        }
+        gate_vectors(vec, g2, b2, len, lane_id);
+    }
+    bool ok = mbar_wait(&bars[0], 0, p.status);
+    if (__syncthreads_or(!ok)) goto done;
+    if (len < 64) {  // rows past the sequence end belong to the next one: zero them
+        const int rows = 64 - len;
+        for (int idx = tid; idx < rows * 6 * 8; idx += kThreads) {
+            const int r = len + idx / 48, blk = (idx / 8) % 6, c16 = idx & 7;
+            st_shared_v4(sm + blk * 8192 + r * 128 + c16 * 16, 0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();
+    }
+    __syncthreads();
+
+    // A3 (+ Q K^T): D1 = [K; Q] K^T
+    if (tid == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a = sb + (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_bf16(tmem + kColD1, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024),
+                      kIdescKK64, kk > 0);
+        }
+        umma_commit(&bars[1]);
+    }
+    ok = mbar_wait(&bars[1], 0, p.status);
+    if (__syncthreads_or(!ok)) goto done;
+    tc_fence_after();
+    {
+        float f[32];
+        tmem_load32f(tmem + lane + kColD1 + 32 * half, f);
+        const int i = row & 63;
+        const int j0 = 32 * half;
+        // A rows keep j < i (beta_i folded in); P rows keep j <= i.
+        const int jlim = quad < 2 ? i : i + 1;
+        const float rowf = quad < 2 ? sBeta[i] : 1.f;
+        if (sScal[2] != 0.f) {  // e^{G_i - G_j} = e^{G_i - G_last} e^{G_last - G_j}
+            const float ri = rowf * sEP[i];
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                f[u] = (j0 + u < jlim) ? f[u] * (ri * sDec[j0 + u]) : 0.f;
+        } else {
+            const float gi = sG[i];
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                f[u] = (j0 + u < jlim) ? f[u] * (rowf * __expf(gi - sG[j0 + u])) : 0.f;
+        }
+        if (quad < 2) {  // row i of A (strictly lower), FP32
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+                *reinterpret_cast<float4 *>(sA + i * kInvLd + j0 + 4 * c4) =
+                    make_float4(f[4 * c4], f[4 * c4 + 1], f[4 * c4 + 2], f[4 * c4 + 3]);
+        } else {  // row i of P (lower, diagonal included), BF16, to the record
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8)
+                st_bf16x8(rec + (kRecP + i) * 128 + 2 * (j0 + 8 * c8), f + 8 * c8);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // A4: T = (I + A)^-1
+    invert_unit_lower64(sA, sT, sX, tid);
+
+    // A5 operands: rows of T diag(beta e^G) (rows 0-63) and T diag(beta)
+    // (rows 64-127), BF16, columns [32 half, 32 half + 32).
+    {
+        const int i = row & 63;
+        const float *scale_vec = quad < 2 ? sBG : sBeta;
+        uint8_t *dst = sm + (quad < 2 ? kOffBW : kOffBU);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+            const int j0 = 32 * half + 8 * c8;
+            const float4 a0 = *reinterpret_cast<const float4 *>(sT + i * kInvLd + j0);
+            const float4 a1 = *reinterpret_cast<const float4 *>(sT + i * kInvLd + j0 + 4);
+            const float tv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] = j0 + u <= i ? tv[u] * scale_vec[j0 + u] : 0.f;
+            st_bf16x8(dst + sw128_off(i, j0, 64), x);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + kColW, sdesc_sw128(sb + kk * 2048, 16384, 1024),
+                      sdesc_sw128(sb + kOffBW + kk * 32, 16, 1024), kIdescMK64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + kColU, sdesc_sw128(sb + 32768 + kk * 2048, 8192, 1024),
+                      sdesc_sw128(sb + kOffBU + kk * 32, 16, 1024), kIdescMK64, kk > 0);
+        umma_commit(&bars[1]);
+    }
+    ok = mbar_wait(&bars[1], 1, p.status);
+    if (__syncthreads_or(!ok)) goto done;
+    tc_fence_after();
+    {  // W (row = key) and U^T (row = v), t in [32 half, 32 half + 32), to the record
+        float f[32];
+        tmem_load32f(tmem + lane + kColW + 32 * half, f);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8)
+            st_bf16x8(rec + (kRecW + row) * 128 + 64 * half + 16 * c8, f + 8 * c8);
+        tmem_load32f(tmem + lane + kColU + 32 * half, f);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8)
+            st_bf16x8(rec + (kRecU + row) * 128 + 64 * half + 16 * c8, f + 8 * c8);
+    }
+    if (tid < 64) {
+        float *rv = reinterpret_cast<float *>(rec + kRecVec * 128);
+        rv[tid] = sDec[tid];
+        rv[64 + tid] = sGam[tid];
+        if (tid == 0) rv[128] = sScal[1];
+    }
+done:
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st) {
+    if (ws.max_chunks == 0) return cudaSuccess;
+    PrepArgs args;
+    args.p = p;
+    args.ws = ws;
+    const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
+    const uint64_t H = (uint64_t)p.H;
+    if (!make_tmap_bf16_3d(&args.tq, p.q, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.tv, p.v, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(k_tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemLaunch);
+    if (err != cudaSuccess) return err;
+    dim3 grid((unsigned)ws.max_chunks, (unsigned)p.H);
+    k_tc_prep<<<grid, kThreads, kSmemLaunch, st>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

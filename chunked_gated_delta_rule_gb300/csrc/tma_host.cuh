@@ -44,4 +44,21 @@ inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, u
     return r == CUDA_SUCCESS;
 }
 
+// 2-D BF16 tensor [d1][d0] (d0 contiguous), byte stride s1; box {b0, b1};
+// 128-byte swizzle; out-of-range elements read as zero.
+inline bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
+                              uint64_t s1, uint32_t b0, uint32_t b1) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {d0, d1};
+    const cuuint64_t strides[1] = {s1};
+    const cuuint32_t box[2] = {b0, b1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace gdr
