@@ -39,7 +39,8 @@ class gdr_options(ctypes.Structure):
 
 
 # Diagnostic entry points declared in include/gdr_selftest.h.
-SELFTEST_EXPORTS = ("gdr_selftest_umma", "gdr_selftest_tma", "gdr_selftest_inverse")
+SELFTEST_EXPORTS = ("gdr_selftest_umma", "gdr_selftest_tma", "gdr_selftest_inverse",
+                    "gdr_selftest_timeout")
 
 # Every symbol include/gdr.h declares.
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_host", "gdr_chunk_fwd_noalloc",
@@ -93,6 +94,8 @@ def load_library():
         lib.gdr_selftest_tma.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
         lib.gdr_selftest_tma.restype = ctypes.c_int
+        lib.gdr_selftest_timeout.argtypes = [vp, ctypes.c_uint64, vp, vp]
+        lib.gdr_selftest_timeout.restype = ctypes.c_int
         lib.gdr_selftest_inverse.argtypes = [vp, vp, vp]
         lib.gdr_selftest_inverse.restype = ctypes.c_int
         lib.gdr_version.argtypes = []
@@ -343,6 +346,18 @@ def gdr_selftest_inverse(A):
     if rc != 0:
         raise GdrError(rc)
     return T
+
+
+def gdr_selftest_timeout(limit_ns=1_000_000):
+    """Runs the bounded-wait failure path once; returns (status, done)."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    done = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = load_library().gdr_selftest_timeout(_ptr(status), int(limit_ns), _ptr(done),
+                                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if rc != 0:
+        raise GdrError(rc)
+    torch.cuda.synchronize()
+    return int(status.item()), int(done.item())
 
 
 def gdr_kernel_name(kid: int) -> str:

@@ -131,10 +131,32 @@ __global__ void __launch_bounds__(256) k_selftest_inverse(const float *__restric
     }
 }
 
+// Waits on an mbarrier that nothing completes, with a time limit: the wait
+// must give up, record GDR_ERR_TIMEOUT in the status word and let the kernel
+// finish normally (the failure path of every bounded wait in the library).
+__global__ void k_selftest_timeout(int32_t *status, uint64_t limit_ns, int32_t *done) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait(&bar, 0, status, limit_ns);
+    if (threadIdx.x == 0) *done = ok ? 1 : 2;
+}
+
 }  // namespace
 }  // namespace gdr
 
 using namespace gdr;
+
+extern "C" int gdr_selftest_timeout(int32_t *status, uint64_t limit_ns, int32_t *done,
+                                    gdr_stream_t stream) {
+    if (!status || !done || limit_ns == 0 || limit_ns > 100000000ull) return GDR_ERR_INVALID;
+    k_selftest_timeout<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, limit_ns,
+                                                                            done);
+    return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
 
 extern "C" int gdr_selftest_inverse(const float *A, float *T, gdr_stream_t stream) {
     if (!A || !T) return GDR_ERR_INVALID;

@@ -40,6 +40,15 @@ int gdr_selftest_tma(const void *src, int64_t T, int64_t H, int64_t K, int t0,
  * above the diagonal of T are written as 0. */
 int gdr_selftest_inverse(const float *A, float *T, gdr_stream_t stream);
 
+/* Waits on an mbarrier that nothing will complete, with the library's
+ * bounded wait limited to `limit_ns` (at most 0.1 s): the wait gives up,
+ * writes GDR_ERR_TIMEOUT to *status (device int32, caller zeroes it) and the
+ * kernel exits normally, writing 2 to *done (1 would mean the wait was
+ * satisfied).  This exercises the failure path of every time-bounded wait
+ * without faulting or hanging the GPU. */
+int gdr_selftest_timeout(int32_t *status, uint64_t limit_ns, int32_t *done,
+                         gdr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -60,3 +60,14 @@ def test_blocked_triangular_inverse(seed):
     ref = torch.linalg.inv(torch.eye(64, dtype=torch.float64) + A.float().double())
     err = ((T.double().cpu() - ref).norm() / ref.norm()).item()
     assert err < 2e-6, err
+
+
+def test_bounded_wait_times_out_cleanly():
+    """A wait on a barrier nothing completes gives up after its limit,
+    reports GDR_ERR_TIMEOUT and leaves the context usable."""
+    pkg.load_library()
+    status, done = api.gdr_selftest_timeout(1_000_000)
+    assert status == -4 and done == 2
+    # the context still works afterwards
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum().item()) == 8.0
