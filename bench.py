@@ -191,14 +191,23 @@ def algorithmic_bytes(kernel, x, c):
     delta = x["beta"] is not None
     th, ch, sh = c["token_heads"], c["chunk_heads"], c["seq_heads"]
     states = sh * K * V * 4 * ((1 if x["h0"] is not None else 0) + 1)
-    if kernel in ("call", "tc_chain_serial"):
-        # whole forward pass (the fused serial chain kernel does all of it):
-        # q, k, v, g, beta read once, o written once, h0 / ht once
+    if kernel in ("call", "tc_gla_serial"):
+        # whole forward pass: q, k, v, g, beta read once, o written once,
+        # h0 / ht once
         return th * ((2 * K + V) * es + 4 + (4 if delta else 0) + V * es) + states
-    if kernel == "tc_chain_prescan":  # k, v, g, beta read; c_s and M_s written
-        return th * ((K + V) * es + 8) + c["segments"] * K * (K + V) * 4
-    if kernel == "tc_chain_segment_out":  # q, k, v, g, beta read, o written, h_s read
-        return th * ((2 * K + V) * es + 8 + V * es) + c["segments"] * K * V * 4
+    if kernel == "tc_chain_serial":  # q, k and the records read, o written, states
+        return th * (2 * K * es + V * es) + ch * 41984 + states
+    if kernel == "tc_gla_prescan":  # k, v, g read; c_s written
+        return th * ((K + V) * es + 4) + c["segments"] * K * V * 4
+    if kernel == "tc_gla_segment_out":  # q, k, v, g read, o written, h_s read
+        return th * ((2 * K + V) * es + 4 + V * es) + c["segments"] * K * V * 4
+    rec = ch * 41984  # per-chunk records of the tensor-core prep kernel
+    if kernel == "tc_prep":  # q, k, v, g, beta read; records written
+        return th * ((2 * K + V) * es + 8) + rec
+    if kernel == "tc_chain_prescan":  # k and the records read; c_s and M_s written
+        return th * K * es + rec + c["segments"] * K * (K + V) * 4
+    if kernel == "tc_chain_segment_out":  # q, k, records read, o written, h_s read
+        return th * (2 * K * es + V * es) + rec + c["segments"] * K * V * 4
     if kernel == "simt_prep":
         b = th * 4 + ch * 64 * 4
         if delta:

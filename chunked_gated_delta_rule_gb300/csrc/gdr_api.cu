@@ -65,9 +65,13 @@ int auto_segments(const gdr_dims &d, int bv) {
     return S;
 }
 
-// Shapes the tensor-core path covers (pointer alignment is checked per call).
+// Shapes the tensor-core path covers (pointer alignment is checked per call):
+// the delta rule at K = V = 128; the beta-free mode at K in {128, 256} with
+// V a multiple of 128.
 bool tc_shape(const gdr_dims &d, bool beta_free) {
-    return d.dtype == GDR_BF16 && d.K == 128 && d.V == 128 && !beta_free;
+    if (d.dtype != GDR_BF16) return false;
+    if (!beta_free) return d.K == 128 && d.V == 128;
+    return (d.K == 128 || d.K == 256) && d.V % 128 == 0;
 }
 
 int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_options *opt,
@@ -125,7 +129,7 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     L.off_segC = take(sizeof(float) * segs * K * V);
     L.off_segH = take(sizeof(float) * segs * K * V);
     L.off_segD = take(delta ? 0 : sizeof(float) * segs);
-    L.off_rec = take(simt ? 0 : (size_t)mc * H * 41984u);
+    L.off_rec = take(simt || !delta ? 0 : (size_t)mc * H * 41984u);
     L.total = off;
     return L;
 }
@@ -188,6 +192,16 @@ int run_simt(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaSt
 int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStream_t st,
            LaunchRecorder &rec) {
     GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
+    if (p.beta == nullptr) {
+        if (plan.n_segments <= 1) {
+            GDR_LAUNCH(rec, kKTcGlaSerial, tc_gla(p, ws, 0, st));
+        } else {
+            GDR_LAUNCH(rec, kKTcGlaPre, tc_gla(p, ws, 1, st));
+            GDR_LAUNCH(rec, kKCompose, simt_compose(p, ws, 64, st));
+            GDR_LAUNCH(rec, kKTcGlaSegOut, tc_gla(p, ws, 2, st));
+        }
+        return GDR_OK;
+    }
     GDR_LAUNCH(rec, kKTcPrep, tc_prep(p, ws, st));
     if (plan.n_segments <= 1) {
         GDR_LAUNCH(rec, kKTcSerial, tc_chain(p, ws, 0, st));
@@ -221,6 +235,9 @@ const char *gdr_kernel_name(int id) {
     case kKTcPre: return "tc_chain_prescan";
     case kKTcSegOut: return "tc_chain_segment_out";
     case kKTcPrep: return "tc_prep";
+    case kKTcGlaSerial: return "tc_gla_serial";
+    case kKTcGlaPre: return "tc_gla_prescan";
+    case kKTcGlaSegOut: return "tc_gla_segment_out";
     default: return "?";
     }
 }
@@ -279,7 +296,8 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
     // The tensor-core path addresses its per-chunk records with 32-bit TMA
     // row coordinates (328 rows per chunk and head).
     const bool rec_fits = max_chunks_of(*dims) * dims->H * 328 < (int64_t)INT32_MAX;
-    if (plan.path == 2 && (!tc_supported(p) || !rec_fits)) {
+    const bool tc_ok = beta_free ? tc_gla_supported(p) : (tc_supported(p) && rec_fits);
+    if (plan.path == 2 && !tc_ok) {
         if (opt && opt->force_path == 2) return GDR_ERR_INVALID;  // misaligned pointers
         plan.path = 1;
         plan.bv = pick_bv(*dims);

@@ -77,6 +77,9 @@ enum KernelId {
     kKTcPre = 8,
     kKTcSegOut = 9,
     kKTcPrep = 10,
+    kKTcGlaSerial = 11,
+    kKTcGlaPre = 12,
+    kKTcGlaSegOut = 13,
     kKNumIds
 };
 
@@ -120,6 +123,9 @@ cudaError_t compose_mt(const Problem &p, const Workspace &ws, cudaStream_t st);
 // ---- tensor-core path (BF16, K = V = 128, delta rule) ---------------------
 // Shapes and pointer alignment the tensor-core kernels take.
 bool tc_supported(const Problem &p);
+// Beta-free mode on tensor cores (BF16, K in {128, 256}, V % 128 == 0).
+bool tc_gla_supported(const Problem &p);
+cudaError_t tc_gla(const Problem &p, const Workspace &ws, int mode, cudaStream_t st);
 // A2-A5 for every (chunk, head) in parallel -> per-chunk records.
 cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st);
 // mode 0: serial scan + output (h0 -> ht); 1: segment pre-scan (c_s and M_s

@@ -72,10 +72,19 @@ def test_bf16_dense_h0_segments(S, path):
     check(synthetic.make_inputs(w), n_segments=S, force_path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("S", [1, 4])
-def test_beta_free_k256_v512(S):
+def test_beta_free_k256_v512(S, path):
     w = synthetic.small(W["gla_k256_v512_bf16"], T=300, H=2)
-    check(synthetic.make_inputs(w), n_segments=S)
+    check(synthetic.make_inputs(w), n_segments=S, force_path=path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("S", [1, 3])
+def test_beta_free_k128_v256_varlen(S, path):
+    w = synthetic.small(W["gla_k256_v512_bf16"], K=128, V=256, H=3)
+    check(synthetic.make_inputs(w, lengths=[1, 64, 65, 200, 0, 130]), n_segments=S,
+          force_path=path)
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -185,7 +194,8 @@ def test_default_plan_uses_tensor_core_path_for_bf16_k128():
     import chunked_gated_delta_rule_gb300 as pkg
     assert pkg.gdr_plan_query(1, 10456, 16, 128, 128, N=32)["path"] == 2
     assert pkg.gdr_plan_query(1, 256, 2, 64, 64, dtype=0)["path"] == 1
-    assert pkg.gdr_plan_query(2, 8192, 4, 256, 512, beta_free=True)["path"] == 1
+    assert pkg.gdr_plan_query(2, 8192, 4, 256, 512, beta_free=True)["path"] == 2
+    assert pkg.gdr_plan_query(2, 8192, 4, 64, 512, beta_free=True)["path"] == 1
 
 
 def test_caller_workspace_matches_internal_allocation():
