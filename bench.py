@@ -201,6 +201,10 @@ def algorithmic_bytes(kernel, x, c):
         return th * ((K + V) * es + 4) + c["segments"] * K * V * 4
     if kernel == "tc_gla_segment_out":  # q, k, v, g read, o written, h_s read
         return th * ((2 * K + V) * es + 4 + V * es) + c["segments"] * K * V * 4
+    if kernel == "compose_scalar":  # c_s, d_s read; h_s written; h0 / ht
+        return c["segments"] * (2 * K * V * 4 + 4) + states
+    if kernel in ("compose_mt", "simt_compose"):  # M_s, c_s read; h_s written; h0 / ht
+        return c["segments"] * ((K * K if delta else 1) + 2 * K * V) * 4 + states
     rec = ch * 41984  # per-chunk records of the tensor-core prep kernel
     if kernel == "tc_prep":  # q, k, v, g, beta read; records written
         return th * ((2 * K + V) * es + 8) + rec

@@ -106,7 +106,42 @@ __global__ void __launch_bounds__(256) k_compose_mt(Problem p, Workspace ws) {
     }
 }
 
+// Beta-free composition (scaled-identity transitions, cuLA PR #127 "Scope":
+// the diagonal affine maps of the gated-linear-attention form): every state
+// element evolves on its own, h_{s+1} = d_s h_s + c_s, so one thread owns one
+// element of one (sequence, head) and walks the segments in order; a warp
+// touches 128 contiguous bytes per access.  Bandwidth-bound: c_s read once,
+// h_s written once.
+__global__ void __launch_bounds__(256) k_compose_scalar(Problem p, Workspace ws) {
+    const int64_t kv = p.K * p.V;
+    const int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (idx >= p.N * p.H * kv) return;
+    const int64_t nh = idx / kv, e = idx - nh * kv;
+    const int64_t n = nh / p.H;
+    const int S = ws.n_segments;
+    const int nc = ws.seq_chunk0[n + 1] - ws.seq_chunk0[n];
+    const int per = (nc + S - 1) / S;
+    const int nseg = per ? (nc + per - 1) / per : 0;
+    const float *__restrict__ C = ws.segC + nh * S * kv + e;
+    float *__restrict__ Hs = ws.segH + nh * S * kv + e;
+    const float *__restrict__ D = ws.segD + nh * S;
+    float h = p.h0 ? p.h0[idx] : 0.f;
+    for (int s = 0; s < nseg; ++s) {
+        const float c = C[s * kv];
+        Hs[s * kv] = h;
+        h = fmaf(D[s], h, c);
+    }
+    if (p.ht) p.ht[idx] = h;
+}
+
 }  // namespace
+
+cudaError_t compose_scalar(const Problem &p, const Workspace &ws, cudaStream_t st) {
+    const int64_t total = p.N * p.H * p.K * p.V;
+    if (total == 0) return cudaSuccess;
+    k_compose_scalar<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(p, ws);
+    return cudaGetLastError();
+}
 
 bool compose_mt_supported(const Problem &p) {
     return p.beta != nullptr && p.K <= 128 && p.K % 16 == 0 && p.V % kCC == 0;

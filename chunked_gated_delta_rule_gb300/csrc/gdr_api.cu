@@ -179,7 +179,9 @@ int run_simt(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaSt
         GDR_LAUNCH(rec, kKScanSerial, simt_scan(p, ws, 0, plan.bv, st));
     } else {
         GDR_LAUNCH(rec, kKScanPre, simt_scan(p, ws, 1, plan.bv, st));
-        if (compose_mt_supported(p))
+        if (p.beta == nullptr)
+            GDR_LAUNCH(rec, kKComposeScalar, compose_scalar(p, ws, st));
+        else if (compose_mt_supported(p))
             GDR_LAUNCH(rec, kKCompose, compose_mt(p, ws, st));
         else
             GDR_LAUNCH(rec, kKCompose, simt_compose(p, ws, plan.bv, st));
@@ -197,7 +199,7 @@ int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStre
             GDR_LAUNCH(rec, kKTcGlaSerial, tc_gla(p, ws, 0, st));
         } else {
             GDR_LAUNCH(rec, kKTcGlaPre, tc_gla(p, ws, 1, st));
-            GDR_LAUNCH(rec, kKCompose, simt_compose(p, ws, 64, st));
+            GDR_LAUNCH(rec, kKComposeScalar, compose_scalar(p, ws, st));
             GDR_LAUNCH(rec, kKTcGlaSegOut, tc_gla(p, ws, 2, st));
         }
         return GDR_OK;
@@ -238,6 +240,7 @@ const char *gdr_kernel_name(int id) {
     case kKTcGlaSerial: return "tc_gla_serial";
     case kKTcGlaPre: return "tc_gla_prescan";
     case kKTcGlaSegOut: return "tc_gla_segment_out";
+    case kKComposeScalar: return "compose_scalar";
     default: return "?";
     }
 }

@@ -80,6 +80,7 @@ enum KernelId {
     kKTcGlaSerial = 11,
     kKTcGlaPre = 12,
     kKTcGlaSegOut = 13,
+    kKComposeScalar = 14,
     kKNumIds
 };
 
@@ -119,6 +120,8 @@ cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st);
 // bulk-copied transposed transitions, 32 value columns per CTA.
 bool compose_mt_supported(const Problem &p);
 cudaError_t compose_mt(const Problem &p, const Workspace &ws, cudaStream_t st);
+// A9 for the beta-free form (scalar transitions d_s).
+cudaError_t compose_scalar(const Problem &p, const Workspace &ws, cudaStream_t st);
 
 // ---- tensor-core path (BF16, K = V = 128, delta rule) ---------------------
 // Shapes and pointer alignment the tensor-core kernels take.
