@@ -185,6 +185,9 @@ def counts(x, n_segments=1):
                 seq_heads=len(lens) * H, n_seqs=len(lens), chunks=chunks, segments=segs * H)
 
 
+REC_BYTES = 73744  # bytes of one record written by tc_prep and read by the scan
+
+
 def algorithmic_bytes(kernel, x, c):
     K, V = x["K"], x["V"]
     es = 2 if x["dtype"] == "bf16" else 4
@@ -195,8 +198,8 @@ def algorithmic_bytes(kernel, x, c):
         # whole forward pass: q, k, v, g, beta read once, o written once,
         # h0 / ht once
         return th * ((2 * K + V) * es + 4 + (4 if delta else 0) + V * es) + states
-    if kernel == "tc_chain_serial":  # q, k and the records read, o written, states
-        return th * (2 * K * es + V * es) + ch * 41984 + states
+    if kernel == "tc_chain_serial":  # the records read, o written, states
+        return th * V * es + ch * REC_BYTES + states
     if kernel == "tc_gla_prescan":  # k, v, g read; c_s written
         return th * ((K + V) * es + 4) + c["segments"] * K * V * 4
     if kernel == "tc_gla_segment_out":  # q, k, v, g read, o written, h_s read
@@ -205,13 +208,13 @@ def algorithmic_bytes(kernel, x, c):
         return c["segments"] * (2 * K * V * 4 + 4) + states
     if kernel in ("compose_mt", "simt_compose"):  # M_s, c_s read; h_s written; h0 / ht
         return c["segments"] * ((K * K if delta else 1) + 2 * K * V) * 4 + states
-    rec = ch * 41984  # per-chunk records of the tensor-core prep kernel
+    rec = ch * REC_BYTES  # per-chunk records of the tensor-core prep kernel
     if kernel == "tc_prep":  # q, k, v, g, beta read; records written
         return th * ((2 * K + V) * es + 8) + rec
-    if kernel == "tc_chain_prescan":  # k and the records read; c_s and M_s written
-        return th * K * es + rec + c["segments"] * K * (K + V) * 4
-    if kernel == "tc_chain_segment_out":  # q, k, records read, o written, h_s read
-        return th * (2 * K * es + V * es) + rec + c["segments"] * K * V * 4
+    if kernel == "tc_chain_prescan":  # W, K~, U^T of the records (once); c_s and M_s written
+        return ch * 3 * 16384 + c["segments"] * K * (K + V) * 4
+    if kernel == "tc_chain_segment_out":  # records read, o written, h_s read
+        return th * V * es + rec + c["segments"] * K * V * 4
     if kernel == "simt_prep":
         b = th * 4 + ch * 64 * 4
         if delta:

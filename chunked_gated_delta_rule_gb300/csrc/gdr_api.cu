@@ -129,7 +129,7 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     L.off_segC = take(sizeof(float) * segs * K * V);
     L.off_segH = take(sizeof(float) * segs * K * V);
     L.off_segD = take(delta ? 0 : sizeof(float) * segs);
-    L.off_rec = take(simt || !delta ? 0 : (size_t)mc * H * 41984u);
+    L.off_rec = take(simt || !delta ? 0 : (size_t)mc * H * 74752u);
     L.total = off;
     return L;
 }
@@ -296,10 +296,7 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
     p.scale = (opt && opt->scale > 0.f) ? opt->scale : 1.0f / std::sqrt((float)dims->K);
     p.status = opt ? opt->status : nullptr;
     if (p.N == 0) return GDR_OK;
-    // The tensor-core path addresses its per-chunk records with 32-bit TMA
-    // row coordinates (328 rows per chunk and head).
-    const bool rec_fits = max_chunks_of(*dims) * dims->H * 328 < (int64_t)INT32_MAX;
-    const bool tc_ok = beta_free ? tc_gla_supported(p) : (tc_supported(p) && rec_fits);
+    const bool tc_ok = beta_free ? tc_gla_supported(p) : tc_supported(p);
     if (plan.path == 2 && !tc_ok) {
         if (opt && opt->force_path == 2) return GDR_ERR_INVALID;  // misaligned pointers
         plan.path = 1;

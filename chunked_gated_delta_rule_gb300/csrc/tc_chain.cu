@@ -1,24 +1,38 @@
 // tc_chain.cu -- A6/A7 (and A8/A10 of the segment split) on the tensor-core
 // path (BF16, K = V = 128, delta rule): the serial state scan and the output.
 //
-// Persistent CTAs (one per SM, 256 threads) pull chains -- all chunks of one
-// (sequence, head), or of one (sequence, segment, head) -- longest first from
-// an atomic counter.  Everything that does not depend on the state was done
-// by tc_prep.cu for all chunks in parallel and left in one record per
-// (chunk, head); here, per chunk, in order:
+// Persistent CTAs (one per SM) pull chains -- all chunks of one (sequence,
+// head), or of one (sequence, segment, head) -- longest first from an atomic
+// counter.  Everything that does not depend on the state was done by
+// tc_prep.cu for all chunks in parallel and left in one record per (chunk,
+// head); here, per chunk, in order:
 //
-//   v_new^T = U^T - h^T W^T           (tcgen05, A = BF16 mirror of h^T)
-//   h^T <- e^{G_last} h^T + (v_new e^{G_last - G})^T K   (tcgen05; the
-//                                      canonical state is FP32 in TMEM)
-//   O^T = scale [(h^T Q^T) * e^G + v_new^T P^T]   (tcgen05, staged, stored)
+//   [v_new^T | O] = h^T [W; Q~]^T      (tcgen05, N = 128; A is the BF16
+//                                       mirror of h^T)
+//   v_new^T = U^T - (h^T W^T)
+//   h^T <- e^{G_last} h^T + v_new^T K~  (tcgen05 accumulating onto the FP32
+//                                       state in TMEM, pre-scaled)
+//   O += v_new^T (scale P)^T            (tcgen05 onto the same columns)
 //
-// The formulation is the transposed one (value columns are TMEM lanes), so
-// every MMA has M = 128.  Warp w reads TMEM lanes 32 (w % 4) .. + 31 (its
-// "row") and handles column half w / 4 of every epilogue.  K, Q and the
-// record's W, U^T, P and decay vectors arrive by TMA / bulk copy with
-// 128-byte swizzle into a two-stage ring (the next chunk, possibly of the
-// next chain, loads while this one runs).  Waits are time-bounded: on expiry
-// the CTA records GDR_ERR_TIMEOUT in the status word and leaves.
+// with K~ = diag(e^{G_last - G}) K and Q~ = scale diag(e^G) Q formed by the
+// prep kernel, so O is the output (one rounding to BF16).  The formulation is
+// the transposed one (value columns are TMEM lanes), so every MMA has M =
+// 128.  The warps specialise:
+//   warps 0-3  the state path, which is the serial dependency: per chunk the
+//              BF16 mirror of h^T (and h^T scaled by e^{G_last} in place),
+//              then v_new^T once the first product lands;
+//   warps 4-7  the output path: each chunk's O, staged and stored (a TMA
+//              store for whole chunks);
+//   warp 8     control: issues every MMA;
+//   warp 9     producer: claims chains, decodes them into a small ring that
+//              the other roles read, and loads each chunk's record (the byte
+//              image of a stage) with one bulk copy into a two-stage ring;
+//              the next chunk, also of the next chain, loads while this one
+//              runs.
+// Roles hand over through mbarriers; the first product's TMEM buffer is
+// double-buffered, so the output of chunk c overlaps chunk c + 1.  Every
+// wait is time-bounded: on expiry the CTA records GDR_ERR_TIMEOUT in the
+// status word, the other roles leave too, and the CTA exits.
 //
 // Chunked form: the project statement; the state scan of fla's
 // chunk_gated_delta_rule_fwd_kernel_h_blockdim64 (Kev PR #259 intro); the
@@ -39,39 +53,73 @@ enum TcMode { kModeSerial = 0, kModePre = 1, kModeSegOut = 2 };
 struct TcArgs {
     Problem p;
     Workspace ws;
-    CUtensorMap tq, tk, trec128, trec64;
+    CUtensorMap to;  // the output o, for TMA stores of whole chunks
 };
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;  // warps 0-3 state, 4-7 output, 8 control, 9 producer
+constexpr int kRing = 3;       // decoded chains handed out ahead (bounds the look-ahead)
 
-// Shared memory (bytes from a 1024-aligned base).  One stage:
-//   [Kb0|Qb0|Kb1|Qb1] 32 KB, W 16 KB, U^T 16 KB, P 8 KB, vectors 1 KB.
-constexpr uint32_t kStW = 32768, kStU = 49152, kStP = 65536, kStVec = 73728;
-constexpr uint32_t kStage = 75776;
-constexpr uint32_t kOffHm = 2 * kStage;            // h^T mirror, K-major, 32 KB
-constexpr uint32_t kOffVn = kOffHm + 32768;        // v_new^T tile; output staging after
-constexpr uint32_t kOffVd = kOffVn + 16384;        // (v_new e^{G_last - G})^T tile
-constexpr uint32_t kOffBar = kOffVd + 16384;
-constexpr uint32_t kSmemLaunch = kOffBar + 256 + 1024;
+// Shared memory (bytes from a 1024-aligned base).  One stage holds one
+// record image (layout in tc_chunk.cuh):
+//   [Wb0|Q~b0|Wb1|Q~b1] 32 KB: B operand [W; Q~] (K-major, N = 128 rows)
+//   [K~b0|K~b1] 16 KB: B operand of the update (MN-major, N = 128)
+//   scale P^T 8 KB: B operand of O (MN-major, N = 64); U^T 16 KB; vectors.
+constexpr uint32_t kStage = kRecBytes;
+constexpr uint32_t kOffHm = 2 * kStage;        // h^T mirror, K-major, 32 KB
+constexpr uint32_t kOffVn = kOffHm + 32768;    // v_new^T tile, 16 KB
+constexpr uint32_t kOffOs = kOffVn + 16384;    // output staging, 16 KB
+constexpr uint32_t kOffRing = kOffOs + 16384;  // decoded chains
+enum : int {
+    kBFull = 0,     // [2] stage landed (bulk-copy bytes)
+    kBMready = 2,   // mirror written (state path, 128)
+    kBAdone = 3,    // [h^T W^T | O] done (commit)
+    kBVready = 4,   // v_new tile written, state scaled (state path, 128)
+    kBHdone = 5,    // state update done (commit)
+    kBO2 = 6,       // [2] O complete (commit)
+    kBOfree = 8,    // [2] O buffer read (output path, 128)
+    kBDrain = 10,   // every issued MMA done (commit, at the end)
+    kBFree = 11,    // [2] every product reading the stage done (commit)
+    kBCfull = 13,   // [kRing] chain posted (producer)
+    kBCempty = 13 + kRing,  // [kRing] chain read (state, output paths and control: 257)
+    kNumBars = 13 + 2 * kRing
+};
+
+// One chain of the work list, decoded: (sequence n, segment s, head h[,
+// transition]); valid == 0 ends the list.
+struct ChainDesc {
+    int64_t n, tstart, tlen;  // the sequence's first token row and length
+    int h, s, trans, c_begin, s0, s1, valid, pad;
+};
+static_assert(sizeof(ChainDesc) == 56, "chain descriptor layout");
+constexpr uint32_t kOffBar = kOffRing + 64 * kRing;
+constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;  // TMEM base, abort flag
+constexpr uint32_t kSmemLaunch = kOffMisc + 16 + 1024;
 
 // TMEM columns (512 allocated; one CTA per SM).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColVn = 0, kColO2 = 0;  // O2 after v_new is read
-constexpr uint32_t kColO1 = 64;
-constexpr uint32_t kColH = 128;             // 128 columns
-constexpr uint32_t kColS = 256;             // FP32 state h^T, 128 columns
+constexpr uint32_t kColA = 0;    // two buffers of [h^T W^T | O], 128 columns each
+constexpr uint32_t kColS = 256;  // FP32 state h^T, 128 columns
 
-constexpr uint32_t kIdescKK64 = idesc_bf16(128, 64, 0, 0);
-constexpr uint32_t kIdescKM64 = idesc_bf16(128, 64, 0, 1);
-constexpr uint32_t kIdescKM128 = idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t kIdescA128 = idesc_bf16(128, 128, 0, 0);
+constexpr uint32_t kIdescA64 = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t kIdescH = idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t kIdescO2 = idesc_bf16(128, 64, 0, 1);
 
-// One chain of the work list: (sequence n, segment s, head h[, transition]).
-struct Chain {
-    int64_t n;
-    int h, s;
-    bool trans;
-    int c_begin, s0, s1;
-};
+// Named barrier of the output path's 128 threads; side_all also ANDs a flag
+// across them, so that all of them take the same branch after a wait.
+__device__ __forceinline__ void side_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool side_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant__ TcArgs args) {
@@ -82,53 +130,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);  // full0, full1, a, h, o
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffBar + 64);
-    int *s_ctl = reinterpret_cast<int *>(sm + kOffBar + 128);  // current, next chain
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffMisc);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+    ChainDesc *ring = reinterpret_cast<ChainDesc *>(sm + kOffRing);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
-    const int row = 32 * quad + lane_id;  // TMEM lane = matrix row
+    const int row = 32 * (warp & 3) + lane_id;  // TMEM lane = matrix row
+    const uint32_t lane = (uint32_t)(32 * (warp & 3)) << 16;
     const int H = (int)p.H;
     const int S = MODE == kModeSerial ? 1 : ws.n_segments;
-    const int kinds = MODE == kModePre ? 2 : 1;
-    const int total = (int)(p.N * S * H * kinds);
-    int32_t *counter = ws.n_chunks + 1 + MODE;
-    const int4 *tab = reinterpret_cast<const int4 *>(ws.chunk_tab);
 
-    // Work list: heads fastest, then (transition kind), segment, and the
-    // sequences longest first.
-    auto decode = [&](int id, Chain &c) {
-        int r = id;
-        c.h = r % H;
-        r /= H;
-        c.trans = false;
-        if (MODE == kModePre) {
-            c.trans = (r & 1) != 0;
-            r >>= 1;
-        }
-        c.s = r % S;
-        r /= S;
-        c.n = ws.seq_order[r];
-        c.c_begin = ws.seq_chunk0[c.n];
-        const int nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
-        c.s0 = 0;
-        c.s1 = nc;
-        if (MODE != kModeSerial) {
-            const int per = (nc + S - 1) / S;
-            c.s0 = c.s * per;
-            c.s1 = min(nc, c.s0 + per);
-        }
+    auto wait = [&](int b, uint32_t parity) -> bool {
+        return mbar_wait_or_abort(&bars[b], parity & 1u, p.status, s_abort);
     };
-    // Thread 0: next chain with work (empty segments are skipped), or total.
-    auto fetch = [&]() -> int {
-        while (true) {
-            const int id = atomicAdd(counter, 1);
-            if (id >= total) return total;
-            Chain c;
-            decode(id, c);
-            if (c.s0 < c.s1) return id;
-        }
+    // Reads chain number k of the ring (all roles but the scheduler).
+    auto take = [&](int k, ChainDesc &c) -> bool {
+        const int slot = k % kRing;
+        if (!wait(kBCfull + slot, (uint32_t)(k / kRing))) return false;
+        c = ring[slot];
+        mbar_arrive(&bars[kBCempty + slot]);
+        return true;
     };
 
     if (warp == 0) {
@@ -136,269 +158,348 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(&bars[b], 1);
+        for (int b = 0; b < kNumBars; ++b) {
+            uint32_t cnt = 1;
+            if (b == kBMready || b == kBVready || b == kBOfree || b == kBOfree + 1)
+                cnt = 128;
+            if (b >= kBCempty) cnt = 257;
+            mbar_init(&bars[b], cnt);
+        }
+        *s_abort = 0;
         mbar_init_fence();
-        tma_prefetch_desc(&args.tk);
-        if (kOut) tma_prefetch_desc(&args.tq);
-        tma_prefetch_desc(&args.trec128);
-        if (kOut) tma_prefetch_desc(&args.trec64);
-        s_ctl[0] = fetch();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t lane = (uint32_t)(32 * quad) << 16;
-    const int kbase = 64 * half;
 
-    // K (and Q) tiles of a chunk plus its record (W, U^T, P, vectors).
-    auto issue_tma = [&](const Chain &c, int cc, int stage) {
-        const int gc = c.c_begin + cc;
-        const int tt = tab[gc].y;
-        const int64_t rid = (int64_t)gc * H + c.h;
-        const int rrow = (int)(rid * kRecRows);  // the host keeps this below 2^31
-        const uint8_t *rec = ws.rec + rid * kRecBytes;
-        uint64_t *bar = &bars[stage];
-        uint8_t *dst = sm + stage * kStage;
-        uint32_t bytes = 16384u + 16384u + 1024u;  // K, W, vectors
-        if (kOut) bytes += 16384u + 8192u;          // Q, P
-        if (!c.trans) bytes += 16384u;              // U^T
-        mbar_arrive_expect_tx(bar, bytes);
-        tma_load_3d(dst, &args.tk, bar, 0, c.h, tt);
-        tma_load_3d(dst + 16384, &args.tk, bar, 64, c.h, tt);
-        if (kOut) {
-            tma_load_3d(dst + 8192, &args.tq, bar, 0, c.h, tt);
-            tma_load_3d(dst + 24576, &args.tq, bar, 64, c.h, tt);
-        }
-        tma_load_2d(dst + kStW, &args.trec128, bar, 0, rrow + kRecW);
-        if (!c.trans) tma_load_2d(dst + kStU, &args.trec128, bar, 0, rrow + kRecU);
-        if (kOut) tma_load_2d(dst + kStP, &args.trec64, bar, 0, rrow + kRecP);
-        bulk_load(dst + kStVec, rec + kRecVec * 128, 1024u, bar);
-    };
-
-    int cur = s_ctl[0];
-    uint32_t gk = 0;  // chunks processed by this CTA: stage and parity
-    uint32_t ph_a = 0, ph_h = 0, ph_o = 0;
-    bool failed = false;
-    if (cur < total && tid == 0) {
-        Chain c;
-        decode(cur, c);
-        issue_tma(c, c.s0, 0);
-    }
-
-    while (cur < total) {
-        Chain C;
-        decode(cur, C);
-        if (tid == 0) s_ctl[1] = fetch();
-        const int h = C.h;
-        const bool trans = C.trans;
-        const int64_t seg_base = (C.n * H + h) * (int64_t)S + C.s;
-
-        // Canonical state: column v = row of h, keys [64 half, 64 half + 64),
-        // FP32 in TMEM; its BF16 mirror (the MMA operand) in shared memory.
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float hv[32];
-#pragma unroll
-            for (int kk = 0; kk < 32; ++kk) {
-                const int key = kbase + 32 * q + kk;
-                float x = 0.f;
-                if (MODE == kModeSerial) {
-                    if (p.h0) x = p.h0[((C.n * H + h) * kD + key) * kD + row];
-                } else if (MODE == kModeSegOut) {
-                    x = ws.segH[(seg_base * kD + key) * kD + row];
-                } else if (trans) {
-                    x = key == row ? 1.f : 0.f;
-                }
-                hv[kk] = x;
-            }
-            tmem_store32f(tmem + lane + kColS + kbase + 32 * q, hv);
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8)
-                st_bf16x8(sm + kOffHm + sw128_off(row, kbase + 32 * q + 8 * c8, 128), hv + 8 * c8);
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        const int nxt = s_ctl[1];
-        Chain Cn;
-        if (nxt < total) decode(nxt, Cn);
-
-        for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
-            const int stage = gk & 1;
-            const int4 e = tab[C.c_begin + cc];
-            const int64_t t0 = e.y;
-            const int len = e.z;
-            uint8_t *st = sm + stage * kStage;
-            const uint32_t sta = sb + stage * kStage;
-            const float *sDec = reinterpret_cast<const float *>(st + kStVec);
-            const float *sGam = sDec + 64;
-            // the chunk after this one: next in this chain, or the next chain's first
-            if (tid == 0) {
-                if (cc + 1 < C.s1)
-                    issue_tma(C, cc + 1, stage ^ 1);
-                else if (nxt < total)
-                    issue_tma(Cn, Cn.s0, stage ^ 1);
-            }
-            bool ok = mbar_wait(&bars[stage], (gk >> 1) & 1u, p.status);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            const float gam_last = sDec[128];
-            if (len < 64) {  // K rows past the sequence end belong to the next one: zero them
-                const int rows = 64 - len;
-                for (int idx = tid; idx < rows * 2 * 8; idx += kThreads) {
-                    const int r = len + idx / 16, blk = (idx / 8) & 1, c16 = idx & 7;
-                    st_shared_v4(st + blk * 16384 + r * 128 + c16 * 16, 0u, 0u, 0u, 0u);
-                }
-                fence_async_smem();
-            }
-            __syncthreads();
-
-            // A6: v_new^T = U^T - h^T W^T   (and O1 = h^T Q^T for the output)
-            if (tid == 0) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    umma_bf16(tmem + kColVn,
-                              sdesc_sw128(sb + kOffHm + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                              sdesc_sw128(sta + kStW + kk * 2048, 8192, 1024), kIdescKM64, kk > 0);
-                umma_commit(&bars[2]);
-                if (kOut) {
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16(tmem + kColO1,
-                                  sdesc_sw128(sb + kOffHm + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
-                                              1024),
-                                  sdesc_sw128(sta + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
-                                              1024),
-                                  kIdescKK64, kk > 0);
-                }
-            }
-            ok = mbar_wait(&bars[2], ph_a, p.status);
-            ph_a ^= 1;
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            tc_fence_after();
-            {
-                float w[32], u[32];
-                tmem_load32f(tmem + lane + kColVn + 32 * half, w);
-                if (!trans) {
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8)
-                        ld_bf16x8(st + kStU + sw128_off(row, 32 * half + 8 * c8, 128), u + 8 * c8);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) u[i] = 0.f;
-                }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    u[i] -= w[i];                        // v_new
-                    w[i] = u[i] * sDec[32 * half + i];   // v_new e^{G_last - G}
-                }
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    st_bf16x8(sm + kOffVn + sw128_off(row, 32 * half + 8 * c8, 128), u + 8 * c8);
-                    st_bf16x8(sm + kOffVd + sw128_off(row, 32 * half + 8 * c8, 128), w + 8 * c8);
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-
-            // h^T update product, and O2 = v_new^T P^T
-            if (tid == 0) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tmem + kColH, sdesc_sw128(sb + kOffVd + kk * 32, 16, 1024),
-                              sdesc_sw128(sta + kk * 2048, 16384, 1024), kIdescKM128, kk > 0);
-                umma_commit(&bars[3]);
-                if (kOut) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + kColO2, sdesc_sw128(sb + kOffVn + kk * 32, 16, 1024),
-                                  sdesc_sw128(sta + kStP + kk * 32, 16, 1024), kIdescKK64, kk > 0);
-                    umma_commit(&bars[4]);
-                }
-            }
-            ok = mbar_wait(&bars[3], ph_h, p.status);
-            ph_h ^= 1;
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            tc_fence_after();
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float f[32], hv[32];
-                tmem_load32f(tmem + lane + kColH + kbase + 32 * q, f);
-                tmem_load32f(tmem + lane + kColS + kbase + 32 * q, hv);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) hv[i] = fmaf(gam_last, hv[i], f[i]);
-                tmem_store32f(tmem + lane + kColS + kbase + 32 * q, hv);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    st_bf16x8(sm + kOffHm + sw128_off(row, kbase + 32 * q + 8 * c8, 128),
-                              hv + 8 * c8);
-            }
-            fence_async_smem();
-
-            // A7: output rows of this chunk, staged over the v_new tile.
-            if (kOut) {
-                ok = mbar_wait(&bars[4], ph_o, p.status);
-                ph_o ^= 1;
-                if (__syncthreads_or(!ok)) { failed = true; break; }
-                tc_fence_after();
-                uint8_t *stage_o = sm + kOffVn;
-                {
-                    float o1[32], o2[32];
-                    tmem_load32f(tmem + lane + kColO1 + 32 * half, o1);
-                    tmem_load32f(tmem + lane + kColO2 + 32 * half, o2);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = 32 * half + i;
-                        const float y = p.scale * fmaf(sGam[t], o1[i], o2[i]);
-                        *reinterpret_cast<__nv_bfloat16 *>(stage_o + t * 256 + row * 2) =
-                            __float2bfloat16_rn(y);
+    if (warp == 9) {
+        // ------------------------------------------------------------ producer
+        // Work list: heads fastest, then (transition kind), segment, and the
+        // sequences longest first; chains without chunks are skipped.
+        if (lane_id == 0) {
+            const int kinds = MODE == kModePre ? 2 : 1;
+            const int total = (int)(p.N * S * H * kinds);
+            int32_t *counter = ws.n_chunks + 1 + MODE;
+            int issued = 0;
+            for (int posted = 0;; ++posted) {
+                ChainDesc c{};
+                while (true) {
+                    const int id = atomicAdd(counter, 1);
+                    if (id >= total) break;
+                    int r = id;
+                    c.h = r % H;
+                    r /= H;
+                    c.trans = 0;
+                    if (MODE == kModePre) {
+                        c.trans = r & 1;
+                        r >>= 1;
+                    }
+                    c.s = r % S;
+                    r /= S;
+                    c.n = ws.seq_order[r];
+                    c.c_begin = ws.seq_chunk0[c.n];
+                    const int nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
+                    c.s0 = 0;
+                    c.s1 = nc;
+                    if (MODE != kModeSerial) {
+                        const int per = (nc + S - 1) / S;
+                        c.s0 = c.s * per;
+                        c.s1 = min(nc, c.s0 + per);
+                    }
+                    if (c.s0 < c.s1) {
+                        c.tstart = p.cu ? (int64_t)p.cu[c.n] : c.n * p.T;
+                        c.tlen = (p.cu ? (int64_t)p.cu[c.n + 1] : (c.n + 1) * p.T) - c.tstart;
+                        c.valid = 1;
+                        break;
                     }
                 }
+                const int slot = posted % kRing;
+                if (posted >= kRing && !wait(kBCempty + slot, (uint32_t)(posted / kRing - 1)))
+                    break;
+                ring[slot] = c;
+                mbar_arrive(&bars[kBCfull + slot]);
+                if (!c.valid) break;
+                bool ok = true;
+                // every chunk's record, into stage issued & 1 once the chunk two
+                // before has released it
+                for (int cc = c.s0; cc < c.s1; ++cc, ++issued) {
+                    const int stage = issued & 1;
+                    if (issued >= 2 && !wait(kBFree + stage, (uint32_t)((issued >> 1) - 1))) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t rid = (int64_t)(c.c_begin + cc) * H + c.h;
+                    const uint8_t *rec = ws.rec + rid * kRecBytes;
+                    uint64_t *bar = &bars[kBFull + stage];
+                    uint8_t *dst = sm + stage * kStage;
+                    if (kOut) {  // the whole image
+                        mbar_arrive_expect_tx(bar, kImgBytes);
+                        bulk_load(dst, rec, kImgBytes, bar);
+                    } else {     // W, K~, U^T (not for the transition), vectors
+                        const uint32_t bytes = 16384u + 16384u + 16u + (c.trans ? 0u : 16384u);
+                        mbar_arrive_expect_tx(bar, bytes);
+                        bulk_load(dst + kImgWQ, rec + kImgWQ, 8192u, bar);
+                        bulk_load(dst + kImgWQ + 16384, rec + kImgWQ + 16384, 8192u, bar);
+                        bulk_load(dst + kImgK, rec + kImgK, 16384u, bar);
+                        if (!c.trans) bulk_load(dst + kImgU, rec + kImgU, 16384u, bar);
+                        bulk_load(dst + kImgVec, rec + kImgVec, 16u, bar);
+                    }
+                }
+                if (!ok) break;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ control
+        if (lane_id == 0) {
+            int k = 0, gk = 0;
+            bool ok = true;
+            while (ok) {
+                ChainDesc C;
+                if (!take(k++, C) || !C.valid) break;
+                for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
+                    const int b = gk & 1;
+                    const uint32_t sta = sb + b * kStage;
+                    if (!wait(kBFull + b, gk >> 1) || !wait(kBMready, gk) ||
+                        (kOut && gk >= 2 && !wait(kBOfree + b, (gk >> 1) - 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // [h^T W^T | O = h^T Q~^T]
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        umma_bf16(tmem + kColA + 128 * b, sdesc_sw128(sb + kOffHm + ko, 16, 1024),
+                                  sdesc_sw128(sta + kImgWQ + ko, 16, 1024),
+                                  kOut ? kIdescA128 : kIdescA64, kk > 0);
+                    }
+                    umma_commit(&bars[kBAdone]);
+                    if (!wait(kBVready, gk)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tmem + kColS, sdesc_sw128(sb + kOffVn + kk * 32, 16, 1024),
+                                  sdesc_sw128(sta + kImgK + kk * 2048, 8192, 1024), kIdescH, 1u);
+                    umma_commit(&bars[kBHdone]);
+                    if (kOut) {  // O += v_new^T (scale P)^T
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_bf16(tmem + kColA + 128 * b + 64,
+                                      sdesc_sw128(sb + kOffVn + kk * 32, 16, 1024),
+                                      sdesc_sw128(sta + kImgP + kk * 2048, 8192, 1024), kIdescO2,
+                                      1u);
+                        umma_commit(&bars[kBO2 + b]);
+                    }
+                    umma_commit(&bars[kBFree + b]);
+                }
+            }
+            // nothing of this CTA may still run on the tensor cores at exit
+            umma_commit(&bars[kBDrain]);
+            mbar_wait(&bars[kBDrain], 0, p.status, 100000000ull);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ state path
+        int k = 0, gk = 0;
+        bool ok = true;
+        while (ok) {
+            ChainDesc C;
+            if (!take(k++, C) || !C.valid) break;
+            const int h = C.h;
+            const bool trans = C.trans != 0;
+            const int64_t seg_base = (C.n * H + h) * (int64_t)S + C.s;
+            for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
+                const int b = gk & 1;
+                const uint8_t *st = sm + b * kStage;
+                if (!wait(kBFull + b, gk >> 1)) { ok = false; break; }
+                tc_fence_after();  // the state written by the previous update product
+                const float gam_last = reinterpret_cast<const float *>(st + kImgVec)[kImgGamLast];
+                // h_pre -> BF16 mirror (the first product's A operand), then the
+                // FP32 state scaled by e^{G_last} for the update product.
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {
+                    uint32_t r0[32], r1[32];
+                    if (cc == C.s0) {  // the chain's initial state, column `row`
+#pragma unroll
+                        for (int kk = 0; kk < 64; ++kk) {
+                            const int key = 64 * hq + kk;
+                            float v = 0.f;
+                            if (MODE == kModeSerial) {
+                                if (p.h0) v = p.h0[((C.n * H + h) * kD + key) * kD + row];
+                            } else if (MODE == kModeSegOut) {
+                                v = ws.segH[(seg_base * kD + key) * kD + row];
+                            } else if (trans) {
+                                v = key == row ? 1.f : 0.f;
+                            }
+                            if (kk < 32) r0[kk] = __float_as_uint(v);
+                            else r1[kk - 32] = __float_as_uint(v);
+                        }
+                    } else {
+                        tmem_ld32(tmem + lane + kColS + 64 * hq, r0);
+                        tmem_ld32(tmem + lane + kColS + 64 * hq + 32, r1);
+                        tmem_wait_ld();
+                        reg_fence(r0);
+                        reg_fence(r1);
+                    }
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        float x[8], y[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            x[u] = __uint_as_float(r0[8 * c8 + u]);
+                            y[u] = __uint_as_float(r1[8 * c8 + u]);
+                        }
+                        st_bf16x8(sm + kOffHm + sw128_off(row, 64 * hq + 8 * c8, 128), x);
+                        st_bf16x8(sm + kOffHm + sw128_off(row, 64 * hq + 32 + 8 * c8, 128), y);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gam_last);
+                        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * gam_last);
+                    }
+                    tmem_st32(tmem + lane + kColS + 64 * hq, r0);
+                    tmem_st32(tmem + lane + kColS + 64 * hq + 32, r1);
+                }
+                fence_async_smem();
+                mbar_arrive(&bars[kBMready]);
+                if (!wait(kBAdone, gk)) { ok = false; break; }
+                tc_fence_after();
+                {  // v_new^T = U^T - h^T W^T
+                    uint32_t w0[32], w1[32];
+                    tmem_ld32(tmem + lane + kColA + 128 * b, w0);
+                    tmem_ld32(tmem + lane + kColA + 128 * b + 32, w1);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float u[32];
+                        if (!trans) {
+#pragma unroll
+                            for (int c8 = 0; c8 < 4; ++c8)
+                                ld_bf16x8(st + kImgU + sw128_off(row, 32 * hh + 8 * c8, 128),
+                                          u + 8 * c8);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) u[i] = 0.f;
+                        }
+                        if (hh == 0) {
+                            tmem_wait_ld();
+                            reg_fence(w0);
+                            reg_fence(w1);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) u[i] -= __uint_as_float(hh ? w1[i] : w0[i]);
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8)
+                            st_bf16x8(sm + kOffVn + sw128_off(row, 32 * hh + 8 * c8, 128),
+                                      u + 8 * c8);
+                    }
+                }
+                fence_async_smem();
+                tmem_wait_st();  // the scaled state, before the update product
                 tc_fence_before();
-                __syncthreads();
+                mbar_arrive(&bars[kBVready]);
+                if (!wait(kBHdone, gk)) { ok = false; break; }
+            }
+            if (!ok) break;
+            if ((MODE != kModeSegOut) && (MODE != kModeSerial || p.ht)) {
+                tc_fence_after();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float hv[32];
+                    tmem_load32f(tmem + lane + kColS + 32 * q, hv);
+                    if (MODE == kModeSerial) {
+#pragma unroll
+                        for (int kk = 0; kk < 32; ++kk)
+                            p.ht[((C.n * H + h) * kD + 32 * q + kk) * kD + row] = hv[kk];
+                    } else if (trans) {  // M_s stored transposed: row `row`
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            ws.segM + (seg_base * kD + row) * kD + 32 * q);
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; ++k4)
+                            dst[k4] = make_float4(hv[4 * k4], hv[4 * k4 + 1], hv[4 * k4 + 2],
+                                                  hv[4 * k4 + 3]);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 32; ++kk)
+                            ws.segC[(seg_base * kD + 32 * q + kk) * kD + row] = hv[kk];
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ output path
+        const int tb = tid - 128;
+        int k = 0, gk = 0;
+        bool ok = true, stores = false;
+        int64_t p_t0 = 0;
+        int p_len = 0, p_h = 0, p_gk = 0;
+        uint8_t *os = sm + kOffOs;  // [t][v] as two swizzled 64-column blocks
+        // A7 for chunk p_gk: its O tile, BF16, to the output.
+        auto out_epilogue = [&]() -> bool {
+            const int b = p_gk & 1;
+            if (tb == 0 && stores) bulk_wait_read();  // the staging tile is free again
+            // all output-path threads agree (and the staging tile's previous
+            // contents are stored) before any of them goes on
+            if (!side_all(wait(kBO2 + b, p_gk >> 1))) return false;
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tmem + lane + kColA + 128 * b + 64, r0);
+            tmem_ld32(tmem + lane + kColA + 128 * b + 96, r1);
+            tmem_wait_ld();
+            reg_fence(r0);
+            reg_fence(r1);
+            tc_fence_before();
+            mbar_arrive(&bars[kBOfree + b]);
+            uint8_t *col = os + (row >> 6) * 8192;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                *reinterpret_cast<__nv_bfloat16 *>(col + sw128_off(i, row & 63, 64)) =
+                    __float2bfloat16_rn(__uint_as_float(r0[i]));
+                *reinterpret_cast<__nv_bfloat16 *>(col + sw128_off(32 + i, row & 63, 64)) =
+                    __float2bfloat16_rn(__uint_as_float(r1[i]));
+            }
+            if (p_len == kChunk) {
+                fence_async_smem();
+                side_sync();
+                if (tb == 0) {
+                    tma_store_3d(&args.to, os, 0, p_h, (int)p_t0);
+                    tma_store_3d(&args.to, os + 8192, 64, p_h, (int)p_t0);
+                    bulk_commit();
+                    stores = true;
+                }
+            } else {  // a sequence's last chunk: rows past its end belong to the next
+                side_sync();
                 __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int idx = tid + kThreads * r;
+                for (int r = 0; r < 8; ++r) {
+                    const int idx = tb + 128 * r;
                     const int t = idx >> 4, c16 = idx & 15;
-                    if (t < len)
-                        *reinterpret_cast<uint4 *>(o + ((t0 + t) * H + h) * (int64_t)kD + c16 * 8) =
-                            *reinterpret_cast<const uint4 *>(stage_o + t * 256 + c16 * 16);
+                    if (t < p_len)
+                        *reinterpret_cast<uint4 *>(o + ((p_t0 + t) * H + p_h) * (int64_t)kD +
+                                                   c16 * 8) =
+                            *reinterpret_cast<const uint4 *>(os + (c16 >> 3) * 8192 +
+                                                             sw128_off(t, (c16 & 7) * 8, 64));
                 }
             }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-        }
-        if (failed) break;
-        if ((MODE != kModeSegOut) && (MODE != kModeSerial || p.ht)) {
-            tc_fence_after();
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float hv[32];
-                tmem_load32f(tmem + lane + kColS + kbase + 32 * q, hv);
-                if (MODE == kModeSerial) {
-#pragma unroll
-                    for (int kk = 0; kk < 32; ++kk)
-                        p.ht[((C.n * H + h) * kD + kbase + 32 * q + kk) * kD + row] = hv[kk];
-                } else if (trans) {  // M_s stored transposed: row `row`
-                    float4 *dst = reinterpret_cast<float4 *>(ws.segM + (seg_base * kD + row) * kD +
-                                                             kbase + 32 * q);
-#pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4)
-                        dst[k4] = make_float4(hv[4 * k4], hv[4 * k4 + 1], hv[4 * k4 + 2],
-                                              hv[4 * k4 + 3]);
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < 32; ++kk)
-                        ws.segC[(seg_base * kD + kbase + 32 * q + kk) * kD + row] = hv[kk];
-                }
+            return true;
+        };
+        while (ok) {
+            ChainDesc C;
+            if (!take(k++, C) || !C.valid) break;
+            for (int cc = C.s0; kOut && cc < C.s1; ++cc, ++gk) {
+                const int64_t rem = C.tlen - (int64_t)kChunk * cc;
+                p_t0 = C.tstart + (int64_t)kChunk * cc;
+                p_len = rem < kChunk ? (int)rem : kChunk;
+                p_h = C.h;
+                p_gk = gk;
+                if (!out_epilogue()) { ok = false; break; }
             }
         }
-        cur = nxt;
+        if (tb == 0 && stores) bulk_wait_read();
     }
     tc_fence_before();
     __syncthreads();
@@ -429,11 +530,7 @@ cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream
     args.ws = ws;
     const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
     const uint64_t H = (uint64_t)p.H;
-    const uint64_t rec_rows = (uint64_t)ws.max_chunks * H * kRecRows;
-    if (!make_tmap_bf16_3d(&args.tq, p.q, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64) ||
-        !make_tmap_bf16_2d(&args.trec128, ws.rec, 64, rec_rows, 128, 64, 128) ||
-        !make_tmap_bf16_2d(&args.trec64, ws.rec, 64, rec_rows, 128, 64, 64))
+    if (!make_tmap_bf16_3d(&args.to, p.o, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     const int S = mode == 0 ? 1 : ws.n_segments;
     const int64_t chains = p.N * S * p.H * (mode == 1 ? 2 : 1);

@@ -10,17 +10,25 @@ namespace tc {
 
 constexpr int kD = 128;  // K = V = 128 on the tensor-core path
 
-// One record per (chunk, head), BF16 rows of 64 elements (128 bytes):
-//   rows   0..127  W, MN-major: row `key` holds W[t][key] for t = 0..63
-//   rows 128..255  U^T: row `v` holds U[t][v] for t = 0..63
-//   rows 256..319  P: row i holds (Q K^T * e^{G_i - G_j}, j <= i)[i][j]
-//   rows 320..327  FP32 vectors: e^{G_last - G_t} (64), e^{G_t} (64),
-//                  e^{G_last} (1), padding
-// Padded tokens (past a sequence end) have zero W rows' entries, zero U and
-// P entries: every later product with them adds exact zeros.
-constexpr int kRecRows = 328;
-constexpr uint32_t kRecBytes = kRecRows * 128;  // 41984, also sized in gdr_api.cu
-constexpr int kRecW = 0, kRecU = 128, kRecP = 256, kRecVec = 320;
+// One record per (chunk, head): the byte image of the scan kernel's
+// shared-memory stage, so that one bulk copy loads it.  BF16 tiles of 64
+// columns in the 128-byte swizzled layout (sw128_off, 64 rows per 8 KB
+// block unless noted):
+//   [0, 32 KB)      W block 0 | Q~ block 0 | W block 1 | Q~ block 1: row t of
+//                   W block b holds W[t][64 b .. 64 b + 63] (K-major), row t
+//                   of Q~ block b holds Q~[t][64 b ..], Q~ = scale e^{G_t} q_t
+//   [32 KB, 48 KB)  K~ block 0 | K~ block 1, K~ = e^{G_last - G_t} k_t
+//                   (rows t, keys: the MN-major B operand of the update)
+//   [48 KB, 56 KB)  P^T: row j holds scale P[i][j] for i = 0..63, where
+//                   P = (Q K^T * e^{G_i - G_j}, j <= i)
+//   [56 KB, 72 KB)  U^T, 128 rows: row v holds U[t][v] for t = 0..63
+//   [72 KB, +16 B)  FP32 G_last, e^{G_last}, two unused floats
+// Padded tokens (past a sequence end) have zero W, Q~, K~, U and P entries:
+// every later product with them adds exact zeros.
+constexpr uint32_t kImgWQ = 0, kImgK = 32768, kImgP = 49152, kImgU = 57344, kImgVec = 73728;
+constexpr uint32_t kImgBytes = kImgVec + 16;    // bytes written and loaded per record
+constexpr uint32_t kRecBytes = 74752;           // record stride (1 KB aligned); gdr_api.cu sizes it
+constexpr int kImgGamLast = 1;                  // float index of e^{G_last} at kImgVec
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);

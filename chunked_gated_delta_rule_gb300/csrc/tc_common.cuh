@@ -76,6 +76,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     }
 }
 
+// As mbar_wait, for kernels whose warps play different roles: a wait also
+// ends (returning false) once another thread has raised `abort`, and a wait
+// that times out raises it, so every role leaves promptly after a failure.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity,
+                                                   int32_t *status, volatile int *abort,
+                                                   uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            if (status) atomicCAS(status, 0, (int32_t)GDR_ERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 // 3-D tiled load into shared memory, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map,
@@ -106,6 +125,45 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
         ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes),
         "r"(smem_u32(bar))
         : "memory");
+}
+
+// 2-D tiled store shared -> global, tracked by this thread's bulk async group.
+// The shared tile must have been written before a fence_async_smem() and a
+// barrier.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src, int c0,
+                                             int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+// 3-D tiled store shared -> global, tracked by this thread's bulk async group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *smem_src, int c0,
+                                             int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// 1-D bulk copy shared -> global (16-B aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every committed bulk store of this thread has finished reading
+// shared memory (the source may then be overwritten or the CTA may exit).
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
@@ -206,6 +264,49 @@ __device__ __forceinline__ void tmem_store32f(uint32_t taddr, const float (&f)[3
         "f"(f[22]), "f"(f[23]), "f"(f[24]), "f"(f[25]), "f"(f[26]), "f"(f[27]), "f"(f[28]),
         "f"(f[29]), "f"(f[30]), "f"(f[31])
         : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Unwaited forms, so that several TMEM transfers overlap under one wait:
+// tmem_ld32 issues a load whose registers are valid only after tmem_wait_ld()
+// and reg_fence() on them; tmem_st32 issues a store that completes at
+// tmem_wait_st().
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// After tmem_wait_ld(): no use of r can be scheduled before the wait.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 

@@ -2,16 +2,18 @@
 // FP32 matrix A in shared memory (row stride kInvLd), by one CTA of 256
 // threads (A4 of the chunked form: the UT transform's triangular inverse).
 //
-//   1. The four 16 x 16 diagonal blocks T_bb = (I + A_bb)^-1 in FP32: one
-//      thread per (block, column) solves (I + A_bb) x = e_m by right-looking
+//   1. invert_diag16: the four 16 x 16 diagonal blocks T_bb = (I + A_bb)^-1
+//      in FP32, one thread per (block, column) (64 threads): right-looking
 //      forward substitution (after x_j is known, every later row's partial
-//      sum takes its A_rj x_j term), so the dependent chain is 16 steps long.
-//   2. Off-diagonal blocks by distance d = 1, 2, 3 (standard block forward
-//      substitution):  T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj,  i = j + d.
-//      Each 16 x 8 column tile of each block is one warp's job: the products
-//      run on warp-level tensor cores as three TF32 products (x = hi + lo;
+//      sum takes its A_rj x_j term), a dependent chain of 16 steps.
+//   2. invert_merge, standard recursive block inversion of
+//      [[T_1, 0], [A_21, T_2]]:  T_21 = -T_2 (A_21 T_1), first for the 16 x 16
+//      blocks (1, 0) and (3, 2), then for the 32 x 32 block of rows 32-63,
+//      columns 0-31.  Every 16 x 8 output tile of a product is one warp's
+//      job on warp-level tensor cores, as three TF32 products (x = hi + lo;
 //      a_hi b_hi + a_hi b_lo + a_lo b_hi, each in its own accumulator), which
-//      keeps close to FP32 accuracy with short dependent chains.
+//      keeps close to FP32 accuracy; tiles of a triangular factor that are
+//      zero are skipped.
 //
 // T's entries above the diagonal of each diagonal block are written as 0;
 // blocks above the block diagonal are not written (callers mask j > i).
@@ -24,7 +26,8 @@ namespace tc {
 
 constexpr int kInvLd = 68;   // row stride of A and T (floats; rows 16-B aligned)
 constexpr int kInvXLd = 8;   // row stride of a warp's 16 x 8 scratch tile
-constexpr int kInvScratchFloats = 6 * 16 * kInvXLd;
+constexpr int kInvYLd = 40;  // row stride of the 32 x 32 scratch product
+constexpr int kInvScratchFloats = 32 * kInvYLd;  // covers 4 warps x 16 x 8 too
 
 // acc_* (16 x 8, mma accumulator layout) += A(16 x 16) * B(16 x 8), both
 // row-major FP32 in shared memory, split into TF32 hi/lo parts.
@@ -54,55 +57,88 @@ __device__ __forceinline__ void warp_gemm16x8_3xtf32(float (&hh)[4], float (&hl)
     }
 }
 
-// sX: kInvScratchFloats floats of scratch.  All 256 threads call this.
-__device__ __forceinline__ void invert_unit_lower64(const float *sA, float *sT, float *sX,
-                                                    int tid) {
-    if (tid < 64) {
-        const int b = tid >> 4, m = tid & 15, o = 16 * b;
-        float s[16], x[16];
+// Stores sign * (sum of the three accumulators) as a 16 x 8 row-major tile.
+__device__ __forceinline__ void warp_store16x8(float *D, int ldd, const float (&hh)[4],
+                                               const float (&hl)[4], const float (&lh)[4],
+                                               float sign, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    D[g * ldd + 2 * t] = sign * ((lh[0] + hl[0]) + hh[0]);
+    D[g * ldd + 2 * t + 1] = sign * ((lh[1] + hl[1]) + hh[1]);
+    D[(g + 8) * ldd + 2 * t] = sign * ((lh[2] + hl[2]) + hh[2]);
+    D[(g + 8) * ldd + 2 * t + 1] = sign * ((lh[3] + hl[3]) + hh[3]);
+}
+
+// Step 1: threads 0..63 only (block tid / 16, column tid % 16).
+__device__ __forceinline__ void invert_diag16(const float *sA, float *sT, int tid) {
+    const int b = tid >> 4, m = tid & 15, o = 16 * b;
+    float s[16], x[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) s[r] = 0.f;
-        // Columns before m are exactly zero, so their (finite) updates add
-        // exact zeros: the loop runs unpredicated, as straight-line code.
+    for (int r = 0; r < 16; ++r) s[r] = 0.f;
+    // Columns before m are exactly zero, so their (finite) updates add
+    // exact zeros: the loop runs unpredicated, as straight-line code.
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            x[j] = j < m ? 0.f : (j == m ? 1.f : -s[j]);
+    for (int j = 0; j < 16; ++j) {
+        x[j] = j < m ? 0.f : (j == m ? 1.f : -s[j]);
 #pragma unroll
-            for (int r = j + 1; r < 16; ++r)
-                s[r] = fmaf(sA[(o + r) * kInvLd + o + j], x[j], s[r]);
-        }
+        for (int r = j + 1; r < 16; ++r) s[r] = fmaf(sA[(o + r) * kInvLd + o + j], x[j], s[r]);
+    }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sT[(o + r) * kInvLd + o + m] = x[r];
+    for (int r = 0; r < 16; ++r) sT[(o + r) * kInvLd + o + m] = x[r];
+}
+
+// Step 2: all 256 threads; the diagonal blocks of sT must be complete (and
+// visible: a barrier after step 1).  sX: kInvScratchFloats floats.  Ends
+// with a barrier.
+__device__ __forceinline__ void invert_merge(const float *sA, float *sT, float *sX, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    // 16 x 16 blocks (1, 0) and (3, 2): warp = 2 (block pair) + column tile
+    if (warp < 4) {
+        const int j = 2 * (warp >> 1), i = j + 1, nt = warp & 1;
+        float hh[4] = {0.f, 0.f, 0.f, 0.f}, hl[4] = {0.f, 0.f, 0.f, 0.f},
+              lh[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_gemm16x8_3xtf32(hh, hl, lh, sA + (16 * i) * kInvLd + 16 * j, kInvLd,
+                             sT + (16 * j) * kInvLd + 16 * j + 8 * nt, kInvLd, lane);
+        float *X = sX + warp * 16 * kInvXLd;
+        warp_store16x8(X, kInvXLd, hh, hl, lh, 1.f, lane);
+        __syncwarp();
+        float th[4] = {0.f, 0.f, 0.f, 0.f}, tl[4] = {0.f, 0.f, 0.f, 0.f},
+              tm[4] = {0.f, 0.f, 0.f, 0.f};
+        warp_gemm16x8_3xtf32(th, tl, tm, sT + (16 * i) * kInvLd + 16 * i, kInvLd, X, kInvXLd,
+                             lane);
+        warp_store16x8(sT + (16 * i) * kInvLd + 16 * j + 8 * nt, kInvLd, th, tl, tm, -1.f, lane);
     }
     __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, t = lane & 3;
-    for (int d = 1; d <= 3; ++d) {
-        if (warp < 2 * (4 - d)) {
-            const int j = warp >> 1, nt = warp & 1, i = j + d;
-            float hh[4] = {0.f, 0.f, 0.f, 0.f}, hl[4] = {0.f, 0.f, 0.f, 0.f},
-                  lh[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k = j; k < i; ++k)
-                warp_gemm16x8_3xtf32(hh, hl, lh, sA + (16 * i) * kInvLd + 16 * k, kInvLd,
-                                     sT + (16 * k) * kInvLd + 16 * j + 8 * nt, kInvLd, lane);
-            float *X = sX + warp * 16 * kInvXLd;
-            X[g * kInvXLd + 2 * t] = (lh[0] + hl[0]) + hh[0];
-            X[g * kInvXLd + 2 * t + 1] = (lh[1] + hl[1]) + hh[1];
-            X[(g + 8) * kInvXLd + 2 * t] = (lh[2] + hl[2]) + hh[2];
-            X[(g + 8) * kInvXLd + 2 * t + 1] = (lh[3] + hl[3]) + hh[3];
-            __syncwarp();
-            float th[4] = {0.f, 0.f, 0.f, 0.f}, tl[4] = {0.f, 0.f, 0.f, 0.f},
-                  tm[4] = {0.f, 0.f, 0.f, 0.f};
-            warp_gemm16x8_3xtf32(th, tl, tm, sT + (16 * i) * kInvLd + 16 * i, kInvLd, X,
-                                 kInvXLd, lane);
-            float *Tij = sT + (16 * i) * kInvLd + 16 * j + 8 * nt;
-            Tij[g * kInvLd + 2 * t] = -((tm[0] + tl[0]) + th[0]);
-            Tij[g * kInvLd + 2 * t + 1] = -((tm[1] + tl[1]) + th[1]);
-            Tij[(g + 8) * kInvLd + 2 * t] = -((tm[2] + tl[2]) + th[2]);
-            Tij[(g + 8) * kInvLd + 2 * t + 1] = -((tm[3] + tl[3]) + th[3]);
-        }
-        __syncthreads();
+    // 32 x 32 block: Y = A[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] =
+    // -T[32:64, 32:64] Y.  Warp = row block rb (16 rows) x column tile nt (8).
+    const int rb = warp >> 2, nt = warp & 3;
+    {
+        float hh[4] = {0.f, 0.f, 0.f, 0.f}, hl[4] = {0.f, 0.f, 0.f, 0.f},
+              lh[4] = {0.f, 0.f, 0.f, 0.f};
+        // T[0:32, 0:32] is lower triangular: rows 0-15 vanish in columns 16-31
+        for (int kb = nt >= 2 ? 1 : 0; kb < 2; ++kb)
+            warp_gemm16x8_3xtf32(hh, hl, lh, sA + (32 + 16 * rb) * kInvLd + 16 * kb, kInvLd,
+                                 sT + (16 * kb) * kInvLd + 8 * nt, kInvLd, lane);
+        warp_store16x8(sX + (16 * rb) * kInvYLd + 8 * nt, kInvYLd, hh, hl, lh, 1.f, lane);
     }
+    __syncthreads();
+    {
+        float hh[4] = {0.f, 0.f, 0.f, 0.f}, hl[4] = {0.f, 0.f, 0.f, 0.f},
+              lh[4] = {0.f, 0.f, 0.f, 0.f};
+        // T[32:64, 32:64] is lower triangular: row block 0 ends at column 15
+        for (int kb = 0; kb <= rb; ++kb)
+            warp_gemm16x8_3xtf32(hh, hl, lh, sT + (32 + 16 * rb) * kInvLd + 32 + 16 * kb, kInvLd,
+                                 sX + (16 * kb) * kInvYLd + 8 * nt, kInvYLd, lane);
+        warp_store16x8(sT + (32 + 16 * rb) * kInvLd + 8 * nt, kInvLd, hh, hl, lh, -1.f, lane);
+    }
+    __syncthreads();
+}
+
+// Both steps, for callers with nothing to overlap with step 1.
+__device__ __forceinline__ void invert_unit_lower64(const float *sA, float *sT, float *sX,
+                                                    int tid) {
+    if (tid < 64) invert_diag16(sA, sT, tid);
+    __syncthreads();
+    invert_merge(sA, sT, sX, tid);
 }
 
 }  // namespace tc

@@ -7,9 +7,12 @@
 //   (tc_inverse.cuh), W^T = K^T (T diag(beta e^G))^T and U^T = V^T
 //   (T diag(beta))^T on tcgen05, P = (Q K^T) * e^{G_i - G_j} for j <= i.
 //
-// The results go to one record per (chunk, head) (layout in tc_chunk.cuh),
-// which the scan kernel (tc_chain.cu) streams back by TMA, so the serial
-// chain only does the state-dependent products.  Chunked form: the project
+// The results, with K~ = diag(e^{G_last - G}) K and Q~ = scale diag(e^G) Q,
+// go to one record per (chunk, head): the byte image of the scan kernel's
+// shared-memory stage (layout in tc_chunk.cuh), assembled here in shared
+// memory and written by bulk async copies, which the scan kernel
+// (tc_chain.cu) loads back with one bulk copy, so the serial chain only does
+// the state-dependent products.  Chunked form: the project
 // statement; the WY/UT preparation ahead of fla's state-scan kernel
 // chunk_gated_delta_rule_fwd_kernel_h_blockdim64 (Kev PR #259 intro).
 #include "gdr_internal.cuh"
@@ -31,15 +34,20 @@ struct PrepArgs {
 constexpr int kThreads = 256;
 
 // Shared memory (bytes from a 1024-aligned base).
-// [0, 48 KB): the K, Q, V tiles [Kb0|Qb0|Kb1|Qb1|Vb0|Vb1]
+// [0, 48 KB): the K, Q, V tiles [Kb0|Qb0|Kb1|Qb1|Vb0|Vb1].  Q~ and K~ are
+// formed in place (once the products reading Q and K are done); W is
+// staged over Vb0|Vb1 and U^T over sA, both after the last product.
+constexpr uint32_t kOffStW = 32768;
 constexpr uint32_t kOffAT = 49152;                      // sA, sT (FP32, ld kInvLd)
 constexpr uint32_t kOffT = kOffAT + 64 * kInvLd * 4;
 constexpr uint32_t kOffBW = kOffAT;                     // B_W, B_U over sA afterwards
 constexpr uint32_t kOffBU = kOffAT + 8192;
+constexpr uint32_t kOffStU = kOffAT;                    // U^T staging, after the last product
 constexpr uint32_t kOffX = kOffAT + 34816;              // inverse scratch
-constexpr uint32_t kOffVec = kOffX + 3072;              // gate vectors
+constexpr uint32_t kOffVec = kOffX + 4 * kInvScratchFloats;  // gate vectors
 constexpr uint32_t kOffBar = kOffVec + 1600;
-constexpr uint32_t kSmemLaunch = kOffBar + 64 + 1024;
+constexpr uint32_t kOffStP = (kOffBar + 64 + 1023) / 1024 * 1024;  // P^T staging, 8 KB
+constexpr uint32_t kSmemLaunch = kOffStP + 8192 + 1024;
 
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColD1 = 0, kColW = 64, kColU = 128;
@@ -47,12 +55,36 @@ constexpr uint32_t kColD1 = 0, kColW = 64, kColU = 128;
 constexpr uint32_t kIdescKK64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescMK64 = idesc_bf16(128, 64, 1, 0);
 
+__device__ __forceinline__ void st_bf16(uint8_t *p, float x) {
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
+}
+
+// Rows of two 8 KB tiles at `a` and `a + 16384` scaled in place by c f[row]
+// (64 rows of 128 bytes each, in 16-byte pieces; thread t of n threads).
+__device__ __forceinline__ void scale_rows_in_place(uint8_t *a, const float *f, float c, int t,
+                                                    int n) {
+    for (int idx = t; idx < 1024; idx += n) {
+        const int row = (idx >> 3) & 63;
+        uint8_t *ptr = a + (idx >> 9) * 16384 + row * 128 + (idx & 7) * 16;
+        float x[8];
+        ld_bf16x8(ptr, x);
+        const float m = c * f[row];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] *= m;
+        st_bf16x8(ptr, x);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__ PrepArgs args) {
     const Problem &p = args.p;
     const Workspace &ws = args.ws;
     const int64_t chunk = blockIdx.x;
     const int h = blockIdx.y;
-    if (chunk >= *ws.n_chunks) return;
+    // Both loads in flight together: the table row exists for every
+    // chunk < max_chunks (the grid), its contents only below n_chunks.
+    const int nck = *ws.n_chunks;
+    const int4 e = reinterpret_cast<const int4 *>(ws.chunk_tab)[chunk];
+    if (chunk >= nck) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -70,26 +102,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
     const int quad = warp & 3, half = warp >> 2;
     const int row = 32 * quad + lane_id;  // TMEM lane = matrix row
     const int H = (int)p.H;
-    const int4 e = reinterpret_cast<const int4 *>(ws.chunk_tab)[chunk];
     const int64_t t0 = e.y;
     const int len = e.z;
-    uint8_t *rec = ws.rec + (chunk * H + h) * (int64_t)kRecBytes;
+    uint8_t *img = ws.rec + (chunk * H + h) * (int64_t)kRecBytes;
 
-    if (warp == 0) {
-        tmem_alloc(s_tmem, kTmemCols);
-        tmem_relinquish();
+    float g2[2] = {0.f, 0.f}, b2[2] = {0.f, 0.f};
+    if (warp == 0) {  // A2 inputs (padded tokens: g = beta = 0), loads in flight early
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int tok = 2 * lane_id + u;
+            if (tok < len) {
+                g2[u] = p.g[(t0 + tok) * H + h];
+                b2[u] = p.beta[(t0 + tok) * H + h];
+            }
+        }
     }
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         mbar_init_fence();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *s_tmem;
-    const uint32_t lane = (uint32_t)(32 * quad) << 16;
-    if (tid == 0) {
         mbar_arrive_expect_tx(&bars[0], 49152u);
         tma_load_3d(sm + 0, &args.tk, &bars[0], 0, h, (int)t0);
         tma_load_3d(sm + 16384, &args.tk, &bars[0], 64, h, (int)t0);
@@ -98,16 +129,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
         tma_load_3d(sm + 32768, &args.tv, &bars[0], 0, h, (int)t0);
         tma_load_3d(sm + 40960, &args.tv, &bars[0], 64, h, (int)t0);
     }
-    if (warp == 0) {  // A2: gates of this chunk (padded tokens: g = beta = 0)
-        float g2[2], b2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int tok = 2 * lane_id + u;
-            g2[u] = tok < len ? p.g[(t0 + tok) * H + h] : 0.f;
-            b2[u] = tok < len ? p.beta[(t0 + tok) * H + h] : 0.f;
-        }
+    if (warp == 0) {
+        tmem_alloc(s_tmem, kTmemCols);
+        tmem_relinquish();
         gate_vectors(vec, g2, b2, len, lane_id);
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const uint32_t lane = (uint32_t)(32 * quad) << 16;
     bool ok = mbar_wait(&bars[0], 0, p.status);
     if (__syncthreads_or(!ok)) goto done;
     if (len < 64) {  // rows past the sequence end belong to the next one: zero them
@@ -158,17 +189,30 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
             for (int c4 = 0; c4 < 8; ++c4)
                 *reinterpret_cast<float4 *>(sA + i * kInvLd + j0 + 4 * c4) =
                     make_float4(f[4 * c4], f[4 * c4 + 1], f[4 * c4 + 2], f[4 * c4 + 3]);
-        } else {  // row i of P (lower, diagonal included), BF16, to the record
+        } else {  // column i of scale P^T
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8)
-                st_bf16x8(rec + (kRecP + i) * 128 + 2 * (j0 + 8 * c8), f + 8 * c8);
+            for (int u = 0; u < 32; ++u)
+                st_bf16(sm + kOffStP + sw128_off(j0 + u, i, 64), p.scale * f[u]);
         }
     }
     tc_fence_before();
     __syncthreads();
 
-    // A4: T = (I + A)^-1
-    invert_unit_lower64(sA, sT, sX, tid);
+    // A4: T = (I + A)^-1.  The diagonal blocks on warps 0-1 while warps 2-7
+    // form Q~ = scale diag(e^G) Q in place (no product reads Q any more).
+    if (tid < 64)
+        invert_diag16(sA, sT, tid);
+    else
+        scale_rows_in_place(sm + 8192, sGam, p.scale, tid - 64, kThreads - 64);
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(img + kImgWQ + 8192, sm + 8192, 8192u);
+        bulk_store(img + kImgWQ + 24576, sm + 24576, 8192u);
+        bulk_store(img + kImgP, sm + kOffStP, 8192u);
+        bulk_commit();
+    }
+    invert_merge(sA, sT, sX, tid);
 
     // A5 operands: rows of T diag(beta e^G) (rows 0-63) and T diag(beta)
     // (rows 64-127), BF16, columns [32 half, 32 half + 32).
@@ -205,24 +249,32 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
     ok = mbar_wait(&bars[1], 1, p.status);
     if (__syncthreads_or(!ok)) goto done;
     tc_fence_after();
-    {  // W (row = key) and U^T (row = v), t in [32 half, 32 half + 32), to the record
+    {  // W (K-major, row t) and U^T (row v), t in [32 half, 32 half + 32), staged
         float f[32];
         tmem_load32f(tmem + lane + kColW + 32 * half, f);
+        uint8_t *wblk = sm + kOffStW + (row >> 6) * 8192;
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8)
-            st_bf16x8(rec + (kRecW + row) * 128 + 64 * half + 16 * c8, f + 8 * c8);
+        for (int u = 0; u < 32; ++u) st_bf16(wblk + sw128_off(32 * half + u, row & 63, 64), f[u]);
         tmem_load32f(tmem + lane + kColU + 32 * half, f);
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8)
-            st_bf16x8(rec + (kRecU + row) * 128 + 64 * half + 16 * c8, f + 8 * c8);
+            st_bf16x8(sm + kOffStU + sw128_off(row, 32 * half + 8 * c8, 128), f + 8 * c8);
     }
-    if (tid < 64) {
-        float *rv = reinterpret_cast<float *>(rec + kRecVec * 128);
-        rv[tid] = sDec[tid];
-        rv[64 + tid] = sGam[tid];
-        if (tid == 0) rv[128] = sScal[1];
+    // K~ = diag(e^{G_last - G}) K in place (the products reading K are done)
+    scale_rows_in_place(sm, sDec, 1.f, tid, kThreads);
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(img + kImgWQ, sm + kOffStW, 8192u);
+        bulk_store(img + kImgWQ + 16384, sm + kOffStW + 8192, 8192u);
+        bulk_store(img + kImgK, sm, 8192u);
+        bulk_store(img + kImgK + 8192, sm + 16384, 8192u);
+        bulk_store(img + kImgU, sm + kOffStU, 16384u);
+        bulk_store(img + kImgVec, vec + 384, 16u);  // G_last, e^{G_last}
+        bulk_commit();
     }
 done:
+    if (tid == 0) bulk_wait_read();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);

@@ -102,11 +102,12 @@ def test_workspace_size_scales_with_problem():
     small = pkg.gdr_workspace_size(1, 256, 2, 64, 64, dtype=0)
     big = pkg.gdr_workspace_size(1, 16384, 16, 64, 64, dtype=0, n_segments=1)
     assert 0 < small < big
-    # tensor-core path: one 41,984-byte BF16 record per (chunk, head) plus the
-    # chunk table, and the FP32 segment summaries when the sequence is split
+    # tensor-core path: one 74,752-byte record (the scan's stage image) per
+    # (chunk, head) plus the chunk table, and the FP32 segment summaries when
+    # the sequence is split
     tc = pkg.gdr_workspace_size(1, 16384, 16, 128, 128, n_segments=1)
     tc_seg = pkg.gdr_workspace_size(1, 16384, 16, 128, 128, n_segments=16)
-    records = 256 * 16 * 41984
+    records = 256 * 16 * 74752
     assert records < tc < records + 64 * 1024
     assert tc_seg >= tc + 16 * 16 * 3 * 128 * 128 * 4
     gla = pkg.gdr_workspace_size(1, 16384, 16, 128, 128, beta_free=True, n_segments=1)
