@@ -1,12 +1,15 @@
 // compose.cu -- A9, the ordered segment composition h_{s+1} = M_s h_s + c_s
-// for the delta rule (cuLA PR #127 "Root cause and implementation": the
-// per-segment FP32 transition chained by a short ordered pass), FP32 on CUDA
-// cores.  One CTA owns 32 value columns of one (sequence, head) and walks its
-// segments in order; each segment's K x K transition (stored transposed, so
-// the 4 output rows a thread needs are one 16-byte load) is streamed into
-// shared memory by a 1-D bulk async copy, double-buffered so the next
-// transition loads while this one is applied.  Every output element is
-// accumulated by one thread in a fixed order.
+// (cuLA PR #127 "Root cause and implementation": the per-segment FP32
+// transition chained by a short ordered pass), FP32 on CUDA cores.
+//
+// Delta rule: one CTA (512 threads, one per SM) owns CC = 8 or 16 value
+// columns of one (sequence, head) and walks its segments in order.  Each
+// segment's K x K transition (stored transposed, [m][r] = M_s[r][m]) is
+// streamed into shared memory by a 1-D bulk async copy, double-buffered so
+// the next one loads while this one is applied.  A thread owns two state
+// rows x four columns over one slice of the reduction index m; the slices'
+// partial sums are added in a fixed order, so every output element has one
+// fixed summation order.
 #include "gdr_internal.cuh"
 #include "tc_common.cuh"
 
@@ -15,32 +18,37 @@ namespace {
 
 using namespace tc;
 
-constexpr int kCC = 32;  // value columns per CTA
+constexpr int kComposeThreads = 512;
 
-__global__ void __launch_bounds__(256) k_compose_mt(Problem p, Workspace ws) {
+template <int CC>
+__global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Workspace ws) {
+    constexpr int NCG = CC / 4;                         // four-column groups
+    constexpr int NMS = kComposeThreads / (64 * NCG);   // slices of m
     const int K = (int)p.K, V = (int)p.V, H = (int)p.H, S = ws.n_segments;
-    const int tile = blockIdx.x;
+    const int col0 = blockIdx.x * CC;
     const int64_t n = blockIdx.y;
     const int h = blockIdx.z;
-    const int col0 = tile * kCC;
     extern __shared__ uint8_t smem_raw[];
     float *sM0 = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     float *sM1 = sM0 + K * K;
-    float *sH = sM1 + K * K;  // [K][kCC]
+    float *sH0 = sM1 + K * K;      // [K][CC], current / next by parity
+    float *sH1 = sH0 + K * CC;
+    float *sPart = sH1 + K * CC;   // [NMS - 1][K][CC] partial sums
     __shared__ uint64_t bars[2];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int cg = lane & 7;                  // columns 4cg .. 4cg+3
-    const int rg = warp * 4 + (lane >> 3);    // rows 4rg .. 4rg+3
-    const bool active = rg < K / 4;
+    const int tid = threadIdx.x;
+    const int cg = tid % NCG, rp = (tid / NCG) % 64, ms = tid / (NCG * 64);
+    const int r0 = 2 * rp, c0 = 4 * cg;
+    const bool active = r0 < K;
+    const int mlen = K / NMS, m0 = ms * mlen;
 
     const int nc = ws.seq_chunk0[n + 1] - ws.seq_chunk0[n];
     const int per = (nc + S - 1) / S;
     const int nseg = per ? (nc + per - 1) / per : 0;
     const int64_t sbase = (n * H + h) * (int64_t)S;
-    for (int idx = tid; idx < K * kCC; idx += 256) {
-        const int key = idx / kCC, c = idx - key * kCC;
-        sH[idx] = p.h0 ? p.h0[((n * H + h) * K + key) * (int64_t)V + col0 + c] : 0.f;
+    for (int idx = tid; idx < K * CC; idx += kComposeThreads) {
+        const int key = idx / CC, c = idx - key * CC;
+        sH0[idx] = p.h0 ? p.h0[((n * H + h) * K + key) * (int64_t)V + col0 + c] : 0.f;
     }
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -55,55 +63,90 @@ __global__ void __launch_bounds__(256) k_compose_mt(Problem p, Workspace ws) {
     }
     for (int s = 0; s < nseg; ++s) {
         const float *sM = (s & 1) ? sM1 : sM0;
+        const float *cur = (s & 1) ? sH1 : sH0;
+        float *nxt = (s & 1) ? sH0 : sH1;
         if (tid == 0 && s + 1 < nseg) {
-            float *nxt = (s & 1) ? sM0 : sM1;
+            float *buf = (s & 1) ? sM0 : sM1;
             mbar_arrive_expect_tx(&bars[(s + 1) & 1], mbytes);
-            bulk_load(nxt, ws.segM + (sbase + s + 1) * K * K, mbytes, &bars[(s + 1) & 1]);
+            bulk_load(buf, ws.segM + (sbase + s + 1) * K * K, mbytes, &bars[(s + 1) & 1]);
         }
-        float *hs_out = ws.segH + (sbase + s) * K * V;
-        for (int idx = tid; idx < K * kCC; idx += 256) {
-            const int key = idx / kCC, c = idx - key * kCC;
-            hs_out[(int64_t)key * V + col0 + c] = sH[idx];
+        const int64_t hrow = (sbase + s) * K;
+        if (ms == 0 && active) {  // h_s, the segment's initial state
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                *reinterpret_cast<float4 *>(ws.segH + (hrow + r0 + i) * V + col0 + c0) =
+                    *reinterpret_cast<const float4 *>(cur + (r0 + i) * CC + c0);
+        }
+        float4 cv[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+        if (ms == 0 && active) {  // c_s, loaded early
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                cv[i] = __ldg(reinterpret_cast<const float4 *>(ws.segC + (hrow + r0 + i) * V +
+                                                               col0 + c0));
         }
         const bool ok = mbar_wait(&bars[s & 1], (uint32_t)(s >> 1) & 1u, p.status);
         if (__syncthreads_or(!ok)) return;
-        float acc[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         if (active) {
-            for (int m = 0; m < K; ++m) {
-                const float4 mt = *reinterpret_cast<const float4 *>(sM + m * K + 4 * rg);
-                const float4 hv = *reinterpret_cast<const float4 *>(sH + m * kCC + 4 * cg);
-                const float a[4] = {mt.x, mt.y, mt.z, mt.w};
+#pragma unroll 8
+            for (int m = m0; m < m0 + mlen; ++m) {
+                const float2 a = *reinterpret_cast<const float2 *>(sM + m * K + r0);
+                const float4 hv = *reinterpret_cast<const float4 *>(cur + m * CC + c0);
                 const float b[4] = {hv.x, hv.y, hv.z, hv.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int j = 0; j < 4; ++j) {
+                    acc[0][j] = fmaf(a.x, b[j], acc[0][j]);
+                    acc[1][j] = fmaf(a.y, b[j], acc[1][j]);
+                }
+            }
+            if (ms > 0) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int i = 0; i < 2; ++i)
+                    *reinterpret_cast<float4 *>(sPart + ((ms - 1) * K + r0 + i) * CC + c0) =
+                        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
             }
         }
-        fence_async_smem();
         __syncthreads();
-        if (active) {
-            const float *C = ws.segC + (sbase + s) * K * V;
+        if (ms == 0 && active) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 2; ++i) {
+                float y[4] = {acc[i][0], acc[i][1], acc[i][2], acc[i][3]};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = 4 * rg + i, c = 4 * cg + j;
-                    sH[r * kCC + c] = acc[i][j] + C[(int64_t)r * V + col0 + c];
+                for (int q = 0; q < NMS - 1; ++q) {
+                    const float4 pv =
+                        *reinterpret_cast<const float4 *>(sPart + (q * K + r0 + i) * CC + c0);
+                    y[0] += pv.x;
+                    y[1] += pv.y;
+                    y[2] += pv.z;
+                    y[3] += pv.w;
                 }
+                *reinterpret_cast<float4 *>(nxt + (r0 + i) * CC + c0) = make_float4(
+                    y[0] + cv[i].x, y[1] + cv[i].y, y[2] + cv[i].z, y[3] + cv[i].w);
+            }
         }
+        fence_async_smem();  // the transition buffer is refilled by the async proxy next
         __syncthreads();
     }
     if (p.ht) {
-        for (int idx = tid; idx < K * kCC; idx += 256) {
-            const int key = idx / kCC, c = idx - key * kCC;
-            p.ht[((n * H + h) * K + key) * (int64_t)V + col0 + c] = sH[idx];
+        const float *fin = (nseg & 1) ? sH1 : sH0;
+        for (int idx = tid; idx < K * CC; idx += kComposeThreads) {
+            const int key = idx / CC, c = idx - key * CC;
+            p.ht[((n * H + h) * K + key) * (int64_t)V + col0 + c] = fin[idx];
         }
     }
+}
+
+template <int CC>
+cudaError_t launch_compose(const Problem &p, const Workspace &ws, cudaStream_t st) {
+    constexpr int NMS = kComposeThreads / (64 * (CC / 4));
+    const size_t smem = 128 + sizeof(float) * (2 * (size_t)p.K * p.K + (1 + NMS) * (size_t)p.K * CC);
+    cudaError_t err = cudaFuncSetAttribute(k_compose_mt<CC>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((unsigned)(p.V / CC), (unsigned)p.N, (unsigned)p.H);
+    k_compose_mt<CC><<<grid, kComposeThreads, smem, st>>>(p, ws);
+    return cudaGetLastError();
 }
 
 // Beta-free composition (scaled-identity transitions, cuLA PR #127 "Scope":
@@ -144,18 +187,17 @@ cudaError_t compose_scalar(const Problem &p, const Workspace &ws, cudaStream_t s
 }
 
 bool compose_mt_supported(const Problem &p) {
-    return p.beta != nullptr && p.K <= 128 && p.K % 16 == 0 && p.V % kCC == 0;
+    // K a multiple of 32 keeps every slice of m the same length
+    return p.beta != nullptr && p.K <= 128 && p.K % 32 == 0 && p.V % 8 == 0;
 }
 
+// 8 value columns per CTA when that still fits one wave, else 16.
 cudaError_t compose_mt(const Problem &p, const Workspace &ws, cudaStream_t st) {
-    const size_t smem = 128 + sizeof(float) * (2 * (size_t)p.K * p.K + (size_t)p.K * kCC);
-    cudaError_t err = cudaFuncSetAttribute(k_compose_mt,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-    if (err != cudaSuccess) return err;
-    dim3 grid((unsigned)(p.V / kCC), (unsigned)p.N, (unsigned)p.H);
-    k_compose_mt<<<grid, 256, smem, st>>>(p, ws);
-    return cudaGetLastError();
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (p.V % 16 == 0 && (p.V / 8) * p.N * p.H > sms) return launch_compose<16>(p, ws, st);
+    return launch_compose<8>(p, ws, st);
 }
 
 }  // namespace gdr

@@ -230,7 +230,7 @@ const char *gdr_kernel_name(int id) {
     case kKPrep: return "simt_prep";
     case kKScanSerial: return "simt_scan_serial";
     case kKScanPre: return "simt_scan_prescan";
-    case kKCompose: return "simt_compose";
+    case kKCompose: return "compose_delta";
     case kKScanSegOut: return "simt_scan_segment_out";
     case kKOutput: return "simt_output";
     case kKTcSerial: return "tc_chain_serial";
