@@ -230,13 +230,18 @@ def algorithmic_bytes(kernel, x, c):
     return None
 
 
+# The translation unit each kernel is compiled from (plus every shared header).
+KERNEL_SOURCES = {"tc_prep": "tc_prep.cu", "tc_chain": "tc_chain.cu", "tc_gla": "tc_gla.cu",
+                  "compose": "compose.cu", "simt": "simt_path.cu"}
+
+
 def traffic_record(kernel, workload):
     """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    on the kernel's current sources (else None)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = source_hash()
+    src = source_hash(kernel)
     for line in open(path):
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
         if (f.get("kernel") == kernel and f.get("workload") == workload
@@ -245,11 +250,17 @@ def traffic_record(kernel, workload):
     return None
 
 
-def source_hash():
+def source_hash(kernel):
+    """sha256 (16 hex digits) of the kernel's .cu file and every header."""
     import glob
+    csrc = os.path.join(ROOT, "chunked_gated_delta_rule_gb300", "csrc")
+    main = next((v for k, v in KERNEL_SOURCES.items() if kernel.startswith(k)), None)
+    if main is None:
+        main = "compose.cu" if "compose" in kernel else "simt_path.cu"
+    files = [os.path.join(csrc, main)] + sorted(glob.glob(os.path.join(csrc, "*.cuh")))
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "chunked_gated_delta_rule_gb300", "csrc", "*"))):
-        h.update(open(p, "rb").read())
+    for f in files:
+        h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -287,12 +298,12 @@ def time_oracle_on(xo, seqs):
 def cpu_baseline(x, budget_s):
     """Times the oracle over groups of 4 sequences (all heads), cycling
     through the batch, until about `budget_s` seconds of CPU work (at most
-    8 passes over the batch)."""
+    64 passes over the batch)."""
     xo = oracle_inputs(x)
     N = xo["N"]
     secs, toks, threads, groups = 0.0, 0, 1, 0
     n = 0
-    while secs < budget_s and n < 8 * N:
+    while secs < budget_s and n < 64 * N:
         group = [(n + j) % N for j in range(min(4, N))]
         dt, tk, threads = time_oracle_on(xo, group)
         secs += dt
@@ -437,6 +448,19 @@ def run_gdr(args):
                 "timing": "CUDA events around each launch on its stream, over a second "
                           "pass of the same K steps",
                 "peak_source": peaks["source"] + " (hbm_gbs, copy bandwidth)"}
+    # the state scan alone (serial or segment output pass), whichever ran
+    scan = next((n for n in ("tc_chain_serial", "tc_chain_segment_out", "tc_gla_serial",
+                             "tc_gla_segment_out", "simt_scan_serial", "simt_scan_segment_out")
+                 if n in per_kernel), None)
+    scan_roofline = None
+    if scan is not None:
+        sb = algorithmic_bytes(scan, x, c)
+        s_ms = statistics.mean(per_kernel[scan])
+        scan_roofline = {"kernel": scan, "bound": "hbm", "achieved": sb / (s_ms * 1e-3) / 1e9,
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": sb / (s_ms * 1e-3) / 1e9 / hbm,
+                         "traffic": traffic_record(scan, args.workload),
+                         "algorithmic_bytes_per_launch": sb, "avg_launch_ms": s_ms}
     call_bytes = algorithmic_bytes("call", x, c)
     call_roofline = {"achieved": call_bytes / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
                      "frac": call_bytes / (ms * 1e-3) / 1e9 / hbm,
@@ -483,7 +507,8 @@ def run_gdr(args):
                 "dtype": "f32" if plan["path"] == 1 else "bf16",
                 "data": "synthetic (seeded; shapes and distributions of the workload)",
                 "config": config_of(args, x, plan),
-                "roofline": roofline, "call_roofline": call_roofline,
+                "roofline": roofline, "scan_roofline": scan_roofline,
+                "call_roofline": call_roofline,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "kernels": kernels, "clocks": clocks,
                 "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
