@@ -109,18 +109,18 @@ __global__ void k_chunk_table(const int32_t *__restrict__ cu, int64_t N, int64_t
     }
     if (in_smem)
         for (int64_t n = threadIdx.x; n <= N; n += blockDim.x) seq_chunk0[n] = c0[n];
-    for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
+    // one warp per sequence, its lanes over the sequence's chunks
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    for (int64_t n = warp; n < N; n += nwarps) {
         const int64_t a = cu ? cu[n] : n * T;
         const int64_t len = (cu ? cu[n + 1] : (n + 1) * T) - a;
         const int32_t first = c0[n];
         const int32_t cnt = c0[n + 1] - first;
-        for (int32_t c = 0; c < cnt; ++c) {
-            int32_t *e = tab + 4 * (int64_t)(first + c);
+        for (int32_t c = lane; c < cnt; c += 32) {
             const int64_t rem = len - (int64_t)c * kChunk;
-            e[0] = (int32_t)n;
-            e[1] = (int32_t)(a + (int64_t)c * kChunk);
-            e[2] = (int32_t)(rem < kChunk ? rem : kChunk);
-            e[3] = c;
+            *reinterpret_cast<int4 *>(tab + 4 * (int64_t)(first + c)) =
+                make_int4((int32_t)n, (int32_t)(a + (int64_t)c * kChunk),
+                          (int32_t)(rem < kChunk ? rem : kChunk), c);
         }
     }
 }

@@ -206,10 +206,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
         scale_rows_in_place(sm + 8192, sGam, p.scale, tid - 64, kThreads - 64);
     fence_async_smem();
     __syncthreads();
-    if (tid == 0) {
-        bulk_store(img + kImgWQ + 8192, sm + 8192, 8192u);
-        bulk_store(img + kImgWQ + 24576, sm + 24576, 8192u);
-        bulk_store(img + kImgP, sm + kOffStP, 8192u);
+    if (lane_id == 0 && warp >= 5) {  // Q~ blocks and P^T, one copy per warp
+        if (warp == 5) bulk_store(img + kImgWQ + 8192, sm + 8192, 8192u);
+        else if (warp == 6) bulk_store(img + kImgWQ + 24576, sm + 24576, 8192u);
+        else bulk_store(img + kImgP, sm + kOffStP, 8192u);
         bulk_commit();
     }
     invert_merge(sA, sT, sX, tid);
@@ -264,17 +264,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
     scale_rows_in_place(sm, sDec, 1.f, tid, kThreads);
     fence_async_smem();
     __syncthreads();
-    if (tid == 0) {
-        bulk_store(img + kImgWQ, sm + kOffStW, 8192u);
-        bulk_store(img + kImgWQ + 16384, sm + kOffStW + 8192, 8192u);
-        bulk_store(img + kImgK, sm, 8192u);
-        bulk_store(img + kImgK + 8192, sm + 16384, 8192u);
-        bulk_store(img + kImgU, sm + kOffStU, 16384u);
-        bulk_store(img + kImgVec, vec + 384, 16u);  // G_last, e^{G_last}
+    // one copy per warp (lane 0), so the six are issued side by side
+    if (lane_id == 0 && warp < 6) {
+        switch (warp) {
+        case 0: bulk_store(img + kImgWQ, sm + kOffStW, 8192u); break;
+        case 1: bulk_store(img + kImgWQ + 16384, sm + kOffStW + 8192, 8192u); break;
+        case 2: bulk_store(img + kImgK, sm, 8192u); break;
+        case 3: bulk_store(img + kImgK + 8192, sm + 16384, 8192u); break;
+        case 4: bulk_store(img + kImgU, sm + kOffStU, 16384u); break;
+        default: bulk_store(img + kImgVec, vec + 384, 16u); break;  // G_last, e^{G_last}
+        }
         bulk_commit();
     }
 done:
-    if (tid == 0) bulk_wait_read();
+    if (lane_id == 0) bulk_wait_read();  // every issuing thread, its own copies
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
