@@ -185,7 +185,7 @@ def counts(x, n_segments=1):
                 seq_heads=len(lens) * H, n_seqs=len(lens), chunks=chunks, segments=segs * H)
 
 
-REC_BYTES = 73744  # bytes of one record written by tc_prep and read by the scan
+REC_BYTES = 57616  # bytes of one record written by tc_prep and read by the scan (k aside)
 
 
 def algorithmic_bytes(kernel, x, c):
@@ -198,8 +198,8 @@ def algorithmic_bytes(kernel, x, c):
         # whole forward pass: q, k, v, g, beta read once, o written once,
         # h0 / ht once
         return th * ((2 * K + V) * es + 4 + (4 if delta else 0) + V * es) + states
-    if kernel == "tc_chain_serial":  # the records read, o written, states
-        return th * V * es + ch * REC_BYTES + states
+    if kernel == "tc_chain_serial":  # the records and k read, o written, states
+        return th * (K + V) * es + ch * REC_BYTES + states
     if kernel == "tc_gla_prescan":  # k, v, g read; c_s written
         return th * ((K + V) * es + 4) + c["segments"] * K * V * 4
     if kernel == "tc_gla_segment_out":  # q, k, v, g read, o written, h_s read
@@ -211,10 +211,10 @@ def algorithmic_bytes(kernel, x, c):
     rec = ch * REC_BYTES  # per-chunk records of the tensor-core prep kernel
     if kernel == "tc_prep":  # q, k, v, g, beta read; records written
         return th * ((2 * K + V) * es + 8) + rec
-    if kernel == "tc_chain_prescan":  # W, K~, U^T of the records (once); c_s and M_s written
-        return ch * 3 * 16384 + c["segments"] * K * (K + V) * 4
-    if kernel == "tc_chain_segment_out":  # records read, o written, h_s read
-        return th * V * es + rec + c["segments"] * K * V * 4
+    if kernel == "tc_chain_prescan":  # W, U^T, decay of the records and k (once); c_s, M_s
+        return th * K * es + ch * (2 * 16384 + 272) + c["segments"] * K * (K + V) * 4
+    if kernel == "tc_chain_segment_out":  # records and k read, o written, h_s read
+        return th * (K + V) * es + rec + c["segments"] * K * V * 4
     if kernel == "simt_prep":
         b = th * 4 + ch * 64 * 4
         if delta:

@@ -14,19 +14,22 @@
 //                                       state in TMEM, pre-scaled)
 //   O += v_new^T (scale P)^T            (tcgen05 onto the same columns)
 //
-// with K~ = diag(e^{G_last - G}) K and Q~ = scale diag(e^G) Q formed by the
-// prep kernel, so O is the output (one rounding to BF16).  The formulation is
+// with Q~ = scale diag(e^G) Q formed by the prep kernel (so O is the output,
+// one rounding to BF16) and K~ = diag(e^{G_last - G}) K formed here, in
+// place in the stage.  The formulation is
 // the transposed one (value columns are TMEM lanes), so every MMA has M =
 // 128.  The warps specialise:
 //   warps 0-3  the state path, which is the serial dependency: per chunk the
 //              BF16 mirror of h^T (and h^T scaled by e^{G_last} in place),
 //              then v_new^T once the first product lands;
-//   warps 4-7  the output path: each chunk's O, staged and stored (a TMA
-//              store for whole chunks);
+//   warps 4-7  the side path: K~ in place once a chunk lands, then the
+//              previous chunk's O, staged and stored (a TMA store for whole
+//              chunks);
 //   warp 8     control: issues every MMA;
 //   warp 9     producer: claims chains, decodes them into a small ring that
 //              the other roles read, and loads each chunk's record (the byte
-//              image of a stage) with one bulk copy into a two-stage ring;
+//              image of a stage) with bulk copies, and its k tile by TMA,
+//              into a two-stage ring;
 //              the next chunk, also of the next chain, loads while this one
 //              runs.
 // Roles hand over through mbarriers; the first product's TMEM buffer is
@@ -53,16 +56,18 @@ enum TcMode { kModeSerial = 0, kModePre = 1, kModeSegOut = 2 };
 struct TcArgs {
     Problem p;
     Workspace ws;
+    CUtensorMap tk;  // k, loaded into the stage for K~
     CUtensorMap to;  // the output o, for TMA stores of whole chunks
 };
 
-constexpr int kThreads = 320;  // warps 0-3 state, 4-7 output, 8 control, 9 producer
+constexpr int kThreads = 320;  // warps 0-3 state, 4-7 side, 8 control, 9 producer
 constexpr int kRing = 3;       // decoded chains handed out ahead (bounds the look-ahead)
 
 // Shared memory (bytes from a 1024-aligned base).  One stage holds one
 // record image (layout in tc_chunk.cuh):
 //   [Wb0|Q~b0|Wb1|Q~b1] 32 KB: B operand [W; Q~] (K-major, N = 128 rows)
-//   [K~b0|K~b1] 16 KB: B operand of the update (MN-major, N = 128)
+//   [K~b0|K~b1] 16 KB: B operand of the update (MN-major, N = 128), k as
+//                      loaded, scaled in place
 //   scale P^T 8 KB: B operand of O (MN-major, N = 64); U^T 16 KB; vectors.
 constexpr uint32_t kStage = kRecBytes;
 constexpr uint32_t kOffHm = 2 * kStage;        // h^T mirror, K-major, 32 KB
@@ -70,18 +75,19 @@ constexpr uint32_t kOffVn = kOffHm + 32768;    // v_new^T tile, 16 KB
 constexpr uint32_t kOffOs = kOffVn + 16384;    // output staging, 16 KB
 constexpr uint32_t kOffRing = kOffOs + 16384;  // decoded chains
 enum : int {
-    kBFull = 0,     // [2] stage landed (bulk-copy bytes)
+    kBFull = 0,     // [2] stage landed (bulk-copy and TMA bytes)
     kBMready = 2,   // mirror written (state path, 128)
     kBAdone = 3,    // [h^T W^T | O] done (commit)
     kBVready = 4,   // v_new tile written, state scaled (state path, 128)
     kBHdone = 5,    // state update done (commit)
     kBO2 = 6,       // [2] O complete (commit)
-    kBOfree = 8,    // [2] O buffer read (output path, 128)
+    kBOfree = 8,    // [2] O buffer read (side path, 128)
     kBDrain = 10,   // every issued MMA done (commit, at the end)
     kBFree = 11,    // [2] every product reading the stage done (commit)
-    kBCfull = 13,   // [kRing] chain posted (producer)
-    kBCempty = 13 + kRing,  // [kRing] chain read (state, output paths and control: 257)
-    kNumBars = 13 + 2 * kRing
+    kBKready = 13,  // [2] K~ formed in the stage (side path, 128)
+    kBCfull = 15,   // [kRing] chain posted (producer)
+    kBCempty = 15 + kRing,  // [kRing] chain read (state, side paths and control: 257)
+    kNumBars = 15 + 2 * kRing
 };
 
 // One chain of the work list, decoded: (sequence n, segment s, head h[,
@@ -105,7 +111,7 @@ constexpr uint32_t kIdescA64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescH = idesc_bf16(128, 128, 0, 1);
 constexpr uint32_t kIdescO2 = idesc_bf16(128, 64, 0, 1);
 
-// Named barrier of the output path's 128 threads; side_all also ANDs a flag
+// Named barrier of the side path's 128 threads; side_all also ANDs a flag
 // across them, so that all of them take the same branch after a wait.
 __device__ __forceinline__ void side_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 __device__ __forceinline__ bool side_all(bool ok) {
@@ -160,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) {
             uint32_t cnt = 1;
-            if (b == kBMready || b == kBVready || b == kBOfree || b == kBOfree + 1)
+            if (b == kBMready || b == kBVready || b == kBOfree || b == kBOfree + 1 ||
+                b == kBKready || b == kBKready + 1)
                 cnt = 128;
             if (b >= kBCempty) cnt = 257;
             mbar_init(&bars[b], cnt);
@@ -233,17 +240,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                     const uint8_t *rec = ws.rec + rid * kRecBytes;
                     uint64_t *bar = &bars[kBFull + stage];
                     uint8_t *dst = sm + stage * kStage;
-                    if (kOut) {  // the whole image
+                    const int tt = (int)(c.tstart + (int64_t)kChunk * cc);
+                    if (kOut) {  // the image (but K~) and the k tile
                         mbar_arrive_expect_tx(bar, kImgBytes);
-                        bulk_load(dst, rec, kImgBytes, bar);
-                    } else {     // W, K~, U^T (not for the transition), vectors
-                        const uint32_t bytes = 16384u + 16384u + 16u + (c.trans ? 0u : 16384u);
+                        bulk_load(dst, rec, kImgK, bar);
+                        tma_load_3d(dst + kImgK, &args.tk, bar, 0, c.h, tt);
+                        tma_load_3d(dst + kImgK + 8192, &args.tk, bar, 64, c.h, tt);
+                        bulk_load(dst + kImgP, rec + kImgP, kImgBytes - kImgP, bar);
+                    } else {     // W, k, U^T (not for the transition), vectors
+                        const uint32_t bytes = 16384u + 16384u + (kImgBytes - kImgVec) +
+                                               (c.trans ? 0u : 16384u);
                         mbar_arrive_expect_tx(bar, bytes);
                         bulk_load(dst + kImgWQ, rec + kImgWQ, 8192u, bar);
                         bulk_load(dst + kImgWQ + 16384, rec + kImgWQ + 16384, 8192u, bar);
-                        bulk_load(dst + kImgK, rec + kImgK, 16384u, bar);
+                        tma_load_3d(dst + kImgK, &args.tk, bar, 0, c.h, tt);
+                        tma_load_3d(dst + kImgK + 8192, &args.tk, bar, 64, c.h, tt);
                         if (!c.trans) bulk_load(dst + kImgU, rec + kImgU, 16384u, bar);
-                        bulk_load(dst + kImgVec, rec + kImgVec, 16u, bar);
+                        bulk_load(dst + kImgVec, rec + kImgVec, kImgBytes - kImgVec, bar);
                     }
                 }
                 if (!ok) break;
@@ -276,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                                   kOut ? kIdescA128 : kIdescA64, kk > 0);
                     }
                     umma_commit(&bars[kBAdone]);
-                    if (!wait(kBVready, gk)) {
+                    if (!wait(kBVready, gk) || !wait(kBKready + b, gk >> 1)) {
                         ok = false;
                         break;
                     }
@@ -431,10 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
             }
         }
     } else {
-        // ------------------------------------------------------------ output path
+        // ------------------------------------------------------------ side path
         const int tb = tid - 128;
         int k = 0, gk = 0;
-        bool ok = true, stores = false;
+        bool ok = true, stores = false, pending = false;
         int64_t p_t0 = 0;
         int p_len = 0, p_h = 0, p_gk = 0;
         uint8_t *os = sm + kOffOs;  // [t][v] as two swizzled 64-column blocks
@@ -442,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
         auto out_epilogue = [&]() -> bool {
             const int b = p_gk & 1;
             if (tb == 0 && stores) bulk_wait_read();  // the staging tile is free again
-            // all output-path threads agree (and the staging tile's previous
+            // all side-path threads agree (and the staging tile's previous
             // contents are stored) before any of them goes on
             if (!side_all(wait(kBO2 + b, p_gk >> 1))) return false;
             tc_fence_after();
@@ -490,15 +503,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
         while (ok) {
             ChainDesc C;
             if (!take(k++, C) || !C.valid) break;
-            for (int cc = C.s0; kOut && cc < C.s1; ++cc, ++gk) {
+            for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
+                const int b = gk & 1;
+                uint8_t *st = sm + b * kStage;
                 const int64_t rem = C.tlen - (int64_t)kChunk * cc;
+                const int len = rem < kChunk ? (int)rem : kChunk;
+                if (!wait(kBFull + b, gk >> 1)) { ok = false; break; }
+                // K~ = diag(e^{G_last - G}) K in place; rows past the sequence
+                // end (they belong to the next one) become zero.
+                const float *dec = reinterpret_cast<const float *>(st + kImgDec);
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int c = tb + 128 * r;
+                    const int t = c >> 4;
+                    uint8_t *ptr = st + kImgK + ((c >> 3) & 1) * 8192 + t * 128 + (c & 7) * 16;
+                    if (t < len) {
+                        float x[8];
+                        ld_bf16x8(ptr, x);
+                        const float d = dec[t];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) x[u] *= d;
+                        st_bf16x8(ptr, x);
+                    } else {
+                        st_shared_v4(ptr, 0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_async_smem();
+                mbar_arrive(&bars[kBKready + b]);
+                // then the output of the chunk before, whose products are done
+                // or close to it
+                if (kOut && pending && !out_epilogue()) { ok = false; break; }
+                pending = kOut;
                 p_t0 = C.tstart + (int64_t)kChunk * cc;
-                p_len = rem < kChunk ? (int)rem : kChunk;
+                p_len = len;
                 p_h = C.h;
                 p_gk = gk;
-                if (!out_epilogue()) { ok = false; break; }
             }
         }
+        if (ok && pending) out_epilogue();
         if (tb == 0 && stores) bulk_wait_read();
     }
     tc_fence_before();
@@ -530,7 +572,8 @@ cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream
     args.ws = ws;
     const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
     const uint64_t H = (uint64_t)p.H;
-    if (!make_tmap_bf16_3d(&args.to, p.o, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
+    if (!make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.to, p.o, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     const int S = mode == 0 ? 1 : ws.n_segments;
     const int64_t chains = p.N * S * p.H * (mode == 1 ? 2 : 1);

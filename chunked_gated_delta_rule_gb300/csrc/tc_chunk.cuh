@@ -11,22 +11,24 @@ namespace tc {
 constexpr int kD = 128;  // K = V = 128 on the tensor-core path
 
 // One record per (chunk, head): the byte image of the scan kernel's
-// shared-memory stage, so that one bulk copy loads it.  BF16 tiles of 64
+// shared-memory stage, so that bulk copies load it.  BF16 tiles of 64
 // columns in the 128-byte swizzled layout (sw128_off, 64 rows per 8 KB
 // block unless noted):
 //   [0, 32 KB)      W block 0 | Q~ block 0 | W block 1 | Q~ block 1: row t of
 //                   W block b holds W[t][64 b .. 64 b + 63] (K-major), row t
 //                   of Q~ block b holds Q~[t][64 b ..], Q~ = scale e^{G_t} q_t
-//   [32 KB, 48 KB)  K~ block 0 | K~ block 1, K~ = e^{G_last - G_t} k_t
-//                   (rows t, keys: the MN-major B operand of the update)
+//   [32 KB, 48 KB)  not written: the scan kernel loads k there and forms
+//                   K~ = e^{G_last - G_t} k_t in place
 //   [48 KB, 56 KB)  P^T: row j holds scale P[i][j] for i = 0..63, where
 //                   P = (Q K^T * e^{G_i - G_j}, j <= i)
 //   [56 KB, 72 KB)  U^T, 128 rows: row v holds U[t][v] for t = 0..63
-//   [72 KB, +16 B)  FP32 G_last, e^{G_last}, two unused floats
-// Padded tokens (past a sequence end) have zero W, Q~, K~, U and P entries:
-// every later product with them adds exact zeros.
+//   [72 KB, +272 B) FP32 G_last, e^{G_last}, two unused floats, then
+//                   e^{G_last - G_t} for t = 0..63
+// Padded tokens (past a sequence end) have zero W, Q~, U and P entries and
+// zero decay: every later product with them adds exact zeros.
 constexpr uint32_t kImgWQ = 0, kImgK = 32768, kImgP = 49152, kImgU = 57344, kImgVec = 73728;
-constexpr uint32_t kImgBytes = kImgVec + 16;    // bytes written and loaded per record
+constexpr uint32_t kImgDec = kImgVec + 16;      // the 64 decay factors
+constexpr uint32_t kImgBytes = kImgDec + 256;   // bytes of one stage image (74,000)
 constexpr uint32_t kRecBytes = 74752;           // record stride (1 KB aligned); gdr_api.cu sizes it
 constexpr int kImgGamLast = 1;                  // float index of e^{G_last} at kImgVec
 

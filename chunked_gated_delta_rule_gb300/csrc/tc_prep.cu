@@ -1,18 +1,21 @@
 // tc_prep.cu -- A2-A5 on the tensor-core path (BF16, K = V = 128, delta rule):
 // everything of the chunked form that does not depend on the state, for
-// every (chunk, head) in parallel (one CTA each, two CTAs per SM):
+// every (chunk, head) in parallel.  Persistent CTAs (two per SM) walk the
+// (chunk, head) items; per item:
 //
 //   G (gate cumsum), D1 = [K; Q] K^T on tcgen05 (rows 0-63 K K^T, rows 64-127
 //   Q K^T), A_ij = beta_i e^{G_i - G_j} (k_i . k_j) for i > j, T = (I + A)^-1
 //   (tc_inverse.cuh), W^T = K^T (T diag(beta e^G))^T and U^T = V^T
 //   (T diag(beta))^T on tcgen05, P = (Q K^T) * e^{G_i - G_j} for j <= i.
 //
-// The results, with K~ = diag(e^{G_last - G}) K and Q~ = scale diag(e^G) Q,
-// go to one record per (chunk, head): the byte image of the scan kernel's
-// shared-memory stage (layout in tc_chunk.cuh), assembled here in shared
-// memory and written by bulk async copies, which the scan kernel
-// (tc_chain.cu) loads back with one bulk copy, so the serial chain only does
-// the state-dependent products.  Chunked form: the project
+// The results, with Q~ = scale diag(e^G) Q, go to one record per (chunk,
+// head): the byte image of the scan kernel's shared-memory stage (layout in
+// tc_chunk.cuh), assembled here in shared memory and written by bulk async
+// copies, which the scan kernel (tc_chain.cu) loads back, so the serial chain
+// only does the state-dependent products.  The next item's table row and
+// gates are loaded early, and its K, Q, V tiles start loading as soon as the
+// current item's last product has consumed them, while the current item's
+// results are still being staged and written.  Chunked form: the project
 // statement; the WY/UT preparation ahead of fla's state-scan kernel
 // chunk_gated_delta_rule_fwd_kernel_h_blockdim64 (Kev PR #259 intro).
 #include "gdr_internal.cuh"
@@ -34,20 +37,21 @@ struct PrepArgs {
 constexpr int kThreads = 256;
 
 // Shared memory (bytes from a 1024-aligned base).
-// [0, 48 KB): the K, Q, V tiles [Kb0|Qb0|Kb1|Qb1|Vb0|Vb1].  Q~ and K~ are
-// formed in place (once the products reading Q and K are done); W is
-// staged over Vb0|Vb1 and U^T over sA, both after the last product.
-constexpr uint32_t kOffStW = 32768;
+// [0, 48 KB): the K, Q, V tiles [Kb0|Qb0|Kb1|Qb1|Vb0|Vb1]; Q~ is formed in
+// place once D1 is done.  After the last product, W is staged over sT and
+// U^T over sA.
 constexpr uint32_t kOffAT = 49152;                      // sA, sT (FP32, ld kInvLd)
 constexpr uint32_t kOffT = kOffAT + 64 * kInvLd * 4;
 constexpr uint32_t kOffBW = kOffAT;                     // B_W, B_U over sA afterwards
 constexpr uint32_t kOffBU = kOffAT + 8192;
 constexpr uint32_t kOffStU = kOffAT;                    // U^T staging, after the last product
+constexpr uint32_t kOffStW = kOffT;                     // W staging, after the last product
 constexpr uint32_t kOffX = kOffAT + 34816;              // inverse scratch
 constexpr uint32_t kOffVec = kOffX + 4 * kInvScratchFloats;  // gate vectors
 constexpr uint32_t kOffBar = kOffVec + 1600;
 constexpr uint32_t kOffStP = (kOffBar + 64 + 1023) / 1024 * 1024;  // P^T staging, 8 KB
 constexpr uint32_t kSmemLaunch = kOffStP + 8192 + 1024;
+static_assert(kOffStW % 1024 == 0 && kOffStU % 1024 == 0, "staging tiles are 1 KB aligned");
 
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColD1 = 0, kColW = 64, kColU = 128;
@@ -78,13 +82,6 @@ __device__ __forceinline__ void scale_rows_in_place(uint8_t *a, const float *f, 
 __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__ PrepArgs args) {
     const Problem &p = args.p;
     const Workspace &ws = args.ws;
-    const int64_t chunk = blockIdx.x;
-    const int h = blockIdx.y;
-    // Both loads in flight together: the table row exists for every
-    // chunk < max_chunks (the grid), its contents only below n_chunks.
-    const int nck = *ws.n_chunks;
-    const int4 e = reinterpret_cast<const int4 *>(ws.chunk_tab)[chunk];
-    if (chunk >= nck) return;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -97,186 +94,223 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
     float *sA = reinterpret_cast<float *>(sm + kOffAT);
     float *sT = reinterpret_cast<float *>(sm + kOffT);
     float *sX = reinterpret_cast<float *>(sm + kOffX);
+    const int4 *tab = reinterpret_cast<const int4 *>(ws.chunk_tab);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
     const int quad = warp & 3, half = warp >> 2;
     const int row = 32 * quad + lane_id;  // TMEM lane = matrix row
     const int H = (int)p.H;
-    const int64_t t0 = e.y;
-    const int len = e.z;
-    uint8_t *img = ws.rec + (chunk * H + h) * (int64_t)kRecBytes;
+    const int64_t n_items = (int64_t)(*ws.n_chunks) * H;
+    int64_t item = blockIdx.x;
+    if (item >= n_items) return;
 
-    float g2[2] = {0.f, 0.f}, b2[2] = {0.f, 0.f};
-    if (warp == 0) {  // A2 inputs (padded tokens: g = beta = 0), loads in flight early
+    // The gates of a chunk-head (padded tokens: g = beta = 0), loaded by warp 0.
+    auto load_gates = [&](const int4 &e, int h, float (&g2)[2], float (&b2)[2]) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int tok = 2 * lane_id + u;
-            if (tok < len) {
-                g2[u] = p.g[(t0 + tok) * H + h];
-                b2[u] = p.beta[(t0 + tok) * H + h];
-            }
+            g2[u] = tok < e.z ? p.g[((int64_t)e.y + tok) * H + h] : 0.f;
+            b2[u] = tok < e.z ? p.beta[((int64_t)e.y + tok) * H + h] : 0.f;
         }
-    }
+    };
+    auto issue_inputs = [&](const int4 &e, int h) {
+        mbar_arrive_expect_tx(&bars[0], 49152u);
+        tma_load_3d(sm + 0, &args.tk, &bars[0], 0, h, e.y);
+        tma_load_3d(sm + 16384, &args.tk, &bars[0], 64, h, e.y);
+        tma_load_3d(sm + 8192, &args.tq, &bars[0], 0, h, e.y);
+        tma_load_3d(sm + 24576, &args.tq, &bars[0], 64, h, e.y);
+        tma_load_3d(sm + 32768, &args.tv, &bars[0], 0, h, e.y);
+        tma_load_3d(sm + 40960, &args.tv, &bars[0], 64, h, e.y);
+    };
+
+    int4 e = tab[item / H];
+    int h = (int)(item % H);
+    float g2[2] = {0.f, 0.f}, b2[2] = {0.f, 0.f};
+    if (warp == 0) load_gates(e, h, g2, b2);
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         mbar_init_fence();
-        mbar_arrive_expect_tx(&bars[0], 49152u);
-        tma_load_3d(sm + 0, &args.tk, &bars[0], 0, h, (int)t0);
-        tma_load_3d(sm + 16384, &args.tk, &bars[0], 64, h, (int)t0);
-        tma_load_3d(sm + 8192, &args.tq, &bars[0], 0, h, (int)t0);
-        tma_load_3d(sm + 24576, &args.tq, &bars[0], 64, h, (int)t0);
-        tma_load_3d(sm + 32768, &args.tv, &bars[0], 0, h, (int)t0);
-        tma_load_3d(sm + 40960, &args.tv, &bars[0], 64, h, (int)t0);
+        issue_inputs(e, h);
     }
     if (warp == 0) {
         tmem_alloc(s_tmem, kTmemCols);
         tmem_relinquish();
-        gate_vectors(vec, g2, b2, len, lane_id);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t lane = (uint32_t)(32 * quad) << 16;
-    bool ok = mbar_wait(&bars[0], 0, p.status);
-    if (__syncthreads_or(!ok)) goto done;
-    if (len < 64) {  // rows past the sequence end belong to the next one: zero them
-        const int rows = 64 - len;
-        for (int idx = tid; idx < rows * 6 * 8; idx += kThreads) {
-            const int r = len + idx / 48, blk = (idx / 8) % 6, c16 = idx & 7;
-            st_shared_v4(sm + blk * 8192 + r * 128 + c16 * 16, 0u, 0u, 0u, 0u);
+
+    for (uint32_t it = 0;; ++it) {
+        const int len = e.z;
+        uint8_t *img = ws.rec + item * (int64_t)kRecBytes;
+        const int64_t nxt = item + gridDim.x;
+        const bool more = nxt < n_items;
+        int4 en = e;
+        int hn = h;
+        float g2n[2] = {0.f, 0.f}, b2n[2] = {0.f, 0.f};
+
+        // The previous item's stores have read their staging tiles; then the
+        // gate vectors of this one.
+        if (lane_id == 0) bulk_wait_read();
+        __syncthreads();
+        if (warp == 0) gate_vectors(vec, g2, b2, len, lane_id);
+        bool ok = mbar_wait(&bars[0], it & 1u, p.status);
+        if (__syncthreads_or(!ok)) break;
+        if (len < 64) {  // rows past the sequence end belong to the next one: zero them
+            const int rows = 64 - len;
+            for (int idx = tid; idx < rows * 6 * 8; idx += kThreads) {
+                const int r = len + idx / 48, blk = (idx / 8) % 6, c16 = idx & 7;
+                st_shared_v4(sm + blk * 8192 + r * 128 + c16 * 16, 0u, 0u, 0u, 0u);
+            }
+            fence_async_smem();
+        }
+        __syncthreads();
+
+        // A3 (+ Q K^T): D1 = [K; Q] K^T
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t a = sb + (kk >> 2) * 16384 + (kk & 3) * 32;
+                umma_bf16(tmem + kColD1, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024),
+                          kIdescKK64, kk > 0);
+            }
+            umma_commit(&bars[1]);
+        }
+        if (more) {  // the next item's table row and gates, in flight early
+            en = tab[nxt / H];
+            hn = (int)(nxt % H);
+            if (warp == 0) load_gates(en, hn, g2n, b2n);
+        }
+        ok = mbar_wait(&bars[1], 0, p.status);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        {
+            float f[32];
+            tmem_load32f(tmem + lane + kColD1 + 32 * half, f);
+            const int i = row & 63;
+            const int j0 = 32 * half;
+            // A rows keep j < i (beta_i folded in); P rows keep j <= i.
+            const int jlim = quad < 2 ? i : i + 1;
+            const float rowf = quad < 2 ? sBeta[i] : 1.f;
+            if (sScal[2] != 0.f) {  // e^{G_i - G_j} = e^{G_i - G_last} e^{G_last - G_j}
+                const float ri = rowf * sEP[i];
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    f[u] = (j0 + u < jlim) ? f[u] * (ri * sDec[j0 + u]) : 0.f;
+            } else {
+                const float gi = sG[i];
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    f[u] = (j0 + u < jlim) ? f[u] * (rowf * __expf(gi - sG[j0 + u])) : 0.f;
+            }
+            if (quad < 2) {  // row i of A (strictly lower), FP32
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    *reinterpret_cast<float4 *>(sA + i * kInvLd + j0 + 4 * c4) =
+                        make_float4(f[4 * c4], f[4 * c4 + 1], f[4 * c4 + 2], f[4 * c4 + 3]);
+            } else {  // column i of scale P^T
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    st_bf16(sm + kOffStP + sw128_off(j0 + u, i, 64), p.scale * f[u]);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+
+        // A4: T = (I + A)^-1.  The diagonal blocks on warps 0-1 while warps 2-7
+        // form Q~ = scale diag(e^G) Q in place (no product reads Q any more).
+        if (tid < 64)
+            invert_diag16(sA, sT, tid);
+        else
+            scale_rows_in_place(sm + 8192, sGam, p.scale, tid - 64, kThreads - 64);
+        fence_async_smem();
+        __syncthreads();
+        if (lane_id == 0 && warp >= 5) {  // Q~ blocks and P^T, one copy per warp
+            if (warp == 5) bulk_store(img + kImgWQ + 8192, sm + 8192, 8192u);
+            else if (warp == 6) bulk_store(img + kImgWQ + 24576, sm + 24576, 8192u);
+            else bulk_store(img + kImgP, sm + kOffStP, 8192u);
+            bulk_commit();
+        }
+        invert_merge(sA, sT, sX, tid);
+
+        // A5 operands: rows of T diag(beta e^G) (rows 0-63) and T diag(beta)
+        // (rows 64-127), BF16, columns [32 half, 32 half + 32).
+        {
+            const int i = row & 63;
+            const float *scale_vec = quad < 2 ? sBG : sBeta;
+            uint8_t *dst = sm + (quad < 2 ? kOffBW : kOffBU);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                const int j0 = 32 * half + 8 * c8;
+                const float4 a0 = *reinterpret_cast<const float4 *>(sT + i * kInvLd + j0);
+                const float4 a1 = *reinterpret_cast<const float4 *>(sT + i * kInvLd + j0 + 4);
+                const float tv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = j0 + u <= i ? tv[u] * scale_vec[j0 + u] : 0.f;
+                st_bf16x8(dst + sw128_off(i, j0, 64), x);
+            }
         }
         fence_async_smem();
-    }
-    __syncthreads();
-
-    // A3 (+ Q K^T): D1 = [K; Q] K^T
-    if (tid == 0) {
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tmem + kColW, sdesc_sw128(sb + kk * 2048, 16384, 1024),
+                          sdesc_sw128(sb + kOffBW + kk * 32, 16, 1024), kIdescMK64, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tmem + kColU, sdesc_sw128(sb + 32768 + kk * 2048, 8192, 1024),
+                          sdesc_sw128(sb + kOffBU + kk * 32, 16, 1024), kIdescMK64, kk > 0);
+            umma_commit(&bars[1]);
+        }
+        ok = mbar_wait(&bars[1], 1, p.status);
+        // K, Q~ and V are free once the products and the Q~ copies have read
+        // them: the next item's tiles start loading now.
+        if (lane_id == 0) bulk_wait_read();
+        if (__syncthreads_or(!ok)) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t a = sb + (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_bf16(tmem + kColD1, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024),
-                      kIdescKK64, kk > 0);
-        }
-        umma_commit(&bars[1]);
-    }
-    ok = mbar_wait(&bars[1], 0, p.status);
-    if (__syncthreads_or(!ok)) goto done;
-    tc_fence_after();
-    {
-        float f[32];
-        tmem_load32f(tmem + lane + kColD1 + 32 * half, f);
-        const int i = row & 63;
-        const int j0 = 32 * half;
-        // A rows keep j < i (beta_i folded in); P rows keep j <= i.
-        const int jlim = quad < 2 ? i : i + 1;
-        const float rowf = quad < 2 ? sBeta[i] : 1.f;
-        if (sScal[2] != 0.f) {  // e^{G_i - G_j} = e^{G_i - G_last} e^{G_last - G_j}
-            const float ri = rowf * sEP[i];
+        if (tid == 0 && more) issue_inputs(en, hn);
+        {  // W (K-major, row t) and U^T (row v), t in [32 half, 32 half + 32), staged
+            float f[32];
+            tmem_load32f(tmem + lane + kColW + 32 * half, f);
+            uint8_t *wblk = sm + kOffStW + (row >> 6) * 8192;
 #pragma unroll
             for (int u = 0; u < 32; ++u)
-                f[u] = (j0 + u < jlim) ? f[u] * (ri * sDec[j0 + u]) : 0.f;
-        } else {
-            const float gi = sG[i];
+                st_bf16(wblk + sw128_off(32 * half + u, row & 63, 64), f[u]);
+            tmem_load32f(tmem + lane + kColU + 32 * half, f);
 #pragma unroll
-            for (int u = 0; u < 32; ++u)
-                f[u] = (j0 + u < jlim) ? f[u] * (rowf * __expf(gi - sG[j0 + u])) : 0.f;
+            for (int c8 = 0; c8 < 4; ++c8)
+                st_bf16x8(sm + kOffStU + sw128_off(row, 32 * half + 8 * c8, 128), f + 8 * c8);
         }
-        if (quad < 2) {  // row i of A (strictly lower), FP32
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-                *reinterpret_cast<float4 *>(sA + i * kInvLd + j0 + 4 * c4) =
-                    make_float4(f[4 * c4], f[4 * c4 + 1], f[4 * c4 + 2], f[4 * c4 + 3]);
-        } else {  // column i of scale P^T
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-                st_bf16(sm + kOffStP + sw128_off(j0 + u, i, 64), p.scale * f[u]);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // one copy per warp (lane 0), so they are issued side by side
+        if (lane_id == 0 && warp < 5) {
+            switch (warp) {
+            case 0: bulk_store(img + kImgWQ, sm + kOffStW, 8192u); break;
+            case 1: bulk_store(img + kImgWQ + 16384, sm + kOffStW + 8192, 8192u); break;
+            case 2: bulk_store(img + kImgU, sm + kOffStU, 16384u); break;
+            case 3: bulk_store(img + kImgVec, vec + 384, 16u); break;  // G_last, e^{G_last}
+            default: bulk_store(img + kImgDec, sDec, 256u); break;     // e^{G_last - G}
+            }
+            bulk_commit();
         }
+        if (!more) break;
+        item = nxt;
+        e = en;
+        h = hn;
+        g2[0] = g2n[0];
+        g2[1] = g2n[1];
+        b2[0] = b2n[0];
+        b2[1] = b2n[1];
     }
-    tc_fence_before();
-    __syncthreads();
-
-    // A4: T = (I + A)^-1.  The diagonal blocks on warps 0-1 while warps 2-7
-    // form Q~ = scale diag(e^G) Q in place (no product reads Q any more).
-    if (tid < 64)
-        invert_diag16(sA, sT, tid);
-    else
-        scale_rows_in_place(sm + 8192, sGam, p.scale, tid - 64, kThreads - 64);
-    fence_async_smem();
-    __syncthreads();
-    if (lane_id == 0 && warp >= 5) {  // Q~ blocks and P^T, one copy per warp
-        if (warp == 5) bulk_store(img + kImgWQ + 8192, sm + 8192, 8192u);
-        else if (warp == 6) bulk_store(img + kImgWQ + 24576, sm + 24576, 8192u);
-        else bulk_store(img + kImgP, sm + kOffStP, 8192u);
-        bulk_commit();
-    }
-    invert_merge(sA, sT, sX, tid);
-
-    // A5 operands: rows of T diag(beta e^G) (rows 0-63) and T diag(beta)
-    // (rows 64-127), BF16, columns [32 half, 32 half + 32).
-    {
-        const int i = row & 63;
-        const float *scale_vec = quad < 2 ? sBG : sBeta;
-        uint8_t *dst = sm + (quad < 2 ? kOffBW : kOffBU);
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-            const int j0 = 32 * half + 8 * c8;
-            const float4 a0 = *reinterpret_cast<const float4 *>(sT + i * kInvLd + j0);
-            const float4 a1 = *reinterpret_cast<const float4 *>(sT + i * kInvLd + j0 + 4);
-            const float tv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            float x[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = j0 + u <= i ? tv[u] * scale_vec[j0 + u] : 0.f;
-            st_bf16x8(dst + sw128_off(i, j0, 64), x);
-        }
-    }
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + kColW, sdesc_sw128(sb + kk * 2048, 16384, 1024),
-                      sdesc_sw128(sb + kOffBW + kk * 32, 16, 1024), kIdescMK64, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + kColU, sdesc_sw128(sb + 32768 + kk * 2048, 8192, 1024),
-                      sdesc_sw128(sb + kOffBU + kk * 32, 16, 1024), kIdescMK64, kk > 0);
-        umma_commit(&bars[1]);
-    }
-    ok = mbar_wait(&bars[1], 1, p.status);
-    if (__syncthreads_or(!ok)) goto done;
-    tc_fence_after();
-    {  // W (K-major, row t) and U^T (row v), t in [32 half, 32 half + 32), staged
-        float f[32];
-        tmem_load32f(tmem + lane + kColW + 32 * half, f);
-        uint8_t *wblk = sm + kOffStW + (row >> 6) * 8192;
-#pragma unroll
-        for (int u = 0; u < 32; ++u) st_bf16(wblk + sw128_off(32 * half + u, row & 63, 64), f[u]);
-        tmem_load32f(tmem + lane + kColU + 32 * half, f);
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8)
-            st_bf16x8(sm + kOffStU + sw128_off(row, 32 * half + 8 * c8, 128), f + 8 * c8);
-    }
-    // K~ = diag(e^{G_last - G}) K in place (the products reading K are done)
-    scale_rows_in_place(sm, sDec, 1.f, tid, kThreads);
-    fence_async_smem();
-    __syncthreads();
-    // one copy per warp (lane 0), so the six are issued side by side
-    if (lane_id == 0 && warp < 6) {
-        switch (warp) {
-        case 0: bulk_store(img + kImgWQ, sm + kOffStW, 8192u); break;
-        case 1: bulk_store(img + kImgWQ + 16384, sm + kOffStW + 8192, 8192u); break;
-        case 2: bulk_store(img + kImgK, sm, 8192u); break;
-        case 3: bulk_store(img + kImgK + 8192, sm + 16384, 8192u); break;
-        case 4: bulk_store(img + kImgU, sm + kOffStU, 16384u); break;
-        default: bulk_store(img + kImgVec, vec + 384, 16u); break;  // G_last, e^{G_last}
-        }
-        bulk_commit();
-    }
-done:
     if (lane_id == 0) bulk_wait_read();  // every issuing thread, its own copies
     tc_fence_before();
     __syncthreads();
@@ -299,8 +333,12 @@ cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st) {
     cudaError_t err = cudaFuncSetAttribute(k_tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemLaunch);
     if (err != cudaSuccess) return err;
-    dim3 grid((unsigned)ws.max_chunks, (unsigned)p.H);
-    k_tc_prep<<<grid, kThreads, kSmemLaunch, st>>>(args);
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t items = ws.max_chunks * p.H;  // an upper bound; the kernel reads the count
+    const int64_t grid = items < 2 * sms ? items : 2 * sms;
+    k_tc_prep<<<(unsigned)grid, kThreads, kSmemLaunch, st>>>(args);
     return cudaGetLastError();
 }
 
