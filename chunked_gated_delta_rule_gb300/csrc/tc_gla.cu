@@ -55,7 +55,7 @@ struct GlaLayout {
 };
 
 struct GlaChain {
-    int64_t n;
+    int64_t n, tstart, tlen;  // the sequence's first token row and length
     int h, s, vt;
     int c_begin, s0, s1;
 };
@@ -86,7 +86,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
     const int S = MODE == kModeSerial ? 1 : ws.n_segments;
     const int total = (int)(p.N * S * H * VT);
     int32_t *counter = ws.n_chunks + 1 + MODE;
-    const int4 *tab = reinterpret_cast<const int4 *>(ws.chunk_tab);
     constexpr int kHalfKeys = KD / 2;
     const int kbase = kHalfKeys * half;
 
@@ -101,6 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
         c.n = ws.seq_order[r];
         c.c_begin = ws.seq_chunk0[c.n];
         const int nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
+        c.tstart = p.cu ? (int64_t)p.cu[c.n] : c.n * p.T;
+        c.tlen = (p.cu ? (int64_t)p.cu[c.n + 1] : (c.n + 1) * p.T) - c.tstart;
         c.s0 = 0;
         c.s1 = nc;
         if (MODE != kModeSerial) {
@@ -124,7 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int b = 0; b < 3; ++b) mbar_init(&bars[b], 1);
+        // the two product barriers count one commit per issuing thread
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], kOut ? 2 : 1);
+        mbar_init(&bars[2], kOut ? 2 : 1);
         mbar_init_fence();
         tma_prefetch_desc(&args.tk);
         tma_prefetch_desc(&args.tq);
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
     const uint32_t lane = (uint32_t)(32 * quad) << 16;
 
     auto issue_tma = [&](const GlaChain &c, int cc) {
-        const int tt = tab[c.c_begin + cc].y;
+        const int tt = (int)(c.tstart + (int64_t)kChunk * cc);
         uint64_t *bar = &bars[0];
         mbar_arrive_expect_tx(bar, L::kInQK + 16384u);
 #pragma unroll
@@ -152,11 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
     float gq[2] = {0.f, 0.f};
     const float bone[2] = {1.f, 1.f};
     auto load_gates = [&](const GlaChain &c, int cc) {
-        const int4 en = tab[c.c_begin + cc];
+        const int64_t t0 = c.tstart + (int64_t)kChunk * cc;
+        const int64_t len = c.tlen - (int64_t)kChunk * cc;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int tok = 2 * lane_id + u;
-            gq[u] = tok < en.z ? p.g[((int64_t)en.y + tok) * H + c.h] : 0.f;
+            gq[u] = tok < len ? p.g[(t0 + tok) * H + c.h] : 0.f;
         }
     };
 
@@ -167,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
     if (cur < total) {
         GlaChain c;
         decode(cur, c);
-        if (tid == 0) issue_tma(c, c.s0);
+        if (tid == 32) issue_tma(c, c.s0);
         if (warp == 0) load_gates(c, c.s0);
     }
     while (cur < total) {
@@ -206,9 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
         float dprod = 1.f;  // product of the chunk decays (pre-scan summary)
 
         for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
-            const int4 e = tab[C.c_begin + cc];
-            const int64_t t0 = e.y;
-            const int len = e.z;
+            const int64_t t0 = C.tstart + (int64_t)kChunk * cc;
+            const int64_t rem = C.tlen - (int64_t)kChunk * cc;
+            const int len = rem < kChunk ? (int)rem : kChunk;
             if (warp == 0) gate_vectors(vec, gq, bone, len, lane_id);
             bool ok = mbar_wait(&bars[0], gk & 1u, p.status);
             if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -225,7 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                 fence_async_smem();
             }
             __syncthreads();
-            if (tid == 0) {  // D1 = [K; Q] K^T and O1 = h_pre^T Q^T
+            // D1 = [K; Q] K^T (thread 0) and O1 = h_pre^T Q^T (thread 128), issued
+            // side by side, each committed by its own thread
+            if (tid == 0) {
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < KD / 16; ++kk) {
@@ -233,16 +240,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                     umma_bf16(tmem + L::kColD1, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024),
                               idesc_bf16(128, 64, 0, 0), kk > 0);
                 }
-                if (kOut) {
+                umma_commit(&bars[1]);
+            }
+            if (kOut && tid == 128) {
+                tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < KD / 16; ++kk)
-                        umma_bf16(tmem + L::kColO1,
-                                  sdesc_sw128(sb + L::kOffHm + (kk >> 2) * 16384 + (kk & 3) * 32,
-                                              16, 1024),
-                                  sdesc_sw128(sb + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32, 16,
-                                              1024),
-                                  idesc_bf16(128, 64, 0, 0), kk > 0);
-                }
+                for (int kk = 0; kk < KD / 16; ++kk)
+                    umma_bf16(tmem + L::kColO1,
+                              sdesc_sw128(sb + L::kOffHm + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
+                                          1024),
+                              sdesc_sw128(sb + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32, 16, 1024),
+                              idesc_bf16(128, 64, 0, 0), kk > 0);
                 umma_commit(&bars[1]);
             }
             {  // state <- e^{G_last} state; (V e^{G_last - G})^T tile, t in [32 half, +32)
@@ -295,21 +303,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
-            if (tid == 0) {  // state += vd^T K ;  O2 = V^T P^T
+            // state += vd^T K (thread 0) and O2 = V^T P^T (thread 128)
+            if (tid == 0) {
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     umma_bf16(tmem + L::kColS, sdesc_sw128(sb + L::kOffVd + kk * 32, 16, 1024),
                               sdesc_sw128(sb + kk * 2048, 16384, 1024), idesc_bf16(128, KD, 0, 1),
                               1u);
-                if (kOut) {
+                umma_commit(&bars[2]);
+            }
+            if (kOut && tid == 128) {
+                tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + L::kColO2,
-                                  sdesc_sw128(sb + L::kInV + kk * 2048, 8192, 1024),
-                                  sdesc_sw128(sb + L::kOffP + kk * 32, 16, 1024),
-                                  idesc_bf16(128, 64, 1, 0), kk > 0);
-                }
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(tmem + L::kColO2, sdesc_sw128(sb + L::kInV + kk * 2048, 8192, 1024),
+                              sdesc_sw128(sb + L::kOffP + kk * 32, 16, 1024),
+                              idesc_bf16(128, 64, 1, 0), kk > 0);
                 umma_commit(&bars[2]);
             }
             ok = mbar_wait(&bars[2], ph2, p.status);
@@ -322,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                 if (here || nxt < total) {
                     const GlaChain &F = here ? C : Cn;
                     const int fcc = here ? cc + 1 : Cn.s0;
-                    if (tid == 0) issue_tma(F, fcc);
+                    if (tid == 32) issue_tma(F, fcc);  // off the MMA issuers' warps
                     if (warp == 0) load_gates(F, fcc);
                 }
             }
