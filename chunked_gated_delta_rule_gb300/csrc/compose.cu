@@ -56,20 +56,28 @@ __global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Wo
         mbar_init_fence();
     }
     __syncthreads();
-    const uint32_t mbytes = (uint32_t)(K * K * 4);
-    if (tid == 0 && nseg > 0) {
-        mbar_arrive_expect_tx(&bars[0], mbytes);
-        bulk_load(sM0, ws.segM + sbase * K * K, mbytes, &bars[0]);
-    }
+    // A transition arrives as 8 bulk copies issued by 8 warps side by side
+    // (one request per SM is far slower than the L2 can serve); the byte
+    // count is announced on the barrier before any copy is issued.
+    const uint32_t mbytes = (uint32_t)(K * K * 4), piece = mbytes / 8;
+    auto load_m = [&](float *buf, int64_t seg, uint64_t *bar) {
+        if ((tid & 31) == 0 && tid < 256) {
+            const int w = tid >> 5;
+            bulk_load(reinterpret_cast<uint8_t *>(buf) + w * piece,
+                      reinterpret_cast<const uint8_t *>(ws.segM + seg * K * K) + w * piece, piece,
+                      bar);
+        }
+    };
+    if (tid == 0 && nseg > 0) mbar_arrive_expect_tx(&bars[0], mbytes);
+    __syncthreads();
+    if (nseg > 0) load_m(sM0, sbase, &bars[0]);
+    if (tid == 0 && nseg > 1) mbar_arrive_expect_tx(&bars[1], mbytes);
+    __syncthreads();
     for (int s = 0; s < nseg; ++s) {
         const float *sM = (s & 1) ? sM1 : sM0;
         const float *cur = (s & 1) ? sH1 : sH0;
         float *nxt = (s & 1) ? sH0 : sH1;
-        if (tid == 0 && s + 1 < nseg) {
-            float *buf = (s & 1) ? sM0 : sM1;
-            mbar_arrive_expect_tx(&bars[(s + 1) & 1], mbytes);
-            bulk_load(buf, ws.segM + (sbase + s + 1) * K * K, mbytes, &bars[(s + 1) & 1]);
-        }
+        if (s + 1 < nseg) load_m((s & 1) ? sM0 : sM1, sbase + s + 1, &bars[(s + 1) & 1]);
         const int64_t hrow = (sbase + s) * K;
         if (ms == 0 && active) {  // h_s, the segment's initial state
 #pragma unroll
@@ -125,6 +133,8 @@ __global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Wo
             }
         }
         fence_async_smem();  // the transition buffer is refilled by the async proxy next
+        // the barrier of the step after next expects its bytes before any copy
+        if (tid == 0 && s + 2 < nseg) mbar_arrive_expect_tx(&bars[s & 1], mbytes);
         __syncthreads();
     }
     if (p.ht) {

@@ -52,17 +52,46 @@ int pick_bv(const gdr_dims &d) {
     return 16;
 }
 
-// Segment count when the caller passes 0: split long sequences until the
-// scan has about two CTAs per SM, at most 16 segments, and only while every
-// segment keeps at least 8 chunks.
-int auto_segments(const gdr_dims &d, int bv) {
+// Segment count when the caller passes 0.
+// Tensor-core path: a cost model fitted to GB300 timings of its kernels.  A
+// chain pass costs t microseconds per chunk and runs its chains in waves of
+// one per SM; a split runs a pre-scan pass (two chains per segment for the
+// delta rule: local state and transition), an ordered composition costing
+// t_step per segment, and an output pass.  The model reproduces the measured
+// best counts (16K x 16 heads: 8; 64K x 8 heads: 16; 64K x 1 head: 32;
+// beta-free K = 256, V = 512, 2 x 8K x 4 heads: 4; the wide varlen batch: 1).
+// CUDA-core path: split until about two CTAs per SM, at most 16 segments,
+// while every segment keeps at least 8 chunks.
+int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     const int64_t nseq = n_seqs(d);
-    const int64_t chunks_per_seq =
-        is_varlen(d) ? (d.N ? (d.T / d.N) / kChunk : 0) : (d.T + kChunk - 1) / kChunk;
-    const int64_t chains = nseq * d.H * (d.V / bv);
-    int S = 1;
-    while (S < 16 && chains * S < 2 * kNumSMs && chunks_per_seq / (2 * S) >= 8) S *= 2;
-    return S;
+    const int64_t cps = is_varlen(d) ? (d.N ? (d.T / d.N + kChunk - 1) / kChunk : 0)
+                                     : (d.T + kChunk - 1) / kChunk;
+    if (path != 2) {
+        const int64_t chains = nseq * d.H * (d.V / bv);
+        int S = 1;
+        while (S < 16 && chains * S < 2 * kNumSMs && cps / (2 * S) >= 8) S *= 2;
+        return S;
+    }
+    const int64_t chains = nseq * d.H * (beta_free ? d.V / 128 : 1);
+    auto waves = [](int64_t c) { return (double)((c + kNumSMs - 1) / kNumSMs); };
+    const double t_serial = beta_free ? 4.7 : 2.4, t_pre = beta_free ? 3.5 : 2.4,
+                 t_out = beta_free ? 4.9 : 2.4;
+    const double state_mb = (double)(nseq * d.H) * (double)(d.K * d.V) * 4.0 / (1 << 20);
+    const double t_step = beta_free ? (0.65 * state_mb > 0.5 ? 0.65 * state_mb : 0.5)
+                                    : (nseq * d.H * (d.V / 8) > kNumSMs ? 4.4 : 2.6);
+    double best = t_serial * (double)cps * waves(chains);
+    int best_s = 1;
+    for (int S = 2; S <= kMaxSegments && S <= cps; S *= 2) {
+        const double per = (double)((cps + S - 1) / S);
+        const double est = per * (t_pre * waves(chains * S * (beta_free ? 1 : 2)) +
+                                  t_out * waves(chains * S)) +
+                           t_step * S;
+        if (est < best) {
+            best = est;
+            best_s = S;
+        }
+    }
+    return best_s;
 }
 
 // Shapes the tensor-core path covers (pointer alignment is checked per call):
@@ -94,7 +123,7 @@ int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_optio
     }
     if (n_segments < 0) return GDR_ERR_INVALID;
     if (n_segments > kMaxSegments) return GDR_ERR_UNSUPPORTED;
-    p.n_segments = n_segments == 0 ? auto_segments(d, p.bv) : n_segments;
+    p.n_segments = n_segments == 0 ? auto_segments(d, beta_free, p.path, p.bv) : n_segments;
     *plan = p;
     return GDR_OK;
 }
