@@ -2,7 +2,7 @@
 // (cuLA PR #127 "Root cause and implementation": the per-segment FP32
 // transition chained by a short ordered pass), FP32 on CUDA cores.
 //
-// Delta rule: one CTA (512 threads, one per SM) owns CC = 8 or 16 value
+// Delta rule: one CTA (512 threads, one per SM) owns CC = 4, 8 or 16 value
 // columns of one (sequence, head) and walks its segments in order.  Each
 // segment's K x K transition (stored transposed, [m][r] = M_s[r][m]) is
 // streamed into shared memory by a 1-D bulk async copy, double-buffered so
@@ -201,12 +201,15 @@ bool compose_mt_supported(const Problem &p) {
     return p.beta != nullptr && p.K <= 128 && p.K % 32 == 0 && p.V % 8 == 0;
 }
 
-// 8 value columns per CTA when that still fits one wave, else 16.
+// The narrowest value tile (4, 8, 16 columns) whose CTAs still fit one wave:
+// a step's time is one CTA's share of the K x K x CC products.
 cudaError_t compose_mt(const Problem &p, const Workspace &ws, cudaStream_t st) {
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (p.V % 16 == 0 && (p.V / 8) * p.N * p.H > sms) return launch_compose<16>(p, ws, st);
+    const int64_t heads = p.N * p.H;
+    if ((p.V / 4) * heads <= sms) return launch_compose<4>(p, ws, st);
+    if (p.V % 16 == 0 && (p.V / 8) * heads > sms) return launch_compose<16>(p, ws, st);
     return launch_compose<8>(p, ws, st);
 }
 

@@ -58,7 +58,7 @@ int pick_bv(const gdr_dims &d) {
 // one per SM; a split runs a pre-scan pass (two chains per segment for the
 // delta rule: local state and transition), an ordered composition costing
 // t_step per segment, and an output pass.  The model reproduces the measured
-// best counts (16K x 16 heads: 8; 64K x 8 heads: 16; 64K x 1 head: 32;
+// best counts (16K x 16 heads: 8; 64K x 8 heads: 16; 64K x 1 head: 64;
 // beta-free K = 256, V = 512, 2 x 8K x 4 heads: 4; the wide varlen batch: 1).
 // CUDA-core path: split until about two CTAs per SM, at most 16 segments,
 // while every segment keeps at least 8 chunks.
@@ -77,8 +77,10 @@ int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     const double t_serial = beta_free ? 4.7 : 2.4, t_pre = beta_free ? 3.5 : 2.4,
                  t_out = beta_free ? 4.9 : 2.4;
     const double state_mb = (double)(nseq * d.H) * (double)(d.K * d.V) * 4.0 / (1 << 20);
+    const int64_t heads = nseq * d.H;  // composition tile: 4, 8 or 16 value columns
     const double t_step = beta_free ? (0.65 * state_mb > 0.5 ? 0.65 * state_mb : 0.5)
-                                    : (nseq * d.H * (d.V / 8) > kNumSMs ? 4.4 : 2.6);
+                          : heads * (d.V / 4) <= kNumSMs ? 1.8
+                          : heads * (d.V / 8) <= kNumSMs ? 2.6 : 4.4;
     double best = t_serial * (double)cps * waves(chains);
     int best_s = 1;
     for (int S = 2; S <= kMaxSegments && S <= cps; S *= 2) {
