@@ -15,7 +15,8 @@ namespace {
 using namespace tc;
 
 // D[128][N] = A[128][Kd] * B[N][Kd]^T with A, B staged by threads into the
-// requested layouts, one tcgen05.mma per 16-wide K step, FP32 in TMEM.
+// requested layouts (a_mn = 2: A in tensor memory, packed two BF16 per
+// column), one tcgen05.mma per 16-wide K step, FP32 in TMEM.
 __global__ void __launch_bounds__(128)
 k_selftest_umma(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__restrict__ B,
                 float *__restrict__ D, int N, int Kd, int a_mn, int b_mn, int32_t *status) {
@@ -28,10 +29,12 @@ k_selftest_umma(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__rest
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, warp = tid >> 5;
 
-    for (int idx = tid; idx < 128 * Kd; idx += 128) {
-        const int m = idx / Kd, k = idx - m * Kd;
-        const uint32_t off = a_mn ? sw128_off(k, m, Kd) : sw128_off(m, k, 128);
-        *reinterpret_cast<__nv_bfloat16 *>(sA + off) = A[idx];
+    if (a_mn != 2) {
+        for (int idx = tid; idx < 128 * Kd; idx += 128) {
+            const int m = idx / Kd, k = idx - m * Kd;
+            const uint32_t off = a_mn ? sw128_off(k, m, Kd) : sw128_off(m, k, 128);
+            *reinterpret_cast<__nv_bfloat16 *>(sA + off) = A[idx];
+        }
     }
     for (int idx = tid; idx < N * Kd; idx += 128) {
         const int n = idx / Kd, k = idx - n * Kd;
@@ -51,20 +54,40 @@ k_selftest_umma(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__rest
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tmem_base;
+    const uint32_t dcol = a_mn == 2 ? 128u : 0u;  // D after A when A is in TMEM
+    if (a_mn == 2) {  // row tid of A, packed, into columns [0, Kd / 2)
+        for (int c0 = 0; c0 < Kd / 2; c0 += 32) {
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const __nv_bfloat16 lo = A[tid * Kd + 2 * (c0 + i)];
+                const __nv_bfloat16 hi = A[tid * Kd + 2 * (c0 + i) + 1];
+                r[i] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+            }
+            tmem_st32(tmem_addr(tbase, 32 * warp, c0), r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
     if (tid == 0) {
-        const uint32_t idesc = idesc_bf16(128, N, a_mn, b_mn);
+        const uint32_t idesc = idesc_bf16(128, N, a_mn == 1, b_mn);
         for (int kk = 0; kk < Kd / 16; ++kk) {
             const int k0 = kk * 16;
-            uint64_t ad, bd;
-            if (!a_mn)
+            uint64_t ad = 0, bd;
+            if (a_mn == 0)
                 ad = sdesc_sw128(smem_u32(sA) + (k0 / 64) * 128 * 128 + (k0 % 64) * 2, 16, 1024);
-            else
+            else if (a_mn == 1)
                 ad = sdesc_sw128(smem_u32(sA) + k0 * 128, Kd * 128, 1024);
             if (!b_mn)
                 bd = sdesc_sw128(smem_u32(sB) + (k0 / 64) * N * 128 + (k0 % 64) * 2, 16, 1024);
             else
                 bd = sdesc_sw128(smem_u32(sB) + k0 * 128, Kd * 128, 1024);
-            umma_bf16(tbase, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            if (a_mn == 2)
+                umma_bf16_ts(tbase + dcol, tbase + (uint32_t)(k0 / 2), bd, idesc, kk > 0 ? 1u : 0u);
+            else
+                umma_bf16(tbase, ad, bd, idesc, kk > 0 ? 1u : 0u);
         }
         umma_commit(&bar);
     }
@@ -74,7 +97,7 @@ k_selftest_umma(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__rest
     if (ok) {
         for (int c0 = 0; c0 < N; c0 += 16) {
             float f[16];
-            tmem_load16f(tmem_addr(tbase, 32 * warp, c0), f);
+            tmem_load16f(tmem_addr(tbase, 32 * warp, dcol + c0), f);
 #pragma unroll
             for (int i = 0; i < 16; ++i) D[tid * N + c0 + i] = f[i];
         }
@@ -167,7 +190,7 @@ extern "C" int gdr_selftest_inverse(const float *A, float *T, gdr_stream_t strea
 extern "C" int gdr_selftest_umma(const void *A, const void *B, float *D, int N, int Kd,
                                  int a_mn, int b_mn, int32_t *status, gdr_stream_t stream) {
     if (!A || !B || !D) return GDR_ERR_INVALID;
-    if ((N != 64 && N != 128) || (Kd != 64 && Kd != 128) || (a_mn & ~1) || (b_mn & ~1))
+    if ((N != 64 && N != 128) || (Kd != 64 && Kd != 128) || a_mn < 0 || a_mn > 2 || (b_mn & ~1))
         return GDR_ERR_INVALID;
     const size_t smem = 1024 + (size_t)(128 + N) * Kd * 2;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

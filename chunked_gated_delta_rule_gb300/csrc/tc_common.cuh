@@ -379,6 +379,20 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B^T over one K-step of 16: A (M = 128 rows on the
+// TMEM lanes, 16 BF16 values of a row packed two per 32-bit column, the
+// lower K index in the low half) read from tensor memory at a_tmem, B from
+// shared memory through its descriptor; issued by a single thread.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every previously issued tcgen05 op of this thread has
 // completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {

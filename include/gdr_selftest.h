@@ -20,8 +20,11 @@ extern "C" {
 
 /* D[128][N] (FP32, row-major) = A[128][Kd] * B[N][Kd]^T with A, B BF16
  * row-major, computed by tcgen05.mma (kind::f16) with A staged K-major
- * (a_mn = 0) or MN-major (a_mn = 1), and B likewise (b_mn), both with the
- * 128-byte swizzle.  N in {64, 128}, Kd in {64, 128}. */
+ * (a_mn = 0) or MN-major (a_mn = 1) in shared memory, or in tensor memory
+ * (a_mn = 2: row m on lane m, two BF16 per 32-bit column, the lower K index
+ * in the low half), and B K-major or MN-major (b_mn) in shared memory, all
+ * shared-memory operands with the 128-byte swizzle.  N in {64, 128}, Kd in
+ * {64, 128}. */
 int gdr_selftest_umma(const void *A, const void *B, float *D, int N, int Kd,
                       int a_mn, int b_mn, int32_t *status, gdr_stream_t stream);
 

@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("N,Kd", [(64, 64), (64, 128), (128, 64), (128, 128)])
-@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1), (2, 0), (2, 1)])
 def test_umma_layouts(N, Kd, a_mn, b_mn):
     pkg.load_library()
     g = torch.Generator(device="cuda").manual_seed(N * 7 + Kd + 3 * a_mn + b_mn)
