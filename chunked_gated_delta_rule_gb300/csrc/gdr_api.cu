@@ -74,8 +74,8 @@ int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     }
     const int64_t chains = nseq * d.H * (beta_free ? d.V / 128 : 1);
     auto waves = [](int64_t c) { return (double)((c + kNumSMs - 1) / kNumSMs); };
-    const double t_serial = beta_free ? 4.7 : 2.4, t_pre = beta_free ? 3.5 : 2.4,
-                 t_out = beta_free ? 4.9 : 2.4;
+    const double t_serial = beta_free ? 3.3 : 2.4, t_pre = beta_free ? 2.0 : 2.4,
+                 t_out = beta_free ? 3.7 : 2.4;
     const double state_mb = (double)(nseq * d.H) * (double)(d.K * d.V) * 4.0 / (1 << 20);
     const int64_t heads = nseq * d.H;  // composition tile: 4, 8 or 16 value columns
     const double t_step = beta_free ? (0.65 * state_mb > 0.5 ? 0.65 * state_mb : 0.5)

@@ -2,24 +2,32 @@
 // scan, S_t = alpha_t S_{t-1} + v_t k_t^T) on the tensor-core path, for BF16
 // q/k/v with K in {128, 256} and V a multiple of 128.
 //
-// Persistent CTAs (one per SM, 256 threads) pull chains -- one (sequence,
-// segment, head, 128-wide value tile) each -- longest sequences first.  Per
-// 64-token chunk, with h^T (value rows x keys) the FP32 state in TMEM:
+// Persistent CTAs (one per SM) pull chains -- one (sequence, segment, head,
+// 128-wide value tile) each -- longest sequences first.  Per 64-token chunk,
+// with h^T (value rows x keys) the FP32 state in TMEM:
 //
 //   D1 = [K; Q] K^T (tcgen05; rows 64-127 are Q K^T),
 //   P = (Q K^T) * e^{G_i - G_j}, j <= i                 (BF16 operand)
-//   O1 = h_pre^T Q^T        (tcgen05, A = BF16 mirror of h^T)
-//   h^T <- e^{G_last} h^T   (in TMEM), then h^T += (V e^{G_last - G})^T K
-//                           (tcgen05, accumulating onto the state)
+//   O1 = h_pre^T Q^T        (tcgen05, A = BF16 mirror of h^T held in TMEM)
+//   h^T <- e^{G_last} h^T (in TMEM), then h^T += (e^{G_last - G} V)^T K
 //   O2 = V^T P^T;  O^T = scale (O1 * e^G + O2)
 //
 // The chunk's transition is the scalar e^{G_last} (the diagonal affine chunk
 // transform of flash-linear-attention issue #23 "Proposed Dataflow"), so the
 // segment pre-scan only emits the local state c_s and the product of the
 // chunk decays; the ordered composition is h_{s+1} = d_s h_s + c_s.
-// Inputs arrive by TMA (128-byte swizzle) into one buffer; the next chunk's
-// load is issued as soon as this chunk's last product has read its tiles.
-// Waits are time-bounded (GDR_ERR_TIMEOUT in the status word on expiry).
+//
+// The warps specialise (as the delta-rule scan in tc_chain.cu):
+//   warps 0-3  state path: the BF16 mirror of h^T into TMEM and h^T scaled
+//              by e^{G_last}, per chunk (the serial dependency);
+//   warps 4-7  side path: (e^{G_last - G} V) into its own tile, P from D1,
+//              then the chunk's output (staged, stored; TMA for whole chunks);
+//   warp 8     control: every tcgen05 MMA;
+//   warp 9     producer: claims and decodes chains, loads K, Q and the value
+//              tile by TMA into a two-stage ring and computes the chunk's gate
+//              vectors (one warp, shuffle scan) beside them.
+// Every wait is time-bounded: on expiry the CTA records GDR_ERR_TIMEOUT in
+// the status word, the other roles leave too, and the CTA exits.
 #include "gdr_internal.cuh"
 #include "tc_chunk.cuh"
 #include "tma_host.cuh"
@@ -34,31 +42,66 @@ enum GlaMode { kModeSerial = 0, kModePre = 1, kModeSegOut = 2 };
 struct GlaArgs {
     Problem p;
     Workspace ws;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
 };
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;  // warps 0-3 state, 4-7 side, 8 control, 9 producer
+constexpr int kRing = 3;       // decoded chains handed out ahead
+
+// One chain of the work list, decoded; valid == 0 ends the list.
+struct GlaDesc {
+    int64_t n, tstart, tlen;  // the sequence's first token row and length
+    int h, s, vt, c_begin, s0, s1, valid, pad;
+};
+static_assert(sizeof(GlaDesc) == 56, "chain descriptor layout");
 
 template <int KD>
 struct GlaLayout {
-    static constexpr uint32_t kKB = KD / 64;               // 64-key blocks
-    static constexpr uint32_t kInQK = kKB * 16384;         // [Kb | Qb] per key block
-    static constexpr uint32_t kInV = kInQK;                // V tile [Vb0 | Vb1]
-    static constexpr uint32_t kOffHm = kInQK + 16384;      // h^T mirror, K-major
-    static constexpr uint32_t kOffVd = kOffHm + kKB * 16384;  // (V e^{G_last-G})^T; output staging
-    static constexpr uint32_t kOffP = kOffVd + 16384;
-    static constexpr uint32_t kOffVec = kOffP + 8192;
-    static constexpr uint32_t kOffBar = kOffVec + 1600;
-    static constexpr uint32_t kSmem = kOffBar + 256 + 1024;
-    // TMEM: state [0, KD), D1, O1, O2
-    static constexpr uint32_t kColS = 0, kColD1 = KD, kColO1 = KD + 64, kColO2 = KD + 128;
+    // one stage: [Kb | Qb] per 64-key block, the value tile [Vb0 | Vb1], the
+    // gate vectors
+    static constexpr uint32_t kKB = KD / 64;
+    static constexpr uint32_t kStV = kKB * 16384;
+    static constexpr uint32_t kStVec = kStV + 16384;
+    static constexpr uint32_t kStage = kStVec + 2048;
+    static constexpr uint32_t kOffVd = 2 * kStage;        // e^{G_last - G} V, V's layout
+    static constexpr uint32_t kOffP = kOffVd + 16384;     // P, K-major
+    static constexpr uint32_t kOffOs = kOffP + 8192;      // output staging
+    static constexpr uint32_t kOffGam = kOffOs + 16384;   // e^G of the chunk (side path copy)
+    static constexpr uint32_t kOffRing = kOffGam + 256;
+    static constexpr uint32_t kOffBar = kOffRing + 64 * kRing;
+    // TMEM: state [0, KD), BF16 mirror, D1 (then O2), O1
+    static constexpr uint32_t kColS = 0, kColM = KD, kColD = KD + KD / 2, kColO = kColD + 64;
 };
 
-struct GlaChain {
-    int64_t n, tstart, tlen;  // the sequence's first token row and length
-    int h, s, vt;
-    int c_begin, s0, s1;
+enum : int {
+    kGFull = 0,     // [2] stage landed: TMA bytes + the gate vectors (2 arrivals)
+    kGD1 = 2,       // D1 done (commit)
+    kGSready = 3,   // mirror written, state scaled (state path, 128)
+    kGVready = 4,   // e^{G_last - G} V written (side path, 128)
+    kGPready = 5,   // P written (side path, 128)
+    kGHdone = 6,    // state update done (commit)
+    kGO2 = 7,       // O2 done (commit)
+    kGOfree = 8,    // O1 / O2 read (side path, 128)
+    kGFree = 9,     // [2] stage free (commit)
+    kGDrain = 11,   // every issued MMA done (commit, at the end)
+    kGCfull = 12,   // [kRing] chain posted (producer)
+    kGCempty = 12 + kRing,  // [kRing] chain read (state, side, control: 257)
+    kGNumBars = 12 + 2 * kRing
 };
+
+__device__ __forceinline__ void side_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool side_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
 
 template <int KD, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ GlaArgs args) {
@@ -71,53 +114,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    float *vec = reinterpret_cast<float *>(sm + L::kOffVec);
-    const float *sG = vec, *sDec = vec + 192, *sGam = vec + 256, *sEP = vec + 320,
-                *sScal = vec + 384;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);  // full, d1o1, ho2
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + L::kOffBar + 64);
-    int *s_ctl = reinterpret_cast<int *>(sm + L::kOffBar + 128);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + L::kOffBar + 8 * kGNumBars);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(sm + L::kOffBar + 8 * kGNumBars + 4);
+    GlaDesc *ring = reinterpret_cast<GlaDesc *>(sm + L::kOffRing);
+    float *s_gam = reinterpret_cast<float *>(sm + L::kOffGam);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
-    const int row = 32 * quad + lane_id;  // TMEM lane = value row of the tile
+    const int row = 32 * (warp & 3) + lane_id;  // TMEM lane = value row of the tile
+    const uint32_t lane = (uint32_t)(32 * (warp & 3)) << 16;
     const int H = (int)p.H, V = (int)p.V;
     const int VT = V / 128;
     const int S = MODE == kModeSerial ? 1 : ws.n_segments;
-    const int total = (int)(p.N * S * H * VT);
-    int32_t *counter = ws.n_chunks + 1 + MODE;
-    constexpr int kHalfKeys = KD / 2;
-    const int kbase = kHalfKeys * half;
 
-    auto decode = [&](int id, GlaChain &c) {
-        int r = id;
-        c.vt = r % VT;
-        r /= VT;
-        c.h = r % H;
-        r /= H;
-        c.s = r % S;
-        r /= S;
-        c.n = ws.seq_order[r];
-        c.c_begin = ws.seq_chunk0[c.n];
-        const int nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
-        c.tstart = p.cu ? (int64_t)p.cu[c.n] : c.n * p.T;
-        c.tlen = (p.cu ? (int64_t)p.cu[c.n + 1] : (c.n + 1) * p.T) - c.tstart;
-        c.s0 = 0;
-        c.s1 = nc;
-        if (MODE != kModeSerial) {
-            const int per = (nc + S - 1) / S;
-            c.s0 = c.s * per;
-            c.s1 = min(nc, c.s0 + per);
-        }
+    auto wait = [&](int b, uint32_t parity) -> bool {
+        return mbar_wait_or_abort(&bars[b], parity & 1u, p.status, s_abort);
     };
-    auto fetch = [&]() -> int {
-        while (true) {
-            const int id = atomicAdd(counter, 1);
-            if (id >= total) return total;
-            GlaChain c;
-            decode(id, c);
-            if (c.s0 < c.s1) return id;
-        }
+    auto take = [&](int k, GlaDesc &c) -> bool {
+        const int slot = k % kRing;
+        if (!wait(kGCfull + slot, (uint32_t)(k / kRing))) return false;
+        c = ring[slot];
+        mbar_arrive(&bars[kGCempty + slot]);
+        return true;
     };
 
     if (warp == 0) {
@@ -125,275 +143,397 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
         tmem_relinquish();
     }
     if (tid == 0) {
-        // the two product barriers count one commit per issuing thread
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], kOut ? 2 : 1);
-        mbar_init(&bars[2], kOut ? 2 : 1);
+        for (int b = 0; b < kGNumBars; ++b) {
+            uint32_t cnt = 1;
+            if (b == kGFull || b == kGFull + 1) cnt = 2;
+            if (b == kGSready || b == kGVready || b == kGPready || b == kGOfree) cnt = 128;
+            if (b >= kGCempty) cnt = 257;
+            mbar_init(&bars[b], cnt);
+        }
+        *s_abort = 0;
         mbar_init_fence();
-        tma_prefetch_desc(&args.tk);
-        tma_prefetch_desc(&args.tq);
-        tma_prefetch_desc(&args.tv);
-        s_ctl[0] = fetch();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t lane = (uint32_t)(32 * quad) << 16;
 
-    auto issue_tma = [&](const GlaChain &c, int cc) {
-        const int tt = (int)(c.tstart + (int64_t)kChunk * cc);
-        uint64_t *bar = &bars[0];
-        mbar_arrive_expect_tx(bar, L::kInQK + 16384u);
-#pragma unroll
-        for (int kb = 0; kb < (int)L::kKB; ++kb) {
-            tma_load_3d(sm + kb * 16384, &args.tk, bar, 64 * kb, c.h, tt);
-            tma_load_3d(sm + kb * 16384 + 8192, &args.tq, bar, 64 * kb, c.h, tt);
-        }
-        tma_load_3d(sm + L::kInV, &args.tv, bar, 128 * c.vt, c.h, tt);
-        tma_load_3d(sm + L::kInV + 8192, &args.tv, bar, 128 * c.vt + 64, c.h, tt);
-    };
-    float gq[2] = {0.f, 0.f};
-    const float bone[2] = {1.f, 1.f};
-    auto load_gates = [&](const GlaChain &c, int cc) {
-        const int64_t t0 = c.tstart + (int64_t)kChunk * cc;
-        const int64_t len = c.tlen - (int64_t)kChunk * cc;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int tok = 2 * lane_id + u;
-            gq[u] = tok < len ? p.g[(t0 + tok) * H + c.h] : 0.f;
-        }
-    };
-
-    int cur = s_ctl[0];
-    uint32_t gk = 0;
-    uint32_t ph1 = 0, ph2 = 0;
-    bool failed = false;
-    if (cur < total) {
-        GlaChain c;
-        decode(cur, c);
-        if (tid == 32) issue_tma(c, c.s0);
-        if (warp == 0) load_gates(c, c.s0);
-    }
-    while (cur < total) {
-        GlaChain C;
-        decode(cur, C);
-        if (tid == 0) s_ctl[1] = fetch();
-        const int h = C.h, v0 = 128 * C.vt;
-        const int64_t seg_base = (C.n * H + h) * (int64_t)S + C.s;
-        // state h^T rows (value v0 + row), keys [kbase, kbase + KD/2), FP32 in TMEM
-#pragma unroll 1
-        for (int q = 0; q < kHalfKeys / 32; ++q) {
-            float hv[32];
-#pragma unroll
-            for (int kk = 0; kk < 32; ++kk) {
-                const int key = kbase + 32 * q + kk;
-                float x = 0.f;
-                if (MODE == kModeSerial) {
-                    if (p.h0) x = p.h0[((C.n * H + h) * KD + key) * (int64_t)V + v0 + row];
-                } else if (MODE == kModeSegOut) {
-                    x = ws.segH[(seg_base * KD + key) * V + v0 + row];
+    if (warp == 9) {
+        // ------------------------------------------------------------ producer
+        const int total = (int)(p.N * S * H * VT);
+        int32_t *counter = ws.n_chunks + 1 + MODE;
+        int issued = 0;
+        bool ok = true;
+        for (int posted = 0; ok; ++posted) {
+            GlaDesc c{};
+            if (lane_id == 0) {  // the next chain with chunks (heads, value tiles fastest)
+                while (true) {
+                    const int id = atomicAdd(counter, 1);
+                    if (id >= total) break;
+                    int r = id;
+                    c.vt = r % VT;
+                    r /= VT;
+                    c.h = r % H;
+                    r /= H;
+                    c.s = r % S;
+                    r /= S;
+                    c.n = ws.seq_order[r];
+                    c.c_begin = ws.seq_chunk0[c.n];
+                    const int nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
+                    c.s0 = 0;
+                    c.s1 = nc;
+                    if (MODE != kModeSerial) {
+                        const int per = (nc + S - 1) / S;
+                        c.s0 = c.s * per;
+                        c.s1 = min(nc, c.s0 + per);
+                    }
+                    if (c.s0 < c.s1) {
+                        c.tstart = p.cu ? (int64_t)p.cu[c.n] : c.n * p.T;
+                        c.tlen = (p.cu ? (int64_t)p.cu[c.n + 1] : (c.n + 1) * p.T) - c.tstart;
+                        c.valid = 1;
+                        break;
+                    }
                 }
-                hv[kk] = x;
+                const int slot = posted % kRing;
+                if (posted >= kRing && !wait(kGCempty + slot, (uint32_t)(posted / kRing - 1))) {
+                    ok = false;
+                } else {
+                    ring[slot] = c;
+                    mbar_arrive(&bars[kGCfull + slot]);
+                }
             }
-            tmem_store32f(tmem + lane + L::kColS + kbase + 32 * q, hv);
+            // the lanes learn the chain through the ring slot
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            __syncwarp();
+            c = ring[posted % kRing];
+            if (!c.valid) break;
+            for (int cc = c.s0; cc < c.s1; ++cc, ++issued) {
+                const int stage = issued & 1;
+                uint64_t *bar = &bars[kGFull + stage];
+                uint8_t *dst = sm + stage * L::kStage;
+                const int64_t t0 = c.tstart + (int64_t)kChunk * cc;
+                const int64_t rem = c.tlen - (int64_t)kChunk * cc;
+                const int len = rem < kChunk ? (int)rem : kChunk;
+                bool free_ok = true;
+                if (lane_id == 0 && issued >= 2)
+                    free_ok = wait(kGFree + stage, (uint32_t)((issued >> 1) - 1));
+                if (!__shfl_sync(0xffffffffu, free_ok ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (lane_id == 0) {
+                    const uint32_t bytes = L::kKB * (kOut ? 16384u : 8192u) + 16384u;
+                    mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8)
-                st_bf16x8(sm + L::kOffHm + sw128_off(row, kbase + 32 * q + 8 * c8, 128),
-                          hv + 8 * c8);
+                    for (int kb = 0; kb < (int)L::kKB; ++kb) {
+                        tma_load_3d(dst + kb * 16384, &args.tk, bar, 64 * kb, c.h, (int)t0);
+                        if (kOut)
+                            tma_load_3d(dst + kb * 16384 + 8192, &args.tq, bar, 64 * kb, c.h,
+                                        (int)t0);
+                    }
+                    tma_load_3d(dst + L::kStV, &args.tv, bar, 128 * c.vt, c.h, (int)t0);
+                    tma_load_3d(dst + L::kStV + 8192, &args.tv, bar, 128 * c.vt + 64, c.h, (int)t0);
+                }
+                // gates of the chunk (padded tokens: g = 0), then their vectors
+                float g2[2];
+                const float one2[2] = {1.f, 1.f};
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int tok = 2 * lane_id + u;
+                    g2[u] = tok < len ? p.g[(t0 + tok) * H + c.h] : 0.f;
+                }
+                gate_vectors(reinterpret_cast<float *>(dst + L::kStVec), g2, one2, len, lane_id);
+                if (lane_id == 0) mbar_arrive(bar);
+            }
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        const int nxt = s_ctl[1];
-        GlaChain Cn;
-        if (nxt < total) decode(nxt, Cn);
-        float dprod = 1.f;  // product of the chunk decays (pre-scan summary)
-
-        for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
-            const int64_t t0 = C.tstart + (int64_t)kChunk * cc;
-            const int64_t rem = C.tlen - (int64_t)kChunk * cc;
-            const int len = rem < kChunk ? (int)rem : kChunk;
-            if (warp == 0) gate_vectors(vec, gq, bone, len, lane_id);
-            bool ok = mbar_wait(&bars[0], gk & 1u, p.status);
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            const float gam_last = sScal[1];
-            const bool fact = sScal[2] != 0.f;
-            dprod *= gam_last;
-            if (len < 64) {  // rows past the sequence end belong to the next one: zero them
-                const int rows = 64 - len;
-                const int nblk = 2 * (int)L::kKB + 2;
-                for (int idx = tid; idx < rows * nblk * 8; idx += kThreads) {
-                    const int r = len + idx / (nblk * 8), blk = (idx / 8) % nblk, c16 = idx & 7;
-                    st_shared_v4(sm + blk * 8192 + r * 128 + c16 * 16, 0u, 0u, 0u, 0u);
+        __syncwarp();
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ control
+        if (lane_id == 0) {
+            int k = 0, gk = 0;
+            bool ok = true;
+            while (ok) {
+                GlaDesc C;
+                if (!take(k++, C) || !C.valid) break;
+                for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
+                    const int b = gk & 1;
+                    const uint32_t sta = sb + b * L::kStage;
+                    if (!wait(kGFull + b, gk >> 1) || (kOut && gk > 0 && !wait(kGOfree, gk - 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (kOut) {  // D1 = [K; Q] K^T
+#pragma unroll
+                        for (int kk = 0; kk < KD / 16; ++kk) {
+                            const uint32_t a = sta + (kk >> 2) * 16384 + (kk & 3) * 32;
+                            umma_bf16(tmem + L::kColD, sdesc_sw128(a, 16, 1024),
+                                      sdesc_sw128(a, 16, 1024), idesc_bf16(128, 64, 0, 0), kk > 0);
+                        }
+                        umma_commit(&bars[kGD1]);
+                    }
+                    if (!wait(kGSready, gk)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (kOut) {  // O1 = h_pre^T Q^T, A = the BF16 mirror in TMEM
+#pragma unroll
+                        for (int kk = 0; kk < KD / 16; ++kk)
+                            umma_bf16_ts(tmem + L::kColO, tmem + L::kColM + 8 * kk,
+                                         sdesc_sw128(sta + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32,
+                                                     16, 1024),
+                                         idesc_bf16(128, 64, 0, 0), kk > 0);
+                    }
+                    if (!wait(kGVready, gk)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // h^T += (e^{G_last - G} V)^T K
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tmem + L::kColS,
+                                  sdesc_sw128(sb + L::kOffVd + kk * 2048, 8192, 1024),
+                                  sdesc_sw128(sta + kk * 2048, 16384, 1024),
+                                  idesc_bf16(128, KD, 1, 1), 1u);
+                    umma_commit(&bars[kGHdone]);
+                    if (kOut) {  // O2 = V^T P^T, over D1 (read by now)
+                        if (!wait(kGPready, gk)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_bf16(tmem + L::kColD,
+                                      sdesc_sw128(sta + L::kStV + kk * 2048, 8192, 1024),
+                                      sdesc_sw128(sb + L::kOffP + kk * 32, 16, 1024),
+                                      idesc_bf16(128, 64, 1, 0), kk > 0);
+                        umma_commit(&bars[kGO2]);
+                    }
+                    umma_commit(&bars[kGFree + b]);
+                }
+            }
+            umma_commit(&bars[kGDrain]);
+            mbar_wait(&bars[kGDrain], 0, p.status, 100000000ull);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ state path
+        int k = 0, gk = 0;
+        bool ok = true;
+        while (ok) {
+            GlaDesc C;
+            if (!take(k++, C) || !C.valid) break;
+            const int h = C.h, v0 = 128 * C.vt;
+            const int64_t seg_base = (C.n * H + h) * (int64_t)S + C.s;
+            float dprod = 1.f;
+            for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
+                const int b = gk & 1;
+                const float *vec = reinterpret_cast<const float *>(sm + b * L::kStage + L::kStVec);
+                if (!wait(kGFull + b, gk >> 1)) { ok = false; break; }
+                tc_fence_after();  // the state written by the previous update
+                const float gam_last = vec[385];
+                dprod *= gam_last;
+                // h_pre -> BF16 mirror (O1's A operand, in TMEM); the FP32 state
+                // scaled by e^{G_last} for the update.
+#pragma unroll 1
+                for (int q = 0; q < KD / 64; ++q) {
+                    uint32_t r0[32], r1[32];
+                    if (cc == C.s0) {  // the chain's initial state, value column v0 + row
+#pragma unroll
+                        for (int kk = 0; kk < 64; ++kk) {
+                            const int key = 64 * q + kk;
+                            float x = 0.f;
+                            if (MODE == kModeSerial) {
+                                if (p.h0) x = p.h0[((C.n * H + h) * KD + key) * (int64_t)V + v0 + row];
+                            } else if (MODE == kModeSegOut) {
+                                x = ws.segH[(seg_base * KD + key) * V + v0 + row];
+                            }
+                            if (kk < 32) r0[kk] = __float_as_uint(x);
+                            else r1[kk - 32] = __float_as_uint(x);
+                        }
+                    } else {
+                        tmem_ld32(tmem + lane + L::kColS + 64 * q, r0);
+                        tmem_ld32(tmem + lane + L::kColS + 64 * q + 32, r1);
+                        tmem_wait_ld();
+                        reg_fence(r0);
+                        reg_fence(r1);
+                    }
+                    if (kOut) {
+                        uint32_t m[32];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            m[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                            m[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]),
+                                                    __uint_as_float(r1[2 * i + 1]));
+                        }
+                        tmem_st32(tmem + lane + L::kColM + 32 * q, m);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gam_last);
+                        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * gam_last);
+                    }
+                    tmem_st32(tmem + lane + L::kColS + 64 * q, r0);
+                    tmem_st32(tmem + lane + L::kColS + 64 * q + 32, r1);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars[kGSready]);
+                if (!wait(kGHdone, gk)) { ok = false; break; }
+            }
+            if (!ok) break;
+            if (MODE != kModeSegOut && (MODE != kModeSerial || p.ht)) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int q = 0; q < KD / 32; ++q) {
+                    float hv[32];
+                    tmem_load32f(tmem + lane + L::kColS + 32 * q, hv);
+#pragma unroll
+                    for (int kk = 0; kk < 32; ++kk) {
+                        const int key = 32 * q + kk;
+                        if (MODE == kModeSerial)
+                            p.ht[((C.n * H + h) * KD + key) * (int64_t)V + v0 + row] = hv[kk];
+                        else
+                            ws.segC[(seg_base * KD + key) * V + v0 + row] = hv[kk];
+                    }
+                }
+                if (MODE == kModePre && C.vt == 0 && tid == 0) ws.segD[seg_base] = dprod;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ side path
+        const int tb = tid - 128;
+        const int q4 = warp & 3;  // lane quarter: rows 32 q4 .. 32 q4 + 31
+        int k = 0, gk = 0;
+        bool ok = true, stores = false;
+        uint8_t *os = sm + L::kOffOs;  // [t][v] as two swizzled 64-column blocks
+        while (ok) {
+            GlaDesc C;
+            if (!take(k++, C) || !C.valid) break;
+            const int h = C.h, v0 = 128 * C.vt;
+            for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
+                const int b = gk & 1;
+                const uint8_t *st = sm + b * L::kStage;
+                const float *vec = reinterpret_cast<const float *>(st + L::kStVec);
+                const float *sG = vec, *sDec = vec + 192, *sGam = vec + 256, *sEP = vec + 320;
+                const int64_t t0 = C.tstart + (int64_t)kChunk * cc;
+                const int64_t rem = C.tlen - (int64_t)kChunk * cc;
+                const int len = rem < kChunk ? (int)rem : kChunk;
+                if (!wait(kGFull + b, gk >> 1)) { ok = false; break; }
+                // (e^{G_last - G} V) in V's layout; rows past the sequence end
+                // (they belong to the next one) become zero
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int idx = tb + 128 * r;
+                    const int t = (idx >> 3) & 63;
+                    const uint32_t off = (idx >> 9) * 8192 + t * 128 + (idx & 7) * 16;
+                    if (t < len) {
+                        float x[8];
+                        ld_bf16x8(st + L::kStV + off, x);
+                        const float d = sDec[t];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) x[u] *= d;
+                        st_bf16x8(sm + L::kOffVd + off, x);
+                    } else {
+                        st_shared_v4(sm + L::kOffVd + off, 0u, 0u, 0u, 0u);
+                    }
+                }
+                if (kOut && tb < 64) s_gam[tb] = sGam[tb];
+                fence_async_smem();
+                mbar_arrive(&bars[kGVready]);
+                if (!kOut) {
+                    // the tile is read by the update product: the next chunk's
+                    // waits for it (the output below orders this otherwise)
+                    if (!wait(kGHdone, gk)) { ok = false; break; }
+                    continue;
+                }
+                // P from D1 (rows 64-127 of D1 are Q K^T): warps of lane quarters 2, 3
+                if (!side_all(wait(kGD1, gk))) { ok = false; break; }
+                tc_fence_after();
+                if (q4 >= 2) {
+                    const int i = row - 64;
+                    const bool fact = vec[386] != 0.f;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float f[32];
+                        tmem_load32f(tmem + lane + L::kColD + 32 * hh, f);
+                        const int j0 = 32 * hh;
+                        if (fact) {
+                            const float ri = sEP[i];
+#pragma unroll
+                            for (int u = 0; u < 32; ++u)
+                                f[u] = (j0 + u <= i && j0 + u < len) ? f[u] * (ri * sDec[j0 + u]) : 0.f;
+                        } else {
+                            const float gi = sG[i];
+#pragma unroll
+                            for (int u = 0; u < 32; ++u)
+                                f[u] = (j0 + u <= i && j0 + u < len) ? f[u] * __expf(gi - sG[j0 + u])
+                                                                      : 0.f;
+                        }
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8)
+                            st_bf16x8(sm + L::kOffP + sw128_off(i, j0 + 8 * c8, 64), f + 8 * c8);
+                    }
                 }
                 fence_async_smem();
-            }
-            __syncthreads();
-            // D1 = [K; Q] K^T (thread 0) and O1 = h_pre^T Q^T (thread 128), issued
-            // side by side, each committed by its own thread
-            if (tid == 0) {
+                tc_fence_before();
+                mbar_arrive(&bars[kGPready]);
+                // the chunk's output once O2 is done: O^T = scale (O1 * e^G + O2)
+                if (tb == 0 && stores) bulk_wait_read();  // the staging tile is free again
+                if (!side_all(wait(kGO2, gk))) { ok = false; break; }
                 tc_fence_after();
+                uint8_t *col = os + (row >> 6) * 8192;
 #pragma unroll
-                for (int kk = 0; kk < KD / 16; ++kk) {
-                    const uint32_t a = sb + (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_bf16(tmem + L::kColD1, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024),
-                              idesc_bf16(128, 64, 0, 0), kk > 0);
-                }
-                umma_commit(&bars[1]);
-            }
-            if (kOut && tid == 128) {
-                tc_fence_after();
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t o1[32], o2[32];
+                    tmem_ld32(tmem + lane + L::kColO + 32 * hh, o1);
+                    tmem_ld32(tmem + lane + L::kColD + 32 * hh, o2);
+                    tmem_wait_ld();
+                    reg_fence(o1);
+                    reg_fence(o2);
 #pragma unroll
-                for (int kk = 0; kk < KD / 16; ++kk)
-                    umma_bf16(tmem + L::kColO1,
-                              sdesc_sw128(sb + L::kOffHm + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
-                                          1024),
-                              sdesc_sw128(sb + (kk >> 2) * 16384 + 8192 + (kk & 3) * 32, 16, 1024),
-                              idesc_bf16(128, 64, 0, 0), kk > 0);
-                umma_commit(&bars[1]);
-            }
-            {  // state <- e^{G_last} state; (V e^{G_last - G})^T tile, t in [32 half, +32)
-#pragma unroll 1
-                for (int q = 0; q < kHalfKeys / 32; ++q) {
-                    float hv[32];
-                    tmem_load32f(tmem + lane + L::kColS + kbase + 32 * q, hv);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) hv[i] *= gam_last;
-                    tmem_store32f(tmem + lane + L::kColS + kbase + 32 * q, hv);
-                }
-                float vd[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int t = 32 * half + i;
-                    const __nv_bfloat16 x = *reinterpret_cast<const __nv_bfloat16 *>(
-                        sm + L::kInV + sw128_off(t, row, 64));
-                    vd[i] = __bfloat162float(x) * sDec[t];
-                }
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    st_bf16x8(sm + L::kOffVd + sw128_off(row, 32 * half + 8 * c8, 128), vd + 8 * c8);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            ok = mbar_wait(&bars[1], ph1, p.status);
-            ph1 ^= 1;
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            tc_fence_after();
-            if (kOut && quad >= 2) {  // row i of P (lower, diagonal included)
-                float f[32];
-                tmem_load32f(tmem + lane + L::kColD1 + 32 * half, f);
-                const int i = row - 64, j0 = 32 * half;
-                if (fact) {
-                    const float ri = sEP[i];
-#pragma unroll
-                    for (int u = 0; u < 32; ++u)
-                        f[u] = (j0 + u <= i) ? f[u] * (ri * sDec[j0 + u]) : 0.f;
-                } else {
-                    const float gi = sG[i];
-#pragma unroll
-                    for (int u = 0; u < 32; ++u)
-                        f[u] = (j0 + u <= i) ? f[u] * __expf(gi - sG[j0 + u]) : 0.f;
-                }
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    st_bf16x8(sm + L::kOffP + sw128_off(i, j0 + 8 * c8, 64), f + 8 * c8);
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            // state += vd^T K (thread 0) and O2 = V^T P^T (thread 128)
-            if (tid == 0) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tmem + L::kColS, sdesc_sw128(sb + L::kOffVd + kk * 32, 16, 1024),
-                              sdesc_sw128(sb + kk * 2048, 16384, 1024), idesc_bf16(128, KD, 0, 1),
-                              1u);
-                umma_commit(&bars[2]);
-            }
-            if (kOut && tid == 128) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tmem + L::kColO2, sdesc_sw128(sb + L::kInV + kk * 2048, 8192, 1024),
-                              sdesc_sw128(sb + L::kOffP + kk * 32, 16, 1024),
-                              idesc_bf16(128, 64, 1, 0), kk > 0);
-                umma_commit(&bars[2]);
-            }
-            ok = mbar_wait(&bars[2], ph2, p.status);
-            ph2 ^= 1;
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            tc_fence_after();
-            // every product has read this chunk's tiles: load the next chunk now
-            {
-                const bool here = cc + 1 < C.s1;
-                if (here || nxt < total) {
-                    const GlaChain &F = here ? C : Cn;
-                    const int fcc = here ? cc + 1 : Cn.s0;
-                    if (tid == 32) issue_tma(F, fcc);  // off the MMA issuers' warps
-                    if (warp == 0) load_gates(F, fcc);
-                }
-            }
-            // mirror of the updated state
-#pragma unroll 1
-            for (int q = 0; q < kHalfKeys / 32; ++q) {
-                float hv[32];
-                tmem_load32f(tmem + lane + L::kColS + kbase + 32 * q, hv);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    st_bf16x8(sm + L::kOffHm + sw128_off(row, kbase + 32 * q + 8 * c8, 128),
-                              hv + 8 * c8);
-            }
-            if (kOut) {  // output rows, staged over the vd tile
-                uint8_t *stage_o = sm + L::kOffVd;
-                float o1[32], o2[32];
-                tmem_load32f(tmem + lane + L::kColO1 + 32 * half, o1);
-                tmem_load32f(tmem + lane + L::kColO2 + 32 * half, o2);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int t = 32 * half + i;
-                    const float y = p.scale * fmaf(sGam[t], o1[i], o2[i]);
-                    *reinterpret_cast<__nv_bfloat16 *>(stage_o + t * 256 + row * 2) =
-                        __float2bfloat16_rn(y);
+                    for (int u = 0; u < 32; ++u) {
+                        const int t = 32 * hh + u;
+                        const float y = p.scale * fmaf(s_gam[t], __uint_as_float(o1[u]),
+                                                       __uint_as_float(o2[u]));
+                        *reinterpret_cast<__nv_bfloat16 *>(col + sw128_off(t, row & 63, 64)) =
+                            __float2bfloat16_rn(y);
+                    }
                 }
                 tc_fence_before();
-                __syncthreads();
-                __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+                mbar_arrive(&bars[kGOfree]);
+                if (len == kChunk) {
+                    fence_async_smem();
+                    side_sync();
+                    if (tb == 0) {
+                        tma_store_3d(&args.to, os, v0, h, (int)t0);
+                        tma_store_3d(&args.to, os + 8192, v0 + 64, h, (int)t0);
+                        bulk_commit();
+                        stores = true;
+                    }
+                } else {  // a sequence's last chunk: rows past its end belong to the next
+                    side_sync();
+                    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int idx = tid + kThreads * r;
-                    const int t = idx >> 4, c16 = idx & 15;
-                    if (t < len)
-                        *reinterpret_cast<uint4 *>(o + ((t0 + t) * H + h) * (int64_t)V + v0 +
-                                                   c16 * 8) =
-                            *reinterpret_cast<const uint4 *>(stage_o + t * 256 + c16 * 16);
+                    for (int r = 0; r < 8; ++r) {
+                        const int idx = tb + 128 * r;
+                        const int t = idx >> 4, c16 = idx & 15;
+                        if (t < len)
+                            *reinterpret_cast<uint4 *>(o + ((t0 + t) * H + h) * (int64_t)V + v0 +
+                                                       c16 * 8) =
+                                *reinterpret_cast<const uint4 *>(os + (c16 >> 3) * 8192 +
+                                                                 sw128_off(t, (c16 & 7) * 8, 64));
+                    }
                 }
+                // s_gam and the staging tile are reused by the next chunk
+                side_sync();
             }
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
         }
-        if (failed) break;
-        if (MODE != kModeSegOut && (MODE != kModeSerial || p.ht)) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int q = 0; q < kHalfKeys / 32; ++q) {
-                float hv[32];
-                tmem_load32f(tmem + lane + L::kColS + kbase + 32 * q, hv);
-#pragma unroll
-                for (int kk = 0; kk < 32; ++kk) {
-                    const int key = kbase + 32 * q + kk;
-                    if (MODE == kModeSerial)
-                        p.ht[((C.n * H + h) * KD + key) * (int64_t)V + v0 + row] = hv[kk];
-                    else
-                        ws.segC[(seg_base * KD + key) * V + v0 + row] = hv[kk];
-                }
-            }
-            if (MODE == kModePre && C.vt == 0 && tid == 0) ws.segD[seg_base] = dprod;
-        }
-        cur = nxt;
+        if (tb == 0 && stores) bulk_wait_read();
     }
     tc_fence_before();
     __syncthreads();
@@ -402,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
 
 template <int KD, int MODE>
 cudaError_t launch_gla(const GlaArgs &args, unsigned grid, cudaStream_t st) {
-    const int smem = (int)GlaLayout<KD>::kSmem;
+    const int smem = (int)(GlaLayout<KD>::kOffBar + 8 * kGNumBars + 16 + 1024);
     cudaError_t err =
         cudaFuncSetAttribute(k_tc_gla<KD, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
@@ -426,7 +566,8 @@ cudaError_t tc_gla(const Problem &p, const Workspace &ws, int mode, cudaStream_t
     const uint64_t H = (uint64_t)p.H, K = (uint64_t)p.K, V = (uint64_t)p.V;
     if (!make_tmap_bf16_3d(&args.tq, p.q, K, H, rows, K * 2, H * K * 2, 64, 1, 64) ||
         !make_tmap_bf16_3d(&args.tk, p.k, K, H, rows, K * 2, H * K * 2, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&args.tv, p.v, V, H, rows, V * 2, H * V * 2, 64, 1, 64))
+        !make_tmap_bf16_3d(&args.tv, p.v, V, H, rows, V * 2, H * V * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.to, p.o, V, H, rows, V * 2, H * V * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     const int S = mode == 0 ? 1 : ws.n_segments;
     const int64_t chains = p.N * S * p.H * (p.V / 128);
