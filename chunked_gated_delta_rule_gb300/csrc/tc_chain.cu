@@ -68,7 +68,7 @@ constexpr int kRing = 3;       // decoded chains handed out ahead (bounds the lo
 //   [Wb0|Q~b0|Wb1|Q~b1] 32 KB: B operand [W; Q~] (K-major, N = 128 rows)
 //   [K~b0|K~b1] 16 KB: B operand of the update (MN-major, N = 128), k as
 //                      loaded, scaled in place
-//   scale P^T 8 KB: B operand of O (MN-major, N = 64); U^T 16 KB; vectors.
+//   scale P 8 KB: B operand of O (K-major, N = 64); U^T 16 KB; vectors.
 constexpr uint32_t kStage = kRecBytes;
 constexpr uint32_t kOffHm = 2 * kStage;        // h^T mirror, K-major, 32 KB
 constexpr uint32_t kOffVn = kOffHm + 32768;    // v_new^T tile, 16 KB
@@ -109,7 +109,7 @@ constexpr uint32_t kColS = 256;  // FP32 state h^T, 128 columns
 constexpr uint32_t kIdescA128 = idesc_bf16(128, 128, 0, 0);
 constexpr uint32_t kIdescA64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescH = idesc_bf16(128, 128, 0, 1);
-constexpr uint32_t kIdescO2 = idesc_bf16(128, 64, 0, 1);
+constexpr uint32_t kIdescO2 = idesc_bf16(128, 64, 0, 0);
 
 // Named barrier of the side path's 128 threads; side_all also ANDs a flag
 // across them, so that all of them take the same branch after a wait.
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         for (int kk = 0; kk < 4; ++kk)
                             umma_bf16(tmem + kColA + 128 * b + 64,
                                       sdesc_sw128(sb + kOffVn + kk * 32, 16, 1024),
-                                      sdesc_sw128(sta + kImgP + kk * 2048, 8192, 1024), kIdescO2,
+                                      sdesc_sw128(sta + kImgP + kk * 32, 16, 1024), kIdescO2,
                                       1u);
                         umma_commit(&bars[kBO2 + b]);
                     }

@@ -19,7 +19,7 @@ constexpr int kD = 128;  // K = V = 128 on the tensor-core path
 //                   of Q~ block b holds Q~[t][64 b ..], Q~ = scale e^{G_t} q_t
 //   [32 KB, 48 KB)  not written: the scan kernel loads k there and forms
 //                   K~ = e^{G_last - G_t} k_t in place
-//   [48 KB, 56 KB)  P^T: row j holds scale P[i][j] for i = 0..63, where
+//   [48 KB, 56 KB)  scale P: row i holds scale P[i][j] for j = 0..63, where
 //                   P = (Q K^T * e^{G_i - G_j}, j <= i)
 //   [56 KB, 72 KB)  U^T, 128 rows: row v holds U[t][v] for t = 0..63
 //   [72 KB, +272 B) FP32 G_last, e^{G_last}, two unused floats, then

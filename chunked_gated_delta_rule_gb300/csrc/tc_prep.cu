@@ -47,9 +47,9 @@ constexpr uint32_t kOffBU = kOffAT + 8192;
 constexpr uint32_t kOffStU = kOffAT;                    // U^T staging, after the last product
 constexpr uint32_t kOffStW = kOffT;                     // W staging, after the last product
 constexpr uint32_t kOffX = kOffAT + 34816;              // inverse scratch
-constexpr uint32_t kOffVec = kOffX + 4 * kInvScratchFloats;  // gate vectors
-constexpr uint32_t kOffBar = kOffVec + 1600;
-constexpr uint32_t kOffStP = (kOffBar + 64 + 1023) / 1024 * 1024;  // P^T staging, 8 KB
+constexpr uint32_t kOffVec = kOffX + 4 * kInvScratchFloats;  // gate vectors, two items'
+constexpr uint32_t kOffBar = kOffVec + 2 * 1600;
+constexpr uint32_t kOffStP = (kOffBar + 64 + 1023) / 1024 * 1024;  // scale P staging, 8 KB
 constexpr uint32_t kSmemLaunch = kOffStP + 8192 + 1024;
 static_assert(kOffStW % 1024 == 0 && kOffStU % 1024 == 0, "staging tiles are 1 KB aligned");
 
@@ -86,9 +86,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    float *vec = reinterpret_cast<float *>(sm + kOffVec);
-    const float *sG = vec, *sBeta = vec + 64, *sBG = vec + 128, *sDec = vec + 192,
-                *sGam = vec + 256, *sEP = vec + 320, *sScal = vec + 384;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);  // tma, mma
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffBar + 16);
     float *sA = reinterpret_cast<float *>(sm + kOffAT);
@@ -152,10 +149,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
         int hn = h;
         float g2n[2] = {0.f, 0.f}, b2n[2] = {0.f, 0.f};
 
-        // The previous item's stores have read their staging tiles; then the
-        // gate vectors of this one.
-        if (lane_id == 0) bulk_wait_read();
-        __syncthreads();
+        // The gate vectors of this item, in the buffer its predecessor's
+        // copies no longer read (they waited for that before it began).
+        float *vec = reinterpret_cast<float *>(sm + kOffVec + (it & 1) * 1600);
+        const float *sG = vec, *sBeta = vec + 64, *sBG = vec + 128, *sDec = vec + 192,
+                    *sGam = vec + 256, *sEP = vec + 320, *sScal = vec + 384;
         if (warp == 0) gate_vectors(vec, g2, b2, len, lane_id);
         bool ok = mbar_wait(&bars[0], it & 1u, p.status);
         if (__syncthreads_or(!ok)) break;
@@ -186,6 +184,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
             if (warp == 0) load_gates(en, hn, g2n, b2n);
         }
         ok = mbar_wait(&bars[1], 0, p.status);
+        // the previous item's copies have read their staging tiles (sA, sT,
+        // P, its gate vectors) before they are written again
+        if (lane_id == 0) bulk_wait_read();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
         {
@@ -212,10 +213,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
                 for (int c4 = 0; c4 < 8; ++c4)
                     *reinterpret_cast<float4 *>(sA + i * kInvLd + j0 + 4 * c4) =
                         make_float4(f[4 * c4], f[4 * c4 + 1], f[4 * c4 + 2], f[4 * c4 + 3]);
-            } else {  // column i of scale P^T
+            } else {  // row i of scale P
 #pragma unroll
-                for (int u = 0; u < 32; ++u)
-                    st_bf16(sm + kOffStP + sw128_off(j0 + u, i, 64), p.scale * f[u]);
+                for (int u = 0; u < 32; ++u) f[u] *= p.scale;
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8)
+                    st_bf16x8(sm + kOffStP + sw128_off(i, j0 + 8 * c8, 64), f + 8 * c8);
             }
         }
         tc_fence_before();
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
             scale_rows_in_place(sm + 8192, sGam, p.scale, tid - 64, kThreads - 64);
         fence_async_smem();
         __syncthreads();
-        if (lane_id == 0 && warp >= 5) {  // Q~ blocks and P^T, one copy per warp
+        if (lane_id == 0 && warp >= 5) {  // Q~ blocks and scale P, one copy per warp
             if (warp == 5) bulk_store(img + kImgWQ + 8192, sm + 8192, 8192u);
             else if (warp == 6) bulk_store(img + kImgWQ + 24576, sm + 24576, 8192u);
             else bulk_store(img + kImgP, sm + kOffStP, 8192u);
