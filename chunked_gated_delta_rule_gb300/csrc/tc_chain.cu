@@ -214,7 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         c.s0 = c.s * per;
                         c.s1 = min(nc, c.s0 + per);
                     }
-                    if (c.s0 < c.s1) {
+                    // the serial scan also takes a sequence without tokens
+                    // (its final state is its initial one)
+                    if (c.s0 < c.s1 || MODE == kModeSerial) {
                         c.tstart = p.cu ? (int64_t)p.cu[c.n] : c.n * p.T;
                         c.tlen = (p.cu ? (int64_t)p.cu[c.n + 1] : (c.n + 1) * p.T) - c.tstart;
                         c.valid = 1;
@@ -418,6 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 if (!wait(kBHdone, gk)) { ok = false; break; }
             }
             if (!ok) break;
+            if (MODE == kModeSerial && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
+                if (p.ht) {
+                    for (int key = 0; key < kD; ++key) {
+                        const int64_t idx = ((C.n * H + h) * kD + key) * kD + row;
+                        p.ht[idx] = p.h0 ? p.h0[idx] : 0.f;
+                    }
+                }
+                continue;
+            }
             if ((MODE != kModeSegOut) && (MODE != kModeSerial || p.ht)) {
                 tc_fence_after();
 #pragma unroll

@@ -187,7 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                         c.s0 = c.s * per;
                         c.s1 = min(nc, c.s0 + per);
                     }
-                    if (c.s0 < c.s1) {
+                    // the serial scan also takes a sequence without tokens
+                    // (its final state is its initial one)
+                    if (c.s0 < c.s1 || MODE == kModeSerial) {
                         c.tstart = p.cu ? (int64_t)p.cu[c.n] : c.n * p.T;
                         c.tlen = (p.cu ? (int64_t)p.cu[c.n + 1] : (c.n + 1) * p.T) - c.tstart;
                         c.valid = 1;
@@ -386,6 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                 if (!wait(kGHdone, gk)) { ok = false; break; }
             }
             if (!ok) break;
+            if (MODE == kModeSerial && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
+                if (p.ht) {
+                    for (int key = 0; key < KD; ++key) {
+                        const int64_t idx = ((C.n * H + h) * KD + key) * (int64_t)V + v0 + row;
+                        p.ht[idx] = p.h0 ? p.h0[idx] : 0.f;
+                    }
+                }
+                continue;
+            }
             if (MODE != kModeSegOut && (MODE != kModeSerial || p.ht)) {
                 tc_fence_after();
 #pragma unroll 1

@@ -18,9 +18,20 @@ pytestmark = pytest.mark.gpu
 W = synthetic.WORKLOADS
 
 
+def poisoned_outputs(x):
+    """o and ht filled with NaN, so an element the library leaves unwritten
+    fails the comparison (a fresh allocation may hold an earlier result)."""
+    n = x["N"] if x["cu_seqlens"] is not None else x["B"]
+    o = torch.full(x["v"].shape, float("nan"), dtype=x["v"].dtype, device="cuda")
+    ht = torch.full((n, x["H"], x["K"], x["V"]), float("nan"), dtype=torch.float32,
+                    device="cuda")
+    return o, ht
+
+
 def check(x, tol=None, **kw):
     tol = tol or tol_of(x)
-    o, ht = run_gpu(x, **kw)
+    o0, ht0 = poisoned_outputs(x)
+    o, ht = run_gpu(x, o=o0, ht=ht0, **kw)
     ro, rht = run_oracle(x)
     eo, eh = rel_l2_masked(o, ro), rel_l2_masked(ht, rht)
     assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
@@ -56,7 +67,8 @@ def test_bf16_ragged_varlen(S, path):
 def test_bf16_varlen_with_empty_sequences_and_h0(path):
     w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True)
     x = synthetic.make_inputs(w, lengths=[0, 70, 0, 129, 0])
-    o, ht = run_gpu(x, force_path=path)
+    o0, ht0 = poisoned_outputs(x)
+    o, ht = run_gpu(x, force_path=path, o=o0, ht=ht0)
     ro, rht = run_oracle(x)
     assert rel_l2_masked(o, ro) <= TOL_BF16
     assert rel_l2_masked(ht, rht) <= TOL_BF16
@@ -85,6 +97,28 @@ def test_beta_free_k128_v256_varlen(S, path):
     w = synthetic.small(W["gla_k256_v512_bf16"], K=128, V=256, H=3)
     check(synthetic.make_inputs(w, lengths=[1, 64, 65, 200, 0, 130]), n_segments=S,
           force_path=path)
+
+
+def many_lengths(n, hi, seed):
+    """Seeded sequence lengths in [0, hi], zeros included."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(0, hi + 1, (n,), generator=g).tolist()
+
+
+@pytest.mark.parametrize("S", [1, 4])
+def test_many_short_sequences_delta(S):
+    """600 sequences of 0-200 tokens: every persistent CTA walks several
+    chains, the chain hand-over ring wraps many times, most chunks are ragged."""
+    w = synthetic.small(W["wide_varlen_bf16"], H=2)
+    check(synthetic.make_inputs(w, lengths=many_lengths(600, 200, 11)), n_segments=S,
+          force_path=2)
+
+
+@pytest.mark.parametrize("S", [1, 2])
+def test_many_short_sequences_beta_free(S):
+    w = synthetic.small(W["gla_k256_v512_bf16"], K=128, V=256, H=2)
+    check(synthetic.make_inputs(w, lengths=many_lengths(300, 200, 12)), n_segments=S,
+          force_path=2)
 
 
 @pytest.mark.parametrize("path", PATHS)
