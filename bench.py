@@ -211,7 +211,8 @@ def algorithmic_bytes(kernel, x, c):
     rec = ch * REC_BYTES  # per-chunk records of the tensor-core prep kernel
     if kernel == "tc_prep":  # q, k, v, g, beta read; records written
         return th * ((2 * K + V) * es + 8) + rec
-    if kernel == "tc_chain_prescan":  # W, U^T, decay of the records and k (once); c_s, M_s
+    if kernel in ("tc_chain_prescan", "tc_prescan_dual"):
+        # W, U^T, decay of the records and k (once); c_s, M_s
         return th * K * es + ch * (2 * 16384 + 272) + c["segments"] * K * (K + V) * 4
     if kernel == "tc_chain_segment_out":  # records and k read, o written, h_s read
         return th * (K + V) * es + rec + c["segments"] * K * V * 4
@@ -232,6 +233,7 @@ def algorithmic_bytes(kernel, x, c):
 
 # The translation unit each kernel is compiled from (plus every shared header).
 KERNEL_SOURCES = {"tc_prep": "tc_prep.cu", "tc_chain": "tc_chain.cu", "tc_gla": "tc_gla.cu",
+                  "tc_prescan": "tc_prescan.cu",
                   "compose": "compose.cu", "simt": "simt_path.cu"}
 
 

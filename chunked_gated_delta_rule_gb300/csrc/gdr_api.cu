@@ -62,6 +62,10 @@ int pick_bv(const gdr_dims &d) {
 // beta-free K = 256, V = 512, 2 x 8K x 4 heads: 4; the wide varlen batch: 1).
 // CUDA-core path: split until about two CTAs per SM, at most 16 segments,
 // while every segment keeps at least 8 chunks.
+// The delta pre-scan of `segs` (sequence, segment, head) chains runs each of
+// their two summaries as its own chain while all of them fit one wave.
+bool prescan_split_kinds(int64_t segs) { return 2 * segs <= kNumSMs; }
+
 int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     const int64_t nseq = n_seqs(d);
     const int64_t cps = is_varlen(d) ? (d.N ? (d.T / d.N + kChunk - 1) / kChunk : 0)
@@ -76,6 +80,12 @@ int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     auto waves = [](int64_t c) { return (double)((c + kNumSMs - 1) / kNumSMs); };
     const double t_serial = beta_free ? 3.3 : 2.4, t_pre = beta_free ? 2.0 : 2.4,
                  t_out = beta_free ? 3.7 : 2.4;
+    // the delta pre-scan: one summary per CTA while both kinds fit one wave,
+    // else both summaries of a segment per CTA at 2.9 us per chunk
+    auto pre_time = [&](int64_t segs) {
+        if (beta_free) return t_pre * waves(segs);
+        return prescan_split_kinds(segs) ? t_pre : 2.9 * waves(segs);
+    };
     const double state_mb = (double)(nseq * d.H) * (double)(d.K * d.V) * 4.0 / (1 << 20);
     const int64_t heads = nseq * d.H;  // composition tile: 4, 8 or 16 value columns
     const double t_step = beta_free ? (0.65 * state_mb > 0.5 ? 0.65 * state_mb : 0.5)
@@ -85,8 +95,7 @@ int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     int best_s = 1;
     for (int S = 2; S <= kMaxSegments && S <= cps; S *= 2) {
         const double per = (double)((cps + S - 1) / S);
-        const double est = per * (t_pre * waves(chains * S * (beta_free ? 1 : 2)) +
-                                  t_out * waves(chains * S)) +
+        const double est = per * (pre_time(chains * S) + t_out * waves(chains * S)) +
                            t_step * S;
         if (est < best) {
             best = est;
@@ -239,7 +248,10 @@ int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStre
     if (plan.n_segments <= 1) {
         GDR_LAUNCH(rec, kKTcSerial, tc_chain(p, ws, 0, st));
     } else {
-        GDR_LAUNCH(rec, kKTcPre, tc_chain(p, ws, 1, st));
+        if (prescan_split_kinds(p.N * plan.n_segments * p.H))
+            GDR_LAUNCH(rec, kKTcPre, tc_chain(p, ws, 1, st));
+        else
+            GDR_LAUNCH(rec, kKTcPreDual, tc_prescan(p, ws, st));
         GDR_LAUNCH(rec, kKCompose, compose_mt(p, ws, st));
         GDR_LAUNCH(rec, kKTcSegOut, tc_chain(p, ws, 2, st));
     }
@@ -272,6 +284,7 @@ const char *gdr_kernel_name(int id) {
     case kKTcGlaPre: return "tc_gla_prescan";
     case kKTcGlaSegOut: return "tc_gla_segment_out";
     case kKComposeScalar: return "compose_scalar";
+    case kKTcPreDual: return "tc_prescan_dual";
     default: return "?";
     }
 }

@@ -114,6 +114,16 @@ def test_many_short_sequences_delta(S):
           force_path=2)
 
 
+@pytest.mark.parametrize("S", [2, 8])
+def test_segment_prescan_both_kernels(S):
+    """Multi-chunk ragged segments, an empty sequence: at 4 heads, S = 2 runs
+    each summary (c_s, M_s) as its own chain; S = 8 has too many segments for
+    one wave and runs both summaries of a segment in one CTA."""
+    w = synthetic.small(W["wide_varlen_bf16"], H=4)
+    check(synthetic.make_inputs(w, lengths=[1000, 700, 64, 0, 333]), n_segments=S,
+          force_path=2)
+
+
 @pytest.mark.parametrize("S", [1, 2])
 def test_many_short_sequences_beta_free(S):
     w = synthetic.small(W["gla_k256_v512_bf16"], K=128, V=256, H=2)
