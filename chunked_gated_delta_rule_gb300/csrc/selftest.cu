@@ -138,19 +138,18 @@ k_selftest_tma(const __grid_constant__ CUtensorMap map, __nv_bfloat16 *__restric
 // device routine the tensor-core chain kernel uses.
 __global__ void __launch_bounds__(256) k_selftest_inverse(const float *__restrict__ A,
                                                           float *__restrict__ T) {
-    __shared__ float sA[64 * kInvLd];
-    __shared__ float sT[64 * kInvLd];
+    __shared__ float sAT[64 * kInvLd];
     __shared__ float sX[kInvScratchFloats];
     const int tid = threadIdx.x;
     for (int idx = tid; idx < 64 * 64; idx += 256) {
         const int i = idx >> 6, j = idx & 63;
-        sA[i * kInvLd + j] = j < i ? A[idx] : 0.f;
+        sAT[i * kInvLd + j] = j < i ? A[idx] : 0.f;
     }
     __syncthreads();
-    invert_unit_lower64(sA, sT, sX, tid);
+    invert_unit_lower64(sAT, sX, tid);
     for (int idx = tid; idx < 64 * 64; idx += 256) {
         const int i = idx >> 6, j = idx & 63;
-        T[idx] = j <= i ? sT[i * kInvLd + j] : 0.f;
+        T[idx] = j <= i ? sAT[i * kInvLd + j] : 0.f;
     }
 }
 

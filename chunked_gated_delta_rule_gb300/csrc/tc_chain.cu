@@ -7,8 +7,9 @@
 // tc_prep.cu for all chunks in parallel and left in one record per (chunk,
 // head); here, per chunk, in order:
 //
-//   [v_new^T | O] = h^T [W; Q~]^T      (tcgen05, N = 128; A is the BF16
-//                                       mirror of h^T)
+//   [v_new^T | O] = h^T [W; Q~]^T      (tcgen05, two N = 64 products: W^T
+//                                       first, committed on its own; A is
+//                                       the BF16 mirror of h^T)
 //   v_new^T = U^T - (h^T W^T)
 //   h^T <- e^{G_last} h^T + v_new^T K~  (tcgen05 accumulating onto the FP32
 //                                       state in TMEM, pre-scaled)
@@ -65,7 +66,8 @@ constexpr int kRing = 3;       // decoded chains handed out ahead (bounds the lo
 
 // Shared memory (bytes from a 1024-aligned base).  One stage holds one
 // record image (layout in tc_chunk.cuh):
-//   [Wb0|Q~b0|Wb1|Q~b1] 32 KB: B operand [W; Q~] (K-major, N = 128 rows)
+//   W^T 16 KB: B operand of h^T W^T (MN-major, N = 64);
+//   [Q~b0|Q~b1] 16 KB: B operand of h^T Q~^T (K-major, N = 64)
 //   [K~b0|K~b1] 16 KB: B operand of the update (MN-major, N = 128), k as
 //                      loaded, scaled in place
 //   scale P 8 KB: B operand of O (K-major, N = 64); U^T 16 KB; vectors.
@@ -77,7 +79,7 @@ constexpr uint32_t kOffRing = kOffOs + 16384;  // decoded chains
 enum : int {
     kBFull = 0,     // [2] stage landed (bulk-copy and TMA bytes)
     kBMready = 2,   // mirror written (state path, 128)
-    kBAdone = 3,    // [h^T W^T | O] done (commit)
+    kBAdone = 3,    // h^T W^T done (commit)
     kBVready = 4,   // v_new tile written, state scaled (state path, 128)
     kBHdone = 5,    // state update done (commit)
     kBO2 = 6,       // [2] O complete (commit)
@@ -106,8 +108,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0;    // two buffers of [h^T W^T | O], 128 columns each
 constexpr uint32_t kColS = 256;  // FP32 state h^T, 128 columns
 
-constexpr uint32_t kIdescA128 = idesc_bf16(128, 128, 0, 0);
-constexpr uint32_t kIdescA64 = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t kIdescW = idesc_bf16(128, 64, 0, 1);   // B = W^T, MN-major
+constexpr uint32_t kIdescQ = idesc_bf16(128, 64, 0, 0);   // B = Q~, K-major
 constexpr uint32_t kIdescH = idesc_bf16(128, 128, 0, 1);
 constexpr uint32_t kIdescO2 = idesc_bf16(128, 64, 0, 0);
 
@@ -253,8 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         const uint32_t bytes = 16384u + 16384u + (kImgBytes - kImgVec) +
                                                (c.trans ? 0u : 16384u);
                         mbar_arrive_expect_tx(bar, bytes);
-                        bulk_load(dst + kImgWQ, rec + kImgWQ, 8192u, bar);
-                        bulk_load(dst + kImgWQ + 16384, rec + kImgWQ + 16384, 8192u, bar);
+                        bulk_load(dst + kImgW, rec + kImgW, 16384u, bar);
                         tma_load_3d(dst + kImgK, &args.tk, bar, 0, c.h, tt);
                         tma_load_3d(dst + kImgK + 8192, &args.tk, bar, 64, c.h, tt);
                         if (!c.trans) bulk_load(dst + kImgU, rec + kImgU, 16384u, bar);
@@ -282,15 +283,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    // [h^T W^T | O = h^T Q~^T]
+                    // h^T W^T, then O = h^T Q~^T while v_new is formed
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        umma_bf16(tmem + kColA + 128 * b, sdesc_sw128(sb + kOffHm + ko, 16, 1024),
-                                  sdesc_sw128(sta + kImgWQ + ko, 16, 1024),
-                                  kOut ? kIdescA128 : kIdescA64, kk > 0);
-                    }
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16(tmem + kColA + 128 * b,
+                                  sdesc_sw128(sb + kOffHm + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
+                                              1024),
+                                  sdesc_sw128(sta + kImgW + kk * 2048, 16384, 1024), kIdescW,
+                                  kk > 0);
                     umma_commit(&bars[kBAdone]);
+                    if (kOut) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            umma_bf16(tmem + kColA + 128 * b + 64,
+                                      sdesc_sw128(sb + kOffHm + (kk >> 2) * 16384 + (kk & 3) * 32,
+                                                  16, 1024),
+                                      sdesc_sw128(sta + kImgQ + (kk >> 2) * 8192 + (kk & 3) * 32,
+                                                  16, 1024),
+                                      kIdescQ, kk > 0);
+                    }
                     if (!wait(kBVready, gk) || !wait(kBKready + b, gk >> 1)) {
                         ok = false;
                         break;

@@ -14,9 +14,10 @@ constexpr int kD = 128;  // K = V = 128 on the tensor-core path
 // shared-memory stage, so that bulk copies load it.  BF16 tiles of 64
 // columns in the 128-byte swizzled layout (sw128_off, 64 rows per 8 KB
 // block unless noted):
-//   [0, 32 KB)      W block 0 | Q~ block 0 | W block 1 | Q~ block 1: row t of
-//                   W block b holds W[t][64 b .. 64 b + 63] (K-major), row t
-//                   of Q~ block b holds Q~[t][64 b ..], Q~ = scale e^{G_t} q_t
+//   [0, 16 KB)      W^T, 128 rows: row k holds W[t][k] for t = 0..63 (the
+//                   MN-major B operand of h^T W^T)
+//   [16 KB, 32 KB)  Q~ block 0 | Q~ block 1: row t of block b holds
+//                   Q~[t][64 b .. 64 b + 63] (K-major), Q~ = scale e^{G_t} q_t
 //   [32 KB, 48 KB)  not written: the scan kernel loads k there and forms
 //                   K~ = e^{G_last - G_t} k_t in place
 //   [48 KB, 56 KB)  scale P: row i holds scale P[i][j] for j = 0..63, where
@@ -26,7 +27,7 @@ constexpr int kD = 128;  // K = V = 128 on the tensor-core path
 //                   e^{G_last - G_t} for t = 0..63
 // Padded tokens (past a sequence end) have zero W, Q~, U and P entries and
 // zero decay: every later product with them adds exact zeros.
-constexpr uint32_t kImgWQ = 0, kImgK = 32768, kImgP = 49152, kImgU = 57344, kImgVec = 73728;
+constexpr uint32_t kImgW = 0, kImgQ = 16384, kImgK = 32768, kImgP = 49152, kImgU = 57344, kImgVec = 73728;
 constexpr uint32_t kImgDec = kImgVec + 16;      // the 64 decay factors
 constexpr uint32_t kImgBytes = kImgDec + 256;   // bytes of one stage image (74,000)
 constexpr uint32_t kRecBytes = 74752;           // record stride (1 KB aligned); gdr_api.cu sizes it

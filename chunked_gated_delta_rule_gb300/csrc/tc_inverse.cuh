@@ -1,6 +1,7 @@
 // tc_inverse.cuh -- T = (I + A)^-1 for a strictly lower-triangular 64 x 64
 // FP32 matrix A in shared memory (row stride kInvLd), by one CTA of 256
-// threads (A4 of the chunked form: the UT transform's triangular inverse).
+// threads (A4 of the chunked form: the UT transform's triangular inverse),
+// in place: the array holds A on entry and T on exit.
 //
 //   1. invert_diag16: the four 16 x 16 diagonal blocks T_bb = (I + A_bb)^-1
 //      in FP32, one thread per (block, column) (64 threads): right-looking
@@ -15,8 +16,10 @@
 //      keeps close to FP32 accuracy; tiles of a triangular factor that are
 //      zero are skipped.
 //
-// T's entries above the diagonal of each diagonal block are written as 0;
-// blocks above the block diagonal are not written (callers mask j > i).
+// Every block is read as A before it is written as T: each step forms its
+// products from A (and blocks of T already final), then a barrier, then the
+// writes.  T's entries above the diagonal of each diagonal block are written
+// as 0; blocks above the block diagonal keep A's zeros.
 #pragma once
 
 #include "tc_common.cuh"
@@ -68,8 +71,10 @@ __device__ __forceinline__ void warp_store16x8(float *D, int ldd, const float (&
     D[(g + 8) * ldd + 2 * t + 1] = sign * ((lh[3] + hl[3]) + hh[3]);
 }
 
-// Step 1: threads 0..63 only (block tid / 16, column tid % 16).
-__device__ __forceinline__ void invert_diag16(const float *sA, float *sT, int tid) {
+// Step 1: threads 0..63 only (block tid / 16, column tid % 16); named
+// barrier 2 among them.
+__device__ __forceinline__ void invert_diag16(float *sAT, int tid) {
+    const float *sA = sAT;
     const int b = tid >> 4, m = tid & 15, o = 16 * b;
     float s[16], x[16];
 #pragma unroll
@@ -82,14 +87,17 @@ __device__ __forceinline__ void invert_diag16(const float *sA, float *sT, int ti
 #pragma unroll
         for (int r = j + 1; r < 16; ++r) s[r] = fmaf(sA[(o + r) * kInvLd + o + j], x[j], s[r]);
     }
+    asm volatile("bar.sync 2, 64;" ::: "memory");  // every column has read A_bb
 #pragma unroll
-    for (int r = 0; r < 16; ++r) sT[(o + r) * kInvLd + o + m] = x[r];
+    for (int r = 0; r < 16; ++r) sAT[(o + r) * kInvLd + o + m] = x[r];
 }
 
-// Step 2: all 256 threads; the diagonal blocks of sT must be complete (and
-// visible: a barrier after step 1).  sX: kInvScratchFloats floats.  Ends
-// with a barrier.
-__device__ __forceinline__ void invert_merge(const float *sA, float *sT, float *sX, int tid) {
+// Step 2: all 256 threads; the diagonal blocks must be complete (and
+// visible: a barrier after step 1).  sX: kInvScratchFloats floats.  Named
+// barrier 3 among warps 0-3; ends with a barrier.
+__device__ __forceinline__ void invert_merge(float *sAT, float *sX, int tid) {
+    const float *sA = sAT;
+    float *sT = sAT;
     const int warp = tid >> 5, lane = tid & 31;
     // 16 x 16 blocks (1, 0) and (3, 2): warp = 2 (block pair) + column tile
     if (warp < 4) {
@@ -100,7 +108,7 @@ __device__ __forceinline__ void invert_merge(const float *sA, float *sT, float *
                              sT + (16 * j) * kInvLd + 16 * j + 8 * nt, kInvLd, lane);
         float *X = sX + warp * 16 * kInvXLd;
         warp_store16x8(X, kInvXLd, hh, hl, lh, 1.f, lane);
-        __syncwarp();
+        asm volatile("bar.sync 3, 128;" ::: "memory");  // A_ij read by both column tiles
         float th[4] = {0.f, 0.f, 0.f, 0.f}, tl[4] = {0.f, 0.f, 0.f, 0.f},
               tm[4] = {0.f, 0.f, 0.f, 0.f};
         warp_gemm16x8_3xtf32(th, tl, tm, sT + (16 * i) * kInvLd + 16 * i, kInvLd, X, kInvXLd,
@@ -134,11 +142,10 @@ __device__ __forceinline__ void invert_merge(const float *sA, float *sT, float *
 }
 
 // Both steps, for callers with nothing to overlap with step 1.
-__device__ __forceinline__ void invert_unit_lower64(const float *sA, float *sT, float *sX,
-                                                    int tid) {
-    if (tid < 64) invert_diag16(sA, sT, tid);
+__device__ __forceinline__ void invert_unit_lower64(float *sAT, float *sX, int tid) {
+    if (tid < 64) invert_diag16(sAT, tid);
     __syncthreads();
-    invert_merge(sA, sT, sX, tid);
+    invert_merge(sAT, sX, tid);
 }
 
 }  // namespace tc

@@ -1,6 +1,6 @@
 // tc_prep.cu -- A2-A5 on the tensor-core path (BF16, K = V = 128, delta rule):
 // everything of the chunked form that does not depend on the state, for
-// every (chunk, head) in parallel.  Persistent CTAs (two per SM) walk the
+// every (chunk, head) in parallel.  Persistent CTAs (three per SM) walk the
 // (chunk, head) items; per item:
 //
 //   G (gate cumsum), D1 = [K; Q] K^T on tcgen05 (rows 0-63 K K^T, rows 64-127
@@ -13,9 +13,10 @@
 // tc_chunk.cuh), assembled here in shared memory and written by bulk async
 // copies, which the scan kernel (tc_chain.cu) loads back, so the serial chain
 // only does the state-dependent products.  The next item's table row and
-// gates are loaded early, and its K, Q, V tiles start loading as soon as the
+// gates are loaded early, and its K and Q tiles start loading as soon as the
 // current item's last product has consumed them, while the current item's
-// results are still being staged and written.  Chunked form: the project
+// results are still being staged and written; V, which only the last
+// product reads, loads while the inverse runs.  Chunked form: the project
 // statement; the WY/UT preparation ahead of fla's state-scan kernel
 // chunk_gated_delta_rule_fwd_kernel_h_blockdim64 (Kev PR #259 intro).
 #include "gdr_internal.cuh"
@@ -36,32 +37,35 @@ struct PrepArgs {
 
 constexpr int kThreads = 256;
 
-// Shared memory (bytes from a 1024-aligned base).
-// [0, 48 KB): the K, Q, V tiles [Kb0|Qb0|Kb1|Qb1|Vb0|Vb1]; Q~ is formed in
-// place once D1 is done.  After the last product, W is staged over sT and
-// U^T over sA.
-constexpr uint32_t kOffAT = 49152;                      // sA, sT (FP32, ld kInvLd)
-constexpr uint32_t kOffT = kOffAT + 64 * kInvLd * 4;
-constexpr uint32_t kOffBW = kOffAT;                     // B_W, B_U over sA afterwards
-constexpr uint32_t kOffBU = kOffAT + 8192;
-constexpr uint32_t kOffStU = kOffAT;                    // U^T staging, after the last product
-constexpr uint32_t kOffStW = kOffT;                     // W staging, after the last product
-constexpr uint32_t kOffX = kOffAT + 34816;              // inverse scratch
+// Shared memory (bytes from a 1024-aligned base), 74 KB so that three CTAs
+// fit an SM.  Each region serves several tiles in turn:
+//   [Kb0|Qb0|Kb1|Qb1]  K and Q (the A operand [K; Q] of D1); Q~ is formed in
+//                      place once D1 is done and, once its copies have read
+//                      it, B_W and B_U take the two Q blocks;
+//   kOffV (16 KB)      the previous item's W staging, this item's scale P
+//                      staging, then this item's V (loaded once the P copy
+//                      has read the slot; only the last product needs it);
+//   kOffAT             A, then T in place (FP32, ld kInvLd); U^T staging
+//                      after the last product.
+constexpr uint32_t kOffBW = 8192, kOffBU = 24576;       // over Qb0, Qb1
+constexpr uint32_t kOffV = 32768;                       // [Vb0|Vb1]
+constexpr uint32_t kOffStP = kOffV;                     // scale P staging, 8 KB
+constexpr uint32_t kOffStW = kOffV;                     // W staging, 16 KB
+constexpr uint32_t kOffAT = 49152;                      // A / T
+constexpr uint32_t kOffStU = kOffAT;                    // U^T staging, 16 KB
+constexpr uint32_t kOffX = kOffAT + 64 * kInvLd * 4;    // inverse scratch
 constexpr uint32_t kOffVec = kOffX + 4 * kInvScratchFloats;  // gate vectors, two items'
-constexpr uint32_t kOffBar = kOffVec + 2 * 1600;
-constexpr uint32_t kOffStP = (kOffBar + 64 + 1023) / 1024 * 1024;  // scale P staging, 8 KB
-constexpr uint32_t kSmemLaunch = kOffStP + 8192 + 1024;
-static_assert(kOffStW % 1024 == 0 && kOffStU % 1024 == 0, "staging tiles are 1 KB aligned");
+constexpr uint32_t kOffBar = kOffVec + 2 * 1600;        // K/Q tiles, products, V tile
+constexpr uint32_t kSmemLaunch = kOffBar + 64 + 1024;
+static_assert(kOffStU % 1024 == 0 && kOffStP % 1024 == 0, "staging tiles are 1 KB aligned");
+static_assert(kSmemLaunch <= 76800, "three CTAs per SM");
 
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColD1 = 0, kColW = 64, kColU = 128;
+// TMEM: D1, then W^T over it (D1 is consumed before the last product), U^T.
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kColD1 = 0, kColW = 0, kColU = 64;
 
 constexpr uint32_t kIdescKK64 = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescMK64 = idesc_bf16(128, 64, 1, 0);
-
-__device__ __forceinline__ void st_bf16(uint8_t *p, float x) {
-    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
-}
 
 // Rows of two 8 KB tiles at `a` and `a + 16384` scaled in place by c f[row]
 // (64 rows of 128 bytes each, in 16-byte pieces; thread t of n threads).
@@ -79,17 +83,16 @@ __device__ __forceinline__ void scale_rows_in_place(uint8_t *a, const float *f, 
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__ PrepArgs args) {
+__global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__ PrepArgs args) {
     const Problem &p = args.p;
     const Workspace &ws = args.ws;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);  // tma, mma
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffBar + 16);
-    float *sA = reinterpret_cast<float *>(sm + kOffAT);
-    float *sT = reinterpret_cast<float *>(sm + kOffT);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);  // K/Q tma, mma, V tma
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffBar + 24);
+    float *sAT = reinterpret_cast<float *>(sm + kOffAT);
     float *sX = reinterpret_cast<float *>(sm + kOffX);
     const int4 *tab = reinterpret_cast<const int4 *>(ws.chunk_tab);
 
@@ -97,8 +100,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
     const int quad = warp & 3, half = warp >> 2;
     const int row = 32 * quad + lane_id;  // TMEM lane = matrix row
     const int H = (int)p.H;
-    const int64_t n_items = (int64_t)(*ws.n_chunks) * H;
-    int64_t item = blockIdx.x;
+    const int n_items = *ws.n_chunks * H;  // below 2^31 (checked by the host)
+    int item = blockIdx.x;
     if (item >= n_items) return;
 
     // The gates of a chunk-head (padded tokens: g = beta = 0), loaded by warp 0.
@@ -111,13 +114,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
         }
     };
     auto issue_inputs = [&](const int4 &e, int h) {
-        mbar_arrive_expect_tx(&bars[0], 49152u);
+        mbar_arrive_expect_tx(&bars[0], 32768u);
         tma_load_3d(sm + 0, &args.tk, &bars[0], 0, h, e.y);
         tma_load_3d(sm + 16384, &args.tk, &bars[0], 64, h, e.y);
         tma_load_3d(sm + 8192, &args.tq, &bars[0], 0, h, e.y);
         tma_load_3d(sm + 24576, &args.tq, &bars[0], 64, h, e.y);
-        tma_load_3d(sm + 32768, &args.tv, &bars[0], 0, h, e.y);
-        tma_load_3d(sm + 40960, &args.tv, &bars[0], 64, h, e.y);
     };
 
     int4 e = tab[item / H];
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
         mbar_init_fence();
         issue_inputs(e, h);
     }
@@ -142,8 +144,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
 
     for (uint32_t it = 0;; ++it) {
         const int len = e.z;
-        uint8_t *img = ws.rec + item * (int64_t)kRecBytes;
-        const int64_t nxt = item + gridDim.x;
+        uint8_t *img = ws.rec + (int64_t)item * kRecBytes;
+        const int nxt = item + (int)gridDim.x;
         const bool more = nxt < n_items;
         int4 en = e;
         int hn = h;
@@ -159,8 +161,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
         if (__syncthreads_or(!ok)) break;
         if (len < 64) {  // rows past the sequence end belong to the next one: zero them
             const int rows = 64 - len;
-            for (int idx = tid; idx < rows * 6 * 8; idx += kThreads) {
-                const int r = len + idx / 48, blk = (idx / 8) % 6, c16 = idx & 7;
+            for (int idx = tid; idx < rows * 4 * 8; idx += kThreads) {
+                const int r = len + idx / 32, blk = (idx / 8) & 3, c16 = idx & 7;
                 st_shared_v4(sm + blk * 8192 + r * 128 + c16 * 16, 0u, 0u, 0u, 0u);
             }
             fence_async_smem();
@@ -184,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
             if (warp == 0) load_gates(en, hn, g2n, b2n);
         }
         ok = mbar_wait(&bars[1], 0, p.status);
-        // the previous item's copies have read their staging tiles (sA, sT,
-        // P, its gate vectors) before they are written again
+        // the previous item's copies have read their staging tiles (W, U^T,
+        // its gate vectors) before they are written again
         if (lane_id == 0) bulk_wait_read();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
             if (quad < 2) {  // row i of A (strictly lower), FP32
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4)
-                    *reinterpret_cast<float4 *>(sA + i * kInvLd + j0 + 4 * c4) =
+                    *reinterpret_cast<float4 *>(sAT + i * kInvLd + j0 + 4 * c4) =
                         make_float4(f[4 * c4], f[4 * c4 + 1], f[4 * c4 + 2], f[4 * c4 + 3]);
             } else {  // row i of scale P
 #pragma unroll
@@ -221,24 +223,33 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
                     st_bf16x8(sm + kOffStP + sw128_off(i, j0 + 8 * c8, 64), f + 8 * c8);
             }
         }
+        fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (tid == 224) {  // scale P out, so that V can take its slot
+            bulk_store(img + kImgP, sm + kOffStP, 8192u);
+            bulk_commit();
+        }
 
         // A4: T = (I + A)^-1.  The diagonal blocks on warps 0-1 while warps 2-7
         // form Q~ = scale diag(e^G) Q in place (no product reads Q any more).
         if (tid < 64)
-            invert_diag16(sA, sT, tid);
+            invert_diag16(sAT, tid);
         else
             scale_rows_in_place(sm + 8192, sGam, p.scale, tid - 64, kThreads - 64);
         fence_async_smem();
         __syncthreads();
-        if (lane_id == 0 && warp >= 5) {  // Q~ blocks and scale P, one copy per warp
-            if (warp == 5) bulk_store(img + kImgWQ + 8192, sm + 8192, 8192u);
-            else if (warp == 6) bulk_store(img + kImgWQ + 24576, sm + 24576, 8192u);
-            else bulk_store(img + kImgP, sm + kOffStP, 8192u);
+        if (lane_id == 0 && (warp == 5 || warp == 6)) {  // Q~ blocks, one copy per warp
+            bulk_store(img + kImgQ + (warp - 5) * 8192, sm + 8192 + (warp - 5) * 16384, 8192u);
             bulk_commit();
+            bulk_wait_read();  // B_W, B_U take these blocks (warps 4-7 idle in the first merge step)
+        } else if (tid == 224) {  // V into the slot P has left
+            bulk_wait_read();
+            mbar_arrive_expect_tx(&bars[2], 16384u);
+            tma_load_3d(sm + kOffV, &args.tv, &bars[2], 0, h, e.y);
+            tma_load_3d(sm + kOffV + 8192, &args.tv, &bars[2], 64, h, e.y);
         }
-        invert_merge(sA, sT, sX, tid);
+        invert_merge(sAT, sX, tid);
 
         // A5 operands: rows of T diag(beta e^G) (rows 0-63) and T diag(beta)
         // (rows 64-127), BF16, columns [32 half, 32 half + 32).
@@ -249,8 +260,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
                 const int j0 = 32 * half + 8 * c8;
-                const float4 a0 = *reinterpret_cast<const float4 *>(sT + i * kInvLd + j0);
-                const float4 a1 = *reinterpret_cast<const float4 *>(sT + i * kInvLd + j0 + 4);
+                const float4 a0 = *reinterpret_cast<const float4 *>(sAT + i * kInvLd + j0);
+                const float4 a1 = *reinterpret_cast<const float4 *>(sAT + i * kInvLd + j0 + 4);
                 const float tv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
                 float x[8];
 #pragma unroll
@@ -258,9 +269,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
                 st_bf16x8(dst + sw128_off(i, j0, 64), x);
             }
         }
+        ok = true;
+        if (len < 64) {  // V's rows past the sequence end, once V has landed
+            ok = mbar_wait(&bars[2], it & 1u, p.status);
+            const int rows = 64 - len;
+            for (int idx = tid; ok && idx < rows * 2 * 8; idx += kThreads) {
+                const int r = len + idx / 16, blk = (idx / 8) & 1, c16 = idx & 7;
+                st_shared_v4(sm + kOffV + blk * 8192 + r * 128 + c16 * 16, 0u, 0u, 0u, 0u);
+            }
+        }
         fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        if (__syncthreads_or(!ok)) break;
+        if (tid == 0 && mbar_wait(&bars[2], it & 1u, p.status)) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -268,24 +288,23 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
                           sdesc_sw128(sb + kOffBW + kk * 32, 16, 1024), kIdescMK64, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                umma_bf16(tmem + kColU, sdesc_sw128(sb + 32768 + kk * 2048, 8192, 1024),
+                umma_bf16(tmem + kColU, sdesc_sw128(sb + kOffV + kk * 2048, 8192, 1024),
                           sdesc_sw128(sb + kOffBU + kk * 32, 16, 1024), kIdescMK64, kk > 0);
             umma_commit(&bars[1]);
         }
         ok = mbar_wait(&bars[1], 1, p.status);
-        // K, Q~ and V are free once the products and the Q~ copies have read
-        // them: the next item's tiles start loading now.
+        // K and the Q blocks are free once the products have read them: the
+        // next item's K and Q start loading now.
         if (lane_id == 0) bulk_wait_read();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
         if (tid == 0 && more) issue_inputs(en, hn);
-        {  // W (K-major, row t) and U^T (row v), t in [32 half, 32 half + 32), staged
+        {  // W^T (row k) and U^T (row v), t in [32 half, 32 half + 32), staged
             float f[32];
             tmem_load32f(tmem + lane + kColW + 32 * half, f);
-            uint8_t *wblk = sm + kOffStW + (row >> 6) * 8192;
 #pragma unroll
-            for (int u = 0; u < 32; ++u)
-                st_bf16(wblk + sw128_off(32 * half + u, row & 63, 64), f[u]);
+            for (int c8 = 0; c8 < 4; ++c8)
+                st_bf16x8(sm + kOffStW + sw128_off(row, 32 * half + 8 * c8, 128), f + 8 * c8);
             tmem_load32f(tmem + lane + kColU + 32 * half, f);
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8)
@@ -297,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_tc_prep(const __grid_constant__
         // one copy per warp (lane 0), so they are issued side by side
         if (lane_id == 0 && warp < 5) {
             switch (warp) {
-            case 0: bulk_store(img + kImgWQ, sm + kOffStW, 8192u); break;
-            case 1: bulk_store(img + kImgWQ + 16384, sm + kOffStW + 8192, 8192u); break;
+            case 0: bulk_store(img + kImgW, sm + kOffStW, 8192u); break;
+            case 1: bulk_store(img + kImgW + 8192, sm + kOffStW + 8192, 8192u); break;
             case 2: bulk_store(img + kImgU, sm + kOffStU, 16384u); break;
             case 3: bulk_store(img + kImgVec, vec + 384, 16u); break;  // G_last, e^{G_last}
             default: bulk_store(img + kImgDec, sDec, 256u); break;     // e^{G_last - G}
@@ -340,7 +359,8 @@ cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st) {
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t items = ws.max_chunks * p.H;  // an upper bound; the kernel reads the count
-    const int64_t grid = items < 2 * sms ? items : 2 * sms;
+    if (items > INT32_MAX - 4 * (int64_t)sms) return cudaErrorInvalidValue;
+    const int64_t grid = items < 3 * sms ? items : 3 * sms;  // three CTAs per SM
     k_tc_prep<<<(unsigned)grid, kThreads, kSmemLaunch, st>>>(args);
     return cudaGetLastError();
 }

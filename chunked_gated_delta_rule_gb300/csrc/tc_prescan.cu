@@ -75,7 +75,7 @@ constexpr uint32_t kColA = 0;     // [2] 64 columns each
 constexpr uint32_t kColS = 128;   // [2] 128 columns each
 constexpr uint32_t kColM = 384;   // [2] 64 columns each
 
-constexpr uint32_t kIdescA = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t kIdescA = idesc_bf16(128, 64, 0, 1);  // B = W^T, MN-major
 constexpr uint32_t kIdescH = idesc_bf16(128, 128, 0, 1);
 
 __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constant__ PreArgs args) {
@@ -177,8 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                     uint64_t *bar = &bars[kPFull + stage];
                     uint8_t *dst = sm + stage * kStage;
                     mbar_arrive_expect_tx(bar, 16384u + 16384u + 16384u + (kImgBytes - kImgVec));
-                    bulk_load(dst + kImgWQ, rec + kImgWQ, 8192u, bar);
-                    bulk_load(dst + kImgWQ + 16384, rec + kImgWQ + 16384, 8192u, bar);
+                    bulk_load(dst + kImgW, rec + kImgW, 16384u, bar);
                     tma_load_3d(dst + kImgK, &args.tk, bar, 0, c.h, tt);
                     tma_load_3d(dst + kImgK + 8192, &args.tk, bar, 64, c.h, tt);
                     bulk_load(dst + kImgU, rec + kImgU, 16384u, bar);
@@ -209,11 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                     tc_fence_after();
                     // h^T W^T, A = the state's BF16 mirror in TMEM
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t ko = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        umma_bf16_ts(cA, cM + 8 * kk, sdesc_sw128(sta + kImgWQ + ko, 16, 1024),
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16_ts(cA, cM + 8 * kk, sdesc_sw128(sta + kImgW + kk * 2048, 16384, 1024),
                                      kIdescA, kk > 0);
-                    }
                     umma_commit(&bars[kPAdone + q]);
                     if (!wait(kPVready + q, gk) || !wait(kPKready + b, gk >> 1)) {
                         ok = false;
