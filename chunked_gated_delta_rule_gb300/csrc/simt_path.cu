@@ -43,74 +43,114 @@ __device__ __forceinline__ void report(int32_t *status, int code) {
 // chunk of every sequence.  Malformed cu_seqlens (not non-decreasing, not
 // starting at 0, not ending at T, or more chunks than the table holds) make
 // the call compute nothing and set GDR_ERR_SEQLENS in the status word.
-// Also writes the sequences in descending order of chunk count (a stable
-// counting sort; counts above 127 share the top bucket) for the persistent
-// tensor-core kernels, which take the longest chains first, and zeroes their
-// chain counters.  Up to kSmemSeqs sequences the serial passes run on shared
-// memory; beyond that on global memory.
+// Also writes the sequences in descending order of chunk count (a counting
+// sort; counts above 127 share the top bucket, and the order inside a bucket
+// is whatever the shared-memory atomics give: it only decides which CTA
+// takes which chain) for the persistent tensor-core kernels, which take the
+// longest chains first, and zeroes their chain counters.  Every pass is
+// block-parallel: each thread owns a contiguous run of sequences, and the
+// chunk offsets come from a block-wide scan.  Up to kSmemSeqs sequences the
+// counts and offsets live in shared memory; beyond that in global memory.
 constexpr int kSmemSeqs = 8192;
 constexpr int kBuckets = 128;
 
-__global__ void k_chunk_table(const int32_t *__restrict__ cu, int64_t N, int64_t T,
-                              int64_t max_chunks, int32_t *__restrict__ tab,
-                              int32_t *__restrict__ seq_chunk0,
-                              int32_t *__restrict__ n_chunks, int32_t *__restrict__ seq_order,
-                              int32_t *status) {
+__device__ __forceinline__ int chunk_bucket(int c) { return c < kBuckets - 1 ? c : kBuckets - 1; }
+
+__global__ void __launch_bounds__(kThreads) k_chunk_table(const int32_t *__restrict__ cu,
+                                                          int64_t N, int64_t T,
+                                                          int64_t max_chunks,
+                                                          int32_t *__restrict__ tab,
+                                                          int32_t *__restrict__ seq_chunk0,
+                                                          int32_t *__restrict__ n_chunks,
+                                                          int32_t *__restrict__ seq_order,
+                                                          int32_t *status) {
     __shared__ int s_bad;
     __shared__ int s_hist[kBuckets];
+    __shared__ long long s_part[kThreads / 32];
     __shared__ int s_c0[kSmemSeqs + 1];
     const bool in_smem = N <= kSmemSeqs;
     int32_t *c0 = in_smem ? s_c0 : seq_chunk0;  // chunk counts, then prefix offsets
-    for (int b = threadIdx.x; b < kBuckets; b += blockDim.x) s_hist[b] = 0;
-    if (threadIdx.x < 3) n_chunks[1 + threadIdx.x] = 0;
-    if (threadIdx.x == 0) s_bad = (cu && (cu[0] != 0 || cu[N] != T)) ? 1 : 0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int b = tid; b < kBuckets; b += kThreads) s_hist[b] = 0;
+    if (tid < 3) n_chunks[1 + tid] = 0;
+    if (tid == 0) s_bad = (cu && (cu[0] != 0 || cu[N] != T)) ? 1 : 0;
     __syncthreads();
-    for (int64_t n = threadIdx.x; n < N; n += blockDim.x) {
+    // this thread's run of sequences, their chunk counts and the histogram
+    const int64_t per = (N + kThreads - 1) / kThreads;
+    const int64_t lo = min(N, (int64_t)tid * per), hi = min(N, lo + per);
+    long long local = 0;
+    for (int64_t n = lo; n < hi; ++n) {
         const int64_t a = cu ? cu[n] : n * T;
         const int64_t len = (cu ? cu[n + 1] : (n + 1) * T) - a;
         if (len < 0) s_bad = 1;
         const int64_t c = len < 0 ? 0 : (len + kChunk - 1) / kChunk;
-        c0[n] = (int32_t)(c <= max_chunks ? c : max_chunks + 1);
+        const int32_t cc = (int32_t)(c <= max_chunks ? c : max_chunks + 1);
+        c0[n] = cc;
+        local += cc;
+        atomicAdd(&s_hist[chunk_bucket(cc)], 1);
     }
-    __syncthreads();
-    if (threadIdx.x == 0 && !s_bad) {
-        int64_t acc = 0;
-        for (int64_t n = 0; n < N; ++n) {
-            const int c = c0[n];
-            ++s_hist[c < kBuckets - 1 ? c : kBuckets - 1];
-            c0[n] = (int32_t)acc;
-            acc += c;
-            if (acc > max_chunks) { s_bad = 1; break; }
-        }
-        if (!s_bad) {
-            c0[N] = (int32_t)acc;
-            int run = 0;  // bucket b starts after every longer bucket
-            for (int b = kBuckets - 1; b >= 0; --b) {
-                const int c = s_hist[b];
-                s_hist[b] = run;
-                run += c;
-            }
-            for (int64_t n = 0; n < N; ++n) {
-                const int c = c0[n + 1] - c0[n];
-                seq_order[s_hist[c < kBuckets - 1 ? c : kBuckets - 1]++] = (int32_t)n;
-            }
-        }
-        *n_chunks = s_bad ? 0 : (int32_t)acc;
-        if (s_bad) report(status, GDR_ERR_SEQLENS);
-    } else if (threadIdx.x == 0) {
-        *n_chunks = 0;
-        report(status, GDR_ERR_SEQLENS);
+    // block-wide exclusive scan of the runs' chunk totals
+    long long incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
     }
+    if (lane == 31) s_part[warp] = incl;
     __syncthreads();
-    if (s_bad) {
-        for (int64_t n = threadIdx.x; n <= N; n += blockDim.x) seq_chunk0[n] = 0;
-        for (int64_t n = threadIdx.x; n < N; n += blockDim.x) seq_order[n] = (int32_t)n;
+    long long before = 0, total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+        if (w < warp) before += s_part[w];
+        total += s_part[w];
+    }
+    const bool bad = s_bad || total > max_chunks;
+    if (!bad) {
+        int32_t run = (int32_t)(before + incl - local);
+        for (int64_t n = lo; n < hi; ++n) {
+            const int32_t c = c0[n];
+            c0[n] = run;
+            run += c;
+        }
+        if (tid == 0) c0[N] = (int32_t)total;
+    }
+    if (tid == 0) {
+        *n_chunks = bad ? 0 : (int32_t)total;
+        if (bad) report(status, GDR_ERR_SEQLENS);
+    }
+    if (bad) {
+        for (int64_t n = tid; n <= N; n += kThreads) seq_chunk0[n] = 0;
+        for (int64_t n = tid; n < N; n += kThreads) seq_order[n] = (int32_t)n;
         return;
     }
+    // bucket b starts after every longer bucket: a reverse exclusive scan of
+    // the histogram by warp 0, four buckets a lane from the top
+    if (warp == 0) {
+        int h4[4], sum = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            h4[u] = s_hist[kBuckets - 1 - (4 * lane + u)];
+            sum += h4[u];
+        }
+        int inc = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += y;
+        }
+        int run = inc - sum;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            s_hist[kBuckets - 1 - (4 * lane + u)] = run;
+            run += h4[u];
+        }
+    }
+    __syncthreads();
+    for (int64_t n = lo; n < hi; ++n)
+        seq_order[atomicAdd(&s_hist[chunk_bucket(c0[n + 1] - c0[n])], 1)] = (int32_t)n;
     if (in_smem)
-        for (int64_t n = threadIdx.x; n <= N; n += blockDim.x) seq_chunk0[n] = c0[n];
+        for (int64_t n = tid; n <= N; n += kThreads) seq_chunk0[n] = c0[n];
     // one warp per sequence, its lanes over the sequence's chunks
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int nwarps = kThreads >> 5;
     for (int64_t n = warp; n < N; n += nwarps) {
         const int64_t a = cu ? cu[n] : n * T;
         const int64_t len = (cu ? cu[n + 1] : (n + 1) * T) - a;
