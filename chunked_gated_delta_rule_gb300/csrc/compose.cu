@@ -41,6 +41,8 @@ __global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Wo
     const int r0 = 2 * rp, c0 = 4 * cg;
     const bool active = r0 < K;
     const int mlen = K / NMS, m0 = ms * mlen;
+    pdl_trigger();
+    pdl_wait();
 
     const int nc = ws.seq_chunk0[n + 1] - ws.seq_chunk0[n];
     const int per = (nc + S - 1) / S;
@@ -155,8 +157,7 @@ cudaError_t launch_compose(const Problem &p, const Workspace &ws, cudaStream_t s
                                            (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid((unsigned)(p.V / CC), (unsigned)p.N, (unsigned)p.H);
-    k_compose_mt<CC><<<grid, kComposeThreads, smem, st>>>(p, ws);
-    return cudaGetLastError();
+    return launch_pdl(k_compose_mt<CC>, grid, dim3(kComposeThreads), smem, st, p, ws);
 }
 
 // Beta-free composition (scaled-identity transitions, cuLA PR #127 "Scope":
@@ -168,6 +169,8 @@ cudaError_t launch_compose(const Problem &p, const Workspace &ws, cudaStream_t s
 __global__ void __launch_bounds__(256) k_compose_scalar(Problem p, Workspace ws) {
     const int64_t kv = p.K * p.V;
     const int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
     if (idx >= p.N * p.H * kv) return;
     const int64_t nh = idx / kv, e = idx - nh * kv;
     const int64_t n = nh / p.H;
@@ -192,8 +195,8 @@ __global__ void __launch_bounds__(256) k_compose_scalar(Problem p, Workspace ws)
 cudaError_t compose_scalar(const Problem &p, const Workspace &ws, cudaStream_t st) {
     const int64_t total = p.N * p.H * p.K * p.V;
     if (total == 0) return cudaSuccess;
-    k_compose_scalar<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(p, ws);
-    return cudaGetLastError();
+    return launch_pdl(k_compose_scalar, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, st,
+                      p, ws);
 }
 
 bool compose_mt_supported(const Problem &p) {

@@ -4,12 +4,42 @@
 
 #include <cstdint>
 #include <cstddef>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
 #include "gdr.h"
 
 namespace gdr {
+
+// Programmatic dependent launch.  Every kernel of a call after the first is
+// launched with launch_pdl, so it may be scheduled while the kernels before
+// it in the stream still run: it sets up (TMEM, barriers) and then calls
+// pdl_wait(), which returns once every earlier kernel of the call has
+// finished and its writes are visible; nothing of the workspace or the
+// outputs is read or written before that.  Kernels call pdl_trigger() early
+// so that the next launch is not held back until they exit.  A grid's
+// dependents are scheduled only after all of its CTAs have started, so a
+// waiting CTA never keeps one of them from running.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args &&...args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kChunk = 64;       // tokens per chunk
 constexpr int kMaxK = 256;       // largest key dim supported

@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads) k_chunk_table(const int32_t *__restr
     const bool in_smem = N <= kSmemSeqs;
     int32_t *c0 = in_smem ? s_c0 : seq_chunk0;  // chunk counts, then prefix offsets
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();  // the first kernel of a call: launched in stream order, it waits for nothing
     for (int b = tid; b < kBuckets; b += kThreads) s_hist[b] = 0;
     if (tid < 3) n_chunks[1 + tid] = 0;
     if (tid == 0) s_bad = (cu && (cu[0] != 0 || cu[N] != T)) ? 1 : 0;

@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
         return true;
     };
 
+    pdl_trigger();
     if (warp == 0) {
         tmem_alloc(s_tmem, kTmemCols);
         tmem_relinquish();
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    pdl_wait();  // the workspace and outputs, once the kernels before have finished
 
     if (warp == 9) {
         // ------------------------------------------------------------ producer
@@ -576,8 +578,7 @@ cudaError_t launch_chain(const TcArgs &args, dim3 grid, cudaStream_t st) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemLaunch);
     if (err != cudaSuccess) return err;
-    k_tc_chain<MODE><<<grid, kThreads, kSmemLaunch, st>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(k_tc_chain<MODE>, grid, dim3(kThreads), kSmemLaunch, st, args);
 }
 
 }  // namespace

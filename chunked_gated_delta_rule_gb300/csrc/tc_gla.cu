@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
         return true;
     };
 
+    pdl_trigger();
     if (warp == 0) {
         tmem_alloc(s_tmem, kTmemCols);
         tmem_relinquish();
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    pdl_wait();  // the workspace and outputs, once the kernels before have finished
 
     if (warp == 9) {
         // ------------------------------------------------------------ producer
@@ -557,8 +559,7 @@ cudaError_t launch_gla(const GlaArgs &args, unsigned grid, cudaStream_t st) {
     cudaError_t err =
         cudaFuncSetAttribute(k_tc_gla<KD, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    k_tc_gla<KD, MODE><<<grid, kThreads, smem, st>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(k_tc_gla<KD, MODE>, grid, dim3(kThreads), smem, st, args);
 }
 
 }  // namespace

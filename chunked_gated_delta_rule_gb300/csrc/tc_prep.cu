@@ -100,9 +100,20 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
     const int quad = warp & 3, half = warp >> 2;
     const int row = 32 * quad + lane_id;  // TMEM lane = matrix row
     const int H = (int)p.H;
+    pdl_trigger();
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        tmem_alloc(s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    pdl_wait();  // the chunk table, once the kernel before has finished
     const int n_items = *ws.n_chunks * H;  // below 2^31 (checked by the host)
     int item = blockIdx.x;
-    if (item >= n_items) return;
 
     // The gates of a chunk-head (padded tokens: g = beta = 0), loaded by warp 0.
     auto load_gates = [&](const int4 &e, int h, float (&g2)[2], float (&b2)[2]) {
@@ -121,25 +132,23 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
         tma_load_3d(sm + 24576, &args.tq, &bars[0], 64, h, e.y);
     };
 
-    int4 e = tab[item / H];
-    int h = (int)(item % H);
+    int4 e = make_int4(0, 0, 0, 0);
+    int h = 0;
     float g2[2] = {0.f, 0.f}, b2[2] = {0.f, 0.f};
-    if (warp == 0) load_gates(e, h, g2, b2);
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
-        mbar_init_fence();
-        issue_inputs(e, h);
-    }
-    if (warp == 0) {
-        tmem_alloc(s_tmem, kTmemCols);
-        tmem_relinquish();
+    if (item < n_items) {
+        e = tab[item / H];
+        h = item % H;
+        if (warp == 0) load_gates(e, h, g2, b2);
+        if (tid == 0) issue_inputs(e, h);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    if (item >= n_items) {  // more CTAs than items
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
     const uint32_t lane = (uint32_t)(32 * quad) << 16;
 
     for (uint32_t it = 0;; ++it) {
@@ -361,8 +370,7 @@ cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st) {
     const int64_t items = ws.max_chunks * p.H;  // an upper bound; the kernel reads the count
     if (items > INT32_MAX - 4 * (int64_t)sms) return cudaErrorInvalidValue;
     const int64_t grid = items < 3 * sms ? items : 3 * sms;  // three CTAs per SM
-    k_tc_prep<<<(unsigned)grid, kThreads, kSmemLaunch, st>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(k_tc_prep, dim3((unsigned)grid), dim3(kThreads), kSmemLaunch, st, args);
 }
 
 }  // namespace gdr

@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
         return true;
     };
 
+    pdl_trigger();
     if (warp == 0) {
         tmem_alloc(s_tmem, kTmemCols);
         tmem_relinquish();
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    pdl_wait();  // the workspace and outputs, once the kernels before have finished
 
     if (warp == 10) {
         // ------------------------------------------------------------ producer
@@ -389,8 +391,8 @@ cudaError_t tc_prescan(const Problem &p, const Workspace &ws, cudaStream_t st) {
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    k_tc_prescan<<<(unsigned)(chains < sms ? chains : sms), kThreads, kSmemLaunch, st>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(k_tc_prescan, dim3((unsigned)(chains < sms ? chains : sms)), dim3(kThreads),
+                      kSmemLaunch, st, args);
 }
 
 }  // namespace gdr
