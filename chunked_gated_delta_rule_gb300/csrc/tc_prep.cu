@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
             const int j0 = 32 * half;
             // A rows keep j < i (beta_i folded in); P rows keep j <= i.
             const int jlim = quad < 2 ? i : i + 1;
-            const float rowf = quad < 2 ? sBeta[i] : 1.f;
+            const float rowf = quad < 2 ? sBeta[i] : p.scale;
             if (sScal[2] != 0.f) {  // e^{G_i - G_j} = e^{G_i - G_last} e^{G_last - G_j}
                 const float ri = rowf * sEP[i];
 #pragma unroll
@@ -225,8 +225,6 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
                     *reinterpret_cast<float4 *>(sAT + i * kInvLd + j0 + 4 * c4) =
                         make_float4(f[4 * c4], f[4 * c4 + 1], f[4 * c4 + 2], f[4 * c4 + 3]);
             } else {  // row i of scale P
-#pragma unroll
-                for (int u = 0; u < 32; ++u) f[u] *= p.scale;
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8)
                     st_bf16x8(sm + kOffStP + sw128_off(i, j0 + 8 * c8, 64), f + 8 * c8);
