@@ -347,12 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 if (!wait(kBFull + b, gk >> 1)) { ok = false; break; }
                 tc_fence_after();  // the state written by the previous update product
                 const float gam_last = reinterpret_cast<const float *>(st + kImgVec)[kImgGamLast];
-                // h_pre -> BF16 mirror (the first product's A operand), then the
-                // FP32 state scaled by e^{G_last} for the update product.
-#pragma unroll
-                for (int hq = 0; hq < 2; ++hq) {
-                    uint32_t r0[32], r1[32];
-                    if (cc == C.s0) {  // the chain's initial state, column `row`
+                // the state before the chunk: column `row` of keys [64 hq, 64 hq + 64)
+                auto state_half = [&](int hq, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+                    if (cc == C.s0) {  // the chain's initial state
 #pragma unroll
                         for (int kk = 0; kk < 64; ++kk) {
                             const int key = 64 * hq + kk;
@@ -374,6 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         reg_fence(r0);
                         reg_fence(r1);
                     }
+                };
+                // h_pre -> BF16 mirror (the first product's A operand): the
+                // chain's critical path, so it goes first
+#pragma unroll 1
+                for (int hq = 0; hq < 2; ++hq) {
+                    uint32_t r0[32], r1[32];
+                    state_half(hq, r0, r1);
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
                         float x[8], y[8];
@@ -385,6 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         st_bf16x8(sm + kOffHm + sw128_off(row, 64 * hq + 8 * c8, 128), x);
                         st_bf16x8(sm + kOffHm + sw128_off(row, 64 * hq + 32 + 8 * c8, 128), y);
                     }
+                }
+                fence_async_smem();
+                mbar_arrive(&bars[kBMready]);
+                // then the FP32 state scaled by e^{G_last} for the update product,
+                // while the first product runs
+#pragma unroll 1
+                for (int hq = 0; hq < 2; ++hq) {
+                    uint32_t r0[32], r1[32];
+                    state_half(hq, r0, r1);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gam_last);
@@ -393,8 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                     tmem_st32(tmem + lane + kColS + 64 * hq, r0);
                     tmem_st32(tmem + lane + kColS + 64 * hq + 32, r1);
                 }
-                fence_async_smem();
-                mbar_arrive(&bars[kBMready]);
                 if (!wait(kBAdone, gk)) { ok = false; break; }
                 tc_fence_after();
                 {  // v_new^T = U^T - h^T W^T

@@ -254,11 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                 tc_fence_after();  // the state written by the previous update
                 const float *vec = reinterpret_cast<const float *>(st + kImgVec);
                 const float gam_last = vec[kImgGamLast];
-                // the state before the chunk -> BF16 mirror in TMEM (two keys per
-                // column); the FP32 state scaled by e^{G_last}
-#pragma unroll
-                for (int hq = 0; hq < 2; ++hq) {
-                    uint32_t r0[32], r1[32];
+                // the state before the chunk, column `row` of keys [64 hq, 64 hq + 64)
+                auto state_half = [&](int hq, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
                     if (cc == C.s0) {
 #pragma unroll
                         for (int kk = 0; kk < 32; ++kk) {
@@ -272,7 +269,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                         reg_fence(r0);
                         reg_fence(r1);
                     }
-                    uint32_t m[32];
+                };
+                // -> BF16 mirror in TMEM (two keys per column): the chain's
+                // critical path, so it goes first
+#pragma unroll 1
+                for (int hq = 0; hq < 2; ++hq) {
+                    uint32_t r0[32], r1[32], m[32];
+                    state_half(hq, r0, r1);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         m[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
@@ -280,6 +283,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                             pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
                     }
                     tmem_st32(tmem + lane + cM + 32 * hq, m);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars[kPMready + path]);
+                // then the FP32 state scaled by e^{G_last}, while h^T W^T runs
+#pragma unroll 1
+                for (int hq = 0; hq < 2; ++hq) {
+                    uint32_t r0[32], r1[32];
+                    state_half(hq, r0, r1);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gam_last);
@@ -288,9 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                     tmem_st32(tmem + lane + cS + 64 * hq, r0);
                     tmem_st32(tmem + lane + cS + 64 * hq + 32, r1);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&bars[kPMready + path]);
                 // half of K~ = diag(e^{G_last - G}) K in place (rows past the
                 // sequence end, which belong to the next one, become zero)
                 const float *dec = reinterpret_cast<const float *>(st + kImgDec);
@@ -343,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                     }
                 }
                 fence_async_smem();
+                tmem_wait_st();  // the scaled state, before the update product
                 tc_fence_before();
                 mbar_arrive(&bars[kPVready + path]);
                 if (!wait(kPHdone + path, gk)) { ok = false; break; }
