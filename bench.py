@@ -233,7 +233,7 @@ def algorithmic_bytes(kernel, x, c):
 
 # The translation unit each kernel is compiled from (plus every shared header).
 KERNEL_SOURCES = {"tc_prep": "tc_prep.cu", "tc_chain": "tc_chain.cu", "tc_gla": "tc_gla.cu",
-                  "tc_prescan": "tc_prescan.cu",
+                  "tc_prescan": "tc_prescan.cu", "recurrent": "recurrent.cu",
                   "compose": "compose.cu", "simt": "simt_path.cu"}
 
 
@@ -529,10 +529,131 @@ def run_gdr(args):
         dist.destroy_process_group()
 
 
+def run_decode(args):
+    """gdr_recurrent_fwd on a decode workload: every sequence one token,
+    continuing a state held at a seeded row of a pool twice the batch."""
+    import torch
+    import chunked_gated_delta_rule_gb300 as pkg
+    from chunked_gated_delta_rule_gb300 import synthetic
+
+    rank, local, world = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synthetic.WORKLOADS[args.workload]
+    x = synthetic.make_inputs(w)
+    pool_h, idx_h = synthetic.make_state_pool(x, 2 * x["N"])
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+    pool, idx = pool_h.to(dev), idx_h.to(dev)
+    o = torch.empty_like(d["v"])
+    args_t = (d["q"], d["k"], d["v"], d["g"], d["beta"])
+    kw = dict(cu_seqlens=d["cu_seqlens"], state=pool, state_indices=idx, o=o)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        pkg.gdr_recurrent_fwd(*args_t, **kw)
+    torch.cuda.synchronize()
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_index_for_smi()) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if hasattr(torch.cuda, "_sleep"):  # outside the timed region, as in run_gdr
+        torch.cuda._sleep(4_000_000)
+    pkg.gdr_recurrent_fwd(*args_t, **kw)
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        pkg.gdr_recurrent_fwd(*args_t, **kw)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = max_over_ranks(statistics.mean(step_ms), world)
+
+    H, Kd, V = x["H"], x["K"], x["V"]
+    es = 2 if x["dtype"] == "bf16" else 4
+    tokens = int(x["cu_seqlens"][-1]) if x["cu_seqlens"] is not None else x["B"] * x["T"]
+    ab = x["N"] * H * 2 * Kd * V * 4 + tokens * H * ((2 * Kd + V) * es + 8 + V * es)
+    peaks = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    achieved = ab / (ms * 1e-3) / 1e9
+    roofline = {"kernel": "recurrent", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic_record("recurrent", args.workload),
+                "algorithmic_bytes_per_launch": ab, "avg_launch_ms": ms,
+                "timing": "CUDA events around each call (one kernel launch) on its stream",
+                "peak_source": peaks["source"] + " (hbm_gbs, copy bandwidth)"}
+
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()}
+        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        names = ("q", "k", "v", "g", "beta", "cu_seqlens")
+
+        def e2e_step():
+            for nme in names:
+                if pin[nme] is not None:
+                    d[nme].copy_(pin[nme], non_blocking=True)
+            pkg.gdr_recurrent_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                  cu_seqlens=d["cu_seqlens"], state=pool, state_indices=idx, o=o)
+            o_h.copy_(o, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        ke = max(3, min(K, 50))
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world)
+        h2d = sum(pin[nme].numel() * pin[nme].element_size() for nme in names
+                  if pin[nme] is not None)
+        e2e = {"value": world * tokens / (e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": o_h.numel() * o_h.element_size(),
+               "ms_per_step": e_ms, "steps": ke,
+               "api": "gdr_recurrent_fwd, inputs and o through pinned host buffers, "
+                      "the state pool resident on the device"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x, args.cpu_seconds)
+    if rank == 0:
+        line = {"metric": METRIC, "value": world * tokens / (ms * 1e-3), "unit": UNIT,
+                "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic (seeded; shapes and distributions of the workload)",
+                "config": {"workload": args.workload, "tokens": tokens, "n_seqs": x["N"],
+                           "H": H, "K": Kd, "V": V, "input_dtype": x["dtype"],
+                           "beta_free": x["beta"] is None, "state_pool_rows": 2 * x["N"],
+                           "l2": "flushed between timed steps (256 MiB write, untimed)",
+                           "entry_point": "gdr_recurrent_fwd"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K,
+                "clocks": clocks,
+                "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
+                            "p10": sorted(step_ms)[len(step_ms) // 10],
+                            "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]}}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload.startswith("decode"):
+        run_decode(args)
     else:
         run_gdr(args)
 

@@ -44,7 +44,7 @@ SELFTEST_EXPORTS = ("gdr_selftest_umma", "gdr_selftest_tma", "gdr_selftest_inver
 
 # Every symbol include/gdr.h declares.
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_host", "gdr_chunk_fwd_noalloc",
-           "gdr_workspace_size", "gdr_plan_query", "gdr_kernel_name", "gdr_error_string",
+           "gdr_workspace_size", "gdr_plan_query", "gdr_recurrent_fwd", "gdr_kernel_name", "gdr_error_string",
            "gdr_version")
 
 _lib = None
@@ -79,6 +79,9 @@ def load_library():
         lib.gdr_chunk_fwd_host.restype = ctypes.c_int
         lib.gdr_chunk_fwd_noalloc.argtypes = fwd_args + [vp]
         lib.gdr_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.gdr_recurrent_fwd.argtypes = [dims_p, vp, vp, vp, vp, vp, i32p, vp, ctypes.c_int64,
+                                          i32p, vp, vp, vp]
+        lib.gdr_recurrent_fwd.restype = ctypes.c_int
         lib.gdr_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.c_int]
         lib.gdr_workspace_size.restype = ctypes.c_size_t
         lib.gdr_plan_query.argtypes = [dims_p, ctypes.c_int, ctypes.c_int,
@@ -220,6 +223,41 @@ def gdr_chunk_fwd(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments
     if rc != 0:
         raise GdrError(rc)
     return o, ht
+
+
+def gdr_recurrent_fwd(q, k, v, g, beta=None, cu_seqlens=None, *, state, state_indices=None,
+                      o=None, status=None, stream=None):
+    """Per-token recurrence from rows of the state pool ``state`` ([P, H, K,
+    V] float32, updated in place): sequence n starts from row
+    ``state_indices[n]`` (row n if None) and writes its final state back
+    there.  Returns ``o``.  Work is enqueued on ``stream`` and not
+    synchronised."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr_recurrent_fwd takes CUDA tensors")
+    _check("q", q, None, dev)
+    for name, t in (("k", k), ("v", v)):
+        _check(name, t, q.dtype, dev)
+    _check("g", g, torch.float32, dev)
+    _check("beta", beta, torch.float32, dev)
+    _check("cu_seqlens", cu_seqlens, torch.int32, dev)
+    _check("state", state, torch.float32, dev)
+    _check("state_indices", state_indices, torch.int32, dev)
+    dims = _dims_of(q, v, cu_seqlens)
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _check("o", o, q.dtype, dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdr_recurrent_fwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(cu_seqlens), _ptr(state),
+                                   ctypes.c_int64(state.shape[0]), _ptr(state_indices), _ptr(o),
+                                   _ptr(status), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise GdrError(rc)
+    return o
 
 
 def gdr_chunk_fwd_host(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments=0,

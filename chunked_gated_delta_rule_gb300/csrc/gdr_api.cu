@@ -298,8 +298,32 @@ const char *gdr_error_string(int code) {
     case GDR_ERR_TIMEOUT: return "device-side bounded wait expired";
     case GDR_ERR_SEQLENS: return "malformed cu_seqlens";
     case GDR_ERR_WORKSPACE: return "workspace too small";
+    case GDR_ERR_INDEX: return "state index out of range";
     default: return "unknown error code";
     }
+}
+
+int gdr_recurrent_fwd(const gdr_dims *dims, const void *q, const void *k, const void *v,
+                      const float *g, const float *beta, const int32_t *cu_seqlens, float *state,
+                      int64_t n_states, const int32_t *state_indices, void *o, int32_t *status,
+                      gdr_stream_t stream) {
+    int rc = validate_dims(dims);
+    if (rc != GDR_OK) return rc;
+    if (!q || !k || !v || !g || !o || !state || n_states < 1) return GDR_ERR_INVALID;
+    if ((cu_seqlens != nullptr) != is_varlen(*dims)) return GDR_ERR_INVALID;
+    if (!state_indices && n_states < n_seqs(*dims)) return GDR_ERR_INVALID;
+    if (n_seqs(*dims) > 65535) return GDR_ERR_UNSUPPORTED;  // one grid row per sequence
+    Problem p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.cu = cu_seqlens;
+    p.o = o;
+    p.B = dims->B; p.T = dims->T; p.H = dims->H; p.K = dims->K; p.V = dims->V;
+    p.N = n_seqs(*dims);
+    p.dtype = dims->dtype;
+    p.scale = 1.0f / std::sqrt((float)dims->K);
+    p.status = status;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return recurrent_fwd(p, state, n_states, state_indices, st) == cudaSuccess ? GDR_OK
+                                                                                 : GDR_ERR_CUDA;
 }
 
 int gdr_plan_query(const gdr_dims *dims, int beta_free, int n_segments, gdr_plan *out) {

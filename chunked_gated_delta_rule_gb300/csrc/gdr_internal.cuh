@@ -165,6 +165,9 @@ cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st);
 // mode 0: serial scan + output (h0 -> ht); 1: segment pre-scan (c_s and M_s
 // chains); 2: segment output pass from the composed segment states.
 cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream_t st);
+// The per-token recurrence from (and back into) rows of a state pool.
+cudaError_t recurrent_fwd(const Problem &p, float *state, int64_t n_states,
+                          const int32_t *state_idx, cudaStream_t st);
 // Segment pre-scan with both summaries (c_s and M_s) of a chain in one CTA.
 // tc_chain's mode 1 runs them as separate chains, which is faster while both
 // kinds fit one wave (prescan_split_kinds).

@@ -66,6 +66,10 @@ WORKLOADS = {
     # Beta-free (pure gated linear attention) geometry, K=256, V=512.
     "gla_k256_v512_bf16": Workload("gla_k256_v512_bf16", 2, 8192, 4, 256, 512,
                                    "bf16", delta=False, with_h0=True),
+    # Decode step: 256 sequences of one token each, every one continuing a
+    # state held in a pool (gdr_recurrent_fwd).
+    "decode_bf16": Workload("decode_bf16", 1, 0, 16, 128, 128, "bf16", n_seqs=256,
+                            len_lo=1, len_hi=1, with_h0=True),
 }
 
 
@@ -120,3 +124,18 @@ def make_inputs(w: Workload, lengths: Optional[list] = None, T: Optional[int] = 
 def small(w: Workload, **overrides) -> Workload:
     """A copy of a workload with some fields replaced (reduced-size cases)."""
     return dataclasses.replace(w, **overrides)
+
+
+def make_state_pool(x: dict, n_states: int, seed: int = 1):
+    """A pool of ``n_states`` states [P, H, K, V] holding each sequence's h0
+    at a distinct seeded row, the other rows random; returns ``(pool,
+    indices)`` with int32 ``indices[n]`` = the row of sequence n."""
+    gen = torch.Generator().manual_seed(seed)
+    N, H, K, V = x["N"], x["H"], x["K"], x["V"]
+    if n_states < N:
+        raise ValueError("the pool needs a row per sequence")
+    idx = torch.randperm(n_states, generator=gen)[:N].to(torch.int32)
+    pool = 0.1 * torch.randn(n_states, H, K, V, generator=gen)
+    if x["h0"] is not None:
+        pool[idx.long()] = x["h0"]
+    return pool, idx

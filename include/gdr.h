@@ -73,7 +73,8 @@ enum gdr_status {
     GDR_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed      */
     GDR_ERR_TIMEOUT = -4,      /* device status: a bounded wait expired     */
     GDR_ERR_SEQLENS = -5,      /* device status: cu_seqlens malformed       */
-    GDR_ERR_WORKSPACE = -6     /* caller workspace too small                */
+    GDR_ERR_WORKSPACE = -6,    /* caller workspace too small                */
+    GDR_ERR_INDEX = -7         /* device status: a state index out of range */
 };
 
 /* Problem size.  Dense layout: N = 0 (there are B sequences of T tokens).
@@ -173,6 +174,31 @@ int gdr_chunk_fwd_noalloc(const gdr_dims *dims, const void *q, const void *k,
                           const void *v, const float *g, const float *beta,
                           const int32_t *cu_seqlens, const float *h0, void *o,
                           float *ht, int n_segments, gdr_stream_t stream);
+
+/*
+ * gdr_recurrent_fwd -- the per-token recurrence itself (the formula at the
+ * top of the file, token by token), for serving: a decode step or a few
+ * tokens a sequence, where a 64-token chunk would be mostly padding (the
+ * "question rows" with states of their own, Kev PR #259 "Not covered").
+ * Every sequence takes its initial state from a row of a caller-owned pool,
+ * runs its tokens in order and writes its final state back into that row.
+ *   dims, q, k, v, g, beta, cu_seqlens, o   as for gdr_chunk_fwd (device
+ *                 pointers; beta NULL selects the beta-free mode).
+ *   state         [n_states, H, K, V] float32 pool of states h = S^T, read
+ *                 and written in place (device).
+ *   state_indices [Nseq] int32 pool row of each sequence (device), or NULL
+ *                 for row n.  The rows of one call must be distinct.
+ *   status        device int32 word or NULL: an index outside [0, n_states)
+ *                 skips its sequence and sets GDR_ERR_INDEX there (malformed
+ *                 cu_seqlens: GDR_ERR_SEQLENS); the caller zeroes it.
+ * FP32 arithmetic for both input types; scale = 1/sqrt(K).  Work is enqueued
+ * on `stream`; no allocation, no synchronisation.
+ */
+int gdr_recurrent_fwd(const gdr_dims *dims, const void *q, const void *k,
+                      const void *v, const float *g, const float *beta,
+                      const int32_t *cu_seqlens, float *state, int64_t n_states,
+                      const int32_t *state_indices, void *o, int32_t *status,
+                      gdr_stream_t stream);
 
 /* Bytes of device scratch gdr_chunk_fwd_ex needs for this problem
  * (beta_free != 0 for the beta-free mode).  0 on invalid arguments. */

@@ -79,6 +79,23 @@ def test_argument_checks_reject_before_any_gpu_work(lib):
     assert _fwd(lib, ok, opt=bad_scale) == -1
 
 
+def _rec(lib, dims, q=1, state=1, n_states=4, idx=None, cu=None):
+    p = lambda x: None if x is None else ctypes.c_void_p(0x1000 * x)
+    return lib.gdr_recurrent_fwd(ctypes.byref(dims), p(q), p(1), p(1), p(1), None, p(cu),
+                                 p(state), ctypes.c_int64(n_states), p(idx), p(1), None, None)
+
+
+def test_recurrent_argument_checks_reject_before_any_gpu_work(lib):
+    ok = api.make_dims(4, 1, 2, 64, 64)
+    assert _rec(lib, ok, q=None) == -1
+    assert _rec(lib, ok, state=None) == -1
+    assert _rec(lib, ok, n_states=0) == -1
+    assert _rec(lib, ok, n_states=3) == -1        # row n for 4 sequences needs 4 rows
+    assert _rec(lib, api.make_dims(4, 1, 2, 60, 64)) == -2
+    assert _rec(lib, api.make_dims(1, 8, 2, 64, 64, N=3)) == -1  # varlen needs cu_seqlens
+    assert pkg.gdr_error_string(-7) == "state index out of range"
+
+
 def test_plan_query_is_deterministic_and_valid():
     for dims in [(1, 256, 2, 64, 64, 0, 0), (1, 10456, 16, 128, 128, 32, 1),
                  (1, 16384, 16, 128, 128, 0, 1), (1, 65536, 1, 128, 128, 0, 1),
