@@ -122,19 +122,39 @@ def _dtype_code(t: torch.dtype) -> int:
     raise TypeError(f"unsupported dtype {t}: q, k, v must be float32 or bfloat16")
 
 
-def make_dims(B, T, H, K, V, N=0, dtype=GDR_BF16) -> gdr_dims:
-    return gdr_dims(B, T, H, K, V, N, dtype, 0)
+GDR_SEQLENS_I64 = 1  # gdr_dims.flags: cu_seqlens holds int64 offsets
+GDR_STATE_VK = 2     # gdr_dims.flags: h0 / ht / state pool are S [.., V, K]
+
+
+def make_dims(B, T, H, K, V, N=0, dtype=GDR_BF16, flags=0) -> gdr_dims:
+    return gdr_dims(B, T, H, K, V, N, dtype, flags)
 
 
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _dims_of(q, v, cu_seqlens) -> gdr_dims:
+def _dims_of(q, v, cu_seqlens, state_layout="kv") -> gdr_dims:
+    """Sizes and flags: int64 cu_seqlens sets GDR_SEQLENS_I64; state_layout
+    "vk" (states as S, [.., V, K]) sets GDR_STATE_VK."""
     B, T, H, K = q.shape
     V = v.shape[-1]
     N = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
-    return make_dims(B, T, H, K, V, N, _dtype_code(q.dtype))
+    if state_layout not in ("kv", "vk"):
+        raise ValueError(f"state_layout must be 'kv' or 'vk', got {state_layout!r}")
+    flags = (GDR_SEQLENS_I64 if cu_seqlens is not None and cu_seqlens.dtype == torch.int64
+             else 0) | (GDR_STATE_VK if state_layout == "vk" else 0)
+    return make_dims(B, T, H, K, V, N, _dtype_code(q.dtype), flags)
+
+
+def _state_dims(dims, state_layout):
+    return (dims.V, dims.K) if state_layout == "vk" else (dims.K, dims.V)
+
+
+def _check_cu(t, device=None):
+    if t is not None and t.dtype not in (torch.int32, torch.int64):
+        raise TypeError(f"cu_seqlens must be int32 or int64, got {t.dtype}")
+    _check("cu_seqlens", t, None, device)
 
 
 def _check(name, t, dtype, device=None):
@@ -178,6 +198,7 @@ class LaunchTimer:
 
 
 def gdr_chunk_fwd(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments=0,
+                  state_layout="kv",
                   output_final_state=True, o=None, ht=None, scale=0.0, force_path=0,
                   force_bv=0, workspace=None, status=None, stream=None, timer=None):
     """Forward pass on CUDA tensors (layouts of include/gdr.h).  Returns
@@ -194,14 +215,15 @@ def gdr_chunk_fwd(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments
         _check(name, t, q.dtype, dev)
     _check("g", g, torch.float32, dev)
     _check("beta", beta, torch.float32, dev)
-    _check("cu_seqlens", cu_seqlens, torch.int32, dev)
+    _check_cu(cu_seqlens, dev)
     _check("h0", h0, torch.float32, dev)
-    dims = _dims_of(q, v, cu_seqlens)
+    dims = _dims_of(q, v, cu_seqlens, state_layout)
     nseq = dims.N if dims.N else dims.B
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
     if ht is None and output_final_state:
-        ht = torch.empty(nseq, dims.H, dims.K, dims.V, dtype=torch.float32, device=dev)
+        ht = torch.empty(nseq, dims.H, *_state_dims(dims, state_layout), dtype=torch.float32,
+                         device=dev)
     _check("o", o, q.dtype, dev)
     _check("ht", ht, torch.float32, dev)
     opt = gdr_options(float(scale), int(force_path), int(force_bv),
@@ -226,6 +248,7 @@ def gdr_chunk_fwd(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments
 
 
 def gdr_recurrent_fwd(q, k, v, g, beta=None, cu_seqlens=None, *, state, state_indices=None,
+                      state_layout="kv",
                       o=None, status=None, stream=None):
     """Per-token recurrence from rows of the state pool ``state`` ([P, H, K,
     V] float32, updated in place): sequence n starts from row
@@ -241,10 +264,10 @@ def gdr_recurrent_fwd(q, k, v, g, beta=None, cu_seqlens=None, *, state, state_in
         _check(name, t, q.dtype, dev)
     _check("g", g, torch.float32, dev)
     _check("beta", beta, torch.float32, dev)
-    _check("cu_seqlens", cu_seqlens, torch.int32, dev)
+    _check_cu(cu_seqlens, dev)
     _check("state", state, torch.float32, dev)
     _check("state_indices", state_indices, torch.int32, dev)
-    dims = _dims_of(q, v, cu_seqlens)
+    dims = _dims_of(q, v, cu_seqlens, state_layout)
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
     _check("o", o, q.dtype, dev)
@@ -261,6 +284,7 @@ def gdr_recurrent_fwd(q, k, v, g, beta=None, cu_seqlens=None, *, state, state_in
 
 
 def gdr_chunk_fwd_host(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments=0,
+                       state_layout="kv",
                        output_final_state=True, o=None, ht=None, stream=None):
     """Forward pass on HOST (CPU) tensors through ``gdr_chunk_fwd_host``: the
     library copies inputs in, runs, copies o / ht out and synchronises.
@@ -274,14 +298,14 @@ def gdr_chunk_fwd_host(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_seg
     _check("v", v, q.dtype)
     _check("g", g, torch.float32)
     _check("beta", beta, torch.float32)
-    _check("cu_seqlens", cu_seqlens, torch.int32)
+    _check_cu(cu_seqlens)
     _check("h0", h0, torch.float32)
-    dims = _dims_of(q, v, cu_seqlens)
+    dims = _dims_of(q, v, cu_seqlens, state_layout)
     nseq = dims.N if dims.N else dims.B
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype)
     if ht is None and output_final_state:
-        ht = torch.empty(nseq, dims.H, dims.K, dims.V, dtype=torch.float32)
+        ht = torch.empty(nseq, dims.H, *_state_dims(dims, state_layout), dtype=torch.float32)
     if stream is None:
         stream = torch.cuda.current_stream()
     rc = lib.gdr_chunk_fwd_host(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
@@ -296,6 +320,7 @@ NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def gdr_chunk_fwd_noalloc(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments=0,
+                          state_layout="kv",
                           output_final_state=True, o=None, ht=None, stream=None):
     """Forward pass through ``gdr_chunk_fwd_noalloc``: the library uses a
     fixed 64 MiB device array as scratch and allocates nothing, for callers
@@ -313,14 +338,15 @@ def gdr_chunk_fwd_noalloc(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_
         _check(name, t, q.dtype, dev)
     _check("g", g, torch.float32, dev)
     _check("beta", beta, torch.float32, dev)
-    _check("cu_seqlens", cu_seqlens, torch.int32, dev)
+    _check_cu(cu_seqlens, dev)
     _check("h0", h0, torch.float32, dev)
-    dims = _dims_of(q, v, cu_seqlens)
+    dims = _dims_of(q, v, cu_seqlens, state_layout)
     nseq = dims.N if dims.N else dims.B
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
     if ht is None and output_final_state:
-        ht = torch.empty(nseq, dims.H, dims.K, dims.V, dtype=torch.float32, device=dev)
+        ht = torch.empty(nseq, dims.H, *_state_dims(dims, state_layout), dtype=torch.float32,
+                         device=dev)
     _check("o", o, q.dtype, dev)
     _check("ht", ht, torch.float32, dev)
     if stream is None:

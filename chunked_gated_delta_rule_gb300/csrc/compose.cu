@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Wo
     const int64_t sbase = (n * H + h) * (int64_t)S;
     for (int idx = tid; idx < K * CC; idx += kComposeThreads) {
         const int key = idx / CC, c = idx - key * CC;
-        sH0[idx] = p.h0 ? p.h0[((n * H + h) * K + key) * (int64_t)V + col0 + c] : 0.f;
+        sH0[idx] = p.h0 ? p.h0[state_off(p, n * H + h, key, col0 + c)] : 0.f;
     }
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Wo
         const float *fin = (nseg & 1) ? sH1 : sH0;
         for (int idx = tid; idx < K * CC; idx += kComposeThreads) {
             const int key = idx / CC, c = idx - key * CC;
-            p.ht[((n * H + h) * K + key) * (int64_t)V + col0 + c] = fin[idx];
+            p.ht[state_off(p, n * H + h, key, col0 + c)] = fin[idx];
         }
     }
 }
@@ -181,13 +181,14 @@ __global__ void __launch_bounds__(256) k_compose_scalar(Problem p, Workspace ws)
     const float *__restrict__ C = ws.segC + nh * S * kv + e;
     float *__restrict__ Hs = ws.segH + nh * S * kv + e;
     const float *__restrict__ D = ws.segD + nh * S;
-    float h = p.h0 ? p.h0[idx] : 0.f;
+    const int64_t sidx = state_off(p, nh, e / p.V, e % p.V);  // this element in h0 / ht
+    float h = p.h0 ? p.h0[sidx] : 0.f;
     for (int s = 0; s < nseg; ++s) {
         const float c = C[s * kv];
         Hs[s * kv] = h;
         h = fmaf(D[s], h, c);
     }
-    if (p.ht) p.ht[idx] = h;
+    if (p.ht) p.ht[sidx] = h;
 }
 
 }  // namespace

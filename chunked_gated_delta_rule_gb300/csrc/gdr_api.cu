@@ -30,6 +30,7 @@ int validate_dims(const gdr_dims *d) {
     if (d->B < 1 || d->T < 0 || d->H < 1 || d->K < 1 || d->V < 1 || d->N < 0)
         return GDR_ERR_INVALID;
     if (d->dtype != GDR_F32 && d->dtype != GDR_BF16) return GDR_ERR_INVALID;
+    if (d->flags & ~(GDR_SEQLENS_I64 | GDR_STATE_VK)) return GDR_ERR_INVALID;
     if (is_varlen(*d) && d->B != 1) return GDR_ERR_INVALID;
     if (d->K % 16 || d->V % 16) return GDR_ERR_UNSUPPORTED;
     if (d->K > kMaxK || d->V > kMaxV) return GDR_ERR_UNSUPPORTED;
@@ -314,7 +315,10 @@ int gdr_recurrent_fwd(const gdr_dims *dims, const void *q, const void *k, const 
     if (!state_indices && n_states < n_seqs(*dims)) return GDR_ERR_INVALID;
     if (n_seqs(*dims) > 65535) return GDR_ERR_UNSUPPORTED;  // one grid row per sequence
     Problem p{};
-    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.cu = cu_seqlens;
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    if (dims->flags & GDR_SEQLENS_I64) p.cu64 = reinterpret_cast<const int64_t *>(cu_seqlens);
+    else p.cu = cu_seqlens;
+    p.state_vk = (dims->flags & GDR_STATE_VK) != 0;
     p.o = o;
     p.B = dims->B; p.T = dims->T; p.H = dims->H; p.K = dims->K; p.V = dims->V;
     p.N = n_seqs(*dims);
@@ -356,7 +360,10 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Problem p{};
-    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.cu = cu_seqlens;
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    if (dims->flags & GDR_SEQLENS_I64) p.cu64 = reinterpret_cast<const int64_t *>(cu_seqlens);
+    else p.cu = cu_seqlens;
+    p.state_vk = (dims->flags & GDR_STATE_VK) != 0;
     p.h0 = h0; p.o = o; p.ht = ht;
     p.B = dims->B; p.T = dims->T; p.H = dims->H; p.K = dims->K; p.V = dims->V;
     p.N = n_seqs(*dims);
@@ -420,7 +427,7 @@ int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k, const
     const size_t ntok = (size_t)dims->B * (size_t)dims->T * (size_t)dims->H;
     const size_t ns = (size_t)n_seqs(*dims);
     const size_t bq = ntok * dims->K * es, bv = ntok * dims->V * es, bg = ntok * 4;
-    const size_t bcu = cu_seqlens ? (ns + 1) * 4 : 0;
+    const size_t bcu = cu_seqlens ? (ns + 1) * ((dims->flags & GDR_SEQLENS_I64) ? 8 : 4) : 0;
     const size_t bh = ns * dims->H * dims->K * dims->V * 4;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes); return at; };

@@ -50,7 +50,8 @@ constexpr int kMaxSegments = 64; // largest segment count
 struct Problem {
     const void *q, *k, *v;      // [B,T,H,K] / [B,T,H,V], dtype
     const float *g, *beta;      // [B,T,H]; beta == nullptr => beta-free
-    const int32_t *cu;          // [N+1] or nullptr (dense)
+    const int32_t *cu;          // [N+1] or nullptr (dense); int32 offsets
+    const int64_t *cu64;        // the same table as int64 (GDR_SEQLENS_I64), or nullptr
     const float *h0;            // [N,H,K,V] or nullptr
     void *o;                    // [B,T,H,V], dtype
     float *ht;                  // [N,H,K,V] or nullptr
@@ -58,7 +59,28 @@ struct Problem {
     int dtype;                  // GDR_F32 | GDR_BF16
     float scale;
     int32_t *status;            // device status word or nullptr
+    int state_vk;               // h0 / ht laid out [N,H,V,K] (S) instead of [N,H,K,V]
 };
+
+// cu_seqlens[i] in either width; a sequence's first token and end.
+__host__ __device__ __forceinline__ int64_t seq_bound(const Problem &p, int64_t i) {
+    return p.cu64 ? p.cu64[i] : (int64_t)p.cu[i];
+}
+__host__ __device__ __forceinline__ bool is_varlen_p(const Problem &p) {
+    return p.cu != nullptr || p.cu64 != nullptr;
+}
+__host__ __device__ __forceinline__ int64_t seq_start(const Problem &p, int64_t n) {
+    return is_varlen_p(p) ? seq_bound(p, n) : n * p.T;
+}
+__host__ __device__ __forceinline__ int64_t seq_end(const Problem &p, int64_t n) {
+    return is_varlen_p(p) ? seq_bound(p, n + 1) : (n + 1) * p.T;
+}
+// Offset of element (key, v) of the state of (sequence, head) nh = n H + h
+// in h0 / ht (and the recurrent pool): h = S^T [K][V], or S [V][K].
+__host__ __device__ __forceinline__ int64_t state_off(const Problem &p, int64_t nh, int64_t key,
+                                                      int64_t v) {
+    return p.state_vk ? (nh * p.V + v) * p.K + key : (nh * p.K + key) * p.V + v;
+}
 
 // Scratch carved out of one device allocation (offsets fixed by the host).
 struct Workspace {

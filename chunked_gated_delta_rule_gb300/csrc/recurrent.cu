@@ -55,8 +55,8 @@ __global__ void __launch_bounds__(kRThreads, RPW <= 16 ? 3 : 2)
     __shared__ float sk[kMaxK], sq[kMaxK], sv[kRCols], sg[2];
     __shared__ float sred[2][8][kRCols];
 
-    const int64_t t0 = p.cu ? (int64_t)p.cu[n] : n * p.T;
-    const int64_t t1 = p.cu ? (int64_t)p.cu[n + 1] : (n + 1) * p.T;
+    const int64_t t0 = seq_start(p, n);
+    const int64_t t1 = seq_end(p, n);
     if (t1 < t0) {  // malformed cu_seqlens: nothing for this sequence
         if (tid == 0 && blockIdx.x == 0 && h == 0 && p.status)
             atomicCAS(p.status, 0, (int32_t)GDR_ERR_SEQLENS);
@@ -68,11 +68,11 @@ __global__ void __launch_bounds__(kRThreads, RPW <= 16 ? 3 : 2)
             atomicCAS(p.status, 0, (int32_t)GDR_ERR_INDEX);
         return;
     }
-    float *hs = state + ((row_id * H + h) * (int64_t)K) * V;
+    // element (key, col) of the pool row's state for head h (either layout)
+    auto at = [&](int key) -> int64_t { return state_off(p, row_id * H + h, key, col); };
     float hr[RPW];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r)
-        hr[r] = (live && r0 + r < K) ? hs[(int64_t)(r0 + r) * V + col] : 0.f;
+    for (int r = 0; r < RPW; ++r) hr[r] = (live && r0 + r < K) ? state[at(r0 + r)] : 0.f;
 
     const bool delta = p.beta != nullptr;
     for (int64_t t = t0; t < t1; ++t) {
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kRThreads, RPW <= 16 ? 3 : 2)
     }
 #pragma unroll
     for (int r = 0; r < RPW; ++r)
-        if (live && r0 + r < K) hs[(int64_t)(r0 + r) * V + col] = hr[r];
+        if (live && r0 + r < K) state[at(r0 + r)] = hr[r];
 }
 
 template <typename Tin>

@@ -56,8 +56,7 @@ constexpr int kBuckets = 128;
 
 __device__ __forceinline__ int chunk_bucket(int c) { return c < kBuckets - 1 ? c : kBuckets - 1; }
 
-__global__ void __launch_bounds__(kThreads) k_chunk_table(const int32_t *__restrict__ cu,
-                                                          int64_t N, int64_t T,
+__global__ void __launch_bounds__(kThreads) k_chunk_table(const Problem p, int64_t N, int64_t T,
                                                           int64_t max_chunks,
                                                           int32_t *__restrict__ tab,
                                                           int32_t *__restrict__ seq_chunk0,
@@ -74,15 +73,15 @@ __global__ void __launch_bounds__(kThreads) k_chunk_table(const int32_t *__restr
     pdl_trigger();  // the first kernel of a call: launched in stream order, it waits for nothing
     for (int b = tid; b < kBuckets; b += kThreads) s_hist[b] = 0;
     if (tid < 3) n_chunks[1 + tid] = 0;
-    if (tid == 0) s_bad = (cu && (cu[0] != 0 || cu[N] != T)) ? 1 : 0;
+    if (tid == 0) s_bad = (is_varlen_p(p) && (seq_bound(p, 0) != 0 || seq_bound(p, N) != T)) ? 1 : 0;
     __syncthreads();
     // this thread's run of sequences, their chunk counts and the histogram
     const int64_t per = (N + kThreads - 1) / kThreads;
     const int64_t lo = min(N, (int64_t)tid * per), hi = min(N, lo + per);
     long long local = 0;
     for (int64_t n = lo; n < hi; ++n) {
-        const int64_t a = cu ? cu[n] : n * T;
-        const int64_t len = (cu ? cu[n + 1] : (n + 1) * T) - a;
+        const int64_t a = seq_start(p, n);
+        const int64_t len = seq_end(p, n) - a;
         if (len < 0) s_bad = 1;
         const int64_t c = len < 0 ? 0 : (len + kChunk - 1) / kChunk;
         const int32_t cc = (int32_t)(c <= max_chunks ? c : max_chunks + 1);
@@ -153,8 +152,8 @@ __global__ void __launch_bounds__(kThreads) k_chunk_table(const int32_t *__restr
     // one warp per sequence, its lanes over the sequence's chunks
     const int nwarps = kThreads >> 5;
     for (int64_t n = warp; n < N; n += nwarps) {
-        const int64_t a = cu ? cu[n] : n * T;
-        const int64_t len = (cu ? cu[n + 1] : (n + 1) * T) - a;
+        const int64_t a = seq_start(p, n);
+        const int64_t len = seq_end(p, n) - a;
         const int32_t first = c0[n];
         const int32_t cnt = c0[n + 1] - first;
         for (int32_t c = lane; c < cnt; c += 32) {
@@ -329,7 +328,7 @@ k_scan(Problem p, Workspace ws, int mode) {
         const int key = idx / BV, c = idx - key * BV;
         float x = 0.f;
         if (mode == 0) {
-            if (p.h0) x = p.h0[((n * H + h) * K + key) * (int64_t)V + col0 + c];
+            if (p.h0) x = p.h0[state_off(p, n * H + h, key, col0 + c)];
         } else if (mode == 2) {
             x = ws.segH[(seg_base * K + key) * V + col0 + c];
         } else if (trans) {
@@ -399,7 +398,7 @@ k_scan(Problem p, Workspace ws, int mode) {
         if (p.ht) {
             for (int idx = tid; idx < K * BV; idx += kThreads) {
                 const int key = idx / BV, c = idx - key * BV;
-                p.ht[((n * H + h) * K + key) * (int64_t)V + col0 + c] = hs[key * ldh + c];
+                p.ht[state_off(p, n * H + h, key, col0 + c)] = hs[key * ldh + c];
             }
         }
     } else if (mode == 1) {
@@ -441,7 +440,7 @@ k_compose(Problem p, Workspace ws) {
     const int nseg = per ? (nc + per - 1) / per : 0;
     for (int idx = tid; idx < K * BV; idx += kThreads) {
         const int key = idx / BV, c = idx - key * BV;
-        hs[key * ldh + c] = p.h0 ? p.h0[((n * H + h) * K + key) * (int64_t)V + col0 + c] : 0.f;
+        hs[key * ldh + c] = p.h0 ? p.h0[state_off(p, n * H + h, key, col0 + c)] : 0.f;
     }
     __syncthreads();
     for (int s = 0; s < nseg; ++s) {
@@ -472,7 +471,7 @@ k_compose(Problem p, Workspace ws) {
     if (p.ht) {
         for (int idx = tid; idx < K * BV; idx += kThreads) {
             const int key = idx / BV, c = idx - key * BV;
-            p.ht[((n * H + h) * K + key) * (int64_t)V + col0 + c] = hs[key * ldh + c];
+            p.ht[state_off(p, n * H + h, key, col0 + c)] = hs[key * ldh + c];
         }
     }
 }
@@ -563,7 +562,7 @@ cudaError_t set_smem(F *f, size_t bytes) {
 
 cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool /*check*/,
                              cudaStream_t st) {
-    k_chunk_table<<<1, kThreads, 0, st>>>(p.cu, p.N, p.T, ws.max_chunks, ws.chunk_tab,
+    k_chunk_table<<<1, kThreads, 0, st>>>(p, p.N, p.T, ws.max_chunks, ws.chunk_tab,
                                           ws.seq_chunk0, ws.n_chunks, ws.seq_order, p.status);
     return cudaGetLastError();
 }

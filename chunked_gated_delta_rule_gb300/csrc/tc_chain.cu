@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                     // the serial scan also takes a sequence without tokens
                     // (its final state is its initial one)
                     if (c.s0 < c.s1 || MODE == kModeSerial) {
-                        c.tstart = p.cu ? (int64_t)p.cu[c.n] : c.n * p.T;
-                        c.tlen = (p.cu ? (int64_t)p.cu[c.n + 1] : (c.n + 1) * p.T) - c.tstart;
+                        c.tstart = seq_start(p, c.n);
+                        c.tlen = seq_end(p, c.n) - c.tstart;
                         c.valid = 1;
                         break;
                     }
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                             const int key = 64 * hq + kk;
                             float v = 0.f;
                             if (MODE == kModeSerial) {
-                                if (p.h0) v = p.h0[((C.n * H + h) * kD + key) * kD + row];
+                                if (p.h0) v = p.h0[state_off(p, C.n * H + h, key, row)];
                             } else if (MODE == kModeSegOut) {
                                 v = ws.segH[(seg_base * kD + key) * kD + row];
                             } else if (trans) {
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
             if (MODE == kModeSerial && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
                 if (p.ht) {
                     for (int key = 0; key < kD; ++key) {
-                        const int64_t idx = ((C.n * H + h) * kD + key) * kD + row;
+                        const int64_t idx = state_off(p, C.n * H + h, key, row);
                         p.ht[idx] = p.h0 ? p.h0[idx] : 0.f;
                     }
                 }
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                     if (MODE == kModeSerial) {
 #pragma unroll
                         for (int kk = 0; kk < 32; ++kk)
-                            p.ht[((C.n * H + h) * kD + 32 * q + kk) * kD + row] = hv[kk];
+                            p.ht[state_off(p, C.n * H + h, 32 * q + kk, row)] = hv[kk];
                     } else if (trans) {  // M_s stored transposed: row `row`
                         float4 *dst = reinterpret_cast<float4 *>(
                             ws.segM + (seg_base * kD + row) * kD + 32 * q);

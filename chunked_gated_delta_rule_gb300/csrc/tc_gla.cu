@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                     // the serial scan also takes a sequence without tokens
                     // (its final state is its initial one)
                     if (c.s0 < c.s1 || MODE == kModeSerial) {
-                        c.tstart = p.cu ? (int64_t)p.cu[c.n] : c.n * p.T;
-                        c.tlen = (p.cu ? (int64_t)p.cu[c.n + 1] : (c.n + 1) * p.T) - c.tstart;
+                        c.tstart = seq_start(p, c.n);
+                        c.tlen = seq_end(p, c.n) - c.tstart;
                         c.valid = 1;
                         break;
                     }
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                             const int key = 64 * q + kk;
                             float x = 0.f;
                             if (MODE == kModeSerial) {
-                                if (p.h0) x = p.h0[((C.n * H + h) * KD + key) * (int64_t)V + v0 + row];
+                                if (p.h0) x = p.h0[state_off(p, C.n * H + h, key, v0 + row)];
                             } else if (MODE == kModeSegOut) {
                                 x = ws.segH[(seg_base * KD + key) * V + v0 + row];
                             }
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
             if (MODE == kModeSerial && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
                 if (p.ht) {
                     for (int key = 0; key < KD; ++key) {
-                        const int64_t idx = ((C.n * H + h) * KD + key) * (int64_t)V + v0 + row;
+                        const int64_t idx = state_off(p, C.n * H + h, key, v0 + row);
                         p.ht[idx] = p.h0 ? p.h0[idx] : 0.f;
                     }
                 }
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                     for (int kk = 0; kk < 32; ++kk) {
                         const int key = 32 * q + kk;
                         if (MODE == kModeSerial)
-                            p.ht[((C.n * H + h) * KD + key) * (int64_t)V + v0 + row] = hv[kk];
+                            p.ht[state_off(p, C.n * H + h, key, v0 + row)] = hv[kk];
                         else
                             ws.segC[(seg_base * KD + key) * V + v0 + row] = hv[kk];
                     }

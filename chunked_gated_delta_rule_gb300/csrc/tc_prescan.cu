@@ -154,8 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                     c.s0 = c.s * per;
                     c.s1 = min(nc, c.s0 + per);
                     if (c.s0 < c.s1) {
-                        c.tstart = p.cu ? (int64_t)p.cu[c.n] : c.n * p.T;
-                        c.tlen = (p.cu ? (int64_t)p.cu[c.n + 1] : (c.n + 1) * p.T) - c.tstart;
+                        c.tstart = seq_start(p, c.n);
+                        c.tlen = seq_end(p, c.n) - c.tstart;
                         c.valid = 1;
                         break;
                     }

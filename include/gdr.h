@@ -30,10 +30,12 @@
  *   q, k        [B, T, H, K]   dtype GDR_BF16 or GDR_F32 (same for q, k, v, o)
  *   v, o        [B, T, H, V]
  *   g, beta     [B, T, H]      float32; g is the per-token LOG gate (<= 0)
- *   cu_seqlens  [N + 1]        int32 prefix offsets of N packed sequences
- *                              (varlen: dims.N = N > 0, B == 1, T = total)
+ *   cu_seqlens  [N + 1]        int32 (int64 with GDR_SEQLENS_I64) prefix
+ *                              offsets of N packed sequences (varlen:
+ *                              dims.N = N > 0, B == 1, T = total)
  *   h0, ht      [Nseq, H, K, V] float32 state h = S^T, Nseq = N (varlen)
- *                              or B (dense)
+ *                              or B (dense); [Nseq, H, V, K] (S itself)
+ *                              with GDR_STATE_VK
  *
  * Ownership: every pointer is caller-owned.  gdr_chunk_fwd* take DEVICE
  * pointers, enqueue work on `stream` and return without synchronising; the
@@ -77,13 +79,21 @@ enum gdr_status {
     GDR_ERR_INDEX = -7         /* device status: a state index out of range */
 };
 
+/* Layout flags of gdr_dims.flags (bitwise OR; 0 = the defaults above). */
+enum gdr_flags {
+    GDR_SEQLENS_I64 = 1, /* cu_seqlens holds int64 offsets (pass the pointer
+                            through the int32_t * parameter)                */
+    GDR_STATE_VK = 2     /* h0, ht and the recurrent state pool are S, laid
+                            out [.., H, V, K], instead of h = S^T           */
+};
+
 /* Problem size.  Dense layout: N = 0 (there are B sequences of T tokens).
  * Varlen layout: N > 0 sequences packed along T (the total length), B == 1,
  * cu_seqlens required. */
 typedef struct gdr_dims {
     int64_t B, T, H, K, V, N;
     int32_t dtype; /* enum gdr_dtype */
-    int32_t reserved;
+    int32_t flags; /* enum gdr_flags */
 } gdr_dims;
 
 /* Launch plan (A13): chosen per shape from measured timings; every plan of

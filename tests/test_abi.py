@@ -77,6 +77,7 @@ def test_argument_checks_reject_before_any_gpu_work(lib):
     assert _fwd(lib, ok, opt=bad_bv) == -1
     bad_scale = api.gdr_options(float("nan"), 0, 0, None, 0, None)
     assert _fwd(lib, ok, opt=bad_scale) == -1
+    assert _fwd(lib, api.make_dims(1, 128, 2, 64, 64, flags=4)) == -1   # unknown flag bit
 
 
 def _rec(lib, dims, q=1, state=1, n_states=4, idx=None, cu=None):
