@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(256) k_compose_scalar(Problem p, Workspace ws)
     const float *__restrict__ C = ws.segC + nh * S * kv + e;
     float *__restrict__ Hs = ws.segH + nh * S * kv + e;
     const float *__restrict__ D = ws.segD + nh * S;
-    const int64_t sidx = state_off(p, nh, e / p.V, e % p.V);  // this element in h0 / ht
+    // this element in h0 / ht: idx itself in the default layout
+    const int64_t sidx = p.state_vk ? state_off(p, nh, e / p.V, e % p.V) : idx;
     float h = p.h0 ? p.h0[sidx] : 0.f;
     for (int s = 0; s < nseg; ++s) {
         const float c = C[s * kv];

@@ -341,6 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
             const int h = C.h;
             const bool trans = C.trans != 0;
             const int64_t seg_base = (C.n * H + h) * (int64_t)S + C.s;
+            // h0 / ht column `row` of this (sequence, head): element `key` at
+            // st_base + key * (1 or kD) by the state layout
+            const int64_t st_base = state_off(p, C.n * H + h, 0, row);
             for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
                 const int b = gk & 1;
                 const uint8_t *st = sm + b * kStage;
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                             const int key = 64 * hq + kk;
                             float v = 0.f;
                             if (MODE == kModeSerial) {
-                                if (p.h0) v = p.h0[state_off(p, C.n * H + h, key, row)];
+                                if (p.h0) v = p.h0[st_base + (p.state_vk ? key : key * kD)];
                             } else if (MODE == kModeSegOut) {
                                 v = ws.segH[(seg_base * kD + key) * kD + row];
                             } else if (trans) {
@@ -447,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
             if (MODE == kModeSerial && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
                 if (p.ht) {
                     for (int key = 0; key < kD; ++key) {
-                        const int64_t idx = state_off(p, C.n * H + h, key, row);
+                        const int64_t idx = st_base + (p.state_vk ? key : key * kD);
                         p.ht[idx] = p.h0 ? p.h0[idx] : 0.f;
                     }
                 }
@@ -459,10 +462,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 for (int q = 0; q < 4; ++q) {
                     float hv[32];
                     tmem_load32f(tmem + lane + kColS + 32 * q, hv);
-                    if (MODE == kModeSerial) {
+                    if (MODE == kModeSerial) {  // compile-time strides in either layout
+                        float *dst = p.ht + st_base + (p.state_vk ? 32 * q : 32 * q * kD);
+                        if (p.state_vk) {
 #pragma unroll
-                        for (int kk = 0; kk < 32; ++kk)
-                            p.ht[state_off(p, C.n * H + h, 32 * q + kk, row)] = hv[kk];
+                            for (int kk = 0; kk < 32; ++kk) dst[kk] = hv[kk];
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < 32; ++kk) dst[kk * kD] = hv[kk];
+                        }
                     } else if (trans) {  // M_s stored transposed: row `row`
                         float4 *dst = reinterpret_cast<float4 *>(
                             ws.segM + (seg_base * kD + row) * kD + 32 * q);

@@ -333,6 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
             if (!take(k++, C) || !C.valid) break;
             const int h = C.h, v0 = 128 * C.vt;
             const int64_t seg_base = (C.n * H + h) * (int64_t)S + C.s;
+            // h0 / ht column v0 + row of this (sequence, head): element `key`
+            // at st_base + key * st_step, in either state layout
+            const int64_t st_base = state_off(p, C.n * H + h, 0, v0 + row);
+            const int64_t st_step = p.state_vk ? 1 : V;
             float dprod = 1.f;
             for (int cc = C.s0; cc < C.s1; ++cc, ++gk) {
                 const int b = gk & 1;
@@ -352,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                             const int key = 64 * q + kk;
                             float x = 0.f;
                             if (MODE == kModeSerial) {
-                                if (p.h0) x = p.h0[state_off(p, C.n * H + h, key, v0 + row)];
+                                if (p.h0) x = p.h0[st_base + key * st_step];
                             } else if (MODE == kModeSegOut) {
                                 x = ws.segH[(seg_base * KD + key) * V + v0 + row];
                             }
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
             if (MODE == kModeSerial && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
                 if (p.ht) {
                     for (int key = 0; key < KD; ++key) {
-                        const int64_t idx = state_off(p, C.n * H + h, key, v0 + row);
+                        const int64_t idx = st_base + key * st_step;
                         p.ht[idx] = p.h0 ? p.h0[idx] : 0.f;
                     }
                 }
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                     for (int kk = 0; kk < 32; ++kk) {
                         const int key = 32 * q + kk;
                         if (MODE == kModeSerial)
-                            p.ht[state_off(p, C.n * H + h, key, v0 + row)] = hv[kk];
+                            p.ht[st_base + key * st_step] = hv[kk];
                         else
                             ws.segC[(seg_base * KD + key) * V + v0 + row] = hv[kk];
                     }
