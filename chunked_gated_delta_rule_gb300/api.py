@@ -16,13 +16,13 @@ import torch
 
 from . import build as _build
 
-GDR_F32, GDR_BF16 = 0, 1
+GDR_F32, GDR_BF16, GDR_F16 = 0, 1, 2
 
 
 class gdr_dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
                 ("K", ctypes.c_int64), ("V", ctypes.c_int64), ("N", ctypes.c_int64),
-                ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class gdr_plan(ctypes.Structure):
@@ -119,7 +119,9 @@ def _dtype_code(t: torch.dtype) -> int:
         return GDR_F32
     if t == torch.bfloat16:
         return GDR_BF16
-    raise TypeError(f"unsupported dtype {t}: q, k, v must be float32 or bfloat16")
+    if t == torch.float16:
+        return GDR_F16
+    raise TypeError(f"unsupported dtype {t}: q, k, v must be float32, bfloat16 or float16")
 
 
 GDR_SEQLENS_I64 = 1  # gdr_dims.flags: cu_seqlens holds int64 offsets

@@ -29,7 +29,7 @@ int validate_dims(const gdr_dims *d) {
     if (!d) return GDR_ERR_INVALID;
     if (d->B < 1 || d->T < 0 || d->H < 1 || d->K < 1 || d->V < 1 || d->N < 0)
         return GDR_ERR_INVALID;
-    if (d->dtype != GDR_F32 && d->dtype != GDR_BF16) return GDR_ERR_INVALID;
+    if (d->dtype != GDR_F32 && d->dtype != GDR_BF16 && d->dtype != GDR_F16) return GDR_ERR_INVALID;
     if (d->flags & ~(GDR_SEQLENS_I64 | GDR_STATE_VK)) return GDR_ERR_INVALID;
     if (is_varlen(*d) && d->B != 1) return GDR_ERR_INVALID;
     if (d->K % 16 || d->V % 16) return GDR_ERR_UNSUPPORTED;
@@ -423,7 +423,7 @@ int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k, const
     if (!q || !k || !v || !g || !o) return GDR_ERR_INVALID;
     if ((cu_seqlens != nullptr) != is_varlen(*dims)) return GDR_ERR_INVALID;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t es = dims->dtype == GDR_BF16 ? 2 : 4;
+    const size_t es = dims->dtype == GDR_F32 ? 4 : 2;
     const size_t ntok = (size_t)dims->B * (size_t)dims->T * (size_t)dims->H;
     const size_t ns = (size_t)n_seqs(*dims);
     const size_t bq = ntok * dims->K * es, bv = ntok * dims->V * es, bg = ntok * 4;

@@ -7,6 +7,7 @@
 #include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gdr.h"
 

@@ -16,6 +16,8 @@
 // [w K/8, (w+1) K/8) of the tile in registers (lane = column), so the state
 // is read once and written once per call; h^T k and h^T q are reduced
 // across the eight warps through shared memory in a fixed order.
+#include <type_traits>
+
 #include "gdr_internal.cuh"
 
 namespace gdr {
@@ -27,17 +29,17 @@ constexpr int kRMaxRows = kMaxK / 8;
 
 template <typename Tin>
 __device__ __forceinline__ float ld_in(const void *p, int64_t i) {
-    if constexpr (sizeof(Tin) == 2)
-        return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
-    else
-        return reinterpret_cast<const float *>(p)[i];
+    const Tin x = reinterpret_cast<const Tin *>(p)[i];
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) return __bfloat162float(x);
+    else if constexpr (std::is_same<Tin, __half>::value) return __half2float(x);
+    else return x;
 }
 template <typename Tin>
 __device__ __forceinline__ void st_out(void *p, int64_t i, float x) {
-    if constexpr (sizeof(Tin) == 2)
-        reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
-    else
-        reinterpret_cast<float *>(p)[i] = x;
+    Tin *q = reinterpret_cast<Tin *>(p);
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) q[i] = __float2bfloat16_rn(x);
+    else if constexpr (std::is_same<Tin, __half>::value) q[i] = __float2half_rn(x);
+    else q[i] = x;
 }
 
 // Three CTAs an SM (at most 80 registers a thread) up to K = 128: the state
@@ -147,8 +149,9 @@ cudaError_t launch_rec(const Problem &p, float *state, int64_t n_states, const i
 cudaError_t recurrent_fwd(const Problem &p, float *state, int64_t n_states,
                           const int32_t *state_idx, cudaStream_t st) {
     if (p.N == 0) return cudaSuccess;
-    return p.dtype == GDR_BF16 ? launch_rec<__nv_bfloat16>(p, state, n_states, state_idx, st)
-                               : launch_rec<float>(p, state, n_states, state_idx, st);
+    if (p.dtype == GDR_BF16) return launch_rec<__nv_bfloat16>(p, state, n_states, state_idx, st);
+    if (p.dtype == GDR_F16) return launch_rec<__half>(p, state, n_states, state_idx, st);
+    return launch_rec<float>(p, state, n_states, state_idx, st);
 }
 
 }  // namespace gdr

@@ -33,6 +33,8 @@ __device__ __forceinline__ void st_out(float *p, int64_t i, float x) { p[i] = x;
 __device__ __forceinline__ void st_out(__nv_bfloat16 *p, int64_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
 }
+__device__ __forceinline__ float ld_in(const __half *p, int64_t i) { return __half2float(p[i]); }
+__device__ __forceinline__ void st_out(__half *p, int64_t i, float x) { p[i] = __float2half_rn(x); }
 
 __device__ __forceinline__ void report(int32_t *status, int code) {
     if (status) atomicCAS(status, 0, code);
@@ -578,6 +580,9 @@ cudaError_t simt_prep(const Problem &p, const Workspace &ws, cudaStream_t st) {
     if (p.dtype == GDR_BF16) {
         if ((err = set_smem(k_prep<__nv_bfloat16>, smem)) != cudaSuccess) return err;
         k_prep<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p, ws);
+    } else if (p.dtype == GDR_F16) {
+        if ((err = set_smem(k_prep<__half>, smem)) != cudaSuccess) return err;
+        k_prep<__half><<<grid, kThreads, smem, st>>>(p, ws);
     } else {
         if ((err = set_smem(k_prep<float>, smem)) != cudaSuccess) return err;
         k_prep<float><<<grid, kThreads, smem, st>>>(p, ws);
@@ -609,6 +614,12 @@ cudaError_t simt_scan(const Problem &p, const Workspace &ws, int mode, int bv,
         case 16: return launch_scan<__nv_bfloat16, 16>(p, ws, mode, st);
         case 32: return launch_scan<__nv_bfloat16, 32>(p, ws, mode, st);
         case 64: return launch_scan<__nv_bfloat16, 64>(p, ws, mode, st);
+        }
+    } else if (p.dtype == GDR_F16) {
+        switch (bv) {
+        case 16: return launch_scan<__half, 16>(p, ws, mode, st);
+        case 32: return launch_scan<__half, 32>(p, ws, mode, st);
+        case 64: return launch_scan<__half, 64>(p, ws, mode, st);
         }
     } else {
         switch (bv) {
@@ -652,6 +663,9 @@ cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st) 
     if (p.dtype == GDR_BF16) {
         if ((err = set_smem(k_output<__nv_bfloat16>, smem)) != cudaSuccess) return err;
         k_output<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p, ws, bvo);
+    } else if (p.dtype == GDR_F16) {
+        if ((err = set_smem(k_output<__half>, smem)) != cudaSuccess) return err;
+        k_output<__half><<<grid, kThreads, smem, st>>>(p, ws, bvo);
     } else {
         if ((err = set_smem(k_output<float>, smem)) != cudaSuccess) return err;
         k_output<float><<<grid, kThreads, smem, st>>>(p, ws, bvo);

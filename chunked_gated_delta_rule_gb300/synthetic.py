@@ -38,7 +38,7 @@ class Workload:
     H: int
     K: int
     V: int
-    dtype: str             # "f32" | "bf16" (q, k, v, o)
+    dtype: str             # "f32" | "bf16" | "f16" (q, k, v, o)
     n_seqs: int = 0        # > 0: varlen, lengths U{len_lo..len_hi}, packed
     len_lo: int = 0
     len_hi: int = 0
@@ -74,7 +74,7 @@ WORKLOADS = {
 
 
 def torch_dtype(name: str) -> torch.dtype:
-    return {"f32": torch.float32, "bf16": torch.bfloat16}[name]
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[name]
 
 
 def make_inputs(w: Workload, lengths: Optional[list] = None, T: Optional[int] = None,

@@ -27,7 +27,8 @@
  *               S_t = alpha_t S_{t-1} + v_t k_t^T, the transition is a scalar.
  *
  * Layouts (all row-major and contiguous, element strides implied):
- *   q, k        [B, T, H, K]   dtype GDR_BF16 or GDR_F32 (same for q, k, v, o)
+ *   q, k        [B, T, H, K]   dtype GDR_BF16, GDR_F16 or GDR_F32 (same for
+ *                              q, k, v, o)
  *   v, o        [B, T, H, V]
  *   g, beta     [B, T, H]      float32; g is the per-token LOG gate (<= 0)
  *   cu_seqlens  [N + 1]        int32 (int64 with GDR_SEQLENS_I64) prefix
@@ -64,8 +65,9 @@ extern "C" {
 /* Same object as cudaStream_t; 0 is the legacy default stream. */
 typedef struct CUstream_st *gdr_stream_t;
 
-/* Element type of q, k, v and o. */
-enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1 };
+/* Element type of q, k, v and o.  GDR_F16 runs on the CUDA-core path (the
+ * tensor-core kernels take BF16). */
+enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1, GDR_F16 = 2 };
 
 /* Return codes. */
 enum gdr_status {

@@ -121,6 +121,13 @@ def test_plan_query_is_deterministic_and_valid():
         assert pkg.gdr_plan_query(B, T, H, K, V, beta_free=bf)["n_segments"] == s
 
 
+def test_fp16_inputs_plan_the_cuda_core_path():
+    """The tensor-core kernels take BF16: FP16 (dtype 2) goes to path 1."""
+    plan = pkg.gdr_plan_query(1, 1000, 16, 128, 128, N=4, dtype=api.GDR_F16)
+    assert plan["path"] == 1
+    assert pkg.gdr_workspace_size(1, 1000, 16, 128, 128, N=4, dtype=api.GDR_F16) > 0
+
+
 def test_workspace_size_scales_with_problem():
     # CUDA-core path keeps W, U, h_pre, v_new in HBM: grows with tokens
     small = pkg.gdr_workspace_size(1, 256, 2, 64, 64, dtype=0)
