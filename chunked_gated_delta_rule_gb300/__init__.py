@@ -7,7 +7,8 @@ point raises if the CUDA library is missing.
 """
 from .api import (GdrError, LaunchTimer, gdr_chunk_fwd, gdr_chunk_fwd_host,  # noqa: F401
                   gdr_chunk_fwd_noalloc, gdr_recurrent_fwd,
-                  gdr_error_string, gdr_kernel_name, gdr_plan_query, gdr_version,
+                  gdr_error_string, gdr_kernel_name, gdr_plan_query, gdr_release_cached,
+                  gdr_version,
                   gdr_workspace_size, load_library)
 
 # gdr_chunk_fwd_ex's options (scale, forced plan, workspace, status word) are

@@ -45,7 +45,7 @@ SELFTEST_EXPORTS = ("gdr_selftest_umma", "gdr_selftest_tma", "gdr_selftest_inver
 # Every symbol include/gdr.h declares.
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_host", "gdr_chunk_fwd_noalloc",
            "gdr_workspace_size", "gdr_plan_query", "gdr_recurrent_fwd", "gdr_kernel_name", "gdr_error_string",
-           "gdr_version")
+           "gdr_release_cached", "gdr_version")
 
 _lib = None
 _lock = threading.Lock()
@@ -101,6 +101,8 @@ def load_library():
         lib.gdr_selftest_timeout.restype = ctypes.c_int
         lib.gdr_selftest_inverse.argtypes = [vp, vp, vp]
         lib.gdr_selftest_inverse.restype = ctypes.c_int
+        lib.gdr_release_cached.argtypes = []
+        lib.gdr_release_cached.restype = ctypes.c_int
         lib.gdr_version.argtypes = []
         lib.gdr_version.restype = ctypes.c_int
         _lib = lib
@@ -432,6 +434,14 @@ def gdr_kernel_name(kid: int) -> str:
 
 def gdr_error_string(code: int) -> str:
     return load_library().gdr_error_string(int(code)).decode()
+
+
+def gdr_release_cached() -> None:
+    """Return the device memory the library keeps between calls (its
+    stream-ordered scratch pools) to the driver."""
+    rc = load_library().gdr_release_cached()
+    if rc != 0:
+        raise GdrError(rc)
 
 
 def gdr_version() -> int:

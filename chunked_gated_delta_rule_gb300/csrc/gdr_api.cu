@@ -1,7 +1,10 @@
 // gdr_api.cu -- host runtime behind include/gdr.h: argument validation, launch
 // plan (A13), workspace layout, and the launch sequence of the forward pass.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "gdr_internal.cuh"
 
@@ -13,6 +16,114 @@ constexpr size_t kAlign = 256;
 constexpr int kNumSMs = 152;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Device memory the library allocates during a call comes from a
+// stream-ordered pool of its own, one per device, whose release threshold
+// keeps freed blocks mapped.  The default pool returns its memory to the
+// driver at every synchronisation, and mapping a call's few hundred MB again
+// costs as much as a host call's copies.  gdr_release_cached() trims these
+// pools.  While the stream is being captured into a graph the allocation
+// stays on the default pool, as graph-owned memory.
+constexpr int kMaxDevices = 64;
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+
+cudaError_t lib_pool(int dev, cudaMemPool_t *out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        cudaError_t e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return e;
+        }
+        g_pools[dev] = pool;
+    }
+    *out = g_pools[dev];
+    return cudaSuccess;
+}
+
+cudaError_t lib_malloc(void **ptr, size_t bytes, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs != cudaStreamCaptureStatusNone) return cudaMallocAsync(ptr, bytes, st);
+    int dev = 0;
+    e = cudaStreamGetDevice(st, &dev);
+    if (e != cudaSuccess) return e;
+    cudaMemPool_t pool = nullptr;
+    e = lib_pool(dev, &pool);
+    if (e != cudaSuccess) return e;
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, st);
+}
+
+// The host entry's copy streams (inputs in, outputs out), one pair per
+// device, created on first use.  The caller's stream must belong to the
+// current device.
+struct CopyStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+};
+CopyStreams g_copy[kMaxDevices];
+
+cudaError_t copy_streams(cudaStream_t st, CopyStreams *out) {
+    int dev = 0, cur = 0;
+    cudaError_t e = cudaStreamGetDevice(st, &dev);
+    if (e == cudaSuccess) e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    if (dev != cur || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    CopyStreams &c = g_copy[dev];
+    if (!c.in) {
+        cudaStream_t a = nullptr, b = nullptr;
+        e = cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            if (a) cudaStreamDestroy(a);
+            return e;
+        }
+        c.in = a;
+        c.out = b;
+    }
+    *out = c;
+    return cudaSuccess;
+}
+
+// Groups of whole sequences (batch rows when dense) for the host entry's
+// overlap of copies and passes: about 32 MB of input a group, at most 4 (a
+// small group's passes cost about 50 us whatever its size).  The first and
+// last groups take half a share of the tokens: the outputs start leaving
+// sooner and the pass and copy out after the last input are shorter.  Group
+// i holds sequences [n[i], n[i + 1]).
+struct HostGroups {
+    std::vector<int64_t> n;
+    int count() const { return (int)n.size() - 1; }
+};
+
+HostGroups host_groups(const std::vector<int64_t> &cu, size_t tok_bytes, size_t seq_bytes) {
+    const int64_t ns = (int64_t)cu.size() - 1, T = cu[ns];
+    const double total = (double)T * (double)tok_bytes + (double)ns * (double)seq_bytes;
+    const int64_t want =
+        std::max<int64_t>(1, std::min<int64_t>({std::llround(total / (32.0 * (1 << 20))), 4, ns}));
+    HostGroups G;
+    G.n.push_back(0);
+    for (int64_t i = 1; i < want; ++i) {  // cut i at (2i - 1) / (2 (want - 1)) of the tokens
+        const int64_t target = T * (2 * i - 1) / (2 * (want - 1));
+        int64_t n = G.n.back() + 1;
+        while (n < ns && cu[n] < target) ++n;
+        if (n >= ns) break;
+        G.n.push_back(n);
+    }
+    G.n.push_back(ns);
+    return G;
+}
 
 bool is_varlen(const gdr_dims &d) { return d.N > 0; }
 int64_t n_seqs(const gdr_dims &d) { return is_varlen(d) ? d.N : d.B; }
@@ -268,6 +379,14 @@ extern "C" {
 
 int gdr_version(void) { return 100; }
 
+int gdr_release_cached(void) {
+    int rc = GDR_OK;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    for (cudaMemPool_t pool : g_pools)
+        if (pool && cudaMemPoolTrimTo(pool, 0) != cudaSuccess) rc = GDR_ERR_CUDA;
+    return rc;
+}
+
 const char *gdr_kernel_name(int id) {
     switch (id) {
     case kKChunkTable: return "simt_chunk_table";
@@ -386,7 +505,7 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
         if (reinterpret_cast<uintptr_t>(opt->workspace) % kAlign) return GDR_ERR_INVALID;
         base = opt->workspace;
     } else {
-        if (cudaMallocAsync(&base, L.total, st) != cudaSuccess) return GDR_ERR_CUDA;
+        if (lib_malloc(&base, L.total, st) != cudaSuccess) return GDR_ERR_CUDA;
         owned = true;
     }
     const Workspace ws = carve_workspace(base, L, plan.n_segments);
@@ -423,46 +542,134 @@ int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k, const
     if (!q || !k || !v || !g || !o) return GDR_ERR_INVALID;
     if ((cu_seqlens != nullptr) != is_varlen(*dims)) return GDR_ERR_INVALID;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t es = dims->dtype == GDR_F32 ? 4 : 2;
-    const size_t ntok = (size_t)dims->B * (size_t)dims->T * (size_t)dims->H;
-    const size_t ns = (size_t)n_seqs(*dims);
-    const size_t bq = ntok * dims->K * es, bv = ntok * dims->V * es, bg = ntok * 4;
-    const size_t bcu = cu_seqlens ? (ns + 1) * ((dims->flags & GDR_SEQLENS_I64) ? 8 : 4) : 0;
-    const size_t bh = ns * dims->H * dims->K * dims->V * 4;
+    const gdr_dims &D = *dims;
+    const bool varlen = is_varlen(D);
+    const int64_t ns = n_seqs(D);
+    // token offsets of the sequences (host data here, so checked on the host)
+    std::vector<int64_t> cu((size_t)ns + 1);
+    for (int64_t n = 0; n <= ns; ++n) {
+        if (!varlen) cu[n] = n * D.T;
+        else if (D.flags & GDR_SEQLENS_I64) cu[n] = reinterpret_cast<const int64_t *>(cu_seqlens)[n];
+        else cu[n] = cu_seqlens[n];
+        if (n > 0 && cu[n] < cu[n - 1]) return GDR_ERR_SEQLENS;
+    }
+    if (cu[0] != 0 || cu[ns] != D.B * D.T) return GDR_ERR_SEQLENS;
+
+    const size_t es = D.dtype == GDR_F32 ? 4 : 2;
+    const size_t rq = (size_t)D.H * D.K * es, rv = (size_t)D.H * D.V * es, rg = (size_t)D.H * 4;
+    const size_t rh = (size_t)D.H * D.K * D.V * 4;  // one sequence's state
+    const size_t ntok = (size_t)cu[ns];
+    const HostGroups G = host_groups(cu, 2 * rq + rv + rg * (beta ? 2 : 1), rh * (h0 ? 1 : 0));
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes); return at; };
-    const size_t oq = take(bq), ok = take(bq), ov = take(bv), og = take(bg);
-    const size_t ob = take(beta ? bg : 0), ocu = take(bcu), oh0 = take(h0 ? bh : 0);
-    const size_t oo = take(bv), oht = take(ht ? bh : 0);
+    const size_t oq = take(ntok * rq), ok = take(ntok * rq), ov = take(ntok * rv);
+    const size_t og = take(ntok * rg), ob = take(beta ? ntok * rg : 0);
+    const size_t oh0 = take(h0 ? ns * rh : 0), oo = take(ntok * rv), oht = take(ht ? ns * rh : 0);
+    const size_t ocu = take(varlen ? (ns + G.count()) * sizeof(int32_t) : 0);
+    // each group's cu_seqlens, rebased to its first token (int32: T < 2^31)
+    std::vector<int32_t> gcu;
+    if (varlen) {
+        gcu.reserve((size_t)(ns + G.count()));
+        for (int i = 0; i < G.count(); ++i)
+            for (int64_t n = G.n[i]; n <= G.n[i + 1]; ++n)
+                gcu.push_back((int32_t)(cu[n] - cu[G.n[i]]));
+    }
     char *d = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&d), off ? off : kAlign, st) != cudaSuccess)
+    if (lib_malloc(reinterpret_cast<void **>(&d), off ? off : kAlign, st) != cudaSuccess)
         return GDR_ERR_CUDA;
+
+    // Copies in on one stream, the passes on `stream`, copies out on a third:
+    // group i + 1 arrives while group i runs and group i - 1 leaves.
+    CopyStreams cs{};
+    const bool piped = G.count() > 1 && copy_streams(st, &cs) == cudaSuccess;
+    cudaStream_t s_in = piped ? cs.in : st, s_out = piped ? cs.out : st;
+    std::vector<cudaEvent_t> ev;
+    auto new_event = [&](cudaEvent_t *e) {
+        if (!piped) return cudaSuccess;
+        const cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+        if (r == cudaSuccess) ev.push_back(*e);
+        return r;
+    };
+    auto order = [&](cudaStream_t from, cudaStream_t to) {  // `to` waits for `from`'s work so far
+        if (!piped || from == to) return cudaSuccess;
+        cudaEvent_t e = nullptr;
+        cudaError_t r = new_event(&e);
+        if (r == cudaSuccess) r = cudaEventRecord(e, from);
+        if (r == cudaSuccess) r = cudaStreamWaitEvent(to, e, 0);
+        return r;
+    };
     auto h2d = [&](size_t at, const void *src, size_t bytes) {
-        return bytes ? cudaMemcpyAsync(d + at, src, bytes, cudaMemcpyHostToDevice, st)
+        return bytes ? cudaMemcpyAsync(d + at, src, bytes, cudaMemcpyHostToDevice, s_in)
                      : cudaSuccess;
     };
+    auto d2h = [&](void *dst, size_t at, size_t bytes) {
+        return bytes ? cudaMemcpyAsync(dst, d + at, bytes, cudaMemcpyDeviceToHost, s_out)
+                     : cudaSuccess;
+    };
+    const char *hq = static_cast<const char *>(q), *hk = static_cast<const char *>(k),
+               *hv = static_cast<const char *>(v), *hg = reinterpret_cast<const char *>(g),
+               *hb = reinterpret_cast<const char *>(beta), *hh0 = reinterpret_cast<const char *>(h0);
+    char *ho = static_cast<char *>(o), *hht = reinterpret_cast<char *>(ht);
     rc = GDR_OK;
-    if (h2d(oq, q, bq) != cudaSuccess || h2d(ok, k, bq) != cudaSuccess ||
-        h2d(ov, v, bv) != cudaSuccess || h2d(og, g, bg) != cudaSuccess ||
-        (beta && h2d(ob, beta, bg) != cudaSuccess) ||
-        (cu_seqlens && h2d(ocu, cu_seqlens, bcu) != cudaSuccess) ||
-        (h0 && h2d(oh0, h0, bh) != cudaSuccess))
+    if (order(st, s_in) != cudaSuccess || order(st, s_out) != cudaSuccess ||
+        (varlen && h2d(ocu, gcu.data(), gcu.size() * sizeof(int32_t)) != cudaSuccess))
         rc = GDR_ERR_CUDA;
-    if (rc == GDR_OK)
-        rc = gdr_chunk_fwd(dims, d + oq, d + ok, d + ov, reinterpret_cast<float *>(d + og),
-                           beta ? reinterpret_cast<float *>(d + ob) : nullptr,
-                           cu_seqlens ? reinterpret_cast<int32_t *>(d + ocu) : nullptr,
-                           h0 ? reinterpret_cast<float *>(d + oh0) : nullptr, d + oo,
-                           ht ? reinterpret_cast<float *>(d + oht) : nullptr, n_segments,
-                           stream);
-    if (rc == GDR_OK && bv &&
-        cudaMemcpyAsync(o, d + oo, bv, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        rc = GDR_ERR_CUDA;
-    if (rc == GDR_OK && ht &&
-        cudaMemcpyAsync(ht, d + oht, bh, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        rc = GDR_ERR_CUDA;
+    // every group's inputs are queued first, so the copies in never wait for
+    // the host to launch a pass
+    std::vector<cudaEvent_t> arrived((size_t)G.count(), nullptr);
+    for (int i = 0; i < G.count() && rc == GDR_OK; ++i) {
+        const size_t t0 = (size_t)cu[G.n[i]], nt = (size_t)cu[G.n[i + 1]] - t0;
+        const size_t n0 = (size_t)G.n[i], nn = (size_t)(G.n[i + 1] - G.n[i]);
+        if (h2d(oq + t0 * rq, hq + t0 * rq, nt * rq) != cudaSuccess ||
+            h2d(ok + t0 * rq, hk + t0 * rq, nt * rq) != cudaSuccess ||
+            h2d(ov + t0 * rv, hv + t0 * rv, nt * rv) != cudaSuccess ||
+            h2d(og + t0 * rg, hg + t0 * rg, nt * rg) != cudaSuccess ||
+            (beta && h2d(ob + t0 * rg, hb + t0 * rg, nt * rg) != cudaSuccess) ||
+            (h0 && h2d(oh0 + n0 * rh, hh0 + n0 * rh, nn * rh) != cudaSuccess) ||
+            new_event(&arrived[i]) != cudaSuccess ||
+            (piped && cudaEventRecord(arrived[i], s_in) != cudaSuccess))
+            rc = GDR_ERR_CUDA;
+    }
+    for (int i = 0; i < G.count() && rc == GDR_OK; ++i) {
+        const size_t t0 = (size_t)cu[G.n[i]], nt = (size_t)cu[G.n[i + 1]] - t0;
+        const size_t n0 = (size_t)G.n[i], nn = (size_t)(G.n[i + 1] - G.n[i]);
+        if (piped && cudaStreamWaitEvent(st, arrived[i], 0) != cudaSuccess) {
+            rc = GDR_ERR_CUDA;
+            break;
+        }
+        gdr_dims gd = D;
+        if (varlen) {
+            gd.N = (int32_t)nn;
+            gd.T = (int64_t)nt;
+            gd.flags &= ~GDR_SEQLENS_I64;
+        } else {
+            gd.B = (int64_t)nn;
+        }
+        const int32_t *gc = varlen ? reinterpret_cast<const int32_t *>(
+                                         d + ocu + (size_t)(G.n[i] + i) * sizeof(int32_t))
+                                   : nullptr;
+        rc = gdr_chunk_fwd(&gd, d + oq + t0 * rq, d + ok + t0 * rq, d + ov + t0 * rv,
+                           reinterpret_cast<float *>(d + og + t0 * rg),
+                           beta ? reinterpret_cast<float *>(d + ob + t0 * rg) : nullptr, gc,
+                           h0 ? reinterpret_cast<float *>(d + oh0 + n0 * rh) : nullptr,
+                           d + oo + t0 * rv,
+                           ht ? reinterpret_cast<float *>(d + oht + n0 * rh) : nullptr,
+                           n_segments, stream);
+        if (rc != GDR_OK) break;
+        if (order(st, s_out) != cudaSuccess || d2h(ho + t0 * rv, oo + t0 * rv, nt * rv) != cudaSuccess ||
+            (ht && d2h(hht + n0 * rh, oht + n0 * rh, nn * rh) != cudaSuccess))
+            rc = GDR_ERR_CUDA;
+    }
+    // `stream` waits for the copy streams before the block is freed; should
+    // that ordering fail, the host waits for them instead
+    if (order(s_in, st) != cudaSuccess || order(s_out, st) != cudaSuccess) {
+        cudaStreamSynchronize(s_in);
+        cudaStreamSynchronize(s_out);
+        if (rc == GDR_OK) rc = GDR_ERR_CUDA;
+    }
     if (cudaFreeAsync(d, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
     return rc;
 }
 

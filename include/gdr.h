@@ -41,8 +41,11 @@
  * Ownership: every pointer is caller-owned.  gdr_chunk_fwd* take DEVICE
  * pointers, enqueue work on `stream` and return without synchronising; the
  * library keeps no pointer after the call returns.  Scratch is taken
- * stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`) unless the
- * caller passes a workspace through gdr_chunk_fwd_ex.
+ * stream-ordered on `stream` unless the caller passes a workspace through
+ * gdr_chunk_fwd_ex: from a pool per device that the library owns and that
+ * keeps freed memory mapped for the next call (gdr_release_cached hands it
+ * back), or, while `stream` is being captured into a graph, from the
+ * device's default pool (cudaMallocAsync / cudaFreeAsync).
  *
  * Errors: every entry point returns 0 on success or a negative GDR_ERR_*
  * code; arguments are checked before any work is enqueued, so a rejected
@@ -155,9 +158,19 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k,
 /*
  * gdr_chunk_fwd_host -- the same pass on HOST buffers (same layouts).  The
  * call copies the inputs to the device, runs gdr_chunk_fwd on `stream`,
- * copies o (and ht) back and synchronises `stream` before returning.  Pinned
- * host memory gives asynchronous copies; pageable memory works but copies
- * synchronously.  Device buffers are stream-ordered allocations.
+ * copies o (and ht) back and synchronises `stream` before returning.
+ *   - Batches of 48 MB of input and more are cut into 2 to 4 groups of
+ *     whole sequences (batch rows when dense), each run as its own
+ *     gdr_chunk_fwd: group i + 1's inputs arrive and group i - 1's outputs
+ *     leave while group i runs, on two copy streams of the library ordered
+ *     against `stream` with events.  Each sequence's result is the one
+ *     gdr_chunk_fwd gives it (plans may differ with the group's size).
+ *   - cu_seqlens is host data here and is checked on the host: a table
+ *     that is not non-decreasing from 0 to T returns GDR_ERR_SEQLENS before
+ *     any work is enqueued.
+ *   - Pinned host memory gives asynchronous copies; pageable memory works
+ *     but copies synchronously.  Device buffers are stream-ordered
+ *     allocations from the library's pool (see Ownership above).
  */
 int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k,
                        const void *v, const float *g, const float *beta,
@@ -227,6 +240,11 @@ const char *gdr_kernel_name(int id);
 
 /* Static description of a return code. */
 const char *gdr_error_string(int code);
+
+/* Hands the device memory that the library's pools keep between calls back
+ * to the driver, on every device the library has allocated on.  Memory that
+ * enqueued work still uses is kept.  Returns GDR_OK or GDR_ERR_CUDA. */
+int gdr_release_cached(void);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int gdr_version(void);

@@ -80,6 +80,23 @@ def test_argument_checks_reject_before_any_gpu_work(lib):
     assert _fwd(lib, api.make_dims(1, 128, 2, 64, 64, flags=4)) == -1   # unknown flag bit
 
 
+def test_host_entry_checks_host_seqlens_before_any_gpu_work(lib):
+    """gdr_chunk_fwd_host reads cu_seqlens on the host: a table that does not
+    rise from 0 to T is rejected with GDR_ERR_SEQLENS before any copy."""
+    p = lambda x: ctypes.c_void_p(0x1000 * x)
+    dims = api.make_dims(1, 128, 2, 64, 64, N=3)
+    for table in ([0, 64, 32, 128], [1, 64, 96, 128], [0, 64, 96, 127]):
+        cu = (ctypes.c_int32 * 4)(*table)
+        rc = lib.gdr_chunk_fwd_host(ctypes.byref(dims), p(1), p(1), p(1), p(1), None,
+                                    ctypes.cast(cu, ctypes.c_void_p), None, p(1), None, 0, None)
+        assert rc == -5, table
+    d64 = api.make_dims(1, 128, 2, 64, 64, N=3, flags=api.GDR_SEQLENS_I64)
+    cu = (ctypes.c_int64 * 4)(0, 96, 64, 128)
+    rc = lib.gdr_chunk_fwd_host(ctypes.byref(d64), p(1), p(1), p(1), p(1), None,
+                                ctypes.cast(cu, ctypes.c_void_p), None, p(1), None, 0, None)
+    assert rc == -5
+
+
 def _rec(lib, dims, q=1, state=1, n_states=4, idx=None, cu=None):
     p = lambda x: None if x is None else ctypes.c_void_p(0x1000 * x)
     return lib.gdr_recurrent_fwd(ctypes.byref(dims), p(q), p(1), p(1), p(1), None, p(cu),

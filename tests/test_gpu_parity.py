@@ -234,6 +234,29 @@ def test_host_entry_matches_device_entry():
     assert torch.equal(_bits(ht_h), _bits(ht_d))
 
 
+def _host_run(x, **kw):
+    import chunked_gated_delta_rule_gb300 as pkg
+    pin = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()}
+    return pkg.gdr_chunk_fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"],
+                                  cu_seqlens=pin["cu_seqlens"], h0=pin["h0"], **kw)
+
+
+@pytest.mark.parametrize("case", ["wide_varlen", "dense_h0"])
+def test_host_entry_groups_match_device_entry(case):
+    """Inputs of 48 MB and more are cut into groups whose copies overlap the
+    passes; with the plan pinned (one segment) every sequence's result is
+    bit-identical to the one-call device entry."""
+    if case == "wide_varlen":  # 130 MB in: 4 groups of whole sequences
+        x = synthetic.make_inputs(W["wide_varlen_bf16"])
+    else:  # 8 rows x 4096 tokens x 4 heads with h0: 3 groups of batch rows
+        x = synthetic.make_inputs(synthetic.small(W["long_16k_bf16"], B=8, T=4096, H=4,
+                                                  with_h0=True))
+    o_d, ht_d = run_gpu(x, n_segments=1)
+    o_h, ht_h = _host_run(x, n_segments=1)
+    assert torch.equal(_bits(o_h), _bits(o_d.cpu()))
+    assert torch.equal(_bits(ht_h), _bits(ht_d.cpu()))
+
+
 def test_default_plan_uses_tensor_core_path_for_bf16_k128():
     import chunked_gated_delta_rule_gb300 as pkg
     assert pkg.gdr_plan_query(1, 10456, 16, 128, 128, N=32)["path"] == 2
