@@ -13,6 +13,12 @@ The arithmetic lives in ``gdr_oracle.c`` (plain C, FP64, token by token):
   the scan of fla's ``chunk_gated_delta_rule_fwd_kernel_h_blockdim64``, Kev
   PR #259 intro), with ``beta=None`` selecting the beta-free gated linear
   attention write ``S_t = alpha_t S_{t-1} + v_t k_t^T``.
+* :func:`backward` -- the gradient of :func:`forward` for the loss
+  ``<do, o> + <dht, ht>`` with respect to q, k, v, g, beta and h0: reverse-mode
+  differentiation of each token step, the state gradient dH running backward
+  through the sequence (the reverse dH recurrence of the flash-linear-attention
+  ABC issue #23 pages, "Problem" and "Proposed Dataflow" step 4; gradients
+  dQ/dK/dV and of the states, its "Fixture-First Correctness Contract").
 * :func:`affine` -- the affine map ``h_out = M h_in + c`` of that recurrence
   over a token range (the per-segment summary of cuLA PR #127 "Root cause and
   implementation").
@@ -68,6 +74,12 @@ def load_library(path: str):
     lib.gdr_oracle_fwd.restype = ctypes.c_int
     lib.gdr_oracle_fwd.argtypes = [
         dp, dp, dp, dp, dp, i64p, dp, dp, dp,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
+        ctypes.POINTER(ctypes.c_uint8), ctypes.c_int]
+    lib.gdr_oracle_bwd.restype = ctypes.c_int
+    lib.gdr_oracle_bwd.argtypes = [
+        dp, dp, dp, dp, dp, i64p, dp, dp, dp, dp, dp, dp, dp, dp, dp,
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
         ctypes.POINTER(ctypes.c_uint8), ctypes.c_int]
@@ -143,6 +155,49 @@ def forward(q, k, v, g, beta=None, cu_seqlens=None, h0=None, scale=None,
     if r < 0:
         raise ValueError("gdr_oracle_fwd rejected its arguments")
     return o, ht, r
+
+
+def backward(q, k, v, g, beta=None, cu_seqlens=None, h0=None, do=None, dht=None,
+             scale=None, pair_mask=None, n_threads=0, lib=None):
+    """Token-by-token FP64 gradients of ``L = <do, o> + <dht, ht>``.
+
+    Shapes as for :func:`forward`; ``do`` [B,T,H,V], ``dht`` [N,H,K,V] or
+    None (no final-state term).  Returns ``(dq, dk, dv, dg, dbeta, dh0)``,
+    FP64, ``dbeta`` None in the beta-free mode.  ``pair_mask`` limits the work
+    to some (sequence, head) pairs; the other pairs' gradients are NaN.
+    """
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(g)
+    beta, h0, do, dht = _f64(beta), _f64(h0), _f64(do), _f64(dht)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+            dtype=np.int64))
+        N = cu.shape[0] - 1
+    else:
+        cu = None
+        N = B
+    if scale is None:
+        scale = 1.0 / math.sqrt(K)
+    dq = np.full((B, T, H, K), np.nan)
+    dk = np.full((B, T, H, K), np.nan)
+    dv = np.full((B, T, H, V), np.nan)
+    dg = np.full((B, T, H), np.nan)
+    dbeta = np.full((B, T, H), np.nan) if beta is not None else None
+    dh0 = np.full((N, H, K, V), np.nan)
+    mask = None
+    if pair_mask is not None:
+        mask = np.ascontiguousarray(np.asarray(pair_mask, dtype=np.uint8).reshape(-1))
+        assert mask.shape[0] == N * H
+    r = (lib or _load()).gdr_oracle_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu, ctypes.c_int64),
+        _ptr(h0), _ptr(do), _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+        _ptr(dbeta), _ptr(dh0), B, T, H, K, V, N, float(scale),
+        _ptr(mask, ctypes.c_uint8), int(n_threads))
+    if r < 0:
+        raise ValueError("gdr_oracle_bwd rejected its arguments")
+    return dq, dk, dv, dg, dbeta, dh0
 
 
 def affine(k, v, g, beta=None, lib=None):

@@ -26,7 +26,8 @@
  *
  *   The readout scale defaults to 1/sqrt(K); the caller passes it.
  *
- * Also provided: the affine map of the recurrence over a token range,
+ * Also provided: the gradient of that forward pass (gdr_oracle_bwd below),
+ * and the affine map of the recurrence over a token range,
  * h_out = M h_in + c (M: K x K, c: K x V), the segment summary the
  * segment-split mode composes (cuLA PR #127 "Root cause and implementation":
  * local state plus affine transition per segment).
@@ -284,4 +285,290 @@ int gdr_oracle_affine(const double *k, const double *v, const double *g,
     }
     free(r);
     return 0;
+}
+
+
+/*
+ * Backward pass: the gradient of the forward recurrence above, by reverse-mode
+ * differentiation of each token step (the reverse dH recurrence that the
+ * flash-linear-attention ABC issue #23 pages run chunk by chunk, "Problem"
+ * and "Proposed Dataflow" step 4; its fixture contract asks for dQ, dK, dV
+ * and state gradients).  The scalar loss is L = <do, o> + <dht, ht>.
+ *
+ * One forward step, with h_prev the state before token t:
+ *     h' = a h_prev                    a = exp(g_t)
+ *     y  = h'^T k,  u = b (v - y)      (beta-free: u = v)
+ *     h  = h' + k u^T
+ *     o  = scale h^T q
+ * Its reverse, with dh = dL/dh entering from the later tokens (dht at the
+ * end of the sequence):
+ *     dh += scale q do^T;  dq = scale h do
+ *     dk  = dh u;          du = dh^T k
+ *     dv  = b du;          db = <du, v - y>;  dy = -b du;
+ *     dh += k dy^T;        dk += h' dy        (beta-free: dv = du)
+ *     dg  = a <dh, h_prev>;  dh <- a dh       (the gradient for h_prev)
+ * and dh0 is dh after the first token.  The states h_prev / h of a token are
+ * replayed forward from a checkpoint kept every 64 tokens.
+ */
+enum { BWD_BLOCK = 64 };
+
+typedef struct {
+    const double *q, *k, *v, *g, *beta, *h0, *dout, *dht;
+    double *dq, *dk, *dv, *dg, *dbeta, *dh0;
+    const int64_t *cu;
+    const uint8_t *pair_mask;
+    int64_t B, T, H, K, V, N;
+    double scale;
+    int64_t next;
+    int failed;
+    pthread_mutex_t mu;
+} bwd_job;
+
+/* One forward token step on S (K x V) for token index tok, in place. */
+static void step_forward(const bwd_job *J, int64_t tok, double *S, double *u)
+{
+    const int64_t K = J->K, V = J->V;
+    const double *kt = J->k + tok * K;
+    const double *vt = J->v + tok * V;
+    const double a = exp(J->g[tok]);
+    for (int64_t i = 0; i < K * V; ++i)
+        S[i] *= a;
+    if (J->beta) {
+        const double b = J->beta[tok];
+        for (int64_t j = 0; j < V; ++j)
+            u[j] = 0.0;
+        for (int64_t i = 0; i < K; ++i)
+            for (int64_t j = 0; j < V; ++j)
+                u[j] += S[i * V + j] * kt[i];
+        for (int64_t j = 0; j < V; ++j)
+            u[j] = b * (vt[j] - u[j]);
+    } else {
+        for (int64_t j = 0; j < V; ++j)
+            u[j] = vt[j];
+    }
+    for (int64_t i = 0; i < K; ++i)
+        for (int64_t j = 0; j < V; ++j)
+            S[i * V + j] += kt[i] * u[j];
+}
+
+static int run_pair_bwd(bwd_job *J, int64_t n, int64_t hh)
+{
+    const int64_t H = J->H, K = J->K, V = J->V, KV = K * V;
+    int64_t row, t0, t1;
+    if (J->cu) {
+        row = 0;
+        t0 = J->cu[n];
+        t1 = J->cu[n + 1];
+    } else {
+        row = n;
+        t0 = 0;
+        t1 = J->T;
+    }
+    const int64_t len = t1 - t0;
+    const int64_t nblk = (len + BWD_BLOCK - 1) / BWD_BLOCK;
+    /* ck[b]: state before block b's first token; st[i]: state after token i
+     * of the block being reversed (st[0] = the block's checkpoint) */
+    double *ck = (double *)malloc(sizeof(double) * (size_t)((nblk > 0 ? nblk : 1) * KV));
+    double *st = (double *)malloc(sizeof(double) * (size_t)((BWD_BLOCK + 1) * KV));
+    double *dh = (double *)malloc(sizeof(double) * (size_t)KV);
+    double *hp = (double *)malloc(sizeof(double) * (size_t)KV);
+    double *u = (double *)malloc(sizeof(double) * (size_t)V);
+    double *y = (double *)malloc(sizeof(double) * (size_t)V);
+    double *du = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!ck || !st || !dh || !hp || !u || !y || !du) {
+        free(ck); free(st); free(dh); free(hp); free(u); free(y); free(du);
+        return -1;
+    }
+    const int64_t sidx = (n * H + hh) * KV;
+    /* forward sweep, keeping each block's starting state */
+    if (J->h0)
+        memcpy(st, J->h0 + sidx, sizeof(double) * (size_t)KV);
+    else
+        memset(st, 0, sizeof(double) * (size_t)KV);
+    for (int64_t b = 0; b < nblk; ++b) {
+        memcpy(ck + b * KV, st, sizeof(double) * (size_t)KV);
+        const int64_t e = (b + 1) * BWD_BLOCK < len ? (b + 1) * BWD_BLOCK : len;
+        for (int64_t t = t0 + b * BWD_BLOCK; t < t0 + e; ++t)
+            step_forward(J, (row * J->T + t) * H + hh, st, u);
+    }
+    /* reverse sweep */
+    if (J->dht)
+        memcpy(dh, J->dht + sidx, sizeof(double) * (size_t)KV);
+    else
+        memset(dh, 0, sizeof(double) * (size_t)KV);
+    for (int64_t b = nblk - 1; b >= 0; --b) {
+        const int64_t s = t0 + b * BWD_BLOCK;
+        const int64_t e = (b + 1) * BWD_BLOCK < len ? t0 + (b + 1) * BWD_BLOCK : t1;
+        memcpy(st, ck + b * KV, sizeof(double) * (size_t)KV);
+        for (int64_t t = s; t < e; ++t) {
+            memcpy(st + (t - s + 1) * KV, st + (t - s) * KV, sizeof(double) * (size_t)KV);
+            step_forward(J, (row * J->T + t) * H + hh, st + (t - s + 1) * KV, u);
+        }
+        for (int64_t t = e - 1; t >= s; --t) {
+            const int64_t tok = (row * J->T + t) * H + hh;
+            const double *kt = J->k + tok * K, *qt = J->q + tok * K;
+            const double *vt = J->v + tok * V, *dot = J->dout + tok * V;
+            const double *hprev = st + (t - s) * KV, *hcur = st + (t - s + 1) * KV;
+            const double a = exp(J->g[tok]);
+            double *dqt = J->dq + tok * K, *dkt = J->dk + tok * K, *dvt = J->dv + tok * V;
+            /* h' = a h_prev, and u (with y = h'^T k) as in the forward step */
+            for (int64_t i = 0; i < KV; ++i)
+                hp[i] = a * hprev[i];
+            if (J->beta) {
+                const double bb = J->beta[tok];
+                for (int64_t j = 0; j < V; ++j)
+                    y[j] = 0.0;
+                for (int64_t i = 0; i < K; ++i)
+                    for (int64_t j = 0; j < V; ++j)
+                        y[j] += hp[i * V + j] * kt[i];
+                for (int64_t j = 0; j < V; ++j)
+                    u[j] = bb * (vt[j] - y[j]);
+            } else {
+                for (int64_t j = 0; j < V; ++j)
+                    u[j] = vt[j];
+            }
+            /* readout: dh += scale q do^T;  dq = scale h do */
+            for (int64_t i = 0; i < K; ++i)
+                for (int64_t j = 0; j < V; ++j)
+                    dh[i * V + j] += J->scale * qt[i] * dot[j];
+            for (int64_t i = 0; i < K; ++i) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < V; ++j)
+                    acc += hcur[i * V + j] * dot[j];
+                dqt[i] = J->scale * acc;
+            }
+            /* write h = h' + k u^T:  dk = dh u;  du = dh^T k */
+            for (int64_t i = 0; i < K; ++i) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < V; ++j)
+                    acc += dh[i * V + j] * u[j];
+                dkt[i] = acc;
+            }
+            for (int64_t j = 0; j < V; ++j)
+                du[j] = 0.0;
+            for (int64_t i = 0; i < K; ++i)
+                for (int64_t j = 0; j < V; ++j)
+                    du[j] += dh[i * V + j] * kt[i];
+            if (J->beta) {
+                /* u = b (v - y):  dv = b du;  db = <du, v - y>;  dy = -b du */
+                const double bb = J->beta[tok];
+                double db = 0.0;
+                for (int64_t j = 0; j < V; ++j) {
+                    dvt[j] = bb * du[j];
+                    db += du[j] * (vt[j] - y[j]);
+                }
+                J->dbeta[tok] = db;
+                /* y = h'^T k:  dh' += k dy^T;  dk += h' dy */
+                for (int64_t i = 0; i < K; ++i) {
+                    double acc = 0.0;
+                    for (int64_t j = 0; j < V; ++j) {
+                        const double dy = -bb * du[j];
+                        dh[i * V + j] += kt[i] * dy;
+                        acc += hp[i * V + j] * dy;
+                    }
+                    dkt[i] += acc;
+                }
+            } else {
+                for (int64_t j = 0; j < V; ++j)
+                    dvt[j] = du[j];
+            }
+            /* h' = a h_prev:  dg = a <dh', h_prev>;  dh_prev = a dh' */
+            double da = 0.0;
+            for (int64_t i = 0; i < KV; ++i)
+                da += dh[i] * hprev[i];
+            J->dg[tok] = a * da;
+            for (int64_t i = 0; i < KV; ++i)
+                dh[i] *= a;
+        }
+    }
+    if (J->dh0)
+        memcpy(J->dh0 + sidx, dh, sizeof(double) * (size_t)KV);
+    free(ck); free(st); free(dh); free(hp); free(u); free(y); free(du);
+    return 0;
+}
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *J = (bwd_job *)arg;
+    const int64_t total = J->N * J->H;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int64_t idx = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (idx >= total)
+            break;
+        if (J->pair_mask && !J->pair_mask[idx])
+            continue;
+        if (run_pair_bwd(J, idx / J->H, idx % J->H) != 0) {
+            pthread_mutex_lock(&J->mu);
+            J->failed = 1;
+            pthread_mutex_unlock(&J->mu);
+        }
+    }
+    return NULL;
+}
+
+/*
+ * gdr_oracle_bwd: gradients of L = <do, o> + <dht, ht> with respect to q, k,
+ * v, g, beta and h0, for every (sequence, head) pair.  Layouts as for
+ * gdr_oracle_fwd; do has o's layout, dht and dh0 the state layout.
+ *   beta == NULL -> beta-free mode (dbeta is not written)
+ *   h0 == NULL   -> zero initial state;  dht == NULL -> no final-state term
+ *   dh0 == NULL  -> the initial-state gradient is not kept
+ *   pair_mask    -> optional [N*H] bytes; pairs with 0 are skipped
+ * Returns the number of threads used (>= 1), or -1 on bad arguments / OOM.
+ */
+int gdr_oracle_bwd(const double *q, const double *k, const double *v,
+                   const double *g, const double *beta, const int64_t *cu,
+                   const double *h0, const double *dout, const double *dht,
+                   double *dq, double *dk, double *dv, double *dg,
+                   double *dbeta, double *dh0, int64_t B, int64_t T,
+                   int64_t H, int64_t K, int64_t V, int64_t N, double scale,
+                   const uint8_t *pair_mask, int n_threads)
+{
+    if (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg ||
+        (beta && !dbeta) || B < 1 || T < 0 || H < 1 || K < 1 || V < 1)
+        return -1;
+    if (cu) {
+        if (B != 1 || N < 0)
+            return -1;
+        if (cu[0] != 0 || cu[N] != T)
+            return -1;
+        for (int64_t n = 0; n < N; ++n)
+            if (cu[n + 1] < cu[n])
+                return -1;
+    } else {
+        N = B;
+    }
+    bwd_job J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.g = g; J.beta = beta; J.h0 = h0;
+    J.dout = dout; J.dht = dht;
+    J.dq = dq; J.dk = dk; J.dv = dv; J.dg = dg; J.dbeta = dbeta; J.dh0 = dh0;
+    J.cu = cu; J.pair_mask = pair_mask;
+    J.B = B; J.T = T; J.H = H; J.K = K; J.V = V; J.N = N;
+    J.scale = scale;
+    pthread_mutex_init(&J.mu, NULL);
+
+    if (n_threads <= 0) {
+        long c = sysconf(_SC_NPROCESSORS_ONLN);
+        n_threads = c > 0 ? (int)c : 1;
+    }
+    if ((int64_t)n_threads > N * H)
+        n_threads = (int)(N * H > 0 ? N * H : 1);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    if (!th) {
+        pthread_mutex_destroy(&J.mu);
+        return -1;
+    }
+    int started = 0;
+    for (int i = 0; i < n_threads - 1; ++i)
+        if (pthread_create(&th[started], NULL, bwd_worker, &J) == 0)
+            ++started;
+    bwd_worker(&J);
+    for (int i = 0; i < started; ++i)
+        pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.mu);
+    return J.failed ? -1 : started + 1;
 }
