@@ -324,31 +324,33 @@ typedef struct {
     pthread_mutex_t mu;
 } bwd_job;
 
-/* One forward token step on S (K x V) for token index tok, in place. */
-static void step_forward(const bwd_job *J, int64_t tok, double *S, double *u)
+/* One forward token step on the state hs (K x V) for token index tok, in
+ * place (the same step as run_pair's loop body, without the readout). */
+static void step_forward(const bwd_job *J, int64_t tok, double *hs, double *u)
 {
     const int64_t K = J->K, V = J->V;
     const double *kt = J->k + tok * K;
     const double *vt = J->v + tok * V;
-    const double a = exp(J->g[tok]);
+    const double g_t = J->g[tok];
+    const double a = exp(g_t);
     for (int64_t i = 0; i < K * V; ++i)
-        S[i] *= a;
+        hs[i] *= a;
     if (J->beta) {
-        const double b = J->beta[tok];
+        const double bb = J->beta[tok];
         for (int64_t j = 0; j < V; ++j)
             u[j] = 0.0;
         for (int64_t i = 0; i < K; ++i)
             for (int64_t j = 0; j < V; ++j)
-                u[j] += S[i * V + j] * kt[i];
+                u[j] += hs[i * V + j] * kt[i];
         for (int64_t j = 0; j < V; ++j)
-            u[j] = b * (vt[j] - u[j]);
+            u[j] = bb * (vt[j] - u[j]);
     } else {
         for (int64_t j = 0; j < V; ++j)
             u[j] = vt[j];
     }
     for (int64_t i = 0; i < K; ++i)
         for (int64_t j = 0; j < V; ++j)
-            S[i * V + j] += kt[i] * u[j];
+            hs[i * V + j] += kt[i] * u[j];
 }
 
 static int run_pair_bwd(bwd_job *J, int64_t n, int64_t hh)
@@ -358,7 +360,7 @@ static int run_pair_bwd(bwd_job *J, int64_t n, int64_t hh)
     if (J->cu) {
         row = 0;
         t0 = J->cu[n];
-        t1 = J->cu[n + 1];
+        t1 = J->cu[1 + n];
     } else {
         row = n;
         t0 = 0;
@@ -405,11 +407,12 @@ static int run_pair_bwd(bwd_job *J, int64_t n, int64_t hh)
             step_forward(J, (row * J->T + t) * H + hh, st + (t - s + 1) * KV, u);
         }
         for (int64_t t = e - 1; t >= s; --t) {
-            const int64_t tok = (row * J->T + t) * H + hh;
+            const int64_t tok = hh + H * (row * J->T + t);
             const double *kt = J->k + tok * K, *qt = J->q + tok * K;
             const double *vt = J->v + tok * V, *dot = J->dout + tok * V;
             const double *hprev = st + (t - s) * KV, *hcur = st + (t - s + 1) * KV;
-            const double a = exp(J->g[tok]);
+            const double g_t = J->g[tok];
+            const double a = exp(g_t);
             double *dqt = J->dq + tok * K, *dkt = J->dk + tok * K, *dvt = J->dv + tok * V;
             /* h' = a h_prev, and u (with y = h'^T k) as in the forward step */
             for (int64_t i = 0; i < KV; ++i)
