@@ -33,6 +33,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s and ms per gdr_chunk_fwd call on 1 GB300; % of roofline"
+METRIC_BWD = "tokens/s and ms per gdr_chunk_bwd call on 1 GB300; % of roofline"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "wide_varlen_bf16"
 L2_FLUSH_BYTES = 256 << 20
@@ -51,6 +52,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
+                    help="bwd times gdr_chunk_bwd (the backward pass) instead")
     return ap.parse_args()
 
 
@@ -231,10 +234,51 @@ def algorithmic_bytes(kernel, x, c):
     return None
 
 
+def bwd_algorithmic(kernel, x, c):
+    """(bytes, flops) per launch of a backward-pass kernel (and of the forward
+    recompute it runs): the operands each must read and the results it must
+    write once, and the multiply-adds of the chunked form's products with
+    causal halves counted once (L = 64 rows a chunk)."""
+    K, V, L = x["K"], x["V"], 64
+    es = 2 if x["dtype"] == "bf16" else 4
+    delta = x["beta"] is not None
+    th, ch, sh = c["token_heads"], c["chunk_heads"], c["seq_heads"]
+    st = sh * K * V * 4
+    f32 = 4
+    if kernel == "bwd_gram":
+        b = th * (2 * K * es + (4 if delta else 0)) + ch * L * f32 + ch * L * L * f32 * (3 if delta else 1)
+        fma = ch * (L * L * K * (1.0 if delta else 0.5) + (L ** 3 / 6 if delta else 0))
+    elif kernel == "bwd_dscan":
+        b = (ch * L * L * f32 + th * (V + 2 * K) * es + ch * L * f32 + ch * K * V * f32
+             + (ch * L * K * f32 + ch * L * V * f32 if delta else th * V * es) + 2 * st)
+        fma = ch * (L * L * V / 2 + (3 if delta else 2) * L * K * V)
+    elif kernel == "bwd_lk":
+        b = (th * V * es + (2 * ch * L * V * f32 if delta else th * V * es) + 2 * ch * K * V * f32
+             + ch * L * K * f32 * (3 if delta else 2))
+        fma = ch * ((3 if delta else 2) * L * K * V + K * V)
+    elif kernel == "bwd_local":
+        b = (ch * L * L * f32 * (3 if delta else 1) + th * (2 * K + 2 * V) * es
+             + ch * L * K * f32 * (3 if delta else 2) + ch * L * f32
+             + (2 * ch * L * V * f32 + th * 4 if delta else th * V * es)
+             + th * ((2 * K + (V if delta else 0)) * es + 4 + (4 if delta else 0)))
+        fma = ch * (L * L * V / 2 + L * L * K)
+        if delta:
+            fma += ch * (1.5 * L * L * V + 2.5 * L * L * K + L ** 3 / 2)
+    elif kernel == "simt_prep":
+        b = algorithmic_bytes(kernel, x, c)
+        fma = ch * ((L * L * K / 2 + L ** 3 / 6 + L * L * (K + V) / 2) if delta else 0)
+    elif kernel == "simt_scan_serial":
+        b = algorithmic_bytes(kernel, x, c)
+        fma = ch * (2 if delta else 1) * L * K * V
+    else:
+        return None, None
+    return b, 2.0 * fma
+
+
 # The translation unit each kernel is compiled from (plus every shared header).
 KERNEL_SOURCES = {"tc_prep": "tc_prep.cu", "tc_chain": "tc_chain.cu", "tc_gla": "tc_gla.cu",
                   "tc_prescan": "tc_prescan.cu", "recurrent": "recurrent.cu",
-                  "compose": "compose.cu", "simt": "simt_path.cu"}
+                  "compose": "compose.cu", "simt": "simt_path.cu", "bwd": "simt_bwd.cu"}
 
 
 def traffic_record(kernel, workload):
@@ -297,6 +341,56 @@ def time_oracle_on(xo, seqs):
     return time.perf_counter() - t0, tokens, threads
 
 
+def time_oracle_bwd_on(xo, seqs, do, dht):
+    """The oracle's backward pass on the (sequence, head) pairs of `seqs`."""
+    import numpy as np
+    import oracle
+    N, H = xo["N"], xo["H"]
+    mask = np.zeros(N * H, dtype=bool)
+    for n in seqs:
+        mask[n * H:(n + 1) * H] = True
+    if xo["cu_seqlens"] is not None:
+        cu = xo["cu_seqlens"].tolist()
+        tokens = sum(cu[n + 1] - cu[n] for n in seqs)
+    else:
+        tokens = xo["T"] * len(seqs)
+    t0 = time.perf_counter()
+    oracle.backward(xo["q"], xo["k"], xo["v"], xo["g"], xo["beta"], cu_seqlens=xo["cu_seqlens"],
+                    h0=xo["h0"], do=do, dht=dht, pair_mask=mask)
+    threads = min(os.cpu_count() or 1, len(seqs) * H)
+    return time.perf_counter() - t0, tokens, threads
+
+
+def bwd_grads_in(x, seed=7):
+    """Seeded incoming gradients of the backward benchmark: do in the input
+    dtype, dht FP32."""
+    import torch
+    gen = torch.Generator().manual_seed(seed)
+    do = torch.randn(x["v"].shape, generator=gen).to(x["v"].dtype)
+    dht = torch.randn(x["N"], x["H"], x["K"], x["V"], generator=gen)
+    return do, dht
+
+
+def cpu_baseline_bwd(x, budget_s):
+    import oracle
+    xo = oracle_inputs(x)
+    do, dht = bwd_grads_in(x)
+    do, dht = oracle._f64(do), oracle._f64(dht)
+    N = xo["N"]
+    secs, toks, threads, groups, n = 0.0, 0, 1, 0, 0
+    while secs < budget_s and n < 64 * N:
+        group = [(n + j) % N for j in range(min(4, N))]
+        dt, tk, threads = time_oracle_bwd_on(xo, group, do, dht)
+        secs += dt
+        toks += tk
+        groups += 1
+        n += len(group)
+    return {"value": toks / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{groups} groups of 4 sequences x all {xo['H']} heads cycling over "
+                      f"the {N}-sequence batch ({toks} tokens), FP64 reverse token "
+                      f"recurrence, {secs:.1f} s"}
+
+
 def cpu_baseline(x, budget_s):
     """Times the oracle over groups of 4 sequences (all heads), cycling
     through the batch, until about `budget_s` seconds of CPU work (at most
@@ -329,21 +423,31 @@ def run_reference(args):
     N = xo["N"]
     per_step = 1 if N >= 1 else 0
     times, toks, threads = [], [], 1
+    if args.which == "bwd":
+        import oracle
+        do, dht = bwd_grads_in(x)
+        do, dht = oracle._f64(do), oracle._f64(dht)
     for i in range(args.warmup + args.steps):
         seqs = [(i * per_step + j) % N for j in range(per_step)]
-        dt, tk, threads = time_oracle_on(xo, seqs)
+        if args.which == "bwd":
+            dt, tk, threads = time_oracle_bwd_on(xo, seqs, do, dht)
+        else:
+            dt, tk, threads = time_oracle_on(xo, seqs)
         if i >= args.warmup:
             times.append(dt)
             toks.append(tk)
     value = sum(toks) / sum(times)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+    line = {"impl": "reference", "metric": METRIC_BWD if args.which == "bwd" else METRIC,
+            "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(args, x, None),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"each step one sequence x all {xo['H']} heads of the "
-                                       "workload (cycling), FP64 token recurrence"},
+                                       "workload (cycling), FP64 token recurrence"
+                                       + (" and its reverse (backward)" if args.which == "bwd"
+                                          else "")},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -648,10 +752,178 @@ def run_decode(args):
         dist.destroy_process_group()
 
 
+def run_bwd(args):
+    """gdr_chunk_bwd on a workload: the gradients of <do, o> + <dht, ht> for
+    seeded do / dht, inputs resident in HBM."""
+    import torch
+    import chunked_gated_delta_rule_gb300 as pkg
+    from chunked_gated_delta_rule_gb300 import synthetic
+
+    rank, local, world = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synthetic.WORKLOADS[args.workload]
+    x = synthetic.make_inputs(w)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+    do_h, dht_h = bwd_grads_in(x)
+    do, dht = do_h.to(dev), dht_h.to(dev)
+    outs = dict(dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]),
+                dv=torch.empty_like(d["v"]), dg=torch.empty_like(d["g"]),
+                dbeta=None if d["beta"] is None else torch.empty_like(d["beta"]),
+                dh0=torch.empty(x["N"], x["H"], x["K"], x["V"], dtype=torch.float32, device=dev))
+    args_t = (d["q"], d["k"], d["v"], d["g"], d["beta"], do)
+    kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], dht=dht, **outs)
+    c = counts(x)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        pkg.gdr_chunk_bwd(*args_t, **kw)
+    torch.cuda.synchronize()
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_index_for_smi()) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if hasattr(torch.cuda, "_sleep"):  # outside the timed region, as in run_gdr
+        torch.cuda._sleep(4_000_000)
+    pkg.gdr_chunk_bwd(*args_t, **kw)
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        pkg.gdr_chunk_bwd(*args_t, **kw)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = max_over_ranks(statistics.mean(step_ms), world)
+
+    timers = [pkg.LaunchTimer(16) for _ in range(K)]
+    kstarts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    kends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        kstarts[i].record(stream)
+        pkg.gdr_chunk_bwd(*args_t, timer=timers[i], **kw)
+        kends[i].record(stream)
+    torch.cuda.synchronize()
+    kstep_ms = [s.elapsed_time(e) for s, e in zip(kstarts, kends)]
+    per_kernel, launches = {}, 0
+    for t in timers:
+        launches += t.count
+        for i, kid in enumerate(t.ids):
+            per_kernel.setdefault(pkg.gdr_kernel_name(kid), []).append(t.elapsed_ms(i))
+    kernels = {}
+    peaks = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    sm_mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    fp32_tflops = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    for n, v in per_kernel.items():
+        b, f = bwd_algorithmic(n, x, c)
+        k_ms = statistics.mean(v)
+        kernels[n] = {"launches": len(v), "avg_ms": k_ms, "share": sum(v) / sum(kstep_ms),
+                      "hbm_frac": b / (k_ms * 1e-3) / 1e9 / hbm if b else None,
+                      "fp32_frac": f / (k_ms * 1e-3) / 1e12 / fp32_tflops if f else None}
+    dom = max(per_kernel, key=lambda n: sum(per_kernel[n]))
+    b, f = bwd_algorithmic(dom, x, c)
+    dom_ms = statistics.mean(per_kernel[dom])
+    hb = b / (dom_ms * 1e-3) / 1e9 if b else 0.0
+    fl = f / (dom_ms * 1e-3) / 1e12 if f else 0.0
+    if f and fl / fp32_tflops >= hb / hbm:
+        roofline = {"kernel": dom, "bound": "alu", "achieved": fl, "peak": fp32_tflops,
+                    "unit": "TFLOP/s", "frac": fl / fp32_tflops, "traffic": traffic_record(dom, args.workload),
+                    "algorithmic_flops_per_launch": f, "avg_launch_ms": dom_ms,
+                    "peak_source": "FP32 CUDA-core peak: 152 SMs x 128 lanes x 2 flops x "
+                                   f"{sm_mhz:.0f} MHz (no measured FP32 peak)"}
+    else:
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": hb, "peak": hbm, "unit": "GB/s",
+                    "frac": hb / hbm, "traffic": traffic_record(dom, args.workload),
+                    "algorithmic_bytes_per_launch": b, "avg_launch_ms": dom_ms,
+                    "peak_source": peaks["source"] + " (hbm_gbs, copy bandwidth)"}
+    roofline["timing"] = ("CUDA events around each launch on its stream, over a second pass "
+                          "of the same K steps")
+    es = 2 if x["dtype"] == "bf16" else 4
+    th, Kd, V = c["token_heads"], x["K"], x["V"]
+    delta = x["beta"] is not None
+    call_bytes = (th * ((2 * Kd + 2 * V) * es + 4 + (4 if delta else 0))      # q k v do g beta
+                  + th * ((2 * Kd + V) * es + 4 + (4 if delta else 0))        # dq dk dv dg dbeta
+                  + c["seq_heads"] * Kd * V * 4 * (2 + (1 if x["h0"] is not None else 0)))
+    call_roofline = {"achieved": call_bytes / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": call_bytes / (ms * 1e-3) / 1e9 / hbm, "algorithmic_bytes": call_bytes}
+
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()}
+        do_p, dht_p = do_h.pin_memory(), dht_h.pin_memory()
+        host_out = {k: (None if v is None else torch.empty(v.shape, dtype=v.dtype).pin_memory())
+                    for k, v in outs.items()}
+        names = ("q", "k", "v", "g", "beta", "cu_seqlens", "h0")
+
+        def e2e_step():
+            for nme in names:
+                if pin[nme] is not None:
+                    d[nme].copy_(pin[nme], non_blocking=True)
+            do.copy_(do_p, non_blocking=True)
+            dht.copy_(dht_p, non_blocking=True)
+            pkg.gdr_chunk_bwd(*args_t, **kw)
+            for k2, t in outs.items():
+                if t is not None:
+                    host_out[k2].copy_(t, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        ke = max(3, min(K, 20))
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, world)
+        h2d = sum(pin[nme].numel() * pin[nme].element_size() for nme in names
+                  if pin[nme] is not None) + do_p.numel() * do_p.element_size() + dht_p.numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values() if t is not None)
+        e2e = {"value": world * c["tokens"] / (e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "steps": ke, "api": "gdr_chunk_bwd, inputs and gradients through pinned host "
+                                   "buffers (copies on the calling stream)"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_bwd(x, args.cpu_seconds)
+    if rank == 0:
+        cfg = config_of(args, x, None)
+        cfg["entry_point"] = "gdr_chunk_bwd"
+        cfg["incoming_gradients"] = "do ~ N(0,1) in the input dtype, dht ~ N(0,1) FP32, seed 7"
+        line = {"metric": METRIC_BWD, "value": world * c["tokens"] / (ms * 1e-3), "unit": UNIT,
+                "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic (seeded; shapes and distributions of the workload)",
+                "config": cfg, "roofline": roofline, "call_roofline": call_roofline,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "kernels": kernels,
+                "clocks": clocks,
+                "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
+                            "p10": sorted(step_ms)[len(step_ms) // 10],
+                            "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]}}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.which == "bwd":
+        run_bwd(args)
     elif args.workload.startswith("decode"):
         run_decode(args)
     else:

@@ -6,6 +6,7 @@ seeded synthetic input generator.  There is no CPU fallback: every entry
 point raises if the CUDA library is missing.
 """
 from .api import (GdrError, LaunchTimer, gdr_chunk_fwd, gdr_chunk_fwd_host,  # noqa: F401
+                  gdr_chunk_bwd, gdr_bwd_workspace_size,
                   gdr_chunk_fwd_noalloc, gdr_recurrent_fwd,
                   gdr_error_string, gdr_kernel_name, gdr_plan_query, gdr_release_cached,
                   gdr_version,

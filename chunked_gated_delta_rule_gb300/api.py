@@ -45,7 +45,7 @@ SELFTEST_EXPORTS = ("gdr_selftest_umma", "gdr_selftest_tma", "gdr_selftest_inver
 # Every symbol include/gdr.h declares.
 EXPORTS = ("gdr_chunk_fwd", "gdr_chunk_fwd_ex", "gdr_chunk_fwd_host", "gdr_chunk_fwd_noalloc",
            "gdr_workspace_size", "gdr_plan_query", "gdr_recurrent_fwd", "gdr_kernel_name", "gdr_error_string",
-           "gdr_release_cached", "gdr_version")
+           "gdr_release_cached", "gdr_version", "gdr_chunk_bwd", "gdr_bwd_workspace_size")
 
 _lib = None
 _lock = threading.Lock()
@@ -82,6 +82,11 @@ def load_library():
         lib.gdr_recurrent_fwd.argtypes = [dims_p, vp, vp, vp, vp, vp, i32p, vp, ctypes.c_int64,
                                           i32p, vp, vp, vp]
         lib.gdr_recurrent_fwd.restype = ctypes.c_int
+        lib.gdr_chunk_bwd.argtypes = [dims_p, vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, vp,
+                                      vp, vp, vp, ctypes.POINTER(gdr_options), vp]
+        lib.gdr_chunk_bwd.restype = ctypes.c_int
+        lib.gdr_bwd_workspace_size.argtypes = [dims_p, ctypes.c_int]
+        lib.gdr_bwd_workspace_size.restype = ctypes.c_size_t
         lib.gdr_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.c_int]
         lib.gdr_workspace_size.restype = ctypes.c_size_t
         lib.gdr_plan_query.argtypes = [dims_p, ctypes.c_int, ctypes.c_int,
@@ -249,6 +254,70 @@ def gdr_chunk_fwd(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments
     if rc != 0:
         raise GdrError(rc)
     return o, ht
+
+
+def gdr_chunk_bwd(q, k, v, g, beta, do, cu_seqlens=None, h0=None, dht=None, *,
+                  state_layout="kv", want_dh0=True, scale=0.0, workspace=None, status=None,
+                  dq=None, dk=None, dv=None, dg=None, dbeta=None, dh0=None, stream=None,
+                  timer=None):
+    """Backward pass on CUDA tensors: the gradients of ``<do, o> + <dht, ht>``
+    for the forward pass on the same inputs.  Returns ``(dq, dk, dv, dg,
+    dbeta, dh0)``: dq, dk, dv in the input dtype, the rest float32; ``dbeta``
+    is None in the beta-free mode and ``dh0`` None unless ``want_dh0``.  Work
+    is enqueued on ``stream`` (default: torch's current stream)."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdr_chunk_bwd takes CUDA tensors")
+    _check("q", q, None, dev)
+    for name, t in (("k", k), ("v", v), ("do", do)):
+        _check(name, t, q.dtype, dev)
+    if do.shape != v.shape:
+        raise ValueError("do must have v's shape")
+    _check("g", g, torch.float32, dev)
+    _check("beta", beta, torch.float32, dev)
+    _check_cu(cu_seqlens, dev)
+    _check("h0", h0, torch.float32, dev)
+    _check("dht", dht, torch.float32, dev)
+    dims = _dims_of(q, v, cu_seqlens, state_layout)
+    nseq = dims.N if dims.N else dims.B
+    dq = torch.empty(q.shape, dtype=q.dtype, device=dev) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=q.dtype, device=dev) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=q.dtype, device=dev) if dv is None else dv
+    dg = torch.empty(g.shape, dtype=torch.float32, device=dev) if dg is None else dg
+    if beta is not None and dbeta is None:
+        dbeta = torch.empty(beta.shape, dtype=torch.float32, device=dev)
+    if want_dh0 and dh0 is None:
+        dh0 = torch.empty(nseq, dims.H, *_state_dims(dims, state_layout), dtype=torch.float32,
+                          device=dev)
+    for name, t, dt in (("dq", dq, q.dtype), ("dk", dk, q.dtype), ("dv", dv, q.dtype),
+                        ("dg", dg, torch.float32), ("dbeta", dbeta, torch.float32),
+                        ("dh0", dh0, torch.float32)):
+        _check(name, t, dt, dev)
+    opt = gdr_options(float(scale), 0, 0,
+                      None if workspace is None else workspace.data_ptr(),
+                      0 if workspace is None else workspace.numel() * workspace.element_size(),
+                      None if status is None else status.data_ptr())
+    if timer is not None:
+        opt.events = ctypes.cast(timer._handles, ctypes.c_void_p)
+        opt.max_launches = timer.max
+        opt.launch_ids = ctypes.cast(timer._ids, ctypes.c_void_p)
+        opt.n_launches = ctypes.cast(ctypes.pointer(timer._count), ctypes.c_void_p)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.gdr_chunk_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                               _ptr(beta), _ptr(cu_seqlens), _ptr(h0), _ptr(do), _ptr(dht),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0),
+                               ctypes.byref(opt), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise GdrError(rc)
+    return dq, dk, dv, dg, dbeta, dh0
+
+
+def gdr_bwd_workspace_size(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, flags=0) -> int:
+    return int(load_library().gdr_bwd_workspace_size(
+        ctypes.byref(make_dims(B, T, H, K, V, N, dtype, flags)), int(beta_free)))
 
 
 def gdr_recurrent_fwd(q, k, v, g, beta=None, cu_seqlens=None, *, state, state_indices=None,

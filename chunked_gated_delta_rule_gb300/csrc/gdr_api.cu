@@ -308,6 +308,54 @@ Workspace carve_workspace(void *base, const WorkspaceLayout &L, int S) {
     return w;
 }
 
+// Backward scratch: the CUDA-core forward workspace (serial plan) followed by
+// the per-(chunk, head) buffers of BwdWs.
+struct BwdLayout {
+    WorkspaceLayout fwd;
+    size_t off_Mq, off_Kd, off_Tm, off_dhend, off_dvn, off_P1, off_P2, off_P3, off_ehp, total;
+};
+
+BwdLayout bwd_layout(const gdr_dims &d, bool beta_free) {
+    BwdLayout B{};
+    B.fwd = workspace_layout(d, beta_free, 1, 1);
+    size_t off = B.fwd.total;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes);
+        return at;
+    };
+    const bool delta = !beta_free;
+    const size_t items = (size_t)B.fwd.max_chunks * (size_t)d.H;
+    const size_t K = (size_t)d.K, V = (size_t)d.V, sq = (size_t)kChunk * kChunk;
+    B.off_Mq = take(sizeof(float) * items * sq);
+    B.off_Kd = take(delta ? sizeof(float) * items * sq : 0);
+    B.off_Tm = take(delta ? sizeof(float) * items * sq : 0);
+    B.off_dhend = take(sizeof(float) * items * K * V);
+    B.off_dvn = take(delta ? sizeof(float) * items * kChunk * V : 0);
+    B.off_P1 = take(sizeof(float) * items * kChunk * K);
+    B.off_P2 = take(delta ? sizeof(float) * items * kChunk * K : 0);
+    B.off_P3 = take(sizeof(float) * items * kChunk * K);
+    B.off_ehp = take(sizeof(float) * items * ((K + 63) / 64));
+    B.total = off;
+    return B;
+}
+
+BwdWs carve_bwd(void *base, const BwdLayout &B) {
+    char *b = static_cast<char *>(base);
+    auto f = [&](size_t at) { return reinterpret_cast<float *>(b + at); };
+    BwdWs w{};
+    w.Mq = f(B.off_Mq);
+    w.Kd = f(B.off_Kd);
+    w.Tm = f(B.off_Tm);
+    w.dhend = f(B.off_dhend);
+    w.dvn = f(B.off_dvn);
+    w.P1 = f(B.off_P1);
+    w.P2 = f(B.off_P2);
+    w.P3 = f(B.off_P3);
+    w.ehp = f(B.off_ehp);
+    return w;
+}
+
 namespace {
 
 #define GDR_TRY(expr)                                                  \
@@ -370,6 +418,17 @@ int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStre
     return GDR_OK;
 }
 
+// Backward: the forward recompute of the CUDA-core path (serial scan: the
+// state before each chunk and V'), then the backward kernels.
+int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw, int bv,
+            cudaStream_t st, LaunchRecorder &rec) {
+    GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
+    GDR_LAUNCH(rec, kKPrep, simt_prep(p, ws, st));
+    GDR_LAUNCH(rec, kKScanSerial, simt_scan(p, ws, 0, bv, st));
+    GDR_TRY(simt_bwd(p, ws, a, bw, st, rec));
+    return GDR_OK;
+}
+
 }  // namespace
 }  // namespace gdr
 
@@ -405,6 +464,10 @@ const char *gdr_kernel_name(int id) {
     case kKTcGlaSegOut: return "tc_gla_segment_out";
     case kKComposeScalar: return "compose_scalar";
     case kKTcPreDual: return "tc_prescan_dual";
+    case kKBwdGram: return "bwd_gram";
+    case kKBwdScan: return "bwd_dscan";
+    case kKBwdLk: return "bwd_lk";
+    case kKBwdLocal: return "bwd_local";
     default: return "?";
     }
 }
@@ -531,6 +594,71 @@ int gdr_chunk_fwd(const gdr_dims *dims, const void *q, const void *k, const void
                   gdr_stream_t stream) {
     return gdr_chunk_fwd_ex(dims, q, k, v, g, beta, cu_seqlens, h0, o, ht, n_segments,
                             nullptr, stream);
+}
+
+size_t gdr_bwd_workspace_size(const gdr_dims *dims, int beta_free) {
+    if (validate_dims(dims) != GDR_OK) return 0;
+    return bwd_layout(*dims, beta_free != 0).total;
+}
+
+int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void *v,
+                  const float *g, const float *beta, const int32_t *cu_seqlens,
+                  const float *h0, const void *dout, const float *dht, void *dq, void *dk,
+                  void *dv, float *dg, float *dbeta, float *dh0, const gdr_options *opt,
+                  gdr_stream_t stream) {
+    int rc = validate_dims(dims);
+    if (rc != GDR_OK) return rc;
+    if (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg) return GDR_ERR_INVALID;
+    if ((beta != nullptr) != (dbeta != nullptr)) return GDR_ERR_INVALID;
+    if ((cu_seqlens != nullptr) != is_varlen(*dims)) return GDR_ERR_INVALID;
+    if (opt && !(opt->scale >= 0.f)) return GDR_ERR_INVALID;  // rejects NaN too
+    if (opt && (opt->force_path != 0 || opt->force_bv != 0)) return GDR_ERR_INVALID;
+    const bool beta_free = beta == nullptr;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    Problem p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+    if (dims->flags & GDR_SEQLENS_I64) p.cu64 = reinterpret_cast<const int64_t *>(cu_seqlens);
+    else p.cu = cu_seqlens;
+    p.state_vk = (dims->flags & GDR_STATE_VK) != 0;
+    p.h0 = h0;
+    p.B = dims->B; p.T = dims->T; p.H = dims->H; p.K = dims->K; p.V = dims->V;
+    p.N = n_seqs(*dims);
+    p.dtype = dims->dtype;
+    p.scale = (opt && opt->scale > 0.f) ? opt->scale : 1.0f / std::sqrt((float)dims->K);
+    p.status = opt ? opt->status : nullptr;
+    if (p.N == 0) return GDR_OK;
+
+    const BwdLayout B = bwd_layout(*dims, beta_free);
+    void *base = nullptr;
+    bool owned = false;
+    if (opt && opt->workspace) {
+        if (opt->workspace_bytes < B.total) return GDR_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(opt->workspace) % kAlign) return GDR_ERR_INVALID;
+        base = opt->workspace;
+    } else {
+        if (lib_malloc(&base, B.total, st) != cudaSuccess) return GDR_ERR_CUDA;
+        owned = true;
+    }
+    const Workspace ws = carve_workspace(base, B.fwd, 1);
+    const BwdWs bw = carve_bwd(base, B);
+    BwdArgs a{};
+    a.dout = dout; a.dht = dht; a.dq = dq; a.dk = dk; a.dv = dv;
+    a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+    LaunchRecorder rec;
+    rec.st = st;
+    if (opt) {
+        rec.events = reinterpret_cast<cudaEvent_t *>(opt->events);
+        rec.max_launches = opt->events ? opt->max_launches : 0;
+        rec.ids = opt->launch_ids;
+        if (!opt->events && opt->launch_ids) rec.max_launches = opt->max_launches;
+    }
+    rc = run_bwd(p, ws, a, bw, pick_bv(*dims), st, rec);
+    if (opt && opt->n_launches) *opt->n_launches = rec.count;
+    if (owned) {
+        if (cudaFreeAsync(base, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;
+    }
+    return rc;
 }
 
 int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k, const void *v,

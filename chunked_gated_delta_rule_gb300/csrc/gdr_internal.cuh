@@ -105,6 +105,29 @@ struct Workspace {
     int n_segments;       // S (1 = serial)
 };
 
+// Backward pass: the caller's gradient tensors (dq, dk, dv in the input
+// dtype; dg, dbeta, dh0 FP32; dht / dh0 in the state layout of h0).
+struct BwdArgs {
+    const void *dout;   // [B,T,H,V] dL/do
+    const float *dht;   // [N,H,K,V] dL/dht or nullptr
+    void *dq, *dk, *dv; // [B,T,H,K] / [B,T,H,V]
+    float *dg, *dbeta;  // [B,T,H]; dbeta nullptr in the beta-free mode
+    float *dh0;         // [N,H,K,V] or nullptr
+};
+
+// Backward scratch, per (chunk, head) item.
+struct BwdWs {
+    float *Mq;     // [items][64][64] causal(Q K^T * D), diagonal included
+    float *Kd;     // [items][64][64] strictly lower K K^T * D (delta)
+    float *Tm;     // [items][64][64] T = (I + A)^-1 (delta)
+    float *dhend;  // [items][K][V] dL/d(state at the chunk's end)
+    float *dvn;    // [items][64][V] dL/dV' (delta)
+    float *P1;     // [items][64][K] dO h^T
+    float *P2;     // [items][64][K] dV' h^T (delta)
+    float *P3;     // [items][64][K] V' E^T
+    float *ehp;    // [items][ceil(K/64)] <E, h> per 64-key slice
+};
+
 // Byte layout of the workspace for one problem.
 struct WorkspaceLayout {
     size_t off_tab, off_seq0, off_nchunks, off_order, off_G, off_W, off_U, off_hpre,
@@ -135,6 +158,10 @@ enum KernelId {
     kKTcGlaSegOut = 13,
     kKComposeScalar = 14,
     kKTcPreDual = 15,
+    kKBwdGram = 16,
+    kKBwdScan = 17,
+    kKBwdLk = 18,
+    kKBwdLocal = 19,
     kKNumIds
 };
 
@@ -170,6 +197,9 @@ cudaError_t simt_scan(const Problem &p, const Workspace &ws, int mode, int bv,
 cudaError_t simt_compose(const Problem &p, const Workspace &ws, int bv,
                          cudaStream_t st);
 cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st);
+// Backward pass after the serial forward recompute (G, W, hpre, vnew in ws).
+cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
+                     cudaStream_t st, LaunchRecorder &rec);
 // Composition for the delta rule with K <= 128 and V % 32 == 0 (both paths):
 // bulk-copied transposed transitions, 32 value columns per CTA.
 bool compose_mt_supported(const Problem &p);

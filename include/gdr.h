@@ -225,6 +225,41 @@ int gdr_recurrent_fwd(const gdr_dims *dims, const void *q, const void *k,
                       const int32_t *state_indices, void *o, int32_t *status,
                       gdr_stream_t stream);
 
+/*
+ * gdr_chunk_bwd -- the backward pass: the gradients of
+ * L = <do, o> + <dht, ht> with respect to q, k, v, g, beta and h0, where o
+ * and ht are what gdr_chunk_fwd computes from the same inputs.  The state
+ * gradient runs backward over the chunks (the reverse dH recurrence of the
+ * flash-linear-attention ABC issue #23 pages, "Problem" and "Proposed
+ * Dataflow" step 4; gradients dQ/dK/dV and of the states, its
+ * "Fixture-First Correctness Contract"), through the chunked form's WY
+ * factors.  FP32 arithmetic on CUDA cores for every input type.
+ *   dims, q, k, v, g, beta, cu_seqlens, h0   as for gdr_chunk_fwd (device).
+ *   dout    [B,T,H,V] dL/do, the input dtype.
+ *   dht     [Nseq,H,K,V] FP32 dL/dht (state layout of h0), or NULL for 0.
+ *   dq, dk  [B,T,H,K], dv [B,T,H,V] outputs in the input dtype.
+ *   dg      [B,T,H] FP32 output;  dbeta [B,T,H] FP32 output, required
+ *           exactly when beta is given (NULL in the beta-free mode).
+ *   dh0     [Nseq,H,K,V] FP32 output (state layout of h0), or NULL.
+ *   opt     NULL, or gdr_options with scale, status, workspace (at least
+ *           gdr_bwd_workspace_size bytes) and the launch events;
+ *           force_path and force_bv must be 0.
+ * The pass recomputes the forward states (the CUDA-core forward kernels)
+ * and then runs four backward kernels; work is enqueued on `stream`, not
+ * synchronised.  Every gradient is written for every token of every
+ * sequence; results are bit-identical from run to run.
+ */
+int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k,
+                  const void *v, const float *g, const float *beta,
+                  const int32_t *cu_seqlens, const float *h0,
+                  const void *dout, const float *dht, void *dq, void *dk,
+                  void *dv, float *dg, float *dbeta, float *dh0,
+                  const gdr_options *opt, gdr_stream_t stream);
+
+/* Bytes of device scratch gdr_chunk_bwd needs for this problem (beta_free
+ * != 0 for the beta-free mode).  0 on invalid arguments. */
+size_t gdr_bwd_workspace_size(const gdr_dims *dims, int beta_free);
+
 /* Bytes of device scratch gdr_chunk_fwd_ex needs for this problem
  * (beta_free != 0 for the beta-free mode).  0 on invalid arguments. */
 size_t gdr_workspace_size(const gdr_dims *dims, int beta_free,
