@@ -95,6 +95,82 @@ __device__ __forceinline__ void load_mat_tile(float *dst, const float *src, int 
     }
 }
 
+// Register-tiled products on shared-memory tiles.  Thread t owns the rows
+// 4 (t >> 4) + r (r < 4) and the columns (t & 15) + 16 s (s < NS) of a
+// 64 x 16 NS result: per reduction step it loads 4 + NS values for 4 NS
+// multiply-adds.  A warp reads two rows of the left operand (two addresses)
+// and sixteen consecutive rows or columns of the right one, so no step has a
+// bank conflict with 65-float rows.  The reduction runs in ascending order
+// for every output, so each element has one fixed summation order.
+template <int NS>
+__device__ __forceinline__ void acc_zero(float (&a)[4][NS]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s = 0; s < NS; ++s) a[r][s] = 0.f;
+}
+
+// a += A B^T over n:  A[i][c] (row stride lda), B[j][c] (ldb)
+template <int NS>
+__device__ __forceinline__ void mm_abT(float (&a)[4][NS], const float *A, int lda, const float *B,
+                                       int ldb, int n, int tid) {
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
+#pragma unroll 4
+    for (int c = 0; c < n; ++c) {
+        float x[4], y[NS];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) x[r] = A[(i0 + r) * lda + c];
+#pragma unroll
+        for (int s = 0; s < NS; ++s) y[s] = B[(j0 + 16 * s) * ldb + c];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int s = 0; s < NS; ++s) a[r][s] = fmaf(x[r], y[s], a[r][s]);
+    }
+}
+
+// a += A^T B over n:  A[m][i] (lda), B[m][j] (ldb)
+template <int NS>
+__device__ __forceinline__ void mm_atb(float (&a)[4][NS], const float *A, int lda, const float *B,
+                                       int ldb, int n, int tid) {
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
+#pragma unroll 4
+    for (int m = 0; m < n; ++m) {
+        float x[4], y[NS];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) x[r] = A[m * lda + i0 + r];
+#pragma unroll
+        for (int s = 0; s < NS; ++s) y[s] = B[m * ldb + j0 + 16 * s];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int s = 0; s < NS; ++s) a[r][s] = fmaf(x[r], y[s], a[r][s]);
+    }
+}
+
+// a += A B over n:  A[i][m] (lda), B[m][j] (ldb)
+template <int NS>
+__device__ __forceinline__ void mm_ab(float (&a)[4][NS], const float *A, int lda, const float *B,
+                                      int ldb, int n, int tid) {
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
+#pragma unroll 4
+    for (int m = 0; m < n; ++m) {
+        float x[4], y[NS];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) x[r] = A[(i0 + r) * lda + m];
+#pragma unroll
+        for (int s = 0; s < NS; ++s) y[s] = B[m * ldb + j0 + 16 * s];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int s = 0; s < NS; ++s) a[r][s] = fmaf(x[r], y[s], a[r][s]);
+    }
+}
+
+#define FOR_TILE(NS)                                                      \
+    _Pragma("unroll") for (int r = 0; r < 4; ++r)                         \
+        _Pragma("unroll") for (int s = 0; s < NS; ++s)
+
 // ---------------------------------------------------------------------------
 // k_bwd_gram: M = causal(Q K^T * D) (diagonal included), Kd = strictly lower
 // (K K^T * D) and, in delta mode, T = (I + diag(beta) Kd)^-1.
@@ -113,9 +189,9 @@ __global__ void __launch_bounds__(kBT) k_bwd_gram(Problem p, Workspace ws, BwdWs
         sG[tid] = ws.G[(gc * H + h) * kChunk + tid];
         sB[tid] = (delta && tid < ci.len) ? p.beta[(ci.t0 + tid) * H + h] : 0.f;
     }
-    float qk[16], kk[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) qk[r] = kk[r] = 0.f;
+    float qk[4][4], kk[4][4];
+    acc_zero(qk);
+    acc_zero(kk);
     const Tin *q = static_cast<const Tin *>(p.q);
     const Tin *k = static_cast<const Tin *>(p.k);
     for (int c0 = 0; c0 < K; c0 += kSl) {
@@ -123,30 +199,20 @@ __global__ void __launch_bounds__(kBT) k_bwd_gram(Problem p, Workspace ws, BwdWs
         load_tok_tile(sQ, q, ci.t0, ci.len, H, h, K, c0, tid);
         load_tok_tile(sK, k, ci.t0, ci.len, H, h, K, c0, tid);
         __syncthreads();
-        const int j = tid & 63;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int i = (tid >> 6) + 4 * r;
-            float a = qk[r], b = kk[r];
-            for (int c = 0; c < kSl; ++c) {
-                a = fmaf(sQ[i * kLd + c], sK[j * kLd + c], a);
-                b = fmaf(sK[i * kLd + c], sK[j * kLd + c], b);
-            }
-            qk[r] = a;
-            kk[r] = b;
-        }
+        const int kn = min(kSl, K - c0);
+        mm_abT<4>(qk, sQ, kLd, sK, kLd, kn, tid);
+        if (delta) mm_abT<4>(kk, sK, kLd, sK, kLd, kn, tid);
     }
     float *Mg = bw.Mq + (gc * H + h) * (int64_t)kChunk * kChunk;
     float *Kdg = bw.Kd + (gc * H + h) * (int64_t)kChunk * kChunk;
-    const int j = tid & 63;
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        const int i = (tid >> 6) + 4 * r;
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
+    FOR_TILE(4) {
+        const int i = i0 + r, j = j0 + 16 * s;
         const bool in = i < ci.len;
         const float d = (in && j <= i) ? expf(sG[i] - sG[j]) : 0.f;
-        Mg[i * kChunk + j] = (in && j <= i) ? qk[r] * d : 0.f;
+        Mg[i * kChunk + j] = (in && j <= i) ? qk[r][s] * d : 0.f;
         if (delta) {
-            const float kd = (in && j < i) ? kk[r] * d : 0.f;
+            const float kd = (in && j < i) ? kk[r][s] * d : 0.f;
             Kdg[i * kChunk + j] = kd;
             sA[i * kLd + j] = sB[i] * kd;
         }
@@ -163,9 +229,9 @@ __global__ void __launch_bounds__(kBT) k_bwd_gram(Problem p, Workspace ws, BwdWs
             } else if (i == m) {
                 x = 1.f;
             } else {
-                float s = 0.f;
-                for (int jj = m; jj < i; ++jj) s = fmaf(sA[i * kLd + jj], sQ[jj * kLd + m], s);
-                x = -s;
+                float sum = 0.f;
+                for (int jj = m; jj < i; ++jj) sum = fmaf(sA[i * kLd + jj], sQ[jj * kLd + m], sum);
+                x = -sum;
             }
             sQ[i * kLd + m] = x;
         }
@@ -183,19 +249,20 @@ template <typename Tin, int BV>
 __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdArgs a,
                                                    BwdWs bw) {
     constexpr int LDE = BV + 1;
-    constexpr int NR = kChunk * BV / kBT;  // (i, c) outputs per thread
+    constexpr int NS = BV / 16;  // column groups of the 64 x BV tiles
     const int H = (int)p.H, K = (int)p.K, V = (int)p.V;
     const int ntiles = V / BV;
     const int64_t n = blockIdx.x / ntiles;
     const int tile = (int)(blockIdx.x % ntiles), col0 = tile * BV;
     const int h = blockIdx.y, tid = threadIdx.x;
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
     const bool delta = p.beta != nullptr;
     extern __shared__ float sm[];
     float *sE = sm;                       // [K][BV+1]
     float *sM = sE + K * LDE;             // [64][65]
     float *sDo = sM + kChunk * kLd;       // [64][BV+1]
     float *sDv = sDo + kChunk * LDE;      // [64][BV+1]
-    float *sX = sDv + kChunk * LDE;       // [64][65] key slice of K / Q
+    float *sX = sDv + kChunk * LDE;       // [64][65] key slice of K, or of diag(gamma) Q
     float *sY = sX + kChunk * kLd;        // [64][65] key slice of W
     float *sGam = sY + kChunk * kLd, *sLam = sGam + kChunk;
 
@@ -232,32 +299,22 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
             sDo[i * LDE + c] =
                 i < ci.len ? ldx(dout, ((ci.t0 + i) * H + h) * (int64_t)V + col0 + c) : 0.f;
         }
-        __syncthreads();
         // dV' = scale M^T dO + diag(lam) K E
-        float acc[NR];
-#pragma unroll
-        for (int r = 0; r < NR; ++r) acc[r] = 0.f;
+        float acc[4][NS];
+        acc_zero(acc);
         for (int k0 = 0; k0 < K; k0 += kSl) {
             __syncthreads();
             load_tok_tile(sX, k, ci.t0, ci.len, H, h, K, k0, tid);
             __syncthreads();
-            const int kn = min(kSl, K - k0);
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                const int idx = tid + r * kBT, i = idx / BV, c = idx - i * BV;
-                float s = acc[r];
-                for (int kk = 0; kk < kn; ++kk)
-                    s = fmaf(sX[i * kLd + kk], sE[(k0 + kk) * LDE + c], s);
-                acc[r] = s;
-            }
+            mm_ab<NS>(acc, sX, kLd, sE + k0 * LDE, LDE, min(kSl, K - k0), tid);
         }
+        float mt[4][NS];
+        acc_zero(mt);
+        mm_atb<NS>(mt, sM, kLd, sDo, LDE, kChunk, tid);
         const float gam_last = expf(ws.G[item * kChunk + ci.len - 1]);
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            const int idx = tid + r * kBT, i = idx / BV, c = idx - i * BV;
-            float mt = 0.f;
-            for (int j = i; j < ci.len; ++j) mt = fmaf(sM[j * kLd + i], sDo[j * LDE + c], mt);
-            const float dvn = i < ci.len ? fmaf(p.scale, mt, sLam[i] * acc[r]) : 0.f;
+        FOR_TILE(NS) {
+            const int i = i0 + r, c = j0 + 16 * s;
+            const float dvn = i < ci.len ? fmaf(p.scale, mt[r][s], sLam[i] * acc[r][s]) : 0.f;
             sDv[i * LDE + c] = dvn;
             if (i < ci.len) {
                 if (delta)
@@ -270,20 +327,28 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
         // E <- Gam E + scale (diag(gamma) Q)^T dO - W^T dV'
         for (int k0 = 0; k0 < K; k0 += kSl) {
             __syncthreads();
-            load_tok_tile(sX, q, ci.t0, ci.len, H, h, K, k0, tid);
+            for (int idx = tid; idx < kChunk * kSl; idx += kBT) {
+                const int i = idx >> 6, c = idx & 63;
+                float x = 0.f;
+                if (i < ci.len && k0 + c < K)
+                    x = sGam[i] * ldx(q, ((ci.t0 + i) * H + h) * (int64_t)K + k0 + c);
+                sX[i * kLd + c] = x;
+            }
             if (delta)
                 load_mat_tile(sY, ws.W + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
             __syncthreads();
+            float e1[4][NS], e2[4][NS];
+            acc_zero(e1);
+            acc_zero(e2);
+            mm_atb<NS>(e1, sX, kLd, sDo, LDE, kChunk, tid);
+            if (delta) mm_atb<NS>(e2, sY, kLd, sDv, LDE, kChunk, tid);
             const int kn = min(kSl, K - k0);
-            for (int idx = tid; idx < kn * BV; idx += kBT) {
-                const int kk = idx / BV, c = idx - kk * BV;
-                float s1 = 0.f, s2 = 0.f;
-                for (int i = 0; i < ci.len; ++i) {
-                    s1 = fmaf(sGam[i] * sX[i * kLd + kk], sDo[i * LDE + c], s1);
-                    if (delta) s2 = fmaf(sY[i * kLd + kk], sDv[i * LDE + c], s2);
+            FOR_TILE(NS) {
+                const int kk = i0 + r, c = j0 + 16 * s;
+                if (kk < kn) {
+                    float *e = &sE[(k0 + kk) * LDE + c];
+                    *e = fmaf(gam_last, *e, fmaf(p.scale, e1[r][s], -e2[r][s]));
                 }
-                float *e = &sE[(k0 + kk) * LDE + c];
-                *e = fmaf(gam_last, *e, fmaf(p.scale, s1, -s2));
             }
         }
     }
@@ -316,9 +381,10 @@ __global__ void __launch_bounds__(kBT) k_bwd_lk(Problem p, Workspace ws, BwdArgs
     const Tin *v = static_cast<const Tin *>(p.v);
     const float *hg = ws.hpre + item * (int64_t)K * V;
     const float *eg = bw.dhend + item * (int64_t)K * V;
-    float p1[16], p2[16], p3[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) p1[r] = p2[r] = p3[r] = 0.f;
+    float p1[4][4], p2[4][4], p3[4][4];
+    acc_zero(p1);
+    acc_zero(p2);
+    acc_zero(p3);
     float eh = 0.f;
     for (int c0 = 0; c0 < V; c0 += kSl) {
         __syncthreads();
@@ -333,21 +399,9 @@ __global__ void __launch_bounds__(kBT) k_bwd_lk(Problem p, Workspace ws, BwdArgs
         load_mat_tile(sE, eg, k0, K, c0, V, V, tid);
         __syncthreads();
         const int cn = min(kSl, V - c0);
-        const int kk = tid & 63;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int i = (tid >> 6) + 4 * r;
-            float s1 = p1[r], s2 = p2[r], s3 = p3[r];
-            for (int c = 0; c < cn; ++c) {
-                const float hv = sH[kk * kLd + c];
-                s1 = fmaf(sDo[i * kLd + c], hv, s1);
-                if (delta) s2 = fmaf(sDv[i * kLd + c], hv, s2);
-                s3 = fmaf(sVn[i * kLd + c], sE[kk * kLd + c], s3);
-            }
-            p1[r] = s1;
-            p2[r] = s2;
-            p3[r] = s3;
-        }
+        mm_abT<4>(p1, sDo, kLd, sH, kLd, cn, tid);
+        if (delta) mm_abT<4>(p2, sDv, kLd, sH, kLd, cn, tid);
+        mm_abT<4>(p3, sVn, kLd, sE, kLd, cn, tid);
         // <E, h> over this key slice: thread tid owns key tid & 63 and a
         // quarter of the slice's columns
         {
@@ -355,28 +409,30 @@ __global__ void __launch_bounds__(kBT) k_bwd_lk(Problem p, Workspace ws, BwdArgs
             for (int c = part; c < cn; c += 4) eh = fmaf(sE[key * kLd + c], sH[key * kLd + c], eh);
         }
     }
-    const int kk = tid & 63;
-    if (k0 + kk < K) {
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int i = (tid >> 6) + 4 * r;
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
+    FOR_TILE(4) {
+        const int i = i0 + r, kk = j0 + 16 * s;
+        if (k0 + kk < K) {
             const int64_t o = (item * kChunk + i) * (int64_t)K + k0 + kk;
-            bw.P1[o] = p1[r];
-            if (delta) bw.P2[o] = p2[r];
-            bw.P3[o] = p3[r];
+            bw.P1[o] = p1[r][s];
+            if (delta) bw.P2[o] = p2[r][s];
+            bw.P3[o] = p3[r][s];
         }
     }
     sRed[tid] = eh;
     __syncthreads();
     if (tid == 0) {
-        float s = 0.f;
-        for (int t = 0; t < kBT; ++t) s += sRed[t];
-        bw.ehp[item * ((K + kSl - 1) / kSl) + ks] = s;
+        float sum = 0.f;
+        for (int t = 0; t < kBT; ++t) sum += sRed[t];
+        bw.ehp[item * ((K + kSl - 1) / kSl) + ks] = sum;
     }
 }
 
 // ---------------------------------------------------------------------------
-// k_bwd_local: every local gradient of one (chunk, head).
+// k_bwd_local: every local gradient of one (chunk, head).  Matrices are
+// stored with exact zeros outside their support (causal, strictly lower,
+// rows past the chunk's length), so full 64-wide products give the masked
+// sums.
 template <typename Tin>
 __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdArgs a,
                                                    BwdWs bw) {
@@ -385,6 +441,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
     if (gc >= *ws.n_chunks) return;
     const ChunkInfo ci = chunk_info(ws, gc);
     const int H = (int)p.H, K = (int)p.K, V = (int)p.V, tid = threadIdx.x, len = ci.len;
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
     const bool delta = p.beta != nullptr;
     const int64_t item = gc * H + h;
     const float scale = p.scale;
@@ -430,120 +487,99 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
     const Tin *dout = static_cast<const Tin *>(a.dout);
-    const int jj = tid & 63;
 
-    // value loop: dMraw = dO V'^T; delta: dTa = dV' (diag(beta) V)^T
-    float dm[16], dt[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) dm[r] = dt[r] = 0.f;
-    for (int c0 = 0; c0 < V; c0 += kSl) {
-        __syncthreads();
-        load_tok_tile(s1, dout, ci.t0, len, H, h, V, c0, tid);
-        if (delta) {
-            load_mat_tile(s2, ws.vnew + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
-            load_mat_tile(s3, bw.dvn + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
-            load_tok_tile(s4, v, ci.t0, len, H, h, V, c0, tid);
-        } else {
-            load_tok_tile(s2, v, ci.t0, len, H, h, V, c0, tid);
-        }
-        __syncthreads();
-        const int cn = min(kSl, V - c0);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int i = (tid >> 6) + 4 * r;
-            float x = dm[r], y = dt[r];
-            for (int c = 0; c < cn; ++c) {
-                x = fmaf(s1[i * kLd + c], s2[jj * kLd + c], x);
-                if (delta) y = fmaf(s3[i * kLd + c], s4[jj * kLd + c], y);
+    // value loop: dMraw = dO V'^T; delta: dTa = dV' V^T (times beta_j below)
+    {
+        float dm[4][4], dt[4][4];
+        acc_zero(dm);
+        acc_zero(dt);
+        for (int c0 = 0; c0 < V; c0 += kSl) {
+            __syncthreads();
+            load_tok_tile(s1, dout, ci.t0, len, H, h, V, c0, tid);
+            if (delta) {
+                load_mat_tile(s2, ws.vnew + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
+                load_mat_tile(s3, bw.dvn + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
+                load_tok_tile(s4, v, ci.t0, len, H, h, V, c0, tid);
+            } else {
+                load_tok_tile(s2, v, ci.t0, len, H, h, V, c0, tid);
             }
-            dm[r] = x;
-            dt[r] = y;
+            __syncthreads();
+            const int cn = min(kSl, V - c0);
+            mm_abT<4>(dm, s1, kLd, s2, kLd, cn, tid);
+            if (delta) mm_abT<4>(dt, s3, kLd, s4, kLd, cn, tid);
         }
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        const int i = (tid >> 6) + 4 * r;
-        const bool causal = i < len && jj <= i;
-        const float d = causal ? expf(sG[i] - sG[jj]) : 0.f;
-        const float z = causal ? scale * dm[r] * d : 0.f;
-        sZ[i * kLd + jj] = z;
-        sR[i * kLd + jj] = causal ? scale * dm[r] * sM[i * kLd + jj] : 0.f;
-        if (delta) sdT[i * kLd + jj] = dt[r] * sB[jj];
+        FOR_TILE(4) {
+            const int i = i0 + r, j = j0 + 16 * s;
+            const bool causal = i < len && j <= i;
+            const float d = causal ? expf(sG[i] - sG[j]) : 0.f;
+            sZ[i * kLd + j] = causal ? scale * dm[r][s] * d : 0.f;
+            sR[i * kLd + j] = causal ? scale * dm[r][s] * sM[i * kLd + j] : 0.f;
+            if (delta) sdT[i * kLd + j] = dt[r][s] * sB[j];
+        }
     }
     __syncthreads();
     // gate terms of M: row sums minus column sums of R
     if (tid < kChunk) {
-        float s = 0.f;
-        for (int j = 0; j < kChunk; ++j) s += sR[tid * kLd + j];
-        rowR[tid] = s;
+        float sum = 0.f;
+        for (int j = 0; j < kChunk; ++j) sum += sR[tid * kLd + j];
+        rowR[tid] = sum;
     } else if (tid < 2 * kChunk) {
         const int j = tid - kChunk;
-        float s = 0.f;
-        for (int i = 0; i < kChunk; ++i) s += sR[i * kLd + j];
-        colR[j] = s;
+        float sum = 0.f;
+        for (int i = 0; i < kChunk; ++i) sum += sR[i * kLd + j];
+        colR[j] = sum;
     }
 
     if (delta) {
         // dTb = -(dV' h^T) (diag(beta gamma) K)^T over the keys; dT = dTa + dTb
-        float tb[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) tb[r] = 0.f;
+        float tb[4][4];
+        acc_zero(tb);
         for (int k0 = 0; k0 < K; k0 += kSl) {
             __syncthreads();
             load_mat_tile(s1, bw.P2 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
             load_tok_tile(s2, k, ci.t0, len, H, h, K, k0, tid);
             __syncthreads();
-            const int kn = min(kSl, K - k0);
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int i = (tid >> 6) + 4 * r;
-                float x = tb[r];
-                for (int c = 0; c < kn; ++c) x = fmaf(s1[i * kLd + c], s2[jj * kLd + c], x);
-                tb[r] = x;
-            }
+            mm_abT<4>(tb, s1, kLd, s2, kLd, min(kSl, K - k0), tid);
+        }
+        FOR_TILE(4) {
+            const int i = i0 + r, j = j0 + 16 * s;
+            sdT[i * kLd + j] = fmaf(-sB[j] * sGam[j], tb[r][s], sdT[i * kLd + j]);
         }
         __syncthreads();
-        const float bg = sB[jj] * sGam[jj];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int i = (tid >> 6) + 4 * r;
-            sdT[i * kLd + jj] = fmaf(-bg, tb[r], sdT[i * kLd + jj]);
-        }
-        __syncthreads();
-        // X = dT T^T  (T lower triangular: T_jm = 0 for m > j)
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int i = (tid >> 6) + 4 * r;
-            float x = 0.f;
-            for (int m = 0; m <= jj; ++m) x = fmaf(sdT[i * kLd + m], sT[jj * kLd + m], x);
-            sX[i * kLd + jj] = x;
+        // X = dT T^T
+        {
+            float x[4][4];
+            acc_zero(x);
+            mm_abT<4>(x, sdT, kLd, sT, kLd, kChunk, tid);
+            FOR_TILE(4) sX[(i0 + r) * kLd + j0 + 16 * s] = x[r][s];
         }
         __syncthreads();
         // dA = -strict_lower(T^T X);  S = diag(beta) dA * D  (into sR)
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int i = (tid >> 6) + 4 * r;
-            float y = 0.f;
-            if (jj < i && i < len) {
-                for (int m = i; m < kChunk; ++m) y = fmaf(sT[m * kLd + i], sX[m * kLd + jj], y);
-                y = -y;
+        {
+            float y[4][4];
+            acc_zero(y);
+            mm_atb<4>(y, sT, kLd, sX, kLd, kChunk, tid);
+            FOR_TILE(4) {
+                const int i = i0 + r, j = j0 + 16 * s;
+                const bool sl = j < i && i < len;
+                const float yv = sl ? -y[r][s] : 0.f;
+                sdT[i * kLd + j] = yv;
+                sR[i * kLd + j] = sl ? sB[i] * yv * expf(sG[i] - sG[j]) : 0.f;
             }
-            sdT[i * kLd + jj] = y;
-            sR[i * kLd + jj] = (jj < i && i < len) ? sB[i] * y * expf(sG[i] - sG[jj]) : 0.f;
         }
         __syncthreads();
         // dbeta from A: rowdot(dA, Kd); the gate terms of A: rows minus columns
         // of dA * A = diag(beta) dA * Kd
         if (tid < kChunk) {
-            float s = 0.f;
-            for (int j = 0; j < kChunk; ++j) s = fmaf(sdT[tid * kLd + j], sKd[tid * kLd + j], s);
-            rdA[tid] = s;
+            float sum = 0.f;
+            for (int j = 0; j < kChunk; ++j) sum = fmaf(sdT[tid * kLd + j], sKd[tid * kLd + j], sum);
+            rdA[tid] = sum;
         } else if (tid < 2 * kChunk) {
             const int j = tid - kChunk;
-            float s = 0.f;
+            float sum = 0.f;
             for (int i = 0; i < kChunk; ++i)
-                s = fmaf(sB[i] * sdT[i * kLd + j], sKd[i * kLd + j], s);
-            colRA[j] = s;
+                sum = fmaf(sB[i] * sdT[i * kLd + j], sKd[i * kLd + j], sum);
+            colRA[j] = sum;
         }
     }
 
@@ -560,39 +596,32 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
         if (delta) load_mat_tile(s5, bw.P2 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
         __syncthreads();
         const int kn = min(kSl, K - k0);
-        const int kk = tid & 63;
-        // dKb = -T^T P2
-        if (delta) {
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int i = (tid >> 6) + 4 * r;
-                float x = 0.f;
-                for (int m = i; m < len; ++m) x = fmaf(sT[m * kLd + i], s5[m * kLd + kk], x);
-                s6[i * kLd + kk] = -x;
-            }
+        if (delta) {  // dKb = -T^T P2
+            float kb[4][4];
+            acc_zero(kb);
+            mm_atb<4>(kb, sT, kLd, s5, kLd, kChunk, tid);
+            FOR_TILE(4) s6[(i0 + r) * kLd + j0 + 16 * s] = -kb[r][s];
             __syncthreads();
         }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int i = (tid >> 6) + 4 * r;
-            if (i >= len || kk >= kn) continue;
-            // dq_i = scale gamma_i P1_i + sum_{j <= i} Z_ij k_j
-            float xq = 0.f;
-            for (int j = 0; j <= i; ++j) xq = fmaf(sZ[i * kLd + j], s2[j * kLd + kk], xq);
-            xq = fmaf(scale * sGam[i], s3[i * kLd + kk], xq);
-            // dk_i = sum_{m >= i} Z_mi q_m + lam_i P3_i (+ beta_i gamma_i dKb_i
-            //        + sum_{m < i} S_im k_m + sum_{m > i} S_mi k_m)
-            float xk = 0.f;
-            for (int m = i; m < len; ++m) xk = fmaf(sZ[m * kLd + i], s1[m * kLd + kk], xk);
-            xk = fmaf(sLam[i], s4[i * kLd + kk], xk);
-            if (delta) {
-                xk = fmaf(sB[i] * sGam[i], s6[i * kLd + kk], xk);
-                for (int m = 0; m < i; ++m) xk = fmaf(sR[i * kLd + m], s2[m * kLd + kk], xk);
-                for (int m = i + 1; m < len; ++m) xk = fmaf(sR[m * kLd + i], s2[m * kLd + kk], xk);
+        float xq[4][4], xk[4][4];
+        acc_zero(xq);
+        acc_zero(xk);
+        mm_ab<4>(xq, sZ, kLd, s2, kLd, kChunk, tid);       // sum_j Z_ij k_j
+        mm_atb<4>(xk, sZ, kLd, s1, kLd, kChunk, tid);      // sum_m Z_mi q_m
+        if (delta) {
+            mm_ab<4>(xk, sR, kLd, s2, kLd, kChunk, tid);   // sum_m S_im k_m
+            mm_atb<4>(xk, sR, kLd, s2, kLd, kChunk, tid);  // sum_m S_mi k_m
+        }
+        FOR_TILE(4) {
+            const int i = i0 + r, kk = j0 + 16 * s;
+            if (i < len && kk < kn) {
+                const float yq = fmaf(scale * sGam[i], s3[i * kLd + kk], xq[r][s]);
+                float yk = fmaf(sLam[i], s4[i * kLd + kk], xk[r][s]);
+                if (delta) yk = fmaf(sB[i] * sGam[i], s6[i * kLd + kk], yk);
+                const int64_t o = ((ci.t0 + i) * H + h) * (int64_t)K + k0 + kk;
+                stx(dq, o, yq);
+                stx(dk, o, yk);
             }
-            const int64_t o = ((ci.t0 + i) * H + h) * (int64_t)K + k0 + kk;
-            stx(dq, o, xq);
-            stx(dk, o, xk);
         }
         if (tid < kChunk) {
             const int i = tid;
@@ -617,15 +646,14 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
             load_tok_tile(s4, v, ci.t0, len, H, h, V, c0, tid);
             __syncthreads();
             const int cn = min(kSl, V - c0);
-            const int c = tid & 63;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int i = (tid >> 6) + 4 * r;
-                float x = 0.f;
-                for (int m = i; m < len; ++m) x = fmaf(sT[m * kLd + i], s3[m * kLd + c], x);
-                s6[i * kLd + c] = x;
+            float vb[4][4];
+            acc_zero(vb);
+            mm_atb<4>(vb, sT, kLd, s3, kLd, kChunk, tid);
+            FOR_TILE(4) {
+                const int i = i0 + r, c = j0 + 16 * s;
+                s6[i * kLd + c] = vb[r][s];
                 if (i < len && c < cn)
-                    stx(dv, ((ci.t0 + i) * H + h) * (int64_t)V + c0 + c, sB[i] * x);
+                    stx(dv, ((ci.t0 + i) * H + h) * (int64_t)V + c0 + c, sB[i] * vb[r][s]);
             }
             __syncthreads();
             if (tid < kChunk) {
@@ -654,7 +682,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
         // sum_j lam_j rowdot(P3, K)_j
         const int nks = (K + kSl - 1) / kSl;
         float eh = 0.f;
-        for (int s = 0; s < nks; ++s) eh += bw.ehp[item * nks + s];
+        for (int sl = 0; sl < nks; ++sl) eh += bw.ehp[item * nks + sl];
         float lam3 = 0.f;
         for (int j = 0; j < len; ++j) lam3 = fmaf(sLam[j], r3[j], lam3);
         sdG[len - 1] += fmaf(sGam[len - 1], eh, lam3);
