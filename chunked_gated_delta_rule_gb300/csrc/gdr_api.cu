@@ -154,10 +154,10 @@ int validate_dims(const gdr_dims *d) {
 // K (the transition tiles of the segment pre-scan cover K columns) and keeps
 // the scan's shared memory within 227 KB.
 int pick_bv(const gdr_dims &d) {
+    const size_t Kp = ((size_t)d.K + 63) & ~(size_t)63;  // keys padded to 64-row tiles
     for (int bv : {64, 32, 16}) {
         if (d.V % bv || d.K % bv) continue;
-        const size_t smem = sizeof(float) * ((size_t)d.K * (bv + 1) +
-                                             2 * (size_t)kChunk * (d.K + 1) +
+        const size_t smem = sizeof(float) * (Kp * (bv + 1) + 2 * (size_t)kChunk * (Kp + 1) +
                                              (size_t)kChunk * (bv + 1) + kChunk);
         if (smem <= 227 * 1024) return bv;
     }

@@ -41,6 +41,7 @@
 // Every output element is summed by one thread in a fixed order, so results
 // are bit-identical from run to run.
 #include "gdr_internal.cuh"
+#include "simt_tile.cuh"
 
 namespace gdr {
 namespace {
@@ -94,82 +95,6 @@ __device__ __forceinline__ void load_mat_tile(float *dst, const float *src, int 
         dst[i * kLd + c] = x;
     }
 }
-
-// Register-tiled products on shared-memory tiles.  Thread t owns the rows
-// 4 (t >> 4) + r (r < 4) and the columns (t & 15) + 16 s (s < NS) of a
-// 64 x 16 NS result: per reduction step it loads 4 + NS values for 4 NS
-// multiply-adds.  A warp reads two rows of the left operand (two addresses)
-// and sixteen consecutive rows or columns of the right one, so no step has a
-// bank conflict with 65-float rows.  The reduction runs in ascending order
-// for every output, so each element has one fixed summation order.
-template <int NS>
-__device__ __forceinline__ void acc_zero(float (&a)[4][NS]) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int s = 0; s < NS; ++s) a[r][s] = 0.f;
-}
-
-// a += A B^T over n:  A[i][c] (row stride lda), B[j][c] (ldb)
-template <int NS>
-__device__ __forceinline__ void mm_abT(float (&a)[4][NS], const float *A, int lda, const float *B,
-                                       int ldb, int n, int tid) {
-    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
-#pragma unroll 4
-    for (int c = 0; c < n; ++c) {
-        float x[4], y[NS];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) x[r] = A[(i0 + r) * lda + c];
-#pragma unroll
-        for (int s = 0; s < NS; ++s) y[s] = B[(j0 + 16 * s) * ldb + c];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int s = 0; s < NS; ++s) a[r][s] = fmaf(x[r], y[s], a[r][s]);
-    }
-}
-
-// a += A^T B over n:  A[m][i] (lda), B[m][j] (ldb)
-template <int NS>
-__device__ __forceinline__ void mm_atb(float (&a)[4][NS], const float *A, int lda, const float *B,
-                                       int ldb, int n, int tid) {
-    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
-#pragma unroll 4
-    for (int m = 0; m < n; ++m) {
-        float x[4], y[NS];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) x[r] = A[m * lda + i0 + r];
-#pragma unroll
-        for (int s = 0; s < NS; ++s) y[s] = B[m * ldb + j0 + 16 * s];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int s = 0; s < NS; ++s) a[r][s] = fmaf(x[r], y[s], a[r][s]);
-    }
-}
-
-// a += A B over n:  A[i][m] (lda), B[m][j] (ldb)
-template <int NS>
-__device__ __forceinline__ void mm_ab(float (&a)[4][NS], const float *A, int lda, const float *B,
-                                      int ldb, int n, int tid) {
-    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
-#pragma unroll 4
-    for (int m = 0; m < n; ++m) {
-        float x[4], y[NS];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) x[r] = A[(i0 + r) * lda + m];
-#pragma unroll
-        for (int s = 0; s < NS; ++s) y[s] = B[m * ldb + j0 + 16 * s];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int s = 0; s < NS; ++s) a[r][s] = fmaf(x[r], y[s], a[r][s]);
-    }
-}
-
-#define FOR_TILE(NS)                                                      \
-    _Pragma("unroll") for (int r = 0; r < 4; ++r)                         \
-        _Pragma("unroll") for (int s = 0; s < NS; ++s)
 
 // ---------------------------------------------------------------------------
 // k_bwd_gram: M = causal(Q K^T * D) (diagonal included), Kd = strictly lower

@@ -19,6 +19,7 @@
 // a local state c_s (scan from 0) and a K x K transition M_s (the same scan
 // on identity columns with U = 0), then h_{s+1} = M_s h_s + c_s.
 #include "gdr_internal.cuh"
+#include "simt_tile.cuh"
 
 namespace gdr {
 namespace {
@@ -180,18 +181,18 @@ k_prep(Problem p, Workspace ws) {
     const int len = e.z;
     const int H = (int)p.H, K = (int)p.K, V = (int)p.V;
     const int tid = threadIdx.x;
-    const int ldk = K + 1;
-    const int VB = V < 128 ? V : 128;
-    const int ldv = VB + 1;
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
+    const int Kp = (K + 63) & ~63;  // keys padded with zero columns to whole 64-column tiles
+    const int ldk = Kp + 1;
 
     extern __shared__ float sm[];
     float *sG = sm;
     float *sB = sG + kChunk;
     float *sBG = sB + kChunk;
-    float *sK = sBG + kChunk;
-    float *sA = sK + kChunk * ldk;
-    float *sT = sA + kChunk * 65;
-    float *sV = sT + kChunk * 65;
+    float *sK = sBG + kChunk;          // [64][Kp+1]
+    float *sA = sK + kChunk * ldk;     // [64][65]
+    float *sT = sA + kChunk * 65;      // [64][65]
+    float *sV = sT + kChunk * 65;      // [64][65] value block
 
     const bool delta = p.beta != nullptr;
     if (tid < kChunk) {
@@ -213,22 +214,21 @@ k_prep(Problem p, Workspace ws) {
 
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
-    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
-        const int i = idx / K, c = idx - i * K;
-        sK[i * ldk + c] = i < len ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
+    for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
+        const int i = idx / Kp, c = idx - i * Kp;
+        sK[i * ldk + c] = (i < len && c < K) ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
     }
     __syncthreads();
     // A3: A_ij = beta_i e^{G_i - G_j} (k_i . k_j), strictly lower (the mask is
     // applied before exp, so e^{G_i - G_j} is only formed for i > j).
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        float a = 0.f;
-        if (j < i && i < len) {
-            float d = 0.f;
-            for (int c = 0; c < K; ++c) d = fmaf(sK[i * ldk + c], sK[j * ldk + c], d);
-            a = sB[i] * expf(sG[i] - sG[j]) * d;
+    {
+        float d[4][4];
+        acc_zero(d);
+        mm_abT<4>(d, sK, ldk, sK, ldk, Kp, tid);
+        FOR_TILE(4) {
+            const int i = i0 + r, jj = j0 + 16 * s;
+            sA[i * 65 + jj] = (jj < i && i < len) ? sB[i] * expf(sG[i] - sG[jj]) * d[r][s] : 0.f;
         }
-        sA[i * 65 + j] = a;
     }
     __syncthreads();
     // A4: T = (I + A)^-1.  Column m solves (I + A) x = e_m by forward
@@ -242,42 +242,47 @@ k_prep(Problem p, Workspace ws) {
             } else if (i == m) {
                 x = 1.f;
             } else {
-                float s = 0.f;
-                for (int j = m; j < i; ++j) s = fmaf(sA[i * 65 + j], sT[j * 65 + m], s);
-                x = -s;
+                float sum = 0.f;
+                for (int jj = m; jj < i; ++jj) sum = fmaf(sA[i * 65 + jj], sT[jj * 65 + m], sum);
+                x = -sum;
             }
             sT[i * 65 + m] = x;
         }
     }
     __syncthreads();
-    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
-        const int i = idx / K, c = idx - i * K;
+    for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
+        const int i = idx / Kp, c = idx - i * Kp;
         sK[i * ldk + c] *= sBG[i];
     }
     __syncthreads();
-    // A5: W = T diag(beta e^G) K
+    // A5: W = T diag(beta e^G) K, in 64-column blocks (T is zero above its
+    // diagonal, so the full product is the triangular one)
     float *Wg = ws.W + (chunk * H + h) * (int64_t)kChunk * K;
-    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
-        const int i = idx / K, c = idx - i * K;
-        float s = 0.f;
-        for (int j = 0; j <= i; ++j) s = fmaf(sT[i * 65 + j], sK[j * ldk + c], s);
-        Wg[idx] = s;
+    for (int kb = 0; kb < Kp; kb += 64) {
+        float w[4][4];
+        acc_zero(w);
+        mm_ab<4>(w, sT, 65, sK + kb, ldk, kChunk, tid);
+        FOR_TILE(4) {
+            const int i = i0 + r, c = kb + j0 + 16 * s;
+            if (c < K) Wg[(int64_t)i * K + c] = w[r][s];
+        }
     }
-    // A5: U = T diag(beta) V, in column blocks of VB
+    // A5: U = T diag(beta) V, in 64-column blocks
     float *Ug = ws.U + (chunk * H + h) * (int64_t)kChunk * V;
-    for (int v0 = 0; v0 < V; v0 += VB) {
+    for (int v0 = 0; v0 < V; v0 += 64) {
         __syncthreads();
-        for (int idx = tid; idx < kChunk * VB; idx += kThreads) {
-            const int i = idx / VB, c = idx - i * VB;
-            sV[i * ldv + c] =
-                i < len ? sB[i] * ld_in(v, ((t0 + i) * H + h) * (int64_t)V + v0 + c) : 0.f;
+        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
+            const int i = idx >> 6, c = idx & 63;
+            sV[i * 65 + c] = (i < len && v0 + c < V)
+                ? sB[i] * ld_in(v, ((t0 + i) * H + h) * (int64_t)V + v0 + c) : 0.f;
         }
         __syncthreads();
-        for (int idx = tid; idx < kChunk * VB; idx += kThreads) {
-            const int i = idx / VB, c = idx - i * VB;
-            float s = 0.f;
-            for (int j = 0; j <= i; ++j) s = fmaf(sT[i * 65 + j], sV[j * ldv + c], s);
-            Ug[(int64_t)i * V + v0 + c] = s;
+        float u[4][4];
+        acc_zero(u);
+        mm_ab<4>(u, sT, 65, sV, 65, kChunk, tid);
+        FOR_TILE(4) {
+            const int i = i0 + r, c = v0 + j0 + 16 * s;
+            if (c < V) Ug[(int64_t)i * V + c] = u[r][s];
         }
     }
 }
@@ -315,21 +320,26 @@ k_scan(Problem p, Workspace ws, int mode) {
     }
     const bool trans = tile >= n_vtiles;
     const int col0 = trans ? (tile - n_vtiles) * BV : tile * BV;
-    const int ldk = K + 1;
+    constexpr int NS = BV / 16;
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
+    const int Kp = (K + 63) & ~63;  // keys padded with zeros to whole 64-row tiles
+    const int ldk = Kp + 1;
     constexpr int ldh = BV + 1;
 
     extern __shared__ float sm[];
-    float *hs = sm;                   // [K][BV+1] state tile
-    float *sK = hs + K * ldh;         // [64][K+1]
-    float *sW = sK + kChunk * ldk;    // [64][K+1] (delta)
+    float *hs = sm;                   // [Kp][BV+1] state tile (rows >= K stay 0)
+    float *sK = hs + Kp * ldh;        // [64][Kp+1]
+    float *sW = sK + kChunk * ldk;    // [64][Kp+1] (delta)
     float *vn = sW + (delta ? kChunk * ldk : 0);  // [64][BV+1]
     float *sG = vn + kChunk * ldh;    // [64]
 
     const int64_t seg_base = ((n * H + h) * (int64_t)S + s);
-    for (int idx = tid; idx < K * BV; idx += kThreads) {
+    for (int idx = tid; idx < Kp * BV; idx += kThreads) {
         const int key = idx / BV, c = idx - key * BV;
         float x = 0.f;
-        if (mode == 0) {
+        if (key >= K) {
+            x = 0.f;
+        } else if (mode == 0) {
             if (p.h0) x = p.h0[state_off(p, n * H + h, key, col0 + c)];
         } else if (mode == 2) {
             x = ws.segH[(seg_base * K + key) * V + col0 + c];
@@ -349,10 +359,12 @@ k_scan(Problem p, Workspace ws, int mode) {
         const int len = e.z;
         __syncthreads();
         if (tid < kChunk) sG[tid] = ws.G[(gc * H + h) * kChunk + tid];
-        for (int idx = tid; idx < kChunk * K; idx += kThreads) {
-            const int i = idx / K, c = idx - i * K;
-            sK[i * ldk + c] = i < len ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
-            if (delta) sW[i * ldk + c] = ws.W[((gc * H + h) * kChunk + i) * (int64_t)K + c];
+        for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
+            const int i = idx / Kp, c = idx - i * Kp;
+            const bool in = i < len && c < K;
+            sK[i * ldk + c] = in ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
+            if (delta)
+                sW[i * ldk + c] = c < K ? ws.W[((gc * H + h) * kChunk + i) * (int64_t)K + c] : 0.f;
         }
         if (mode != 1) {
             float *hp = ws.hpre + (gc * H + h) * (int64_t)K * V;
@@ -365,33 +377,38 @@ k_scan(Problem p, Workspace ws, int mode) {
         const float gl = sG[len - 1];
         const float gam = expf(gl);
         // v_new = U - W h (delta) or V (beta-free), then scaled by e^{G_last - G}
-        for (int idx = tid; idx < kChunk * BV; idx += kThreads) {
-            const int i = idx / BV, c = idx - i * BV;
-            float x = 0.f;
-            if (i < len) {
-                if (delta) {
-                    float acc = 0.f;
-                    for (int key = 0; key < K; ++key)
-                        acc = fmaf(sW[i * ldk + key], hs[key * ldh + c], acc);
-                    const float u = trans ? 0.f
-                        : ws.U[((gc * H + h) * kChunk + i) * (int64_t)V + col0 + c];
-                    x = u - acc;
-                    if (mode != 1)
-                        ws.vnew[((gc * H + h) * kChunk + i) * (int64_t)V + col0 + c] = x;
-                } else {
-                    x = ld_in(v, ((t0 + i) * H + h) * (int64_t)V + col0 + c);
+        {
+            float acc[4][NS];
+            acc_zero(acc);
+            if (delta) mm_ab<NS>(acc, sW, ldk, hs, ldh, Kp, tid);
+            FOR_TILE(NS) {
+                const int i = i0 + r, c = j0 + 16 * s;
+                float x = 0.f;
+                if (i < len) {
+                    if (delta) {
+                        const float u = trans ? 0.f
+                            : ws.U[((gc * H + h) * kChunk + i) * (int64_t)V + col0 + c];
+                        x = u - acc[r][s];
+                        if (mode != 1)
+                            ws.vnew[((gc * H + h) * kChunk + i) * (int64_t)V + col0 + c] = x;
+                    } else {
+                        x = ld_in(v, ((t0 + i) * H + h) * (int64_t)V + col0 + c);
+                    }
+                    x *= expf(gl - sG[i]);
                 }
-                x *= expf(gl - sG[i]);
+                vn[i * ldh + c] = x;
             }
-            vn[i * ldh + c] = x;
         }
         __syncthreads();
-        // h <- e^{G_last} h + K^T (v_new e^{G_last - G})
-        for (int idx = tid; idx < K * BV; idx += kThreads) {
-            const int key = idx / BV, c = idx - key * BV;
-            float acc = 0.f;
-            for (int i = 0; i < len; ++i) acc = fmaf(sK[i * ldk + key], vn[i * ldh + c], acc);
-            hs[key * ldh + c] = fmaf(gam, hs[key * ldh + c], acc);
+        // h <- e^{G_last} h + K^T (v_new e^{G_last - G}), in 64-key blocks
+        for (int kb = 0; kb < Kp; kb += 64) {
+            float acc[4][NS];
+            acc_zero(acc);
+            mm_atb<NS>(acc, sK + kb, ldk, vn, ldh, len, tid);
+            FOR_TILE(NS) {
+                const int key = kb + i0 + r, c = j0 + 16 * s;
+                if (key < K) hs[key * ldh + c] = fmaf(gam, hs[key * ldh + c], acc[r][s]);
+            }
         }
         dprod *= gam;
     }
@@ -571,10 +588,8 @@ cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool /*check
 
 cudaError_t simt_prep(const Problem &p, const Workspace &ws, cudaStream_t st) {
     if (ws.max_chunks == 0) return cudaSuccess;
-    const int K = (int)p.K, V = (int)p.V;
-    const int VB = V < 128 ? V : 128;
-    const size_t smem = sizeof(float) *
-        (3 * kChunk + kChunk * (K + 1) + 2 * kChunk * 65 + kChunk * (VB + 1));
+    const int Kp = ((int)p.K + 63) & ~63;
+    const size_t smem = sizeof(float) * (3 * kChunk + kChunk * (Kp + 1) + 3 * kChunk * 65);
     dim3 grid((unsigned)ws.max_chunks, (unsigned)p.H);
     cudaError_t err;
     if (p.dtype == GDR_BF16) {
@@ -597,8 +612,9 @@ static cudaError_t launch_scan(const Problem &p, const Workspace &ws, int mode,
     const bool delta = p.beta != nullptr;
     const int S = mode == 0 ? 1 : ws.n_segments;
     const int ntiles = (mode == 1 && delta) ? (V + K) / BV : V / BV;
+    const int Kp = (K + 63) & ~63;
     const size_t smem = sizeof(float) *
-        ((size_t)K * (BV + 1) + (size_t)kChunk * (K + 1) * (delta ? 2 : 1) +
+        ((size_t)Kp * (BV + 1) + (size_t)kChunk * (Kp + 1) * (delta ? 2 : 1) +
          (size_t)kChunk * (BV + 1) + kChunk);
     cudaError_t err = set_smem(k_scan<Tin, BV>, smem);
     if (err != cudaSuccess) return err;
