@@ -71,11 +71,42 @@ __device__ __forceinline__ ChunkInfo chunk_info(const Workspace &ws, int64_t gc)
     return ChunkInfo{(int64_t)e.y, e.z};
 }
 
+// True when every caller tensor the backward kernels read by rows (q, k, v,
+// dout) starts on a 16-byte boundary: rows are then 16-byte aligned too (K
+// and V are multiples of 16) and the tiles load in 16-byte pieces.
+__device__ __forceinline__ bool inputs_vec16(const Problem &p, const BwdArgs &a) {
+    const uintptr_t u = reinterpret_cast<uintptr_t>(p.q) | reinterpret_cast<uintptr_t>(p.k) |
+                        reinterpret_cast<uintptr_t>(p.v) | reinterpret_cast<uintptr_t>(a.dout);
+    return (u & 15) == 0;
+}
+
 // Rows [0, 64) x columns [c0, c0 + 64) of a token-major input [tokens][H][D]
-// (rows beyond len and columns beyond D read as 0) into a 64 x 65 tile.
+// (rows beyond len and columns beyond D read as 0) into a 64 x 65 tile, in
+// 16-byte pieces when `vec` (D is a multiple of 16, so a piece is entirely
+// inside or outside the row).
 template <typename T>
 __device__ __forceinline__ void load_tok_tile(float *dst, const T *src, int64_t t0, int len,
-                                              int H, int h, int D, int c0, int tid) {
+                                              int H, int h, int D, int c0, int tid,
+                                              bool vec = false) {
+    if (vec) {
+        constexpr int E = 16 / (int)sizeof(T);
+        constexpr int PR = kSl / E;  // pieces per row
+        for (int idx = tid; idx < kChunk * PR; idx += kBT) {
+            const int i = idx / PR, c = (idx - i * PR) * E;
+            float x[E];
+            if (i < len && c0 + c < D) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+                    src + ((t0 + i) * H + h) * (int64_t)D + c0 + c));
+                unpack16(raw, src, x);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) x[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < E; ++e) dst[i * kLd + c + e] = x[e];
+        }
+        return;
+    }
     for (int idx = tid; idx < kChunk * kSl; idx += kBT) {
         const int i = idx >> 6, c = idx & 63;
         float x = 0.f;
@@ -84,15 +115,22 @@ __device__ __forceinline__ void load_tok_tile(float *dst, const T *src, int64_t 
     }
 }
 
-// Rows [r0, r0 + 64) x columns [c0, c0 + 64) of a row-major FP32 matrix with
-// `rows` rows and row stride `ld` (columns beyond `cols` read as 0).
+// Rows [r0, r0 + 64) x columns [c0, c0 + 64) of a row-major FP32 workspace
+// matrix with `rows` rows and row stride `ld` (columns beyond `cols` read as
+// 0), in float4 pieces: workspace matrices start on 256-byte boundaries and
+// ld, cols and c0 are multiples of 16.
 __device__ __forceinline__ void load_mat_tile(float *dst, const float *src, int r0, int rows,
                                               int c0, int cols, int64_t ld, int tid) {
-    for (int idx = tid; idx < kSl * kSl; idx += kBT) {
-        const int i = idx >> 6, c = idx & 63;
-        float x = 0.f;
-        if (r0 + i < rows && c0 + c < cols) x = src[(int64_t)(r0 + i) * ld + c0 + c];
-        dst[i * kLd + c] = x;
+    for (int idx = tid; idx < kSl * (kSl / 4); idx += kBT) {
+        const int i = idx >> 4, c = (idx & 15) * 4;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r0 + i < rows && c0 + c < cols)
+            x = __ldg(reinterpret_cast<const float4 *>(src + (int64_t)(r0 + i) * ld + c0 + c));
+        float *d = dst + i * kLd + c;
+        d[0] = x.x;
+        d[1] = x.y;
+        d[2] = x.z;
+        d[3] = x.w;
     }
 }
 
@@ -114,6 +152,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_gram(Problem p, Workspace ws, BwdWs
         sG[tid] = ws.G[(gc * H + h) * kChunk + tid];
         sB[tid] = (delta && tid < ci.len) ? p.beta[(ci.t0 + tid) * H + h] : 0.f;
     }
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.q) | reinterpret_cast<uintptr_t>(p.k)) & 15) == 0;
     float qk[4][4], kk[4][4];
     acc_zero(qk);
     acc_zero(kk);
@@ -121,8 +160,8 @@ __global__ void __launch_bounds__(kBT) k_bwd_gram(Problem p, Workspace ws, BwdWs
     const Tin *k = static_cast<const Tin *>(p.k);
     for (int c0 = 0; c0 < K; c0 += kSl) {
         __syncthreads();
-        load_tok_tile(sQ, q, ci.t0, ci.len, H, h, K, c0, tid);
-        load_tok_tile(sK, k, ci.t0, ci.len, H, h, K, c0, tid);
+        load_tok_tile(sQ, q, ci.t0, ci.len, H, h, K, c0, tid, vec);
+        load_tok_tile(sK, k, ci.t0, ci.len, H, h, K, c0, tid, vec);
         __syncthreads();
         const int kn = min(kSl, K - c0);
         mm_abT<4>(qk, sQ, kLd, sK, kLd, kn, tid);
@@ -201,6 +240,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
     const Tin *q = static_cast<const Tin *>(p.q);
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *dout = static_cast<const Tin *>(a.dout);
+    const bool vec = inputs_vec16(p, a);
     for (int cc = nc - 1; cc >= 0; --cc) {
         const int64_t gc = c_begin + cc;
         const ChunkInfo ci = chunk_info(ws, gc);
@@ -229,7 +269,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
         acc_zero(acc);
         for (int k0 = 0; k0 < K; k0 += kSl) {
             __syncthreads();
-            load_tok_tile(sX, k, ci.t0, ci.len, H, h, K, k0, tid);
+            load_tok_tile(sX, k, ci.t0, ci.len, H, h, K, k0, tid, vec);
             __syncthreads();
             mm_ab<NS>(acc, sX, kLd, sE + k0 * LDE, LDE, min(kSl, K - k0), tid);
         }
@@ -306,6 +346,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_lk(Problem p, Workspace ws, BwdArgs
     const Tin *v = static_cast<const Tin *>(p.v);
     const float *hg = ws.hpre + item * (int64_t)K * V;
     const float *eg = bw.dhend + item * (int64_t)K * V;
+    const bool vec = inputs_vec16(p, a);
     float p1[4][4], p2[4][4], p3[4][4];
     acc_zero(p1);
     acc_zero(p2);
@@ -313,12 +354,12 @@ __global__ void __launch_bounds__(kBT) k_bwd_lk(Problem p, Workspace ws, BwdArgs
     float eh = 0.f;
     for (int c0 = 0; c0 < V; c0 += kSl) {
         __syncthreads();
-        load_tok_tile(sDo, dout, ci.t0, ci.len, H, h, V, c0, tid);
+        load_tok_tile(sDo, dout, ci.t0, ci.len, H, h, V, c0, tid, vec);
         if (delta) {
             load_mat_tile(sDv, bw.dvn + item * (int64_t)kChunk * V, 0, ci.len, c0, V, V, tid);
             load_mat_tile(sVn, ws.vnew + item * (int64_t)kChunk * V, 0, ci.len, c0, V, V, tid);
         } else {
-            load_tok_tile(sVn, v, ci.t0, ci.len, H, h, V, c0, tid);
+            load_tok_tile(sVn, v, ci.t0, ci.len, H, h, V, c0, tid, vec);
         }
         load_mat_tile(sH, hg, k0, K, c0, V, V, tid);
         load_mat_tile(sE, eg, k0, K, c0, V, V, tid);
@@ -412,6 +453,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
     const Tin *dout = static_cast<const Tin *>(a.dout);
+    const bool v16 = inputs_vec16(p, a);
 
     // value loop: dMraw = dO V'^T; delta: dTa = dV' V^T (times beta_j below)
     {
@@ -420,13 +462,13 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
         acc_zero(dt);
         for (int c0 = 0; c0 < V; c0 += kSl) {
             __syncthreads();
-            load_tok_tile(s1, dout, ci.t0, len, H, h, V, c0, tid);
+            load_tok_tile(s1, dout, ci.t0, len, H, h, V, c0, tid, v16);
             if (delta) {
                 load_mat_tile(s2, ws.vnew + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
                 load_mat_tile(s3, bw.dvn + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
-                load_tok_tile(s4, v, ci.t0, len, H, h, V, c0, tid);
+                load_tok_tile(s4, v, ci.t0, len, H, h, V, c0, tid, v16);
             } else {
-                load_tok_tile(s2, v, ci.t0, len, H, h, V, c0, tid);
+                load_tok_tile(s2, v, ci.t0, len, H, h, V, c0, tid, v16);
             }
             __syncthreads();
             const int cn = min(kSl, V - c0);
@@ -462,7 +504,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
         for (int k0 = 0; k0 < K; k0 += kSl) {
             __syncthreads();
             load_mat_tile(s1, bw.P2 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
-            load_tok_tile(s2, k, ci.t0, len, H, h, K, k0, tid);
+            load_tok_tile(s2, k, ci.t0, len, H, h, K, k0, tid, v16);
             __syncthreads();
             mm_abT<4>(tb, s1, kLd, s2, kLd, min(kSl, K - k0), tid);
         }
@@ -514,8 +556,8 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
     Tin *dk = static_cast<Tin *>(a.dk);
     for (int k0 = 0; k0 < K; k0 += kSl) {
         __syncthreads();
-        load_tok_tile(s1, q, ci.t0, len, H, h, K, k0, tid);
-        load_tok_tile(s2, k, ci.t0, len, H, h, K, k0, tid);
+        load_tok_tile(s1, q, ci.t0, len, H, h, K, k0, tid, v16);
+        load_tok_tile(s2, k, ci.t0, len, H, h, K, k0, tid, v16);
         load_mat_tile(s3, bw.P1 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
         load_mat_tile(s4, bw.P3 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
         if (delta) load_mat_tile(s5, bw.P2 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
@@ -568,7 +610,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
         for (int c0 = 0; c0 < V; c0 += kSl) {
             __syncthreads();
             load_mat_tile(s3, bw.dvn + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
-            load_tok_tile(s4, v, ci.t0, len, H, h, V, c0, tid);
+            load_tok_tile(s4, v, ci.t0, len, H, h, V, c0, tid, v16);
             __syncthreads();
             const int cn = min(kSl, V - c0);
             float vb[4][4];

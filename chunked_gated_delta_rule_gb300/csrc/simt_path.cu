@@ -214,9 +214,30 @@ k_prep(Problem p, Workspace ws) {
 
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
-    for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
-        const int i = idx / Kp, c = idx - i * Kp;
-        sK[i * ldk + c] = (i < len && c < K) ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
+    const bool vin = ((reinterpret_cast<uintptr_t>(p.k) | reinterpret_cast<uintptr_t>(p.v)) & 15) == 0;
+    constexpr int E = 16 / (int)sizeof(Tin);  // elements per 16-byte piece
+    if (vin) {
+        const int pr = Kp / E;
+        for (int idx = tid; idx < kChunk * pr; idx += kThreads) {
+            const int i = idx / pr, c = (idx - i * pr) * E;
+            float x[E];
+            if (i < len && c < K) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+                    k + ((t0 + i) * H + h) * (int64_t)K + c));
+                unpack16(raw, k, x);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) x[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < E; ++e) sK[i * ldk + c + e] = x[e];
+        }
+    } else {
+        for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
+            const int i = idx / Kp, c = idx - i * Kp;
+            sK[i * ldk + c] =
+                (i < len && c < K) ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
+        }
     }
     __syncthreads();
     // A3: A_ij = beta_i e^{G_i - G_j} (k_i . k_j), strictly lower (the mask is
@@ -271,10 +292,27 @@ k_prep(Problem p, Workspace ws) {
     float *Ug = ws.U + (chunk * H + h) * (int64_t)kChunk * V;
     for (int v0 = 0; v0 < V; v0 += 64) {
         __syncthreads();
-        for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
-            const int i = idx >> 6, c = idx & 63;
-            sV[i * 65 + c] = (i < len && v0 + c < V)
-                ? sB[i] * ld_in(v, ((t0 + i) * H + h) * (int64_t)V + v0 + c) : 0.f;
+        if (vin) {
+            for (int idx = tid; idx < kChunk * (64 / E); idx += kThreads) {
+                const int i = idx / (64 / E), c = (idx - i * (64 / E)) * E;
+                float x[E];
+                if (i < len && v0 + c < V) {
+                    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+                        v + ((t0 + i) * H + h) * (int64_t)V + v0 + c));
+                    unpack16(raw, v, x);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) x[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < E; ++e) sV[i * 65 + c + e] = sB[i] * x[e];
+            }
+        } else {
+            for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
+                const int i = idx >> 6, c = idx & 63;
+                sV[i * 65 + c] = (i < len && v0 + c < V)
+                    ? sB[i] * ld_in(v, ((t0 + i) * H + h) * (int64_t)V + v0 + c) : 0.f;
+            }
         }
         __syncthreads();
         float u[4][4];
@@ -350,6 +388,7 @@ k_scan(Problem p, Workspace ws, int mode) {
     }
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
+    const bool vk = (reinterpret_cast<uintptr_t>(p.k) & 15) == 0;
     float dprod = 1.f;
 
     for (int cc = s0; cc < s1; ++cc) {
@@ -359,12 +398,42 @@ k_scan(Problem p, Workspace ws, int mode) {
         const int len = e.z;
         __syncthreads();
         if (tid < kChunk) sG[tid] = ws.G[(gc * H + h) * kChunk + tid];
-        for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
-            const int i = idx / Kp, c = idx - i * Kp;
-            const bool in = i < len && c < K;
-            sK[i * ldk + c] = in ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
-            if (delta)
-                sW[i * ldk + c] = c < K ? ws.W[((gc * H + h) * kChunk + i) * (int64_t)K + c] : 0.f;
+        if (vk) {  // 16-byte pieces (K is a multiple of 16)
+            constexpr int E = 16 / (int)sizeof(Tin);
+            const int pr = Kp / E;
+            for (int idx = tid; idx < kChunk * pr; idx += kThreads) {
+                const int i = idx / pr, c = (idx - i * pr) * E;
+                float x[E];
+                if (i < len && c < K) {
+                    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+                        k + ((t0 + i) * H + h) * (int64_t)K + c));
+                    unpack16(raw, k, x);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) x[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < E; ++e) sK[i * ldk + c + e] = x[e];
+            }
+        } else {
+            for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
+                const int i = idx / Kp, c = idx - i * Kp;
+                sK[i * ldk + c] =
+                    (i < len && c < K) ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
+            }
+        }
+        if (delta) {  // W rows: float4 pieces of the workspace
+            const float *Wg = ws.W + (gc * H + h) * (int64_t)kChunk * K;
+            for (int idx = tid; idx < kChunk * (Kp / 4); idx += kThreads) {
+                const int i = idx / (Kp / 4), c = (idx - i * (Kp / 4)) * 4;
+                float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c < K) w = __ldg(reinterpret_cast<const float4 *>(Wg + (int64_t)i * K + c));
+                float *d = sW + i * ldk + c;
+                d[0] = w.x;
+                d[1] = w.y;
+                d[2] = w.z;
+                d[3] = w.w;
+            }
         }
         if (mode != 1) {
             float *hp = ws.hpre + (gc * H + h) * (int64_t)K * V;

@@ -4,6 +4,32 @@
 
 namespace gdr {
 
+// Eight (four for FP32) consecutive input elements from one 16-byte load.
+__device__ __forceinline__ void unpack16(const uint4 &raw, const __nv_bfloat16 *, float *x) {
+    const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(b[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void unpack16(const uint4 &raw, const __half *, float *x) {
+    const __half2 *b = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(b[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void unpack16(const uint4 &raw, const float *, float *x) {
+    x[0] = __uint_as_float(raw.x);
+    x[1] = __uint_as_float(raw.y);
+    x[2] = __uint_as_float(raw.z);
+    x[3] = __uint_as_float(raw.w);
+}
+
 // Register-tiled products on shared-memory tiles.  Thread t owns the rows
 // 4 (t >> 4) + r (r < 4) and the columns (t & 15) + 16 s (s < NS) of a
 // 64 x 16 NS result: per reduction step it loads 4 + NS values for 4 NS
