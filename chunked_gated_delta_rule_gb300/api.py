@@ -83,9 +83,9 @@ def load_library():
                                           i32p, vp, vp, vp]
         lib.gdr_recurrent_fwd.restype = ctypes.c_int
         lib.gdr_chunk_bwd.argtypes = [dims_p, vp, vp, vp, vp, vp, i32p, vp, vp, vp, vp, vp, vp,
-                                      vp, vp, vp, ctypes.POINTER(gdr_options), vp]
+                                      vp, vp, vp, ctypes.c_int, ctypes.POINTER(gdr_options), vp]
         lib.gdr_chunk_bwd.restype = ctypes.c_int
-        lib.gdr_bwd_workspace_size.argtypes = [dims_p, ctypes.c_int]
+        lib.gdr_bwd_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.c_int]
         lib.gdr_bwd_workspace_size.restype = ctypes.c_size_t
         lib.gdr_workspace_size.argtypes = [dims_p, ctypes.c_int, ctypes.c_int]
         lib.gdr_workspace_size.restype = ctypes.c_size_t
@@ -256,7 +256,7 @@ def gdr_chunk_fwd(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments
     return o, ht
 
 
-def gdr_chunk_bwd(q, k, v, g, beta, do, cu_seqlens=None, h0=None, dht=None, *,
+def gdr_chunk_bwd(q, k, v, g, beta, do, cu_seqlens=None, h0=None, dht=None, *, n_segments=0,
                   state_layout="kv", want_dh0=True, scale=0.0, workspace=None, status=None,
                   dq=None, dk=None, dv=None, dg=None, dbeta=None, dh0=None, stream=None,
                   timer=None):
@@ -309,15 +309,18 @@ def gdr_chunk_bwd(q, k, v, g, beta, do, cu_seqlens=None, h0=None, dht=None, *,
         rc = lib.gdr_chunk_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                _ptr(beta), _ptr(cu_seqlens), _ptr(h0), _ptr(do), _ptr(dht),
                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0),
-                               ctypes.byref(opt), ctypes.c_void_p(stream.cuda_stream))
+                               int(n_segments), ctypes.byref(opt),
+                               ctypes.c_void_p(stream.cuda_stream))
     if rc != 0:
         raise GdrError(rc)
     return dq, dk, dv, dg, dbeta, dh0
 
 
-def gdr_bwd_workspace_size(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, flags=0) -> int:
+def gdr_bwd_workspace_size(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, flags=0,
+                           n_segments=0) -> int:
     return int(load_library().gdr_bwd_workspace_size(
-        ctypes.byref(make_dims(B, T, H, K, V, N, dtype, flags)), int(beta_free)))
+        ctypes.byref(make_dims(B, T, H, K, V, N, dtype, flags)), int(beta_free),
+        int(n_segments)))
 
 
 def gdr_recurrent_fwd(q, k, v, g, beta=None, cu_seqlens=None, *, state, state_indices=None,

@@ -315,9 +315,9 @@ struct BwdLayout {
     size_t off_Mq, off_Kd, off_Tm, off_dhend, off_dvn, off_P1, off_P2, off_P3, off_ehp, total;
 };
 
-BwdLayout bwd_layout(const gdr_dims &d, bool beta_free) {
+BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments) {
     BwdLayout B{};
-    B.fwd = workspace_layout(d, beta_free, 1, 1);
+    B.fwd = workspace_layout(d, beta_free, n_segments, 1);
     size_t off = B.fwd.total;
     auto take = [&](size_t bytes) {
         const size_t at = off;
@@ -424,7 +424,18 @@ int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs
             cudaStream_t st, LaunchRecorder &rec) {
     GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
     GDR_LAUNCH(rec, kKPrep, simt_prep(p, ws, st));
-    GDR_LAUNCH(rec, kKScanSerial, simt_scan(p, ws, 0, bv, st));
+    if (ws.n_segments <= 1) {
+        GDR_LAUNCH(rec, kKScanSerial, simt_scan(p, ws, 0, bv, st));
+    } else {
+        GDR_LAUNCH(rec, kKScanPre, simt_scan(p, ws, 1, bv, st));
+        if (p.beta == nullptr)
+            GDR_LAUNCH(rec, kKComposeScalar, compose_scalar(p, ws, st));
+        else if (compose_mt_supported(p))
+            GDR_LAUNCH(rec, kKCompose, compose_mt(p, ws, st));
+        else
+            GDR_LAUNCH(rec, kKCompose, simt_compose(p, ws, bv, st));
+        GDR_LAUNCH(rec, kKScanSegOut, simt_scan(p, ws, 2, bv, st));
+    }
     GDR_TRY(simt_bwd(p, ws, a, bw, st, rec));
     return GDR_OK;
 }
@@ -468,6 +479,8 @@ const char *gdr_kernel_name(int id) {
     case kKBwdScan: return "bwd_dscan";
     case kKBwdLk: return "bwd_lk";
     case kKBwdLocal: return "bwd_local";
+    case kKBwdPre: return "bwd_dscan_prescan";
+    case kKBwdSegOut: return "bwd_dscan_segment_out";
     default: return "?";
     }
 }
@@ -596,16 +609,30 @@ int gdr_chunk_fwd(const gdr_dims *dims, const void *q, const void *k, const void
                             nullptr, stream);
 }
 
-size_t gdr_bwd_workspace_size(const gdr_dims *dims, int beta_free) {
+// The backward's plan: the forward recompute's scan takes 32-column tiles
+// where they fit (twice the chains of the forward plan's 64; measured faster
+// inside the backward), and the segment count follows the CUDA-core path's
+// rule unless the caller fixes it.
+int bwd_plan(const gdr_dims &d, bool beta_free, int n_segments, int *bv, int *S) {
+    if (n_segments < 0) return GDR_ERR_INVALID;
+    if (n_segments > kMaxSegments) return GDR_ERR_UNSUPPORTED;
+    *bv = (d.V % 32 == 0 && d.K % 32 == 0) ? 32 : pick_bv(d);
+    *S = n_segments > 0 ? n_segments : auto_segments(d, beta_free, 1, *bv);
+    return GDR_OK;
+}
+
+size_t gdr_bwd_workspace_size(const gdr_dims *dims, int beta_free, int n_segments) {
     if (validate_dims(dims) != GDR_OK) return 0;
-    return bwd_layout(*dims, beta_free != 0).total;
+    int bv = 0, S = 1;
+    if (bwd_plan(*dims, beta_free != 0, n_segments, &bv, &S) != GDR_OK) return 0;
+    return bwd_layout(*dims, beta_free != 0, S).total;
 }
 
 int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void *v,
                   const float *g, const float *beta, const int32_t *cu_seqlens,
                   const float *h0, const void *dout, const float *dht, void *dq, void *dk,
-                  void *dv, float *dg, float *dbeta, float *dh0, const gdr_options *opt,
-                  gdr_stream_t stream) {
+                  void *dv, float *dg, float *dbeta, float *dh0, int n_segments,
+                  const gdr_options *opt, gdr_stream_t stream) {
     int rc = validate_dims(dims);
     if (rc != GDR_OK) return rc;
     if (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg) return GDR_ERR_INVALID;
@@ -614,6 +641,9 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
     if (opt && !(opt->scale >= 0.f)) return GDR_ERR_INVALID;  // rejects NaN too
     if (opt && (opt->force_path != 0 || opt->force_bv != 0)) return GDR_ERR_INVALID;
     const bool beta_free = beta == nullptr;
+    int bv_rec = 0, S = 1;
+    rc = bwd_plan(*dims, beta_free, n_segments, &bv_rec, &S);
+    if (rc != GDR_OK) return rc;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Problem p{};
@@ -629,7 +659,7 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
     p.status = opt ? opt->status : nullptr;
     if (p.N == 0) return GDR_OK;
 
-    const BwdLayout B = bwd_layout(*dims, beta_free);
+    const BwdLayout B = bwd_layout(*dims, beta_free, S);
     void *base = nullptr;
     bool owned = false;
     if (opt && opt->workspace) {
@@ -640,7 +670,7 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
         if (lib_malloc(&base, B.total, st) != cudaSuccess) return GDR_ERR_CUDA;
         owned = true;
     }
-    const Workspace ws = carve_workspace(base, B.fwd, 1);
+    const Workspace ws = carve_workspace(base, B.fwd, S);
     const BwdWs bw = carve_bwd(base, B);
     BwdArgs a{};
     a.dout = dout; a.dht = dht; a.dq = dq; a.dk = dk; a.dv = dv;
@@ -653,7 +683,7 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
         rec.ids = opt->launch_ids;
         if (!opt->events && opt->launch_ids) rec.max_launches = opt->max_launches;
     }
-    rc = run_bwd(p, ws, a, bw, pick_bv(*dims), st, rec);
+    rc = run_bwd(p, ws, a, bw, bv_rec, st, rec);
     if (opt && opt->n_launches) *opt->n_launches = rec.count;
     if (owned) {
         if (cudaFreeAsync(base, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;

@@ -162,6 +162,8 @@ enum KernelId {
     kKBwdScan = 17,
     kKBwdLk = 18,
     kKBwdLocal = 19,
+    kKBwdPre = 20,
+    kKBwdSegOut = 21,
     kKNumIds
 };
 

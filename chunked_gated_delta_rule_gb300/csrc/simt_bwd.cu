@@ -208,16 +208,35 @@ __global__ void __launch_bounds__(kBT) k_bwd_gram(Problem p, Workspace ws, BwdWs
 
 // ---------------------------------------------------------------------------
 // k_bwd_dscan: the reverse scan of one (sequence, head, value tile), chunks
-// from last to first.  E is dL/d(state at the chunk's end).
+// from last to first.  E is dL/d(state at the chunk's end).  Each step is
+// affine in E: E_start = (Gam I - W^T diag(lam) K) E_end + C, C collecting
+// the dO terms, so the scan splits into segments like the forward one (the
+// pages' "Proposed Dataflow" step 4: the reverse recurrence mirrors the
+// split).  mode 0: whole sequence from dht, writes dh0; mode 1: segment
+// pre-scan, value columns from E = 0 (-> the segment's offset c) and, in
+// delta mode, transition columns from the identity with dO taken as 0 (-> its
+// K x K map, stored transposed); mode 2: segment output pass from the
+// composed E at the segment's end.  Modes 0 and 2 store E and dV' per chunk.
+// Segment s of a sequence's nseg segments keeps its summaries in slot
+// nseg - 1 - s, so the ordered composition runs from the last segment to the
+// first: it starts from dht and ends at dh0.
 template <typename Tin, int BV>
 __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdArgs a,
-                                                   BwdWs bw) {
+                                                   BwdWs bw, int mode) {
     constexpr int LDE = BV + 1;
     constexpr int NS = BV / 16;  // column groups of the 64 x BV tiles
     const int H = (int)p.H, K = (int)p.K, V = (int)p.V;
-    const int ntiles = V / BV;
-    const int64_t n = blockIdx.x / ntiles;
-    const int tile = (int)(blockIdx.x % ntiles), col0 = tile * BV;
+    const bool delta_mode = p.beta != nullptr;
+    const int S = mode == 0 ? 1 : ws.n_segments;
+    const int n_vtiles = V / BV;
+    const int ntiles = (mode == 1 && delta_mode) ? (V + K) / BV : n_vtiles;
+    int64_t bid = blockIdx.x;
+    const int tile = (int)(bid % ntiles);
+    bid /= ntiles;
+    const int seg = (int)(bid % S);
+    const int64_t n = bid / S;
+    const bool trans = tile >= n_vtiles;
+    const int col0 = trans ? (tile - n_vtiles) * BV : tile * BV;
     const int h = blockIdx.y, tid = threadIdx.x;
     const int i0 = 4 * (tid >> 4), j0 = tid & 15;
     const bool delta = p.beta != nullptr;
@@ -231,25 +250,45 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
     float *sGam = sY + kChunk * kLd, *sLam = sGam + kChunk;
 
     const int64_t nh = n * H + h;
-    for (int idx = tid; idx < K * BV; idx += kBT) {
-        const int key = idx / BV, c = idx - key * BV;
-        sE[key * LDE + c] = a.dht ? a.dht[state_off(p, nh, key, col0 + c)] : 0.f;
-    }
     const int c_begin = ws.seq_chunk0[n];
     const int nc = ws.seq_chunk0[n + 1] - c_begin;
+    int s0 = 0, s1 = nc, slot = 0;
+    if (mode != 0) {
+        const int per = (nc + S - 1) / S;
+        const int nseg = per ? (nc + per - 1) / per : 0;
+        s0 = seg * per;
+        s1 = min(nc, s0 + per);
+        if (s0 >= s1) return;
+        slot = nseg - 1 - seg;
+    }
+    const int64_t seg_base = nh * (int64_t)S + slot;
+    for (int idx = tid; idx < K * BV; idx += kBT) {
+        const int key = idx / BV, c = idx - key * BV;
+        float x = 0.f;
+        if (mode == 0)
+            x = a.dht ? a.dht[state_off(p, nh, key, col0 + c)] : 0.f;
+        else if (mode == 2)
+            x = ws.segH[(seg_base * K + key) * V + col0 + c];
+        else if (trans)
+            x = (key == col0 + c) ? 1.f : 0.f;
+        sE[key * LDE + c] = x;
+    }
     const Tin *q = static_cast<const Tin *>(p.q);
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *dout = static_cast<const Tin *>(a.dout);
     const bool vec = inputs_vec16(p, a);
-    for (int cc = nc - 1; cc >= 0; --cc) {
+    float dprod = 1.f;
+    for (int cc = s1 - 1; cc >= s0; --cc) {
         const int64_t gc = c_begin + cc;
         const ChunkInfo ci = chunk_info(ws, gc);
         const int64_t item = gc * H + h;
         __syncthreads();
-        float *Eg = bw.dhend + item * (int64_t)K * V;
-        for (int idx = tid; idx < K * BV; idx += kBT) {
-            const int key = idx / BV, c = idx - key * BV;
-            Eg[(int64_t)key * V + col0 + c] = sE[key * LDE + c];
+        if (mode != 1) {
+            float *Eg = bw.dhend + item * (int64_t)K * V;
+            for (int idx = tid; idx < K * BV; idx += kBT) {
+                const int key = idx / BV, c = idx - key * BV;
+                Eg[(int64_t)key * V + col0 + c] = sE[key * LDE + c];
+            }
         }
         if (tid < kChunk) {
             const float *G = ws.G + item * kChunk;
@@ -261,8 +300,8 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
             sM[(idx >> 6) * kLd + (idx & 63)] = bw.Mq[item * kChunk * kChunk + idx];
         for (int idx = tid; idx < kChunk * BV; idx += kBT) {
             const int i = idx / BV, c = idx - i * BV;
-            sDo[i * LDE + c] =
-                i < ci.len ? ldx(dout, ((ci.t0 + i) * H + h) * (int64_t)V + col0 + c) : 0.f;
+            sDo[i * LDE + c] = (i < ci.len && !trans)
+                ? ldx(dout, ((ci.t0 + i) * H + h) * (int64_t)V + col0 + c) : 0.f;
         }
         // dV' = scale M^T dO + diag(lam) K E
         float acc[4][NS];
@@ -281,7 +320,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
             const int i = i0 + r, c = j0 + 16 * s;
             const float dvn = i < ci.len ? fmaf(p.scale, mt[r][s], sLam[i] * acc[r][s]) : 0.f;
             sDv[i * LDE + c] = dvn;
-            if (i < ci.len) {
+            if (i < ci.len && mode != 1) {
                 if (delta)
                     bw.dvn[(item * kChunk + i) * (int64_t)V + col0 + c] = dvn;
                 else
@@ -316,13 +355,25 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
                 }
             }
         }
+        dprod *= gam_last;
     }
     __syncthreads();
-    if (a.dh0) {
+    if (mode == 0) {
+        if (a.dh0) {
+            for (int idx = tid; idx < K * BV; idx += kBT) {
+                const int key = idx / BV, c = idx - key * BV;
+                a.dh0[state_off(p, nh, key, col0 + c)] = sE[key * LDE + c];
+            }
+        }
+    } else if (mode == 1) {
         for (int idx = tid; idx < K * BV; idx += kBT) {
             const int key = idx / BV, c = idx - key * BV;
-            a.dh0[state_off(p, nh, key, col0 + c)] = sE[key * LDE + c];
+            if (trans)  // stored transposed: row m of the map's transpose is its column m
+                ws.segM[(seg_base * K + col0 + c) * K + key] = sE[key * LDE + c];
+            else
+                ws.segC[(seg_base * K + key) * V + col0 + c] = sE[key * LDE + c];
         }
+        if (!delta_mode && tile == 0 && tid == 0) ws.segD[seg_base] = dprod;
     }
 }
 
@@ -684,23 +735,48 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = rec.end()) != cudaSuccess) return e;
     }
-    // reverse scan
+    // reverse scan: serial, or segment pre-scan + ordered composition from the
+    // last segment to the first + segment output pass
     {
-        const bool wide = V % 32 == 0;
-        const int bv = wide ? 32 : 16;
+        const int S = ws.n_segments;
+        const int bv = (V % 32 == 0 && (S <= 1 || K % 32 == 0)) ? 32 : 16;
         const size_t smem = sizeof(float) * ((size_t)K * (bv + 1) + 3 * kChunk * kLd +
                                              2 * kChunk * (bv + 1) + 2 * kChunk);
-        const dim3 grid((unsigned)(p.N * (V / bv)), H);
-        if ((e = rec.begin(kKBwdScan)) != cudaSuccess) return e;
-        if (wide) {
-            if ((e = set_smem_bwd(k_bwd_dscan<Tin, 32>, smem)) != cudaSuccess) return e;
-            k_bwd_dscan<Tin, 32><<<grid, kBT, smem, st>>>(p, ws, a, bw);
+        auto launch = [&](int mode) -> cudaError_t {
+            const int ntiles = (mode == 1 && delta) ? (V + K) / bv : V / bv;
+            const dim3 grid((unsigned)(p.N * (mode == 0 ? 1 : S) * ntiles), H);
+            cudaError_t r;
+            if (bv == 32) {
+                if ((r = set_smem_bwd(k_bwd_dscan<Tin, 32>, smem)) != cudaSuccess) return r;
+                k_bwd_dscan<Tin, 32><<<grid, kBT, smem, st>>>(p, ws, a, bw, mode);
+            } else {
+                if ((r = set_smem_bwd(k_bwd_dscan<Tin, 16>, smem)) != cudaSuccess) return r;
+                k_bwd_dscan<Tin, 16><<<grid, kBT, smem, st>>>(p, ws, a, bw, mode);
+            }
+            return cudaGetLastError();
+        };
+        if (S <= 1) {
+            if ((e = rec.begin(kKBwdScan)) != cudaSuccess) return e;
+            if ((e = launch(0)) != cudaSuccess) return e;
+            if ((e = rec.end()) != cudaSuccess) return e;
         } else {
-            if ((e = set_smem_bwd(k_bwd_dscan<Tin, 16>, smem)) != cudaSuccess) return e;
-            k_bwd_dscan<Tin, 16><<<grid, kBT, smem, st>>>(p, ws, a, bw);
+            if ((e = rec.begin(kKBwdPre)) != cudaSuccess) return e;
+            if ((e = launch(1)) != cudaSuccess) return e;
+            if ((e = rec.end()) != cudaSuccess) return e;
+            // the composition starts from dht and ends at dh0
+            Problem pr = p;
+            pr.h0 = a.dht;
+            pr.ht = a.dh0;
+            if ((e = rec.begin(delta ? kKCompose : kKComposeScalar)) != cudaSuccess) return e;
+            if (!delta) e = compose_scalar(pr, ws, st);
+            else if (compose_mt_supported(pr)) e = compose_mt(pr, ws, st);
+            else e = simt_compose(pr, ws, bv, st);
+            if (e != cudaSuccess) return e;
+            if ((e = rec.end()) != cudaSuccess) return e;
+            if ((e = rec.begin(kKBwdSegOut)) != cudaSuccess) return e;
+            if ((e = launch(2)) != cudaSuccess) return e;
+            if ((e = rec.end()) != cudaSuccess) return e;
         }
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if ((e = rec.end()) != cudaSuccess) return e;
     }
     // L x K products
     {

@@ -241,6 +241,13 @@ int gdr_recurrent_fwd(const gdr_dims *dims, const void *q, const void *k,
  *   dg      [B,T,H] FP32 output;  dbeta [B,T,H] FP32 output, required
  *           exactly when beta is given (NULL in the beta-free mode).
  *   dh0     [Nseq,H,K,V] FP32 output (state layout of h0), or NULL.
+ *   n_segments  0 = automatic; S > 1 splits every sequence into S runs of
+ *           whole chunks for both the forward recompute and the reverse
+ *           scan: each step of the reverse recurrence is affine in the
+ *           state gradient, so per segment a pre-scan produces its offset
+ *           and K x K map, an ordered composition runs from the last segment
+ *           to the first (from dht to dh0), and an output pass rebuilds the
+ *           per-chunk gradients (the pages' "Proposed Dataflow" step 4).
  *   opt     NULL, or gdr_options with scale, status, workspace (at least
  *           gdr_bwd_workspace_size bytes) and the launch events;
  *           force_path and force_bv must be 0.
@@ -254,11 +261,12 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k,
                   const int32_t *cu_seqlens, const float *h0,
                   const void *dout, const float *dht, void *dq, void *dk,
                   void *dv, float *dg, float *dbeta, float *dh0,
-                  const gdr_options *opt, gdr_stream_t stream);
+                  int n_segments, const gdr_options *opt, gdr_stream_t stream);
 
 /* Bytes of device scratch gdr_chunk_bwd needs for this problem (beta_free
- * != 0 for the beta-free mode).  0 on invalid arguments. */
-size_t gdr_bwd_workspace_size(const gdr_dims *dims, int beta_free);
+ * != 0 for the beta-free mode; n_segments as passed to gdr_chunk_bwd).
+ * 0 on invalid arguments. */
+size_t gdr_bwd_workspace_size(const gdr_dims *dims, int beta_free, int n_segments);
 
 /* Bytes of device scratch gdr_chunk_fwd_ex needs for this problem
  * (beta_free != 0 for the beta-free mode).  0 on invalid arguments. */

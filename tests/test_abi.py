@@ -97,10 +97,11 @@ def test_host_entry_checks_host_seqlens_before_any_gpu_work(lib):
     assert rc == -5
 
 
-def _bwd(lib, dims, q=1, do=1, dq=1, dg=1, beta=None, dbeta=None, cu=None, opt=None):
+def _bwd(lib, dims, q=1, do=1, dq=1, dg=1, beta=None, dbeta=None, cu=None, opt=None,
+         n_segments=0):
     p = lambda x: None if x is None else ctypes.c_void_p(0x1000 * x)
     return lib.gdr_chunk_bwd(ctypes.byref(dims), p(q), p(1), p(1), p(1), p(beta), p(cu), None,
-                             p(do), None, p(dq), p(1), p(1), p(dg), p(dbeta), None,
+                             p(do), None, p(dq), p(1), p(1), p(dg), p(dbeta), None, n_segments,
                              None if opt is None else ctypes.byref(opt), None)
 
 
@@ -116,6 +117,8 @@ def test_backward_argument_checks_reject_before_any_gpu_work(lib):
     assert _bwd(lib, api.make_dims(1, 128, 2, 64, 64, N=3)) == -1  # varlen needs cu
     assert _bwd(lib, ok, opt=api.gdr_options(0.0, 2, 0, None, 0, None)) == -1  # no forced plan
     assert _bwd(lib, ok, opt=api.gdr_options(float("nan"), 0, 0, None, 0, None)) == -1
+    assert _bwd(lib, ok, n_segments=-1) == -1
+    assert _bwd(lib, ok, n_segments=1000) == -2
     assert pkg.gdr_kernel_name(16) == "bwd_gram" and pkg.gdr_kernel_name(19) == "bwd_local"
 
 
@@ -125,6 +128,8 @@ def test_backward_workspace_size_grows_with_the_problem(lib):
     c = pkg.gdr_bwd_workspace_size(1, 1024, 4, 128, 128, beta_free=True)
     assert 0 < c < a < b
     assert pkg.gdr_bwd_workspace_size(1, 1024, 4, 60, 128) == 0
+    # a split keeps per-segment summaries as well
+    assert pkg.gdr_bwd_workspace_size(1, 1024, 4, 128, 128, n_segments=4) > a
 
 
 def _rec(lib, dims, q=1, state=1, n_states=4, idx=None, cu=None):

@@ -167,3 +167,31 @@ def test_full_size_sampled_pairs(name):
     mask = np.zeros(pairs, dtype=bool)
     mask[[0, pairs // 2, pairs - 1]] = True
     check(x, pair_mask=mask)
+
+
+@pytest.mark.parametrize("S", [2, 4, 16])
+@pytest.mark.parametrize("case", ["bf16_varlen_h0", "f32_k64", "f32_k256", "beta_free"])
+def test_segment_split(case, S):
+    """The forward recompute and the reverse scan split into S segments: the
+    pre-scan, the ordered composition from the last segment to the first (the
+    delta-rule composition at K <= 128, the generic one at K = 256, the
+    scalar one for beta-free) and the output pass give the same gradients
+    within the tolerances."""
+    if case == "bf16_varlen_h0":
+        w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True)
+        x = synthetic.make_inputs(w, lengths=[700, 65, 1, 300, 0])
+    elif case == "f32_k64":
+        x = synthetic.make_inputs(synthetic.small(W["tiny_dense_f32"], T=900, B=2))
+    elif case == "f32_k256":
+        x = synthetic.make_inputs(synthetic.small(W["tiny_dense_f32"], K=256, V=64, T=600))
+    else:
+        x = synthetic.make_inputs(synthetic.small(W["gla_k256_v512_bf16"], B=1, T=1000, H=2,
+                                                  V=128))
+    check(x, n_segments=S)
+
+
+def test_long_single_sequence_split_matches_oracle():
+    """One 4096-token sequence, one head (the low-wave shape the split is
+    for), automatic plan, against the oracle."""
+    w = synthetic.small(W["stress_64k_h1_bf16"], T=4096)
+    check(synthetic.make_inputs(w))
