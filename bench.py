@@ -297,16 +297,25 @@ def traffic_record(kernel, workload):
 
 
 def source_hash(kernel):
-    """sha256 (16 hex digits) of the kernel's .cu file and every header."""
-    import glob
+    """sha256 (16 hex digits) of the kernel's .cu file and of every header it
+    includes, directly or through other headers of the package."""
+    import re
     csrc = os.path.join(ROOT, "chunked_gated_delta_rule_gb300", "csrc")
     main = next((v for k, v in KERNEL_SOURCES.items() if kernel.startswith(k)), None)
     if main is None:
         main = "compose.cu" if "compose" in kernel else "simt_path.cu"
-    files = [os.path.join(csrc, main)] + sorted(glob.glob(os.path.join(csrc, "*.cuh")))
+    seen, order, todo = set(), [], [main]
+    while todo:
+        f = todo.pop(0)
+        if f in seen or not os.path.exists(os.path.join(csrc, f)):
+            continue
+        seen.add(f)
+        order.append(f)
+        text = open(os.path.join(csrc, f)).read()
+        todo += re.findall(r'#include\s+"([^"]+)"', text)
     h = hashlib.sha256()
-    for f in files:
-        h.update(open(f, "rb").read())
+    for f in [order[0]] + sorted(order[1:]):
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -772,7 +781,7 @@ def run_bwd(args):
                 dbeta=None if d["beta"] is None else torch.empty_like(d["beta"]),
                 dh0=torch.empty(x["N"], x["H"], x["K"], x["V"], dtype=torch.float32, device=dev))
     args_t = (d["q"], d["k"], d["v"], d["g"], d["beta"], do)
-    kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], dht=dht, **outs)
+    kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], dht=dht, n_segments=args.segments, **outs)
     c = counts(x)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -900,6 +909,7 @@ def run_bwd(args):
     if rank == 0:
         cfg = config_of(args, x, None)
         cfg["entry_point"] = "gdr_chunk_bwd"
+        cfg["n_segments"] = args.segments or "auto"
         cfg["incoming_gradients"] = "do ~ N(0,1) in the input dtype, dht ~ N(0,1) FP32, seed 7"
         line = {"metric": METRIC_BWD, "value": world * c["tokens"] / (ms * 1e-3), "unit": UNIT,
                 "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
