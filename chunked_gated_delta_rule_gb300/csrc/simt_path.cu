@@ -567,9 +567,11 @@ k_compose(Problem p, Workspace ws) {
 // A7: o = scale [(Q e^G) h_pre + (Q K^T * e^{G_i - G_j}, j <= i) v_new]
 // per (chunk, head, value block).  The causal mask includes the diagonal:
 // o_t reads the state after token t's own write.
-template <typename Tin>
+template <typename Tin, int BVO>
 __global__ void __launch_bounds__(kThreads)
-k_output(Problem p, Workspace ws, int bvo) {
+k_output(Problem p, Workspace ws) {
+    constexpr int NS = BVO / 16;
+    constexpr int ldo = BVO + 1;
     const int64_t chunk = blockIdx.x;
     const int h = blockIdx.y;
     if (chunk >= *ws.n_chunks) return;
@@ -577,36 +579,62 @@ k_output(Problem p, Workspace ws, int bvo) {
     const int64_t t0 = e.y;
     const int len = e.z;
     const int H = (int)p.H, K = (int)p.K, V = (int)p.V;
-    const int col0 = blockIdx.z * bvo;
+    const int col0 = blockIdx.z * BVO;
     const int tid = threadIdx.x;
-    const int ldk = K + 1, ldo = bvo + 1;
+    const int i0 = 4 * (tid >> 4), j0 = tid & 15;
+    const int Kp = (K + 63) & ~63;  // keys padded with zeros to whole 64-column tiles
+    const int ldk = Kp + 1;
     const bool delta = p.beta != nullptr;
 
     extern __shared__ float sm[];
-    float *sQ = sm;
-    float *sK = sQ + kChunk * ldk;
-    float *sP = sK + kChunk * ldk;
-    float *sHp = sP + kChunk * 65;
-    float *sVn = sHp + K * ldo;
+    float *sQ = sm;                  // [64][Kp+1]
+    float *sK = sQ + kChunk * ldk;   // [64][Kp+1]
+    float *sP = sK + kChunk * ldk;   // [64][65]
+    float *sHp = sP + kChunk * 65;   // [Kp][BVO+1]
+    float *sVn = sHp + Kp * ldo;     // [64][BVO+1]
     float *sG = sVn + kChunk * ldo;
 
     const Tin *q = static_cast<const Tin *>(p.q);
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
     if (tid < kChunk) sG[tid] = ws.G[(chunk * H + h) * kChunk + tid];
-    for (int idx = tid; idx < kChunk * K; idx += kThreads) {
-        const int i = idx / K, c = idx - i * K;
-        const int64_t off = ((t0 + i) * H + h) * (int64_t)K + c;
-        sQ[i * ldk + c] = i < len ? ld_in(q, off) : 0.f;
-        sK[i * ldk + c] = i < len ? ld_in(k, off) : 0.f;
+    const bool vin = ((reinterpret_cast<uintptr_t>(p.q) | reinterpret_cast<uintptr_t>(p.k)) & 15) == 0;
+    if (vin) {  // 16-byte pieces (K is a multiple of 16)
+        constexpr int E = 16 / (int)sizeof(Tin);
+        const int pr = Kp / E;
+        for (int idx = tid; idx < kChunk * pr; idx += kThreads) {
+            const int i = idx / pr, c = (idx - i * pr) * E;
+            float xq[E], xk[E];
+            if (i < len && c < K) {
+                const int64_t off = ((t0 + i) * H + h) * (int64_t)K + c;
+                unpack16(__ldg(reinterpret_cast<const uint4 *>(q + off)), q, xq);
+                unpack16(__ldg(reinterpret_cast<const uint4 *>(k + off)), k, xk);
+            } else {
+#pragma unroll
+                for (int e2 = 0; e2 < E; ++e2) xq[e2] = xk[e2] = 0.f;
+            }
+#pragma unroll
+            for (int e2 = 0; e2 < E; ++e2) {
+                sQ[i * ldk + c + e2] = xq[e2];
+                sK[i * ldk + c + e2] = xk[e2];
+            }
+        }
+    } else {
+        for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
+            const int i = idx / Kp, c = idx - i * Kp;
+            const bool in = i < len && c < K;
+            const int64_t off = ((t0 + i) * H + h) * (int64_t)K + c;
+            sQ[i * ldk + c] = in ? ld_in(q, off) : 0.f;
+            sK[i * ldk + c] = in ? ld_in(k, off) : 0.f;
+        }
     }
     const float *hp = ws.hpre + (chunk * H + h) * (int64_t)K * V;
-    for (int idx = tid; idx < K * bvo; idx += kThreads) {
-        const int key = idx / bvo, c = idx - key * bvo;
-        sHp[key * ldo + c] = hp[(int64_t)key * V + col0 + c];
+    for (int idx = tid; idx < Kp * BVO; idx += kThreads) {
+        const int key = idx / BVO, c = idx - key * BVO;
+        sHp[key * ldo + c] = key < K ? hp[(int64_t)key * V + col0 + c] : 0.f;
     }
-    for (int idx = tid; idx < kChunk * bvo; idx += kThreads) {
-        const int i = idx / bvo, c = idx - i * bvo;
+    for (int idx = tid; idx < kChunk * BVO; idx += kThreads) {
+        const int i = idx / BVO, c = idx - i * BVO;
         float x = 0.f;
         if (i < len) {
             x = delta ? ws.vnew[((chunk * H + h) * kChunk + i) * (int64_t)V + col0 + c]
@@ -615,27 +643,28 @@ k_output(Problem p, Workspace ws, int bvo) {
         sVn[i * ldo + c] = x;
     }
     __syncthreads();
-    for (int idx = tid; idx < kChunk * kChunk; idx += kThreads) {
-        const int i = idx >> 6, j = idx & 63;
-        float a = 0.f;
-        if (j <= i && i < len) {
-            float d = 0.f;
-            for (int c = 0; c < K; ++c) d = fmaf(sQ[i * ldk + c], sK[j * ldk + c], d);
-            a = d * expf(sG[i] - sG[j]);
+    {  // P = Q K^T * e^{G_i - G_j}, causal with the diagonal
+        float d[4][4];
+        acc_zero(d);
+        mm_abT<4>(d, sQ, ldk, sK, ldk, Kp, tid);
+        FOR_TILE(4) {
+            const int i = i0 + r, jj = j0 + 16 * s;
+            sP[i * 65 + jj] = (jj <= i && i < len) ? d[r][s] * expf(sG[i] - sG[jj]) : 0.f;
         }
-        sP[i * 65 + j] = a;
     }
     __syncthreads();
     Tin *o = static_cast<Tin *>(p.o);
-    for (int idx = tid; idx < kChunk * bvo; idx += kThreads) {
-        const int i = idx / bvo, c = idx - i * bvo;
-        if (i >= len) continue;
-        float a1 = 0.f;
-        for (int key = 0; key < K; ++key) a1 = fmaf(sQ[i * ldk + key], sHp[key * ldo + c], a1);
-        float a2 = 0.f;
-        for (int j = 0; j <= i; ++j) a2 = fmaf(sP[i * 65 + j], sVn[j * ldo + c], a2);
-        const float y = p.scale * fmaf(expf(sG[i]), a1, a2);
-        st_out(o, ((t0 + i) * H + h) * (int64_t)V + col0 + c, y);
+    float a1[4][NS], a2[4][NS];
+    acc_zero(a1);
+    acc_zero(a2);
+    mm_ab<NS>(a1, sQ, ldk, sHp, ldo, Kp, tid);
+    mm_ab<NS>(a2, sP, 65, sVn, ldo, kChunk, tid);
+    FOR_TILE(NS) {
+        const int i = i0 + r, c = j0 + 16 * s;
+        if (i < len) {
+            const float y = p.scale * fmaf(expf(sG[i]), a1[r][s], a2[r][s]);
+            st_out(o, ((t0 + i) * H + h) * (int64_t)V + col0 + c, y);
+        }
     }
 }
 
@@ -735,27 +764,33 @@ cudaError_t simt_compose(const Problem &p, const Workspace &ws, int bv, cudaStre
     return cudaErrorInvalidValue;
 }
 
+template <typename Tin, int BVO>
+static cudaError_t launch_output(const Problem &p, const Workspace &ws, cudaStream_t st) {
+    const int Kp = ((int)p.K + 63) & ~63;
+    const size_t smem = sizeof(float) *
+        (2 * (size_t)kChunk * (Kp + 1) + kChunk * 65 + (size_t)Kp * (BVO + 1) +
+         (size_t)kChunk * (BVO + 1) + kChunk);
+    cudaError_t err = set_smem(k_output<Tin, BVO>, smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((unsigned)ws.max_chunks, (unsigned)p.H, (unsigned)(p.V / BVO));
+    k_output<Tin, BVO><<<grid, kThreads, smem, st>>>(p, ws);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+static cudaError_t output_for(const Problem &p, const Workspace &ws, cudaStream_t st) {
+    int bvo = p.K <= 128 ? 64 : 32;
+    while (p.V % bvo) bvo >>= 1;
+    if (bvo == 64) return launch_output<Tin, 64>(p, ws, st);
+    if (bvo == 32) return launch_output<Tin, 32>(p, ws, st);
+    return launch_output<Tin, 16>(p, ws, st);
+}
+
 cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st) {
     if (ws.max_chunks == 0) return cudaSuccess;
-    const int K = (int)p.K, V = (int)p.V;
-    int bvo = K <= 128 ? 64 : 32;
-    while (V % bvo) bvo >>= 1;
-    const size_t smem = sizeof(float) *
-        (2 * (size_t)kChunk * (K + 1) + kChunk * 65 + (size_t)K * (bvo + 1) +
-         (size_t)kChunk * (bvo + 1) + kChunk);
-    dim3 grid((unsigned)ws.max_chunks, (unsigned)p.H, (unsigned)(V / bvo));
-    cudaError_t err;
-    if (p.dtype == GDR_BF16) {
-        if ((err = set_smem(k_output<__nv_bfloat16>, smem)) != cudaSuccess) return err;
-        k_output<__nv_bfloat16><<<grid, kThreads, smem, st>>>(p, ws, bvo);
-    } else if (p.dtype == GDR_F16) {
-        if ((err = set_smem(k_output<__half>, smem)) != cudaSuccess) return err;
-        k_output<__half><<<grid, kThreads, smem, st>>>(p, ws, bvo);
-    } else {
-        if ((err = set_smem(k_output<float>, smem)) != cudaSuccess) return err;
-        k_output<float><<<grid, kThreads, smem, st>>>(p, ws, bvo);
-    }
-    return cudaGetLastError();
+    if (p.dtype == GDR_BF16) return output_for<__nv_bfloat16>(p, ws, st);
+    if (p.dtype == GDR_F16) return output_for<__half>(p, ws, st);
+    return output_for<float>(p, ws, st);
 }
 
 }  // namespace gdr
