@@ -150,17 +150,27 @@ int validate_dims(const gdr_dims *d) {
     return GDR_OK;
 }
 
-// Value columns per scan CTA: the widest of 64/32/16 that divides both V and
-// K (the transition tiles of the segment pre-scan cover K columns) and keeps
-// the scan's shared memory within 227 KB.
+// Value columns per scan CTA, among the widths that divide both V and K (the
+// transition tiles of the segment pre-scan cover K columns) and keep the
+// scan's shared memory within 227 KB: 32 columns, measured fastest on GB300
+// (wide varlen batch 2.29 ms against 2.53 at 64 and 2.64 at 16; beta-free
+// K = 256, V = 512: 5.51 against 5.66 and 6.92); 16 when 32-column tiles
+// leave SMs without a chain (tiny dense FP32: 0.102 ms against 0.110 and
+// 0.129); 64 only when neither divides.
 int pick_bv(const gdr_dims &d) {
     const size_t Kp = ((size_t)d.K + 63) & ~(size_t)63;  // keys padded to 64-row tiles
-    for (int bv : {64, 32, 16}) {
-        if (d.V % bv || d.K % bv) continue;
+    auto fits = [&](int bv) {
+        if (d.V % bv || d.K % bv) return false;
         const size_t smem = sizeof(float) * (Kp * (bv + 1) + 2 * (size_t)kChunk * (Kp + 1) +
                                              (size_t)kChunk * (bv + 1) + kChunk);
-        if (smem <= 227 * 1024) return bv;
+        return smem <= 227 * 1024;
+    };
+    if (fits(32)) {
+        const int64_t chains = n_seqs(d) * d.H * (d.V / 32);
+        return (chains < kNumSMs && fits(16)) ? 16 : 32;
     }
+    for (int bv : {16, 64})
+        if (fits(bv)) return bv;
     return 16;
 }
 
@@ -609,14 +619,13 @@ int gdr_chunk_fwd(const gdr_dims *dims, const void *q, const void *k, const void
                             nullptr, stream);
 }
 
-// The backward's plan: the forward recompute's scan takes 32-column tiles
-// where they fit (twice the chains of the forward plan's 64; measured faster
-// inside the backward), and the segment count follows the CUDA-core path's
-// rule unless the caller fixes it.
+// The backward's plan: the CUDA-core path's value tile for the forward
+// recompute (32 columns on the wide varlen batch: its scan 0.98 ms at 64,
+// 0.74 ms at 32) and its segment rule unless the caller fixes the count.
 int bwd_plan(const gdr_dims &d, bool beta_free, int n_segments, int *bv, int *S) {
     if (n_segments < 0) return GDR_ERR_INVALID;
     if (n_segments > kMaxSegments) return GDR_ERR_UNSUPPORTED;
-    *bv = (d.V % 32 == 0 && d.K % 32 == 0) ? 32 : pick_bv(d);
+    *bv = pick_bv(d);
     *S = n_segments > 0 ? n_segments : auto_segments(d, beta_free, 1, *bv);
     return GDR_OK;
 }
