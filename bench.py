@@ -497,9 +497,13 @@ def run_gdr(args):
                               x["cu_seqlens"] is not None else 0,
                               dtype=0 if x["dtype"] == "f32" else 1,
                               beta_free=x["beta"] is None, n_segments=args.segments)
-    if args.force_path:
-        plan["path"] = args.force_path
-    c = counts(x, plan["n_segments"])
+    seg_count = plan["n_segments"]
+    if args.force_path and args.force_path != plan["path"]:
+        # the query plans the default path; a forced path applies its own rules
+        seg_count = args.segments or 1
+        plan = {"path": args.force_path, "bv": "per the forced path's rule",
+                "n_segments": args.segments or "per the forced path's rule"}
+    c = counts(x, seg_count)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
