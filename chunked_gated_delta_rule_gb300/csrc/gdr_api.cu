@@ -155,8 +155,9 @@ int validate_dims(const gdr_dims *d) {
 // scan's shared memory within 227 KB: 32 columns, measured fastest on GB300
 // (wide varlen batch 2.29 ms against 2.53 at 64 and 2.64 at 16; beta-free
 // K = 256, V = 512: 5.51 against 5.66 and 6.92); 16 when 32-column tiles
-// leave SMs without a chain (tiny dense FP32: 0.102 ms against 0.110 and
-// 0.129); 64 only when neither divides.
+// leave SMs without a chain and the sequences are too short for a segment
+// split to add chains (tiny dense FP32: 0.102 ms against 0.110 and 0.129);
+// 64 only when neither divides.
 int pick_bv(const gdr_dims &d) {
     const size_t Kp = ((size_t)d.K + 63) & ~(size_t)63;  // keys padded to 64-row tiles
     auto fits = [&](int bv) {
@@ -167,7 +168,9 @@ int pick_bv(const gdr_dims &d) {
     };
     if (fits(32)) {
         const int64_t chains = n_seqs(d) * d.H * (d.V / 32);
-        return (chains < kNumSMs && fits(16)) ? 16 : 32;
+        const int64_t cps = is_varlen(d) ? (d.N ? (d.T / d.N + kChunk - 1) / kChunk : 0)
+                                         : (d.T + kChunk - 1) / kChunk;
+        return (chains < kNumSMs && cps < 32 && fits(16)) ? 16 : 32;  // a split needs 32 chunks
     }
     for (int bv : {16, 64})
         if (fits(bv)) return bv;
@@ -322,7 +325,8 @@ Workspace carve_workspace(void *base, const WorkspaceLayout &L, int S) {
 // the per-(chunk, head) buffers of BwdWs.
 struct BwdLayout {
     WorkspaceLayout fwd;
-    size_t off_Mq, off_Kd, off_Tm, off_dhend, off_dvn, off_P1, off_P2, off_P3, off_ehp, total;
+    size_t off_Mq, off_Kd, off_Tm, off_dhend, off_dvn, off_P1, off_P2, off_P3, off_ehp,
+        off_segMb, total;
 };
 
 BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments) {
@@ -346,6 +350,8 @@ BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments) {
     B.off_P2 = take(delta ? sizeof(float) * items * kChunk * K : 0);
     B.off_P3 = take(sizeof(float) * items * kChunk * K);
     B.off_ehp = take(sizeof(float) * items * ((K + 63) / 64));
+    const size_t segs = n_segments > 1 ? (size_t)n_seqs(d) * d.H * (size_t)n_segments : 0;
+    B.off_segMb = take(delta ? sizeof(float) * segs * K * K : 0);
     B.total = off;
     return B;
 }
@@ -363,6 +369,7 @@ BwdWs carve_bwd(void *base, const BwdLayout &B) {
     w.P2 = f(B.off_P2);
     w.P3 = f(B.off_P3);
     w.ehp = f(B.off_ehp);
+    w.segMb = f(B.off_segMb);
     return w;
 }
 
@@ -491,6 +498,7 @@ const char *gdr_kernel_name(int id) {
     case kKBwdLocal: return "bwd_local";
     case kKBwdPre: return "bwd_dscan_prescan";
     case kKBwdSegOut: return "bwd_dscan_segment_out";
+    case kKBwdMaps: return "bwd_maps";
     default: return "?";
     }
 }

@@ -126,6 +126,7 @@ struct BwdWs {
     float *P2;     // [items][64][K] dV' h^T (delta)
     float *P3;     // [items][64][K] V' E^T
     float *ehp;    // [items][ceil(K/64)] <E, h> per 64-key slice
+    float *segMb;  // [N][H][S][K][K] the reverse scan's segment maps (delta, split)
 };
 
 // Byte layout of the workspace for one problem.
@@ -164,6 +165,7 @@ enum KernelId {
     kKBwdLocal = 19,
     kKBwdPre = 20,
     kKBwdSegOut = 21,
+    kKBwdMaps = 22,
     kKNumIds
 };
 

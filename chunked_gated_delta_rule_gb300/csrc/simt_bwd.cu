@@ -213,10 +213,10 @@ __global__ void __launch_bounds__(kBT) k_bwd_gram(Problem p, Workspace ws, BwdWs
 // the dO terms, so the scan splits into segments like the forward one (the
 // pages' "Proposed Dataflow" step 4: the reverse recurrence mirrors the
 // split).  mode 0: whole sequence from dht, writes dh0; mode 1: segment
-// pre-scan, value columns from E = 0 (-> the segment's offset c) and, in
-// delta mode, transition columns from the identity with dO taken as 0 (-> its
-// K x K map, stored transposed); mode 2: segment output pass from the
-// composed E at the segment's end.  Modes 0 and 2 store E and dV' per chunk.
+// pre-scan from E = 0 (-> the segment's offset c; its K x K map is the
+// transpose of the forward map, see k_bwd_maps); mode 2: segment output pass
+// from the composed E at the segment's end.  Modes 0 and 2 store E and dV'
+// per chunk.
 // Segment s of a sequence's nseg segments keeps its summaries in slot
 // nseg - 1 - s, so the ordered composition runs from the last segment to the
 // first: it starts from dht and ends at dh0.
@@ -229,14 +229,13 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
     const bool delta_mode = p.beta != nullptr;
     const int S = mode == 0 ? 1 : ws.n_segments;
     const int n_vtiles = V / BV;
-    const int ntiles = (mode == 1 && delta_mode) ? (V + K) / BV : n_vtiles;
+    const int ntiles = n_vtiles;
     int64_t bid = blockIdx.x;
     const int tile = (int)(bid % ntiles);
     bid /= ntiles;
     const int seg = (int)(bid % S);
     const int64_t n = bid / S;
-    const bool trans = tile >= n_vtiles;
-    const int col0 = trans ? (tile - n_vtiles) * BV : tile * BV;
+    const int col0 = tile * BV;
     const int h = blockIdx.y, tid = threadIdx.x;
     const int i0 = 4 * (tid >> 4), j0 = tid & 15;
     const bool delta = p.beta != nullptr;
@@ -269,8 +268,6 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
             x = a.dht ? a.dht[state_off(p, nh, key, col0 + c)] : 0.f;
         else if (mode == 2)
             x = ws.segH[(seg_base * K + key) * V + col0 + c];
-        else if (trans)
-            x = (key == col0 + c) ? 1.f : 0.f;
         sE[key * LDE + c] = x;
     }
     const Tin *q = static_cast<const Tin *>(p.q);
@@ -300,8 +297,8 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
             sM[(idx >> 6) * kLd + (idx & 63)] = bw.Mq[item * kChunk * kChunk + idx];
         for (int idx = tid; idx < kChunk * BV; idx += kBT) {
             const int i = idx / BV, c = idx - i * BV;
-            sDo[i * LDE + c] = (i < ci.len && !trans)
-                ? ldx(dout, ((ci.t0 + i) * H + h) * (int64_t)V + col0 + c) : 0.f;
+            sDo[i * LDE + c] =
+                i < ci.len ? ldx(dout, ((ci.t0 + i) * H + h) * (int64_t)V + col0 + c) : 0.f;
         }
         // dV' = scale M^T dO + diag(lam) K E
         float acc[4][NS];
@@ -368,12 +365,46 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
     } else if (mode == 1) {
         for (int idx = tid; idx < K * BV; idx += kBT) {
             const int key = idx / BV, c = idx - key * BV;
-            if (trans)  // stored transposed: row m of the map's transpose is its column m
-                ws.segM[(seg_base * K + col0 + c) * K + key] = sE[key * LDE + c];
-            else
-                ws.segC[(seg_base * K + key) * V + col0 + c] = sE[key * LDE + c];
+            ws.segC[(seg_base * K + key) * V + col0 + c] = sE[key * LDE + c];
         }
         if (!delta_mode && tile == 0 && tid == 0) ws.segD[seg_base] = dprod;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// k_bwd_maps: the K x K maps of the reverse scan's segments, from the forward
+// recompute's.  The reverse step is the transpose of the forward step
+// (Gam I - W^T diag(lam) K = (Gam I - K^T diag(lam) W)^T), so a segment's
+// reverse map is the transpose of its forward map.  The forward pre-scan
+// stores map M_s of segment s transposed; the composition of the reverse
+// scan reads its maps transposed too, in reversed slots, so block s is
+// copied untransposed (M_s^T transposed back) into slot nseg - 1 - s of
+// segMb.  One CTA per (sequence, head, segment), 32 x 32 tiles through
+// shared memory.
+__global__ void __launch_bounds__(kBT) k_bwd_maps(Problem p, Workspace ws, float *segMb) {
+    const int K = (int)p.K, H = (int)p.H, S = ws.n_segments, tid = threadIdx.x;
+    const int s = (int)(blockIdx.x % S);
+    const int64_t nh = blockIdx.x / S, n = nh / H;
+    const int nc = ws.seq_chunk0[n + 1] - ws.seq_chunk0[n];
+    const int per = (nc + S - 1) / S;
+    const int nseg = per ? (nc + per - 1) / per : 0;
+    if (s >= nseg) return;
+    const float *src = ws.segM + (nh * S + s) * (int64_t)K * K;
+    float *dst = segMb + (nh * S + (nseg - 1 - s)) * (int64_t)K * K;
+    __shared__ float tile[32][33];
+    for (int r0 = 0; r0 < K; r0 += 32) {
+        for (int c0 = 0; c0 < K; c0 += 32) {
+            __syncthreads();
+            for (int idx = tid; idx < 32 * 32; idx += kBT) {
+                const int y = idx >> 5, x = idx & 31;
+                if (r0 + y < K && c0 + x < K) tile[y][x] = src[(int64_t)(r0 + y) * K + c0 + x];
+            }
+            __syncthreads();
+            for (int idx = tid; idx < 32 * 32; idx += kBT) {
+                const int y = idx >> 5, x = idx & 31;
+                if (c0 + y < K && r0 + x < K) dst[(int64_t)(c0 + y) * K + r0 + x] = tile[x][y];
+            }
+        }
     }
 }
 
@@ -739,11 +770,11 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
     // last segment to the first + segment output pass
     {
         const int S = ws.n_segments;
-        const int bv = (V % 32 == 0 && (S <= 1 || K % 32 == 0)) ? 32 : 16;
+        const int bv = V % 32 == 0 ? 32 : 16;
         const size_t smem = sizeof(float) * ((size_t)K * (bv + 1) + 3 * kChunk * kLd +
                                              2 * kChunk * (bv + 1) + 2 * kChunk);
         auto launch = [&](int mode) -> cudaError_t {
-            const int ntiles = (mode == 1 && delta) ? (V + K) / bv : V / bv;
+            const int ntiles = V / bv;
             const dim3 grid((unsigned)(p.N * (mode == 0 ? 1 : S) * ntiles), H);
             cudaError_t r;
             if (bv == 32) {
@@ -763,14 +794,23 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
             if ((e = rec.begin(kKBwdPre)) != cudaSuccess) return e;
             if ((e = launch(1)) != cudaSuccess) return e;
             if ((e = rec.end()) != cudaSuccess) return e;
-            // the composition starts from dht and ends at dh0
+            // the composition starts from dht and ends at dh0, with the
+            // transposed forward maps in reversed slots
             Problem pr = p;
             pr.h0 = a.dht;
             pr.ht = a.dh0;
+            Workspace wr = ws;
+            if (delta) {
+                if ((e = rec.begin(kKBwdMaps)) != cudaSuccess) return e;
+                k_bwd_maps<<<(unsigned)(p.N * H * S), kBT, 0, st>>>(p, ws, bw.segMb);
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+                if ((e = rec.end()) != cudaSuccess) return e;
+                wr.segM = bw.segMb;
+            }
             if ((e = rec.begin(delta ? kKCompose : kKComposeScalar)) != cudaSuccess) return e;
-            if (!delta) e = compose_scalar(pr, ws, st);
-            else if (compose_mt_supported(pr)) e = compose_mt(pr, ws, st);
-            else e = simt_compose(pr, ws, bv, st);
+            if (!delta) e = compose_scalar(pr, wr, st);
+            else if (compose_mt_supported(pr)) e = compose_mt(pr, wr, st);
+            else e = simt_compose(pr, wr, bv, st);
             if (e != cudaSuccess) return e;
             if ((e = rec.end()) != cudaSuccess) return e;
             if ((e = rec.begin(kKBwdSegOut)) != cudaSuccess) return e;
