@@ -185,8 +185,9 @@ int pick_bv(const gdr_dims &d) {
 // t_step per segment, and an output pass.  The model reproduces the measured
 // best counts (16K x 16 heads: 8; 64K x 8 heads: 16; 64K x 1 head: 64;
 // beta-free K = 256, V = 512, 2 x 8K x 4 heads: 4; the wide varlen batch: 1).
-// CUDA-core path: split until about two CTAs per SM, at most 16 segments,
-// while every segment keeps at least 8 chunks.
+// CUDA-core path: split until about two CTAs per SM, at most 64 segments,
+// while every segment keeps at least 8 chunks (one 64K-token head's
+// backward: 8.2 ms at 16 segments, 5.1 at 32, 3.8 at 64).
 // The delta pre-scan of `segs` (sequence, segment, head) chains runs each of
 // their two summaries as its own chain while all of them fit one wave.
 bool prescan_split_kinds(int64_t segs) { return 2 * segs <= kNumSMs; }
@@ -198,7 +199,7 @@ int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     if (path != 2) {
         const int64_t chains = nseq * d.H * (d.V / bv);
         int S = 1;
-        while (S < 16 && chains * S < 2 * kNumSMs && cps / (2 * S) >= 8) S *= 2;
+        while (S < kMaxSegments && chains * S < 2 * kNumSMs && cps / (2 * S) >= 8) S *= 2;
         return S;
     }
     const int64_t chains = nseq * d.H * (beta_free ? d.V / 128 : 1);

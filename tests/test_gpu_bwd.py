@@ -169,7 +169,7 @@ def test_full_size_sampled_pairs(name):
     check(x, pair_mask=mask)
 
 
-@pytest.mark.parametrize("S", [2, 4, 16])
+@pytest.mark.parametrize("S", [2, 4, 16, 64])
 @pytest.mark.parametrize("case", ["bf16_varlen_h0", "f32_k64", "f32_k256", "beta_free"])
 def test_segment_split(case, S):
     """The forward recompute and the reverse scan split into S segments: the
