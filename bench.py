@@ -495,7 +495,7 @@ def run_gdr(args):
     args_t = (d["q"], d["k"], d["v"], d["g"], d["beta"])
     plan = pkg.gdr_plan_query(x["B"], x["T"], x["H"], x["K"], x["V"], N=x["N"] if
                               x["cu_seqlens"] is not None else 0,
-                              dtype=0 if x["dtype"] == "f32" else 1,
+                              dtype={"f32": 0, "bf16": 1, "f16": 2}[x["dtype"]],
                               beta_free=x["beta"] is None, n_segments=args.segments)
     seg_count = plan["n_segments"]
     if args.force_path and args.force_path != plan["path"]:

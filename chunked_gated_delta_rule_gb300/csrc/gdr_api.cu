@@ -234,10 +234,13 @@ int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
 // Shapes the tensor-core path covers (pointer alignment is checked per call):
 // the delta rule at K = V = 128; the beta-free mode at K in {128, 256} with
 // V a multiple of 128.
-bool tc_shape(const gdr_dims &d, bool beta_free) {
-    if (d.dtype != GDR_BF16) return false;
+bool tc_shape_any_dtype(const gdr_dims &d, bool beta_free) {
     if (!beta_free) return d.K == 128 && d.V == 128;
     return (d.K == 128 || d.K == 256) && d.V % 128 == 0;
+}
+
+bool tc_shape(const gdr_dims &d, bool beta_free) {
+    return d.dtype == GDR_BF16 && tc_shape_any_dtype(d, beta_free);
 }
 
 int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_options *opt,
@@ -247,7 +250,10 @@ int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_optio
     p.bv = p.path == 2 ? 128 : pick_bv(d);
     if (opt && opt->force_path) {
         if (opt->force_path != 1 && opt->force_path != 2) return GDR_ERR_INVALID;
-        if (opt->force_path == 2 && !tc_shape(d, beta_free)) return GDR_ERR_UNSUPPORTED;
+        // FP16 inputs run the tensor-core kernels on BF16 copies, when forced
+        const bool tc_ok = tc_shape(d, beta_free) ||
+                           (d.dtype == GDR_F16 && tc_shape_any_dtype(d, beta_free));
+        if (opt->force_path == 2 && !tc_ok) return GDR_ERR_UNSUPPORTED;
         p.path = opt->force_path;
         p.bv = p.path == 2 ? 128 : pick_bv(d);
     }
@@ -500,6 +506,8 @@ const char *gdr_kernel_name(int id) {
     case kKBwdPre: return "bwd_dscan_prescan";
     case kKBwdSegOut: return "bwd_dscan_segment_out";
     case kKBwdMaps: return "bwd_maps";
+    case kKConvertIn: return "convert_f16_to_bf16";
+    case kKConvertOut: return "convert_bf16_to_f16";
     default: return "?";
     }
 }
@@ -585,25 +593,12 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
     p.scale = (opt && opt->scale > 0.f) ? opt->scale : 1.0f / std::sqrt((float)dims->K);
     p.status = opt ? opt->status : nullptr;
     if (p.N == 0) return GDR_OK;
-    const bool tc_ok = beta_free ? tc_gla_supported(p) : tc_supported(p);
-    if (plan.path == 2 && !tc_ok) {
-        if (opt && opt->force_path == 2) return GDR_ERR_INVALID;  // misaligned pointers
-        plan.path = 1;
-        plan.bv = pick_bv(*dims);
-    }
-
-    const WorkspaceLayout L = workspace_layout(*dims, beta_free, plan.n_segments, plan.path);
-    void *base = nullptr;
-    bool owned = false;
-    if (opt && opt->workspace) {
-        if (opt->workspace_bytes < L.total) return GDR_ERR_WORKSPACE;
-        if (reinterpret_cast<uintptr_t>(opt->workspace) % kAlign) return GDR_ERR_INVALID;
-        base = opt->workspace;
-    } else {
-        if (lib_malloc(&base, L.total, st) != cudaSuccess) return GDR_ERR_CUDA;
-        owned = true;
-    }
-    const Workspace ws = carve_workspace(base, L, plan.n_segments);
+    // FP16 inputs on the tensor-core path: the kernels read BF16 copies of q,
+    // k, v and write o in BF16, converted back to FP16 after the pass
+    void *conv = nullptr;
+    void *o_f16 = nullptr;
+    const int64_t nqk = dims->B * dims->T * dims->H * dims->K;
+    const int64_t nvo = dims->B * dims->T * dims->H * dims->V;
     LaunchRecorder rec;
     rec.st = st;
     if (opt) {
@@ -612,7 +607,60 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
         rec.ids = opt->launch_ids;
         if (!opt->events && opt->launch_ids) rec.max_launches = opt->max_launches;
     }
+    if (plan.path == 2 && p.dtype == GDR_F16) {
+        const size_t bqk = align_up(sizeof(uint16_t) * (size_t)nqk);
+        const size_t bvo = align_up(sizeof(uint16_t) * (size_t)nvo);
+        if (lib_malloc(&conv, 2 * bqk + 2 * bvo + kAlign, st) != cudaSuccess) return GDR_ERR_CUDA;
+        char *c = static_cast<char *>(conv);
+        void *qb = c, *kb = c + bqk, *vb = c + 2 * bqk, *ob = c + 2 * bqk + bvo;
+        const void *src[3] = {q, k, v};
+        void *dst[3] = {qb, kb, vb};
+        const int64_t cnt[3] = {nqk, nqk, nvo};
+        for (int i = 0; i < 3; ++i) {
+            if (rec.begin(kKConvertIn) != cudaSuccess ||
+                convert_f16_to_bf16(src[i], dst[i], cnt[i], st) != cudaSuccess ||
+                rec.end() != cudaSuccess) {
+                cudaFreeAsync(conv, st);
+                return GDR_ERR_CUDA;
+            }
+        }
+        p.q = qb; p.k = kb; p.v = vb;
+        o_f16 = p.o;
+        p.o = ob;
+        p.dtype = GDR_BF16;
+    }
+    // every return from here on releases the conversion scratch
+    auto fail = [&](int code) {
+        if (conv) cudaFreeAsync(conv, st);
+        return code;
+    };
+    const bool tc_ok = beta_free ? tc_gla_supported(p) : tc_supported(p);
+    if (plan.path == 2 && !tc_ok) {
+        if (opt && opt->force_path == 2) return fail(GDR_ERR_INVALID);  // misaligned pointers
+        plan.path = 1;
+        plan.bv = pick_bv(*dims);
+    }
+
+    const WorkspaceLayout L = workspace_layout(*dims, beta_free, plan.n_segments, plan.path);
+    void *base = nullptr;
+    bool owned = false;
+    if (opt && opt->workspace) {
+        if (opt->workspace_bytes < L.total) return fail(GDR_ERR_WORKSPACE);
+        if (reinterpret_cast<uintptr_t>(opt->workspace) % kAlign) return fail(GDR_ERR_INVALID);
+        base = opt->workspace;
+    } else {
+        if (lib_malloc(&base, L.total, st) != cudaSuccess) return fail(GDR_ERR_CUDA);
+        owned = true;
+    }
+    const Workspace ws = carve_workspace(base, L, plan.n_segments);
     rc = plan.path == 2 ? run_tc(p, ws, plan, st, rec) : run_simt(p, ws, plan, st, rec);
+    if (conv) {
+        if (rc == GDR_OK && (rec.begin(kKConvertOut) != cudaSuccess ||
+                             convert_bf16_to_f16(p.o, o_f16, nvo, st) != cudaSuccess ||
+                             rec.end() != cudaSuccess))
+            rc = GDR_ERR_CUDA;
+        if (cudaFreeAsync(conv, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;
+    }
     if (opt && opt->n_launches) *opt->n_launches = rec.count;
     if (owned) {
         if (cudaFreeAsync(base, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;

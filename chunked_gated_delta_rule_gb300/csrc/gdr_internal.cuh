@@ -166,6 +166,8 @@ enum KernelId {
     kKBwdPre = 20,
     kKBwdSegOut = 21,
     kKBwdMaps = 22,
+    kKConvertIn = 23,
+    kKConvertOut = 24,
     kKNumIds
 };
 
@@ -201,6 +203,10 @@ cudaError_t simt_scan(const Problem &p, const Workspace &ws, int mode, int bv,
 cudaError_t simt_compose(const Problem &p, const Workspace &ws, int bv,
                          cudaStream_t st);
 cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st);
+// FP16 <-> BF16 element copies (n elements), for FP16 inputs on the
+// tensor-core path.
+cudaError_t convert_f16_to_bf16(const void *src, void *dst, int64_t n, cudaStream_t st);
+cudaError_t convert_bf16_to_f16(const void *src, void *dst, int64_t n, cudaStream_t st);
 // Backward pass after the serial forward recompute (G, W, hpre, vnew in ws).
 cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
                      cudaStream_t st, LaunchRecorder &rec);

@@ -66,6 +66,9 @@ WORKLOADS = {
     # Beta-free (pure gated linear attention) geometry, K=256, V=512.
     "gla_k256_v512_bf16": Workload("gla_k256_v512_bf16", 2, 8192, 4, 256, 512,
                                    "bf16", delta=False, with_h0=True),
+    # The wide varlen batch with FP16 q / k / v.
+    "wide_varlen_f16": Workload("wide_varlen_f16", 1, 0, 16, 128, 128,
+                                "f16", n_seqs=32, len_lo=128, len_hi=512),
     # Decode step: 256 sequences of one token each, every one continuing a
     # state held in a pool (gdr_recurrent_fwd).
     "decode_bf16": Workload("decode_bf16", 1, 0, 16, 128, 128, "bf16", n_seqs=256,

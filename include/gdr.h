@@ -113,7 +113,10 @@ typedef struct gdr_plan {
 /* Options of gdr_chunk_fwd_ex.  Zero-initialise, then set what you need. */
 typedef struct gdr_options {
     float scale;            /* readout scale; 0 => 1/sqrt(K)                */
-    int32_t force_path;     /* 0 => plan; 1 CUDA-core path; 2 tensor cores  */
+    int32_t force_path;     /* 0 => plan; 1 CUDA-core path; 2 tensor cores
+                               (FP16 inputs: the kernels read BF16 copies of
+                               q, k, v and o is converted back to FP16, in
+                               one extra stream-ordered allocation)         */
     int32_t force_bv;       /* 0 => plan; else value columns per scan CTA   */
     void *workspace;        /* device scratch, NULL => stream-ordered alloc */
     size_t workspace_bytes; /* size of `workspace`                          */

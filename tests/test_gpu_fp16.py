@@ -49,3 +49,32 @@ def test_recurrent_fp16():
     ro, rht = run_oracle(x)
     assert rel_l2_masked(o, ro) <= TOL_O_F16
     assert rel_l2_masked(p.cpu()[idx.long()], rht) <= TOL_F32
+
+
+TOL_BF16_OPERANDS = 6e-3  # the BF16 bar: the tensor-core kernels take BF16 operands
+
+
+@pytest.mark.parametrize("case", ["delta_varlen", "beta_free"])
+def test_tensor_core_path_on_fp16_inputs(case):
+    """force_path=2 with FP16 inputs: the kernels read BF16 copies of q, k, v
+    and o comes back in FP16.  Against the oracle on the FP16 inputs the
+    result meets the BF16 bar (BF16 operands); against the BF16 path run on
+    the same BF16-rounded inputs it is bit-identical (ht) and equal after
+    o's final conversion to FP16."""
+    if case == "delta_varlen":
+        w = synthetic.small(W["wide_varlen_bf16"], H=2, dtype="f16", with_h0=True)
+        x = synthetic.make_inputs(w, lengths=LENS)
+    else:
+        w = synthetic.small(W["gla_k256_v512_bf16"], K=128, V=256, H=2, dtype="f16", T=300)
+        x = synthetic.make_inputs(w)
+    o, ht = run_gpu(x, force_path=2)
+    assert o.dtype == torch.float16
+    ro, rht = run_oracle(x)
+    eo, eh = rel_l2_masked(o, ro), rel_l2_masked(ht, rht)
+    assert eo <= TOL_BF16_OPERANDS and eh <= TOL_BF16_OPERANDS, (eo, eh)
+    xb = dict(x)
+    for name in ("q", "k", "v"):
+        xb[name] = x[name].to(torch.bfloat16)
+    ob, htb = run_gpu(xb, force_path=2)
+    assert torch.equal(ht, htb)
+    assert torch.equal(o, ob.to(torch.float16))
