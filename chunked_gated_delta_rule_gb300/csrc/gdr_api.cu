@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "gdr_internal.cuh"
+#include "gdr_launch.cuh"
 
 namespace gdr {
 

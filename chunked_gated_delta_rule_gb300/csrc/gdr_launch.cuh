@@ -1,0 +1,119 @@
+// gdr_launch.cuh -- host-side declarations shared by the runtime's
+// translation units: workspace layout, kernel ids, the launch recorder and
+// the launch functions of every kernel family (each defined in its own .cu
+// file).  Device code does not include this header, so editing it leaves
+// the kernels' sources untouched.
+#pragma once
+
+#include "gdr_internal.cuh"
+
+namespace gdr {
+
+// Byte layout of the workspace for one problem.
+struct WorkspaceLayout {
+    size_t off_tab, off_seq0, off_nchunks, off_order, off_G, off_W, off_U, off_hpre,
+        off_vnew, off_segM, off_segC, off_segH, off_segD, off_rec, total;
+    int64_t max_chunks;
+};
+
+// path 1: CUDA-core path (chunk table, G, W, U, h_pre, v_new, segments);
+// path 2: tensor-core path (chunk table and segment summaries only).
+WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int n_segments, int path);
+Workspace carve_workspace(void *base, const WorkspaceLayout &L, int n_segments);
+
+// Kernel ids reported through gdr_options.launch_ids.
+enum KernelId {
+    kKChunkTable = 0,
+    kKPrep = 1,
+    kKScanSerial = 2,
+    kKScanPre = 3,
+    kKCompose = 4,
+    kKScanSegOut = 5,
+    kKOutput = 6,
+    kKTcSerial = 7,
+    kKTcPre = 8,
+    kKTcSegOut = 9,
+    kKTcPrep = 10,
+    kKTcGlaSerial = 11,
+    kKTcGlaPre = 12,
+    kKTcGlaSegOut = 13,
+    kKComposeScalar = 14,
+    kKTcPreDual = 15,
+    kKBwdGram = 16,
+    kKBwdScan = 17,
+    kKBwdLk = 18,
+    kKBwdLocal = 19,
+    kKBwdPre = 20,
+    kKBwdSegOut = 21,
+    kKBwdMaps = 22,
+    kKConvertIn = 23,
+    kKConvertOut = 24,
+    kKNumIds
+};
+
+// Records caller-provided events around each launch (benchmark hook).
+struct LaunchRecorder {
+    cudaEvent_t *events = nullptr;
+    int max_launches = 0;
+    int32_t *ids = nullptr;
+    int count = 0;
+    cudaStream_t st = nullptr;
+    cudaError_t begin(int id) {
+        if (ids && count < max_launches) ids[count] = id;
+        if (events && count < max_launches) return cudaEventRecord(events[2 * count], st);
+        return cudaSuccess;
+    }
+    cudaError_t end() {
+        cudaError_t e = cudaSuccess;
+        if (events && count < max_launches) e = cudaEventRecord(events[2 * count + 1], st);
+        ++count;
+        return e;
+    }
+};
+
+// ---- CUDA-core FP32 path (any supported shape; arithmetic in FP32) --------
+cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool check,
+                             cudaStream_t st);
+cudaError_t simt_prep(const Problem &p, const Workspace &ws, cudaStream_t st);
+// mode 0: serial scan (h0 -> ht), stores hpre / vnew
+// mode 1: segment pre-scan (zero / identity start), stores segC / segM / segD
+// mode 2: segment output pass (start from segH), stores hpre / vnew
+cudaError_t simt_scan(const Problem &p, const Workspace &ws, int mode, int bv,
+                      cudaStream_t st);
+cudaError_t simt_compose(const Problem &p, const Workspace &ws, int bv,
+                         cudaStream_t st);
+cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st);
+// FP16 <-> BF16 element copies (n elements), for FP16 inputs on the
+// tensor-core path.
+cudaError_t convert_f16_to_bf16(const void *src, void *dst, int64_t n, cudaStream_t st);
+cudaError_t convert_bf16_to_f16(const void *src, void *dst, int64_t n, cudaStream_t st);
+// Backward pass after the serial forward recompute (G, W, hpre, vnew in ws).
+cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
+                     cudaStream_t st, LaunchRecorder &rec);
+// Composition for the delta rule with K <= 128 and V % 32 == 0 (both paths):
+// bulk-copied transposed transitions, 32 value columns per CTA.
+bool compose_mt_supported(const Problem &p);
+cudaError_t compose_mt(const Problem &p, const Workspace &ws, cudaStream_t st);
+// A9 for the beta-free form (scalar transitions d_s).
+cudaError_t compose_scalar(const Problem &p, const Workspace &ws, cudaStream_t st);
+
+// ---- tensor-core path (BF16, K = V = 128, delta rule) ---------------------
+// Shapes and pointer alignment the tensor-core kernels take.
+bool tc_supported(const Problem &p);
+// Beta-free mode on tensor cores (BF16, K in {128, 256}, V % 128 == 0).
+bool tc_gla_supported(const Problem &p);
+cudaError_t tc_gla(const Problem &p, const Workspace &ws, int mode, cudaStream_t st);
+// A2-A5 for every (chunk, head) in parallel -> per-chunk records.
+cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st);
+// mode 0: serial scan + output (h0 -> ht); 1: segment pre-scan (c_s and M_s
+// chains); 2: segment output pass from the composed segment states.
+cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream_t st);
+// The per-token recurrence from (and back into) rows of a state pool.
+cudaError_t recurrent_fwd(const Problem &p, float *state, int64_t n_states,
+                          const int32_t *state_idx, cudaStream_t st);
+// Segment pre-scan with both summaries (c_s and M_s) of a chain in one CTA.
+// tc_chain's mode 1 runs them as separate chains, which is faster while both
+// kinds fit one wave (prescan_split_kinds).
+cudaError_t tc_prescan(const Problem &p, const Workspace &ws, cudaStream_t st);
+
+}  // namespace gdr

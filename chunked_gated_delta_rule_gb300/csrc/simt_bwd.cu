@@ -41,6 +41,7 @@
 // Every output element is summed by one thread in a fixed order, so results
 // are bit-identical from run to run.
 #include "gdr_internal.cuh"
+#include "gdr_launch.cuh"
 #include "simt_tile.cuh"
 
 namespace gdr {
