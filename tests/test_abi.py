@@ -173,8 +173,23 @@ def test_plan_query_is_deterministic_and_valid():
         assert pkg.gdr_plan_query(B, T, H, K, V, beta_free=bf)["n_segments"] == s
 
 
+def test_cuda_core_plan_rules():
+    """The CUDA-core plan (FP32 inputs): 32-column value tiles, 16 when the
+    sequences are too short to split and 32-column tiles leave SMs without a
+    chain; up to 64 segments for a long sequence with few heads (the
+    measurements behind each rule are stated beside pick_bv and
+    auto_segments)."""
+    q = lambda *a, **k: pkg.gdr_plan_query(*a, dtype=0, **k)
+    assert q(1, 256, 2, 64, 64) == {"path": 1, "bv": 16, "n_segments": 1}
+    assert q(1, 10456, 16, 128, 128, N=32) == {"path": 1, "bv": 32, "n_segments": 1}
+    assert q(1, 16384, 16, 128, 128) == {"path": 1, "bv": 32, "n_segments": 8}
+    assert q(1, 65536, 1, 128, 128) == {"path": 1, "bv": 32, "n_segments": 64}
+    assert q(2, 8192, 4, 256, 512, beta_free=True) == {"path": 1, "bv": 32, "n_segments": 4}
+
+
 def test_fp16_inputs_plan_the_cuda_core_path():
-    """The tensor-core kernels take BF16: FP16 (dtype 2) goes to path 1."""
+    """FP16 (dtype 2) goes to path 1 by default (FP32 arithmetic); the
+    tensor-core kernels take it only when forced, on BF16 copies."""
     plan = pkg.gdr_plan_query(1, 1000, 16, 128, 128, N=4, dtype=api.GDR_F16)
     assert plan["path"] == 1
     assert pkg.gdr_workspace_size(1, 1000, 16, 128, 128, N=4, dtype=api.GDR_F16) > 0
