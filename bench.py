@@ -296,9 +296,9 @@ def traffic_record(kernel, workload):
     return None
 
 
-def source_hash(kernel):
-    """sha256 (16 hex digits) of the kernel's .cu file and of every header it
-    includes, directly or through other headers of the package."""
+def kernel_sources(kernel):
+    """The kernel's .cu file and every package header it includes, directly
+    or through other headers (file names, the .cu file first)."""
     import re
     csrc = os.path.join(ROOT, "chunked_gated_delta_rule_gb300", "csrc")
     main = next((v for k, v in KERNEL_SOURCES.items() if kernel.startswith(k)), None)
@@ -311,10 +311,15 @@ def source_hash(kernel):
             continue
         seen.add(f)
         order.append(f)
-        text = open(os.path.join(csrc, f)).read()
-        todo += re.findall(r'#include\s+"([^"]+)"', text)
+        todo += re.findall(r'#include\s+"([^"]+)"', open(os.path.join(csrc, f)).read())
+    return [order[0]] + sorted(order[1:])
+
+
+def source_hash(kernel):
+    """sha256 (16 hex digits) of kernel_sources(kernel)."""
+    csrc = os.path.join(ROOT, "chunked_gated_delta_rule_gb300", "csrc")
     h = hashlib.sha256()
-    for f in [order[0]] + sorted(order[1:]):
+    for f in kernel_sources(kernel):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
