@@ -12,7 +12,9 @@ The pins stand on the forward oracle (itself pinned in
   <do, o> + <dht, ht> = <dv, v> + <dh0, h0>; o is linear in q and ht does not
   depend on it, so <do, o> = <dq, q>;
 * an empty sequence passes the final-state gradient straight through
-  (dh0 = dht); varlen equals independent per-sequence runs.
+  (dh0 = dht); varlen equals independent per-sequence runs;
+* the closed form of the scalar case (K = V = 1, two tokens), derived by
+  the chain rule on the explicit composition of the two steps.
 
 Planted mistakes in copies of the C source (a dropped term, a wrong sign, a
 state read one token off, a missing decay factor) must each fail one pin.
@@ -68,10 +70,70 @@ def _cases(rng):
     return out
 
 
+def scalar_two_token_grads(q, k, v, g, b, s0, do, dht, scale, delta=True):
+    """Gradients of L = do1 o1 + do2 o2 + dht h2 for K = V = 1 and two
+    tokens, by the chain rule on the explicit composition
+        h1 = a1 s0 (1 - b1 k1^2) + b1 k1 v1,  h2 = a2 h1 (1 - b2 k2^2) + b2 k2 v2
+    (beta-free: h_t = a_t h_{t-1} + k_t v_t), o_t = scale q_t h_t.
+    Returns dq, dk, dv, dg, dbeta (arrays of 2) and ds0."""
+    a = np.exp(g)
+    if not delta:
+        b = np.zeros(2)
+    p = 1 - b * k * k if delta else np.ones(2)       # the transition factor
+    w = b * k * v if delta else k * v                # the write
+    h1 = a[0] * s0 * p[0] + w[0]
+    h2 = a[1] * h1 * p[1] + w[1]
+    D2 = scale * q[1] * do[1] + dht                  # dL/dh2
+    D1 = scale * q[0] * do[0] + D2 * a[1] * p[1]     # dL/dh1
+    hp = np.array([s0, h1])                          # state before each token
+    D = np.array([D1, D2])
+    dq = scale * np.array([h1, h2]) * do
+    dg = D * a * hp * p
+    if delta:
+        dk = D * (a * hp * (-2 * b * k) + b * v)
+        dv = D * b * k
+        db = D * (-a * hp * k * k + k * v)
+    else:
+        dk = D * v
+        dv = D * k
+        db = None
+    ds0 = D1 * a[0] * p[0]
+    return dq, dk, dv, dg, db, ds0
+
+
+def scalar_closed_form_errors(lib, rng):
+    """Largest relative gap between the oracle and the scalar closed form
+    over a few random cases, delta rule and beta-free."""
+    worst = 0.0
+    for delta in (True, False):
+        for _ in range(4):
+            q, k, v = rng.standard_normal(2), rng.standard_normal(2), rng.standard_normal(2)
+            g = -np.abs(rng.standard_normal(2))
+            b = 1 / (1 + np.exp(-rng.standard_normal(2)))
+            s0, dht = rng.standard_normal(), rng.standard_normal()
+            do = rng.standard_normal(2)
+            scale = 0.7
+            ref = scalar_two_token_grads(q, k, v, g, b, s0, do, dht, scale, delta)
+            out = oracle.backward(q.reshape(1, 2, 1, 1), k.reshape(1, 2, 1, 1),
+                                  v.reshape(1, 2, 1, 1), g.reshape(1, 2, 1),
+                                  b.reshape(1, 2, 1) if delta else None,
+                                  h0=np.array(s0).reshape(1, 1, 1, 1), do=do.reshape(1, 2, 1, 1),
+                                  dht=np.array(dht).reshape(1, 1, 1, 1), scale=scale, lib=lib)
+            for got, want in zip(out, ref):
+                if want is None:
+                    continue
+                got = np.asarray(got).reshape(-1)
+                want = np.asarray(want).reshape(-1)
+                worst = max(worst, float(np.max(np.abs(got - want) / (np.abs(want) + 1e-12))))
+    return worst
+
+
 def bwd_battery(lib) -> list:
     """Runs the backward pins against ``lib``; returns the names that failed."""
     failed = []
     rng = np.random.default_rng(1)
+    if not scalar_closed_form_errors(lib, rng) < 1e-12:
+        failed.append("scalar_two_token_closed_form")
     for ci, (args, cu, do, dht) in enumerate(_cases(rng)):
         for name, err in fd_errors(lib, args, cu, do, dht, rng).items():
             if not err < 1e-6:
@@ -108,6 +170,12 @@ def bwd_battery(lib) -> list:
 
 def test_backward_pins_hold():
     assert bwd_battery(None) == []
+
+
+def test_scalar_two_token_closed_form():
+    """K = V = 1, two tokens: the oracle's gradients equal the hand-derived
+    chain rule of the explicit composition, delta rule and beta-free."""
+    assert scalar_closed_form_errors(None, np.random.default_rng(11)) < 1e-12
 
 
 def test_finite_differences_are_tight():
