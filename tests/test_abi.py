@@ -211,3 +211,24 @@ def test_workspace_size_scales_with_problem():
     gla = pkg.gdr_workspace_size(1, 16384, 16, 128, 128, beta_free=True, n_segments=1)
     assert gla > 0
     assert pkg.gdr_workspace_size(1, 256, 2, 60, 64) == 0  # unsupported -> 0
+
+
+def test_binding_rejects_misuse_before_calling_the_library(lib):
+    """The Python binding checks devices, dtypes and shapes before any CUDA
+    call: host tensors to the device entry points, mixed input dtypes, a
+    do of the wrong shape."""
+    import torch
+    q = torch.zeros(1, 64, 2, 64, dtype=torch.bfloat16)
+    g = torch.zeros(1, 64, 2)
+    with pytest.raises(ValueError):
+        pkg.gdr_chunk_fwd(q, q, q, g)
+    with pytest.raises(ValueError):
+        pkg.gdr_chunk_bwd(q, q, q, g, None, q)
+    with pytest.raises(ValueError):
+        pkg.chunk_gated_delta_rule(q, q, q, g)
+    with pytest.raises(TypeError):  # k in another dtype than q
+        pkg.gdr_chunk_fwd_host(q, q.float(), q, g)
+    with pytest.raises(TypeError):  # g must be float32
+        pkg.gdr_chunk_fwd_host(q, q, q, g.double())
+    with pytest.raises(ValueError):  # host entry wants host tensors; meta is not one
+        pkg.gdr_chunk_fwd_host(q.to("meta"), q, q, g)
