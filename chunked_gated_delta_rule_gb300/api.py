@@ -1,9 +1,9 @@
 """ctypes binding of ``include/gdr.h``: argument marshalling only.
 
 Every step of the forward and backward passes runs in the CUDA library; these
-functions pass
-tensor pointers, sizes and the current CUDA stream across the C ABI.  If the
-library has not been built (``__graft_entry__.build()``), every call raises.
+functions pass tensor pointers, sizes and the current CUDA stream across the
+C ABI.  If the library has not been built (``__graft_entry__.build()``),
+every call raises.
 """
 from __future__ import annotations
 
