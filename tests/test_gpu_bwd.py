@@ -195,3 +195,16 @@ def test_long_single_sequence_split_matches_oracle():
     for), automatic plan, against the oracle."""
     w = synthetic.small(W["stress_64k_h1_bf16"], T=4096)
     check(synthetic.make_inputs(w))
+
+
+@pytest.mark.parametrize("combo", ["vk_layout", "int64_seqlens", "f16"])
+def test_split_with_layout_and_dtype_options(combo):
+    """The segment split combined with the transposed state layout (dht in,
+    dh0 out through the reverse composition), int64 cu_seqlens and FP16
+    inputs."""
+    dtype = "f16" if combo == "f16" else "bf16"
+    w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True, dtype=dtype)
+    x = synthetic.make_inputs(w, lengths=[700, 65, 1, 300])
+    if combo == "int64_seqlens":
+        x = dict(x, cu_seqlens=x["cu_seqlens"].to(torch.int64))
+    check(x, layout="vk" if combo == "vk_layout" else "kv", n_segments=4)

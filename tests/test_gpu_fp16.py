@@ -69,7 +69,10 @@ def test_tensor_core_path_on_fp16_inputs(case):
         x = synthetic.make_inputs(w)
     o, ht = run_gpu(x, force_path=2)
     assert o.dtype == torch.float16
+    o2, ht2 = run_gpu(x, force_path=2, n_segments=2)  # the split on the same copies
     ro, rht = run_oracle(x)
+    assert rel_l2_masked(o2, ro) <= TOL_BF16_OPERANDS
+    assert rel_l2_masked(ht2, rht) <= TOL_BF16_OPERANDS
     eo, eh = rel_l2_masked(o, ro), rel_l2_masked(ht, rht)
     assert eo <= TOL_BF16_OPERANDS and eh <= TOL_BF16_OPERANDS, (eo, eh)
     xb = dict(x)
