@@ -93,3 +93,34 @@ def test_traffic_records_follow_each_kernels_includes():
             kernels.add(f["kernel"])
             assert float(f["dram_bytes_per_launch"]) >= 0
     assert {"tc_prep", "tc_chain_serial", "bwd_local", "recurrent"} <= kernels
+
+
+def test_measured_traffic_stays_near_the_algorithmic_bytes():
+    """Every committed DRAM record is within 1.25x of the kernel's
+    algorithmic bytes for its workload (no kernel re-reads its operands
+    wholesale); values below 1 are writes still in L2 when the launch ends."""
+    import chunked_gated_delta_rule_gb300 as pkg
+    from chunked_gated_delta_rule_gb300 import synthetic
+    b = _bench()
+    cache = {}
+    checked = 0
+    for line in open(os.path.join(ROOT, "profiles", "ncu_traffic.txt")):
+        if not line.startswith("kernel="):
+            continue
+        f = dict(kv.split("=", 1) for kv in line.split())
+        k, w, t = f["kernel"], f["workload"], float(f["dram_bytes_per_launch"])
+        if w not in cache:
+            x = synthetic.make_inputs(synthetic.WORKLOADS[w])
+            plan = pkg.gdr_plan_query(x["B"], x["T"], x["H"], x["K"], x["V"],
+                                      N=x["N"] if x["cu_seqlens"] is not None else 0,
+                                      dtype={"f32": 0, "bf16": 1, "f16": 2}[x["dtype"]],
+                                      beta_free=x["beta"] is None)
+            cache[w] = (x, b.counts(x, plan["n_segments"]))
+        x, c = cache[w]
+        a = b.bwd_algorithmic(k, x, b.counts(x, 1))[0] if k.startswith("bwd_") else \
+            b.algorithmic_bytes(k, x, c)
+        if not a or a < (1 << 20):
+            continue
+        assert t <= 1.25 * a, (k, w, t / a)
+        checked += 1
+    assert checked >= 20
