@@ -23,7 +23,10 @@ GDR_F32, GDR_BF16, GDR_F16 = 0, 1, 2
 class gdr_dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
                 ("K", ctypes.c_int64), ("V", ctypes.c_int64), ("N", ctypes.c_int64),
-                ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("max_len", ctypes.c_int64),
+                ("q_stride", ctypes.c_int64 * 2), ("k_stride", ctypes.c_int64 * 2),
+                ("v_stride", ctypes.c_int64 * 2), ("o_stride", ctypes.c_int64 * 2)]
 
 
 class gdr_plan(ctypes.Structure):
@@ -36,7 +39,8 @@ class gdr_options(ctypes.Structure):
                 ("force_bv", ctypes.c_int32), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t), ("status", ctypes.c_void_p),
                 ("events", ctypes.c_void_p), ("max_launches", ctypes.c_int32),
-                ("launch_ids", ctypes.c_void_p), ("n_launches", ctypes.c_void_p)]
+                ("launch_ids", ctypes.c_void_p), ("n_launches", ctypes.c_void_p),
+                ("grid_limit", ctypes.c_int32)]
 
 
 # Diagnostic entry points declared in include/gdr_selftest.h.
@@ -136,17 +140,33 @@ GDR_SEQLENS_I64 = 1  # gdr_dims.flags: cu_seqlens holds int64 offsets
 GDR_STATE_VK = 2     # gdr_dims.flags: h0 / ht / state pool are S [.., V, K]
 
 
-def make_dims(B, T, H, K, V, N=0, dtype=GDR_BF16, flags=0) -> gdr_dims:
-    return gdr_dims(B, T, H, K, V, N, dtype, flags)
+def make_dims(B, T, H, K, V, N=0, dtype=GDR_BF16, flags=0, max_len=0) -> gdr_dims:
+    return gdr_dims(B, T, H, K, V, N, dtype, flags, max_len)
 
 
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _dims_of(q, v, cu_seqlens, state_layout="kv") -> gdr_dims:
+def _row_strides(t):
+    """(token, head) element strides of a [B, T, H, D] tensor, or (0, 0)
+    when it is contiguous.  The last dimension must be contiguous and B, T
+    must flatten into one token dimension."""
+    if t.is_contiguous():
+        return (0, 0)
+    B, T = t.shape[0], t.shape[1]
+    if t.stride(-1) != 1 or (B > 1 and t.stride(0) != T * t.stride(1)):
+        raise ValueError("q, k, v and o need a contiguous last dimension and batch rows "
+                         "T token strides apart")
+    return (t.stride(1), t.stride(2))
+
+
+def _dims_of(q, v, cu_seqlens, state_layout="kv", max_seqlen=None, k=None, o=None) -> gdr_dims:
     """Sizes and flags: int64 cu_seqlens sets GDR_SEQLENS_I64; state_layout
-    "vk" (states as S, [.., V, K]) sets GDR_STATE_VK."""
+    "vk" (states as S, [.., V, K]) sets GDR_STATE_VK; ``max_seqlen`` (the
+    longest sequence's token count, a planning hint; None = unknown) goes
+    to gdr_dims.max_len; the token / head strides of q, k, v, o (views of a
+    larger tensor) go to the stride fields."""
     B, T, H, K = q.shape
     V = v.shape[-1]
     N = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
@@ -154,7 +174,12 @@ def _dims_of(q, v, cu_seqlens, state_layout="kv") -> gdr_dims:
         raise ValueError(f"state_layout must be 'kv' or 'vk', got {state_layout!r}")
     flags = (GDR_SEQLENS_I64 if cu_seqlens is not None and cu_seqlens.dtype == torch.int64
              else 0) | (GDR_STATE_VK if state_layout == "vk" else 0)
-    return make_dims(B, T, H, K, V, N, _dtype_code(q.dtype), flags)
+    dims = make_dims(B, T, H, K, V, N, _dtype_code(q.dtype), flags,
+                     0 if max_seqlen is None else int(max_seqlen))
+    for name, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", o)):
+        if t is not None:
+            getattr(dims, name)[:] = _row_strides(t)
+    return dims
 
 
 def _state_dims(dims, state_layout):
@@ -167,10 +192,15 @@ def _check_cu(t, device=None):
     _check("cu_seqlens", t, None, device)
 
 
-def _check(name, t, dtype, device=None):
+def _check(name, t, dtype, device=None, strided=False):
+    """dtype / device checks; contiguous unless ``strided`` (q, k, v, o of
+    the device entry points, whose token and head strides go to the
+    library)."""
     if t is None:
         return
-    if not t.is_contiguous():
+    if strided:
+        _row_strides(t)
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -208,38 +238,42 @@ class LaunchTimer:
 
 
 def gdr_chunk_fwd(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments=0,
-                  state_layout="kv",
+                  state_layout="kv", max_seqlen=None,
                   output_final_state=True, o=None, ht=None, scale=0.0, force_path=0,
-                  force_bv=0, workspace=None, status=None, stream=None, timer=None):
+                  force_bv=0, workspace=None, status=None, stream=None, timer=None,
+                  grid_limit=0):
     """Forward pass on CUDA tensors (layouts of include/gdr.h).  Returns
     ``(o, ht)``; ``ht`` is None unless ``output_final_state``.  Work is
     enqueued on ``stream`` (default: torch's current stream) and not
-    synchronised.  ``timer`` (a :class:`LaunchTimer`) records events around
-    every kernel launch."""
+    synchronised.  ``max_seqlen`` is the longest sequence's token count when
+    the caller knows it (a planning hint: cu_seqlens stays on the device).
+    ``timer`` (a :class:`LaunchTimer`) records events around every kernel
+    launch; ``grid_limit`` caps the CTAs of the persistent kernels."""
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("gdr_chunk_fwd takes CUDA tensors; use gdr_chunk_fwd_host for host buffers")
-    _check("q", q, None, dev)
+    _check("q", q, None, dev, strided=True)
     for name, t in (("k", k), ("v", v)):
-        _check(name, t, q.dtype, dev)
+        _check(name, t, q.dtype, dev, strided=True)
     _check("g", g, torch.float32, dev)
     _check("beta", beta, torch.float32, dev)
     _check_cu(cu_seqlens, dev)
     _check("h0", h0, torch.float32, dev)
-    dims = _dims_of(q, v, cu_seqlens, state_layout)
-    nseq = dims.N if dims.N else dims.B
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _check("o", o, q.dtype, dev, strided=True)
+    dims = _dims_of(q, v, cu_seqlens, state_layout, max_seqlen, k=k, o=o)
+    nseq = dims.N if dims.N else dims.B
     if ht is None and output_final_state:
         ht = torch.empty(nseq, dims.H, *_state_dims(dims, state_layout), dtype=torch.float32,
                          device=dev)
-    _check("o", o, q.dtype, dev)
     _check("ht", ht, torch.float32, dev)
     opt = gdr_options(float(scale), int(force_path), int(force_bv),
                       None if workspace is None else workspace.data_ptr(),
                       0 if workspace is None else workspace.numel() * workspace.element_size(),
                       None if status is None else status.data_ptr())
+    opt.grid_limit = int(grid_limit)
     if timer is not None:
         opt.events = ctypes.cast(timer._handles, ctypes.c_void_p)
         opt.max_launches = timer.max
@@ -270,9 +304,10 @@ def gdr_chunk_bwd(q, k, v, g, beta, do, cu_seqlens=None, h0=None, dht=None, *, n
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("gdr_chunk_bwd takes CUDA tensors")
-    _check("q", q, None, dev)
-    for name, t in (("k", k), ("v", v), ("do", do)):
-        _check(name, t, q.dtype, dev)
+    _check("q", q, None, dev, strided=True)
+    for name, t in (("k", k), ("v", v)):
+        _check(name, t, q.dtype, dev, strided=True)
+    _check("do", do, q.dtype, dev)
     if do.shape != v.shape:
         raise ValueError("do must have v's shape")
     _check("g", g, torch.float32, dev)
@@ -280,7 +315,7 @@ def gdr_chunk_bwd(q, k, v, g, beta, do, cu_seqlens=None, h0=None, dht=None, *, n
     _check_cu(cu_seqlens, dev)
     _check("h0", h0, torch.float32, dev)
     _check("dht", dht, torch.float32, dev)
-    dims = _dims_of(q, v, cu_seqlens, state_layout)
+    dims = _dims_of(q, v, cu_seqlens, state_layout, k=k)
     nseq = dims.N if dims.N else dims.B
     dq = torch.empty(q.shape, dtype=q.dtype, device=dev) if dq is None else dq
     dk = torch.empty(k.shape, dtype=q.dtype, device=dev) if dk is None else dk
@@ -336,18 +371,18 @@ def gdr_recurrent_fwd(q, k, v, g, beta=None, cu_seqlens=None, *, state, state_in
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("gdr_recurrent_fwd takes CUDA tensors")
-    _check("q", q, None, dev)
+    _check("q", q, None, dev, strided=True)
     for name, t in (("k", k), ("v", v)):
-        _check(name, t, q.dtype, dev)
+        _check(name, t, q.dtype, dev, strided=True)
     _check("g", g, torch.float32, dev)
     _check("beta", beta, torch.float32, dev)
     _check_cu(cu_seqlens, dev)
     _check("state", state, torch.float32, dev)
     _check("state_indices", state_indices, torch.int32, dev)
-    dims = _dims_of(q, v, cu_seqlens, state_layout)
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    _check("o", o, q.dtype, dev)
+    _check("o", o, q.dtype, dev, strided=True)
+    dims = _dims_of(q, v, cu_seqlens, state_layout, k=k, o=o)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     with torch.cuda.device(dev):
@@ -397,7 +432,7 @@ NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def gdr_chunk_fwd_noalloc(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments=0,
-                          state_layout="kv",
+                          state_layout="kv", max_seqlen=None,
                           output_final_state=True, o=None, ht=None, stream=None):
     """Forward pass through ``gdr_chunk_fwd_noalloc``: the library uses a
     fixed 64 MiB device array as scratch and allocates nothing, for callers
@@ -410,21 +445,21 @@ def gdr_chunk_fwd_noalloc(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("gdr_chunk_fwd_noalloc takes CUDA tensors")
-    _check("q", q, None, dev)
+    _check("q", q, None, dev, strided=True)
     for name, t in (("k", k), ("v", v)):
-        _check(name, t, q.dtype, dev)
+        _check(name, t, q.dtype, dev, strided=True)
     _check("g", g, torch.float32, dev)
     _check("beta", beta, torch.float32, dev)
     _check_cu(cu_seqlens, dev)
     _check("h0", h0, torch.float32, dev)
-    dims = _dims_of(q, v, cu_seqlens, state_layout)
-    nseq = dims.N if dims.N else dims.B
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _check("o", o, q.dtype, dev, strided=True)
+    dims = _dims_of(q, v, cu_seqlens, state_layout, max_seqlen, k=k, o=o)
+    nseq = dims.N if dims.N else dims.B
     if ht is None and output_final_state:
         ht = torch.empty(nseq, dims.H, *_state_dims(dims, state_layout), dtype=torch.float32,
                          device=dev)
-    _check("o", o, q.dtype, dev)
     _check("ht", ht, torch.float32, dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
@@ -437,14 +472,18 @@ def gdr_chunk_fwd_noalloc(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_
     return o, ht
 
 
-def gdr_workspace_size(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, n_segments=0) -> int:
+def gdr_workspace_size(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, n_segments=0,
+                       max_len=0) -> int:
     return int(load_library().gdr_workspace_size(
-        ctypes.byref(make_dims(B, T, H, K, V, N, dtype)), int(bool(beta_free)), int(n_segments)))
+        ctypes.byref(make_dims(B, T, H, K, V, N, dtype, max_len=max_len)), int(bool(beta_free)),
+        int(n_segments)))
 
 
-def gdr_plan_query(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, n_segments=0) -> dict:
+def gdr_plan_query(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, n_segments=0,
+                   max_len=0) -> dict:
     plan = gdr_plan()
-    rc = load_library().gdr_plan_query(ctypes.byref(make_dims(B, T, H, K, V, N, dtype)),
+    rc = load_library().gdr_plan_query(ctypes.byref(make_dims(B, T, H, K, V, N, dtype,
+                                                              max_len=max_len)),
                                        int(bool(beta_free)), int(n_segments), ctypes.byref(plan))
     if rc != 0:
         raise GdrError(rc)

@@ -44,9 +44,10 @@ def chunk_gated_delta_rule(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g:
                            ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """o, final_state of the chunked gated delta rule, differentiable with
     respect to q, k, v, g, beta and initial_state.  ``scale`` defaults to
-    1/sqrt(K).  ``final_state`` is None unless ``output_final_state``."""
-    return _ChunkGatedDeltaRule.apply(q.contiguous(), k.contiguous(), v.contiguous(),
-                                      g.contiguous(),
+    1/sqrt(K).  ``final_state`` is None unless ``output_final_state``.  q, k
+    and v may be views with token and head strides (e.g. slices of one fused
+    projection); the library reads them in place."""
+    return _ChunkGatedDeltaRule.apply(q, k, v, g.contiguous(),
                                       None if beta is None else beta.contiguous(),
                                       0.0 if scale is None else float(scale),
                                       None if initial_state is None else initial_state.contiguous(),

@@ -209,9 +209,7 @@ bool compose_mt_supported(const Problem &p) {
 // The narrowest value tile (4, 8, 16 columns) whose CTAs still fit one wave:
 // a step's time is one CTA's share of the K x K x CC products.
 cudaError_t compose_mt(const Problem &p, const Workspace &ws, cudaStream_t st) {
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t sms = device_sms();
     const int64_t heads = p.N * p.H;
     if ((p.V / 4) * heads <= sms) return launch_compose<4>(p, ws, st);
     if (p.V % 16 == 0 && (p.V / 8) * heads > sms) return launch_compose<16>(p, ws, st);

@@ -14,7 +14,6 @@ namespace gdr {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kNumSMs = 152;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -137,18 +136,78 @@ int64_t max_chunks_of(const gdr_dims &d) {
     return d.B * ((d.T + kChunk - 1) / kChunk);
 }
 
+// The token / head strides of a tensor whose last dimension has D elements:
+// the caller's pair, or the contiguous one for {0, 0}.
+TokStride stride_of(const int64_t (&s)[2], int64_t H, int64_t D) {
+    if (s[0] == 0 && s[1] == 0) return dense_stride(H, D);
+    return TokStride{s[0], s[1]};
+}
+
+bool has_strides(const gdr_dims &d) {
+    for (const int64_t *s : {d.q_stride, d.k_stride, d.v_stride, d.o_stride})
+        if (s[0] || s[1]) return true;
+    return false;
+}
+
+// Both entries zero or both positive; o's rows must not overlap: the inner
+// of its two dimensions spaces rows at least V apart and the outer spans it.
+int validate_strides(const gdr_dims &d) {
+    for (const int64_t *s : {d.q_stride, d.k_stride, d.v_stride, d.o_stride})
+        if ((s[0] == 0) != (s[1] == 0) || s[0] < 0 || s[1] < 0) return GDR_ERR_INVALID;
+    const TokStride o = stride_of(d.o_stride, d.H, d.V);
+    const int64_t tokens = d.B * d.T;
+    bool ok;
+    if (d.H == 1) ok = tokens <= 1 || o.t >= d.V;
+    else if (tokens <= 1) ok = o.h >= d.V;
+    else if (o.h <= o.t) ok = o.h >= d.V && o.t >= d.H * o.h;  // heads inside tokens
+    else ok = o.t >= d.V && o.h >= tokens * o.t;                // tokens inside heads
+    return ok ? GDR_OK : GDR_ERR_INVALID;
+}
+
+// Fills the tensor strides of a problem from its dims.
+void set_strides(Problem &p, const gdr_dims &d) {
+    p.sq = stride_of(d.q_stride, d.H, d.K);
+    p.sk = stride_of(d.k_stride, d.H, d.K);
+    p.sv = stride_of(d.v_stride, d.H, d.V);
+    p.so = stride_of(d.o_stride, d.H, d.V);
+}
+
 int validate_dims(const gdr_dims *d) {
     if (!d) return GDR_ERR_INVALID;
     if (d->B < 1 || d->T < 0 || d->H < 1 || d->K < 1 || d->V < 1 || d->N < 0)
         return GDR_ERR_INVALID;
     if (d->dtype != GDR_F32 && d->dtype != GDR_BF16 && d->dtype != GDR_F16) return GDR_ERR_INVALID;
     if (d->flags & ~(GDR_SEQLENS_I64 | GDR_STATE_VK)) return GDR_ERR_INVALID;
+    if (d->max_len < 0) return GDR_ERR_INVALID;
+    if (validate_strides(*d) != GDR_OK) return GDR_ERR_INVALID;
     if (is_varlen(*d) && d->B != 1) return GDR_ERR_INVALID;
     if (d->K % 16 || d->V % 16) return GDR_ERR_UNSUPPORTED;
     if (d->K > kMaxK || d->V > kMaxV) return GDR_ERR_UNSUPPORTED;
     if (d->H > 65535) return GDR_ERR_UNSUPPORTED;
     if (d->B * d->T >= (int64_t)INT32_MAX) return GDR_ERR_UNSUPPORTED;
     return GDR_OK;
+}
+
+// Chunks of the longest sequence and the mean chunks per sequence.  Varlen:
+// the longest from the caller's max_len hint (clamped to T), else the mean;
+// dense: every sequence has T tokens.
+struct ChunkStats {
+    int64_t longest, mean, total;  // total = chunks of all sequences
+};
+
+ChunkStats chunk_stats(const gdr_dims &d) {
+    ChunkStats c{};
+    if (!is_varlen(d)) {
+        c.longest = c.mean = (d.T + kChunk - 1) / kChunk;
+        c.total = c.mean * d.B;
+        return c;
+    }
+    c.mean = d.N ? (d.T / d.N + kChunk - 1) / kChunk : 0;
+    const int64_t L = d.max_len > 0 ? std::min<int64_t>(d.max_len, d.T) : 0;
+    c.longest = L > 0 ? std::max<int64_t>(c.mean, (L + kChunk - 1) / kChunk) : c.mean;
+    // every sequence adds at most one partial chunk
+    c.total = std::max<int64_t>(c.longest, d.T / kChunk + (d.N + 1) / 2);
+    return c;
 }
 
 // Value columns per scan CTA, among the widths that divide both V and K (the
@@ -169,9 +228,8 @@ int pick_bv(const gdr_dims &d) {
     };
     if (fits(32)) {
         const int64_t chains = n_seqs(d) * d.H * (d.V / 32);
-        const int64_t cps = is_varlen(d) ? (d.N ? (d.T / d.N + kChunk - 1) / kChunk : 0)
-                                         : (d.T + kChunk - 1) / kChunk;
-        return (chains < kNumSMs && cps < 32 && fits(16)) ? 16 : 32;  // a split needs 32 chunks
+        const int64_t cps = chunk_stats(d).longest;
+        return (chains < device_sms() && cps < 32 && fits(16)) ? 16 : 32;  // a split needs 32 chunks
     }
     for (int bv : {16, 64})
         if (fits(bv)) return bv;
@@ -180,50 +238,70 @@ int pick_bv(const gdr_dims &d) {
 
 // Segment count when the caller passes 0.
 // Tensor-core path: a cost model fitted to GB300 timings of its kernels.  A
-// chain pass costs t microseconds per chunk and runs its chains in waves of
-// one per SM; a split runs a pre-scan pass (two chains per segment for the
-// delta rule: local state and transition), an ordered composition costing
-// t_step per segment, and an output pass.  The model reproduces the measured
-// best counts (16K x 16 heads: 8; 64K x 8 heads: 16; 64K x 1 head: 64;
-// beta-free K = 256, V = 512, 2 x 8K x 4 heads: 4; the wide varlen batch: 1).
+// chain pass costs t microseconds per chunk; its chains run one per SM,
+// longest first, so a pass lasts about t times the larger of the longest
+// chain and the chunk steps each SM takes (all chains' chunks over the SMs,
+// in whole waves when the chains are alike).  A split runs a pre-scan pass
+// (two summaries per segment for the delta rule: local state and
+// transition), an ordered composition costing t_step per segment, and an
+// output pass; every sequence is cut into at most S runs of whole chunks, so
+// the longest chain shrinks to ceil(longest / S) chunks while the work stays
+// the same.  The model reproduces the measured best counts (16K x 16 heads:
+// 8; 64K x 8 heads: 16; 64K x 1 head: 64; beta-free K = 256, V = 512,
+// 2 x 8K x 4 heads: 4; the wide varlen batch: 1), and splits a batch whose
+// longest sequence (the max_len hint) dwarfs the rest.
 // CUDA-core path: split until about two CTAs per SM, at most 64 segments,
-// while every segment keeps at least 8 chunks (one 64K-token head's
-// backward: 8.2 ms at 16 segments, 5.1 at 32, 3.8 at 64).
+// while every segment of the longest sequence keeps at least 8 chunks (one
+// 64K-token head's backward: 8.2 ms at 16 segments, 5.1 at 32, 3.8 at 64).
 // The delta pre-scan of `segs` (sequence, segment, head) chains runs each of
 // their two summaries as its own chain while all of them fit one wave.
-bool prescan_split_kinds(int64_t segs) { return 2 * segs <= kNumSMs; }
+bool prescan_split_kinds(int64_t segs) { return 2 * segs <= device_sms(); }
 
 int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     const int64_t nseq = n_seqs(d);
-    const int64_t cps = is_varlen(d) ? (d.N ? (d.T / d.N + kChunk - 1) / kChunk : 0)
-                                     : (d.T + kChunk - 1) / kChunk;
+    const ChunkStats cs = chunk_stats(d);
+    const int64_t cps = cs.longest;
+    const int64_t sms = device_sms();
     if (path != 2) {
         const int64_t chains = nseq * d.H * (d.V / bv);
         int S = 1;
-        while (S < kMaxSegments && chains * S < 2 * kNumSMs && cps / (2 * S) >= 8) S *= 2;
+        while (S < kMaxSegments && chains * S < 2 * sms && cps / (2 * S) >= 8) S *= 2;
         return S;
     }
-    const int64_t chains = nseq * d.H * (beta_free ? d.V / 128 : 1);
-    auto waves = [](int64_t c) { return (double)((c + kNumSMs - 1) / kNumSMs); };
+    const int64_t tiles = beta_free ? d.V / 128 : 1;  // chains per (sequence, head)
+    const int64_t chains = nseq * d.H * tiles;
+    const double steps = (double)cs.total * (double)(d.H * tiles);  // chunk steps of a pass
+    auto waves = [&](int64_t c) { return (double)((c + sms - 1) / sms); };
+    // chunk steps one SM runs in a pass whose longest chain has `per` chunks
+    // and whose `n` chains are as long as their work allows
+    auto pass = [&](double per, int64_t n) {
+        const double uniform = per * waves(n);          // alike chains, in whole waves
+        const double spread = steps / (double)sms;      // a mix, packed longest first
+        return std::max(per, cs.longest == cs.mean ? uniform : std::max(spread, per));
+    };
     const double t_serial = beta_free ? 3.3 : 2.4, t_pre = beta_free ? 2.0 : 2.4,
                  t_out = beta_free ? 3.7 : 2.4;
-    // the delta pre-scan: one summary per CTA while both kinds fit one wave,
-    // else both summaries of a segment per CTA at 2.9 us per chunk
-    auto pre_time = [&](int64_t segs) {
-        if (beta_free) return t_pre * waves(segs);
-        return prescan_split_kinds(segs) ? t_pre : 2.9 * waves(segs);
-    };
     const double state_mb = (double)(nseq * d.H) * (double)(d.K * d.V) * 4.0 / (1 << 20);
     const int64_t heads = nseq * d.H;  // composition tile: 4, 8 or 16 value columns
+    // a delta composition step per wave of its CTAs (one value tile of one
+    // (sequence, head) each, one CTA per SM): a batch of many sequences pays
+    // it many times over (101 x 16 heads: 85 waves, 1.1 ms at 3 segments)
+    const int64_t cc = heads * (d.V / 4) <= sms ? 4 : heads * (d.V / 8) <= sms ? 8 : 16;
     const double t_step = beta_free ? (0.65 * state_mb > 0.5 ? 0.65 * state_mb : 0.5)
-                          : heads * (d.V / 4) <= kNumSMs ? 1.8
-                          : heads * (d.V / 8) <= kNumSMs ? 2.6 : 4.4;
-    double best = t_serial * (double)cps * waves(chains);
+                          : (cc == 4 ? 1.8 : cc == 8 ? 2.6 : 4.4) * waves(heads * (d.V / cc));
+    double best = t_serial * pass((double)cps, chains);
     int best_s = 1;
-    for (int S = 2; S <= kMaxSegments && S <= cps; S *= 2) {
-        const double per = (double)((cps + S - 1) / S);
-        const double est = per * (pre_time(chains * S) + t_out * waves(chains * S)) +
-                           t_step * S;
+    for (int S = 2; S <= kMaxSegments && S <= cps; ++S) {
+        const int64_t per = (cps + S - 1) / S;
+        if (S > 2 && (cps + S - 2) / (S - 1) == per) continue;  // same runs as S - 1
+        // segment chains: the longest sequence's S, the mean one's as many
+        // as its chunks allow
+        const int64_t segs = nseq * d.H * tiles * std::min<int64_t>(S, std::max<int64_t>(cs.mean, 1));
+        double pre;
+        if (beta_free) pre = t_pre * pass((double)per, segs);
+        else if (prescan_split_kinds(segs)) pre = t_pre * (double)per;
+        else pre = 2.9 * pass((double)per, segs);
+        const double est = pre + t_out * pass((double)per, segs) + t_step * S;
         if (est < best) {
             best = est;
             best_s = S;
@@ -273,6 +351,39 @@ int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_optio
 }
 
 }  // namespace
+
+// The plan a forward call runs and the scratch it needs: the shape's plan,
+// moved to the CUDA-core path when the tensor-core kernels cannot take the
+// pointers (16-byte aligned q, k, v, o), with that path's own value tile and
+// (for n_segments = 0) segment count.  Every forward entry point plans
+// through here, so a caller that sizes scratch in advance
+// (gdr_chunk_fwd_noalloc) sizes it for the path that will run.  FP16 inputs
+// forced onto the tensor cores run on aligned BF16 copies.
+int plan_for_call(const gdr_dims &d, bool beta_free, int n_segments, const gdr_options *opt,
+                  const void *q, const void *k, const void *v, const void *o, gdr_plan *plan,
+                  size_t *ws_bytes) {
+    gdr_plan p{};
+    int rc = validate_dims(&d);
+    if (rc != GDR_OK) return rc;
+    rc = make_plan(d, beta_free, n_segments, opt, &p);
+    if (rc != GDR_OK) return rc;
+    const bool copies = p.path == 2 && d.dtype == GDR_F16;
+    if (copies && has_strides(d)) return GDR_ERR_UNSUPPORTED;  // the copies are contiguous
+    const int es = d.dtype == GDR_F32 ? 4 : 2;
+    if (p.path == 2 && !copies &&
+        !(rows_aligned16(q, stride_of(d.q_stride, d.H, d.K), es) &&
+          rows_aligned16(k, stride_of(d.k_stride, d.H, d.K), es) &&
+          rows_aligned16(v, stride_of(d.v_stride, d.H, d.V), es) &&
+          rows_aligned16(o, stride_of(d.o_stride, d.H, d.V), es))) {
+        if (opt && opt->force_path == 2) return GDR_ERR_INVALID;  // misaligned pointers
+        p.path = 1;
+        p.bv = pick_bv(d);
+        if (n_segments == 0) p.n_segments = auto_segments(d, beta_free, 1, p.bv);
+    }
+    *plan = p;
+    if (ws_bytes) *ws_bytes = workspace_layout(d, beta_free, p.n_segments, p.path).total;
+    return GDR_OK;
+}
 
 WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int path) {
     const bool delta = !beta_free;
@@ -544,6 +655,7 @@ int gdr_recurrent_fwd(const gdr_dims *dims, const void *q, const void *k, const 
     p.state_vk = (dims->flags & GDR_STATE_VK) != 0;
     p.o = o;
     p.B = dims->B; p.T = dims->T; p.H = dims->H; p.K = dims->K; p.V = dims->V;
+    set_strides(p, *dims);
     p.N = n_seqs(*dims);
     p.dtype = dims->dtype;
     p.scale = 1.0f / std::sqrt((float)dims->K);
@@ -567,6 +679,7 @@ size_t gdr_workspace_size(const gdr_dims *dims, int beta_free, int n_segments) {
     return workspace_layout(*dims, beta_free != 0, plan.n_segments, plan.path).total;
 }
 
+
 int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const void *v,
                      const float *g, const float *beta, const int32_t *cu_seqlens,
                      const float *h0, void *o, float *ht, int n_segments,
@@ -576,10 +689,13 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
     if (!q || !k || !v || !g || !o) return GDR_ERR_INVALID;
     if ((cu_seqlens != nullptr) != is_varlen(*dims)) return GDR_ERR_INVALID;
     const bool beta_free = beta == nullptr;
-    gdr_plan plan;
-    rc = make_plan(*dims, beta_free, n_segments, opt, &plan);
-    if (rc != GDR_OK) return rc;
     if (opt && !(opt->scale >= 0.f)) return GDR_ERR_INVALID;  // rejects NaN too
+    if (opt && opt->grid_limit < 0) return GDR_ERR_INVALID;
+    gdr_plan plan;
+    size_t ws_need = 0;
+    rc = plan_for_call(*dims, beta_free, n_segments, opt, q, k, v, o, &plan, &ws_need);
+    if (rc != GDR_OK) return rc;
+    if (opt && opt->workspace && opt->workspace_bytes < ws_need) return GDR_ERR_WORKSPACE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Problem p{};
@@ -589,10 +705,12 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
     p.state_vk = (dims->flags & GDR_STATE_VK) != 0;
     p.h0 = h0; p.o = o; p.ht = ht;
     p.B = dims->B; p.T = dims->T; p.H = dims->H; p.K = dims->K; p.V = dims->V;
+    set_strides(p, *dims);
     p.N = n_seqs(*dims);
     p.dtype = dims->dtype;
     p.scale = (opt && opt->scale > 0.f) ? opt->scale : 1.0f / std::sqrt((float)dims->K);
     p.status = opt ? opt->status : nullptr;
+    p.grid_limit = opt ? opt->grid_limit : 0;
     if (p.N == 0) return GDR_OK;
     // FP16 inputs on the tensor-core path: the kernels read BF16 copies of q,
     // k, v and write o in BF16, converted back to FP16 after the pass
@@ -635,12 +753,9 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
         if (conv) cudaFreeAsync(conv, st);
         return code;
     };
-    const bool tc_ok = beta_free ? tc_gla_supported(p) : tc_supported(p);
-    if (plan.path == 2 && !tc_ok) {
-        if (opt && opt->force_path == 2) return fail(GDR_ERR_INVALID);  // misaligned pointers
-        plan.path = 1;
-        plan.bv = pick_bv(*dims);
-    }
+    // plan_for_call moved misaligned calls to the CUDA-core path already
+    if (plan.path == 2 && !(beta_free ? tc_gla_supported(p) : tc_supported(p)))
+        return fail(GDR_ERR_INVALID);
 
     const WorkspaceLayout L = workspace_layout(*dims, beta_free, plan.n_segments, plan.path);
     void *base = nullptr;
@@ -720,6 +835,7 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
     p.state_vk = (dims->flags & GDR_STATE_VK) != 0;
     p.h0 = h0;
     p.B = dims->B; p.T = dims->T; p.H = dims->H; p.K = dims->K; p.V = dims->V;
+    set_strides(p, *dims);
     p.N = n_seqs(*dims);
     p.dtype = dims->dtype;
     p.scale = (opt && opt->scale > 0.f) ? opt->scale : 1.0f / std::sqrt((float)dims->K);
@@ -764,6 +880,7 @@ int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k, const
                        gdr_stream_t stream) {
     int rc = validate_dims(dims);
     if (rc != GDR_OK) return rc;
+    if (has_strides(*dims)) return GDR_ERR_UNSUPPORTED;  // host buffers are copied whole
     if (!q || !k || !v || !g || !o) return GDR_ERR_INVALID;
     if ((cu_seqlens != nullptr) != is_varlen(*dims)) return GDR_ERR_INVALID;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -867,6 +984,8 @@ int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k, const
             gd.N = (int32_t)nn;
             gd.T = (int64_t)nt;
             gd.flags &= ~GDR_SEQLENS_I64;
+            gd.max_len = 0;  // the group's longest sequence, read from the host table
+            for (size_t n = n0; n < n0 + nn; ++n) gd.max_len = std::max(gd.max_len, cu[n + 1] - cu[n]);
         } else {
             gd.B = (int64_t)nn;
         }

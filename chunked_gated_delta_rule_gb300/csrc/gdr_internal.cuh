@@ -47,9 +47,18 @@ constexpr int kMaxK = 256;       // largest key dim supported
 constexpr int kMaxV = 1024;      // largest value dim supported
 constexpr int kMaxSegments = 64; // largest segment count
 
+// Element strides of the token and head dimensions of a [tokens, H, D]
+// tensor whose last dimension is contiguous (tokens flatten B and T).
+struct TokStride {
+    int64_t t, h;
+};
+__host__ __device__ __forceinline__ int64_t tok_at(const TokStride &s, int64_t t, int64_t h) {
+    return t * s.t + h * s.h;
+}
+
 // Everything a kernel needs to address the caller's tensors.
 struct Problem {
-    const void *q, *k, *v;      // [B,T,H,K] / [B,T,H,V], dtype
+    const void *q, *k, *v;      // [B,T,H,K] / [B,T,H,V], dtype (strides sq, sk, sv)
     const float *g, *beta;      // [B,T,H]; beta == nullptr => beta-free
     const int32_t *cu;          // [N+1] or nullptr (dense); int32 offsets
     const int64_t *cu64;        // the same table as int64 (GDR_SEQLENS_I64), or nullptr
@@ -61,7 +70,46 @@ struct Problem {
     float scale;
     int32_t *status;            // device status word or nullptr
     int state_vk;               // h0 / ht laid out [N,H,V,K] (S) instead of [N,H,K,V]
+    int grid_limit;             // > 0: at most this many CTAs per persistent kernel
+    TokStride sq, sk, sv, so;   // strides of q, k, v, o (contiguous: H*K, K / H*V, V)
 };
+
+// 16-byte vector loads of a [tokens, H, D] tensor: an aligned base and
+// strides that keep every row start aligned (es = element size in bytes).
+__host__ __device__ __forceinline__ bool rows_aligned16(const void *ptr, const TokStride &s,
+                                                        int es) {
+    return ((reinterpret_cast<uintptr_t>(ptr) | (uintptr_t)(s.t * es) | (uintptr_t)(s.h * es)) &
+            15u) == 0;
+}
+
+// Contiguous [tokens, H, D] strides.
+__host__ __device__ __forceinline__ TokStride dense_stride(int64_t H, int64_t D) {
+    return TokStride{H * D, D};
+}
+
+// Streaming multiprocessors of the current device (152 on GB300 when no
+// device can be queried: host-only plan lookups).
+inline int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();  // clear the sticky error of a failed query
+        return 152;
+    }
+    return sms;
+}
+
+// CTAs of a persistent kernel that pulls `items` work units: per_sm CTAs on
+// every SM, fewer when there are fewer units, and at most p.grid_limit when
+// that is set.  Results never depend on the grid: every unit is computed by
+// one CTA in a fixed order whichever CTA takes it.
+inline int64_t persistent_grid(const Problem &p, int64_t items, int per_sm) {
+    int64_t g = (int64_t)device_sms() * per_sm;
+    if (items < g) g = items;
+    if (p.grid_limit > 0 && g > p.grid_limit) g = p.grid_limit;
+    return g < 1 ? 1 : g;
+}
 
 // cu_seqlens[i] in either width; a sequence's first token and end.
 __host__ __device__ __forceinline__ int64_t seq_bound(const Problem &p, int64_t i) {

@@ -21,6 +21,13 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int n_segments, int path);
 Workspace carve_workspace(void *base, const WorkspaceLayout &L, int n_segments);
 
+// The plan a forward call runs (the shape's plan, on the CUDA-core path when
+// the tensor-core kernels cannot take the pointers) and its scratch bytes;
+// GDR_OK or the code the call itself would return for these arguments.
+int plan_for_call(const gdr_dims &d, bool beta_free, int n_segments, const gdr_options *opt,
+                  const void *q, const void *k, const void *v, const void *o, gdr_plan *plan,
+                  size_t *ws_bytes);
+
 // Kernel ids reported through gdr_options.launch_ids.
 enum KernelId {
     kKChunkTable = 0,

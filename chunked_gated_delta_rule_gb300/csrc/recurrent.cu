@@ -81,12 +81,12 @@ __global__ void __launch_bounds__(kRThreads, RPW <= 16 ? 4 : 2)
     for (int64_t t = t0; t < t1; ++t) {
         const int64_t th = t * H + h;
         for (int i = tid; i < K; i += kRThreads) {
-            sk[i] = ld_in<Tin>(p.k, th * K + i);
-            sq[i] = ld_in<Tin>(p.q, th * K + i);
+            sk[i] = ld_in<Tin>(p.k, tok_at(p.sk, t, h) + i);
+            sq[i] = ld_in<Tin>(p.q, tok_at(p.sq, t, h) + i);
         }
         if (tid < kRCols) {
             const int c = blockIdx.x * kRCols + tid;
-            sv[tid] = c < V ? ld_in<Tin>(p.v, th * V + c) : 0.f;
+            sv[tid] = c < V ? ld_in<Tin>(p.v, tok_at(p.sv, t, h) + c) : 0.f;
         }
         if (tid == 0) {
             sg[0] = __expf(p.g[th]);
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kRThreads, RPW <= 16 ? 4 : 2)
             float o = 0.f;
 #pragma unroll
             for (int w = 0; w < 8; ++w) o += sred[1][w][lane];
-            st_out<Tin>(p.o, th * V + col, p.scale * o);
+            st_out<Tin>(p.o, tok_at(p.so, t, h) + col, p.scale * o);
         }
         __syncthreads();  // sk, sq, sv, sred are refilled for the next token
     }

@@ -72,13 +72,14 @@ __device__ __forceinline__ ChunkInfo chunk_info(const Workspace &ws, int64_t gc)
     return ChunkInfo{(int64_t)e.y, e.z};
 }
 
-// True when every caller tensor the backward kernels read by rows (q, k, v,
-// dout) starts on a 16-byte boundary: rows are then 16-byte aligned too (K
-// and V are multiples of 16) and the tiles load in 16-byte pieces.
+// True when every caller tensor the backward kernels read by rows (q, k, v
+// with their strides, dout contiguous) has 16-byte aligned rows (K and V are
+// multiples of 16): the tiles then load in 16-byte pieces.
+template <typename T>
 __device__ __forceinline__ bool inputs_vec16(const Problem &p, const BwdArgs &a) {
-    const uintptr_t u = reinterpret_cast<uintptr_t>(p.q) | reinterpret_cast<uintptr_t>(p.k) |
-                        reinterpret_cast<uintptr_t>(p.v) | reinterpret_cast<uintptr_t>(a.dout);
-    return (u & 15) == 0;
+    const int es = (int)sizeof(T);
+    return rows_aligned16(p.q, p.sq, es) && rows_aligned16(p.k, p.sk, es) &&
+           rows_aligned16(p.v, p.sv, es) && rows_aligned16(a.dout, dense_stride(p.H, p.V), es);
 }
 
 // Rows [0, 64) x columns [c0, c0 + 64) of a token-major input [tokens][H][D]
@@ -87,7 +88,7 @@ __device__ __forceinline__ bool inputs_vec16(const Problem &p, const BwdArgs &a)
 // inside or outside the row).
 template <typename T>
 __device__ __forceinline__ void load_tok_tile(float *dst, const T *src, int64_t t0, int len,
-                                              int H, int h, int D, int c0, int tid,
+                                              const TokStride &st, int h, int D, int c0, int tid,
                                               bool vec = false) {
     if (vec) {
         constexpr int E = 16 / (int)sizeof(T);
@@ -97,7 +98,7 @@ __device__ __forceinline__ void load_tok_tile(float *dst, const T *src, int64_t 
             float x[E];
             if (i < len && c0 + c < D) {
                 const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-                    src + ((t0 + i) * H + h) * (int64_t)D + c0 + c));
+                    src + tok_at(st, t0 + i, h) + c0 + c));
                 unpack16(raw, src, x);
             } else {
 #pragma unroll
@@ -111,7 +112,7 @@ __device__ __forceinline__ void load_tok_tile(float *dst, const T *src, int64_t 
     for (int idx = tid; idx < kChunk * kSl; idx += kBT) {
         const int i = idx >> 6, c = idx & 63;
         float x = 0.f;
-        if (i < len && c0 + c < D) x = ldx(src, ((t0 + i) * H + h) * (int64_t)D + c0 + c);
+        if (i < len && c0 + c < D) x = ldx(src, tok_at(st, t0 + i, h) + c0 + c);
         dst[i * kLd + c] = x;
     }
 }
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_gram(Problem p, Workspace ws, BwdWs
         sG[tid] = ws.G[(gc * H + h) * kChunk + tid];
         sB[tid] = (delta && tid < ci.len) ? p.beta[(ci.t0 + tid) * H + h] : 0.f;
     }
-    const bool vec = ((reinterpret_cast<uintptr_t>(p.q) | reinterpret_cast<uintptr_t>(p.k)) & 15) == 0;
+    const bool vec = rows_aligned16(p.q, p.sq, sizeof(Tin)) && rows_aligned16(p.k, p.sk, sizeof(Tin));
     float qk[4][4], kk[4][4];
     acc_zero(qk);
     acc_zero(kk);
@@ -161,8 +162,8 @@ __global__ void __launch_bounds__(kBT) k_bwd_gram(Problem p, Workspace ws, BwdWs
     const Tin *k = static_cast<const Tin *>(p.k);
     for (int c0 = 0; c0 < K; c0 += kSl) {
         __syncthreads();
-        load_tok_tile(sQ, q, ci.t0, ci.len, H, h, K, c0, tid, vec);
-        load_tok_tile(sK, k, ci.t0, ci.len, H, h, K, c0, tid, vec);
+        load_tok_tile(sQ, q, ci.t0, ci.len, p.sq, h, K, c0, tid, vec);
+        load_tok_tile(sK, k, ci.t0, ci.len, p.sk, h, K, c0, tid, vec);
         __syncthreads();
         const int kn = min(kSl, K - c0);
         mm_abT<4>(qk, sQ, kLd, sK, kLd, kn, tid);
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
     const Tin *q = static_cast<const Tin *>(p.q);
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *dout = static_cast<const Tin *>(a.dout);
-    const bool vec = inputs_vec16(p, a);
+    const bool vec = inputs_vec16<Tin>(p, a);
     float dprod = 1.f;
     for (int cc = s1 - 1; cc >= s0; --cc) {
         const int64_t gc = c_begin + cc;
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
         acc_zero(acc);
         for (int k0 = 0; k0 < K; k0 += kSl) {
             __syncthreads();
-            load_tok_tile(sX, k, ci.t0, ci.len, H, h, K, k0, tid, vec);
+            load_tok_tile(sX, k, ci.t0, ci.len, p.sk, h, K, k0, tid, vec);
             __syncthreads();
             mm_ab<NS>(acc, sX, kLd, sE + k0 * LDE, LDE, min(kSl, K - k0), tid);
         }
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_dscan(Problem p, Workspace ws, BwdA
                 const int i = idx >> 6, c = idx & 63;
                 float x = 0.f;
                 if (i < ci.len && k0 + c < K)
-                    x = sGam[i] * ldx(q, ((ci.t0 + i) * H + h) * (int64_t)K + k0 + c);
+                    x = sGam[i] * ldx(q, tok_at(p.sq, ci.t0 + i, h) + k0 + c);
                 sX[i * kLd + c] = x;
             }
             if (delta)
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_lk(Problem p, Workspace ws, BwdArgs
     const Tin *v = static_cast<const Tin *>(p.v);
     const float *hg = ws.hpre + item * (int64_t)K * V;
     const float *eg = bw.dhend + item * (int64_t)K * V;
-    const bool vec = inputs_vec16(p, a);
+    const bool vec = inputs_vec16<Tin>(p, a);
     float p1[4][4], p2[4][4], p3[4][4];
     acc_zero(p1);
     acc_zero(p2);
@@ -437,12 +438,12 @@ __global__ void __launch_bounds__(kBT) k_bwd_lk(Problem p, Workspace ws, BwdArgs
     float eh = 0.f;
     for (int c0 = 0; c0 < V; c0 += kSl) {
         __syncthreads();
-        load_tok_tile(sDo, dout, ci.t0, ci.len, H, h, V, c0, tid, vec);
+        load_tok_tile(sDo, dout, ci.t0, ci.len, dense_stride(H, V), h, V, c0, tid, vec);
         if (delta) {
             load_mat_tile(sDv, bw.dvn + item * (int64_t)kChunk * V, 0, ci.len, c0, V, V, tid);
             load_mat_tile(sVn, ws.vnew + item * (int64_t)kChunk * V, 0, ci.len, c0, V, V, tid);
         } else {
-            load_tok_tile(sVn, v, ci.t0, ci.len, H, h, V, c0, tid, vec);
+            load_tok_tile(sVn, v, ci.t0, ci.len, p.sv, h, V, c0, tid, vec);
         }
         load_mat_tile(sH, hg, k0, K, c0, V, V, tid);
         load_mat_tile(sE, eg, k0, K, c0, V, V, tid);
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
     const Tin *dout = static_cast<const Tin *>(a.dout);
-    const bool v16 = inputs_vec16(p, a);
+    const bool v16 = inputs_vec16<Tin>(p, a);
 
     // value loop: dMraw = dO V'^T; delta: dTa = dV' V^T (times beta_j below)
     {
@@ -545,13 +546,13 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
         acc_zero(dt);
         for (int c0 = 0; c0 < V; c0 += kSl) {
             __syncthreads();
-            load_tok_tile(s1, dout, ci.t0, len, H, h, V, c0, tid, v16);
+            load_tok_tile(s1, dout, ci.t0, len, dense_stride(H, V), h, V, c0, tid, v16);
             if (delta) {
                 load_mat_tile(s2, ws.vnew + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
                 load_mat_tile(s3, bw.dvn + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
-                load_tok_tile(s4, v, ci.t0, len, H, h, V, c0, tid, v16);
+                load_tok_tile(s4, v, ci.t0, len, p.sv, h, V, c0, tid, v16);
             } else {
-                load_tok_tile(s2, v, ci.t0, len, H, h, V, c0, tid, v16);
+                load_tok_tile(s2, v, ci.t0, len, p.sv, h, V, c0, tid, v16);
             }
             __syncthreads();
             const int cn = min(kSl, V - c0);
@@ -587,7 +588,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
         for (int k0 = 0; k0 < K; k0 += kSl) {
             __syncthreads();
             load_mat_tile(s1, bw.P2 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
-            load_tok_tile(s2, k, ci.t0, len, H, h, K, k0, tid, v16);
+            load_tok_tile(s2, k, ci.t0, len, p.sk, h, K, k0, tid, v16);
             __syncthreads();
             mm_abT<4>(tb, s1, kLd, s2, kLd, min(kSl, K - k0), tid);
         }
@@ -639,8 +640,8 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
     Tin *dk = static_cast<Tin *>(a.dk);
     for (int k0 = 0; k0 < K; k0 += kSl) {
         __syncthreads();
-        load_tok_tile(s1, q, ci.t0, len, H, h, K, k0, tid, v16);
-        load_tok_tile(s2, k, ci.t0, len, H, h, K, k0, tid, v16);
+        load_tok_tile(s1, q, ci.t0, len, p.sq, h, K, k0, tid, v16);
+        load_tok_tile(s2, k, ci.t0, len, p.sk, h, K, k0, tid, v16);
         load_mat_tile(s3, bw.P1 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
         load_mat_tile(s4, bw.P3 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
         if (delta) load_mat_tile(s5, bw.P2 + item * (int64_t)kChunk * K, 0, kChunk, k0, K, K, tid);
@@ -693,7 +694,7 @@ __global__ void __launch_bounds__(kBT) k_bwd_local(Problem p, Workspace ws, BwdA
         for (int c0 = 0; c0 < V; c0 += kSl) {
             __syncthreads();
             load_mat_tile(s3, bw.dvn + item * (int64_t)kChunk * V, 0, len, c0, V, V, tid);
-            load_tok_tile(s4, v, ci.t0, len, H, h, V, c0, tid, v16);
+            load_tok_tile(s4, v, ci.t0, len, p.sv, h, V, c0, tid, v16);
             __syncthreads();
             const int cn = min(kSl, V - c0);
             float vb[4][4];

@@ -214,7 +214,7 @@ k_prep(Problem p, Workspace ws) {
 
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
-    const bool vin = ((reinterpret_cast<uintptr_t>(p.k) | reinterpret_cast<uintptr_t>(p.v)) & 15) == 0;
+    const bool vin = rows_aligned16(p.k, p.sk, sizeof(Tin)) && rows_aligned16(p.v, p.sv, sizeof(Tin));
     constexpr int E = 16 / (int)sizeof(Tin);  // elements per 16-byte piece
     if (vin) {
         const int pr = Kp / E;
@@ -223,7 +223,7 @@ k_prep(Problem p, Workspace ws) {
             float x[E];
             if (i < len && c < K) {
                 const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-                    k + ((t0 + i) * H + h) * (int64_t)K + c));
+                    k + tok_at(p.sk, t0 + i, h) + c));
                 unpack16(raw, k, x);
             } else {
 #pragma unroll
@@ -236,7 +236,7 @@ k_prep(Problem p, Workspace ws) {
         for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
             const int i = idx / Kp, c = idx - i * Kp;
             sK[i * ldk + c] =
-                (i < len && c < K) ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
+                (i < len && c < K) ? ld_in(k, tok_at(p.sk, t0 + i, h) + c) : 0.f;
         }
     }
     __syncthreads();
@@ -298,7 +298,7 @@ k_prep(Problem p, Workspace ws) {
                 float x[E];
                 if (i < len && v0 + c < V) {
                     const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-                        v + ((t0 + i) * H + h) * (int64_t)V + v0 + c));
+                        v + tok_at(p.sv, t0 + i, h) + v0 + c));
                     unpack16(raw, v, x);
                 } else {
 #pragma unroll
@@ -311,7 +311,7 @@ k_prep(Problem p, Workspace ws) {
             for (int idx = tid; idx < kChunk * 64; idx += kThreads) {
                 const int i = idx >> 6, c = idx & 63;
                 sV[i * 65 + c] = (i < len && v0 + c < V)
-                    ? sB[i] * ld_in(v, ((t0 + i) * H + h) * (int64_t)V + v0 + c) : 0.f;
+                    ? sB[i] * ld_in(v, tok_at(p.sv, t0 + i, h) + v0 + c) : 0.f;
             }
         }
         __syncthreads();
@@ -388,7 +388,7 @@ k_scan(Problem p, Workspace ws, int mode) {
     }
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
-    const bool vk = (reinterpret_cast<uintptr_t>(p.k) & 15) == 0;
+    const bool vk = rows_aligned16(p.k, p.sk, sizeof(Tin));
     float dprod = 1.f;
 
     for (int cc = s0; cc < s1; ++cc) {
@@ -406,7 +406,7 @@ k_scan(Problem p, Workspace ws, int mode) {
                 float x[E];
                 if (i < len && c < K) {
                     const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-                        k + ((t0 + i) * H + h) * (int64_t)K + c));
+                        k + tok_at(p.sk, t0 + i, h) + c));
                     unpack16(raw, k, x);
                 } else {
 #pragma unroll
@@ -419,7 +419,7 @@ k_scan(Problem p, Workspace ws, int mode) {
             for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
                 const int i = idx / Kp, c = idx - i * Kp;
                 sK[i * ldk + c] =
-                    (i < len && c < K) ? ld_in(k, ((t0 + i) * H + h) * (int64_t)K + c) : 0.f;
+                    (i < len && c < K) ? ld_in(k, tok_at(p.sk, t0 + i, h) + c) : 0.f;
             }
         }
         if (delta) {  // W rows: float4 pieces of the workspace
@@ -461,7 +461,7 @@ k_scan(Problem p, Workspace ws, int mode) {
                         if (mode != 1)
                             ws.vnew[((gc * H + h) * kChunk + i) * (int64_t)V + col0 + c] = x;
                     } else {
-                        x = ld_in(v, ((t0 + i) * H + h) * (int64_t)V + col0 + c);
+                        x = ld_in(v, tok_at(p.sv, t0 + i, h) + col0 + c);
                     }
                     x *= expf(gl - sG[i]);
                 }
@@ -598,7 +598,7 @@ k_output(Problem p, Workspace ws) {
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
     if (tid < kChunk) sG[tid] = ws.G[(chunk * H + h) * kChunk + tid];
-    const bool vin = ((reinterpret_cast<uintptr_t>(p.q) | reinterpret_cast<uintptr_t>(p.k)) & 15) == 0;
+    const bool vin = rows_aligned16(p.q, p.sq, sizeof(Tin)) && rows_aligned16(p.k, p.sk, sizeof(Tin));
     if (vin) {  // 16-byte pieces (K is a multiple of 16)
         constexpr int E = 16 / (int)sizeof(Tin);
         const int pr = Kp / E;
@@ -606,9 +606,10 @@ k_output(Problem p, Workspace ws) {
             const int i = idx / pr, c = (idx - i * pr) * E;
             float xq[E], xk[E];
             if (i < len && c < K) {
-                const int64_t off = ((t0 + i) * H + h) * (int64_t)K + c;
-                unpack16(__ldg(reinterpret_cast<const uint4 *>(q + off)), q, xq);
-                unpack16(__ldg(reinterpret_cast<const uint4 *>(k + off)), k, xk);
+                unpack16(__ldg(reinterpret_cast<const uint4 *>(q + tok_at(p.sq, t0 + i, h) + c)),
+                         q, xq);
+                unpack16(__ldg(reinterpret_cast<const uint4 *>(k + tok_at(p.sk, t0 + i, h) + c)),
+                         k, xk);
             } else {
 #pragma unroll
                 for (int e2 = 0; e2 < E; ++e2) xq[e2] = xk[e2] = 0.f;
@@ -623,9 +624,8 @@ k_output(Problem p, Workspace ws) {
         for (int idx = tid; idx < kChunk * Kp; idx += kThreads) {
             const int i = idx / Kp, c = idx - i * Kp;
             const bool in = i < len && c < K;
-            const int64_t off = ((t0 + i) * H + h) * (int64_t)K + c;
-            sQ[i * ldk + c] = in ? ld_in(q, off) : 0.f;
-            sK[i * ldk + c] = in ? ld_in(k, off) : 0.f;
+            sQ[i * ldk + c] = in ? ld_in(q, tok_at(p.sq, t0 + i, h) + c) : 0.f;
+            sK[i * ldk + c] = in ? ld_in(k, tok_at(p.sk, t0 + i, h) + c) : 0.f;
         }
     }
     const float *hp = ws.hpre + (chunk * H + h) * (int64_t)K * V;
@@ -638,7 +638,7 @@ k_output(Problem p, Workspace ws) {
         float x = 0.f;
         if (i < len) {
             x = delta ? ws.vnew[((chunk * H + h) * kChunk + i) * (int64_t)V + col0 + c]
-                      : ld_in(v, ((t0 + i) * H + h) * (int64_t)V + col0 + c);
+                      : ld_in(v, tok_at(p.sv, t0 + i, h) + col0 + c);
         }
         sVn[i * ldo + c] = x;
     }
@@ -663,7 +663,7 @@ k_output(Problem p, Workspace ws) {
         const int i = i0 + r, c = j0 + 16 * s;
         if (i < len) {
             const float y = p.scale * fmaf(expf(sG[i]), a1[r][s], a2[r][s]);
-            st_out(o, ((t0 + i) * H + h) * (int64_t)V + col0 + c, y);
+            st_out(o, tok_at(p.so, t0 + i, h) + col0 + c, y);
         }
     }
 }

@@ -535,8 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                     const int idx = tb + 128 * r;
                     const int t = idx >> 4, c16 = idx & 15;
                     if (t < p_len)
-                        *reinterpret_cast<uint4 *>(o + ((p_t0 + t) * H + p_h) * (int64_t)kD +
-                                                   c16 * 8) =
+                        *reinterpret_cast<uint4 *>(o + tok_at(p.so, p_t0 + t, p_h) + c16 * 8) =
                             *reinterpret_cast<const uint4 *>(os + (c16 >> 3) * 8192 +
                                                              sw128_off(t, (c16 & 7) * 8, 64));
                 }
@@ -603,9 +602,10 @@ cudaError_t launch_chain(const TcArgs &args, dim3 grid, cudaStream_t st) {
 }  // namespace
 
 bool tc_supported(const Problem &p) {
-    auto al = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
-    return p.dtype == GDR_BF16 && p.K == kD && p.V == kD && p.beta != nullptr && al(p.q) &&
-           al(p.k) && al(p.v) && al(p.o);
+    // TMA and the 16-byte stores of partial chunks: aligned bases and strides
+    return p.dtype == GDR_BF16 && p.K == kD && p.V == kD && p.beta != nullptr &&
+           rows_aligned16(p.q, p.sq, 2) && rows_aligned16(p.k, p.sk, 2) &&
+           rows_aligned16(p.v, p.sv, 2) && rows_aligned16(p.o, p.so, 2);
 }
 
 cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream_t st) {
@@ -614,15 +614,12 @@ cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream
     args.ws = ws;
     const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
     const uint64_t H = (uint64_t)p.H;
-    if (!make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&args.to, p.o, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
+    if (!make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.to, p.o, kD, H, rows, p.so.h * 2, p.so.t * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     const int S = mode == 0 ? 1 : ws.n_segments;
     const int64_t chains = p.N * S * p.H * (mode == 1 ? 2 : 1);
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    dim3 grid((unsigned)(chains < sms ? chains : sms));
+    dim3 grid((unsigned)persistent_grid(p, chains, 1));
     switch (mode) {
     case 0: return launch_chain<kModeSerial>(args, grid, st);
     case 1: return launch_chain<kModePre>(args, grid, st);

@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                         const int idx = tb + 128 * r;
                         const int t = idx >> 4, c16 = idx & 15;
                         if (t < len)
-                            *reinterpret_cast<uint4 *>(o + ((t0 + t) * H + h) * (int64_t)V + v0 +
+                            *reinterpret_cast<uint4 *>(o + tok_at(p.so, t0 + t, h) + v0 +
                                                        c16 * 8) =
                                 *reinterpret_cast<const uint4 *>(os + (c16 >> 3) * 8192 +
                                                                  sw128_off(t, (c16 & 7) * 8, 64));
@@ -569,9 +569,11 @@ cudaError_t launch_gla(const GlaArgs &args, unsigned grid, cudaStream_t st) {
 }  // namespace
 
 bool tc_gla_supported(const Problem &p) {
-    auto al = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+    // TMA and the 16-byte stores of partial chunks: aligned bases and strides
     return p.dtype == GDR_BF16 && p.beta == nullptr && (p.K == 128 || p.K == 256) &&
-           p.V % 128 == 0 && p.V <= kMaxV && al(p.q) && al(p.k) && al(p.v) && al(p.o);
+           p.V % 128 == 0 && p.V <= kMaxV && rows_aligned16(p.q, p.sq, 2) &&
+           rows_aligned16(p.k, p.sk, 2) && rows_aligned16(p.v, p.sv, 2) &&
+           rows_aligned16(p.o, p.so, 2);
 }
 
 cudaError_t tc_gla(const Problem &p, const Workspace &ws, int mode, cudaStream_t st) {
@@ -580,17 +582,14 @@ cudaError_t tc_gla(const Problem &p, const Workspace &ws, int mode, cudaStream_t
     args.ws = ws;
     const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
     const uint64_t H = (uint64_t)p.H, K = (uint64_t)p.K, V = (uint64_t)p.V;
-    if (!make_tmap_bf16_3d(&args.tq, p.q, K, H, rows, K * 2, H * K * 2, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&args.tk, p.k, K, H, rows, K * 2, H * K * 2, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&args.tv, p.v, V, H, rows, V * 2, H * V * 2, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&args.to, p.o, V, H, rows, V * 2, H * V * 2, 64, 1, 64))
+    if (!make_tmap_bf16_3d(&args.tq, p.q, K, H, rows, p.sq.h * 2, p.sq.t * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.tk, p.k, K, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.tv, p.v, V, H, rows, p.sv.h * 2, p.sv.t * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.to, p.o, V, H, rows, p.so.h * 2, p.so.t * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     const int S = mode == 0 ? 1 : ws.n_segments;
     const int64_t chains = p.N * S * p.H * (p.V / 128);
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const unsigned grid = (unsigned)(chains < sms ? chains : sms);
+    const unsigned grid = (unsigned)persistent_grid(p, chains, 1);
     if (p.K == 128) {
         switch (mode) {
         case 0: return launch_gla<128, kModeSerial>(args, grid, st);

@@ -355,19 +355,16 @@ cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st) {
     args.ws = ws;
     const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
     const uint64_t H = (uint64_t)p.H;
-    if (!make_tmap_bf16_3d(&args.tq, p.q, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&args.tv, p.v, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
+    if (!make_tmap_bf16_3d(&args.tq, p.q, kD, H, rows, p.sq.h * 2, p.sq.t * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.tv, p.v, kD, H, rows, p.sv.h * 2, p.sv.t * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(k_tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemLaunch);
     if (err != cudaSuccess) return err;
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t items = ws.max_chunks * p.H;  // an upper bound; the kernel reads the count
-    if (items > INT32_MAX - 4 * (int64_t)sms) return cudaErrorInvalidValue;
-    const int64_t grid = items < 3 * sms ? items : 3 * sms;  // three CTAs per SM
+    if (items > INT32_MAX - 4 * (int64_t)device_sms()) return cudaErrorInvalidValue;
+    const int64_t grid = persistent_grid(p, items, 3);  // three CTAs per SM
     return launch_pdl(k_tc_prep, dim3((unsigned)grid), dim3(kThreads), kSmemLaunch, st, args);
 }
 

@@ -391,18 +391,15 @@ cudaError_t tc_prescan(const Problem &p, const Workspace &ws, cudaStream_t st) {
     args.ws = ws;
     const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
     const uint64_t H = (uint64_t)p.H;
-    if (!make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
+    if (!make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(k_tc_prescan,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemLaunch);
     if (err != cudaSuccess) return err;
     const int64_t chains = p.N * ws.n_segments * p.H;
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    return launch_pdl(k_tc_prescan, dim3((unsigned)(chains < sms ? chains : sms)), dim3(kThreads),
-                      kSmemLaunch, st, args);
+    return launch_pdl(k_tc_prescan, dim3((unsigned)persistent_grid(p, chains, 1)),
+                      dim3(kThreads), kSmemLaunch, st, args);
 }
 
 }  // namespace gdr

@@ -26,7 +26,8 @@
  *               flash-linear-attention issue #23 "Proposed Dataflow"):
  *               S_t = alpha_t S_{t-1} + v_t k_t^T, the transition is a scalar.
  *
- * Layouts (all row-major and contiguous, element strides implied):
+ * Layouts (row-major; q, k, v and o may carry token and head strides,
+ * see gdr_dims, everything else is contiguous):
  *   q, k        [B, T, H, K]   dtype GDR_BF16, GDR_F16 or GDR_F32 (same for
  *                              q, k, v, o)
  *   v, o        [B, T, H, V]
@@ -94,11 +95,38 @@ enum gdr_flags {
 
 /* Problem size.  Dense layout: N = 0 (there are B sequences of T tokens).
  * Varlen layout: N > 0 sequences packed along T (the total length), B == 1,
- * cu_seqlens required. */
+ * cu_seqlens required.
+ * max_len is a planning hint for the varlen layout, like the max_seqlen
+ * argument of varlen attention kernels: the number of tokens of the longest
+ * sequence, or 0 when the caller does not know it (the plan then assumes the
+ * mean length T / N).  cu_seqlens is device data that the host never reads,
+ * so without the hint a batch with one long sequence among many short ones
+ * looks uniform and the plan keeps the serial scan, whose time is set by the
+ * longest sequence.  The hint only steers the automatic segment count
+ * (n_segments = 0); a wrong value costs time, never correctness.  Ignored
+ * for the dense layout (every sequence has T tokens). */
 typedef struct gdr_dims {
     int64_t B, T, H, K, V, N;
-    int32_t dtype; /* enum gdr_dtype */
-    int32_t flags; /* enum gdr_flags */
+    int32_t dtype;   /* enum gdr_dtype */
+    int32_t flags;   /* enum gdr_flags */
+    int64_t max_len; /* longest sequence (varlen), 0 = unknown */
+    /* Element strides of q, k, v and o: [0] from one token to the next, [1]
+     * from one head to the next; {0, 0} means contiguous ({H*K, K} for q and
+     * k, {H*V, V} for v and o).  The key / value dimension is always
+     * contiguous, and tokens flatten B and T (a dense batch row starts T
+     * token strides after the previous one).  So q, k and v may be views of
+     * one fused projection, e.g. of a [B, T, 3, H, K] tensor: token stride
+     * 3*H*K, head stride K, base pointers K*H elements apart.  Both entries
+     * of a pair are zero or both positive; o's two strides must not let two
+     * elements share an address (its rows are at least V apart and one of
+     * its dimensions spans the other).  The tensor-core kernels read through
+     * TMA, which wants 16-byte multiples: a stride of a BF16 tensor that is
+     * not a multiple of 8 elements, like a misaligned base, moves the call
+     * to the CUDA-core path.  gdr_chunk_fwd_host takes contiguous tensors
+     * only (GDR_ERR_UNSUPPORTED otherwise); gdr_chunk_bwd reads q, k, v
+     * through their strides and ignores o_stride (its dout and gradients
+     * are contiguous). */
+    int64_t q_stride[2], k_stride[2], v_stride[2], o_stride[2];
 } gdr_dims;
 
 /* Launch plan (A13): chosen per shape from measured timings; every plan of
@@ -134,6 +162,12 @@ typedef struct gdr_options {
     int32_t max_launches;
     int32_t *launch_ids;
     int32_t *n_launches;
+    /* 0 => the plan's grids.  > 0: the persistent tensor-core kernels (which
+     * pull their work items from a counter) run with at most this many
+     * CTAs.  Results are identical for every value: each chain or chunk is
+     * computed by one CTA in a fixed order whichever CTA takes it (tests of
+     * bit-identity across launch configurations). */
+    int32_t grid_limit;
 } gdr_options;
 
 /*

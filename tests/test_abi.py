@@ -166,11 +166,35 @@ def test_plan_query_is_deterministic_and_valid():
     assert pkg.gdr_plan_query(1, 65536, 1, 128, 128)["n_segments"] > 1
     assert pkg.gdr_plan_query(1, 10456, 16, 128, 128, N=32)["n_segments"] == 1
     # the tensor-core plan's cost model picks the counts measured fastest on
-    # GB300 for the four split workloads
-    best = {(1, 16384, 16, 128, 128, False): 8, (1, 65536, 8, 128, 128, False): 16,
-            (1, 65536, 1, 128, 128, False): 64, (2, 8192, 4, 256, 512, True): 4}
+    # GB300 for the four split workloads (segments that fill the 152 SMs)
+    best = {(1, 16384, 16, 128, 128, False): 9, (1, 65536, 8, 128, 128, False): 19,
+            (1, 65536, 1, 128, 128, False): 54, (2, 8192, 4, 256, 512, True): 4}
     for (B, T, H, K, V, bf), s in best.items():
         assert pkg.gdr_plan_query(B, T, H, K, V, beta_free=bf)["n_segments"] == s
+
+
+def test_plan_keys_on_the_longest_sequence():
+    """Varlen plans read the longest sequence from the max_len hint
+    (cu_seqlens is device data): at 4 heads one 16K-token sequence among 31
+    short ones is split, the same batch without the hint (mean length 822)
+    or a uniform batch is not, and a negative hint is rejected."""
+    skew = (1, 26304, 4, 128, 128)  # one 16K-token sequence and 31 of 320 tokens
+    assert pkg.gdr_plan_query(*skew, N=32)["n_segments"] == 1
+    assert pkg.gdr_plan_query(*skew, N=32, max_len=16384)["n_segments"] > 1
+    # with 16 heads and 100 short sequences the composition would run in 85
+    # waves (1.1 ms measured at 3 segments against 0.88 ms serial): serial
+    assert pkg.gdr_plan_query(1, 50360, 16, 128, 128, N=101, max_len=16384)["n_segments"] == 1
+    assert pkg.gdr_plan_query(1, 10456, 16, 128, 128, N=32, max_len=512)["n_segments"] == 1
+    # a hint longer than the batch is clamped to it: one sequence of T tokens
+    assert (pkg.gdr_plan_query(1, 16384, 16, 128, 128, N=1, max_len=1 << 40)
+            == pkg.gdr_plan_query(1, 16384, 16, 128, 128))
+    # the CUDA-core rule (FP32 inputs, fewer than two chains an SM) splits on
+    # the longest sequence too
+    one_head = (1, 26304, 1, 128, 128)
+    assert pkg.gdr_plan_query(*one_head, N=32, dtype=0, max_len=16384)["n_segments"] > 1
+    assert pkg.gdr_plan_query(*one_head, N=32, dtype=0)["n_segments"] == 1
+    with pytest.raises(pkg.GdrError):
+        pkg.gdr_plan_query(*skew, N=32, max_len=-1)
 
 
 def test_cuda_core_plan_rules():
@@ -232,3 +256,39 @@ def test_binding_rejects_misuse_before_calling_the_library(lib):
         pkg.gdr_chunk_fwd_host(q, q, q, g.double())
     with pytest.raises(ValueError):  # host entry wants host tensors; meta is not one
         pkg.gdr_chunk_fwd_host(q.to("meta"), q, q, g)
+
+
+def test_stride_validation():
+    """Tensor strides in gdr_dims: a pair is both zero or both positive; o's
+    rows may not overlap; the host entry takes contiguous tensors only.
+    Checked on the host before any CUDA call."""
+    lib = pkg.load_library()
+    p = ctypes.c_void_p(0x1000)
+
+    def fwd(dims):
+        return lib.gdr_chunk_fwd(ctypes.byref(dims), p, p, p, p, p, None, None, p, p, 0, None)
+
+    d = api.make_dims(1, 128, 2, 64, 64)
+    d.q_stride[:] = (0, 64)
+    assert fwd(d) == -1                      # half a pair
+    d = api.make_dims(1, 128, 2, 64, 64)
+    d.o_stride[:] = (64, 32)                 # heads 32 apart: rows of 64 overlap
+    assert fwd(d) == -1
+    d = api.make_dims(1, 128, 2, 64, 64)
+    d.o_stride[:] = (64, 64)                 # two heads on one row
+    assert fwd(d) == -1
+    d = api.make_dims(1, 128, 2, 64, 64)
+    d.k_stride[:] = (-384, 64)
+    assert fwd(d) == -1
+    # a fused [B, T, 3, H, K] projection's views are fine; the host entry
+    # refuses them (it copies whole contiguous buffers)
+    d = api.make_dims(1, 128, 2, 64, 64)
+    for f in ("q_stride", "k_stride", "v_stride"):
+        getattr(d, f)[:] = (3 * 2 * 64, 64)
+    assert pkg.gdr_plan_query(1, 128, 2, 64, 64)["path"] in (1, 2)
+    assert lib.gdr_chunk_fwd_host(ctypes.byref(d), p, p, p, p, p, None, None, p, p, 0,
+                                  None) == -2
+    # head-major o (tokens inside heads) is a valid layout
+    d = api.make_dims(1, 128, 2, 64, 64)
+    d.o_stride[:] = (64, 128 * 64)
+    assert api.gdr_dims.o_stride.size == 16 and d.o_stride[1] == 8192
