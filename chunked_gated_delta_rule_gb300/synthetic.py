@@ -14,6 +14,8 @@ Recipe (one CPU ``torch.Generator`` per draw, seeded; draw order: lengths
 * g = log(sigmoid(N(mu, sigma))) per token and head (mu = 3, sigma = 1; the
   near non-contracting stress workload uses mu = 6, sigma = 0.5);
 * h0 ~ 0.1 * N(0, 1) where an initial state is passed;
+* a skewed batch draws its lengths like the others, then sets the middle
+  sequence's length to ``long_len``;
 * q, k, v are then cast to the workload dtype (BF16 or FP32); g, beta, h0
   stay FP32.
 
@@ -47,6 +49,7 @@ class Workload:
     delta: bool = True     # False: beta-free (beta=None)
     with_h0: bool = False
     seed: int = 0
+    long_len: int = 0      # > 0: sequence n_seqs // 2 has this length instead
 
 
 WORKLOADS = {
@@ -66,6 +69,14 @@ WORKLOADS = {
     # Beta-free (pure gated linear attention) geometry, K=256, V=512.
     "gla_k256_v512_bf16": Workload("gla_k256_v512_bf16", 2, 8192, 4, 256, 512,
                                    "bf16", delta=False, with_h0=True),
+    # One 16K-token sequence among 100 of 128..512 tokens (the longest
+    # sequence, not the mean, sets the serial scan's time).
+    "skewed_varlen_bf16": Workload("skewed_varlen_bf16", 1, 0, 16, 128, 128, "bf16",
+                                   n_seqs=101, len_lo=128, len_hi=512, long_len=16384),
+    # The same skew with 4 heads and 31 short sequences: few chains besides
+    # the long sequence's, so splitting it pays.
+    "skewed_varlen_h4_bf16": Workload("skewed_varlen_h4_bf16", 1, 0, 4, 128, 128, "bf16",
+                                      n_seqs=32, len_lo=128, len_hi=512, long_len=16384),
     # The wide varlen batch with FP16 q / k / v.
     "wide_varlen_f16": Workload("wide_varlen_f16", 1, 0, 16, 128, 128,
                                 "f16", n_seqs=32, len_lo=128, len_hi=512),
@@ -96,6 +107,8 @@ def make_inputs(w: Workload, lengths: Optional[list] = None, T: Optional[int] = 
     if lengths is not None or w.n_seqs > 0:
         if lengths is None:
             lens = torch.randint(w.len_lo, w.len_hi + 1, (w.n_seqs,), generator=gen)
+            if w.long_len:
+                lens[w.n_seqs // 2] = w.long_len
         else:
             lens = torch.tensor(lengths, dtype=torch.int64)
         cu = torch.zeros(lens.numel() + 1, dtype=torch.int32)

@@ -8,7 +8,7 @@ import torch
 
 import chunked_gated_delta_rule_gb300 as pkg
 from chunked_gated_delta_rule_gb300 import synthetic
-from gpu_util import TOL_F32, rel_l2_masked, run_gpu, run_oracle, to_dev
+from gpu_util import TOL_F32, assert_parity, rel_l2_masked, run_gpu, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -21,8 +21,7 @@ def check(x, **kw):
     o, ht = run_gpu(x, **kw)
     ro, rht = run_oracle(x)
     assert o.dtype == torch.float16
-    eo, eh = rel_l2_masked(o, ro), rel_l2_masked(ht, rht)
-    assert eo <= TOL_O_F16 and eh <= TOL_F32, (eo, eh)
+    assert_parity(x, o, ht, ro, rht, TOL_O_F16, TOL_F32, label=f"fp16 {kw}")
 
 
 @pytest.mark.parametrize("S", [1, 4])
@@ -47,8 +46,7 @@ def test_recurrent_fp16():
                               cu_seqlens=d["cu_seqlens"], state=p, state_indices=idx.cuda())
     torch.cuda.synchronize()
     ro, rht = run_oracle(x)
-    assert rel_l2_masked(o, ro) <= TOL_O_F16
-    assert rel_l2_masked(p.cpu()[idx.long()], rht) <= TOL_F32
+    assert_parity(x, o, p.cpu()[idx.long()], ro, rht, TOL_O_F16, TOL_F32, label="fp16 recurrent")
 
 
 TOL_BF16_OPERANDS = 6e-3  # the BF16 bar: the tensor-core kernels take BF16 operands
@@ -71,10 +69,8 @@ def test_tensor_core_path_on_fp16_inputs(case):
     assert o.dtype == torch.float16
     o2, ht2 = run_gpu(x, force_path=2, n_segments=2)  # the split on the same copies
     ro, rht = run_oracle(x)
-    assert rel_l2_masked(o2, ro) <= TOL_BF16_OPERANDS
-    assert rel_l2_masked(ht2, rht) <= TOL_BF16_OPERANDS
-    eo, eh = rel_l2_masked(o, ro), rel_l2_masked(ht, rht)
-    assert eo <= TOL_BF16_OPERANDS and eh <= TOL_BF16_OPERANDS, (eo, eh)
+    assert_parity(x, o2, ht2, ro, rht, TOL_BF16_OPERANDS, label=f"{case} split")
+    assert_parity(x, o, ht, ro, rht, TOL_BF16_OPERANDS, label=case)
     xb = dict(x)
     for name in ("q", "k", "v"):
         xb[name] = x[name].to(torch.bfloat16)

@@ -7,7 +7,7 @@ import torch
 
 import chunked_gated_delta_rule_gb300 as pkg
 from chunked_gated_delta_rule_gb300 import synthetic
-from gpu_util import TOL_BF16, TOL_F32, rel_l2_masked, run_oracle, to_dev
+from gpu_util import TOL_BF16, TOL_F32, assert_parity, rel_l2_masked, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -32,10 +32,8 @@ def run_pool(x, n_states, use_indices=True, seed=1):
 def check(x, n_states, tol_o, tol_h, **kw):
     o, after, before, idx = run_pool(x, n_states, **kw)
     ro, rht = run_oracle(x)
-    eo = rel_l2_masked(o, ro)
-    eh = rel_l2_masked(after[idx.long()], rht)
     assert torch.isfinite(o.float()).all()
-    assert eo <= tol_o and eh <= tol_h, (eo, eh)
+    eo, eh, _, _ = assert_parity(x, o, after[idx.long()], ro, rht, tol_o, tol_h, label="recurrent")
     untouched = torch.ones(n_states, dtype=torch.bool)
     untouched[idx.long()] = False
     assert torch.equal(after[untouched], before[untouched])
@@ -95,8 +93,7 @@ def test_chained_steps_equal_the_chunked_forward():
                               o=ostep)
         o[:, sel] = ostep
     torch.cuda.synchronize()
-    assert rel_l2_masked(o, ro) <= TOL_F32
-    assert rel_l2_masked(pool, rht) <= TOL_F32
+    assert_parity(x, o, pool, ro, rht, TOL_F32, label="chained decode steps")
     oc, htc = pkg.gdr_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
                                 cu_seqlens=d["cu_seqlens"])
     torch.cuda.synchronize()

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 from chunked_gated_delta_rule_gb300 import synthetic
-from gpu_util import TOL_BF16, rel_l2_masked, run_gpu, run_oracle, sample_mask
+from gpu_util import TOL_BF16, assert_parity, run_gpu, run_oracle, sample_mask
 
 pytestmark = pytest.mark.gpu
 
@@ -27,9 +27,7 @@ def reference(name, pairs=None):
 def check(name, pairs=None, **kw):
     x, (ro, rht) = reference(name, pairs)
     o, ht = run_gpu(x, **kw)
-    eo, eh = rel_l2_masked(o, ro), rel_l2_masked(ht, rht)
-    print(f"{name} {kw}: rel_l2 o={eo:.3e} ht={eh:.3e}")
-    assert eo <= TOL_BF16 and eh <= TOL_BF16, (eo, eh)
+    assert_parity(x, o, ht, ro, rht, TOL_BF16, label=f"{name} {kw}")
 
 
 def test_wide_varlen_all_pairs():
@@ -54,3 +52,18 @@ def test_stress_64k_h1(S):
 @pytest.mark.parametrize("S", [0, 1, 8])
 def test_gla_k256_v512(S):
     check("gla_k256_v512_bf16", pairs=[(0, 0), (1, 3)], n_segments=S)
+
+
+@pytest.mark.parametrize("S", [0, 1])
+def test_skewed_varlen(S):
+    """One 16K-token sequence (number 50) among 100 of 128..512 tokens: with
+    the longest-sequence hint the plan splits (S = 0), the serial scan is
+    the reference plan; pairs on the long sequence and on short ones."""
+    check("skewed_varlen_bf16", pairs=[(50, 0), (50, 15), (0, 3), (100, 7)], n_segments=S)
+
+
+@pytest.mark.parametrize("S", [0, 1])
+def test_skewed_varlen_h4(S):
+    """One 16K-token sequence (number 16) among 31 short ones at 4 heads: the
+    longest-sequence hint makes the plan split (S = 0)."""
+    check("skewed_varlen_h4_bf16", pairs=[(16, 0), (16, 3), (0, 1), (31, 2)], n_segments=S)

@@ -35,7 +35,11 @@ def test_workload_recipe(name):
         cu = x["cu_seqlens"]
         lens = cu[1:] - cu[:-1]
         assert cu[0] == 0 and cu[-1] == T and N == w.n_seqs and B == 1
-        assert ((lens >= w.len_lo) & (lens <= w.len_hi)).all()
+        rest = torch.ones_like(lens, dtype=torch.bool)
+        if w.long_len:  # the skewed batch: its middle sequence has long_len tokens
+            assert lens[w.n_seqs // 2] == w.long_len
+            rest[w.n_seqs // 2] = False
+        assert ((lens[rest] >= w.len_lo) & (lens[rest] <= w.len_hi)).all()
     else:
         assert x["cu_seqlens"] is None and N == B
     assert (x["h0"] is not None) == w.with_h0
