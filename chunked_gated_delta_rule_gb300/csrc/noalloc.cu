@@ -23,6 +23,7 @@
 #include <mutex>
 
 #include "gdr_internal.cuh"
+#include "gdr_launch.cuh"
 
 namespace {
 
@@ -54,9 +55,16 @@ extern "C" int gdr_chunk_fwd_noalloc(const gdr_dims *dims, const void *q, const 
                                      const void *v, const float *g, const float *beta,
                                      const int32_t *cu_seqlens, const float *h0, void *o,
                                      float *ht, int n_segments, gdr_stream_t stream) {
-    if (!dims) return GDR_ERR_INVALID;
-    const size_t need = gdr_workspace_size(dims, beta == nullptr, n_segments);
-    if (need == 0) return GDR_ERR_INVALID;  // dims or n_segments rejected
+    if (!dims || !q || !k || !v || !g || !o) return GDR_ERR_INVALID;
+    if ((cu_seqlens != nullptr) != (dims->N > 0)) return GDR_ERR_INVALID;
+    // the scratch of the path this call will run (misaligned pointers move a
+    // tensor-core shape to the CUDA-core path, which needs more); invalid or
+    // unsupported arguments return the code gdr_chunk_fwd would
+    gdr_plan plan;
+    size_t need = 0;
+    const int rc = gdr::plan_for_call(*dims, beta == nullptr, n_segments, nullptr, q, k, v, o,
+                                      &plan, &need);
+    if (rc != GDR_OK) return rc;
     if (need > kNoAllocScratchBytes) return GDR_ERR_WORKSPACE;  // problem too large
     void *scratch = scratch_for_current_device();
     if (!scratch) return GDR_ERR_CUDA;
