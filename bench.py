@@ -3,17 +3,26 @@
 roofline fraction of the dominant kernel.
 
 One step is one gdr_chunk_fwd call (the whole forward path: chunk indexing,
-gate cumsum, Gram / inverse / WY factors, state scan, output) over one batch
-of the wide varlen workload (32 packed sequences of 128..512 tokens, H=16,
-K=V=128, BF16 q/k/v), inputs resident in HBM.  L2 is flushed (a 256 MiB
-write) between timed steps, outside the timed events.
+gate cumsum, Gram / inverse / WY factors, state scan, output, and for a long
+sequence the segment pre-scan and composition) over one batch of the
+headline workload, inputs resident in HBM: the largest configuration that
+fits one GPU, one 65,536-token sequence with 8 heads (K = V = 128, BF16
+q/k/v, near non-contracting decay), at the plan's segment count.  L2 is
+flushed (a 256 MiB write) between timed steps, outside the timed events.
+
+The same JSON line carries a sub-record per configuration ("configs"): ms
+per call, tokens/s, the call's roofline fraction, per-kernel times; serial
+beside split at 64K tokens (8 heads and 1); at 16K tokens every split count
+with its error against the FP64 oracle on sampled (sequence, head) pairs;
+the plan's pick beside serial on a batch with one long sequence.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdr|reference]
+                  [--workload NAME] [--no-configs]
 
---impl reference times the FP64 CPU oracle (the slow reference program) on a
-bounded sample of the same workload.  Under torchrun every rank runs an
-independent replica (the path needs no exchange between GPUs); rank 0
-prints one JSON line.
+--impl reference times the FP64 CPU oracle (the slow reference program) on
+bounded samples of the same workload, drawn by the same sampler as the
+cpu_baseline record.  Under torchrun every rank runs an independent replica
+(the path needs no exchange between GPUs); rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
@@ -35,7 +44,7 @@ if ROOT not in sys.path:
 METRIC = "tokens/s and ms per gdr_chunk_fwd call on 1 GB300; % of roofline"
 METRIC_BWD = "tokens/s and ms per gdr_chunk_bwd call on 1 GB300; % of roofline"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "wide_varlen_bf16"
+DEFAULT_WORKLOAD = "stress_64k_h8_bf16"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -52,6 +61,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration sub-records")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
                     help="bwd times gdr_chunk_bwd (the backward pass) instead")
     return ap.parse_args()
@@ -170,7 +181,7 @@ def gpu_index_for_smi():
 
 # ----------------------------------------------------------------------------
 # algorithmic bytes per kernel launch (units: token-heads, chunk-heads,
-# sequence-heads; figures stated in DESIGN.md "Measurement")
+# sequence-heads, segment summaries)
 # ----------------------------------------------------------------------------
 def counts(x, n_segments=1):
     H = x["H"]
@@ -325,54 +336,78 @@ def source_hash(kernel):
 
 
 # ----------------------------------------------------------------------------
-# CPU oracle timing (reported baseline / reference arm)
+# CPU oracle timing (reported baseline / reference arm).  One sampler serves
+# both: a sample is whole heads of a few sequences taken in order (cycling),
+# each cut to its first ORACLE_SAMPLE_TOKENS tokens, until that many tokens
+# are taken; the oracle's cost per token does not depend on the position.
 # ----------------------------------------------------------------------------
-def oracle_inputs(x):
+ORACLE_SAMPLE_TOKENS = 4096
+
+
+def oracle_sample(x, first, cap=ORACLE_SAMPLE_TOKENS):
+    """Rows of one sample: a list of (sequence, first row, rows) along the
+    flattened token axis, starting at sequence `first`; returns (pieces,
+    tokens, next sequence)."""
+    if x["cu_seqlens"] is not None:
+        cu = [int(c) for c in x["cu_seqlens"].tolist()]
+    else:
+        cu = [n * x["T"] for n in range(x["B"] + 1)]
+    N = len(cu) - 1
+    pieces, tokens, n, seen = [], 0, first % N, 0
+    while tokens < cap and seen < N:
+        a, b = cu[n], cu[n + 1]
+        take = min(b - a, cap - tokens)
+        if take > 0:
+            pieces.append((n, a, take))
+            tokens += take
+        n = (n + 1) % N
+        seen += 1
+    return pieces, tokens, n
+
+
+def sample_inputs(xo, pieces, extra=None):
+    """The sample as its own varlen problem (FP64 arrays, all heads):
+    q, k, v, g, beta, h0 and the optional per-token / per-sequence extras
+    (do, dht) cut to the sample's rows and sequences."""
     import numpy as np
+
+    def rows(a):
+        if a is None:
+            return None
+        flat = a.reshape((-1,) + a.shape[2:])
+        return np.ascontiguousarray(np.concatenate([flat[r:r + n] for _, r, n in pieces])[None])
+
+    def seqs(a):
+        return None if a is None else np.ascontiguousarray(a[[s for s, _, _ in pieces]])
+
+    cu = np.zeros(len(pieces) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum([n for _, _, n in pieces])
+    sub = {k: rows(xo[k]) for k in ("q", "k", "v", "g", "beta")}
+    sub.update(cu_seqlens=cu, h0=seqs(xo["h0"]), H=xo["H"])
+    if extra:
+        sub["do"] = rows(extra[0])
+        sub["dht"] = seqs(extra[1])
+    return sub
+
+
+def oracle_inputs(x):
     import oracle
     return {k: (oracle._f64(v) if k in ("q", "k", "v", "g", "beta", "h0") else v)
             for k, v in x.items()}
 
 
-def time_oracle_on(xo, seqs):
-    """Runs the oracle on the (sequence, head) pairs of `seqs` (all heads);
-    returns (seconds, tokens, threads)."""
-    import numpy as np
+def time_oracle_sample(sub, backward=False):
+    """Seconds and threads of one oracle run on a sample (all heads)."""
     import oracle
-    N, H = xo["N"], xo["H"]
-    mask = np.zeros(N * H, dtype=bool)
-    for n in seqs:
-        mask[n * H:(n + 1) * H] = True
-    if xo["cu_seqlens"] is not None:
-        cu = xo["cu_seqlens"].tolist()
-        tokens = sum(cu[n + 1] - cu[n] for n in seqs)
-    else:
-        tokens = xo["T"] * len(seqs)
     t0 = time.perf_counter()
-    _, _, threads = oracle.forward(xo["q"], xo["k"], xo["v"], xo["g"], xo["beta"],
-                                   cu_seqlens=xo["cu_seqlens"], h0=xo["h0"],
-                                   pair_mask=mask, want_ht=True)
-    return time.perf_counter() - t0, tokens, threads
-
-
-def time_oracle_bwd_on(xo, seqs, do, dht):
-    """The oracle's backward pass on the (sequence, head) pairs of `seqs`."""
-    import numpy as np
-    import oracle
-    N, H = xo["N"], xo["H"]
-    mask = np.zeros(N * H, dtype=bool)
-    for n in seqs:
-        mask[n * H:(n + 1) * H] = True
-    if xo["cu_seqlens"] is not None:
-        cu = xo["cu_seqlens"].tolist()
-        tokens = sum(cu[n + 1] - cu[n] for n in seqs)
+    if backward:
+        oracle.backward(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"],
+                        cu_seqlens=sub["cu_seqlens"], h0=sub["h0"], do=sub["do"], dht=sub["dht"])
+        threads = min(os.cpu_count() or 1, (len(sub["cu_seqlens"]) - 1) * sub["H"])
     else:
-        tokens = xo["T"] * len(seqs)
-    t0 = time.perf_counter()
-    oracle.backward(xo["q"], xo["k"], xo["v"], xo["g"], xo["beta"], cu_seqlens=xo["cu_seqlens"],
-                    h0=xo["h0"], do=do, dht=dht, pair_mask=mask)
-    threads = min(os.cpu_count() or 1, len(seqs) * H)
-    return time.perf_counter() - t0, tokens, threads
+        _, _, threads = oracle.forward(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"],
+                                       cu_seqlens=sub["cu_seqlens"], h0=sub["h0"], want_ht=True)
+    return time.perf_counter() - t0, threads
 
 
 def bwd_grads_in(x, seed=7):
@@ -385,83 +420,73 @@ def bwd_grads_in(x, seed=7):
     return do, dht
 
 
-def cpu_baseline_bwd(x, budget_s):
+def oracle_samples(x, backward=False):
+    """Generator of (seconds, tokens, threads) over successive samples of
+    the workload; the first untimed run loads the oracle."""
     import oracle
     xo = oracle_inputs(x)
-    do, dht = bwd_grads_in(x)
-    do, dht = oracle._f64(do), oracle._f64(dht)
-    N = xo["N"]
-    secs, toks, threads, groups, n = 0.0, 0, 1, 0, 0
-    while secs < budget_s and n < 64 * N:
-        group = [(n + j) % N for j in range(min(4, N))]
-        dt, tk, threads = time_oracle_bwd_on(xo, group, do, dht)
-        secs += dt
-        toks += tk
-        groups += 1
-        n += len(group)
-    return {"value": toks / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{groups} groups of 4 sequences x all {xo['H']} heads cycling over "
-                      f"the {N}-sequence batch ({toks} tokens), FP64 reverse token "
-                      f"recurrence, {secs:.1f} s"}
+    extra = None
+    if backward:
+        do, dht = bwd_grads_in(x)
+        extra = (oracle._f64(do), oracle._f64(dht))
+    nxt = 0
+    pieces, _, _ = oracle_sample(x, 0, cap=64)
+    time_oracle_sample(sample_inputs(xo, pieces, extra), backward)  # load, untimed
+    while True:
+        pieces, tokens, nxt = oracle_sample(x, nxt)
+        secs, threads = time_oracle_sample(sample_inputs(xo, pieces, extra), backward)
+        yield secs, tokens, threads, len(pieces)
 
 
-def cpu_baseline(x, budget_s):
-    """Times the oracle over groups of 4 sequences (all heads), cycling
-    through the batch, until about `budget_s` seconds of CPU work (at most
-    64 passes over the batch)."""
-    xo = oracle_inputs(x)
-    N = xo["N"]
-    secs, toks, threads, groups = 0.0, 0, 1, 0
-    n = 0
-    while secs < budget_s and n < 64 * N:
-        group = [(n + j) % N for j in range(min(4, N))]
-        dt, tk, threads = time_oracle_on(xo, group)
+def sample_text(x, backward):
+    return (f"samples of up to {ORACLE_SAMPLE_TOKENS} tokens: whole heads ({x['H']}) of "
+            f"sequences taken in order, each cut to its first {ORACLE_SAMPLE_TOKENS} tokens; "
+            "FP64 token recurrence" + (" and its reverse (backward)" if backward else ""))
+
+
+def cpu_baseline(x, budget_s, backward=False):
+    """The oracle on successive samples until about `budget_s` seconds of
+    CPU work."""
+    secs = toks = n = 0
+    threads = 1
+    for dt, tk, threads, _ in oracle_samples(x, backward):
         secs += dt
         toks += tk
-        groups += 1
-        n += len(group)
+        n += 1
+        if secs >= budget_s or n >= 256:
+            break
     return {"value": toks / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{groups} groups of 4 sequences x all {xo['H']} heads cycling over "
-                      f"the {N}-sequence batch ({toks} tokens), FP64 token recurrence, "
-                      f"{secs:.1f} s"}
+            "sample": f"{n} {sample_text(x, backward)}; {toks} tokens in {secs:.1f} s"}
+
+
+def cpu_baseline_bwd(x, budget_s):
+    return cpu_baseline(x, budget_s, backward=True)
 
 
 def run_reference(args):
     from chunked_gated_delta_rule_gb300 import synthetic
-    rank, _, world = int(os.environ.get("RANK", "0")), 0, int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = synthetic.WORKLOADS[args.workload]
     x = synthetic.make_inputs(w)
-    xo = oracle_inputs(x)
-    N = xo["N"]
-    per_step = 1 if N >= 1 else 0
+    backward = args.which == "bwd"
     times, toks, threads = [], [], 1
-    if args.which == "bwd":
-        import oracle
-        do, dht = bwd_grads_in(x)
-        do, dht = oracle._f64(do), oracle._f64(dht)
+    gen = oracle_samples(x, backward)
     for i in range(args.warmup + args.steps):
-        seqs = [(i * per_step + j) % N for j in range(per_step)]
-        if args.which == "bwd":
-            dt, tk, threads = time_oracle_bwd_on(xo, seqs, do, dht)
-        else:
-            dt, tk, threads = time_oracle_on(xo, seqs)
+        dt, tk, threads, _ = next(gen)
         if i >= args.warmup:
             times.append(dt)
             toks.append(tk)
     value = sum(toks) / sum(times)
-    line = {"impl": "reference", "metric": METRIC_BWD if args.which == "bwd" else METRIC,
+    line = {"impl": "reference", "metric": METRIC_BWD if backward else METRIC,
             "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(args, x, None),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"each step one sequence x all {xo['H']} heads of the "
-                                       "workload (cycling), FP64 token recurrence"
-                                       + (" and its reverse (backward)" if args.which == "bwd"
-                                          else "")},
+                             "sample": "each step one of the " + sample_text(x, backward)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -479,6 +504,205 @@ def config_of(args, x, plan):
     return c
 
 
+def scan_bytes(x, c):
+    """Algorithmic bytes of the state scan alone (its unfused form, the BF16
+    state stored once a chunk), per the hot-path table: per token-head W and
+    U (delta rule), k, g, v_new, and K*V*2/64 of state; 1,540 B at K = V =
+    128 BF16."""
+    K, V = x["K"], x["V"]
+    es = 2 if x["dtype"] == "bf16" else 4
+    delta = x["beta"] is not None
+    per = ((K + V) * es if delta else 0) + K * es + 4 + V * es + K * V * 2 / 64
+    return c["token_heads"] * per
+
+
+def max_seqlen_of(x):
+    if x["cu_seqlens"] is None:
+        return None
+    cu = x["cu_seqlens"]
+    return int((cu[1:] - cu[:-1]).max()) if cu.numel() > 1 else 0
+
+
+def plan_of(pkg, x, segments=0):
+    return pkg.gdr_plan_query(x["B"], x["T"], x["H"], x["K"], x["V"],
+                              N=x["N"] if x["cu_seqlens"] is not None else 0,
+                              dtype={"f32": 0, "bf16": 1, "f16": 2}[x["dtype"]],
+                              beta_free=x["beta"] is None, n_segments=segments,
+                              max_len=max_seqlen_of(x) or 0)
+
+
+class Measured:
+    """Timed gdr_chunk_fwd calls on one workload: `steps` calls bracketed by
+    CUDA events on the launching stream with L2 flushed between them, then a
+    second pass of the same calls with the library's per-launch events."""
+
+    def __init__(self, pkg, x, dev, steps, warmup, flush, n_segments=0, force_path=0,
+                 sampler=None, kernels=True):
+        import torch
+        self.x = x
+        d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+        self.d = d
+        o = torch.empty_like(d["v"])
+        ht = torch.empty(x["N"], x["H"], x["K"], x["V"], dtype=torch.float32, device=dev)
+        self.kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], o=o, ht=ht,
+                       n_segments=n_segments, force_path=force_path,
+                       max_seqlen=max_seqlen_of(x))
+        self.args = (d["q"], d["k"], d["v"], d["g"], d["beta"])
+        stream = torch.cuda.current_stream(dev)
+        for _ in range(max(3, warmup)):
+            pkg.gdr_chunk_fwd(*self.args, **self.kw)
+        torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        # A bounded ~2 ms spin on the GPU and one untimed call behind it,
+        # outside the timed region, so that the host is already enqueueing
+        # the steps when the first one starts.
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(4_000_000)
+        pkg.gdr_chunk_fwd(*self.args, **self.kw)
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            pkg.gdr_chunk_fwd(*self.args, **self.kw)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        self.clocks = sampler.stop() if sampler else None
+        self.step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        self.ms = statistics.mean(self.step_ms)
+        self.per_kernel, self.launches, self.kstep_ms = {}, 0, []
+        if not kernels:
+            return
+        timers = [pkg.LaunchTimer(16) for _ in range(steps)]
+        ks = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ke = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ks[i].record(stream)
+            pkg.gdr_chunk_fwd(*self.args, timer=timers[i], **self.kw)
+            ke[i].record(stream)
+        torch.cuda.synchronize()
+        self.kstep_ms = [a.elapsed_time(b) for a, b in zip(ks, ke)]
+        for t in timers:
+            self.launches += t.count
+            for i, kid in enumerate(t.ids):
+                self.per_kernel.setdefault(pkg.gdr_kernel_name(kid), []).append(t.elapsed_ms(i))
+
+    def kernels(self):
+        tot = sum(self.kstep_ms) or 1.0
+        return {n: {"launches": len(v), "avg_ms": statistics.mean(v), "share": sum(v) / tot}
+                for n, v in self.per_kernel.items()}
+
+    def outputs(self):
+        return self.kw["o"], self.kw["ht"]
+
+
+def rooflines(x, c, m, hbm, workload):
+    """Fractions of the measured copy bandwidth, by the hot-path table's
+    algorithmic bytes: the whole call's 1,032 B per token-head (K = V = 128
+    BF16) over the dominant kernel's mean launch time (`roofline`) and over
+    the call (`call_roofline`); the scan alone's 1,540 B per token-head over
+    the scan kernel's time (`scan_roofline`).  Each kernel's own bytes
+    (its records and summaries included) go under kernel_bytes."""
+    call = algorithmic_bytes("call", x, c)
+    out = {"call_roofline": {"achieved": call / (m.ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                             "frac": call / (m.ms * 1e-3) / 1e9 / hbm, "algorithmic_bytes": call}}
+    if not m.per_kernel:
+        return out
+    dom = max(m.per_kernel, key=lambda n: sum(m.per_kernel[n]))
+    dom_ms = statistics.mean(m.per_kernel[dom])
+    own = algorithmic_bytes(dom, x, c)
+    out["roofline"] = {
+        "kernel": dom, "bound": "hbm", "achieved": call / (dom_ms * 1e-3) / 1e9, "peak": hbm,
+        "unit": "GB/s", "frac": call / (dom_ms * 1e-3) / 1e9 / hbm,
+        "traffic": traffic_record(dom, workload),
+        "algorithmic_bytes_per_launch": call, "avg_launch_ms": dom_ms,
+        "kernel_bytes": own,
+        "kernel_frac": own / (dom_ms * 1e-3) / 1e9 / hbm if own else None,
+        "basis": "the whole call's algorithmic bytes (q, k, v, g, beta read once, o written "
+                 "once, h0 / ht) over the dominant kernel's mean launch time; kernel_bytes "
+                 "is the kernel's own traffic, per-chunk records included"}
+    scan = next((n for n in ("tc_chain_serial", "tc_chain_segment_out", "tc_gla_serial",
+                             "tc_gla_segment_out", "simt_scan_serial", "simt_scan_segment_out")
+                 if n in m.per_kernel), None)
+    if scan is not None:
+        sb = scan_bytes(x, c)
+        s_ms = statistics.mean(m.per_kernel[scan])
+        own = algorithmic_bytes(scan, x, c)
+        out["scan_roofline"] = {
+            "kernel": scan, "bound": "hbm", "achieved": sb / (s_ms * 1e-3) / 1e9, "peak": hbm,
+            "unit": "GB/s", "frac": sb / (s_ms * 1e-3) / 1e9 / hbm,
+            "traffic": traffic_record(scan, workload), "algorithmic_bytes_per_launch": sb,
+            "avg_launch_ms": s_ms, "kernel_bytes": own,
+            "kernel_frac": own / (s_ms * 1e-3) / 1e9 / hbm if own else None}
+    return out
+
+
+# Per-configuration sub-records: the five configurations of the project
+# statement (64K at 8 and 1 heads) and a batch with one long sequence.
+CONFIG_WORKLOADS = ("tiny_dense_f32", "wide_varlen_bf16", "long_16k_bf16", "stress_64k_h8_bf16",
+                    "stress_64k_h1_bf16", "gla_k256_v512_bf16", "skewed_varlen_bf16",
+                    "skewed_varlen_h4_bf16")
+
+
+def config_record(pkg, name, dev, steps, flush, hbm):
+    from chunked_gated_delta_rule_gb300 import synthetic
+    x = synthetic.make_inputs(synthetic.WORKLOADS[name])
+    plan = plan_of(pkg, x)
+    c = counts(x, plan["n_segments"])
+    m = Measured(pkg, x, dev, steps, 3, flush)
+    rec = {"plan": plan, "tokens": c["tokens"], "ms_per_call": m.ms,
+           "tokens_per_s": c["tokens"] / (m.ms * 1e-3),
+           "token_heads_per_s": c["token_heads"] / (m.ms * 1e-3),
+           "kernels": m.kernels()}
+    rec.update(rooflines(x, c, m, hbm, name))
+    if name.startswith("skewed"):
+        ser = Measured(pkg, x, dev, steps, 3, flush, n_segments=1, kernels=False)
+        rec["serial_ms_per_call"] = ser.ms
+        rec["split_over_serial_speedup"] = ser.ms / m.ms
+        del ser
+    if name in SPLIT_SWEEPS:
+        add_split_sweep(rec, pkg, x, dev, steps, flush, plan["n_segments"], SPLIT_SWEEPS[name])
+    return x, m, rec
+
+
+def add_split_sweep(rec, pkg, x, dev, steps, flush, plan_s, counts_):
+    """ms per call at each split count and the error against the serial
+    result on the same inputs (the pages' "CP vs serial" accuracy table;
+    the errors against the FP64 oracle at each count are the GPU parity
+    tests', on sampled pairs).  At strong decay (g ~ log sigmoid(N(3, 1)))
+    a segment's transition underflows to zero in FP32 and the split is
+    bit-identical to serial; the near non-contracting 64K workload is where
+    split counts differ."""
+    sweep = {}
+    o1 = ht1 = None
+    for S in sorted(set(counts_) | {plan_s, 1}):
+        mS = Measured(pkg, x, dev, steps, 3, flush, n_segments=S, kernels=False)
+        o, ht = mS.outputs()
+        if S == 1:
+            o1, ht1 = o.clone(), ht.clone()
+        sweep[str(S)] = {"ms_per_call": mS.ms, "rel_l2_vs_serial_o": rel_l2(o, o1),
+                         "rel_l2_vs_serial_ht": rel_l2(ht, ht1)}
+        del mS, o, ht
+    rec["split_sweep"] = sweep
+    rec["serial_ms_per_call"] = sweep["1"]["ms_per_call"]
+    rec["split_over_serial_speedup"] = sweep["1"]["ms_per_call"] / sweep[str(plan_s)]["ms_per_call"]
+
+
+# split counts swept per configuration (the plan's count is always added)
+SPLIT_SWEEPS = {"long_16k_bf16": (1, 2, 4, 8, 16), "stress_64k_h8_bf16": (1, 4, 8, 16),
+                "stress_64k_h1_bf16": (1, 16, 32, 64)}
+
+
+def rel_l2(a, ref):
+    """||a - ref|| / ||ref|| in FP64 on the device."""
+    a64, r64 = a.double(), ref.double()
+    den = float(r64.norm())
+    return float((a64 - r64).norm()) / den if den > 0 else float((a64 - r64).norm())
+
+
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
@@ -492,16 +716,7 @@ def run_gdr(args):
     torch.cuda.set_device(dev)
     w = synthetic.WORKLOADS[args.workload]
     x = synthetic.make_inputs(w)
-    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
-    o = torch.empty_like(d["v"])
-    ht = torch.empty(x["N"], x["H"], x["K"], x["V"], dtype=torch.float32, device=dev)
-    kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], o=o, ht=ht, n_segments=args.segments,
-              force_path=args.force_path)
-    args_t = (d["q"], d["k"], d["v"], d["g"], d["beta"])
-    plan = pkg.gdr_plan_query(x["B"], x["T"], x["H"], x["K"], x["V"], N=x["N"] if
-                              x["cu_seqlens"] is not None else 0,
-                              dtype={"f32": 0, "bf16": 1, "f16": 2}[x["dtype"]],
-                              beta_free=x["beta"] is None, n_segments=args.segments)
+    plan = plan_of(pkg, x, args.segments)
     seg_count = plan["n_segments"]
     if args.force_path and args.force_path != plan["path"]:
         # the query plans the default path; a forced path applies its own rules
@@ -511,95 +726,35 @@ def run_gdr(args):
     c = counts(x, seg_count)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    for i in range(max(3, args.warmup)):
-        pkg.gdr_chunk_fwd(*args_t, **kw)
-    torch.cuda.synchronize()
+    peaks = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
 
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     sampler = ClockSampler(gpu_index_for_smi()) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize()
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
-    # A bounded ~2 ms spin on the GPU and one untimed call behind it, outside
-    # the timed region, so that the host is already enqueueing the steps when
-    # the first one starts (else step 0 also times the host's first call after
-    # a synchronisation).
-    if hasattr(torch.cuda, "_sleep"):
-        torch.cuda._sleep(4_000_000)
-    pkg.gdr_chunk_fwd(*args_t, **kw)
-    for i in range(K):
-        flush.fill_(i & 0xFF)
-        starts[i].record(stream)
-        pkg.gdr_chunk_fwd(*args_t, **kw)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    m = Measured(pkg, x, dev, K, args.warmup, flush, n_segments=args.segments,
+                 force_path=args.force_path, sampler=sampler)
     barrier(world)
-    clocks = sampler.stop() if sampler else None
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_local = statistics.mean(step_ms)
-    ms = max_over_ranks(ms_local, world)
-
-    # Per-kernel durations: the same K steps again, with events recorded by
-    # the library around every launch on the launching stream (kept out of
-    # the timed steps above: recording them costs host time between launches).
-    timers = [pkg.LaunchTimer(16) for _ in range(K)]
-    kstarts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    kends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for i in range(K):
-        flush.fill_(i & 0xFF)
-        kstarts[i].record(stream)
-        pkg.gdr_chunk_fwd(*args_t, timer=timers[i], **kw)
-        kends[i].record(stream)
-    torch.cuda.synchronize()
-    kstep_ms = [s.elapsed_time(e) for s, e in zip(kstarts, kends)]
-    per_kernel = {}
-    launches = 0
-    for t in timers:
-        launches += t.count
-        for i, kid in enumerate(t.ids):
-            name = pkg.gdr_kernel_name(kid)
-            per_kernel.setdefault(name, []).append(t.elapsed_ms(i))
-    kernels = {n: {"launches": len(v), "avg_ms": statistics.mean(v),
-                   "share": sum(v) / sum(kstep_ms)} for n, v in per_kernel.items()}
-    dom = max(per_kernel, key=lambda n: sum(per_kernel[n]))
-    peaks = load_peaks()
-    hbm = float(peaks["hbm_gbs"])
-    ab = algorithmic_bytes(dom, x, c)
-    dom_ms = statistics.mean(per_kernel[dom])
-    achieved = ab / (dom_ms * 1e-3) / 1e9 if ab else None
-    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
-                "unit": "GB/s", "frac": achieved / hbm if achieved else None,
-                "traffic": traffic_record(dom, args.workload),
-                "algorithmic_bytes_per_launch": ab, "avg_launch_ms": dom_ms,
-                "timing": "CUDA events around each launch on its stream, over a second "
-                          "pass of the same K steps",
-                "peak_source": peaks["source"] + " (hbm_gbs, copy bandwidth)"}
-    # the state scan alone (serial or segment output pass), whichever ran
-    scan = next((n for n in ("tc_chain_serial", "tc_chain_segment_out", "tc_gla_serial",
-                             "tc_gla_segment_out", "simt_scan_serial", "simt_scan_segment_out")
-                 if n in per_kernel), None)
-    scan_roofline = None
-    if scan is not None:
-        sb = algorithmic_bytes(scan, x, c)
-        s_ms = statistics.mean(per_kernel[scan])
-        scan_roofline = {"kernel": scan, "bound": "hbm", "achieved": sb / (s_ms * 1e-3) / 1e9,
-                         "peak": hbm, "unit": "GB/s",
-                         "frac": sb / (s_ms * 1e-3) / 1e9 / hbm,
-                         "traffic": traffic_record(scan, args.workload),
-                         "algorithmic_bytes_per_launch": sb, "avg_launch_ms": s_ms}
-    call_bytes = algorithmic_bytes("call", x, c)
-    call_roofline = {"achieved": call_bytes / (ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
-                     "frac": call_bytes / (ms * 1e-3) / 1e9 / hbm,
-                     "algorithmic_bytes": call_bytes}
+    clocks = m.clocks
+    ms = max_over_ranks(m.ms, world)
+    roof = rooflines(x, c, m, hbm, args.workload)
+    roofline = roof.get("roofline")
+    if roofline is not None:
+        roofline["timing"] = ("CUDA events around each launch on its stream, over a second "
+                              "pass of the same K steps")
+        roofline["peak_source"] = peaks["source"] + " (hbm_gbs, copy bandwidth)"
+    call_roofline = dict(roof["call_roofline"])
+    call_roofline.update(achieved=roof["call_roofline"]["algorithmic_bytes"] / (ms * 1e-3) / 1e9,
+                         frac=roof["call_roofline"]["algorithmic_bytes"] / (ms * 1e-3) / 1e9 / hbm)
+    kernels = m.kernels()
+    launches = m.launches
+    step_ms = m.step_ms
 
     e2e = None
     if not args.no_e2e:
         pin = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()}
+        o, ht = m.outputs()
         o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         ht_h = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
         hargs = (pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"])
@@ -625,6 +780,27 @@ def run_gdr(args):
         e2e = {"value": world * c["tokens"] / (e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "steps": ke, "api": "gdr_chunk_fwd_host (pinned host buffers)"}
+        del pin, o_h, ht_h
+
+    configs = None
+    if rank == 0 and not args.no_configs and not args.force_path and args.segments == 0:
+        configs = {}
+        del m
+        torch.cuda.empty_cache()
+        for name in CONFIG_WORKLOADS:
+            if name == args.workload:
+                configs[name] = {"plan": plan, "tokens": c["tokens"], "ms_per_call": ms,
+                                 "tokens_per_s": c["tokens"] / (ms * 1e-3),
+                                 "token_heads_per_s": c["token_heads"] / (ms * 1e-3),
+                                 "kernels": kernels, **roof, "headline": True}
+                if name in SPLIT_SWEEPS:
+                    add_split_sweep(configs[name], pkg, x, dev, min(K, 20), flush,
+                                    plan["n_segments"], SPLIT_SWEEPS[name])
+                continue
+            _, cm, rec = config_record(pkg, name, dev, min(K, 20), flush, hbm)
+            configs[name] = rec
+            del cm
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -638,17 +814,20 @@ def run_gdr(args):
                 "dtype": "f32" if plan["path"] == 1 else "bf16",
                 "data": "synthetic (seeded; shapes and distributions of the workload)",
                 "config": config_of(args, x, plan),
-                "roofline": roofline, "scan_roofline": scan_roofline,
+                "roofline": roofline, "scan_roofline": roof.get("scan_roofline"),
                 "call_roofline": call_roofline,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "kernels": kernels, "clocks": clocks,
                 "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
                             "p10": sorted(step_ms)[len(step_ms) // 10],
-                            "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]}}
+                            "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
+                "configs": configs}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
 
 
 def run_decode(args):
