@@ -692,8 +692,10 @@ def add_split_sweep(rec, pkg, x, dev, steps, flush, plan_s, counts_):
 
 
 # split counts swept per configuration (the plan's count is always added)
+# (128 segments of the beta-free batch: one chunk each, the chunk-parallel
+# producer dataflow)
 SPLIT_SWEEPS = {"long_16k_bf16": (1, 2, 4, 8, 16), "stress_64k_h8_bf16": (1, 4, 8, 16),
-                "stress_64k_h1_bf16": (1, 16, 32, 64)}
+                "stress_64k_h1_bf16": (1, 16, 32, 64), "gla_k256_v512_bf16": (1, 4, 16, 128)}
 
 
 def rel_l2(a, ref):

@@ -75,6 +75,20 @@ __global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Wo
     if (nseg > 0) load_m(sM0, sbase, &bars[0]);
     if (tid == 0 && nseg > 1) mbar_arrive_expect_tx(&bars[1], mbytes);
     __syncthreads();
+    // c_s is loaded one step ahead (a global load's latency would otherwise
+    // sit on every step's critical path)
+    auto load_c = [&](int s, float4 (&cv)[2]) {
+        cv[0] = cv[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ms == 0 && active && s < nseg) {
+            const int64_t hrow = (sbase + s) * K;
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                cv[i] = __ldg(reinterpret_cast<const float4 *>(ws.segC + (hrow + r0 + i) * V +
+                                                               col0 + c0));
+        }
+    };
+    float4 cnext[2];
+    load_c(0, cnext);
     for (int s = 0; s < nseg; ++s) {
         const float *sM = (s & 1) ? sM1 : sM0;
         const float *cur = (s & 1) ? sH1 : sH0;
@@ -87,17 +101,13 @@ __global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Wo
                 *reinterpret_cast<float4 *>(ws.segH + (hrow + r0 + i) * V + col0 + c0) =
                     *reinterpret_cast<const float4 *>(cur + (r0 + i) * CC + c0);
         }
-        float4 cv[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-        if (ms == 0 && active) {  // c_s, loaded early
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                cv[i] = __ldg(reinterpret_cast<const float4 *>(ws.segC + (hrow + r0 + i) * V +
-                                                               col0 + c0));
-        }
+        const float4 cv[2] = {cnext[0], cnext[1]};  // c_s
+        load_c(s + 1, cnext);
+        // every thread waits for the transition itself; whether all of them
+        // got it is agreed at the barrier after the partial sums
         const bool ok = mbar_wait(&bars[s & 1], (uint32_t)(s >> 1) & 1u, p.status);
-        if (__syncthreads_or(!ok)) return;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if (active) {
+        if (active && ok) {
 #pragma unroll 8
             for (int m = m0; m < m0 + mlen; ++m) {
                 const float2 a = *reinterpret_cast<const float2 *>(sM + m * K + r0);
@@ -116,7 +126,7 @@ __global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Wo
                         make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
             }
         }
-        __syncthreads();
+        if (__syncthreads_or(!ok)) return;
         if (ms == 0 && active) {
 #pragma unroll
             for (int i = 0; i < 2; ++i) {

@@ -344,7 +344,8 @@ int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_optio
         p.bv = bv;
     }
     if (n_segments < 0) return GDR_ERR_INVALID;
-    if (n_segments > kMaxSegments) return GDR_ERR_UNSUPPORTED;
+    if (n_segments > (beta_free ? kMaxSegmentsBetaFree : kMaxSegments))
+        return GDR_ERR_UNSUPPORTED;
     p.n_segments = n_segments == 0 ? auto_segments(d, beta_free, p.path, p.bv) : n_segments;
     *plan = p;
     return GDR_OK;

@@ -45,7 +45,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 constexpr int kChunk = 64;       // tokens per chunk
 constexpr int kMaxK = 256;       // largest key dim supported
 constexpr int kMaxV = 1024;      // largest value dim supported
-constexpr int kMaxSegments = 64; // largest segment count
+constexpr int kMaxSegments = 64; // largest segment count (delta rule, backward)
+// Largest segment count of the beta-free forward pass.  A count at or above
+// a sequence's chunk count gives every chunk its own segment: the
+// chunk-parallel producer dataflow of the ABC issue's "Proposed Dataflow"
+// (per-chunk FP32 contributions, an ordered scalar-decay scan, an output
+// pass from each chunk's boundary state).
+constexpr int kMaxSegmentsBetaFree = 4096;
 
 // Element strides of the token and head dimensions of a [tokens, H, D]
 // tensor whose last dimension is contiguous (tokens flatten B and T).

@@ -176,7 +176,14 @@ typedef struct gdr_options {
  *   cu_seqlens  NULL selects the dense layout.
  *   h0          NULL: zero initial state.   ht  NULL: final state not written.
  *   n_segments  0: plan chooses; 1: serial scan; S > 1: split every sequence
- *               into runs of ceil(chunks / S) whole chunks.
+ *               into runs of ceil(chunks / S) whole chunks.  At most 64 for
+ *               the delta rule; at most 4096 in the beta-free mode, where a
+ *               count at or above the chunk count gives every chunk its own
+ *               segment: the chunk-parallel producer dataflow of
+ *               flash-linear-attention issue #23 "Proposed Dataflow" (each
+ *               chunk's FP32 contribution computed in parallel, an ordered
+ *               scan applying the scalar decays, the output of every chunk
+ *               from its boundary state).
  * Returns GDR_OK or GDR_ERR_*.
  */
 int gdr_chunk_fwd(const gdr_dims *dims, const void *q, const void *k,

@@ -72,7 +72,12 @@ def test_argument_checks_reject_before_any_gpu_work(lib):
     assert _fwd(lib, api.make_dims(1, 128, 2, 64, 64, N=3), cu=None) == -1  # N>0 needs cu
     assert _fwd(lib, ok, cu=5) == -1                                # cu given, N == 0
     assert _fwd(lib, ok, n_segments=-1) == -1
-    assert _fwd(lib, ok, n_segments=1000) == -2
+    # at most 4096 segments in the beta-free mode (beta NULL, as here), 64
+    # for the delta rule (the plan query needs no pointers)
+    assert _fwd(lib, ok, n_segments=4097) == -2
+    with pytest.raises(pkg.GdrError):
+        pkg.gdr_plan_query(1, 128, 2, 64, 64, n_segments=65)
+    assert pkg.gdr_plan_query(1, 128, 2, 64, 64, beta_free=True, n_segments=4096)["n_segments"] == 4096
     bad_bv = api.gdr_options(0.0, 0, 48, None, 0, None)
     assert _fwd(lib, ok, opt=bad_bv) == -1
     bad_scale = api.gdr_options(float("nan"), 0, 0, None, 0, None)

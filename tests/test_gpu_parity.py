@@ -97,6 +97,17 @@ def test_beta_free_k128_v256_varlen(S, path):
           force_path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
+def test_beta_free_one_chunk_per_segment(path):
+    """n_segments at or above the chunk count: every chunk its own segment,
+    the chunk-parallel producer dataflow (per-chunk FP32 contributions, the
+    ordered scalar-decay scan, each chunk's output from its boundary
+    state)."""
+    w = synthetic.small(W["gla_k256_v512_bf16"], K=128, V=256, H=2, with_h0=True)
+    check(synthetic.make_inputs(w, lengths=[1, 64, 65, 700, 0, 300]), n_segments=4096,
+          force_path=path)
+
+
 def many_lengths(n, hi, seed):
     """Seeded sequence lengths in [0, hi], zeros included."""
     g = torch.Generator().manual_seed(seed)

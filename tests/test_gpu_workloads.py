@@ -49,7 +49,7 @@ def test_stress_64k_h1(S):
     check("stress_64k_h1_bf16", n_segments=S)
 
 
-@pytest.mark.parametrize("S", [0, 1, 8])
+@pytest.mark.parametrize("S", [0, 1, 8, 128])
 def test_gla_k256_v512(S):
     check("gla_k256_v512_bf16", pairs=[(0, 0), (1, 3)], n_segments=S)
 
