@@ -45,6 +45,7 @@ METRIC = "tokens/s and ms per gdr_chunk_fwd call on 1 GB300; % of roofline"
 METRIC_BWD = "tokens/s and ms per gdr_chunk_bwd call on 1 GB300; % of roofline"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "stress_64k_h8_bf16"
+DEFAULT_WORKLOAD_BWD = "wide_varlen_bf16"  # the backward's headline: the wide varlen batch
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -55,7 +56,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gdr", "reference"], default="gdr")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=None,
+                    help=f"default {DEFAULT_WORKLOAD} ({DEFAULT_WORKLOAD_BWD} with --pass bwd)")
     ap.add_argument("--segments", type=int, default=0)
     ap.add_argument("--force-path", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -65,7 +67,10 @@ def parse_args():
                     help="skip the per-configuration sub-records")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
                     help="bwd times gdr_chunk_bwd (the backward pass) instead")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.workload is None:
+        args.workload = DEFAULT_WORKLOAD_BWD if args.which == "bwd" else DEFAULT_WORKLOAD
+    return args
 
 
 # ----------------------------------------------------------------------------
@@ -275,6 +280,14 @@ def bwd_algorithmic(kernel, x, c):
         fma = ch * (L * L * V / 2 + L * L * K)
         if delta:
             fma += ch * (1.5 * L * L * V + 2.5 * L * L * K + L ** 3 / 2)
+    elif kernel == "tc_prep":  # the forward's preparation, plus G for the backward
+        return algorithmic_bytes(kernel, x, c) + ch * L * f32, None
+    elif kernel == "tc_chain_recompute":  # W^T, U^T, vectors, k read; h_pre, v_new written
+        return (ch * (2 * 16384 + 272) + th * K * es + ch * K * V * f32 + ch * L * V * f32,
+                None)
+    elif kernel == "tc_bwd_scan":  # W^T, Q~, P, vectors, k, dO read; E, dV' written
+        return (ch * (2 * 16384 + 8192 + 272) + th * (K + V) * es + ch * K * V * f32
+                + ch * L * V * f32 + 2 * st, None)
     elif kernel == "simt_prep":
         b = algorithmic_bytes(kernel, x, c)
         fma = ch * ((L * L * K / 2 + L ** 3 / 6 + L * L * (K + V) / 2) if delta else 0)
@@ -971,7 +984,8 @@ def run_bwd(args):
                 dbeta=None if d["beta"] is None else torch.empty_like(d["beta"]),
                 dh0=torch.empty(x["N"], x["H"], x["K"], x["V"], dtype=torch.float32, device=dev))
     args_t = (d["q"], d["k"], d["v"], d["g"], d["beta"], do)
-    kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], dht=dht, n_segments=args.segments, **outs)
+    kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], dht=dht, n_segments=args.segments,
+              force_path=args.force_path, **outs)
     c = counts(x)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)

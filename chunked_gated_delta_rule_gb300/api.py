@@ -294,12 +294,14 @@ def gdr_chunk_fwd(q, k, v, g, beta=None, cu_seqlens=None, h0=None, *, n_segments
 def gdr_chunk_bwd(q, k, v, g, beta, do, cu_seqlens=None, h0=None, dht=None, *, n_segments=0,
                   state_layout="kv", want_dh0=True, scale=0.0, workspace=None, status=None,
                   dq=None, dk=None, dv=None, dg=None, dbeta=None, dh0=None, stream=None,
-                  timer=None):
+                  timer=None, force_path=0, grid_limit=0):
     """Backward pass on CUDA tensors: the gradients of ``<do, o> + <dht, ht>``
     for the forward pass on the same inputs.  Returns ``(dq, dk, dv, dg,
     dbeta, dh0)``: dq, dk, dv in the input dtype, the rest float32; ``dbeta``
     is None in the beta-free mode and ``dh0`` None unless ``want_dh0``.  Work
-    is enqueued on ``stream`` (default: torch's current stream)."""
+    is enqueued on ``stream`` (default: torch's current stream).
+    ``force_path`` 1 takes the CUDA-core route (FP32 arithmetic), 2 the
+    tensor-core route (BF16, K = V = 128, delta rule, serial), 0 the plan's."""
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":
@@ -330,10 +332,11 @@ def gdr_chunk_bwd(q, k, v, g, beta, do, cu_seqlens=None, h0=None, dht=None, *, n
                         ("dg", dg, torch.float32), ("dbeta", dbeta, torch.float32),
                         ("dh0", dh0, torch.float32)):
         _check(name, t, dt, dev)
-    opt = gdr_options(float(scale), 0, 0,
+    opt = gdr_options(float(scale), int(force_path), 0,
                       None if workspace is None else workspace.data_ptr(),
                       0 if workspace is None else workspace.numel() * workspace.element_size(),
                       None if status is None else status.data_ptr())
+    opt.grid_limit = int(grid_limit)
     if timer is not None:
         opt.events = ctypes.cast(timer._handles, ctypes.c_void_p)
         opt.max_launches = timer.max

@@ -389,6 +389,7 @@ int plan_for_call(const gdr_dims &d, bool beta_free, int n_segments, const gdr_o
 WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int path) {
     const bool delta = !beta_free;
     const bool simt = path == 1;
+    const bool recompute = path == 3;  // the tensor-core backward's recompute
     const int64_t mc = max_chunks_of(d);
     const int64_t ns = n_seqs(d);
     const size_t H = (size_t)d.H, K = (size_t)d.K, V = (size_t)d.V;
@@ -404,17 +405,18 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     L.off_seq0 = take(sizeof(int32_t) * (size_t)(ns + 1));
     L.off_nchunks = take(sizeof(int32_t) * 4);
     L.off_order = take(sizeof(int32_t) * (size_t)ns);
-    L.off_G = take(simt ? sizeof(float) * (size_t)mc * H * kChunk : 0);
+    L.off_G = take(simt || recompute ? sizeof(float) * (size_t)mc * H * kChunk : 0);
     L.off_W = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
     L.off_U = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
-    L.off_hpre = take(simt ? sizeof(float) * (size_t)mc * H * K * V : 0);
-    L.off_vnew = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
+    L.off_hpre = take(simt || recompute ? sizeof(float) * (size_t)mc * H * K * V : 0);
+    L.off_vnew = take((simt || recompute) && delta ? sizeof(float) * (size_t)mc * H * kChunk * V
+                                                   : 0);
     const size_t segs = S > 1 ? (size_t)ns * H * (size_t)S : 0;
     L.off_segM = take(delta ? sizeof(float) * segs * K * K : 0);
     L.off_segC = take(sizeof(float) * segs * K * V);
     L.off_segH = take(sizeof(float) * segs * K * V);
     L.off_segD = take(delta ? 0 : sizeof(float) * segs);
-    L.off_rec = take(simt || !delta ? 0 : (size_t)mc * H * 74752u);
+    L.off_rec = take(simt || !delta ? 0 : (size_t)mc * H * 74752u);  // paths 2 and 3
     L.total = off;
     return L;
 }
@@ -449,9 +451,9 @@ struct BwdLayout {
         off_segMb, total;
 };
 
-BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments) {
+BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments, bool tc_route) {
     BwdLayout B{};
-    B.fwd = workspace_layout(d, beta_free, n_segments, 1);
+    B.fwd = workspace_layout(d, beta_free, n_segments, tc_route ? 3 : 1);
     size_t off = B.fwd.total;
     auto take = [&](size_t bytes) {
         const size_t at = off;
@@ -555,11 +557,19 @@ int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStre
     return GDR_OK;
 }
 
-// Backward: the forward recompute of the CUDA-core path (serial scan: the
-// state before each chunk and V'), then the backward kernels.
+// Backward: the forward recompute (the state before each chunk and V'),
+// then the backward kernels.  Route 2: the tensor-core preparation (records,
+// and G) and the serial chain in its recompute mode, the reverse scan on the
+// tensor cores; route 1: the CUDA-core forward and reverse scans.
 int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw, int bv,
-            cudaStream_t st, LaunchRecorder &rec) {
+            int route, cudaStream_t st, LaunchRecorder &rec) {
     GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
+    if (route == 2) {
+        GDR_LAUNCH(rec, kKTcPrep, tc_prep(p, ws, st));
+        GDR_LAUNCH(rec, kKTcRecompute, tc_chain(p, ws, 3, st));
+        GDR_TRY(simt_bwd(p, ws, a, bw, true, st, rec));
+        return GDR_OK;
+    }
     GDR_LAUNCH(rec, kKPrep, simt_prep(p, ws, st));
     if (ws.n_segments <= 1) {
         GDR_LAUNCH(rec, kKScanSerial, simt_scan(p, ws, 0, bv, st));
@@ -573,7 +583,7 @@ int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs
             GDR_LAUNCH(rec, kKCompose, simt_compose(p, ws, bv, st));
         GDR_LAUNCH(rec, kKScanSegOut, simt_scan(p, ws, 2, bv, st));
     }
-    GDR_TRY(simt_bwd(p, ws, a, bw, st, rec));
+    GDR_TRY(simt_bwd(p, ws, a, bw, false, st, rec));
     return GDR_OK;
 }
 
@@ -621,6 +631,8 @@ const char *gdr_kernel_name(int id) {
     case kKBwdMaps: return "bwd_maps";
     case kKConvertIn: return "convert_f16_to_bf16";
     case kKConvertOut: return "convert_bf16_to_f16";
+    case kKTcRecompute: return "tc_chain_recompute";
+    case kKTcBwdScan: return "tc_bwd_scan";
     default: return "?";
     }
 }
@@ -793,22 +805,38 @@ int gdr_chunk_fwd(const gdr_dims *dims, const void *q, const void *k, const void
                             nullptr, stream);
 }
 
-// The backward's plan: the CUDA-core path's value tile for the forward
-// recompute (32 columns on the wide varlen batch: its scan 0.98 ms at 64,
-// 0.74 ms at 32) and its segment rule unless the caller fixes the count.
-int bwd_plan(const gdr_dims &d, bool beta_free, int n_segments, int *bv, int *S) {
+// The backward's plan.  Route 2, the tensor-core route (the tensor-core
+// forward recompute and reverse scan; BF16 operands, see gdr.h), for BF16
+// inputs with K = V = 128 and the delta rule, whose reverse scan runs
+// serially: unless the caller asks for a segment split, or the serial chain
+// would be long with few chains beside it (a 64K-token sequence with 1 or 8
+// heads: the CUDA-core route's split is faster there).  Route 1, the
+// CUDA-core route (FP32 arithmetic), otherwise, with the CUDA-core path's
+// value tile (32 columns on the wide varlen batch: its scan 0.98 ms at 64,
+// 0.74 ms at 32) and segment rule unless the caller fixes the count.
+// force_path 1 or 2 picks a route.
+int bwd_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_options *opt,
+             int *route, int *bv, int *S) {
     if (n_segments < 0) return GDR_ERR_INVALID;
     if (n_segments > kMaxSegments) return GDR_ERR_UNSUPPORTED;
+    const int force = opt ? opt->force_path : 0;
+    if (force < 0 || force > 2) return GDR_ERR_INVALID;
+    const bool tc_ok = d.dtype == GDR_BF16 && d.K == 128 && d.V == 128 && !beta_free &&
+                       n_segments <= 1;
+    if (force == 2 && !tc_ok) return GDR_ERR_UNSUPPORTED;
+    const ChunkStats cs = chunk_stats(d);
+    const bool long_few = cs.longest > 256 && n_seqs(d) * d.H < device_sms() / 4;
+    *route = force ? force : (tc_ok && !long_few ? 2 : 1);
     *bv = pick_bv(d);
-    *S = n_segments > 0 ? n_segments : auto_segments(d, beta_free, 1, *bv);
+    *S = *route == 2 ? 1 : n_segments > 0 ? n_segments : auto_segments(d, beta_free, 1, *bv);
     return GDR_OK;
 }
 
 size_t gdr_bwd_workspace_size(const gdr_dims *dims, int beta_free, int n_segments) {
     if (validate_dims(dims) != GDR_OK) return 0;
-    int bv = 0, S = 1;
-    if (bwd_plan(*dims, beta_free != 0, n_segments, &bv, &S) != GDR_OK) return 0;
-    return bwd_layout(*dims, beta_free != 0, S).total;
+    int route = 1, bv = 0, S = 1;
+    if (bwd_plan(*dims, beta_free != 0, n_segments, nullptr, &route, &bv, &S) != GDR_OK) return 0;
+    return bwd_layout(*dims, beta_free != 0, S, route == 2).total;
 }
 
 int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void *v,
@@ -822,11 +850,22 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
     if ((beta != nullptr) != (dbeta != nullptr)) return GDR_ERR_INVALID;
     if ((cu_seqlens != nullptr) != is_varlen(*dims)) return GDR_ERR_INVALID;
     if (opt && !(opt->scale >= 0.f)) return GDR_ERR_INVALID;  // rejects NaN too
-    if (opt && (opt->force_path != 0 || opt->force_bv != 0)) return GDR_ERR_INVALID;
+    if (opt && (opt->force_bv != 0 || opt->grid_limit < 0)) return GDR_ERR_INVALID;
     const bool beta_free = beta == nullptr;
-    int bv_rec = 0, S = 1;
-    rc = bwd_plan(*dims, beta_free, n_segments, &bv_rec, &S);
+    int route = 1, bv_rec = 0, S = 1;
+    rc = bwd_plan(*dims, beta_free, n_segments, opt, &route, &bv_rec, &S);
     if (rc != GDR_OK) return rc;
+    if (route == 2) {  // TMA reads q, k, v and dO: aligned rows
+        const bool aligned = rows_aligned16(q, stride_of(dims->q_stride, dims->H, dims->K), 2) &&
+                             rows_aligned16(k, stride_of(dims->k_stride, dims->H, dims->K), 2) &&
+                             rows_aligned16(v, stride_of(dims->v_stride, dims->H, dims->V), 2) &&
+                             rows_aligned16(dout, dense_stride(dims->H, dims->V), 2);
+        if (!aligned) {
+            if (opt && opt->force_path == 2) return GDR_ERR_INVALID;
+            route = 1;
+            S = n_segments > 0 ? n_segments : auto_segments(*dims, beta_free, 1, bv_rec);
+        }
+    }
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     Problem p{};
@@ -841,9 +880,10 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
     p.dtype = dims->dtype;
     p.scale = (opt && opt->scale > 0.f) ? opt->scale : 1.0f / std::sqrt((float)dims->K);
     p.status = opt ? opt->status : nullptr;
+    p.grid_limit = opt ? opt->grid_limit : 0;
     if (p.N == 0) return GDR_OK;
 
-    const BwdLayout B = bwd_layout(*dims, beta_free, S);
+    const BwdLayout B = bwd_layout(*dims, beta_free, S, route == 2);
     void *base = nullptr;
     bool owned = false;
     if (opt && opt->workspace) {
@@ -854,7 +894,8 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
         if (lib_malloc(&base, B.total, st) != cudaSuccess) return GDR_ERR_CUDA;
         owned = true;
     }
-    const Workspace ws = carve_workspace(base, B.fwd, S);
+    Workspace ws = carve_workspace(base, B.fwd, S);
+    ws.bwd_tc = route == 2;
     const BwdWs bw = carve_bwd(base, B);
     BwdArgs a{};
     a.dout = dout; a.dht = dht; a.dq = dq; a.dk = dk; a.dv = dv;
@@ -867,7 +908,7 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
         rec.ids = opt->launch_ids;
         if (!opt->events && opt->launch_ids) rec.max_launches = opt->max_launches;
     }
-    rc = run_bwd(p, ws, a, bw, bv_rec, st, rec);
+    rc = run_bwd(p, ws, a, bw, bv_rec, route, st, rec);
     if (opt && opt->n_launches) *opt->n_launches = rec.count;
     if (owned) {
         if (cudaFreeAsync(base, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;

@@ -157,6 +157,8 @@ struct Workspace {
                           // tensor-core path (tc_chunk.cuh)
     int64_t max_chunks;
     int n_segments;       // S (1 = serial)
+    int bwd_tc;           // the tensor-core backward's forward recompute: tc_prep
+                          // also stores G, the chain also h_pre and v_new (FP32)
 };
 
 // Backward pass: the caller's gradient tensors (dq, dk, dv in the input

@@ -17,7 +17,9 @@ struct WorkspaceLayout {
 };
 
 // path 1: CUDA-core path (chunk table, G, W, U, h_pre, v_new, segments);
-// path 2: tensor-core path (chunk table and segment summaries only).
+// path 2: tensor-core path (chunk table, records and segment summaries);
+// path 3: the tensor-core backward's forward recompute (chunk table, G,
+// h_pre, v_new and the records).
 WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int n_segments, int path);
 Workspace carve_workspace(void *base, const WorkspaceLayout &L, int n_segments);
 
@@ -55,6 +57,8 @@ enum KernelId {
     kKBwdMaps = 22,
     kKConvertIn = 23,
     kKConvertOut = 24,
+    kKTcRecompute = 25,
+    kKTcBwdScan = 26,
     kKNumIds
 };
 
@@ -94,9 +98,15 @@ cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st);
 // tensor-core path.
 cudaError_t convert_f16_to_bf16(const void *src, void *dst, int64_t n, cudaStream_t st);
 cudaError_t convert_bf16_to_f16(const void *src, void *dst, int64_t n, cudaStream_t st);
-// Backward pass after the serial forward recompute (G, W, hpre, vnew in ws).
+// Backward pass after the forward recompute (G, hpre, vnew in ws; W too for
+// the CUDA-core reverse scan).  tc_scan: the reverse scan runs on the tensor
+// cores (tc_bwd_scan, from the records of the tensor-core recompute; serial).
 cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
-                     cudaStream_t st, LaunchRecorder &rec);
+                     bool tc_scan, cudaStream_t st, LaunchRecorder &rec);
+// The reverse state-gradient scan on the tensor cores (BF16, K = V = 128,
+// delta rule, serial): E at every chunk's end into dhend, dV' into dvn, dh0.
+cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, float *dhend, float *dvn,
+                        const float *dht, float *dh0, const void *dout, cudaStream_t st);
 // Composition for the delta rule with K <= 128 and V % 32 == 0 (both paths):
 // bulk-copied transposed transitions, 32 value columns per CTA.
 bool compose_mt_supported(const Problem &p);
@@ -113,7 +123,8 @@ cudaError_t tc_gla(const Problem &p, const Workspace &ws, int mode, cudaStream_t
 // A2-A5 for every (chunk, head) in parallel -> per-chunk records.
 cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st);
 // mode 0: serial scan + output (h0 -> ht); 1: segment pre-scan (c_s and M_s
-// chains); 2: segment output pass from the composed segment states.
+// chains); 2: segment output pass from the composed segment states; 3: the
+// backward's recompute (serial from h0, h_pre and v_new stored, no output).
 cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream_t st);
 // The per-token recurrence from (and back into) rows of a state pool.
 cudaError_t recurrent_fwd(const Problem &p, float *state, int64_t n_states,

@@ -754,7 +754,7 @@ cudaError_t set_smem_bwd(F *f, size_t bytes) {
 
 template <typename Tin>
 cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
-                       cudaStream_t st, LaunchRecorder &rec) {
+                       bool tc_scan, cudaStream_t st, LaunchRecorder &rec) {
     const bool delta = p.beta != nullptr;
     const unsigned mc = (unsigned)ws.max_chunks, H = (unsigned)p.H;
     const int K = (int)p.K, V = (int)p.V;
@@ -788,7 +788,13 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
             }
             return cudaGetLastError();
         };
-        if (S <= 1) {
+        if (tc_scan) {
+            if ((e = rec.begin(kKTcBwdScan)) != cudaSuccess) return e;
+            if ((e = tc_bwd_scan(p, ws, bw.dhend, bw.dvn, a.dht, a.dh0, a.dout, st)) !=
+                cudaSuccess)
+                return e;
+            if ((e = rec.end()) != cudaSuccess) return e;
+        } else if (S <= 1) {
             if ((e = rec.begin(kKBwdScan)) != cudaSuccess) return e;
             if ((e = launch(0)) != cudaSuccess) return e;
             if ((e = rec.end()) != cudaSuccess) return e;
@@ -844,10 +850,10 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
 }  // namespace
 
 cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
-                     cudaStream_t st, LaunchRecorder &rec) {
-    if (p.dtype == GDR_BF16) return launch_bwd<__nv_bfloat16>(p, ws, a, bw, st, rec);
-    if (p.dtype == GDR_F16) return launch_bwd<__half>(p, ws, a, bw, st, rec);
-    return launch_bwd<float>(p, ws, a, bw, st, rec);
+                     bool tc_scan, cudaStream_t st, LaunchRecorder &rec) {
+    if (p.dtype == GDR_BF16) return launch_bwd<__nv_bfloat16>(p, ws, a, bw, tc_scan, st, rec);
+    if (p.dtype == GDR_F16) return launch_bwd<__half>(p, ws, a, bw, false, st, rec);
+    return launch_bwd<float>(p, ws, a, bw, false, st, rec);
 }
 
 }  // namespace gdr

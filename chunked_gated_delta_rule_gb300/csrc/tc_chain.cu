@@ -52,7 +52,10 @@ namespace {
 
 using namespace tc;
 
-enum TcMode { kModeSerial = 0, kModePre = 1, kModeSegOut = 2 };
+// kModeRecompute: the serial scan of the tensor-core backward's forward
+// recompute: no output, and per chunk the FP32 state before the chunk and
+// v_new go to the workspace (h_pre, v_new) for the backward's kernels.
+enum TcMode { kModeSerial = 0, kModePre = 1, kModeSegOut = 2, kModeRecompute = 3 };
 
 struct TcArgs {
     Problem p;
@@ -133,7 +136,8 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant__ TcArgs args) {
     const Problem &p = args.p;
     const Workspace &ws = args.ws;
-    constexpr bool kOut = MODE != kModePre;
+    constexpr bool kOut = MODE == kModeSerial || MODE == kModeSegOut;
+    constexpr bool kFromH0 = MODE == kModeSerial || MODE == kModeRecompute;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
     const int row = 32 * (warp & 3) + lane_id;  // TMEM lane = matrix row
     const uint32_t lane = (uint32_t)(32 * (warp & 3)) << 16;
     const int H = (int)p.H;
-    const int S = MODE == kModeSerial ? 1 : ws.n_segments;
+    const int S = kFromH0 ? 1 : ws.n_segments;
 
     auto wait = [&](int b, uint32_t parity) -> bool {
         return mbar_wait_or_abort(&bars[b], parity & 1u, p.status, s_abort);
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
         if (lane_id == 0) {
             const int kinds = MODE == kModePre ? 2 : 1;
             const int total = (int)(p.N * S * H * kinds);
-            int32_t *counter = ws.n_chunks + 1 + MODE;
+            int32_t *counter = ws.n_chunks + 1 + (MODE == kModeRecompute ? 0 : MODE);
             int issued = 0;
             for (int posted = 0;; ++posted) {
                 ChainDesc c{};
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                     const int nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
                     c.s0 = 0;
                     c.s1 = nc;
-                    if (MODE != kModeSerial) {
+                    if (!kFromH0) {
                         const int per = (nc + S - 1) / S;
                         c.s0 = c.s * per;
                         c.s1 = min(nc, c.s0 + per);
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         for (int kk = 0; kk < 64; ++kk) {
                             const int key = 64 * hq + kk;
                             float v = 0.f;
-                            if (MODE == kModeSerial) {
+                            if (kFromH0) {
                                 if (p.h0) v = p.h0[st_base + (p.state_vk ? key : key * kD)];
                             } else if (MODE == kModeSegOut) {
                                 v = ws.segH[(seg_base * kD + key) * kD + row];
@@ -377,10 +381,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 };
                 // h_pre -> BF16 mirror (the first product's A operand): the
                 // chain's critical path, so it goes first
+                // the recompute's FP32 state before the chunk, [key][v]
+                float *hpre = MODE == kModeRecompute
+                                  ? ws.hpre + ((int64_t)(C.c_begin + cc) * H + h) * kD * kD + row
+                                  : nullptr;
 #pragma unroll 1
                 for (int hq = 0; hq < 2; ++hq) {
                     uint32_t r0[32], r1[32];
                     state_half(hq, r0, r1);
+                    if (MODE == kModeRecompute) {
+#pragma unroll
+                        for (int kk = 0; kk < 32; ++kk) {
+                            hpre[(64 * hq + kk) * kD] = __uint_as_float(r0[kk]);
+                            hpre[(64 * hq + 32 + kk) * kD] = __uint_as_float(r1[kk]);
+                        }
+                    }
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
                         float x[8], y[8];
@@ -434,6 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         }
 #pragma unroll
                         for (int i = 0; i < 32; ++i) u[i] -= __uint_as_float(hh ? w1[i] : w0[i]);
+                        if (MODE == kModeRecompute) {  // FP32 v_new, [t][v]
+                            float *vn = ws.vnew + (((int64_t)(C.c_begin + cc) * H + h) * kChunk +
+                                                   32 * hh) * kD + row;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) vn[i * kD] = u[i];
+                        }
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8)
                             st_bf16x8(sm + kOffVn + sw128_off(row, 32 * hh + 8 * c8, 128),
@@ -456,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 }
                 continue;
             }
-            if ((MODE != kModeSegOut) && (MODE != kModeSerial || p.ht)) {
+            if (MODE == kModePre || (MODE == kModeSerial && p.ht)) {
                 tc_fence_after();
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -614,16 +635,21 @@ cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream
     args.ws = ws;
     const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
     const uint64_t H = (uint64_t)p.H;
-    if (!make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&args.to, p.o, kD, H, rows, p.so.h * 2, p.so.t * 2, 64, 1, 64))
+    if (!make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
-    const int S = mode == 0 ? 1 : ws.n_segments;
+    if (mode == 3) {
+        args.to = args.tk;  // the recompute writes no output
+    } else if (!make_tmap_bf16_3d(&args.to, p.o, kD, H, rows, p.so.h * 2, p.so.t * 2, 64, 1, 64)) {
+        return cudaErrorInvalidValue;
+    }
+    const int S = (mode == 0 || mode == 3) ? 1 : ws.n_segments;
     const int64_t chains = p.N * S * p.H * (mode == 1 ? 2 : 1);
     dim3 grid((unsigned)persistent_grid(p, chains, 1));
     switch (mode) {
     case 0: return launch_chain<kModeSerial>(args, grid, st);
     case 1: return launch_chain<kModePre>(args, grid, st);
     case 2: return launch_chain<kModeSegOut>(args, grid, st);
+    case 3: return launch_chain<kModeRecompute>(args, grid, st);
     }
     return cudaErrorInvalidValue;
 }

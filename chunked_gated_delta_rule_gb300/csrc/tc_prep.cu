@@ -165,7 +165,13 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
         float *vec = reinterpret_cast<float *>(sm + kOffVec + (it & 1) * 1600);
         const float *sG = vec, *sBeta = vec + 64, *sBG = vec + 128, *sDec = vec + 192,
                     *sGam = vec + 256, *sEP = vec + 320, *sScal = vec + 384;
-        if (warp == 0) gate_vectors(vec, g2, b2, len, lane_id);
+        if (warp == 0) {
+            gate_vectors(vec, g2, b2, len, lane_id);
+            if (ws.bwd_tc) {  // G for the backward's per-chunk kernels
+                ws.G[(int64_t)item * kChunk + lane_id] = vec[lane_id];
+                ws.G[(int64_t)item * kChunk + 32 + lane_id] = vec[32 + lane_id];
+            }
+        }
         bool ok = mbar_wait(&bars[0], it & 1u, p.status);
         if (__syncthreads_or(!ok)) break;
         if (len < 64) {  // rows past the sequence end belong to the next one: zero them

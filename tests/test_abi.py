@@ -120,7 +120,10 @@ def test_backward_argument_checks_reject_before_any_gpu_work(lib):
     assert _bwd(lib, ok, beta=None, dbeta=1) == -1
     assert _bwd(lib, api.make_dims(1, 128, 2, 60, 64)) == -2
     assert _bwd(lib, api.make_dims(1, 128, 2, 64, 64, N=3)) == -1  # varlen needs cu
-    assert _bwd(lib, ok, opt=api.gdr_options(0.0, 2, 0, None, 0, None)) == -1  # no forced plan
+    # the tensor-core route takes BF16, K = V = 128, the delta rule; a route
+    # number past 2 is invalid
+    assert _bwd(lib, ok, opt=api.gdr_options(0.0, 2, 0, None, 0, None)) == -2
+    assert _bwd(lib, ok, opt=api.gdr_options(0.0, 3, 0, None, 0, None)) == -1
     assert _bwd(lib, ok, opt=api.gdr_options(float("nan"), 0, 0, None, 0, None)) == -1
     assert _bwd(lib, ok, n_segments=-1) == -1
     assert _bwd(lib, ok, n_segments=1000) == -2

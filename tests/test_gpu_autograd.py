@@ -1,6 +1,8 @@
 """The differentiable entry point (chunk_gated_delta_rule): torch autograd
 through the library's forward and backward passes, checked against the FP64
-oracle's gradients of the same loss (tolerances of test_gpu_bwd.py)."""
+oracle's gradients of the same loss (tolerances of test_gpu_bwd.py: BF16
+delta-rule inputs at K = V = 128 take the tensor-core route, 1e-2 for every
+gradient)."""
 import numpy as np
 import pytest
 import torch
@@ -24,7 +26,7 @@ def test_autograd_matches_oracle(case):
     if case == "bf16_varlen_h0":
         x = synthetic.make_inputs(synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True),
                                   lengths=[70, 5, 129])
-        want_state, tol = True, (6e-3, 1e-5)
+        want_state, tol = True, (1e-2, 1e-2)
     elif case == "f32_dense_no_state":
         x = synthetic.make_inputs(synthetic.small(W["tiny_dense_f32"], with_h0=False, B=2, T=150))
         want_state, tol = False, (1e-5, 1e-5)

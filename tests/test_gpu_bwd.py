@@ -9,6 +9,13 @@ dh0 are FP32 arithmetic on the exact BF16 values the oracle also reads, so
 they keep 1e-5.  FP16 inputs: dq, dk, dv rounded to FP16 once (2^-11), 2e-3;
 the rest 1e-5.  The oracle reads the inputs after rounding to the input
 dtype, so the comparison measures the kernels' arithmetic only.
+
+The tensor-core route (BF16, K = V = 128, delta rule, serial reverse scan;
+force_path=2, and the plan's choice for those shapes) computes with BF16
+operands in its forward recompute and reverse scan: every gradient is held
+to 1e-2, two sets of BF16 operand roundings of the kind the forward's 6e-3
+bar covers once.  The other tests here pin the CUDA-core route
+(force_path=1), whose bars are the FP32 ones above.
 """
 import numpy as np
 import pytest
@@ -24,7 +31,12 @@ NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
 RAGGED = [1, 63, 64, 65, 127, 128, 257, 7, 300, 0]
 
 
-def tols(x):
+TOL_TC = 1e-2  # every gradient of the tensor-core route
+
+
+def tols(x, route=1):
+    if route == 2:
+        return {name: TOL_TC for name in NAMES}
     rounded = {"f32": 1e-5, "bf16": 6e-3, "f16": 2e-3}[x["dtype"]]
     return {"dq": rounded, "dk": rounded, "dv": rounded, "dg": 1e-5, "dbeta": 1e-5, "dh0": 1e-5}
 
@@ -39,7 +51,10 @@ def grads_in(x, seed=7, with_dht=True):
 
 
 def run_bwd(x, do, dht, layout="kv", **kw):
+    """The backward on the GPU; the CUDA-core route unless force_path says
+    otherwise."""
     import chunked_gated_delta_rule_gb300 as pkg
+    kw.setdefault("force_path", 1)
     d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
     h0, dhtd = d["h0"], None if dht is None else dht.cuda()
     if layout == "vk":
@@ -60,7 +75,7 @@ def check(x, with_dht=True, layout="kv", pair_mask=None, **kw):
     out = run_bwd(x, do, dht, layout=layout, **kw)
     ref = oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], cu_seqlens=x["cu_seqlens"],
                           h0=x["h0"], do=do, dht=dht, pair_mask=pair_mask)
-    tol = tols(x)
+    tol = tols(x, kw.get("force_path", 1))
     errs = {}
     for name, a, r in zip(NAMES, out, ref):
         if r is None:
@@ -208,3 +223,53 @@ def test_split_with_layout_and_dtype_options(combo):
     if combo == "int64_seqlens":
         x = dict(x, cu_seqlens=x["cu_seqlens"].to(torch.int64))
     check(x, layout="vk" if combo == "vk_layout" else "kv", n_segments=4)
+
+
+# --------------------------------------------------------------------------
+# the tensor-core route
+# --------------------------------------------------------------------------
+def _bits(t):
+    return None if t is None else t.detach().contiguous().view(torch.uint8).cpu()
+
+
+def test_tc_route_varlen_ragged_empty_h0_dht():
+    w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True)
+    print(check(synthetic.make_inputs(w, lengths=RAGGED), force_path=2))
+
+
+def test_tc_route_without_dht_or_h0():
+    w = synthetic.small(W["wide_varlen_bf16"], H=3)
+    print(check(synthetic.make_inputs(w, lengths=[200, 64, 1, 129]), with_dht=False,
+                force_path=2))
+
+
+def test_tc_route_state_layout_vk_dense_batch():
+    w = synthetic.small(W["long_16k_bf16"], B=2, T=700, H=2, with_h0=True)
+    print(check(synthetic.make_inputs(w), layout="vk", force_path=2))
+
+
+@pytest.mark.parametrize("name", ["wide_varlen_bf16", "long_16k_bf16"])
+def test_tc_route_full_size_sampled_pairs(name):
+    x = synthetic.make_inputs(W[name])
+    n = x["N"] if x["cu_seqlens"] is not None else x["B"]
+    pairs = n * x["H"]
+    mask = np.zeros(pairs, dtype=bool)
+    mask[[0, pairs // 2, pairs - 1]] = True
+    print(check(x, pair_mask=mask, force_path=2))
+
+
+def test_tc_route_is_the_default_for_its_shapes_and_bits_do_not_depend_on_the_grid():
+    """BF16, K = V = 128, delta rule, serial: the plan takes the tensor-core
+    route; its gradients are the same bits at any grid of the persistent
+    kernels and from run to run."""
+    w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True)
+    x = synthetic.make_inputs(w, lengths=[300, 65, 7, 129])
+    do, dht = grads_in(x)
+    ref = run_bwd(x, do, dht, force_path=2)
+    for kw in (dict(force_path=0), dict(force_path=2, grid_limit=1),
+               dict(force_path=2, grid_limit=7), dict(force_path=2)):
+        out = run_bwd(x, do, dht, **kw)
+        for name, a, b in zip(NAMES, out, ref):
+            assert (a is None) == (b is None), name
+            if a is not None:
+                assert torch.equal(_bits(a), _bits(b)), (name, kw)
