@@ -280,8 +280,8 @@ def bwd_algorithmic(kernel, x, c):
         fma = ch * (L * L * V / 2 + L * L * K)
         if delta:
             fma += ch * (1.5 * L * L * V + 2.5 * L * L * K + L ** 3 / 2)
-    elif kernel == "tc_prep":  # the forward's preparation, plus G for the backward
-        return algorithmic_bytes(kernel, x, c) + ch * L * f32, None
+    elif kernel == "tc_prep":  # the forward's preparation, plus G, Kd, Mq, T for the backward
+        return algorithmic_bytes(kernel, x, c) + ch * L * f32 + 3 * ch * L * L * f32, None
     elif kernel == "tc_chain_recompute":  # W^T, U^T, vectors, k read; h_pre, v_new written
         return (ch * (2 * 16384 + 272) + th * K * es + ch * K * V * f32 + ch * L * V * f32,
                 None)

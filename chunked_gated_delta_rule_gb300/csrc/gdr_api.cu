@@ -895,8 +895,13 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
         owned = true;
     }
     Workspace ws = carve_workspace(base, B.fwd, S);
-    ws.bwd_tc = route == 2;
     const BwdWs bw = carve_bwd(base, B);
+    ws.bwd_tc = route == 2;
+    if (ws.bwd_tc) {
+        ws.bwd_Mq = bw.Mq;
+        ws.bwd_Kd = bw.Kd;
+        ws.bwd_Tm = bw.Tm;
+    }
     BwdArgs a{};
     a.dout = dout; a.dht = dht; a.dq = dq; a.dk = dk; a.dv = dv;
     a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;

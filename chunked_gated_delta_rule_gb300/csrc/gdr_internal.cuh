@@ -158,7 +158,9 @@ struct Workspace {
     int64_t max_chunks;
     int n_segments;       // S (1 = serial)
     int bwd_tc;           // the tensor-core backward's forward recompute: tc_prep
-                          // also stores G, the chain also h_pre and v_new (FP32)
+                          // also stores G, Mq, Kd and T, the chain also h_pre
+                          // and v_new (FP32)
+    float *bwd_Mq, *bwd_Kd, *bwd_Tm;  // [chunks][H][64][64], as BwdWs (bwd_tc)
 };
 
 // Backward pass: the caller's gradient tensors (dq, dk, dv in the input

@@ -759,8 +759,8 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
     const unsigned mc = (unsigned)ws.max_chunks, H = (unsigned)p.H;
     const int K = (int)p.K, V = (int)p.V;
     cudaError_t e;
-    // gram
-    {
+    // gram (the tensor-core route's preparation stored Mq, Kd and T already)
+    if (!tc_scan) {
         const size_t smem = sizeof(float) * (3 * kChunk * kLd + 2 * kChunk);
         if ((e = set_smem_bwd(k_bwd_gram<Tin>, smem)) != cudaSuccess) return e;
         if ((e = rec.begin(kKBwdGram)) != cudaSuccess) return e;

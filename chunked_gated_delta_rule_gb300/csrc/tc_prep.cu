@@ -83,6 +83,9 @@ __device__ __forceinline__ void scale_rows_in_place(uint8_t *a, const float *f, 
     }
 }
 
+// kBwd: the backward's recompute also stores G, Kd, Mq and T (a separate
+// instantiation, so that the forward's kernel carries none of it).
+template <bool kBwd>
 __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__ PrepArgs args) {
     const Problem &p = args.p;
     const Workspace &ws = args.ws;
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
                     *sGam = vec + 256, *sEP = vec + 320, *sScal = vec + 384;
         if (warp == 0) {
             gate_vectors(vec, g2, b2, len, lane_id);
-            if (ws.bwd_tc) {  // G for the backward's per-chunk kernels
+            if (kBwd) {  // G for the backward's per-chunk kernels
                 ws.G[(int64_t)item * kChunk + lane_id] = vec[lane_id];
                 ws.G[(int64_t)item * kChunk + 32 + lane_id] = vec[32 + lane_id];
             }
@@ -213,6 +216,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
             const int j0 = 32 * half;
             // A rows keep j < i (beta_i folded in); P rows keep j <= i.
             const int jlim = quad < 2 ? i : i + 1;
+            if (kBwd) {  // the backward's Kd = (K K^T * D, j < i), Mq = (Q K^T * D, j <= i)
+                float x[32];
+                if (sScal[2] != 0.f) {
+                    const float ri = sEP[i];
+#pragma unroll
+                    for (int u = 0; u < 32; ++u)
+                        x[u] = (j0 + u < jlim) ? f[u] * (ri * sDec[j0 + u]) : 0.f;
+                } else {
+                    const float gi = sG[i];
+#pragma unroll
+                    for (int u = 0; u < 32; ++u)
+                        x[u] = (j0 + u < jlim) ? f[u] * __expf(gi - sG[j0 + u]) : 0.f;
+                }
+                float4 *dst = reinterpret_cast<float4 *>(
+                    (quad < 2 ? ws.bwd_Kd : ws.bwd_Mq) + ((int64_t)item * kChunk + i) * kChunk + j0);
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    dst[c4] = make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
+            }
             const float rowf = quad < 2 ? sBeta[i] : p.scale;
             if (sScal[2] != 0.f) {  // e^{G_i - G_j} = e^{G_i - G_last} e^{G_last - G_j}
                 const float ri = rowf * sEP[i];
@@ -276,6 +298,14 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
                 const float4 a0 = *reinterpret_cast<const float4 *>(sAT + i * kInvLd + j0);
                 const float4 a1 = *reinterpret_cast<const float4 *>(sAT + i * kInvLd + j0 + 4);
                 const float tv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                if (kBwd && quad < 2) {  // T for the backward, zero above the diagonal
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        ws.bwd_Tm + ((int64_t)item * kChunk + i) * kChunk + j0);
+                    dst[0] = make_float4(j0 <= i ? tv[0] : 0.f, j0 + 1 <= i ? tv[1] : 0.f,
+                                         j0 + 2 <= i ? tv[2] : 0.f, j0 + 3 <= i ? tv[3] : 0.f);
+                    dst[1] = make_float4(j0 + 4 <= i ? tv[4] : 0.f, j0 + 5 <= i ? tv[5] : 0.f,
+                                         j0 + 6 <= i ? tv[6] : 0.f, j0 + 7 <= i ? tv[7] : 0.f);
+                }
                 float x[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) x[u] = j0 + u <= i ? tv[u] * scale_vec[j0 + u] : 0.f;
@@ -365,13 +395,14 @@ cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st) {
         !make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64) ||
         !make_tmap_bf16_3d(&args.tv, p.v, kD, H, rows, p.sv.h * 2, p.sv.t * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(k_tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kernel = ws.bwd_tc ? k_tc_prep<true> : k_tc_prep<false>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemLaunch);
     if (err != cudaSuccess) return err;
     const int64_t items = ws.max_chunks * p.H;  // an upper bound; the kernel reads the count
     if (items > INT32_MAX - 4 * (int64_t)device_sms()) return cudaErrorInvalidValue;
     const int64_t grid = persistent_grid(p, items, 3);  // three CTAs per SM
-    return launch_pdl(k_tc_prep, dim3((unsigned)grid), dim3(kThreads), kSmemLaunch, st, args);
+    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kThreads), kSmemLaunch, st, args);
 }
 
 }  // namespace gdr
