@@ -408,7 +408,7 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     L.off_G = take(simt || recompute ? sizeof(float) * (size_t)mc * H * kChunk : 0);
     L.off_W = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
     L.off_U = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
-    L.off_hpre = take(simt || recompute ? sizeof(float) * (size_t)mc * H * K * V : 0);
+    L.off_hpre = take(simt ? sizeof(float) * (size_t)mc * H * K * V : 0);
     L.off_vnew = take((simt || recompute) && delta ? sizeof(float) * (size_t)mc * H * kChunk * V
                                                    : 0);
     const size_t segs = S > 1 ? (size_t)ns * H * (size_t)S : 0;
@@ -448,7 +448,7 @@ Workspace carve_workspace(void *base, const WorkspaceLayout &L, int S) {
 struct BwdLayout {
     WorkspaceLayout fwd;
     size_t off_Mq, off_Kd, off_Tm, off_dhend, off_dvn, off_P1, off_P2, off_P3, off_ehp,
-        off_segMb, total;
+        off_segMb, off_lkimg, total;
 };
 
 BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments, bool tc_route) {
@@ -466,7 +466,7 @@ BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments, bool tc_
     B.off_Mq = take(sizeof(float) * items * sq);
     B.off_Kd = take(delta ? sizeof(float) * items * sq : 0);
     B.off_Tm = take(delta ? sizeof(float) * items * sq : 0);
-    B.off_dhend = take(sizeof(float) * items * K * V);
+    B.off_dhend = take(tc_route ? 0 : sizeof(float) * items * K * V);
     B.off_dvn = take(delta ? sizeof(float) * items * kChunk * V : 0);
     B.off_P1 = take(sizeof(float) * items * kChunk * K);
     B.off_P2 = take(delta ? sizeof(float) * items * kChunk * K : 0);
@@ -474,6 +474,7 @@ BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments, bool tc_
     B.off_ehp = take(sizeof(float) * items * ((K + 63) / 64));
     const size_t segs = n_segments > 1 ? (size_t)n_seqs(d) * d.H * (size_t)n_segments : 0;
     B.off_segMb = take(delta ? sizeof(float) * segs * K * K : 0);
+    B.off_lkimg = take(tc_route ? items * (size_t)kLkImgBytes : 0);
     B.total = off;
     return B;
 }
@@ -633,6 +634,7 @@ const char *gdr_kernel_name(int id) {
     case kKConvertOut: return "convert_bf16_to_f16";
     case kKTcRecompute: return "tc_chain_recompute";
     case kKTcBwdScan: return "tc_bwd_scan";
+    case kKTcBwdLk: return "tc_bwd_lk";
     default: return "?";
     }
 }
@@ -836,7 +838,18 @@ size_t gdr_bwd_workspace_size(const gdr_dims *dims, int beta_free, int n_segment
     if (validate_dims(dims) != GDR_OK) return 0;
     int route = 1, bv = 0, S = 1;
     if (bwd_plan(*dims, beta_free != 0, n_segments, nullptr, &route, &bv, &S) != GDR_OK) return 0;
-    return bwd_layout(*dims, beta_free != 0, S, route == 2).total;
+    // enough for either route (force_path may pick the other one, and a
+    // misaligned call moves to the CUDA-core route)
+    gdr_options o{};
+    o.force_path = 1;
+    int r1 = 1, S1 = 1;
+    if (bwd_plan(*dims, beta_free != 0, n_segments, &o, &r1, &bv, &S1) != GDR_OK) return 0;
+    size_t bytes = bwd_layout(*dims, beta_free != 0, S1, false).total;
+    o.force_path = 2;
+    int r2 = 2, S2 = 1;
+    if (bwd_plan(*dims, beta_free != 0, n_segments, &o, &r2, &bv, &S2) == GDR_OK)
+        bytes = std::max(bytes, bwd_layout(*dims, beta_free != 0, S2, true).total);
+    return bytes;
 }
 
 int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void *v,
@@ -901,6 +914,7 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
         ws.bwd_Mq = bw.Mq;
         ws.bwd_Kd = bw.Kd;
         ws.bwd_Tm = bw.Tm;
+        ws.bwd_lkimg = static_cast<uint8_t *>(base) + B.off_lkimg;
     }
     BwdArgs a{};
     a.dout = dout; a.dht = dht; a.dq = dq; a.dk = dk; a.dv = dv;

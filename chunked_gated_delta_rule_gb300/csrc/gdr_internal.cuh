@@ -161,7 +161,15 @@ struct Workspace {
                           // also stores G, Mq, Kd and T, the chain also h_pre
                           // and v_new (FP32)
     float *bwd_Mq, *bwd_Kd, *bwd_Tm;  // [chunks][H][64][64], as BwdWs (bwd_tc)
+    // [chunks][H][kLkImgBytes] (bwd_tc): the BF16 tiles of the L x K
+    // products, byte images of the chains' shared-memory operands (128-byte
+    // swizzled): h^T [v][key] and v_new^T [v][t] from the recompute, E^T
+    // [v][key] and -dV'^T [v][t] from the reverse scan
+    uint8_t *bwd_lkimg;
 };
+
+constexpr uint32_t kLkImgH = 0, kLkImgV = 32768, kLkImgE = 49152, kLkImgDv = 81920;
+constexpr uint32_t kLkImgBytes = 98304;
 
 // Backward pass: the caller's gradient tensors (dq, dk, dv in the input
 // dtype; dg, dbeta, dh0 FP32; dht / dh0 in the state layout of h0).

@@ -790,8 +790,7 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
         };
         if (tc_scan) {
             if ((e = rec.begin(kKTcBwdScan)) != cudaSuccess) return e;
-            if ((e = tc_bwd_scan(p, ws, bw.dhend, bw.dvn, a.dht, a.dh0, a.dout, st)) !=
-                cudaSuccess)
+            if ((e = tc_bwd_scan(p, ws, bw.dvn, a.dht, a.dh0, a.dout, st)) != cudaSuccess)
                 return e;
             if ((e = rec.end()) != cudaSuccess) return e;
         } else if (S <= 1) {
@@ -827,7 +826,12 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
         }
     }
     // L x K products
-    {
+    if (tc_scan) {
+        if ((e = rec.begin(kKTcBwdLk)) != cudaSuccess) return e;
+        if ((e = tc_bwd_lk(p, ws, a.dout, bw.P1, bw.P2, bw.P3, bw.ehp, st)) != cudaSuccess)
+            return e;
+        if ((e = rec.end()) != cudaSuccess) return e;
+    } else {
         const size_t smem = sizeof(float) * (5 * kChunk * kLd + kBT);
         if ((e = set_smem_bwd(k_bwd_lk<Tin>, smem)) != cudaSuccess) return e;
         if ((e = rec.begin(kKBwdLk)) != cudaSuccess) return e;

@@ -24,12 +24,12 @@
 //   E^T += dO^T Q~               tcgen05
 //   E^T += (-dV'^T) W            tcgen05, A = BF16 -dV'^T
 //
-// E at each chunk's end and dV' are stored in FP32 for the backward's
-// per-chunk kernels (L x K products, local gradients); dh0 is E after the
-// sequence's first chunk.  The state stays FP32 in TMEM; its BF16 mirror,
+// dV' is stored in FP32 for the local-gradient kernel, and the BF16 images
+// of the E^T mirror and the -dV'^T tile for the L x K products
+// (tc_bwd_lk.cu); dh0 is E after the sequence's first chunk.  The state stays FP32 in TMEM; its BF16 mirror,
 // dV' and dO are the MMA operands (the route's tolerance covers them).
 //
-// Warps: 0-3 state path (the serial dependency: dhend store, mirror, decay,
+// Warps: 0-3 state path (the serial dependency: E mirror and image, decay,
 // dV'), 4-7 side path (K~ in place; rows past a sequence's end zeroed in
 // the k and dO tiles), 8 control (every MMA), 9 producer (chains longest
 // first, record and tile loads into a two-stage ring, last chunk first).
@@ -47,7 +47,7 @@ using namespace tc;
 struct BwdScanArgs {
     Problem p;
     Workspace ws;
-    float *dhend;       // [chunks][H][K][V] E at each chunk's end
+    uint8_t *lkimg;     // [chunks][H][kLkImgBytes]: E^T and -dV'^T images written here
     float *dvn;         // [chunks][H][64][V] dV'
     const float *dht;   // state layout of h0, or nullptr
     float *dh0;         // state layout of h0, or nullptr
@@ -69,7 +69,7 @@ constexpr uint32_t kOffDv = kOffEm + 32768;
 constexpr uint32_t kOffRing = kOffDv + 16384;
 enum : int {
     kBFull = 0,     // [2] stage landed
-    kBMready = 2,   // mirror of E^T written, dhend stored (state path, 128)
+    kBMready = 2,   // mirror of E^T written (state path, 128)
     kBAdone = 3,    // D = dV'^T complete (commit)
     kBVready = 4,   // -dV'^T written, E^T decayed (state path, 128)
     kBHdone = 5,    // E^T update done (commit)
@@ -294,9 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                         reg_fence(r1);
                     }
                 };
-                // E stored for the per-chunk kernels, and its BF16 mirror (the
-                // A operand of E^T K~^T): the chain's critical path goes first
-                float *eg = args.dhend + item * kD * kD + row;  // [key][v]
+                // E's BF16 mirror (the A operand of E^T K~^T), and its image
+                // for the L x K products: the chain's critical path goes first
+                uint8_t *limg = args.lkimg + item * kLkImgBytes;
 #pragma unroll 1
                 for (int hq = 0; hq < 2; ++hq) {
                     uint32_t r0[32], r1[32];
@@ -309,13 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                             x[u] = __uint_as_float(r0[8 * c8 + u]);
                             y[u] = __uint_as_float(r1[8 * c8 + u]);
                         }
-                        st_bf16x8(sm + kOffEm + sw128_off(row, 64 * hq + 8 * c8, 128), x);
-                        st_bf16x8(sm + kOffEm + sw128_off(row, 64 * hq + 32 + 8 * c8, 128), y);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 32; ++kk) {
-                        eg[(64 * hq + kk) * kD] = __uint_as_float(r0[kk]);
-                        eg[(64 * hq + 32 + kk) * kD] = __uint_as_float(r1[kk]);
+                        const uint32_t ox = sw128_off(row, 64 * hq + 8 * c8, 128);
+                        const uint32_t oy = sw128_off(row, 64 * hq + 32 + 8 * c8, 128);
+                        st_bf16x8(sm + kOffEm + ox, x);
+                        st_bf16x8(sm + kOffEm + oy, y);
+                        st_bf16x8(limg + kLkImgE + ox, x);
+                        st_bf16x8(limg + kLkImgE + oy, y);
                     }
                 }
                 fence_async_smem();
@@ -353,9 +352,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                             u[i] = -d;
                         }
 #pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8)
-                            st_bf16x8(sm + kOffDv + sw128_off(row, 32 * hh + 8 * c8, 128),
-                                      u + 8 * c8);
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
+                            st_bf16x8(sm + kOffDv + ou, u + 8 * c8);
+                            st_bf16x8(args.lkimg + item * kLkImgBytes + kLkImgDv + ou, u + 8 * c8);
+                        }
                     }
                 }
                 fence_async_smem();
@@ -431,12 +432,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
 
 }  // namespace
 
-cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, float *dhend, float *dvn,
-                        const float *dht, float *dh0, const void *dout, cudaStream_t st) {
+cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, float *dvn, const float *dht,
+                        float *dh0, const void *dout, cudaStream_t st) {
     BwdScanArgs args;
     args.p = p;
     args.ws = ws;
-    args.dhend = dhend;
+    args.lkimg = ws.bwd_lkimg;
     args.dvn = dvn;
     args.dht = dht;
     args.dh0 = dh0;

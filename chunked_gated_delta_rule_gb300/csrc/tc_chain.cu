@@ -381,21 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 };
                 // h_pre -> BF16 mirror (the first product's A operand): the
                 // chain's critical path, so it goes first
-                // the recompute's FP32 state before the chunk, [key][v]
-                float *hpre = MODE == kModeRecompute
-                                  ? ws.hpre + ((int64_t)(C.c_begin + cc) * H + h) * kD * kD + row
-                                  : nullptr;
+                // the recompute's images of the chunk's h^T mirror and
+                // v_new^T tile, for the backward's L x K products
+                uint8_t *limg = MODE == kModeRecompute
+                                    ? ws.bwd_lkimg + ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes
+                                    : nullptr;
 #pragma unroll 1
                 for (int hq = 0; hq < 2; ++hq) {
                     uint32_t r0[32], r1[32];
                     state_half(hq, r0, r1);
-                    if (MODE == kModeRecompute) {
-#pragma unroll
-                        for (int kk = 0; kk < 32; ++kk) {
-                            hpre[(64 * hq + kk) * kD] = __uint_as_float(r0[kk]);
-                            hpre[(64 * hq + 32 + kk) * kD] = __uint_as_float(r1[kk]);
-                        }
-                    }
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
                         float x[8], y[8];
@@ -404,8 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                             x[u] = __uint_as_float(r0[8 * c8 + u]);
                             y[u] = __uint_as_float(r1[8 * c8 + u]);
                         }
-                        st_bf16x8(sm + kOffHm + sw128_off(row, 64 * hq + 8 * c8, 128), x);
-                        st_bf16x8(sm + kOffHm + sw128_off(row, 64 * hq + 32 + 8 * c8, 128), y);
+                        const uint32_t ox = sw128_off(row, 64 * hq + 8 * c8, 128);
+                        const uint32_t oy = sw128_off(row, 64 * hq + 32 + 8 * c8, 128);
+                        st_bf16x8(sm + kOffHm + ox, x);
+                        st_bf16x8(sm + kOffHm + oy, y);
+                        if (MODE == kModeRecompute) {
+                            st_bf16x8(limg + kLkImgH + ox, x);
+                            st_bf16x8(limg + kLkImgH + oy, y);
+                        }
                     }
                 }
                 fence_async_smem();
@@ -456,9 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                             for (int i = 0; i < 32; ++i) vn[i * kD] = u[i];
                         }
 #pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8)
-                            st_bf16x8(sm + kOffVn + sw128_off(row, 32 * hh + 8 * c8, 128),
-                                      u + 8 * c8);
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
+                            st_bf16x8(sm + kOffVn + ou, u + 8 * c8);
+                            if (MODE == kModeRecompute)
+                                st_bf16x8(ws.bwd_lkimg +
+                                              ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes +
+                                              kLkImgV + ou,
+                                          u + 8 * c8);
+                        }
                     }
                 }
                 fence_async_smem();

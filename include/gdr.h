@@ -277,7 +277,19 @@ int gdr_recurrent_fwd(const gdr_dims *dims, const void *q, const void *k,
  * flash-linear-attention ABC issue #23 pages, "Problem" and "Proposed
  * Dataflow" step 4; gradients dQ/dK/dV and of the states, its
  * "Fixture-First Correctness Contract"), through the chunked form's WY
- * factors.  FP32 arithmetic on CUDA cores for every input type.
+ * factors.  Two routes:
+ *   - tensor-core route (BF16 inputs, K = V = 128, delta rule, serial
+ *     reverse scan): the forward recompute is the tensor-core forward's
+ *     (per-chunk records, the serial chain storing the state before each
+ *     chunk and v_new), the reverse scan and the L x K products run on
+ *     tcgen05 with BF16 operands and FP32 accumulation, the local gradients
+ *     in FP32 on CUDA cores; every gradient lies within 1e-2 (relative L2)
+ *     of the exact one;
+ *   - CUDA-core route (every input type): FP32 arithmetic throughout.
+ *   The plan takes the tensor-core route where it applies, unless the
+ *   caller asks for a segment split or the serial chain would be long with
+ *   few chains beside it (a 64K-token sequence with few heads).
+ *   opt->force_path 1 or 2 picks the route.
  *   dims, q, k, v, g, beta, cu_seqlens, h0   as for gdr_chunk_fwd (device).
  *   dout    [B,T,H,V] dL/do, the input dtype.
  *   dht     [Nseq,H,K,V] FP32 dL/dht (state layout of h0), or NULL for 0.
@@ -293,11 +305,11 @@ int gdr_recurrent_fwd(const gdr_dims *dims, const void *q, const void *k,
  *           to the first (from dht to dh0), and an output pass rebuilds the
  *           per-chunk gradients (the pages' "Proposed Dataflow" step 4).
  *   opt     NULL, or gdr_options with scale, status, workspace (at least
- *           gdr_bwd_workspace_size bytes) and the launch events;
- *           force_path and force_bv must be 0.
- * The pass recomputes the forward states (the CUDA-core forward kernels)
- * and then runs four backward kernels; work is enqueued on `stream`, not
- * synchronised.  Every gradient is written for every token of every
+ *           gdr_bwd_workspace_size bytes), the launch events, force_path
+ *           (0 plan, 1 CUDA-core route, 2 tensor-core route) and
+ *           grid_limit; force_bv must be 0.
+ * The pass recomputes the forward states and then runs the backward
+ * kernels; work is enqueued on `stream`, not synchronised.  Every gradient is written for every token of every
  * sequence; results are bit-identical from run to run.
  */
 int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k,
@@ -308,8 +320,8 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k,
                   int n_segments, const gdr_options *opt, gdr_stream_t stream);
 
 /* Bytes of device scratch gdr_chunk_bwd needs for this problem (beta_free
- * != 0 for the beta-free mode; n_segments as passed to gdr_chunk_bwd).
- * 0 on invalid arguments. */
+ * != 0 for the beta-free mode; n_segments as passed to gdr_chunk_bwd),
+ * enough for either route (force_path 0, 1 or 2).  0 on invalid arguments. */
 size_t gdr_bwd_workspace_size(const gdr_dims *dims, int beta_free, int n_segments);
 
 /* Bytes of device scratch gdr_chunk_fwd_ex needs for this problem
