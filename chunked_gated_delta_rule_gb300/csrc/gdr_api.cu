@@ -935,6 +935,140 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
     return rc;
 }
 
+}  // extern "C"
+
+namespace gdr {
+namespace {
+
+// The host entry for one long sequence (dense with B == 1, or varlen with one
+// sequence), which cannot be cut into groups of whole sequences: it is cut
+// into `want` pieces of whole chunks (the first and last half a share), run
+// as consecutive passes, each starting from the state the previous one
+// ended with (kept on the device), while the next piece's inputs arrive and
+// the previous piece's outputs leave.  The state carries exactly across any
+// split point, so the result is the sequence's up to rounding.
+int host_fwd_pieces(const gdr_dims &D, int64_t T, int want, const void *q, const void *k,
+                    const void *v, const float *g, const float *beta, const float *h0, void *o,
+                    float *ht, int n_segments, cudaStream_t st) {
+    const size_t es = D.dtype == GDR_F32 ? 4 : 2;
+    const size_t rq = (size_t)D.H * D.K * es, rv = (size_t)D.H * D.V * es, rg = (size_t)D.H * 4;
+    const size_t rh = (size_t)D.H * D.K * D.V * 4;
+    const int64_t chunks = (T + kChunk - 1) / kChunk;
+    std::vector<int64_t> cut{0};  // token offsets of the pieces
+    for (int i = 1; i < want; ++i) {
+        const int64_t c = chunks * (2 * i - 1) / (2 * (want - 1)) * kChunk;
+        if (c > cut.back() && c < T) cut.push_back(c);
+    }
+    cut.push_back(T);
+    const int P = (int)cut.size() - 1;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes); return at; };
+    const size_t oq = take(T * rq), ok = take(T * rq), ov = take(T * rv), og = take(T * rg);
+    const size_t ob = take(beta ? T * rg : 0), oo = take(T * rv);
+    const size_t oh0 = take(h0 ? rh : 0), os0 = take(rh), os1 = take(rh);  // states in flight
+    const size_t ocu = take(D.N > 0 ? 2 * P * sizeof(int32_t) : 0);
+    char *d = nullptr;
+    if (lib_malloc(reinterpret_cast<void **>(&d), off, st) != cudaSuccess) return GDR_ERR_CUDA;
+    CopyStreams cs{};
+    const bool piped = copy_streams(st, &cs) == cudaSuccess;
+    cudaStream_t s_in = piped ? cs.in : st, s_out = piped ? cs.out : st;
+    std::vector<cudaEvent_t> ev;
+    auto order = [&](cudaStream_t from, cudaStream_t to) {
+        if (!piped || from == to) return cudaSuccess;
+        cudaEvent_t e = nullptr;
+        cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+        if (r != cudaSuccess) return r;
+        ev.push_back(e);
+        r = cudaEventRecord(e, from);
+        return r == cudaSuccess ? cudaStreamWaitEvent(to, e, 0) : r;
+    };
+    auto h2d = [&](size_t at, const void *src, size_t bytes) {
+        return bytes ? cudaMemcpyAsync(d + at, src, bytes, cudaMemcpyHostToDevice, s_in)
+                     : cudaSuccess;
+    };
+    const char *hq = static_cast<const char *>(q), *hk = static_cast<const char *>(k),
+               *hv = static_cast<const char *>(v), *hg = reinterpret_cast<const char *>(g),
+               *hb = reinterpret_cast<const char *>(beta);
+    char *ho = static_cast<char *>(o);
+    // every piece's cu_seqlens (varlen: one sequence of the piece's length)
+    std::vector<int32_t> pcu;
+    for (int i = 0; i < P; ++i) {
+        pcu.push_back(0);
+        pcu.push_back((int32_t)(cut[i + 1] - cut[i]));
+    }
+    int rc = GDR_OK;
+    if (order(st, s_in) != cudaSuccess || order(st, s_out) != cudaSuccess ||
+        (D.N > 0 && h2d(ocu, pcu.data(), pcu.size() * sizeof(int32_t)) != cudaSuccess) ||
+        (h0 && h2d(oh0, h0, rh) != cudaSuccess))
+        rc = GDR_ERR_CUDA;
+    std::vector<cudaEvent_t> arrived((size_t)P, nullptr);
+    for (int i = 0; i < P && rc == GDR_OK; ++i) {  // every piece's inputs queued first
+        const size_t t0 = (size_t)cut[i], nt = (size_t)(cut[i + 1] - cut[i]);
+        if (h2d(oq + t0 * rq, hq + t0 * rq, nt * rq) != cudaSuccess ||
+            h2d(ok + t0 * rq, hk + t0 * rq, nt * rq) != cudaSuccess ||
+            h2d(ov + t0 * rv, hv + t0 * rv, nt * rv) != cudaSuccess ||
+            h2d(og + t0 * rg, hg + t0 * rg, nt * rg) != cudaSuccess ||
+            (beta && h2d(ob + t0 * rg, hb + t0 * rg, nt * rg) != cudaSuccess)) {
+            rc = GDR_ERR_CUDA;
+            break;
+        }
+        if (piped) {
+            if (cudaEventCreateWithFlags(&arrived[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventRecord(arrived[i], s_in) != cudaSuccess) {
+                rc = GDR_ERR_CUDA;
+                break;
+            }
+            ev.push_back(arrived[i]);
+        }
+    }
+    for (int i = 0; i < P && rc == GDR_OK; ++i) {
+        const size_t t0 = (size_t)cut[i], nt = (size_t)(cut[i + 1] - cut[i]);
+        if (piped && cudaStreamWaitEvent(st, arrived[i], 0) != cudaSuccess) {
+            rc = GDR_ERR_CUDA;
+            break;
+        }
+        gdr_dims gd = D;
+        gd.flags &= ~GDR_SEQLENS_I64;
+        if (D.N > 0) {
+            gd.T = (int64_t)nt;
+            gd.max_len = (int64_t)nt;
+        } else {
+            gd.T = (int64_t)nt;
+        }
+        const float *pin = i == 0 ? (h0 ? reinterpret_cast<float *>(d + oh0) : nullptr)
+                                  : reinterpret_cast<float *>(d + ((i - 1) & 1 ? os1 : os0));
+        float *pout = reinterpret_cast<float *>(d + (i & 1 ? os1 : os0));
+        const int32_t *gc =
+            D.N > 0 ? reinterpret_cast<const int32_t *>(d + ocu + 2 * i * sizeof(int32_t)) : nullptr;
+        rc = gdr_chunk_fwd(&gd, d + oq + t0 * rq, d + ok + t0 * rq, d + ov + t0 * rv,
+                           reinterpret_cast<float *>(d + og + t0 * rg),
+                           beta ? reinterpret_cast<float *>(d + ob + t0 * rg) : nullptr, gc, pin,
+                           d + oo + t0 * rv, pout, n_segments,
+                           reinterpret_cast<gdr_stream_t>(st));
+        if (rc != GDR_OK) break;
+        if (order(st, s_out) != cudaSuccess ||
+            cudaMemcpyAsync(ho + t0 * rv, d + oo + t0 * rv, nt * rv, cudaMemcpyDeviceToHost,
+                            s_out) != cudaSuccess ||
+            (ht && i == P - 1 &&
+             cudaMemcpyAsync(ht, pout, rh, cudaMemcpyDeviceToHost, s_out) != cudaSuccess))
+            rc = GDR_ERR_CUDA;
+    }
+    if (order(s_in, st) != cudaSuccess || order(s_out, st) != cudaSuccess) {
+        cudaStreamSynchronize(s_in);
+        cudaStreamSynchronize(s_out);
+        if (rc == GDR_OK) rc = GDR_ERR_CUDA;
+    }
+    if (cudaFreeAsync(d, st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess && rc == GDR_OK) rc = GDR_ERR_CUDA;
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    return rc;
+}
+
+}  // namespace
+}  // namespace gdr
+
+extern "C" {
+
 int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k, const void *v,
                        const float *g, const float *beta, const int32_t *cu_seqlens,
                        const float *h0, void *o, float *ht, int n_segments,
@@ -963,6 +1097,13 @@ int gdr_chunk_fwd_host(const gdr_dims *dims, const void *q, const void *k, const
     const size_t rh = (size_t)D.H * D.K * D.V * 4;  // one sequence's state
     const size_t ntok = (size_t)cu[ns];
     const HostGroups G = host_groups(cu, 2 * rq + rv + rg * (beta ? 2 : 1), rh * (h0 ? 1 : 0));
+    if (ns == 1 && ntok >= 2 * (size_t)kChunk) {  // one long sequence: pieces of it
+        const double total = (double)ntok * (double)(2 * rq + rv + rg * (beta ? 2 : 1));
+        const int want = (int)std::min<int64_t>(4, std::llround(total / (32.0 * (1 << 20))));
+        if (want >= 2)
+            return host_fwd_pieces(D, (int64_t)ntok, want, q, k, v, g, beta, h0, o, ht,
+                                   n_segments, st);
+    }
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes); return at; };
     const size_t oq = take(ntok * rq), ok = take(ntok * rq), ov = take(ntok * rv);

@@ -209,6 +209,10 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k,
  *     leave while group i runs, on two copy streams of the library ordered
  *     against `stream` with events.  Each sequence's result is the one
  *     gdr_chunk_fwd gives it (plans may differ with the group's size).
+ *     One long sequence is cut into pieces of whole chunks instead, run as
+ *     consecutive passes, each starting from the state the previous one
+ *     ended with (kept on the device): the same result up to rounding
+ *     (identical bits with n_segments = 1).
  *   - cu_seqlens is host data here and is checked on the host: a table
  *     that is not non-decreasing from 0 to T returns GDR_ERR_SEQLENS before
  *     any work is enqueued.

@@ -276,16 +276,24 @@ def _host_run(x, **kw):
                                   cu_seqlens=pin["cu_seqlens"], h0=pin["h0"], **kw)
 
 
-@pytest.mark.parametrize("case", ["wide_varlen", "dense_h0"])
+@pytest.mark.parametrize("case", ["wide_varlen", "dense_h0", "one_sequence", "one_varlen_f32"])
 def test_host_entry_groups_match_device_entry(case):
     """Inputs of 48 MB and more are cut into groups whose copies overlap the
-    passes; with the plan pinned (one segment) every sequence's result is
-    bit-identical to the one-call device entry."""
+    passes: groups of whole sequences, or pieces of one long sequence run as
+    consecutive passes with the state carried on the device.  With the plan
+    pinned (one segment) every result is bit-identical to the one-call
+    device entry (the serial chain hands its FP32 state across a piece
+    boundary unchanged)."""
     if case == "wide_varlen":  # 130 MB in: 4 groups of whole sequences
         x = synthetic.make_inputs(W["wide_varlen_bf16"])
-    else:  # 8 rows x 4096 tokens x 4 heads with h0: 3 groups of batch rows
+    elif case == "dense_h0":  # 8 rows x 4096 tokens x 4 heads with h0: 3 groups of batch rows
         x = synthetic.make_inputs(synthetic.small(W["long_16k_bf16"], B=8, T=4096, H=4,
                                                   with_h0=True))
+    elif case == "one_sequence":  # 1 row x 16K tokens x 4 heads, h0: 2 pieces
+        x = synthetic.make_inputs(synthetic.small(W["long_16k_bf16"], H=4, with_h0=True))
+    else:  # one varlen sequence, FP32 (the CUDA-core path), 3 pieces, ragged end
+        x = synthetic.make_inputs(synthetic.small(W["tiny_dense_f32"], H=4, K=128, V=128),
+                                  lengths=[20000 + 37])
     o_d, ht_d = run_gpu(x, n_segments=1)
     o_h, ht_h = _host_run(x, n_segments=1)
     assert torch.equal(_bits(o_h), _bits(o_d.cpu()))
