@@ -280,21 +280,25 @@ def bwd_algorithmic(kernel, x, c):
         fma = ch * (L * L * V / 2 + L * L * K)
         if delta:
             fma += ch * (1.5 * L * L * V + 2.5 * L * L * K + L ** 3 / 2)
-    elif kernel == "tc_prep":  # the forward's preparation, plus G, Kd, Mq, T for the backward
-        return algorithmic_bytes(kernel, x, c) + ch * L * f32 + 3 * ch * L * L * f32, None
+    elif kernel == "tc_prep":  # the forward's preparation, plus G and T for the backward
+        return algorithmic_bytes(kernel, x, c) + ch * L * f32 + ch * L * L * f32, None
     elif kernel == "tc_chain_recompute":
-        # W^T, U^T, vectors, k read; v_new (FP32) and the BF16 images of the
-        # h and v_new tiles written
-        return (ch * (2 * 16384 + 272) + th * K * es + ch * L * V * f32
-                + ch * (K * V + L * V) * 2, None)
+        # W^T, U^T, vectors, k read; v_new (FP32) and the BF16 image of the
+        # h mirror written
+        return (ch * (2 * 16384 + 272) + th * K * es + ch * L * V * f32 + ch * K * V * 2,
+                None)
     elif kernel == "tc_bwd_scan":
-        # W^T, Q~, P, vectors, k, dO read; dV' (FP32) and the BF16 images of
-        # E and dV' written; dht / dh0
+        # W^T, Q~, P, vectors, k, dO read; dV' (FP32) and the BF16 image of
+        # the E mirror written; dht / dh0
         return (ch * (2 * 16384 + 8192 + 272) + th * (K + V) * es + ch * L * V * f32
-                + ch * (K * V + L * V) * 2 + 2 * st, None)
-    elif kernel == "tc_bwd_lk":  # the four images and dO read; P1, P2, P3, <E, h> written
-        return (ch * 98304 + th * V * es + 3 * ch * L * K * f32 + ch * 2 * f32,
-                ch * 3.0 * L * K * V * 2)
+                + ch * K * V * 2 + 2 * st, None)
+    elif kernel == "tc_bwd_grad":
+        # h and E images, dO, q, k, v, T, dV', v_new, G, beta read; dq, dk,
+        # dv, dbeta, dg written.  Multiply-adds as issued: the hi / lo halves
+        # of the FP32 operands count twice (27 products of 128 x 64 x 64).
+        return (ch * 2 * K * V * 2 + th * (2 * V + 2 * K) * es + ch * L * L * f32
+                + 2 * ch * L * V * f32 + ch * L * f32 + th * f32
+                + th * (2 * K + V) * es + 2 * th * f32, 2.0 * ch * 27 * 128 * 64 * 64)
     elif kernel == "simt_prep":
         b = algorithmic_bytes(kernel, x, c)
         fma = ch * ((L * L * K / 2 + L ** 3 / 6 + L * L * (K + V) / 2) if delta else 0)

@@ -463,15 +463,18 @@ BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments, bool tc_
     const bool delta = !beta_free;
     const size_t items = (size_t)B.fwd.max_chunks * (size_t)d.H;
     const size_t K = (size_t)d.K, V = (size_t)d.V, sq = (size_t)kChunk * kChunk;
-    B.off_Mq = take(sizeof(float) * items * sq);
-    B.off_Kd = take(delta ? sizeof(float) * items * sq : 0);
+    // the tensor-core route keeps T, dV' and the images; the CUDA-core route
+    // every buffer of BwdWs
+    const bool cc = !tc_route;
+    B.off_Mq = take(cc ? sizeof(float) * items * sq : 0);
+    B.off_Kd = take(cc && delta ? sizeof(float) * items * sq : 0);
     B.off_Tm = take(delta ? sizeof(float) * items * sq : 0);
-    B.off_dhend = take(tc_route ? 0 : sizeof(float) * items * K * V);
+    B.off_dhend = take(cc ? sizeof(float) * items * K * V : 0);
     B.off_dvn = take(delta ? sizeof(float) * items * kChunk * V : 0);
-    B.off_P1 = take(sizeof(float) * items * kChunk * K);
-    B.off_P2 = take(delta ? sizeof(float) * items * kChunk * K : 0);
-    B.off_P3 = take(sizeof(float) * items * kChunk * K);
-    B.off_ehp = take(sizeof(float) * items * ((K + 63) / 64));
+    B.off_P1 = take(cc ? sizeof(float) * items * kChunk * K : 0);
+    B.off_P2 = take(cc && delta ? sizeof(float) * items * kChunk * K : 0);
+    B.off_P3 = take(cc ? sizeof(float) * items * kChunk * K : 0);
+    B.off_ehp = take(cc ? sizeof(float) * items * ((K + 63) / 64) : 0);
     const size_t segs = n_segments > 1 ? (size_t)n_seqs(d) * d.H * (size_t)n_segments : 0;
     B.off_segMb = take(delta ? sizeof(float) * segs * K * K : 0);
     B.off_lkimg = take(tc_route ? items * (size_t)kLkImgBytes : 0);
@@ -559,16 +562,18 @@ int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStre
 }
 
 // Backward: the forward recompute (the state before each chunk and V'),
-// then the backward kernels.  Route 2: the tensor-core preparation (records,
-// and G) and the serial chain in its recompute mode, the reverse scan on the
-// tensor cores; route 1: the CUDA-core forward and reverse scans.
+// then the backward kernels.  Route 2, all on the tensor cores: the
+// preparation (records, G and T), the serial chain in its recompute mode, the
+// reverse scan and the per-chunk gradients; route 1: the CUDA-core forward
+// and backward kernels.
 int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw, int bv,
             int route, cudaStream_t st, LaunchRecorder &rec) {
     GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
     if (route == 2) {
         GDR_LAUNCH(rec, kKTcPrep, tc_prep(p, ws, st));
         GDR_LAUNCH(rec, kKTcRecompute, tc_chain(p, ws, 3, st));
-        GDR_TRY(simt_bwd(p, ws, a, bw, true, st, rec));
+        GDR_LAUNCH(rec, kKTcBwdScan, tc_bwd_scan(p, ws, bw.dvn, a.dht, a.dh0, a.dout, st));
+        GDR_LAUNCH(rec, kKTcBwdGrad, tc_bwd_grad(p, ws, a, bw.dvn, bw.Tm, st));
         return GDR_OK;
     }
     GDR_LAUNCH(rec, kKPrep, simt_prep(p, ws, st));
@@ -584,7 +589,7 @@ int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs
             GDR_LAUNCH(rec, kKCompose, simt_compose(p, ws, bv, st));
         GDR_LAUNCH(rec, kKScanSegOut, simt_scan(p, ws, 2, bv, st));
     }
-    GDR_TRY(simt_bwd(p, ws, a, bw, false, st, rec));
+    GDR_TRY(simt_bwd(p, ws, a, bw, st, rec));
     return GDR_OK;
 }
 
@@ -634,7 +639,7 @@ const char *gdr_kernel_name(int id) {
     case kKConvertOut: return "convert_bf16_to_f16";
     case kKTcRecompute: return "tc_chain_recompute";
     case kKTcBwdScan: return "tc_bwd_scan";
-    case kKTcBwdLk: return "tc_bwd_lk";
+    case kKTcBwdGrad: return "tc_bwd_grad";
     default: return "?";
     }
 }
@@ -911,8 +916,6 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
     const BwdWs bw = carve_bwd(base, B);
     ws.bwd_tc = route == 2;
     if (ws.bwd_tc) {
-        ws.bwd_Mq = bw.Mq;
-        ws.bwd_Kd = bw.Kd;
         ws.bwd_Tm = bw.Tm;
         ws.bwd_lkimg = static_cast<uint8_t *>(base) + B.off_lkimg;
     }

@@ -158,18 +158,19 @@ struct Workspace {
     int64_t max_chunks;
     int n_segments;       // S (1 = serial)
     int bwd_tc;           // the tensor-core backward's forward recompute: tc_prep
-                          // also stores G, Mq, Kd and T, the chain also h_pre
-                          // and v_new (FP32)
-    float *bwd_Mq, *bwd_Kd, *bwd_Tm;  // [chunks][H][64][64], as BwdWs (bwd_tc)
-    // [chunks][H][kLkImgBytes] (bwd_tc): the BF16 tiles of the L x K
-    // products, byte images of the chains' shared-memory operands (128-byte
-    // swizzled): h^T [v][key] and v_new^T [v][t] from the recompute, E^T
-    // [v][key] and -dV'^T [v][t] from the reverse scan
+                          // also stores G and T, the chain v_new (FP32) and
+                          // the image of its h mirror
+    float *bwd_Tm;        // [chunks][H][64][64] T (bwd_tc)
+    // [chunks][H][kLkImgBytes] (bwd_tc): byte images of the chains' BF16
+    // state mirrors (128-byte swizzled, [v][key], two 16 KB key blocks), the
+    // MMA operands of the backward's per-chunk gradients: h^T (the state
+    // before the chunk) from the recompute, E^T (the gradient at the chunk's
+    // end) from the reverse scan
     uint8_t *bwd_lkimg;
 };
 
-constexpr uint32_t kLkImgH = 0, kLkImgV = 32768, kLkImgE = 49152, kLkImgDv = 81920;
-constexpr uint32_t kLkImgBytes = 98304;
+constexpr uint32_t kLkImgH = 0, kLkImgE = 32768;
+constexpr uint32_t kLkImgBytes = 65536;
 
 // Backward pass: the caller's gradient tensors (dq, dk, dv in the input
 // dtype; dg, dbeta, dh0 FP32; dht / dh0 in the state layout of h0).

@@ -59,7 +59,7 @@ enum KernelId {
     kKConvertOut = 24,
     kKTcRecompute = 25,
     kKTcBwdScan = 26,
-    kKTcBwdLk = 27,
+    kKTcBwdGrad = 27,
     kKNumIds
 };
 
@@ -99,21 +99,20 @@ cudaError_t simt_output(const Problem &p, const Workspace &ws, cudaStream_t st);
 // tensor-core path.
 cudaError_t convert_f16_to_bf16(const void *src, void *dst, int64_t n, cudaStream_t st);
 cudaError_t convert_bf16_to_f16(const void *src, void *dst, int64_t n, cudaStream_t st);
-// Backward pass after the forward recompute (G, hpre, vnew in ws; W too for
-// the CUDA-core reverse scan).  tc_scan: the reverse scan runs on the tensor
-// cores (tc_bwd_scan, from the records of the tensor-core recompute; serial).
+// Backward pass on CUDA cores after the CUDA-core forward recompute (G,
+// W, hpre, vnew in ws).
 cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
-                     bool tc_scan, cudaStream_t st, LaunchRecorder &rec);
+                     cudaStream_t st, LaunchRecorder &rec);
 // The reverse state-gradient scan on the tensor cores (BF16, K = V = 128,
 // delta rule, serial): dV' into dvn, the E^T and -dV'^T images into
 // ws.bwd_lkimg, dh0.
 cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, float *dvn, const float *dht,
                         float *dh0, const void *dout, cudaStream_t st);
-// The L x K products of the backward on the tensor cores, from the images in
-// ws.bwd_lkimg and dO: P1 = dO h^T, P2 = dV' h^T, P3 = V' E^T, and <E, h>
-// per 64-key slice.
-cudaError_t tc_bwd_lk(const Problem &p, const Workspace &ws, const void *dout, float *P1,
-                      float *P2, float *P3, float *ehp, cudaStream_t st);
+// Every per-chunk gradient of the backward on the tensor cores (dq, dk, dv,
+// dbeta, dg), from the images in ws.bwd_lkimg (h and E), dO, q, k, v, dV'
+// (dvn), v_new (ws.vnew), T (Tm) and G (ws.G).
+cudaError_t tc_bwd_grad(const Problem &p, const Workspace &ws, const BwdArgs &a, const float *dvn,
+                        const float *Tm, cudaStream_t st);
 // Composition for the delta rule with K <= 128 and V % 32 == 0 (both paths):
 // bulk-copied transposed transitions, 32 value columns per CTA.
 bool compose_mt_supported(const Problem &p);

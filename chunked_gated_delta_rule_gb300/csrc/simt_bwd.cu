@@ -754,13 +754,13 @@ cudaError_t set_smem_bwd(F *f, size_t bytes) {
 
 template <typename Tin>
 cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
-                       bool tc_scan, cudaStream_t st, LaunchRecorder &rec) {
+                       cudaStream_t st, LaunchRecorder &rec) {
     const bool delta = p.beta != nullptr;
     const unsigned mc = (unsigned)ws.max_chunks, H = (unsigned)p.H;
     const int K = (int)p.K, V = (int)p.V;
     cudaError_t e;
-    // gram (the tensor-core route's preparation stored Mq, Kd and T already)
-    if (!tc_scan) {
+    // gram
+    {
         const size_t smem = sizeof(float) * (3 * kChunk * kLd + 2 * kChunk);
         if ((e = set_smem_bwd(k_bwd_gram<Tin>, smem)) != cudaSuccess) return e;
         if ((e = rec.begin(kKBwdGram)) != cudaSuccess) return e;
@@ -788,12 +788,7 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
             }
             return cudaGetLastError();
         };
-        if (tc_scan) {
-            if ((e = rec.begin(kKTcBwdScan)) != cudaSuccess) return e;
-            if ((e = tc_bwd_scan(p, ws, bw.dvn, a.dht, a.dh0, a.dout, st)) != cudaSuccess)
-                return e;
-            if ((e = rec.end()) != cudaSuccess) return e;
-        } else if (S <= 1) {
+        if (S <= 1) {
             if ((e = rec.begin(kKBwdScan)) != cudaSuccess) return e;
             if ((e = launch(0)) != cudaSuccess) return e;
             if ((e = rec.end()) != cudaSuccess) return e;
@@ -826,12 +821,7 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
         }
     }
     // L x K products
-    if (tc_scan) {
-        if ((e = rec.begin(kKTcBwdLk)) != cudaSuccess) return e;
-        if ((e = tc_bwd_lk(p, ws, a.dout, bw.P1, bw.P2, bw.P3, bw.ehp, st)) != cudaSuccess)
-            return e;
-        if ((e = rec.end()) != cudaSuccess) return e;
-    } else {
+    {
         const size_t smem = sizeof(float) * (5 * kChunk * kLd + kBT);
         if ((e = set_smem_bwd(k_bwd_lk<Tin>, smem)) != cudaSuccess) return e;
         if ((e = rec.begin(kKBwdLk)) != cudaSuccess) return e;
@@ -854,10 +844,10 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
 }  // namespace
 
 cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
-                     bool tc_scan, cudaStream_t st, LaunchRecorder &rec) {
-    if (p.dtype == GDR_BF16) return launch_bwd<__nv_bfloat16>(p, ws, a, bw, tc_scan, st, rec);
-    if (p.dtype == GDR_F16) return launch_bwd<__half>(p, ws, a, bw, false, st, rec);
-    return launch_bwd<float>(p, ws, a, bw, false, st, rec);
+                     cudaStream_t st, LaunchRecorder &rec) {
+    if (p.dtype == GDR_BF16) return launch_bwd<__nv_bfloat16>(p, ws, a, bw, st, rec);
+    if (p.dtype == GDR_F16) return launch_bwd<__half>(p, ws, a, bw, st, rec);
+    return launch_bwd<float>(p, ws, a, bw, st, rec);
 }
 
 }  // namespace gdr

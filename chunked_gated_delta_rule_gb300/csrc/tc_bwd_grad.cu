@@ -1,0 +1,569 @@
+// tc_bwd_grad.cu -- every per-chunk gradient of the backward pass on the
+// tensor cores (the tensor-core route: BF16 inputs, K = V = 128, delta rule).
+// Per (chunk, head), with h the state before the chunk (forward recompute),
+// E the gradient at the chunk's end and dV' the gradient of the chunk's v_new
+// V' (reverse scan), T = (I + A)^-1 and the gate factors of the chunked form
+// (gamma = e^G, lam = e^{G_last - G}, D_ij = e^{G_i - G_j}):
+//
+//   dVb = T^T dV'                      dv = diag(beta) dVb
+//   dm  = dO V'^T,  Y = dVb V'^T       Z = scale causal(dm) * D,  dA = -strict_lower(Y)
+//   S   = diag(beta) dA * D            dKb = -dVb h^T
+//   dq  = scale diag(gamma) dO h^T + Z K
+//   dk  = diag(lam) V' E^T + Z^T Q + (S + S^T) K + diag(beta gamma) dKb
+//   dbeta, dg: row sums of the same terms (below)
+//
+// Y = T^T (dT T^T) with dT = dV' B'^T the gradient of T in V' = T B'
+// (B' = diag(beta)(V - diag(gamma) K h)): dT T^T = dV' (T B')^T = dV' V'^T,
+// so neither dT nor B' is formed.
+//
+// Every product runs on tcgen05 (kind::f16, FP32 accumulators in TMEM).
+// The BF16 inputs q, k, dO and the chains' BF16 h and E mirrors enter as
+// they are; every FP32 operand (T, dV', V', dVb, Z, S + S^T) enters as a
+// pair of BF16 tiles hi + lo (lo = x - hi, rounded), so each product carries
+// about 16 significant bits of its FP32 operands and the local gradients
+// keep FP32-grade accuracy.  Products whose rows are tokens are stacked to
+// M = 128: [Q; K] K^T, [dO; dVb] V'^T; the rest are transposed, keys or
+// value columns on the TMEM lanes and tokens as N = 64.
+//
+// Persistent CTAs (one per SM) stride over the (chunk, head) items in three
+// MMA groups per item, each followed by an epilogue that reads TMEM; the
+// next item's tiles load while the last epilogue runs.  Row sums over keys
+// or values are warp transposing reductions in a fixed order, so results are
+// identical at any grid.  Every wait is time-bounded.
+#include "gdr_internal.cuh"
+#include "tc_chunk.cuh"
+#include "tma_host.cuh"
+
+namespace gdr {
+namespace {
+
+using namespace tc;
+
+struct GradArgs {
+    Problem p;
+    Workspace ws;
+    BwdArgs a;
+    const float *dvn;  // [items][64][V] dV'
+    const float *Tm;   // [items][64][64] T
+    CUtensorMap tq, tk, tdo;
+};
+
+constexpr int kThreads = 256;
+
+// Shared memory.  BF16 tiles are 128-byte swizzled (sw128_off), 64 rows per
+// 8 KB block of 64 columns unless noted.
+//   H  [0, 32 KB)      h^T image [v][key], two key blocks of 128 rows
+//   B  [32, 80 KB)     per value block b (24 KB): dO rows | dVb hi | dVb lo;
+//                      the E^T image's key block b sits in the dVb rows until
+//                      dVb is written
+//   C  [80, 112 KB)    per key block b (16 KB): q rows | k rows
+//   D  [112, 144 KB)   V' hi | V' lo ([t][v])
+//   F  [144, 192 KB)   dV' hi | dV' lo ([i][v]) | T hi | T lo ([i][j]); after
+//                      the first group: Z hi | Z lo | (S + S^T) hi | lo |
+//                      S in FP32 (row i at 64 i, column j at j ^ (i % 32))
+constexpr uint32_t kOffH = 0;
+constexpr uint32_t kOffB = 32768;
+constexpr uint32_t kBlkB = 24576;
+constexpr uint32_t kOffC = kOffB + 2 * kBlkB;
+constexpr uint32_t kBlkC = 16384;
+constexpr uint32_t kOffD = kOffC + 2 * kBlkC;
+constexpr uint32_t kOffF = kOffD + 32768;
+constexpr uint32_t kFdvHi = 0, kFdvLo = 16384, kFtHi = 32768, kFtLo = 40960;
+constexpr uint32_t kFzHi = 0, kFzLo = 8192, kFsHi = 16384, kFsLo = 24576, kFs32 = 32768;
+constexpr uint32_t kOffMisc = kOffF + 49152;
+// FP32 scalars in the misc area: gate vectors, per-warp partial row sums
+constexpr int kVG = 0, kVGam = 64, kVLam = 128, kVB = 192;
+constexpr int kR1 = 256, kR2 = kR1 + 256, kR3 = kR2 + 256, kR4 = kR3 + 256;  // [4 lane quarters][64]
+constexpr int kRowR = kR4 + 256, kColR = kRowR + 128, kRdA = kColR + 128, kColRA = kRdA + 128;  // [2][64]
+constexpr int kR3f = kColRA + 128, kDg = kR3f + 64, kEh = kDg + 64;
+constexpr int kMiscFloats = kEh + 8;
+constexpr uint32_t kOffBar = kOffMisc + kMiscFloats * 4;
+constexpr int kNumBars = 4;  // tiles landed, then one per MMA group
+constexpr uint32_t kSmemLaunch = kOffBar + 8 * kNumBars + 16 + 1024;
+static_assert(kOffBar % 8 == 0, "barrier alignment");
+static_assert(kSmemLaunch <= 232448, "shared memory per CTA");
+constexpr uint32_t kLoadBytes = 32768 + 32768 + 3 * 16384;  // h, E images; dO, q, k tiles
+
+// TMEM columns (128 lanes each, FP32), 64 columns per accumulator
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kCP1 = 0;     // (dO h^T)^T            [key][t]
+constexpr uint32_t kCP3 = 64;    // (V' E^T)^T            [key][t]
+constexpr uint32_t kCQK = 128;   // [Q K^T; K K^T]        [t | 64 + t][j]
+constexpr uint32_t kCDvb = 192;  // dVb^T [v][j]; then rows 64-127: dVb lo V' hi^T
+constexpr uint32_t kCDmY = 256;  // [dO V'^T; dVb V'^T]  [i | 64 + i][j]
+constexpr uint32_t kCKb = 320;   // (dVb h^T)^T           [key][i]
+constexpr uint32_t kCXq = 384;   // (Z K)^T               [key][i]
+constexpr uint32_t kCXk = 448;   // (Z^T Q + (S + S^T) K)^T
+
+constexpr uint32_t kIdMnK = idesc_bf16(128, 64, 1, 0);   // A MN-major, B K-major
+constexpr uint32_t kIdKK = idesc_bf16(128, 64, 0, 0);    // both K-major
+constexpr uint32_t kIdMnMn = idesc_bf16(128, 64, 1, 1);  // both MN-major
+
+// Column sums of a warp's 32 x 32 block: on entry lane l holds x[c] = entry
+// (l, c); on return x[0] of lane l is the sum over the 32 lanes of column l.
+// Five exchange rounds halve the columns each lane keeps; the order of the
+// additions is fixed.
+__device__ __forceinline__ float warp_colsum32(float (&x)[32], int lane_id) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool up = (lane_id & s) != 0;
+#pragma unroll
+        for (int c = 0; c < s; ++c) {
+            const float send = up ? x[c] : x[c + s];
+            const float keep = up ? x[c + s] : x[c];
+            x[c] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return x[0];
+}
+
+__device__ __forceinline__ float bf16_at(const uint8_t *p) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
+}
+
+// Eight FP32 values -> the BF16 chunk of their rounded values (hi) and of
+// the rounded remainders (lo).
+__device__ __forceinline__ void st_split8(uint8_t *hi, uint8_t *lo, const float *x) {
+    float h[8], l[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        h[u] = __bfloat162float(__float2bfloat16_rn(x[u]));
+        l[u] = x[u] - h[u];
+    }
+    st_bf16x8(hi, h);
+    st_bf16x8(lo, l);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_constant__ GradArgs args) {
+    const Problem &p = args.p;
+    const Workspace &ws = args.ws;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    float *mf = reinterpret_cast<float *>(sm + kOffMisc);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffBar + 8 * kNumBars);
+    float *sS = reinterpret_cast<float *>(sm + kOffF + kFs32);
+    const int4 *tab = reinterpret_cast<const int4 *>(ws.chunk_tab);
+    const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int r = 32 * q4 + lane_id;              // TMEM lane of this thread
+    const uint32_t lane = (uint32_t)(32 * q4) << 16;
+    const int j0 = 32 * hf;                       // this thread's 32 columns
+    const int H = (int)p.H;
+    const float scale = p.scale;
+    const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(p.v);
+    __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(args.a.dq);
+    __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(args.a.dk);
+    __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(args.a.dv);
+
+    pdl_trigger();
+    if (warp == 0) {
+        tmem_alloc(s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], 1);
+        mbar_init_fence();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const uint32_t tl = tmem + lane;
+    pdl_wait();  // images, dV', v_new, T and G from the kernels before
+    const int n_items = *ws.n_chunks * H;
+
+    auto issue_loads = [&](int it_) {
+        const int4 e = tab[it_ / H];
+        const int hh = it_ % H;
+        const uint8_t *img = ws.bwd_lkimg + (int64_t)it_ * kLkImgBytes;
+        mbar_arrive_expect_tx(&bars[0], kLoadBytes);
+        bulk_load(sm + kOffH, img + kLkImgH, 16384u, &bars[0]);
+        bulk_load(sm + kOffH + 16384, img + kLkImgH + 16384, 16384u, &bars[0]);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            bulk_load(sm + kOffB + b * kBlkB + 8192, img + kLkImgE + b * 16384, 16384u, &bars[0]);
+            tma_load_3d(sm + kOffB + b * kBlkB, &args.tdo, &bars[0], 64 * b, hh, e.y);
+            tma_load_3d(sm + kOffC + b * kBlkC, &args.tq, &bars[0], 64 * b, hh, e.y);
+            tma_load_3d(sm + kOffC + b * kBlkC + 8192, &args.tk, &bars[0], 64 * b, hh, e.y);
+        }
+    };
+    // Rows [0, len) of a row-major FP32 [64][ncols] matrix (later rows read
+    // as zero) -> hi / lo BF16 tiles at off_hi / off_lo.
+    auto split_tile = [&](const float *src, int ncols, uint32_t off_hi, uint32_t off_lo, int len) {
+        const int cpr = ncols / 8;
+        for (int c = tid; c < 64 * cpr; c += kThreads) {
+            const int row = c / cpr, j = c % cpr;
+            float x[8];
+            if (row < len) {
+                const float4 a = *reinterpret_cast<const float4 *>(src + row * ncols + 8 * j);
+                const float4 b = *reinterpret_cast<const float4 *>(src + row * ncols + 8 * j + 4);
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = 0.f;
+            }
+            const uint32_t o = sw128_chunk(row, j, 64);
+            st_split8(sm + off_hi + o, sm + off_lo + o, x);
+        }
+    };
+
+    int item = blockIdx.x;
+    if (tid == 0 && item < n_items) issue_loads(item);
+    for (uint32_t it = 0; item < n_items; ++it) {
+        const uint32_t ph = it & 1u;
+        const int4 e = tab[item / H];
+        const int hh = item % H;
+        const int64_t t0 = e.y;
+        const int len = e.z;
+        const int next = item + (int)gridDim.x;
+
+        // gate vectors; the FP32 operands as hi / lo tiles
+        if (tid < 64) {
+            const bool in = tid < len;
+            const float G = ws.G[(int64_t)item * kChunk + tid];
+            const float Gl = ws.G[(int64_t)item * kChunk + len - 1];
+            mf[kVG + tid] = G;
+            mf[kVGam + tid] = in ? expf(G) : 0.f;
+            mf[kVLam + tid] = in ? expf(Gl - G) : 0.f;
+            mf[kVB + tid] = in ? p.beta[(t0 + tid) * H + hh] : 0.f;
+        }
+        split_tile(args.Tm + (int64_t)item * kChunk * kChunk, 64, kOffF + kFtHi, kOffF + kFtLo,
+                   len);
+        split_tile(args.dvn + (int64_t)item * kChunk * kD, kD, kOffF + kFdvHi, kOffF + kFdvLo, len);
+        split_tile(ws.vnew + (int64_t)item * kChunk * kD, kD, kOffD, kOffD + 16384, len);
+        bool ok = mbar_wait(&bars[0], ph, p.status);
+        if (__syncthreads_or(!ok)) break;
+        if (len < kChunk) {  // tile rows past the sequence end belong to the next one
+            for (int idx = tid; idx < 6 * (kChunk - len) * 8; idx += kThreads) {
+                const int tile = idx / ((kChunk - len) * 8), rem = idx % ((kChunk - len) * 8);
+                const int t = len + (rem >> 3), c = rem & 7;
+                const uint32_t base = tile < 2 ? kOffB + tile * kBlkB
+                                               : kOffC + ((tile - 2) >> 1) * kBlkC + ((tile - 2) & 1) * 8192;
+                st_shared_v4(sm + base + (t >> 3) * 1024 + (t & 7) * 128 + c * 16, 0u, 0u, 0u, 0u);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- group 1: P1^T, P3^T, [Q K^T; K K^T], dVb^T
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // over v
+                umma_bf16(tmem + kCP1, sdesc_sw128(sb + kOffH + kk * 2048, 16384, 1024),
+                          sdesc_sw128(sb + kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32, 16, 1024),
+                          kIdMnK, kk > 0);
+#pragma unroll
+            for (int pz = 0; pz < 2; ++pz)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // over v; V' hi, then lo
+                    umma_bf16(tmem + kCP3, sdesc_sw128(sb + kOffB + 8192 + kk * 2048, kBlkB, 1024),
+                              sdesc_sw128(sb + kOffD + pz * 16384 + (kk >> 2) * 8192 + (kk & 3) * 32,
+                                          16, 1024),
+                              kIdMnK, (pz | kk) != 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // over keys
+                umma_bf16(tmem + kCQK,
+                          sdesc_sw128(sb + kOffC + (kk >> 2) * kBlkC + (kk & 3) * 32, 16, 1024),
+                          sdesc_sw128(sb + kOffC + 8192 + (kk >> 2) * kBlkC + (kk & 3) * 32, 16,
+                                      1024),
+                          kIdKK, kk > 0);
+#pragma unroll
+            for (int t3 = 0; t3 < 3; ++t3) {  // dV' hi T hi, dV' hi T lo, dV' lo T hi
+                const uint32_t oa = kOffF + (t3 == 2 ? kFdvLo : kFdvHi);
+                const uint32_t ob = kOffF + (t3 == 1 ? kFtLo : kFtHi);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // over tokens i
+                    umma_bf16(tmem + kCDvb, sdesc_sw128(sb + oa + kk * 2048, 8192, 1024),
+                              sdesc_sw128(sb + ob + kk * 2048, 8192, 1024), kIdMnMn,
+                              (t3 | kk) != 0);
+            }
+            umma_commit(&bars[1]);
+        }
+        {  // <E, h> over the two images (the same layout), meanwhile
+            float eh = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+                const int c = tid + kThreads * rr;  // 16-byte chunk of a 32 KB image
+                float ev[8], hv[8];
+                ld_bf16x8(sm + kOffB + (c >> 10) * kBlkB + 8192 + (c & 1023) * 16, ev);
+                ld_bf16x8(sm + kOffH + c * 16, hv);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) eh = fmaf(ev[u], hv[u], eh);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) eh += __shfl_xor_sync(0xffffffffu, eh, off);
+            if (lane_id == 0) mf[kEh + warp] = eh;
+        }
+        ok = mbar_wait(&bars[1], ph, p.status);
+        if (__syncthreads_or(!ok)) break;  // also: every thread is done with the E image
+        tc_fence_after();
+        // ---- epilogue 1 (lanes = value columns / keys, columns = tokens)
+        {
+            float f[32], x[32];
+            tmem_load32f(tl + kCDvb + j0, f);  // dVb[j][v = r]
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int j = j0 + u;
+                const bool in = j < len;
+                if (in)
+                    dv[((t0 + j) * H + hh) * kD + r] = __float2bfloat16_rn(mf[kVB + j] * f[u]);
+                x[u] = in ? f[u] * __bfloat162float(vin[tok_at(p.sv, t0 + j, hh) + r]) : 0.f;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(f[u]);
+                const uint32_t o = kOffB + (r >> 6) * kBlkB + sw128_off(j, r & 63, 64);
+                *reinterpret_cast<__nv_bfloat16 *>(sm + o + 8192) = hi;
+                *reinterpret_cast<__nv_bfloat16 *>(sm + o + 16384) =
+                    __float2bfloat16_rn(f[u] - __bfloat162float(hi));
+            }
+            mf[kR4 + 64 * q4 + j0 + lane_id] = warp_colsum32(x, lane_id);
+            const uint32_t oq = kOffC + (r >> 6) * kBlkC;
+            tmem_load32f(tl + kCP1 + j0, f);  // P1[i][key = r]
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[u] = f[u] * bf16_at(sm + oq + sw128_off(j0 + u, r & 63, 64));
+            mf[kR1 + 64 * q4 + j0 + lane_id] = warp_colsum32(x, lane_id);
+            tmem_load32f(tl + kCP3 + j0, f);  // P3[i][key = r]
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                x[u] = f[u] * bf16_at(sm + oq + 8192 + sw128_off(j0 + u, r & 63, 64));
+            mf[kR3 + 64 * q4 + j0 + lane_id] = warp_colsum32(x, lane_id);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- group 2: [dm; Y], the dVb lo part of Y, (dVb h^T)^T
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int pz = 0; pz < 2; ++pz)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // over v; V' hi, then lo
+                    umma_bf16(tmem + kCDmY,
+                              sdesc_sw128(sb + kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32, 16, 1024),
+                              sdesc_sw128(sb + kOffD + pz * 16384 + (kk >> 2) * 8192 + (kk & 3) * 32,
+                                          16, 1024),
+                              kIdKK, (pz | kk) != 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // [dVb hi; dVb lo] V' hi^T: rows 64-127 used
+                umma_bf16(tmem + kCDvb,
+                          sdesc_sw128(sb + kOffB + 8192 + (kk >> 2) * kBlkB + (kk & 3) * 32, 16,
+                                      1024),
+                          sdesc_sw128(sb + kOffD + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                          kIdKK, kk > 0);
+#pragma unroll
+            for (int pz = 0; pz < 2; ++pz)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // over v; dVb hi, then lo
+                    umma_bf16(tmem + kCKb, sdesc_sw128(sb + kOffH + kk * 2048, 16384, 1024),
+                              sdesc_sw128(sb + kOffB + 8192 + pz * 8192 + (kk >> 2) * kBlkB +
+                                              (kk & 3) * 32,
+                                          16, 1024),
+                              kIdMnK, (pz | kk) != 0);
+            umma_commit(&bars[2]);
+        }
+        ok = mbar_wait(&bars[2], ph, p.status);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        // ---- epilogue 2 (stacked rows: lanes 0-63 row i of dm, 64-127 of Y)
+        {
+            float f[32], g[32];
+            if (q4 < 2) {
+                const int i = r;
+                tmem_load32f(tl + kCDmY + j0, f);  // dm[i][j]
+                tmem_load32f(tl + kCQK + j0, g);   // (Q K^T)[i][j]
+                const float Gi = mf[kVG + i];
+                float z[32], rowR = 0.f;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int j = j0 + u;
+                    const bool c = i < len && j <= i;
+                    const float d = c ? expf(Gi - mf[kVG + j]) : 0.f;
+                    z[u] = scale * f[u] * d;
+                    g[u] = z[u] * g[u];  // R = Z * (Q K^T)
+                    rowR += g[u];
+                }
+                mf[kRowR + 64 * hf + i] = rowR;
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    const uint32_t o = sw128_chunk(i, (j0 >> 3) + c8, 64);
+                    st_split8(sm + kOffF + kFzHi + o, sm + kOffF + kFzLo + o, z + 8 * c8);
+                }
+                mf[kColR + 64 * q4 + j0 + lane_id] = warp_colsum32(g, lane_id);
+            } else {
+                const int i = r - 64;
+                tmem_load32f(tl + kCDmY + j0, f);  // Y[i][j], dVb hi part
+                tmem_load32f(tl + kCDvb + j0, g);  // dVb lo part
+#pragma unroll
+                for (int u = 0; u < 32; ++u) f[u] += g[u];
+                tmem_load32f(tl + kCQK + j0, g);  // (K K^T)[i][j]
+                const float Gi = mf[kVG + i], bi = mf[kVB + i];
+                float rdA = 0.f;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int j = j0 + u;
+                    const bool sl = i < len && j < i;
+                    const float d = sl ? expf(Gi - mf[kVG + j]) : 0.f;
+                    const float dA = sl ? -f[u] : 0.f;
+                    const float kd = g[u] * d;
+                    rdA = fmaf(dA, kd, rdA);
+                    g[u] = bi * dA * kd;
+                    sS[i * 64 + (j ^ (i & 31))] = bi * dA * d;
+                }
+                mf[kRdA + 64 * hf + i] = rdA;
+                mf[kColRA + 64 * (q4 - 2) + j0 + lane_id] = warp_colsum32(g, lane_id);
+            }
+            // r2 = rowdot(dKb, K), dKb = -dVb h^T
+            tmem_load32f(tl + kCKb + j0, f);
+            const uint32_t ok_ = kOffC + (r >> 6) * kBlkC + 8192;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) f[u] = -f[u] * bf16_at(sm + ok_ + sw128_off(j0 + u, r & 63, 64));
+            mf[kR2 + 64 * q4 + j0 + lane_id] = warp_colsum32(f, lane_id);
+        }
+        __syncthreads();
+        // S + S^T (S strictly lower) -> hi / lo tiles
+        for (int c = tid; c < 512; c += kThreads) {
+            const int i = c >> 3, jc = c & 7;
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = 8 * jc + u;
+                x[u] = j < i ? sS[i * 64 + (j ^ (i & 31))]
+                             : (j > i ? sS[j * 64 + (i ^ (j & 31))] : 0.f);
+            }
+            const uint32_t o = sw128_chunk(i, jc, 64);
+            st_split8(sm + kOffF + kFsHi + o, sm + kOffF + kFsLo + o, x);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- group 3: (Z K)^T, (Z^T Q + (S + S^T) K)^T
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int pz = 0; pz < 2; ++pz)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)  // over tokens j; Z hi, then lo
+                    umma_bf16(tmem + kCXq, sdesc_sw128(sb + kOffC + 8192 + kk * 2048, kBlkC, 1024),
+                              sdesc_sw128(sb + kOffF + kFzHi + pz * 8192 + kk * 32, 16, 1024),
+                              kIdMnK, (pz | kk) != 0);
+#pragma unroll
+            for (int t4 = 0; t4 < 4; ++t4) {  // Q^T Z hi, Q^T Z lo, K^T Ss hi, K^T Ss lo
+                const uint32_t oa = kOffC + (t4 < 2 ? 0u : 8192u);
+                const uint32_t ob = kOffF + (t4 < 2 ? kFzHi : kFsHi) + (t4 & 1) * 8192;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(tmem + kCXk, sdesc_sw128(sb + oa + kk * 2048, kBlkC, 1024),
+                              sdesc_sw128(sb + ob + kk * 2048, 8192, 1024), kIdMnMn,
+                              (t4 | kk) != 0);
+            }
+            umma_commit(&bars[3]);
+        }
+        ok = mbar_wait(&bars[3], ph, p.status);
+        if (__syncthreads_or(!ok)) break;  // every MMA of the item done: tiles free
+        tc_fence_after();
+        if (tid == 0 && next < n_items) issue_loads(next);
+        // ---- epilogue 3: dq, dk (lanes = keys)
+        {
+            float f[32], x[32];
+            tmem_load32f(tl + kCP1 + j0, f);
+            tmem_load32f(tl + kCXq + j0, x);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int i = j0 + u;
+                if (i < len)
+                    dq[((t0 + i) * H + hh) * kD + r] =
+                        __float2bfloat16_rn(fmaf(scale * mf[kVGam + i], f[u], x[u]));
+            }
+            float kb[32];
+            tmem_load32f(tl + kCP3 + j0, f);
+            tmem_load32f(tl + kCXk + j0, x);
+            tmem_load32f(tl + kCKb + j0, kb);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int i = j0 + u;
+                if (i < len) {
+                    const float y = fmaf(mf[kVLam + i], f[u], x[u]);
+                    dk[((t0 + i) * H + hh) * kD + r] =
+                        __float2bfloat16_rn(fmaf(-mf[kVB + i] * mf[kVGam + i], kb[u], y));
+                }
+            }
+        }
+        __syncthreads();
+        // ---- dbeta and the gate gradient
+        if (tid < 64) {
+            const int i = tid;
+            float r1 = 0.f, r2 = 0.f, r3 = 0.f, r4 = 0.f;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                r1 += mf[kR1 + 64 * qq + i];
+                r2 += mf[kR2 + 64 * qq + i];
+                r3 += mf[kR3 + 64 * qq + i];
+                r4 += mf[kR4 + 64 * qq + i];
+            }
+            const float rowR = mf[kRowR + i] + mf[kRowR + 64 + i];
+            const float colR = mf[kColR + i] + mf[kColR + 64 + i];
+            const float rdA = mf[kRdA + i] + mf[kRdA + 64 + i];
+            const float colRA = mf[kColRA + i] + mf[kColRA + 64 + i];
+            const float gam = mf[kVGam + i], lam = mf[kVLam + i], bi = mf[kVB + i];
+            float dG = 0.f;
+            if (i < len) {
+                dG = scale * gam * r1 + (rowR - colR) - lam * r3 + bi * rdA - colRA + bi * gam * r2;
+                args.a.dbeta[(t0 + i) * H + hh] = r4 + gam * r2 + rdA;
+            }
+            mf[kDg + i] = dG;
+            mf[kR3f + i] = r3;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            // the chunk's last token also carries the state terms: e^{G_last}
+            // <E, h> and sum_j lam_j rowdot(P3, K)_j
+            float eh = 0.f;
+            for (int w = 0; w < kThreads / 32; ++w) eh += mf[kEh + w];
+            float lam3 = 0.f;
+            for (int j = 0; j < len; ++j) lam3 = fmaf(mf[kVLam + j], mf[kR3f + j], lam3);
+            mf[kDg + len - 1] += fmaf(mf[kVGam + len - 1], eh, lam3);
+            float run = 0.f;
+            for (int i = len - 1; i >= 0; --i) {
+                run += mf[kDg + i];
+                args.a.dg[(t0 + i) * H + hh] = run;
+            }
+        }
+        tc_fence_before();
+        __syncthreads();  // TMEM, the tiles and the scalars are reused
+        item = next;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t tc_bwd_grad(const Problem &p, const Workspace &ws, const BwdArgs &a, const float *dvn,
+                        const float *Tm, cudaStream_t st) {
+    if (ws.max_chunks == 0) return cudaSuccess;
+    GradArgs args;
+    args.p = p;
+    args.ws = ws;
+    args.a = a;
+    args.dvn = dvn;
+    args.Tm = Tm;
+    const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
+    const uint64_t H = (uint64_t)p.H;
+    if (!make_tmap_bf16_3d(&args.tq, p.q, kD, H, rows, p.sq.h * 2, p.sq.t * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.tdo, a.dout, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(k_tc_bwd_grad,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemLaunch);
+    if (err != cudaSuccess) return err;
+    const int64_t items = ws.max_chunks * p.H;  // an upper bound; the kernel reads the count
+    const dim3 grid((unsigned)persistent_grid(p, items, 1));
+    return launch_pdl(k_tc_bwd_grad, grid, dim3(kThreads), kSmemLaunch, st, args);
+}
+
+}  // namespace gdr

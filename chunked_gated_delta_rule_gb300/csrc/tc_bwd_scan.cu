@@ -24,9 +24,9 @@
 //   E^T += dO^T Q~               tcgen05
 //   E^T += (-dV'^T) W            tcgen05, A = BF16 -dV'^T
 //
-// dV' is stored in FP32 for the local-gradient kernel, and the BF16 images
-// of the E^T mirror and the -dV'^T tile for the L x K products
-// (tc_bwd_lk.cu); dh0 is E after the sequence's first chunk.  The state stays FP32 in TMEM; its BF16 mirror,
+// dV' is stored in FP32 and the byte image of the E^T mirror in BF16, for the
+// per-chunk gradients (tc_bwd_grad.cu); dh0 is E after the sequence's first
+// chunk.  The state stays FP32 in TMEM; its BF16 mirror,
 // dV' and dO are the MMA operands (the route's tolerance covers them).
 //
 // Warps: 0-3 state path (the serial dependency: E mirror and image, decay,
@@ -47,7 +47,7 @@ using namespace tc;
 struct BwdScanArgs {
     Problem p;
     Workspace ws;
-    uint8_t *lkimg;     // [chunks][H][kLkImgBytes]: E^T and -dV'^T images written here
+    uint8_t *lkimg;     // [chunks][H][kLkImgBytes]: the E^T image written here
     float *dvn;         // [chunks][H][64][V] dV'
     const float *dht;   // state layout of h0, or nullptr
     float *dh0;         // state layout of h0, or nullptr
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                     }
                 };
                 // E's BF16 mirror (the A operand of E^T K~^T), and its image
-                // for the L x K products: the chain's critical path goes first
+                // for the per-chunk gradients: the chain's critical path goes first
                 uint8_t *limg = args.lkimg + item * kLkImgBytes;
 #pragma unroll 1
                 for (int hq = 0; hq < 2; ++hq) {
@@ -355,7 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                         for (int c8 = 0; c8 < 4; ++c8) {
                             const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
                             st_bf16x8(sm + kOffDv + ou, u + 8 * c8);
-                            st_bf16x8(args.lkimg + item * kLkImgBytes + kLkImgDv + ou, u + 8 * c8);
                         }
                     }
                 }

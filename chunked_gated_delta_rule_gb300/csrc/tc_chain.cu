@@ -53,8 +53,9 @@ namespace {
 using namespace tc;
 
 // kModeRecompute: the serial scan of the tensor-core backward's forward
-// recompute: no output, and per chunk the FP32 state before the chunk and
-// v_new go to the workspace (h_pre, v_new) for the backward's kernels.
+// recompute: no output; per chunk v_new (FP32) and the byte image of the BF16
+// mirror of the state before the chunk go to the workspace for the
+// backward's kernels.
 enum TcMode { kModeSerial = 0, kModePre = 1, kModeSegOut = 2, kModeRecompute = 3 };
 
 struct TcArgs {
@@ -381,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 };
                 // h_pre -> BF16 mirror (the first product's A operand): the
                 // chain's critical path, so it goes first
-                // the recompute's images of the chunk's h^T mirror and
-                // v_new^T tile, for the backward's L x K products
+                // the recompute's image of the chunk's h^T mirror, for the
+                // backward's per-chunk gradients
                 uint8_t *limg = MODE == kModeRecompute
                                     ? ws.bwd_lkimg + ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes
                                     : nullptr;
@@ -459,11 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         for (int c8 = 0; c8 < 4; ++c8) {
                             const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
                             st_bf16x8(sm + kOffVn + ou, u + 8 * c8);
-                            if (MODE == kModeRecompute)
-                                st_bf16x8(ws.bwd_lkimg +
-                                              ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes +
-                                              kLkImgV + ou,
-                                          u + 8 * c8);
                         }
                     }
                 }

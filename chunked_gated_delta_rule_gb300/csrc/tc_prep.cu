@@ -83,7 +83,7 @@ __device__ __forceinline__ void scale_rows_in_place(uint8_t *a, const float *f, 
     }
 }
 
-// kBwd: the backward's recompute also stores G, Kd, Mq and T (a separate
+// kBwd: the backward's recompute also stores G and T (a separate
 // instantiation, so that the forward's kernel carries none of it).
 template <bool kBwd>
 __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__ PrepArgs args) {
@@ -216,25 +216,6 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
             const int j0 = 32 * half;
             // A rows keep j < i (beta_i folded in); P rows keep j <= i.
             const int jlim = quad < 2 ? i : i + 1;
-            if (kBwd) {  // the backward's Kd = (K K^T * D, j < i), Mq = (Q K^T * D, j <= i)
-                float x[32];
-                if (sScal[2] != 0.f) {
-                    const float ri = sEP[i];
-#pragma unroll
-                    for (int u = 0; u < 32; ++u)
-                        x[u] = (j0 + u < jlim) ? f[u] * (ri * sDec[j0 + u]) : 0.f;
-                } else {
-                    const float gi = sG[i];
-#pragma unroll
-                    for (int u = 0; u < 32; ++u)
-                        x[u] = (j0 + u < jlim) ? f[u] * __expf(gi - sG[j0 + u]) : 0.f;
-                }
-                float4 *dst = reinterpret_cast<float4 *>(
-                    (quad < 2 ? ws.bwd_Kd : ws.bwd_Mq) + ((int64_t)item * kChunk + i) * kChunk + j0);
-#pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4)
-                    dst[c4] = make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
-            }
             const float rowf = quad < 2 ? sBeta[i] : p.scale;
             if (sScal[2] != 0.f) {  // e^{G_i - G_j} = e^{G_i - G_last} e^{G_last - G_j}
                 const float ri = rowf * sEP[i];
