@@ -293,12 +293,13 @@ def bwd_algorithmic(kernel, x, c):
         return (ch * (2 * 16384 + 8192 + 272) + th * (K + V) * es + ch * L * V * f32
                 + ch * K * V * 2 + 2 * st, None)
     elif kernel == "tc_bwd_grad":
-        # h and E images, dO, q, k, v, T, dV', v_new, G, beta read; dq, dk,
-        # dv, dbeta, dg written.  Multiply-adds as issued: the hi / lo halves
-        # of the FP32 operands count twice (27 products of 128 x 64 x 64).
+        # h and E images, dO, q, k, v, T, dV', v_new (the FP32 operands as
+        # BF16 hi + lo pairs: as many bytes as FP32), G, beta read; dq, dk,
+        # dv, dbeta, dg written.  Its products run on the tensor cores, well
+        # below their peak: HBM-bound.
         return (ch * 2 * K * V * 2 + th * (2 * V + 2 * K) * es + ch * L * L * f32
                 + 2 * ch * L * V * f32 + ch * L * f32 + th * f32
-                + th * (2 * K + V) * es + 2 * th * f32, 2.0 * ch * 27 * 128 * 64 * 64)
+                + th * (2 * K + V) * es + 2 * th * f32, None)
     elif kernel == "simt_prep":
         b = algorithmic_bytes(kernel, x, c)
         fma = ch * ((L * L * K / 2 + L ** 3 / 6 + L * L * (K + V) / 2) if delta else 0)

@@ -409,8 +409,7 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     L.off_W = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
     L.off_U = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
     L.off_hpre = take(simt ? sizeof(float) * (size_t)mc * H * K * V : 0);
-    L.off_vnew = take((simt || recompute) && delta ? sizeof(float) * (size_t)mc * H * kChunk * V
-                                                   : 0);
+    L.off_vnew = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
     const size_t segs = S > 1 ? (size_t)ns * H * (size_t)S : 0;
     L.off_segM = take(delta ? sizeof(float) * segs * K * K : 0);
     L.off_segC = take(sizeof(float) * segs * K * V);
@@ -463,14 +462,14 @@ BwdLayout bwd_layout(const gdr_dims &d, bool beta_free, int n_segments, bool tc_
     const bool delta = !beta_free;
     const size_t items = (size_t)B.fwd.max_chunks * (size_t)d.H;
     const size_t K = (size_t)d.K, V = (size_t)d.V, sq = (size_t)kChunk * kChunk;
-    // the tensor-core route keeps T, dV' and the images; the CUDA-core route
-    // every buffer of BwdWs
+    // the tensor-core route keeps its operands in the images; the CUDA-core
+    // route every buffer of BwdWs
     const bool cc = !tc_route;
     B.off_Mq = take(cc ? sizeof(float) * items * sq : 0);
     B.off_Kd = take(cc && delta ? sizeof(float) * items * sq : 0);
-    B.off_Tm = take(delta ? sizeof(float) * items * sq : 0);
+    B.off_Tm = take(cc && delta ? sizeof(float) * items * sq : 0);
     B.off_dhend = take(cc ? sizeof(float) * items * K * V : 0);
-    B.off_dvn = take(delta ? sizeof(float) * items * kChunk * V : 0);
+    B.off_dvn = take(cc && delta ? sizeof(float) * items * kChunk * V : 0);
     B.off_P1 = take(cc ? sizeof(float) * items * kChunk * K : 0);
     B.off_P2 = take(cc && delta ? sizeof(float) * items * kChunk * K : 0);
     B.off_P3 = take(cc ? sizeof(float) * items * kChunk * K : 0);
@@ -572,8 +571,8 @@ int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs
     if (route == 2) {
         GDR_LAUNCH(rec, kKTcPrep, tc_prep(p, ws, st));
         GDR_LAUNCH(rec, kKTcRecompute, tc_chain(p, ws, 3, st));
-        GDR_LAUNCH(rec, kKTcBwdScan, tc_bwd_scan(p, ws, bw.dvn, a.dht, a.dh0, a.dout, st));
-        GDR_LAUNCH(rec, kKTcBwdGrad, tc_bwd_grad(p, ws, a, bw.dvn, bw.Tm, st));
+        GDR_LAUNCH(rec, kKTcBwdScan, tc_bwd_scan(p, ws, a.dht, a.dh0, a.dout, st));
+        GDR_LAUNCH(rec, kKTcBwdGrad, tc_bwd_grad(p, ws, a, st));
         return GDR_OK;
     }
     GDR_LAUNCH(rec, kKPrep, simt_prep(p, ws, st));
@@ -916,7 +915,6 @@ int gdr_chunk_bwd(const gdr_dims *dims, const void *q, const void *k, const void
     const BwdWs bw = carve_bwd(base, B);
     ws.bwd_tc = route == 2;
     if (ws.bwd_tc) {
-        ws.bwd_Tm = bw.Tm;
         ws.bwd_lkimg = static_cast<uint8_t *>(base) + B.off_lkimg;
     }
     BwdArgs a{};

@@ -104,15 +104,14 @@ cudaError_t convert_bf16_to_f16(const void *src, void *dst, int64_t n, cudaStrea
 cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
                      cudaStream_t st, LaunchRecorder &rec);
 // The reverse state-gradient scan on the tensor cores (BF16, K = V = 128,
-// delta rule, serial): dV' into dvn, the E^T and -dV'^T images into
-// ws.bwd_lkimg, dh0.
-cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, float *dvn, const float *dht,
-                        float *dh0, const void *dout, cudaStream_t st);
+// delta rule, serial): the E^T and dV'^T images into ws.bwd_lkimg, dh0.
+cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, const float *dht, float *dh0,
+                        const void *dout, cudaStream_t st);
 // Every per-chunk gradient of the backward on the tensor cores (dq, dk, dv,
-// dbeta, dg), from the images in ws.bwd_lkimg (h and E), dO, q, k, v, dV'
-// (dvn), v_new (ws.vnew), T (Tm) and G (ws.G).
-cudaError_t tc_bwd_grad(const Problem &p, const Workspace &ws, const BwdArgs &a, const float *dvn,
-                        const float *Tm, cudaStream_t st);
+// dbeta, dg), from the images in ws.bwd_lkimg (h, E, v_new, dV', T), dO, q,
+// k, v and G (ws.G).
+cudaError_t tc_bwd_grad(const Problem &p, const Workspace &ws, const BwdArgs &a,
+                        cudaStream_t st);
 // Composition for the delta rule with K <= 128 and V % 32 == 0 (both paths):
 // bulk-copied transposed transitions, 32 value columns per CTA.
 bool compose_mt_supported(const Problem &p);

@@ -43,9 +43,7 @@ struct GradArgs {
     Problem p;
     Workspace ws;
     BwdArgs a;
-    const float *dvn;  // [items][64][V] dV'
-    const float *Tm;   // [items][64][64] T
-    CUtensorMap tq, tk, tdo;
+    CUtensorMap tq, tk, tv, tdo;
 };
 
 constexpr int kThreads = 256;
@@ -57,10 +55,13 @@ constexpr int kThreads = 256;
 //                      the E^T image's key block b sits in the dVb rows until
 //                      dVb is written
 //   C  [80, 112 KB)    per key block b (16 KB): q rows | k rows
-//   D  [112, 144 KB)   V' hi | V' lo ([t][v])
-//   F  [144, 192 KB)   dV' hi | dV' lo ([i][v]) | T hi | T lo ([i][j]); after
-//                      the first group: Z hi | Z lo | (S + S^T) hi | lo |
-//                      S in FP32 (row i at 64 i, column j at j ^ (i % 32))
+//   D  [112, 144 KB)   V'^T hi | V'^T lo ([v][t], 128 rows)
+//   F  [144, 192 KB)   dV'^T hi | dV'^T lo ([v][i], 128 rows) | T hi | T lo
+//                      ([i][j]); after the first group: Z hi | Z lo |
+//                      (S + S^T) hi | lo | S in FP32 (row i at 64 i, column j
+//                      at j ^ (i % 32))
+//   V  [192, 208 KB)   v rows
+// The images (h, E, V', dV', T) arrive by bulk copies, dO, q, k and v by TMA.
 constexpr uint32_t kOffH = 0;
 constexpr uint32_t kOffB = 32768;
 constexpr uint32_t kBlkB = 24576;
@@ -70,7 +71,8 @@ constexpr uint32_t kOffD = kOffC + 2 * kBlkC;
 constexpr uint32_t kOffF = kOffD + 32768;
 constexpr uint32_t kFdvHi = 0, kFdvLo = 16384, kFtHi = 32768, kFtLo = 40960;
 constexpr uint32_t kFzHi = 0, kFzLo = 8192, kFsHi = 16384, kFsLo = 24576, kFs32 = 32768;
-constexpr uint32_t kOffMisc = kOffF + 49152;
+constexpr uint32_t kOffV = kOffF + 49152;  // v rows ([t][v], two 64-column blocks)
+constexpr uint32_t kOffMisc = kOffV + 16384;
 // FP32 scalars in the misc area: gate vectors, per-warp partial row sums
 constexpr int kVG = 0, kVGam = 64, kVLam = 128, kVB = 192;
 constexpr int kR1 = 256, kR2 = kR1 + 256, kR3 = kR2 + 256, kR4 = kR3 + 256;  // [4 lane quarters][64]
@@ -82,7 +84,7 @@ constexpr int kNumBars = 4;  // tiles landed, then one per MMA group
 constexpr uint32_t kSmemLaunch = kOffBar + 8 * kNumBars + 16 + 1024;
 static_assert(kOffBar % 8 == 0, "barrier alignment");
 static_assert(kSmemLaunch <= 232448, "shared memory per CTA");
-constexpr uint32_t kLoadBytes = 32768 + 32768 + 3 * 16384;  // h, E images; dO, q, k tiles
+constexpr uint32_t kLoadBytes = 4 * 32768 + 16384 + 4 * 16384;  // h, E, V', dV', T; dO, q, k, v
 
 // TMEM columns (128 lanes each, FP32), 64 columns per accumulator
 constexpr uint32_t kTmemCols = 512;
@@ -97,6 +99,7 @@ constexpr uint32_t kCXk = 448;   // (Z^T Q + (S + S^T) K)^T
 
 constexpr uint32_t kIdMnK = idesc_bf16(128, 64, 1, 0);   // A MN-major, B K-major
 constexpr uint32_t kIdKK = idesc_bf16(128, 64, 0, 0);    // both K-major
+constexpr uint32_t kIdKMn = idesc_bf16(128, 64, 0, 1);   // A K-major, B MN-major
 constexpr uint32_t kIdMnMn = idesc_bf16(128, 64, 1, 1);  // both MN-major
 
 // Column sums of a warp's 32 x 32 block: on entry lane l holds x[c] = entry
@@ -121,19 +124,6 @@ __device__ __forceinline__ float bf16_at(const uint8_t *p) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
 }
 
-// Eight FP32 values -> the BF16 chunk of their rounded values (hi) and of
-// the rounded remainders (lo).
-__device__ __forceinline__ void st_split8(uint8_t *hi, uint8_t *lo, const float *x) {
-    float h[8], l[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        h[u] = __bfloat162float(__float2bfloat16_rn(x[u]));
-        l[u] = x[u] - h[u];
-    }
-    st_bf16x8(hi, h);
-    st_bf16x8(lo, l);
-}
-
 __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_constant__ GradArgs args) {
     const Problem &p = args.p;
     const Workspace &ws = args.ws;
@@ -153,7 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
     const int j0 = 32 * hf;                       // this thread's 32 columns
     const int H = (int)p.H;
     const float scale = p.scale;
-    const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(p.v);
     __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(args.a.dq);
     __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(args.a.dk);
     __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(args.a.dv);
@@ -172,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tl = tmem + lane;
-    pdl_wait();  // images, dV', v_new, T and G from the kernels before
+    pdl_wait();  // the images and G from the kernels before
     const int n_items = *ws.n_chunks * H;
 
     auto issue_loads = [&](int it_) {
@@ -182,35 +171,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         mbar_arrive_expect_tx(&bars[0], kLoadBytes);
         bulk_load(sm + kOffH, img + kLkImgH, 16384u, &bars[0]);
         bulk_load(sm + kOffH + 16384, img + kLkImgH + 16384, 16384u, &bars[0]);
+        bulk_load(sm + kOffD, img + kLkImgVh, 16384u, &bars[0]);
+        bulk_load(sm + kOffD + 16384, img + kLkImgVl, 16384u, &bars[0]);
+        bulk_load(sm + kOffF + kFdvHi, img + kLkImgDh, 16384u, &bars[0]);
+        bulk_load(sm + kOffF + kFdvLo, img + kLkImgDl, 16384u, &bars[0]);
+        bulk_load(sm + kOffF + kFtHi, img + kLkImgTh, 8192u, &bars[0]);
+        bulk_load(sm + kOffF + kFtLo, img + kLkImgTl, 8192u, &bars[0]);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             bulk_load(sm + kOffB + b * kBlkB + 8192, img + kLkImgE + b * 16384, 16384u, &bars[0]);
             tma_load_3d(sm + kOffB + b * kBlkB, &args.tdo, &bars[0], 64 * b, hh, e.y);
             tma_load_3d(sm + kOffC + b * kBlkC, &args.tq, &bars[0], 64 * b, hh, e.y);
             tma_load_3d(sm + kOffC + b * kBlkC + 8192, &args.tk, &bars[0], 64 * b, hh, e.y);
+            tma_load_3d(sm + kOffV + b * 8192, &args.tv, &bars[0], 64 * b, hh, e.y);
         }
     };
-    // Rows [0, len) of a row-major FP32 [64][ncols] matrix (later rows read
-    // as zero) -> hi / lo BF16 tiles at off_hi / off_lo.
-    auto split_tile = [&](const float *src, int ncols, uint32_t off_hi, uint32_t off_lo, int len) {
-        const int cpr = ncols / 8;
-        for (int c = tid; c < 64 * cpr; c += kThreads) {
-            const int row = c / cpr, j = c % cpr;
-            float x[8];
-            if (row < len) {
-                const float4 a = *reinterpret_cast<const float4 *>(src + row * ncols + 8 * j);
-                const float4 b = *reinterpret_cast<const float4 *>(src + row * ncols + 8 * j + 4);
-                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-                x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-            } else {
-#pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = 0.f;
-            }
-            const uint32_t o = sw128_chunk(row, j, 64);
-            st_split8(sm + off_hi + o, sm + off_lo + o, x);
-        }
-    };
-
     int item = blockIdx.x;
     if (tid == 0 && item < n_items) issue_loads(item);
     for (uint32_t it = 0; item < n_items; ++it) {
@@ -221,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         const int len = e.z;
         const int next = item + (int)gridDim.x;
 
-        // gate vectors; the FP32 operands as hi / lo tiles
+        // gate vectors
         if (tid < 64) {
             const bool in = tid < len;
             const float G = ws.G[(int64_t)item * kChunk + tid];
@@ -231,10 +206,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
             mf[kVLam + tid] = in ? expf(Gl - G) : 0.f;
             mf[kVB + tid] = in ? p.beta[(t0 + tid) * H + hh] : 0.f;
         }
-        split_tile(args.Tm + (int64_t)item * kChunk * kChunk, 64, kOffF + kFtHi, kOffF + kFtLo,
-                   len);
-        split_tile(args.dvn + (int64_t)item * kChunk * kD, kD, kOffF + kFdvHi, kOffF + kFdvLo, len);
-        split_tile(ws.vnew + (int64_t)item * kChunk * kD, kD, kOffD, kOffD + 16384, len);
         bool ok = mbar_wait(&bars[0], ph, p.status);
         if (__syncthreads_or(!ok)) break;
         if (len < kChunk) {  // tile rows past the sequence end belong to the next one
@@ -262,9 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // over v; V' hi, then lo
                     umma_bf16(tmem + kCP3, sdesc_sw128(sb + kOffB + 8192 + kk * 2048, kBlkB, 1024),
-                              sdesc_sw128(sb + kOffD + pz * 16384 + (kk >> 2) * 8192 + (kk & 3) * 32,
-                                          16, 1024),
-                              kIdMnK, (pz | kk) != 0);
+                              sdesc_sw128(sb + kOffD + pz * 16384 + kk * 2048, 8192, 1024),
+                              kIdMnMn, (pz | kk) != 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // over keys
                 umma_bf16(tmem + kCQK,
@@ -278,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                 const uint32_t ob = kOffF + (t3 == 1 ? kFtLo : kFtHi);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // over tokens i
-                    umma_bf16(tmem + kCDvb, sdesc_sw128(sb + oa + kk * 2048, 8192, 1024),
-                              sdesc_sw128(sb + ob + kk * 2048, 8192, 1024), kIdMnMn,
+                    umma_bf16(tmem + kCDvb, sdesc_sw128(sb + oa + kk * 32, 16, 1024),
+                              sdesc_sw128(sb + ob + kk * 2048, 8192, 1024), kIdKMn,
                               (t3 | kk) != 0);
             }
             umma_commit(&bars[1]);
@@ -312,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                 const bool in = j < len;
                 if (in)
                     dv[((t0 + j) * H + hh) * kD + r] = __float2bfloat16_rn(mf[kVB + j] * f[u]);
-                x[u] = in ? f[u] * __bfloat162float(vin[tok_at(p.sv, t0 + j, hh) + r]) : 0.f;
+                x[u] = in ? f[u] * bf16_at(sm + kOffV + (r >> 6) * 8192 + sw128_off(j, r & 63, 64))
+                          : 0.f;
                 const __nv_bfloat16 hi = __float2bfloat16_rn(f[u]);
                 const uint32_t o = kOffB + (r >> 6) * kBlkB + sw128_off(j, r & 63, 64);
                 *reinterpret_cast<__nv_bfloat16 *>(sm + o + 8192) = hi;
@@ -343,16 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                 for (int kk = 0; kk < 8; ++kk)  // over v; V' hi, then lo
                     umma_bf16(tmem + kCDmY,
                               sdesc_sw128(sb + kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32, 16, 1024),
-                              sdesc_sw128(sb + kOffD + pz * 16384 + (kk >> 2) * 8192 + (kk & 3) * 32,
-                                          16, 1024),
-                              kIdKK, (pz | kk) != 0);
+                              sdesc_sw128(sb + kOffD + pz * 16384 + kk * 2048, 8192, 1024),
+                              kIdKMn, (pz | kk) != 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // [dVb hi; dVb lo] V' hi^T: rows 64-127 used
                 umma_bf16(tmem + kCDvb,
                           sdesc_sw128(sb + kOffB + 8192 + (kk >> 2) * kBlkB + (kk & 3) * 32, 16,
                                       1024),
-                          sdesc_sw128(sb + kOffD + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                          kIdKK, kk > 0);
+                          sdesc_sw128(sb + kOffD + kk * 2048, 8192, 1024), kIdKMn, kk > 0);
 #pragma unroll
             for (int pz = 0; pz < 2; ++pz)
 #pragma unroll
@@ -389,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
                     const uint32_t o = sw128_chunk(i, (j0 >> 3) + c8, 64);
-                    st_split8(sm + kOffF + kFzHi + o, sm + kOffF + kFzLo + o, z + 8 * c8);
+                    st_split_bf16x8(sm + kOffF + kFzHi + o, sm + kOffF + kFzLo + o, z + 8 * c8);
                 }
                 mf[kColR + 64 * q4 + j0 + lane_id] = warp_colsum32(g, lane_id);
             } else {
@@ -434,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                              : (j > i ? sS[j * 64 + (i ^ (j & 31))] : 0.f);
             }
             const uint32_t o = sw128_chunk(i, jc, 64);
-            st_split8(sm + kOffF + kFsHi + o, sm + kOffF + kFsLo + o, x);
+            st_split_bf16x8(sm + kOffF + kFsHi + o, sm + kOffF + kFsLo + o, x);
         }
         fence_async_smem();
         tc_fence_before();
@@ -517,19 +486,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
             mf[kR3f + i] = r3;
         }
         __syncthreads();
-        if (tid == 0) {
+        if (warp == 0) {
             // the chunk's last token also carries the state terms: e^{G_last}
-            // <E, h> and sum_j lam_j rowdot(P3, K)_j
-            float eh = 0.f;
-            for (int w = 0; w < kThreads / 32; ++w) eh += mf[kEh + w];
-            float lam3 = 0.f;
-            for (int j = 0; j < len; ++j) lam3 = fmaf(mf[kVLam + j], mf[kR3f + j], lam3);
-            mf[kDg + len - 1] += fmaf(mf[kVGam + len - 1], eh, lam3);
-            float run = 0.f;
-            for (int i = len - 1; i >= 0; --i) {
-                run += mf[kDg + i];
-                args.a.dg[(t0 + i) * H + hh] = run;
+            // <E, h> and sum_j lam_j rowdot(P3, K)_j (lam is zero past len);
+            // then dg = the suffix sums of dG, in a fixed order: lane l holds
+            // tokens 2l and 2l + 1
+            float lam3 = fmaf(mf[kVLam + lane_id], mf[kR3f + lane_id],
+                              mf[kVLam + 32 + lane_id] * mf[kR3f + 32 + lane_id]);
+            float eh = lane_id < kThreads / 32 ? mf[kEh + lane_id] : 0.f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                lam3 += __shfl_xor_sync(0xffffffffu, lam3, off);
+                eh += __shfl_xor_sync(0xffffffffu, eh, off);
             }
+            float d0 = mf[kDg + 2 * lane_id], d1 = mf[kDg + 2 * lane_id + 1];
+            const float extra = fmaf(mf[kVGam + len - 1], eh, lam3);
+            if (2 * lane_id == len - 1) d0 += extra;
+            if (2 * lane_id + 1 == len - 1) d1 += extra;
+            float suf = d0 + d1;  // inclusive suffix sum over the lanes' pairs
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, suf, off);
+                if (lane_id + off < 32) suf += y;
+            }
+            float above = __shfl_down_sync(0xffffffffu, suf, 1);
+            if (lane_id == 31) above = 0.f;
+            const float run1 = above + d1, run0 = run1 + d0;
+            if (2 * lane_id < len) args.a.dg[(t0 + 2 * lane_id) * H + hh] = run0;
+            if (2 * lane_id + 1 < len) args.a.dg[(t0 + 2 * lane_id + 1) * H + hh] = run1;
         }
         tc_fence_before();
         __syncthreads();  // TMEM, the tiles and the scalars are reused
@@ -542,19 +526,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
 
 }  // namespace
 
-cudaError_t tc_bwd_grad(const Problem &p, const Workspace &ws, const BwdArgs &a, const float *dvn,
-                        const float *Tm, cudaStream_t st) {
+cudaError_t tc_bwd_grad(const Problem &p, const Workspace &ws, const BwdArgs &a,
+                        cudaStream_t st) {
     if (ws.max_chunks == 0) return cudaSuccess;
     GradArgs args;
     args.p = p;
     args.ws = ws;
     args.a = a;
-    args.dvn = dvn;
-    args.Tm = Tm;
     const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;
     const uint64_t H = (uint64_t)p.H;
     if (!make_tmap_bf16_3d(&args.tq, p.q, kD, H, rows, p.sq.h * 2, p.sq.t * 2, 64, 1, 64) ||
         !make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&args.tv, p.v, kD, H, rows, p.sv.h * 2, p.sv.t * 2, 64, 1, 64) ||
         !make_tmap_bf16_3d(&args.tdo, a.dout, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(k_tc_bwd_grad,

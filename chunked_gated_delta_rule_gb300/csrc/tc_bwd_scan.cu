@@ -24,9 +24,9 @@
 //   E^T += dO^T Q~               tcgen05
 //   E^T += (-dV'^T) W            tcgen05, A = BF16 -dV'^T
 //
-// dV' is stored in FP32 and the byte image of the E^T mirror in BF16, for the
-// per-chunk gradients (tc_bwd_grad.cu); dh0 is E after the sequence's first
-// chunk.  The state stays FP32 in TMEM; its BF16 mirror,
+// dV'^T is stored as a pair of BF16 images (hi + lo) and the E^T mirror as
+// its byte image, for the per-chunk gradients (tc_bwd_grad.cu); dh0 is E
+// after the sequence's first chunk.  The state stays FP32 in TMEM; its BF16 mirror,
 // dV' and dO are the MMA operands (the route's tolerance covers them).
 //
 // Warps: 0-3 state path (the serial dependency: E mirror and image, decay,
@@ -47,8 +47,7 @@ using namespace tc;
 struct BwdScanArgs {
     Problem p;
     Workspace ws;
-    uint8_t *lkimg;     // [chunks][H][kLkImgBytes]: the E^T image written here
-    float *dvn;         // [chunks][H][64][V] dV'
+    uint8_t *lkimg;     // [chunks][H][kLkImgBytes]: the E^T and dV'^T images written here
     const float *dht;   // state layout of h0, or nullptr
     float *dh0;         // state layout of h0, or nullptr
     CUtensorMap tk;     // k, loaded into the stage for K~
@@ -334,27 +333,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                 }
                 if (!wait(kBAdone, gk)) { ok = false; break; }
                 tc_fence_after();
-                {  // dV'^T: stored in FP32, and -dV'^T in BF16 for the update
+                {  // dV'^T: its hi + lo images for the gradients, -dV'^T in BF16 for the update
                     uint32_t w0[32], w1[32];
                     tmem_ld32(tmem + lane + kColD + 128 * b, w0);
                     tmem_ld32(tmem + lane + kColD + 128 * b + 32, w1);
                     tmem_wait_ld();
                     reg_fence(w0);
                     reg_fence(w1);
-                    float *dv = args.dvn + item * kChunk * kD + row;  // [t][v]
+                    uint8_t *dimg = args.lkimg + item * kLkImgBytes;
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        float u[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float d = __uint_as_float(hh ? w1[i] : w0[i]);
-                            dv[(32 * hh + i) * kD] = d;
-                            u[i] = -d;
-                        }
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8) {
+                            float d[8], u[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                d[i] = __uint_as_float(hh ? w1[8 * c8 + i] : w0[8 * c8 + i]);
+                                u[i] = -d[i];
+                            }
                             const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
-                            st_bf16x8(sm + kOffDv + ou, u + 8 * c8);
+                            st_bf16x8(sm + kOffDv + ou, u);
+                            st_split_bf16x8(dimg + kLkImgDh + ou, dimg + kLkImgDl + ou, d);
                         }
                     }
                 }
@@ -431,13 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
 
 }  // namespace
 
-cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, float *dvn, const float *dht,
-                        float *dh0, const void *dout, cudaStream_t st) {
+cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, const float *dht, float *dh0,
+                        const void *dout, cudaStream_t st) {
     BwdScanArgs args;
     args.p = p;
     args.ws = ws;
     args.lkimg = ws.bwd_lkimg;
-    args.dvn = dvn;
     args.dht = dht;
     args.dh0 = dh0;
     const uint64_t rows = (uint64_t)p.B * (uint64_t)p.T;

@@ -53,9 +53,9 @@ namespace {
 using namespace tc;
 
 // kModeRecompute: the serial scan of the tensor-core backward's forward
-// recompute: no output; per chunk v_new (FP32) and the byte image of the BF16
-// mirror of the state before the chunk go to the workspace for the
-// backward's kernels.
+// recompute: no output; per chunk the byte image of the BF16 mirror of the
+// state before the chunk, and v_new as a pair of BF16 images (hi + lo), go
+// to the workspace for the backward's kernels.
 enum TcMode { kModeSerial = 0, kModePre = 1, kModeSegOut = 2, kModeRecompute = 3 };
 
 struct TcArgs {
@@ -450,16 +450,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         }
 #pragma unroll
                         for (int i = 0; i < 32; ++i) u[i] -= __uint_as_float(hh ? w1[i] : w0[i]);
-                        if (MODE == kModeRecompute) {  // FP32 v_new, [t][v]
-                            float *vn = ws.vnew + (((int64_t)(C.c_begin + cc) * H + h) * kChunk +
-                                                   32 * hh) * kD + row;
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) vn[i * kD] = u[i];
-                        }
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8) {
                             const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
                             st_bf16x8(sm + kOffVn + ou, u + 8 * c8);
+                            if (MODE == kModeRecompute) {  // v_new^T as BF16 hi + lo images
+                                uint8_t *vimg = ws.bwd_lkimg +
+                                                ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes;
+                                st_split_bf16x8(vimg + kLkImgVh + ou, vimg + kLkImgVl + ou,
+                                                u + 8 * c8);
+                            }
                         }
                     }
                 }

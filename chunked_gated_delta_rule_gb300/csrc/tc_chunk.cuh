@@ -50,6 +50,20 @@ __device__ __forceinline__ void st_bf16x8(void *p, const float *x) {
                    pack_bf16x2(x[6], x[7]));
 }
 
+// Eight FP32 values -> the BF16 chunk of their rounded values at `hi` and of
+// the rounded remainders x - hi at `lo` (shared or global): the pair carries
+// about 16 significant bits of x.
+__device__ __forceinline__ void st_split_bf16x8(void *hi, void *lo, const float *x) {
+    float h[8], l[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        h[u] = __bfloat162float(__float2bfloat16_rn(x[u]));
+        l[u] = x[u] - h[u];
+    }
+    st_bf16x8(hi, h);
+    st_bf16x8(lo, l);
+}
+
 // Eight BF16 of a 16-byte chunk -> FP32.
 __device__ __forceinline__ void ld_bf16x8(const void *p, float *x) {
     const uint4 u = *reinterpret_cast<const uint4 *>(p);

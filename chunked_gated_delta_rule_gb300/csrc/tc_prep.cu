@@ -83,7 +83,7 @@ __device__ __forceinline__ void scale_rows_in_place(uint8_t *a, const float *f, 
     }
 }
 
-// kBwd: the backward's recompute also stores G and T (a separate
+// kBwd: the backward's recompute also stores G and the T images (a separate
 // instantiation, so that the forward's kernel carries none of it).
 template <bool kBwd>
 __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__ PrepArgs args) {
@@ -279,13 +279,14 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
                 const float4 a0 = *reinterpret_cast<const float4 *>(sAT + i * kInvLd + j0);
                 const float4 a1 = *reinterpret_cast<const float4 *>(sAT + i * kInvLd + j0 + 4);
                 const float tv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                if (kBwd && quad < 2) {  // T for the backward, zero above the diagonal
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        ws.bwd_Tm + ((int64_t)item * kChunk + i) * kChunk + j0);
-                    dst[0] = make_float4(j0 <= i ? tv[0] : 0.f, j0 + 1 <= i ? tv[1] : 0.f,
-                                         j0 + 2 <= i ? tv[2] : 0.f, j0 + 3 <= i ? tv[3] : 0.f);
-                    dst[1] = make_float4(j0 + 4 <= i ? tv[4] : 0.f, j0 + 5 <= i ? tv[5] : 0.f,
-                                         j0 + 6 <= i ? tv[6] : 0.f, j0 + 7 <= i ? tv[7] : 0.f);
+                if (kBwd && quad < 2) {  // T for the backward as BF16 hi + lo images:
+                    // zero above the diagonal and in rows past the sequence end
+                    float tz[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) tz[u] = (j0 + u <= i && i < len) ? tv[u] : 0.f;
+                    uint8_t *timg = ws.bwd_lkimg + (int64_t)item * kLkImgBytes;
+                    const uint32_t ot = sw128_off(i, j0, 64);
+                    st_split_bf16x8(timg + kLkImgTh + ot, timg + kLkImgTl + ot, tz);
                 }
                 float x[8];
 #pragma unroll
