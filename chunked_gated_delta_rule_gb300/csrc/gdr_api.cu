@@ -389,7 +389,6 @@ int plan_for_call(const gdr_dims &d, bool beta_free, int n_segments, const gdr_o
 WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int path) {
     const bool delta = !beta_free;
     const bool simt = path == 1;
-    const bool recompute = path == 3;  // the tensor-core backward's recompute
     const int64_t mc = max_chunks_of(d);
     const int64_t ns = n_seqs(d);
     const size_t H = (size_t)d.H, K = (size_t)d.K, V = (size_t)d.V;
@@ -405,7 +404,7 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     L.off_seq0 = take(sizeof(int32_t) * (size_t)(ns + 1));
     L.off_nchunks = take(sizeof(int32_t) * 4);
     L.off_order = take(sizeof(int32_t) * (size_t)ns);
-    L.off_G = take(simt || recompute ? sizeof(float) * (size_t)mc * H * kChunk : 0);
+    L.off_G = take(simt ? sizeof(float) * (size_t)mc * H * kChunk : 0);
     L.off_W = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
     L.off_U = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * V : 0);
     L.off_hpre = take(simt ? sizeof(float) * (size_t)mc * H * K * V : 0);
@@ -562,7 +561,8 @@ int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStre
 
 // Backward: the forward recompute (the state before each chunk and V'),
 // then the backward kernels.  Route 2, all on the tensor cores: the
-// preparation (records, G and T), the serial chain in its recompute mode, the
+// preparation (records, and the T, G and beta images), the serial chain in
+// its recompute mode (the h and v_new images), the
 // reverse scan and the per-chunk gradients; route 1: the CUDA-core forward
 // and backward kernels.
 int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw, int bv,

@@ -158,15 +158,16 @@ struct Workspace {
     int64_t max_chunks;
     int n_segments;       // S (1 = serial)
     int bwd_tc;           // the tensor-core backward's forward recompute: tc_prep
-                          // also stores G and the T images, the chain the h
-                          // mirror and v_new images (bwd_lkimg)
+                          // also stores the T images, G and beta, the chain
+                          // the h mirror and v_new images (bwd_lkimg)
     // [chunks][H][kLkImgBytes] (bwd_tc): the MMA operands of the backward's
     // per-chunk gradients as byte images of BF16 tiles (128-byte swizzled
     // rows, sw128_off): the chains' state mirrors h^T (the state before the
     // chunk, from the recompute) and E^T (the gradient at the chunk's end,
     // from the reverse scan), [v][key] in two 16 KB key blocks; and the FP32
     // operands as hi + lo pairs: v_new^T (recompute) and dV'^T (reverse
-    // scan), [v][t] with 128 rows; T (prep), [i][j] with 64 rows
+    // scan), [v][t] with 128 rows; T (prep), [i][j] with 64 rows; and the
+    // chunk's gate cumsum G and beta (prep, FP32)
     uint8_t *bwd_lkimg;
 };
 
@@ -174,7 +175,9 @@ constexpr uint32_t kLkImgH = 0, kLkImgE = 32768;
 constexpr uint32_t kLkImgVh = 65536, kLkImgVl = 81920;    // v_new^T hi, lo
 constexpr uint32_t kLkImgDh = 98304, kLkImgDl = 114688;   // dV'^T hi, lo
 constexpr uint32_t kLkImgTh = 131072, kLkImgTl = 139264;  // T hi, lo
-constexpr uint32_t kLkImgBytes = 147456;
+constexpr uint32_t kLkImgVec = 147456;                    // FP32 G[64], beta[64] (prep)
+constexpr uint32_t kLkImgVecBytes = 512;
+constexpr uint32_t kLkImgBytes = kLkImgVec + kLkImgVecBytes;
 
 // Backward pass: the caller's gradient tensors (dq, dk, dv in the input
 // dtype; dg, dbeta, dh0 FP32; dht / dh0 in the state layout of h0).

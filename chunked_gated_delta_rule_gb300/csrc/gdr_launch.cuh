@@ -18,8 +18,8 @@ struct WorkspaceLayout {
 
 // path 1: CUDA-core path (chunk table, G, W, U, h_pre, v_new, segments);
 // path 2: tensor-core path (chunk table, records and segment summaries);
-// path 3: the tensor-core backward's forward recompute (chunk table, G,
-// h_pre, v_new and the records).
+// path 3: the tensor-core backward's forward recompute (chunk table and
+// records; its images are in the backward's own scratch).
 WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int n_segments, int path);
 Workspace carve_workspace(void *base, const WorkspaceLayout &L, int n_segments);
 

@@ -27,9 +27,11 @@
 //
 // Persistent CTAs (one per SM) stride over the (chunk, head) items in three
 // MMA groups per item, each followed by an epilogue that reads TMEM; the
-// next item's tiles load while the last epilogue runs.  Row sums over keys
-// or values are warp transposing reductions in a fixed order, so results are
-// identical at any grid.  Every wait is time-bounded.
+// epilogue work the next group does not need runs while that group
+// executes, and the next item's tiles load during the last epilogue.  dq,
+// dk and dv leave from registers, adjacent columns paired by a shuffle.  Row
+// sums over keys or values are warp transposing reductions in a fixed order,
+// so results are identical at any grid.  Every wait is time-bounded.
 #include "gdr_internal.cuh"
 #include "tc_chunk.cuh"
 #include "tma_host.cuh"
@@ -61,7 +63,10 @@ constexpr int kThreads = 256;
 //                      (S + S^T) hi | lo | S in FP32 (row i at 64 i, column j
 //                      at j ^ (i % 32))
 //   V  [192, 208 KB)   v rows
-// The images (h, E, V', dV', T) arrive by bulk copies, dO, q, k and v by TMA.
+//   G, beta of the item (FP32, 512 B), then the FP32 scalars
+// The images arrive by bulk copies, dO, q, k and v by TMA, in two groups:
+// H, B, D, V and the vectors once the item before has finished its second
+// group of products, C and F once it has finished its last.
 constexpr uint32_t kOffH = 0;
 constexpr uint32_t kOffB = 32768;
 constexpr uint32_t kBlkB = 24576;
@@ -71,20 +76,22 @@ constexpr uint32_t kOffD = kOffC + 2 * kBlkC;
 constexpr uint32_t kOffF = kOffD + 32768;
 constexpr uint32_t kFdvHi = 0, kFdvLo = 16384, kFtHi = 32768, kFtLo = 40960;
 constexpr uint32_t kFzHi = 0, kFzLo = 8192, kFsHi = 16384, kFsLo = 24576, kFs32 = 32768;
-constexpr uint32_t kOffV = kOffF + 49152;  // v rows ([t][v], two 64-column blocks)
-constexpr uint32_t kOffMisc = kOffV + 16384;
+constexpr uint32_t kOffV = kOffF + 49152;
+constexpr uint32_t kOffVec = kOffV + 16384;
+constexpr uint32_t kOffMisc = kOffVec + kLkImgVecBytes;
 // FP32 scalars in the misc area: gate vectors, per-warp partial row sums
-constexpr int kVG = 0, kVGam = 64, kVLam = 128, kVB = 192;
-constexpr int kR1 = 256, kR2 = kR1 + 256, kR3 = kR2 + 256, kR4 = kR3 + 256;  // [4 lane quarters][64]
+constexpr int kVG = 0, kVGam = 64, kVLam = 128, kVB = 192, kVEp = 256;
+constexpr int kR1 = 320, kR2 = kR1 + 256, kR3 = kR2 + 256, kR4 = kR3 + 256;  // [4 lane quarters][64]
 constexpr int kRowR = kR4 + 256, kColR = kRowR + 128, kRdA = kColR + 128, kColRA = kRdA + 128;  // [2][64]
 constexpr int kR3f = kColRA + 128, kDg = kR3f + 64, kEh = kDg + 64;
 constexpr int kMiscFloats = kEh + 8;
 constexpr uint32_t kOffBar = kOffMisc + kMiscFloats * 4;
-constexpr int kNumBars = 4;  // tiles landed, then one per MMA group
+constexpr int kNumBars = 5;  // first load group landed, groups 1-3 done, second load group landed
 constexpr uint32_t kSmemLaunch = kOffBar + 8 * kNumBars + 16 + 1024;
 static_assert(kOffBar % 8 == 0, "barrier alignment");
 static_assert(kSmemLaunch <= 232448, "shared memory per CTA");
-constexpr uint32_t kLoadBytes = 4 * 32768 + 16384 + 4 * 16384;  // h, E, V', dV', T; dO, q, k, v
+constexpr uint32_t kLoadA = 3 * 32768 + 2 * 16384 + kLkImgVecBytes;  // h, E, V'; dO, v; G, beta
+constexpr uint32_t kLoadB = 2 * 16384 + 32768 + 16384;                // q, k; dV', T
 
 // TMEM columns (128 lanes each, FP32), 64 columns per accumulator
 constexpr uint32_t kTmemCols = 512;
@@ -124,6 +131,43 @@ __device__ __forceinline__ float bf16_at(const uint8_t *p) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
 }
 
+__device__ __forceinline__ void st_bf16_at(uint8_t *p, float x) {
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
+}
+
+// Two / three 32-column TMEM loads under one wait.
+__device__ __forceinline__ void tmem_load2(uint32_t a0, uint32_t a1, float (&f0)[32],
+                                           float (&f1)[32]) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(a0, r0);
+    tmem_ld32(a1, r1);
+    tmem_wait_ld();
+    reg_fence(r0);
+    reg_fence(r1);
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+        f0[u] = __uint_as_float(r0[u]);
+        f1[u] = __uint_as_float(r1[u]);
+    }
+}
+__device__ __forceinline__ void tmem_load3(uint32_t a0, uint32_t a1, uint32_t a2, float (&f0)[32],
+                                           float (&f1)[32], float (&f2)[32]) {
+    uint32_t r0[32], r1[32], r2[32];
+    tmem_ld32(a0, r0);
+    tmem_ld32(a1, r1);
+    tmem_ld32(a2, r2);
+    tmem_wait_ld();
+    reg_fence(r0);
+    reg_fence(r1);
+    reg_fence(r2);
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+        f0[u] = __uint_as_float(r0[u]);
+        f1[u] = __uint_as_float(r1[u]);
+        f2[u] = __uint_as_float(r2[u]);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_constant__ GradArgs args) {
     const Problem &p = args.p;
     const Workspace &ws = args.ws;
@@ -132,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
     float *mf = reinterpret_cast<float *>(sm + kOffMisc);
+    const float *vecs = reinterpret_cast<const float *>(sm + kOffVec);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffBar + 8 * kNumBars);
     float *sS = reinterpret_cast<float *>(sm + kOffF + kFs32);
@@ -143,9 +188,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
     const int j0 = 32 * hf;                       // this thread's 32 columns
     const int H = (int)p.H;
     const float scale = p.scale;
-    __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(args.a.dq);
-    __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(args.a.dk);
-    __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(args.a.dv);
 
     pdl_trigger();
     if (warp == 0) {
@@ -161,33 +203,71 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t tl = tmem + lane;
-    pdl_wait();  // the images and G from the kernels before
+    pdl_wait();  // the images from the kernels before
     const int n_items = *ws.n_chunks * H;
 
-    auto issue_loads = [&](int it_) {
+    auto issue_a = [&](int it_) {  // h, E, V', dO, v, G and beta
         const int4 e = tab[it_ / H];
         const int hh = it_ % H;
         const uint8_t *img = ws.bwd_lkimg + (int64_t)it_ * kLkImgBytes;
-        mbar_arrive_expect_tx(&bars[0], kLoadBytes);
+        mbar_arrive_expect_tx(&bars[0], kLoadA);
         bulk_load(sm + kOffH, img + kLkImgH, 16384u, &bars[0]);
         bulk_load(sm + kOffH + 16384, img + kLkImgH + 16384, 16384u, &bars[0]);
         bulk_load(sm + kOffD, img + kLkImgVh, 16384u, &bars[0]);
         bulk_load(sm + kOffD + 16384, img + kLkImgVl, 16384u, &bars[0]);
-        bulk_load(sm + kOffF + kFdvHi, img + kLkImgDh, 16384u, &bars[0]);
-        bulk_load(sm + kOffF + kFdvLo, img + kLkImgDl, 16384u, &bars[0]);
-        bulk_load(sm + kOffF + kFtHi, img + kLkImgTh, 8192u, &bars[0]);
-        bulk_load(sm + kOffF + kFtLo, img + kLkImgTl, 8192u, &bars[0]);
+        bulk_load(sm + kOffVec, img + kLkImgVec, kLkImgVecBytes, &bars[0]);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             bulk_load(sm + kOffB + b * kBlkB + 8192, img + kLkImgE + b * 16384, 16384u, &bars[0]);
             tma_load_3d(sm + kOffB + b * kBlkB, &args.tdo, &bars[0], 64 * b, hh, e.y);
-            tma_load_3d(sm + kOffC + b * kBlkC, &args.tq, &bars[0], 64 * b, hh, e.y);
-            tma_load_3d(sm + kOffC + b * kBlkC + 8192, &args.tk, &bars[0], 64 * b, hh, e.y);
             tma_load_3d(sm + kOffV + b * 8192, &args.tv, &bars[0], 64 * b, hh, e.y);
         }
     };
+    auto issue_b = [&](int it_) {  // q, k, dV', T
+        const int4 e = tab[it_ / H];
+        const int hh = it_ % H;
+        const uint8_t *img = ws.bwd_lkimg + (int64_t)it_ * kLkImgBytes;
+        mbar_arrive_expect_tx(&bars[4], kLoadB);
+        bulk_load(sm + kOffF + kFdvHi, img + kLkImgDh, 16384u, &bars[4]);
+        bulk_load(sm + kOffF + kFdvLo, img + kLkImgDl, 16384u, &bars[4]);
+        bulk_load(sm + kOffF + kFtHi, img + kLkImgTh, 8192u, &bars[4]);
+        bulk_load(sm + kOffF + kFtLo, img + kLkImgTl, 8192u, &bars[4]);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sm + kOffC + b * kBlkC, &args.tq, &bars[4], 64 * b, hh, e.y);
+            tma_load_3d(sm + kOffC + b * kBlkC + 8192, &args.tk, &bars[4], 64 * b, hh, e.y);
+        }
+    };
+    // Descriptor bases: a descriptor of the tile at byte offset o from the
+    // base is base + o / 16 (the start address field; o stays below 256 KB).
+    const uint64_t dK = sdesc_sw128(sb, 16, 1024);        // K-major
+    const uint64_t dM8 = sdesc_sw128(sb, 8192, 1024);     // MN-major, atoms 8 KB apart
+    const uint64_t dM16 = sdesc_sw128(sb, 16384, 1024);   // MN-major, atoms 16 KB apart
+    const uint64_t dM24 = sdesc_sw128(sb, kBlkB, 1024);   // MN-major, atoms 24 KB apart
+    auto at = [](uint64_t base, uint32_t off) { return base + (uint64_t)(off >> 4); };
+    // Values v[u] of column r for tokens j0 + u -> rows t0 + j0 + u of a
+    // [tokens][H][128] BF16 output, rows past len skipped: adjacent columns
+    // are paired through one shuffle per two tokens (4-byte stores).
+    auto store_cols = [&](__nv_bfloat16 *out, const float (&v)[32], int64_t t0, int hh, int len) {
+        const bool odd = (lane_id & 1) != 0;
+        const int c0 = r & ~1;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const float send = odd ? v[u] : v[16 + u];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const int tok = j0 + (odd ? 16 + u : u);
+            const float x0 = odd ? recv : v[u], x1 = odd ? v[16 + u] : recv;
+            if (tok < len)
+                *reinterpret_cast<__nv_bfloat162 *>(out + ((t0 + tok) * H + hh) * kD + c0) =
+                    __floats2bfloat162_rn(x0, x1);
+        }
+    };
+
     int item = blockIdx.x;
-    if (tid == 0 && item < n_items) issue_loads(item);
+    if (tid == 0 && item < n_items) {
+        issue_a(item);
+        issue_b(item);
+    }
     for (uint32_t it = 0; item < n_items; ++it) {
         const uint32_t ph = it & 1u;
         const int4 e = tab[item / H];
@@ -196,19 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         const int len = e.z;
         const int next = item + (int)gridDim.x;
 
-        // gate vectors
-        if (tid < 64) {
-            const bool in = tid < len;
-            const float G = ws.G[(int64_t)item * kChunk + tid];
-            const float Gl = ws.G[(int64_t)item * kChunk + len - 1];
-            mf[kVG + tid] = G;
-            mf[kVGam + tid] = in ? expf(G) : 0.f;
-            mf[kVLam + tid] = in ? expf(Gl - G) : 0.f;
-            mf[kVB + tid] = in ? p.beta[(t0 + tid) * H + hh] : 0.f;
-        }
-        bool ok = mbar_wait(&bars[0], ph, p.status);
+        bool ok = mbar_wait(&bars[0], ph, p.status) && mbar_wait(&bars[4], ph, p.status);
         if (__syncthreads_or(!ok)) break;
-        if (len < kChunk) {  // tile rows past the sequence end belong to the next one
+        if (len < kChunk) {  // dO, q, k rows past the sequence end belong to the next one
             for (int idx = tid; idx < 6 * (kChunk - len) * 8; idx += kThreads) {
                 const int tile = idx / ((kChunk - len) * 8), rem = idx % ((kChunk - len) * 8);
                 const int t = len + (rem >> 3), c = rem & 7;
@@ -218,38 +288,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
             }
         }
         fence_async_smem();
+        // gate vectors; e^{G_i - G_j} = e^{G_i - G_last} e^{G_last - G_j} unless
+        // the chunk's log gates spread over 80 (then one exponential each)
+        bool wide = false;
+        if (tid < 64) {
+            const bool in = tid < len;
+            const float G = vecs[tid], Gl = vecs[len - 1];
+            mf[kVG + tid] = G;
+            mf[kVGam + tid] = in ? expf(G) : 0.f;
+            mf[kVLam + tid] = in ? expf(Gl - G) : 0.f;
+            mf[kVEp + tid] = in ? expf(G - Gl) : 0.f;
+            mf[kVB + tid] = in ? vecs[64 + tid] : 0.f;
+            wide = in && fabsf(G - Gl) >= 80.f;
+        }
         tc_fence_before();
-        __syncthreads();
+        wide = __syncthreads_or(wide);
         // ---- group 1: P1^T, P3^T, [Q K^T; K K^T], dVb^T
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // over v
-                umma_bf16(tmem + kCP1, sdesc_sw128(sb + kOffH + kk * 2048, 16384, 1024),
-                          sdesc_sw128(sb + kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32, 16, 1024),
-                          kIdMnK, kk > 0);
+                umma_bf16(tmem + kCP1, at(dM16, kOffH + kk * 2048),
+                          at(dK, kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32), kIdMnK, kk > 0);
 #pragma unroll
             for (int pz = 0; pz < 2; ++pz)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // over v; V' hi, then lo
-                    umma_bf16(tmem + kCP3, sdesc_sw128(sb + kOffB + 8192 + kk * 2048, kBlkB, 1024),
-                              sdesc_sw128(sb + kOffD + pz * 16384 + kk * 2048, 8192, 1024),
-                              kIdMnMn, (pz | kk) != 0);
+                    umma_bf16(tmem + kCP3, at(dM24, kOffB + 8192 + kk * 2048),
+                              at(dM8, kOffD + pz * 16384 + kk * 2048), kIdMnMn, (pz | kk) != 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // over keys
-                umma_bf16(tmem + kCQK,
-                          sdesc_sw128(sb + kOffC + (kk >> 2) * kBlkC + (kk & 3) * 32, 16, 1024),
-                          sdesc_sw128(sb + kOffC + 8192 + (kk >> 2) * kBlkC + (kk & 3) * 32, 16,
-                                      1024),
-                          kIdKK, kk > 0);
+                umma_bf16(tmem + kCQK, at(dK, kOffC + (kk >> 2) * kBlkC + (kk & 3) * 32),
+                          at(dK, kOffC + 8192 + (kk >> 2) * kBlkC + (kk & 3) * 32), kIdKK, kk > 0);
 #pragma unroll
             for (int t3 = 0; t3 < 3; ++t3) {  // dV' hi T hi, dV' hi T lo, dV' lo T hi
                 const uint32_t oa = kOffF + (t3 == 2 ? kFdvLo : kFdvHi);
                 const uint32_t ob = kOffF + (t3 == 1 ? kFtLo : kFtHi);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // over tokens i
-                    umma_bf16(tmem + kCDvb, sdesc_sw128(sb + oa + kk * 32, 16, 1024),
-                              sdesc_sw128(sb + ob + kk * 2048, 8192, 1024), kIdKMn,
+                    umma_bf16(tmem + kCDvb, at(dK, oa + kk * 32), at(dM8, ob + kk * 2048), kIdKMn,
                               (t3 | kk) != 0);
             }
             umma_commit(&bars[1]);
@@ -272,35 +349,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         ok = mbar_wait(&bars[1], ph, p.status);
         if (__syncthreads_or(!ok)) break;  // also: every thread is done with the E image
         tc_fence_after();
-        // ---- epilogue 1 (lanes = value columns / keys, columns = tokens)
+        // ---- epilogue 1 (lanes = value columns, columns = tokens): dVb -> its
+        // hi / lo tiles (group 2's operand), dv, rowdot(dVb, V)
         {
             float f[32], x[32];
             tmem_load32f(tl + kCDvb + j0, f);  // dVb[j][v = r]
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 const int j = j0 + u;
-                const bool in = j < len;
-                if (in)
-                    dv[((t0 + j) * H + hh) * kD + r] = __float2bfloat16_rn(mf[kVB + j] * f[u]);
-                x[u] = in ? f[u] * bf16_at(sm + kOffV + (r >> 6) * 8192 + sw128_off(j, r & 63, 64))
-                          : 0.f;
+                x[u] = j < len
+                           ? f[u] * bf16_at(sm + kOffV + (r >> 6) * 8192 + sw128_off(j, r & 63, 64))
+                           : 0.f;
                 const __nv_bfloat16 hi = __float2bfloat16_rn(f[u]);
                 const uint32_t o = kOffB + (r >> 6) * kBlkB + sw128_off(j, r & 63, 64);
                 *reinterpret_cast<__nv_bfloat16 *>(sm + o + 8192) = hi;
-                *reinterpret_cast<__nv_bfloat16 *>(sm + o + 16384) =
-                    __float2bfloat16_rn(f[u] - __bfloat162float(hi));
+                st_bf16_at(sm + o + 16384, f[u] - __bfloat162float(hi));
             }
             mf[kR4 + 64 * q4 + j0 + lane_id] = warp_colsum32(x, lane_id);
-            const uint32_t oq = kOffC + (r >> 6) * kBlkC;
-            tmem_load32f(tl + kCP1 + j0, f);  // P1[i][key = r]
 #pragma unroll
-            for (int u = 0; u < 32; ++u) x[u] = f[u] * bf16_at(sm + oq + sw128_off(j0 + u, r & 63, 64));
-            mf[kR1 + 64 * q4 + j0 + lane_id] = warp_colsum32(x, lane_id);
-            tmem_load32f(tl + kCP3 + j0, f);  // P3[i][key = r]
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-                x[u] = f[u] * bf16_at(sm + oq + 8192 + sw128_off(j0 + u, r & 63, 64));
-            mf[kR3 + 64 * q4 + j0 + lane_id] = warp_colsum32(x, lane_id);
+            for (int u = 0; u < 32; ++u) x[u] = mf[kVB + j0 + u] * f[u];
+            store_cols(static_cast<__nv_bfloat16 *>(args.a.dv), x, t0, hh, len);
         }
         fence_async_smem();
         tc_fence_before();
@@ -312,44 +380,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
             for (int pz = 0; pz < 2; ++pz)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // over v; V' hi, then lo
-                    umma_bf16(tmem + kCDmY,
-                              sdesc_sw128(sb + kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32, 16, 1024),
-                              sdesc_sw128(sb + kOffD + pz * 16384 + kk * 2048, 8192, 1024),
-                              kIdKMn, (pz | kk) != 0);
+                    umma_bf16(tmem + kCDmY, at(dK, kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32),
+                              at(dM8, kOffD + pz * 16384 + kk * 2048), kIdKMn, (pz | kk) != 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // [dVb hi; dVb lo] V' hi^T: rows 64-127 used
-                umma_bf16(tmem + kCDvb,
-                          sdesc_sw128(sb + kOffB + 8192 + (kk >> 2) * kBlkB + (kk & 3) * 32, 16,
-                                      1024),
-                          sdesc_sw128(sb + kOffD + kk * 2048, 8192, 1024), kIdKMn, kk > 0);
+                umma_bf16(tmem + kCDvb, at(dK, kOffB + 8192 + (kk >> 2) * kBlkB + (kk & 3) * 32),
+                          at(dM8, kOffD + kk * 2048), kIdKMn, kk > 0);
 #pragma unroll
             for (int pz = 0; pz < 2; ++pz)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // over v; dVb hi, then lo
-                    umma_bf16(tmem + kCKb, sdesc_sw128(sb + kOffH + kk * 2048, 16384, 1024),
-                              sdesc_sw128(sb + kOffB + 8192 + pz * 8192 + (kk >> 2) * kBlkB +
-                                              (kk & 3) * 32,
-                                          16, 1024),
+                    umma_bf16(tmem + kCKb, at(dM16, kOffH + kk * 2048),
+                              at(dK, kOffB + 8192 + pz * 8192 + (kk >> 2) * kBlkB + (kk & 3) * 32),
                               kIdMnK, (pz | kk) != 0);
             umma_commit(&bars[2]);
+        }
+        // while group 2 runs: rowdot(P1, Q), rowdot(P3, K)
+        {
+            float f[32], g[32], x[32];
+            const uint32_t oq = kOffC + (r >> 6) * kBlkC;
+            tmem_load2(tl + kCP1 + j0, tl + kCP3 + j0, f, g);  // P1, P3 [i][key = r]
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[u] = f[u] * bf16_at(sm + oq + sw128_off(j0 + u, r & 63, 64));
+            mf[kR1 + 64 * q4 + j0 + lane_id] = warp_colsum32(x, lane_id);
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                x[u] = g[u] * bf16_at(sm + oq + 8192 + sw128_off(j0 + u, r & 63, 64));
+            mf[kR3 + 64 * q4 + j0 + lane_id] = warp_colsum32(x, lane_id);
         }
         ok = mbar_wait(&bars[2], ph, p.status);
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
+        if (tid == 0 && next < n_items) issue_a(next);  // H, B, D, V and the vectors are free
         // ---- epilogue 2 (stacked rows: lanes 0-63 row i of dm, 64-127 of Y)
         {
             float f[32], g[32];
             if (q4 < 2) {
                 const int i = r;
-                tmem_load32f(tl + kCDmY + j0, f);  // dm[i][j]
-                tmem_load32f(tl + kCQK + j0, g);   // (Q K^T)[i][j]
-                const float Gi = mf[kVG + i];
+                tmem_load2(tl + kCDmY + j0, tl + kCQK + j0, f, g);  // dm, Q K^T [i][j]
+                const float Gi = mf[kVG + i], epi = mf[kVEp + i];
                 float z[32], rowR = 0.f;
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
                     const int j = j0 + u;
                     const bool c = i < len && j <= i;
-                    const float d = c ? expf(Gi - mf[kVG + j]) : 0.f;
+                    const float d = c ? (wide ? expf(Gi - mf[kVG + j]) : epi * mf[kVLam + j]) : 0.f;
                     z[u] = scale * f[u] * d;
                     g[u] = z[u] * g[u];  // R = Z * (Q K^T)
                     rowR += g[u];
@@ -363,18 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                 mf[kColR + 64 * q4 + j0 + lane_id] = warp_colsum32(g, lane_id);
             } else {
                 const int i = r - 64;
-                tmem_load32f(tl + kCDmY + j0, f);  // Y[i][j], dVb hi part
-                tmem_load32f(tl + kCDvb + j0, g);  // dVb lo part
+                float y2[32];
+                tmem_load3(tl + kCDmY + j0, tl + kCDvb + j0, tl + kCQK + j0, f, y2, g);
 #pragma unroll
-                for (int u = 0; u < 32; ++u) f[u] += g[u];
-                tmem_load32f(tl + kCQK + j0, g);  // (K K^T)[i][j]
-                const float Gi = mf[kVG + i], bi = mf[kVB + i];
+                for (int u = 0; u < 32; ++u) f[u] += y2[u];  // Y[i][j]: dVb hi + lo parts; g: K K^T
+                const float Gi = mf[kVG + i], bi = mf[kVB + i], epi = mf[kVEp + i];
                 float rdA = 0.f;
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
                     const int j = j0 + u;
                     const bool sl = i < len && j < i;
-                    const float d = sl ? expf(Gi - mf[kVG + j]) : 0.f;
+                    const float d = sl ? (wide ? expf(Gi - mf[kVG + j]) : epi * mf[kVLam + j]) : 0.f;
                     const float dA = sl ? -f[u] : 0.f;
                     const float kd = g[u] * d;
                     rdA = fmaf(dA, kd, rdA);
@@ -384,12 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                 mf[kRdA + 64 * hf + i] = rdA;
                 mf[kColRA + 64 * (q4 - 2) + j0 + lane_id] = warp_colsum32(g, lane_id);
             }
-            // r2 = rowdot(dKb, K), dKb = -dVb h^T
-            tmem_load32f(tl + kCKb + j0, f);
-            const uint32_t ok_ = kOffC + (r >> 6) * kBlkC + 8192;
-#pragma unroll
-            for (int u = 0; u < 32; ++u) f[u] = -f[u] * bf16_at(sm + ok_ + sw128_off(j0 + u, r & 63, 64));
-            mf[kR2 + 64 * q4 + j0 + lane_id] = warp_colsum32(f, lane_id);
         }
         __syncthreads();
         // S + S^T (S strictly lower) -> hi / lo tiles
@@ -415,52 +483,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
             for (int pz = 0; pz < 2; ++pz)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)  // over tokens j; Z hi, then lo
-                    umma_bf16(tmem + kCXq, sdesc_sw128(sb + kOffC + 8192 + kk * 2048, kBlkC, 1024),
-                              sdesc_sw128(sb + kOffF + kFzHi + pz * 8192 + kk * 32, 16, 1024),
-                              kIdMnK, (pz | kk) != 0);
+                    umma_bf16(tmem + kCXq, at(dM16, kOffC + 8192 + kk * 2048),
+                              at(dK, kOffF + kFzHi + pz * 8192 + kk * 32), kIdMnK, (pz | kk) != 0);
 #pragma unroll
             for (int t4 = 0; t4 < 4; ++t4) {  // Q^T Z hi, Q^T Z lo, K^T Ss hi, K^T Ss lo
                 const uint32_t oa = kOffC + (t4 < 2 ? 0u : 8192u);
                 const uint32_t ob = kOffF + (t4 < 2 ? kFzHi : kFsHi) + (t4 & 1) * 8192;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tmem + kCXk, sdesc_sw128(sb + oa + kk * 2048, kBlkC, 1024),
-                              sdesc_sw128(sb + ob + kk * 2048, 8192, 1024), kIdMnMn,
+                    umma_bf16(tmem + kCXk, at(dM16, oa + kk * 2048), at(dM8, ob + kk * 2048), kIdMnMn,
                               (t4 | kk) != 0);
             }
             umma_commit(&bars[3]);
         }
+        {  // while group 3 runs: r2 = rowdot(dKb, K), dKb = -dVb h^T
+            float f[32];
+            tmem_load32f(tl + kCKb + j0, f);
+            const uint32_t ok_ = kOffC + (r >> 6) * kBlkC + 8192;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) f[u] = -f[u] * bf16_at(sm + ok_ + sw128_off(j0 + u, r & 63, 64));
+            mf[kR2 + 64 * q4 + j0 + lane_id] = warp_colsum32(f, lane_id);
+        }
         ok = mbar_wait(&bars[3], ph, p.status);
-        if (__syncthreads_or(!ok)) break;  // every MMA of the item done: tiles free
+        if (__syncthreads_or(!ok)) break;  // every MMA of the item done: C and F free
         tc_fence_after();
-        if (tid == 0 && next < n_items) issue_loads(next);
+        if (tid == 0 && next < n_items) issue_b(next);
         // ---- epilogue 3: dq, dk (lanes = keys)
         {
-            float f[32], x[32];
-            tmem_load32f(tl + kCP1 + j0, f);
-            tmem_load32f(tl + kCXq + j0, x);
+            float f[32], x[32], kb[32];
+            tmem_load2(tl + kCP1 + j0, tl + kCXq + j0, f, x);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[u] = fmaf(scale * mf[kVGam + j0 + u], f[u], x[u]);
+            store_cols(static_cast<__nv_bfloat16 *>(args.a.dq), x, t0, hh, len);
+            tmem_load3(tl + kCP3 + j0, tl + kCXk + j0, tl + kCKb + j0, f, x, kb);
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 const int i = j0 + u;
-                if (i < len)
-                    dq[((t0 + i) * H + hh) * kD + r] =
-                        __float2bfloat16_rn(fmaf(scale * mf[kVGam + i], f[u], x[u]));
+                x[u] = fmaf(-mf[kVB + i] * mf[kVGam + i], kb[u], fmaf(mf[kVLam + i], f[u], x[u]));
             }
-            float kb[32];
-            tmem_load32f(tl + kCP3 + j0, f);
-            tmem_load32f(tl + kCXk + j0, x);
-            tmem_load32f(tl + kCKb + j0, kb);
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int i = j0 + u;
-                if (i < len) {
-                    const float y = fmaf(mf[kVLam + i], f[u], x[u]);
-                    dk[((t0 + i) * H + hh) * kD + r] =
-                        __float2bfloat16_rn(fmaf(-mf[kVB + i] * mf[kVGam + i], kb[u], y));
-                }
-            }
+            store_cols(static_cast<__nv_bfloat16 *>(args.a.dk), x, t0, hh, len);
         }
-        __syncthreads();
         // ---- dbeta and the gate gradient
         if (tid < 64) {
             const int i = tid;
@@ -516,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
             if (2 * lane_id + 1 < len) args.a.dg[(t0 + 2 * lane_id + 1) * H + hh] = run1;
         }
         tc_fence_before();
-        __syncthreads();  // TMEM, the tiles and the scalars are reused
+        __syncthreads();  // TMEM and the scalars are reused
         item = next;
     }
     tc_fence_before();

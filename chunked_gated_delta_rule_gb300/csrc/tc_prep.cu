@@ -83,7 +83,7 @@ __device__ __forceinline__ void scale_rows_in_place(uint8_t *a, const float *f, 
     }
 }
 
-// kBwd: the backward's recompute also stores G and the T images (a separate
+// kBwd: the backward's recompute also stores the T images, G and beta (a separate
 // instantiation, so that the forward's kernel carries none of it).
 template <bool kBwd>
 __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__ PrepArgs args) {
@@ -170,9 +170,11 @@ __global__ void __launch_bounds__(kThreads, 3) k_tc_prep(const __grid_constant__
                     *sGam = vec + 256, *sEP = vec + 320, *sScal = vec + 384;
         if (warp == 0) {
             gate_vectors(vec, g2, b2, len, lane_id);
-            if (kBwd) {  // G for the backward's per-chunk kernels
-                ws.G[(int64_t)item * kChunk + lane_id] = vec[lane_id];
-                ws.G[(int64_t)item * kChunk + 32 + lane_id] = vec[32 + lane_id];
+            if (kBwd) {  // G and beta for the backward's per-chunk gradients
+                float *gv = reinterpret_cast<float *>(ws.bwd_lkimg + (int64_t)item * kLkImgBytes +
+                                                      kLkImgVec);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) gv[32 * c + lane_id] = vec[32 * c + lane_id];
             }
         }
         bool ok = mbar_wait(&bars[0], it & 1u, p.status);
