@@ -18,7 +18,7 @@
 //
 // Every product runs on tcgen05 (kind::f16, FP32 accumulators in TMEM).
 // The BF16 inputs q, k, dO and the chains' BF16 h and E mirrors enter as
-// they are; every FP32 operand (T, dV', V', dVb, Z, S + S^T) enters as a
+// they are; every FP32 operand (T, dV', V', dVb, Z, S) enters as a
 // pair of BF16 tiles hi + lo (lo = x - hi, rounded), so each product carries
 // about 16 significant bits of its FP32 operands and the local gradients
 // keep FP32-grade accuracy.  Products whose rows are tokens are stacked to
@@ -29,7 +29,8 @@
 // MMA groups per item, each followed by an epilogue that reads TMEM; the
 // epilogue work the next group does not need runs while that group
 // executes, and the next item's tiles load during the last epilogue.  dq,
-// dk and dv leave from registers, adjacent columns paired by a shuffle.  Row
+// dk and dv turn from columns into rows through a small per-warp buffer and
+// leave in 16-byte pieces.  Row
 // sums over keys or values are warp transposing reductions in a fixed order,
 // so results are identical at any grid.  Every wait is time-bounded.
 #include "gdr_internal.cuh"
@@ -59,11 +60,12 @@ constexpr int kThreads = 256;
 //   C  [80, 112 KB)    per key block b (16 KB): q rows | k rows
 //   D  [112, 144 KB)   V'^T hi | V'^T lo ([v][t], 128 rows)
 //   F  [144, 192 KB)   dV'^T hi | dV'^T lo ([v][i], 128 rows) | T hi | T lo
-//                      ([i][j]); after the first group: Z hi | Z lo |
-//                      (S + S^T) hi | lo | S in FP32 (row i at 64 i, column j
-//                      at j ^ (i % 32))
+//                      ([i][j]); after the first group: Z hi | Z lo | S hi
+//                      | S lo ([i][j])
 //   V  [192, 208 KB)   v rows
-//   G, beta of the item (FP32, 512 B), then the FP32 scalars
+//   G, beta of the item (FP32, 512 B); per warp 1 KB where a 16-token x
+//   32-column block of dq, dk or dv turns from columns into rows; the FP32
+//   scalars
 // The images arrive by bulk copies, dO, q, k and v by TMA, in two groups:
 // H, B, D, V and the vectors once the item before has finished its second
 // group of products, C and F once it has finished its last.
@@ -75,10 +77,11 @@ constexpr uint32_t kBlkC = 16384;
 constexpr uint32_t kOffD = kOffC + 2 * kBlkC;
 constexpr uint32_t kOffF = kOffD + 32768;
 constexpr uint32_t kFdvHi = 0, kFdvLo = 16384, kFtHi = 32768, kFtLo = 40960;
-constexpr uint32_t kFzHi = 0, kFzLo = 8192, kFsHi = 16384, kFsLo = 24576, kFs32 = 32768;
+constexpr uint32_t kFzHi = 0, kFzLo = 8192, kFsHi = 16384, kFsLo = 24576;
 constexpr uint32_t kOffV = kOffF + 49152;
 constexpr uint32_t kOffVec = kOffV + 16384;
-constexpr uint32_t kOffMisc = kOffVec + kLkImgVecBytes;
+constexpr uint32_t kOffOut = kOffVec + kLkImgVecBytes;  // per warp 1 KB: output rows in transit
+constexpr uint32_t kOffMisc = kOffOut + 8 * 1024;
 // FP32 scalars in the misc area: gate vectors, per-warp partial row sums
 constexpr int kVG = 0, kVGam = 64, kVLam = 128, kVB = 192, kVEp = 256;
 constexpr int kR1 = 320, kR2 = kR1 + 256, kR3 = kR2 + 256, kR4 = kR3 + 256;  // [4 lane quarters][64]
@@ -102,7 +105,7 @@ constexpr uint32_t kCDvb = 192;  // dVb^T [v][j]; then rows 64-127: dVb lo V' hi
 constexpr uint32_t kCDmY = 256;  // [dO V'^T; dVb V'^T]  [i | 64 + i][j]
 constexpr uint32_t kCKb = 320;   // (dVb h^T)^T           [key][i]
 constexpr uint32_t kCXq = 384;   // (Z K)^T               [key][i]
-constexpr uint32_t kCXk = 448;   // (Z^T Q + (S + S^T) K)^T
+constexpr uint32_t kCXk = 448;   // (Z^T Q + S^T K + S K)^T
 
 constexpr uint32_t kIdMnK = idesc_bf16(128, 64, 1, 0);   // A MN-major, B K-major
 constexpr uint32_t kIdKK = idesc_bf16(128, 64, 0, 0);    // both K-major
@@ -179,7 +182,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
     const float *vecs = reinterpret_cast<const float *>(sm + kOffVec);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + kOffBar + 8 * kNumBars);
-    float *sS = reinterpret_cast<float *>(sm + kOffF + kFs32);
     const int4 *tab = reinterpret_cast<const int4 *>(ws.chunk_tab);
     const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
     const int q4 = warp & 3, hf = warp >> 2;
@@ -246,20 +248,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
     const uint64_t dM24 = sdesc_sw128(sb, kBlkB, 1024);   // MN-major, atoms 24 KB apart
     auto at = [](uint64_t base, uint32_t off) { return base + (uint64_t)(off >> 4); };
     // Values v[u] of column r for tokens j0 + u -> rows t0 + j0 + u of a
-    // [tokens][H][128] BF16 output, rows past len skipped: adjacent columns
-    // are paired through one shuffle per two tokens (4-byte stores).
+    // [tokens][H][128] BF16 output, rows past len skipped.  The warp's 32
+    // columns x 32 tokens turn into rows through its 1 KB of shared memory,
+    // 16 tokens at a time, and leave in 16-byte pieces.
+    uint8_t *wout = sm + kOffOut + warp * 1024;
     auto store_cols = [&](__nv_bfloat16 *out, const float (&v)[32], int64_t t0, int hh, int len) {
-        const bool odd = (lane_id & 1) != 0;
-        const int c0 = r & ~1;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const float send = odd ? v[u] : v[16 + u];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            const int tok = j0 + (odd ? 16 + u : u);
-            const float x0 = odd ? recv : v[u], x1 = odd ? v[16 + u] : recv;
-            if (tok < len)
-                *reinterpret_cast<__nv_bfloat162 *>(out + ((t0 + tok) * H + hh) * kD + c0) =
-                    __floats2bfloat162_rn(x0, x1);
+        for (int half = 0; half < 2; ++half) {
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) st_bf16_at(wout + u * 64 + lane_id * 2, v[16 * half + u]);
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int c = lane_id + 32 * k, row = c >> 2, piece = c & 3;
+                const int tok = j0 + 16 * half + row;
+                if (tok < len)
+                    *reinterpret_cast<uint4 *>(out + ((t0 + tok) * H + hh) * kD + 32 * q4 + piece * 8) =
+                        *reinterpret_cast<const uint4 *>(wout + row * 64 + piece * 16);
+            }
         }
     };
 
@@ -414,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         if (tid == 0 && next < n_items) issue_a(next);  // H, B, D, V and the vectors are free
         // ---- epilogue 2 (stacked rows: lanes 0-63 row i of dm, 64-127 of Y)
         {
-            float f[32], g[32];
+            float f[32], g[32], srow[32];
             if (q4 < 2) {
                 const int i = r;
                 tmem_load2(tl + kCDmY + j0, tl + kCQK + j0, f, g);  // dm, Q K^T [i][j]
@@ -453,30 +460,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                     const float kd = g[u] * d;
                     rdA = fmaf(dA, kd, rdA);
                     g[u] = bi * dA * kd;
-                    sS[i * 64 + (j ^ (i & 31))] = bi * dA * d;
+                    srow[u] = bi * dA * d;
                 }
                 mf[kRdA + 64 * hf + i] = rdA;
+                // row i of S (zero on and above the diagonal)
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    const uint32_t o = sw128_chunk(i, (j0 >> 3) + c8, 64);
+                    st_split_bf16x8(sm + kOffF + kFsHi + o, sm + kOffF + kFsLo + o, srow + 8 * c8);
+                }
                 mf[kColRA + 64 * (q4 - 2) + j0 + lane_id] = warp_colsum32(g, lane_id);
             }
-        }
-        __syncthreads();
-        // S + S^T (S strictly lower) -> hi / lo tiles
-        for (int c = tid; c < 512; c += kThreads) {
-            const int i = c >> 3, jc = c & 7;
-            float x[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = 8 * jc + u;
-                x[u] = j < i ? sS[i * 64 + (j ^ (i & 31))]
-                             : (j > i ? sS[j * 64 + (i ^ (j & 31))] : 0.f);
-            }
-            const uint32_t o = sw128_chunk(i, jc, 64);
-            st_split_bf16x8(sm + kOffF + kFsHi + o, sm + kOffF + kFsLo + o, x);
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // ---- group 3: (Z K)^T, (Z^T Q + (S + S^T) K)^T
+        // ---- group 3: (Z K)^T, (Z^T Q + S^T K + S K)^T
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -486,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                     umma_bf16(tmem + kCXq, at(dM16, kOffC + 8192 + kk * 2048),
                               at(dK, kOffF + kFzHi + pz * 8192 + kk * 32), kIdMnK, (pz | kk) != 0);
 #pragma unroll
-            for (int t4 = 0; t4 < 4; ++t4) {  // Q^T Z hi, Q^T Z lo, K^T Ss hi, K^T Ss lo
+            for (int t4 = 0; t4 < 4; ++t4) {  // Q^T Z hi, Q^T Z lo, K^T S hi, K^T S lo
                 const uint32_t oa = kOffC + (t4 < 2 ? 0u : 8192u);
                 const uint32_t ob = kOffF + (t4 < 2 ? kFzHi : kFsHi) + (t4 & 1) * 8192;
 #pragma unroll
@@ -494,6 +493,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                     umma_bf16(tmem + kCXk, at(dM16, oa + kk * 2048), at(dM8, ob + kk * 2048), kIdMnMn,
                               (t4 | kk) != 0);
             }
+#pragma unroll
+            for (int pz = 0; pz < 2; ++pz)  // K^T S^T: S hi, then lo as the K-major operand
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(tmem + kCXk, at(dM16, kOffC + 8192 + kk * 2048),
+                              at(dK, kOffF + kFsHi + pz * 8192 + kk * 32), kIdMnK, 1);
             umma_commit(&bars[3]);
         }
         {  // while group 3 runs: r2 = rowdot(dKb, K), dKb = -dVb h^T
