@@ -14,7 +14,9 @@ The same JSON line carries a sub-record per configuration ("configs"): ms
 per call, tokens/s, the call's roofline fraction, per-kernel times; serial
 beside split at 64K tokens (8 heads and 1); at 16K tokens every split count
 with its error against the FP64 oracle on sampled (sequence, head) pairs;
-the plan's pick beside serial on a batch with one long sequence.
+the plan's pick beside serial on a batch with one long sequence; and the
+backward pass (gdr_chunk_bwd, at its plan's route) on the wide varlen batch,
+16K tokens and 64K tokens x 8 heads ("backward_<workload>").
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdr|reference]
                   [--workload NAME] [--no-configs]
@@ -693,6 +695,49 @@ def config_record(pkg, name, dev, steps, flush, hbm):
     return x, m, rec
 
 
+# Backward sub-records of the default line: gdr_chunk_bwd at its plan's
+# route, do / dht seeded, L2 flushed between timed calls.
+BWD_CONFIG_WORKLOADS = ("wide_varlen_bf16", "long_16k_bf16", "stress_64k_h8_bf16")
+
+
+def bwd_config_record(pkg, name, dev, steps, flush):
+    import torch
+    from chunked_gated_delta_rule_gb300 import synthetic
+    x = synthetic.make_inputs(synthetic.WORKLOADS[name])
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+    do_h, dht_h = bwd_grads_in(x)
+    do, dht = do_h.to(dev), dht_h.to(dev)
+    args_t = (d["q"], d["k"], d["v"], d["g"], d["beta"], do)
+    kw = dict(cu_seqlens=d["cu_seqlens"], h0=d["h0"], dht=dht)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        pkg.gdr_chunk_bwd(*args_t, **kw)
+    ts, per = [], {}
+    for i in range(2 * steps):
+        flush.fill_(i & 0xFF)
+        timer = pkg.LaunchTimer(16) if i % 2 else None
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pkg.gdr_chunk_bwd(*args_t, timer=timer, **kw)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if timer is None:
+            ts.append(e0.elapsed_time(e1))
+        else:
+            for j, kid in enumerate(timer.ids):
+                per.setdefault(pkg.gdr_kernel_name(kid), []).append(timer.elapsed_ms(j))
+    ms = statistics.mean(ts)
+    c = counts(x)
+    kernels = {k: {"launches_per_call": len(v) // steps, "avg_ms": statistics.mean(v)}
+               for k, v in per.items()}
+    route = "tensor cores" if "tc_bwd_grad" in kernels else "CUDA cores (FP32)"
+    rec = {"route": route, "tokens": c["tokens"], "ms_per_call": ms,
+           "tokens_per_s": c["tokens"] / (ms * 1e-3), "kernels": kernels}
+    del d, do, dht
+    return rec
+
+
 def add_split_sweep(rec, pkg, x, dev, steps, flush, plan_s, counts_):
     """ms per call at each split count and the error against the serial
     result on the same inputs (the pages' "CP vs serial" accuracy table;
@@ -827,6 +872,9 @@ def run_gdr(args):
             _, cm, rec = config_record(pkg, name, dev, min(K, 20), flush, hbm)
             configs[name] = rec
             del cm
+            torch.cuda.empty_cache()
+        for name in BWD_CONFIG_WORKLOADS:
+            configs["backward_" + name] = bwd_config_record(pkg, name, dev, min(K, 10), flush)
             torch.cuda.empty_cache()
 
     cpu = None

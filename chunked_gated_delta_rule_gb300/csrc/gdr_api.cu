@@ -812,15 +812,19 @@ int gdr_chunk_fwd(const gdr_dims *dims, const void *q, const void *k, const void
 }
 
 // The backward's plan.  Route 2, the tensor-core route (the tensor-core
-// forward recompute and reverse scan; BF16 operands, see gdr.h), for BF16
-// inputs with K = V = 128 and the delta rule, whose reverse scan runs
-// serially: unless the caller asks for a segment split, or the serial chain
-// would be long with few chains beside it (a 64K-token sequence with 1 or 8
-// heads: the CUDA-core route's split is faster there).  Route 1, the
-// CUDA-core route (FP32 arithmetic), otherwise, with the CUDA-core path's
-// value tile (32 columns on the wide varlen batch: its scan 0.98 ms at 64,
-// 0.74 ms at 32) and segment rule unless the caller fixes the count.
-// force_path 1 or 2 picks a route.
+// forward recompute, reverse scan and per-chunk gradients; BF16 operands,
+// see gdr.h), for BF16 inputs with K = V = 128 and the delta rule, whose
+// scans run serially, unless the caller asks for a segment split or the
+// CUDA-core route's split is estimated faster.  Cost models fitted to GB300
+// timings, in microseconds: the tensor-core route's two serial chain passes
+// take about 3.6 a chunk of the longest sequence each, in waves of one chain
+// per SM, and its other kernels about 0.09 a chunk-head; the CUDA-core
+// route's split about 3.15 a chunk-head (64K tokens: 8 heads 8.5 ms against
+// 25.8, 1 head 7.6 against 3.6).  Route 1, the CUDA-core route (FP32
+// arithmetic), otherwise, with the CUDA-core path's value tile (32 columns
+// on the wide varlen batch: its scan 0.98 ms at 64, 0.74 ms at 32) and
+// segment rule unless the caller fixes the count.  force_path 1 or 2 picks
+// a route.
 int bwd_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_options *opt,
              int *route, int *bv, int *S) {
     if (n_segments < 0) return GDR_ERR_INVALID;
@@ -831,8 +835,12 @@ int bwd_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_option
                        n_segments <= 1;
     if (force == 2 && !tc_ok) return GDR_ERR_UNSUPPORTED;
     const ChunkStats cs = chunk_stats(d);
-    const bool long_few = cs.longest > 256 && n_seqs(d) * d.H < device_sms() / 4;
-    *route = force ? force : (tc_ok && !long_few ? 2 : 1);
+    const double items = (double)cs.total * (double)d.H;
+    const double chains = (double)n_seqs(d) * (double)d.H;
+    const double waves = std::ceil(chains / (double)device_sms());
+    const double t_tc = 7.2 * (double)cs.longest * waves + 0.09 * items;
+    const double t_cc = 3.15 * items;
+    *route = force ? force : (tc_ok && t_tc <= t_cc ? 2 : 1);
     *bv = pick_bv(d);
     *S = *route == 2 ? 1 : n_segments > 0 ? n_segments : auto_segments(d, beta_free, 1, *bv);
     return GDR_OK;
