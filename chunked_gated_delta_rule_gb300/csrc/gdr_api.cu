@@ -402,7 +402,7 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     };
     L.off_tab = take(sizeof(int32_t) * 4 * (size_t)mc);
     L.off_seq0 = take(sizeof(int32_t) * (size_t)(ns + 1));
-    L.off_nchunks = take(sizeof(int32_t) * 4);
+    L.off_nchunks = take(sizeof(int32_t) * kNumCtr);
     L.off_order = take(sizeof(int32_t) * (size_t)ns);
     L.off_G = take(simt ? sizeof(float) * (size_t)mc * H * kChunk : 0);
     L.off_W = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
@@ -570,8 +570,32 @@ int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs
     GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
     if (route == 2) {
         GDR_LAUNCH(rec, kKTcPrep, tc_prep(p, ws, st));
-        GDR_LAUNCH(rec, kKTcRecompute, tc_chain(p, ws, 3, st));
-        GDR_LAUNCH(rec, kKTcBwdScan, tc_bwd_scan(p, ws, a.dht, a.dh0, a.dout, st));
+        if (ws.n_segments <= 1) {
+            GDR_LAUNCH(rec, kKTcRecompute, tc_chain(p, ws, 3, st));
+            GDR_LAUNCH(rec, kKTcBwdScan, tc_bwd_scan(p, ws, 0, a.dht, a.dh0, a.dout, st));
+        } else {
+            // the forward's split, its output pass keeping the images; then
+            // the reverse scan's: offsets from E = 0, the composition from
+            // dht to dh0 over the transposed forward maps in reversed slots,
+            // and the output pass from each segment's composed end
+            Problem pf = p;
+            pf.ht = nullptr;
+            if (prescan_split_kinds(p.N * ws.n_segments * p.H))
+                GDR_LAUNCH(rec, kKTcPre, tc_chain(pf, ws, 1, st));
+            else
+                GDR_LAUNCH(rec, kKTcPreDual, tc_prescan(pf, ws, st));
+            GDR_LAUNCH(rec, kKCompose, compose_mt(pf, ws, st));
+            GDR_LAUNCH(rec, kKTcSegRecompute, tc_chain(pf, ws, 4, st));
+            GDR_LAUNCH(rec, kKBwdMaps, bwd_maps(p, ws, bw.segMb, st));
+            GDR_LAUNCH(rec, kKTcBwdPre, tc_bwd_scan(p, ws, 1, nullptr, nullptr, a.dout, st));
+            Problem pr = p;
+            pr.h0 = a.dht;
+            pr.ht = a.dh0;
+            Workspace wr = ws;
+            wr.segM = bw.segMb;
+            GDR_LAUNCH(rec, kKCompose, compose_mt(pr, wr, st));
+            GDR_LAUNCH(rec, kKTcBwdSegOut, tc_bwd_scan(p, ws, 2, nullptr, nullptr, a.dout, st));
+        }
         GDR_LAUNCH(rec, kKTcBwdGrad, tc_bwd_grad(p, ws, a, st));
         return GDR_OK;
     }
@@ -639,6 +663,9 @@ const char *gdr_kernel_name(int id) {
     case kKTcRecompute: return "tc_chain_recompute";
     case kKTcBwdScan: return "tc_bwd_scan";
     case kKTcBwdGrad: return "tc_bwd_grad";
+    case kKTcSegRecompute: return "tc_chain_segment_recompute";
+    case kKTcBwdPre: return "tc_bwd_scan_prescan";
+    case kKTcBwdSegOut: return "tc_bwd_scan_segment_out";
     default: return "?";
     }
 }
@@ -831,18 +858,11 @@ int bwd_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_option
     if (n_segments > kMaxSegments) return GDR_ERR_UNSUPPORTED;
     const int force = opt ? opt->force_path : 0;
     if (force < 0 || force > 2) return GDR_ERR_INVALID;
-    const bool tc_ok = d.dtype == GDR_BF16 && d.K == 128 && d.V == 128 && !beta_free &&
-                       n_segments <= 1;
+    const bool tc_ok = d.dtype == GDR_BF16 && d.K == 128 && d.V == 128 && !beta_free;
     if (force == 2 && !tc_ok) return GDR_ERR_UNSUPPORTED;
-    const ChunkStats cs = chunk_stats(d);
-    const double items = (double)cs.total * (double)d.H;
-    const double chains = (double)n_seqs(d) * (double)d.H;
-    const double waves = std::ceil(chains / (double)device_sms());
-    const double t_tc = 7.2 * (double)cs.longest * waves + 0.09 * items;
-    const double t_cc = 3.15 * items;
-    *route = force ? force : (tc_ok && t_tc <= t_cc ? 2 : 1);
+    *route = force ? force : (tc_ok ? 2 : 1);
     *bv = pick_bv(d);
-    *S = *route == 2 ? 1 : n_segments > 0 ? n_segments : auto_segments(d, beta_free, 1, *bv);
+    *S = n_segments > 0 ? n_segments : auto_segments(d, beta_free, *route == 2 ? 2 : 1, *bv);
     return GDR_OK;
 }
 

@@ -141,8 +141,9 @@ __host__ __device__ __forceinline__ int64_t state_off(const Problem &p, int64_t 
 struct Workspace {
     int32_t *chunk_tab;   // [max_chunks][4]: seq, first flat token, len, chunk-in-seq
     int32_t *seq_chunk0;  // [N+1]: first global chunk of each sequence
-    int32_t *n_chunks;    // [4]: total chunks, then the chain counters of the
-                          // persistent tensor-core kernels (zeroed per call)
+    int32_t *n_chunks;    // [8]: total chunks, then the chain counters of the
+                          // persistent tensor-core kernels (zeroed per call;
+                          // indices kCtr*)
     int32_t *seq_order;   // [N]: sequences by descending chunk count
     float *G;             // [max_chunks][H][64]: chunk-local gate cumsum
     float *W;             // [max_chunks][H][64][K]   (delta mode)
@@ -170,6 +171,10 @@ struct Workspace {
     // chunk's gate cumsum G and beta (prep, FP32)
     uint8_t *bwd_lkimg;
 };
+
+// Chain counters in Workspace::n_chunks, one per persistent pass of a call.
+constexpr int kCtrSerial = 1, kCtrPre = 2, kCtrSegOut = 3, kCtrSegRecompute = 4,
+              kCtrBwdSerial = 5, kCtrBwdPre = 6, kCtrBwdSegOut = 7, kNumCtr = 8;
 
 constexpr uint32_t kLkImgH = 0, kLkImgE = 32768;
 constexpr uint32_t kLkImgVh = 65536, kLkImgVl = 81920;    // v_new^T hi, lo

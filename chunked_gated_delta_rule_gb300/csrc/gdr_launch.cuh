@@ -60,6 +60,9 @@ enum KernelId {
     kKTcRecompute = 25,
     kKTcBwdScan = 26,
     kKTcBwdGrad = 27,
+    kKTcSegRecompute = 28,
+    kKTcBwdPre = 29,
+    kKTcBwdSegOut = 30,
     kKNumIds
 };
 
@@ -104,9 +107,17 @@ cudaError_t convert_bf16_to_f16(const void *src, void *dst, int64_t n, cudaStrea
 cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
                      cudaStream_t st, LaunchRecorder &rec);
 // The reverse state-gradient scan on the tensor cores (BF16, K = V = 128,
-// delta rule, serial): the E^T and dV'^T images into ws.bwd_lkimg, dh0.
-cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, const float *dht, float *dh0,
-                        const void *dout, cudaStream_t st);
+// delta rule).  mode 0: serial from dht to dh0, the E^T and dV'^T images
+// into ws.bwd_lkimg; 1: segment pre-scan from E = 0, each segment's offset
+// into ws.segC (segment s of nseg non-empty ones in slot nseg - 1 - s); 2:
+// segment output pass from the composed ends in ws.segH (the same slots),
+// the images.
+cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, int mode, const float *dht,
+                        float *dh0, const void *dout, cudaStream_t st);
+// The reverse scan's segment maps from the forward recompute's (ws.segM):
+// the transposes, in reversed slots, for the composition from the last
+// segment to the first.
+cudaError_t bwd_maps(const Problem &p, const Workspace &ws, float *segMb, cudaStream_t st);
 // Every per-chunk gradient of the backward on the tensor cores (dq, dk, dv,
 // dbeta, dg), from the images in ws.bwd_lkimg (h, E, v_new, dV', T), dO, q,
 // k, v and G (ws.G).
@@ -129,7 +140,8 @@ cudaError_t tc_gla(const Problem &p, const Workspace &ws, int mode, cudaStream_t
 cudaError_t tc_prep(const Problem &p, const Workspace &ws, cudaStream_t st);
 // mode 0: serial scan + output (h0 -> ht); 1: segment pre-scan (c_s and M_s
 // chains); 2: segment output pass from the composed segment states; 3: the
-// backward's recompute (serial from h0, h_pre and v_new stored, no output).
+// backward's recompute (serial from h0, the h mirror and v_new images
+// stored, no output); 4: the same per segment from the composed states.
 cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream_t st);
 // The per-token recurrence from (and back into) rows of a state pool.
 cudaError_t recurrent_fwd(const Problem &p, float *state, int64_t n_states,

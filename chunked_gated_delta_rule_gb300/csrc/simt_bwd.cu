@@ -843,6 +843,11 @@ cudaError_t launch_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, 
 
 }  // namespace
 
+cudaError_t bwd_maps(const Problem &p, const Workspace &ws, float *segMb, cudaStream_t st) {
+    k_bwd_maps<<<(unsigned)(p.N * p.H * ws.n_segments), kBT, 0, st>>>(p, ws, segMb);
+    return cudaGetLastError();
+}
+
 cudaError_t simt_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw,
                      cudaStream_t st, LaunchRecorder &rec) {
     if (p.dtype == GDR_BF16) return launch_bwd<__nv_bfloat16>(p, ws, a, bw, st, rec);

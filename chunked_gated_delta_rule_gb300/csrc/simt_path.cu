@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads) k_chunk_table(const Problem p, int64
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();  // the first kernel of a call: launched in stream order, it waits for nothing
     for (int b = tid; b < kBuckets; b += kThreads) s_hist[b] = 0;
-    if (tid < 3) n_chunks[1 + tid] = 0;
+    if (tid < kNumCtr - 1) n_chunks[1 + tid] = 0;
     if (tid == 0) s_bad = (is_varlen_p(p) && (seq_bound(p, 0) != 0 || seq_bound(p, N) != T)) ? 1 : 0;
     __syncthreads();
     // this thread's run of sequences, their chunk counts and the histogram

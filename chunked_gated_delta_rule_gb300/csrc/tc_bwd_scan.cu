@@ -80,9 +80,11 @@ enum : int {
     kNumBars = 11 + 2 * kRing
 };
 
+// One chain: (sequence n, head h, segment s) over the sequence's chunks
+// [s0, s0 + nc), last first.
 struct ChainDesc {
     int64_t n, tstart, tlen;
-    int h, c_begin, nc, valid, pad0, pad1, pad2, pad3;
+    int h, c_begin, nc, valid, s, s0, nseg, pad0;  // nseg: non-empty segments of the sequence
 };
 static_assert(sizeof(ChainDesc) == 56, "chain descriptor layout");
 constexpr uint32_t kOffBar = kOffRing + 64 * kRing;
@@ -98,6 +100,13 @@ constexpr uint32_t kIdescEK = idesc_bf16(128, 64, 0, 0);    // E^T K~^T
 constexpr uint32_t kIdescDQ = idesc_bf16(128, 128, 1, 1);   // dO^T Q~
 constexpr uint32_t kIdescVW = idesc_bf16(128, 128, 0, 0);   // (-dV'^T) W
 
+// MODE 0: serial, from dht at each sequence's end to dh0; 1: segment
+// pre-scan, from E = 0 at each segment's end, storing only E at its start
+// (the segment's offset; segment s of a sequence's nseg non-empty segments
+// in slot nseg - 1 - s of the summaries, for the composition from the last
+// segment to the first); 2: segment output pass, from the composed E at
+// each segment's end (the same slot).  Modes 0 and 2 store the images.
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_constant__ BwdScanArgs args) {
     const Problem &p = args.p;
     const Workspace &ws = args.ws;
@@ -114,6 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
     const int row = 32 * (warp & 3) + lane_id;  // TMEM lane = value column v
     const uint32_t lane = (uint32_t)(32 * (warp & 3)) << 16;
     const int H = (int)p.H;
+    const int S = MODE == 0 ? 1 : ws.n_segments;
+    constexpr bool kImages = MODE != 1;
 
     auto wait = [&](int b, uint32_t parity) -> bool {
         return mbar_wait_or_abort(&bars[b], parity & 1u, p.status, s_abort);
@@ -149,24 +160,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
 
     if (warp == 9) {
         // ------------------------------------------------------------ producer
-        // Chains: (sequence, head), heads fastest, sequences longest first;
-        // a sequence without chunks is posted too (dh0 = dht).  Chunks of a
-        // chain load last first.
+        // Chains: (sequence, head, segment), heads fastest, then segments,
+        // sequences longest first; serially a sequence without chunks is
+        // posted too (dh0 = dht), split an empty segment is skipped.  Chunks
+        // of a chain load last first.
         if (lane_id == 0) {
-            const int total = (int)(p.N * H);
-            int32_t *counter = ws.n_chunks + 2;
+            const int total = (int)(p.N * S * H);
+            int32_t *counter =
+                ws.n_chunks + (MODE == 0 ? kCtrBwdSerial : MODE == 1 ? kCtrBwdPre : kCtrBwdSegOut);
             int issued = 0;
             for (int posted = 0;; ++posted) {
                 ChainDesc c{};
-                const int id = atomicAdd(counter, 1);
-                if (id < total) {
+                while (true) {
+                    const int id = atomicAdd(counter, 1);
+                    if (id >= total) break;
                     c.h = id % H;
-                    c.n = ws.seq_order[id / H];
+                    c.s = (id / H) % S;
+                    c.n = ws.seq_order[id / H / S];
                     c.c_begin = ws.seq_chunk0[c.n];
-                    c.nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
-                    c.tstart = seq_start(p, c.n);
-                    c.tlen = seq_end(p, c.n) - c.tstart;
-                    c.valid = 1;
+                    const int nseq = ws.seq_chunk0[c.n + 1] - c.c_begin;
+                    const int per = (nseq + S - 1) / S;  // the forward's segment bounds
+                    c.s0 = min(nseq, c.s * per);
+                    c.nc = min(nseq, c.s0 + per) - c.s0;
+                    c.nseg = per ? (nseq + per - 1) / per : 0;
+                    if (c.nc > 0 || MODE == 0) {
+                        c.tstart = seq_start(p, c.n);
+                        c.tlen = seq_end(p, c.n) - c.tstart;
+                        c.valid = 1;
+                        break;
+                    }
                 }
                 const int slot = posted % kRing;
                 if (posted >= kRing && !wait(kBCempty + slot, (uint32_t)(posted / kRing - 1)))
@@ -176,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                 if (!c.valid) break;
                 bool ok = true;
                 for (int j = 0; j < c.nc; ++j, ++issued) {
-                    const int cc = c.nc - 1 - j;
+                    const int cc = c.s0 + c.nc - 1 - j;
                     const int stage = issued & 1;
                     if (issued >= 2 && !wait(kBFree + stage, (uint32_t)((issued >> 1) - 1))) {
                         ok = false;
@@ -268,8 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
             // st_base + key * kst, by the state layout
             const int64_t st_base = state_off(p, C.n * H + h, 0, row);
             const int64_t kst = p.state_vk ? 1 : kD;
+            // the segment's summary slot: segment s of the sequence's nseg
+            // non-empty ones in slot nseg - 1 - s, so that the composition
+            // runs from the last segment to the first
+            const int64_t slot = (C.n * H + h) * (int64_t)S + (C.nseg - 1 - C.s);
             for (int j = 0; j < C.nc; ++j, ++gk) {
-                const int cc = C.nc - 1 - j;
+                const int cc = C.s0 + C.nc - 1 - j;
                 const int b = gk & 1;
                 const uint8_t *st = sm + b * kStage;
                 const int64_t item = (int64_t)(C.c_begin + cc) * H + h;
@@ -278,10 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                 const float gam_last = reinterpret_cast<const float *>(st + kImgVec)[kImgGamLast];
                 // E at the chunk's end, keys [64 hq, 64 hq + 64) of column `row`
                 auto state_half = [&](int hq, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
-                    if (j == 0) {  // the sequence's end: dht (or 0)
+                    if (j == 0) {  // the chain's end: dht (or 0), 0, or the composed E
 #pragma unroll
                         for (int kk = 0; kk < 64; ++kk) {
-                            const float v = args.dht ? args.dht[st_base + (64 * hq + kk) * kst] : 0.f;
+                            const int key = 64 * hq + kk;
+                            float v = 0.f;
+                            if (MODE == 0) {
+                                if (args.dht) v = args.dht[st_base + key * kst];
+                            } else if (MODE == 2) {
+                                v = ws.segH[(slot * kD + key) * kD + row];
+                            }
                             if (kk < 32) r0[kk] = __float_as_uint(v);
                             else r1[kk - 32] = __float_as_uint(v);
                         }
@@ -312,8 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                         const uint32_t oy = sw128_off(row, 64 * hq + 32 + 8 * c8, 128);
                         st_bf16x8(sm + kOffEm + ox, x);
                         st_bf16x8(sm + kOffEm + oy, y);
-                        st_bf16x8(limg + kLkImgE + ox, x);
-                        st_bf16x8(limg + kLkImgE + oy, y);
+                        if (kImages) {
+                            st_bf16x8(limg + kLkImgE + ox, x);
+                            st_bf16x8(limg + kLkImgE + oy, y);
+                        }
                     }
                 }
                 fence_async_smem();
@@ -353,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                             }
                             const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
                             st_bf16x8(sm + kOffDv + ou, u);
-                            st_split_bf16x8(dimg + kLkImgDh + ou, dimg + kLkImgDl + ou, d);
+                            if (kImages)
+                                st_split_bf16x8(dimg + kLkImgDh + ou, dimg + kLkImgDl + ou, d);
                         }
                     }
                 }
@@ -364,7 +399,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                 if (!wait(kBHdone, gk)) { ok = false; break; }
             }
             if (!ok) break;
-            if (args.dh0) {
+            if (MODE == 1) {  // E at the segment's start: its offset
+                tc_fence_after();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float hv[32];
+                    tmem_load32f(tmem + lane + kColE + 32 * q, hv);
+#pragma unroll
+                    for (int kk = 0; kk < 32; ++kk)
+                        ws.segC[(slot * kD + 32 * q + kk) * kD + row] = hv[kk];
+                }
+            } else if (MODE == 0 && args.dh0) {
                 if (C.nc == 0) {  // no tokens: dh0 = dht (or 0)
                     for (int key = 0; key < kD; ++key) {
                         const int64_t idx = st_base + key * kst;
@@ -391,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
             ChainDesc C;
             if (!take(k++, C) || !C.valid) break;
             for (int j = 0; j < C.nc; ++j, ++gk) {
-                const int cc = C.nc - 1 - j;
+                const int cc = C.s0 + C.nc - 1 - j;
                 const int b = gk & 1;
                 uint8_t *st = sm + b * kStage;
                 const int64_t rem = C.tlen - (int64_t)kChunk * cc;
@@ -428,10 +473,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+
+template <int MODE>
+cudaError_t launch_scan(const BwdScanArgs &args, dim3 grid, cudaStream_t st) {
+    cudaError_t err = cudaFuncSetAttribute(k_tc_bwd_scan<MODE>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemLaunch);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(k_tc_bwd_scan<MODE>, grid, dim3(kThreads), kSmemLaunch, st, args);
+}
+
 }  // namespace
 
-cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, const float *dht, float *dh0,
-                        const void *dout, cudaStream_t st) {
+cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, int mode, const float *dht,
+                        float *dh0, const void *dout, cudaStream_t st) {
     BwdScanArgs args;
     args.p = p;
     args.ws = ws;
@@ -443,12 +498,14 @@ cudaError_t tc_bwd_scan(const Problem &p, const Workspace &ws, const float *dht,
     if (!make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64) ||
         !make_tmap_bf16_3d(&args.tdo, dout, kD, H, rows, kD * 2, H * kD * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(k_tc_bwd_scan,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kSmemLaunch);
-    if (err != cudaSuccess) return err;
-    const dim3 grid((unsigned)persistent_grid(p, p.N * p.H, 1));
-    return launch_pdl(k_tc_bwd_scan, grid, dim3(kThreads), kSmemLaunch, st, args);
+    const int S = mode == 0 ? 1 : ws.n_segments;
+    const dim3 grid((unsigned)persistent_grid(p, p.N * S * p.H, 1));
+    switch (mode) {
+    case 0: return launch_scan<0>(args, grid, st);
+    case 1: return launch_scan<1>(args, grid, st);
+    case 2: return launch_scan<2>(args, grid, st);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gdr

@@ -55,8 +55,16 @@ using namespace tc;
 // kModeRecompute: the serial scan of the tensor-core backward's forward
 // recompute: no output; per chunk the byte image of the BF16 mirror of the
 // state before the chunk, and v_new as a pair of BF16 images (hi + lo), go
-// to the workspace for the backward's kernels.
-enum TcMode { kModeSerial = 0, kModePre = 1, kModeSegOut = 2, kModeRecompute = 3 };
+// to the workspace for the backward's kernels.  kModeSegRecompute: the same
+// per segment, from the composed segment states (the recompute's output
+// pass when the sequences are split).
+enum TcMode {
+    kModeSerial = 0,
+    kModePre = 1,
+    kModeSegOut = 2,
+    kModeRecompute = 3,
+    kModeSegRecompute = 4
+};
 
 struct TcArgs {
     Problem p;
@@ -139,6 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
     const Workspace &ws = args.ws;
     constexpr bool kOut = MODE == kModeSerial || MODE == kModeSegOut;
     constexpr bool kFromH0 = MODE == kModeSerial || MODE == kModeRecompute;
+    constexpr bool kFromSeg = MODE == kModeSegOut || MODE == kModeSegRecompute;
+    constexpr bool kImages = MODE == kModeRecompute || MODE == kModeSegRecompute;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -196,7 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
         if (lane_id == 0) {
             const int kinds = MODE == kModePre ? 2 : 1;
             const int total = (int)(p.N * S * H * kinds);
-            int32_t *counter = ws.n_chunks + 1 + (MODE == kModeRecompute ? 0 : MODE);
+            int32_t *counter =
+                ws.n_chunks + (MODE == kModeSerial || MODE == kModeRecompute ? kCtrSerial
+                               : MODE == kModePre                            ? kCtrPre
+                               : MODE == kModeSegOut                         ? kCtrSegOut
+                                                                             : kCtrSegRecompute);
             int issued = 0;
             for (int posted = 0;; ++posted) {
                 ChainDesc c{};
@@ -364,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                             float v = 0.f;
                             if (kFromH0) {
                                 if (p.h0) v = p.h0[st_base + (p.state_vk ? key : key * kD)];
-                            } else if (MODE == kModeSegOut) {
+                            } else if (kFromSeg) {
                                 v = ws.segH[(seg_base * kD + key) * kD + row];
                             } else if (trans) {
                                 v = key == row ? 1.f : 0.f;
@@ -384,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 // chain's critical path, so it goes first
                 // the recompute's image of the chunk's h^T mirror, for the
                 // backward's per-chunk gradients
-                uint8_t *limg = MODE == kModeRecompute
+                uint8_t *limg = kImages
                                     ? ws.bwd_lkimg + ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes
                                     : nullptr;
 #pragma unroll 1
@@ -403,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         const uint32_t oy = sw128_off(row, 64 * hq + 32 + 8 * c8, 128);
                         st_bf16x8(sm + kOffHm + ox, x);
                         st_bf16x8(sm + kOffHm + oy, y);
-                        if (MODE == kModeRecompute) {
+                        if (kImages) {
                             st_bf16x8(limg + kLkImgH + ox, x);
                             st_bf16x8(limg + kLkImgH + oy, y);
                         }
@@ -454,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         for (int c8 = 0; c8 < 4; ++c8) {
                             const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
                             st_bf16x8(sm + kOffVn + ou, u + 8 * c8);
-                            if (MODE == kModeRecompute) {  // v_new^T as BF16 hi + lo images
+                            if (kImages) {  // v_new^T as BF16 hi + lo images
                                 uint8_t *vimg = ws.bwd_lkimg +
                                                 ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes;
                                 st_split_bf16x8(vimg + kLkImgVh + ou, vimg + kLkImgVl + ou,
@@ -639,7 +653,7 @@ cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream
     const uint64_t H = (uint64_t)p.H;
     if (!make_tmap_bf16_3d(&args.tk, p.k, kD, H, rows, p.sk.h * 2, p.sk.t * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
-    if (mode == 3) {
+    if (mode == 3 || mode == 4) {
         args.to = args.tk;  // the recompute writes no output
     } else if (!make_tmap_bf16_3d(&args.to, p.o, kD, H, rows, p.so.h * 2, p.so.t * 2, 64, 1, 64)) {
         return cudaErrorInvalidValue;
@@ -652,6 +666,7 @@ cudaError_t tc_chain(const Problem &p, const Workspace &ws, int mode, cudaStream
     case 1: return launch_chain<kModePre>(args, grid, st);
     case 2: return launch_chain<kModeSegOut>(args, grid, st);
     case 3: return launch_chain<kModeRecompute>(args, grid, st);
+    case 4: return launch_chain<kModeSegRecompute>(args, grid, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
     if (warp == 9) {
         // ------------------------------------------------------------ producer
         const int total = (int)(p.N * S * H * VT);
-        int32_t *counter = ws.n_chunks + 1 + MODE;
+        int32_t *counter = ws.n_chunks + (MODE == 0 ? kCtrSerial : MODE == 1 ? kCtrPre : kCtrSegOut);
         int issued = 0;
         bool ok = true;
         for (int posted = 0; ok; ++posted) {

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
         // ------------------------------------------------------------ producer
         if (lane_id == 0) {
             const int total = (int)(p.N * S * H);
-            int32_t *counter = ws.n_chunks + 2;  // the pre-scan's chain counter
+            int32_t *counter = ws.n_chunks + kCtrPre;
             tma_prefetch_desc(&args.tk);
             int issued = 0;
             for (int posted = 0;; ++posted) {

@@ -273,3 +273,44 @@ def test_tc_route_is_the_default_for_its_shapes_and_bits_do_not_depend_on_the_gr
             assert (a is None) == (b is None), name
             if a is not None:
                 assert torch.equal(_bits(a), _bits(b)), (name, kw)
+
+
+# the tensor-core route split into segments: the forward's pre-scan,
+# composition and an output pass keeping the images, then the reverse
+# scan's offsets from E = 0, the composition from dht to dh0 over the
+# transposed forward maps and its output pass
+@pytest.mark.parametrize("S", [2, 5])
+def test_tc_route_segments_varlen_ragged(S):
+    """Sequences with fewer chunks than segments (their empty segments are
+    skipped and the reversed summary slots count the others), h0 and dht."""
+    w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True)
+    x = synthetic.make_inputs(w, lengths=[700, 65, 1, 300, 129])
+    print(check(x, force_path=2, n_segments=S))
+
+
+def test_tc_route_segments_state_layout_vk_without_dht():
+    w = synthetic.small(W["long_16k_bf16"], B=2, T=1000, H=2, with_h0=True)
+    print(check(synthetic.make_inputs(w), layout="vk", with_dht=False, force_path=2,
+                n_segments=4))
+
+
+def test_tc_route_segments_bits_do_not_depend_on_the_grid():
+    w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True)
+    x = synthetic.make_inputs(w, lengths=[900, 65, 7, 300])
+    do, dht = grads_in(x)
+    ref = run_bwd(x, do, dht, force_path=2, n_segments=4)
+    for kw in (dict(grid_limit=1), dict(grid_limit=7), dict()):
+        out = run_bwd(x, do, dht, force_path=2, n_segments=4, **kw)
+        for name, a, b in zip(NAMES, out, ref):
+            if a is not None:
+                assert torch.equal(_bits(a), _bits(b)), (name, kw)
+
+
+@pytest.mark.parametrize("name,pairs", [("stress_64k_h8_bf16", (0, 7)),
+                                        ("stress_64k_h1_bf16", (0,))])
+def test_tc_route_plan_split_full_size_sampled_pairs(name, pairs):
+    """64K tokens at the plan's segment count (the route's default)."""
+    x = synthetic.make_inputs(W[name])
+    mask = np.zeros(x["B"] * x["H"], dtype=bool)
+    mask[list(pairs)] = True
+    print(check(x, pair_mask=mask, force_path=2))
