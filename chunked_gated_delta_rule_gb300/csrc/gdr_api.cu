@@ -840,14 +840,12 @@ int gdr_chunk_fwd(const gdr_dims *dims, const void *q, const void *k, const void
 
 // The backward's plan.  Route 2, the tensor-core route (the tensor-core
 // forward recompute, reverse scan and per-chunk gradients; BF16 operands,
-// see gdr.h), for BF16 inputs with K = V = 128 and the delta rule, whose
-// scans run serially, unless the caller asks for a segment split or the
-// CUDA-core route's split is estimated faster.  Cost models fitted to GB300
-// timings, in microseconds: the tensor-core route's two serial chain passes
-// take about 3.6 a chunk of the longest sequence each, in waves of one chain
-// per SM, and its other kernels about 0.09 a chunk-head; the CUDA-core
-// route's split about 3.15 a chunk-head (64K tokens: 8 heads 8.5 ms against
-// 25.8, 1 head 7.6 against 3.6).  Route 1, the CUDA-core route (FP32
+// see gdr.h), for BF16 inputs with K = V = 128 and the delta rule, split
+// into segments by the tensor-core forward's rule unless the caller fixes
+// the count (its scans cost about 1.5 times the forward's per chunk, its
+// compositions the same, so the forward's cost model picks close to the
+// backward's best; 64K tokens: 8 heads 1.85 ms at 19 segments against 8.5
+// serial, 1 head 0.64 ms at 54).  Route 1, the CUDA-core route (FP32
 // arithmetic), otherwise, with the CUDA-core path's value tile (32 columns
 // on the wide varlen batch: its scan 0.98 ms at 64, 0.74 ms at 32) and
 // segment rule unless the caller fixes the count.  force_path 1 or 2 picks

@@ -282,20 +282,19 @@ int gdr_recurrent_fwd(const gdr_dims *dims, const void *q, const void *k,
  * Dataflow" step 4; gradients dQ/dK/dV and of the states, its
  * "Fixture-First Correctness Contract"), through the chunked form's WY
  * factors.  Two routes:
- *   - tensor-core route (BF16 inputs, K = V = 128, delta rule, serial
- *     scans): the forward recompute is the tensor-core forward's
- *     (per-chunk records, the serial chain keeping the BF16 state mirror
- *     and v_new of each chunk), then the reverse scan and every per-chunk
- *     gradient, all on tcgen05 with FP32 accumulation: BF16 operands in the
- *     scans (the forward's own rounding), FP32 operands of the per-chunk
- *     products as BF16 hi + lo pairs; every gradient lies within 1e-2
- *     (relative L2) of the exact one;
+ *   - tensor-core route (BF16 inputs, K = V = 128, delta rule): the
+ *     forward recompute is the tensor-core forward's (per-chunk records,
+ *     the chain keeping the BF16 state mirror and v_new of each chunk),
+ *     then the reverse scan and every per-chunk gradient, all on tcgen05
+ *     with FP32 accumulation: BF16 operands in the scans (the forward's own
+ *     rounding), FP32 operands of the per-chunk products as BF16 hi + lo
+ *     pairs; every gradient lies within 1e-2 (relative L2) of the exact
+ *     one.  Long sequences split into segments like the forward pass (the
+ *     reverse scan composed from dht to dh0 over the transposed forward
+ *     maps), at the forward's segment rule unless n_segments says;
  *   - CUDA-core route (every input type): FP32 arithmetic throughout, with
  *     a segment split of long sequences.
- *   The plan takes the tensor-core route where it applies, unless the
- *   caller asks for a segment split or a cost model fitted to GB300
- *   timings estimates the CUDA-core route's split faster (one 64K-token
- *   sequence with one or two heads).
+ *   The plan takes the tensor-core route where it applies;
  *   opt->force_path 1 or 2 picks the route.
  *   dims, q, k, v, g, beta, cu_seqlens, h0   as for gdr_chunk_fwd (device).
  *   dout    [B,T,H,V] dL/do, the input dtype.

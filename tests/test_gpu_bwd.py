@@ -10,11 +10,12 @@ they keep 1e-5.  FP16 inputs: dq, dk, dv rounded to FP16 once (2^-11), 2e-3;
 the rest 1e-5.  The oracle reads the inputs after rounding to the input
 dtype, so the comparison measures the kernels' arithmetic only.
 
-The tensor-core route (BF16, K = V = 128, delta rule, serial reverse scan;
-force_path=2, and the plan's choice for those shapes) computes with BF16
-operands in its forward recompute and reverse scan: every gradient is held
-to 1e-2, two sets of BF16 operand roundings of the kind the forward's 6e-3
-bar covers once.  The other tests here pin the CUDA-core route
+The tensor-core route (BF16, K = V = 128, delta rule, serial or split into
+segments; force_path=2, and the plan's choice for those shapes) computes
+with BF16 operands in its forward recompute and reverse scan, and with
+FP32 operands carried as BF16 hi + lo pairs in its per-chunk products:
+every gradient is held to 1e-2, two sets of BF16 operand roundings of the
+kind the forward's 6e-3 bar covers once.  The other tests here pin the CUDA-core route
 (force_path=1), whose bars are the FP32 ones above.
 """
 import numpy as np
