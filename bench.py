@@ -315,7 +315,8 @@ def bwd_algorithmic(kernel, x, c):
 
 # The translation unit each kernel is compiled from (plus every shared header).
 KERNEL_SOURCES = {"tc_prep": "tc_prep.cu", "tc_chain": "tc_chain.cu", "tc_gla": "tc_gla.cu",
-                  "tc_prescan": "tc_prescan.cu", "recurrent": "recurrent.cu",
+                  "tc_prescan": "tc_prescan.cu", "tc_bwd_scan": "tc_bwd_scan.cu",
+                  "tc_bwd_grad": "tc_bwd_grad.cu", "recurrent": "recurrent.cu",
                   "compose": "compose.cu", "simt": "simt_path.cu", "bwd": "simt_bwd.cu"}
 
 
@@ -1108,13 +1109,14 @@ def run_bwd(args):
     fl = f / (dom_ms * 1e-3) / 1e12 if f else 0.0
     if f and fl / fp32_tflops >= hb / hbm:
         roofline = {"kernel": dom, "bound": "alu", "achieved": fl, "peak": fp32_tflops,
-                    "unit": "TFLOP/s", "frac": fl / fp32_tflops, "traffic": traffic_record(dom, args.workload),
+                    "unit": "TFLOP/s", "frac": fl / fp32_tflops,
+                    "traffic": traffic_record(dom, "bwd_" + args.workload),
                     "algorithmic_flops_per_launch": f, "avg_launch_ms": dom_ms,
                     "peak_source": "FP32 CUDA-core peak: 152 SMs x 128 lanes x 2 flops x "
                                    f"{sm_mhz:.0f} MHz (no measured FP32 peak)"}
     else:
         roofline = {"kernel": dom, "bound": "hbm", "achieved": hb, "peak": hbm, "unit": "GB/s",
-                    "frac": hb / hbm, "traffic": traffic_record(dom, args.workload),
+                    "frac": hb / hbm, "traffic": traffic_record(dom, "bwd_" + args.workload),
                     "algorithmic_bytes_per_launch": b, "avg_launch_ms": dom_ms,
                     "peak_source": peaks["source"] + " (hbm_gbs, copy bandwidth)"}
     roofline["timing"] = ("CUDA events around each launch on its stream, over a second pass "
