@@ -289,11 +289,20 @@ def bwd_algorithmic(kernel, x, c):
         # h mirror written
         return (ch * (2 * 16384 + 272) + th * K * es + ch * L * V * f32 + ch * K * V * 2,
                 None)
+    elif kernel == "tc_chain_segment_recompute":  # as the serial recompute, from the segment states
+        return (ch * (2 * 16384 + 272) + th * K * es + ch * L * V * f32 + ch * K * V * 2
+                + c["segments"] * K * V * f32, None)
     elif kernel == "tc_bwd_scan":
-        # W^T, Q~, P, vectors, k, dO read; dV' (FP32) and the BF16 image of
-        # the E mirror written; dht / dh0
+        # W^T, Q~, P, vectors, k, dO read; dV' (a BF16 hi + lo pair) and the
+        # BF16 image of the E mirror written; dht / dh0
         return (ch * (2 * 16384 + 8192 + 272) + th * (K + V) * es + ch * L * V * f32
                 + ch * K * V * 2 + 2 * st, None)
+    elif kernel == "tc_bwd_scan_prescan":  # the same reads; each segment's offset written
+        return (ch * (2 * 16384 + 8192 + 272) + th * (K + V) * es
+                + c["segments"] * K * V * f32, None)
+    elif kernel == "tc_bwd_scan_segment_out":  # the serial scan's bytes from the segment ends
+        return (ch * (2 * 16384 + 8192 + 272) + th * (K + V) * es + ch * L * V * f32
+                + ch * K * V * 2 + c["segments"] * K * V * f32, None)
     elif kernel == "tc_bwd_grad":
         # h and E images, dO, q, k, v, T, dV', v_new (the FP32 operands as
         # BF16 hi + lo pairs: as many bytes as FP32), G, beta read; dq, dk,

@@ -92,7 +92,7 @@ def test_traffic_records_follow_each_kernels_includes():
             f = dict(kv.split("=", 1) for kv in line.split())
             kernels.add(f["kernel"])
             assert float(f["dram_bytes_per_launch"]) >= 0
-    assert {"tc_prep", "tc_chain_serial", "bwd_local", "recurrent"} <= kernels
+    assert {"tc_prep", "tc_chain_serial", "tc_bwd_grad", "tc_bwd_scan"} <= kernels
 
 
 def test_measured_traffic_stays_near_the_algorithmic_bytes():
@@ -109,18 +109,23 @@ def test_measured_traffic_stays_near_the_algorithmic_bytes():
             continue
         f = dict(kv.split("=", 1) for kv in line.split())
         k, w, t = f["kernel"], f["workload"], float(f["dram_bytes_per_launch"])
+        backward = w.startswith("bwd_")  # a backward-pass kernel, on workload w[4:]
         if w not in cache:
-            x = synthetic.make_inputs(synthetic.WORKLOADS[w])
+            x = synthetic.make_inputs(synthetic.WORKLOADS[w[4:] if backward else w])
             plan = pkg.gdr_plan_query(x["B"], x["T"], x["H"], x["K"], x["V"],
                                       N=x["N"] if x["cu_seqlens"] is not None else 0,
                                       dtype={"f32": 0, "bf16": 1, "f16": 2}[x["dtype"]],
                                       beta_free=x["beta"] is None)
             cache[w] = (x, b.counts(x, plan["n_segments"]))
         x, c = cache[w]
-        a = b.bwd_algorithmic(k, x, b.counts(x, 1))[0] if k.startswith("bwd_") else \
-            b.algorithmic_bytes(k, x, c)
+        if backward:
+            a = b.bwd_algorithmic(k, x, c)[0]
+        elif k.startswith("bwd_"):
+            a = b.bwd_algorithmic(k, x, b.counts(x, 1))[0]
+        else:
+            a = b.algorithmic_bytes(k, x, c)
         if not a or a < (1 << 20):
             continue
         assert t <= 1.25 * a, (k, w, t / a)
         checked += 1
-    assert checked >= 20
+    assert checked >= 25
