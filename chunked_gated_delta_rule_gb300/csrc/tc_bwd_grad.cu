@@ -96,21 +96,29 @@ static_assert(kSmemLaunch <= 232448, "shared memory per CTA");
 constexpr uint32_t kLoadA = 3 * 32768 + 2 * 16384 + kLkImgVecBytes;  // h, E, V'; dO, v; G, beta
 constexpr uint32_t kLoadB = 2 * 16384 + 32768 + 16384;                // q, k; dV', T
 
-// TMEM columns (128 lanes each, FP32), 64 columns per accumulator
+// TMEM columns (128 lanes each, FP32).  Products of an FP32 operand's hi and
+// lo halves run as one N = 128 MMA into two 64-column halves, summed when
+// read; a region is reused once its readers are done:
+//   group 1: P1 [0, 64)  P3 [64, 192)  [Q K^T; K K^T] [192, 256)  dVb^T [256, 384)
+//   group 2: [dm; Y] [256, 384)  dVb lo V' hi^T (rows 64-127) [384, 448)  dVb h^T [448, 512)
+//   group 3: (Z K)^T [192, 320)  (Z^T Q + S^T K + S K)^T [320, 448)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kCP1 = 0;     // (dO h^T)^T            [key][t]
-constexpr uint32_t kCP3 = 64;    // (V' E^T)^T            [key][t]
-constexpr uint32_t kCQK = 128;   // [Q K^T; K K^T]        [t | 64 + t][j]
-constexpr uint32_t kCDvb = 192;  // dVb^T [v][j]; then rows 64-127: dVb lo V' hi^T
-constexpr uint32_t kCDmY = 256;  // [dO V'^T; dVb V'^T]  [i | 64 + i][j]
-constexpr uint32_t kCKb = 320;   // (dVb h^T)^T           [key][i]
-constexpr uint32_t kCXq = 384;   // (Z K)^T               [key][i]
-constexpr uint32_t kCXk = 448;   // (Z^T Q + S^T K + S K)^T
+constexpr uint32_t kCP3 = 64;    // (V' E^T)^T            [key][t], hi | lo halves
+constexpr uint32_t kCQK = 192;   // [Q K^T; K K^T]        [t | 64 + t][j]
+constexpr uint32_t kCDvb = 256;  // dVb^T [v][j]: T hi | T lo halves (dV' lo T hi in the first)
+constexpr uint32_t kCDmY = 256;  // [dO V'^T; dVb V'^T]  [i | 64 + i][j], V' hi | lo halves
+constexpr uint32_t kCD2 = 384;   // rows 64-127: dVb lo V' hi^T
+constexpr uint32_t kCKb = 448;   // (dVb h^T)^T           [key][i]
+constexpr uint32_t kCXq = 192;   // (Z K)^T               [key][i], Z hi | lo halves
+constexpr uint32_t kCXk = 320;   // (Z^T Q + S^T K + S K)^T, hi | lo halves
 
-constexpr uint32_t kIdMnK = idesc_bf16(128, 64, 1, 0);   // A MN-major, B K-major
-constexpr uint32_t kIdKK = idesc_bf16(128, 64, 0, 0);    // both K-major
-constexpr uint32_t kIdKMn = idesc_bf16(128, 64, 0, 1);   // A K-major, B MN-major
-constexpr uint32_t kIdMnMn = idesc_bf16(128, 64, 1, 1);  // both MN-major
+constexpr uint32_t kIdMnK = idesc_bf16(128, 64, 1, 0);    // A MN-major, B K-major
+constexpr uint32_t kIdKK = idesc_bf16(128, 64, 0, 0);     // both K-major
+constexpr uint32_t kIdKMn = idesc_bf16(128, 64, 0, 1);    // A K-major, B MN-major
+constexpr uint32_t kIdMnMn2 = idesc_bf16(128, 128, 1, 1);  // N = 128 (hi | lo)
+constexpr uint32_t kIdKMn2 = idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t kIdMnK2 = idesc_bf16(128, 128, 1, 0);
 
 // Column sums of a warp's 32 x 32 block: on entry lane l holds x[c] = entry
 // (l, c); on return x[0] of lane l is the sum over the 32 lanes of column l.
@@ -318,24 +326,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
                 umma_bf16(tmem + kCP1, at(dM16, kOffH + kk * 2048),
                           at(dK, kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32), kIdMnK, kk > 0);
 #pragma unroll
-            for (int pz = 0; pz < 2; ++pz)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // over v; V' hi, then lo
-                    umma_bf16(tmem + kCP3, at(dM24, kOffB + 8192 + kk * 2048),
-                              at(dM8, kOffD + pz * 16384 + kk * 2048), kIdMnMn, (pz | kk) != 0);
+            for (int kk = 0; kk < 8; ++kk)  // over v; B = [V' hi | V' lo]
+                umma_bf16(tmem + kCP3, at(dM24, kOffB + 8192 + kk * 2048),
+                          at(dM16, kOffD + kk * 2048), kIdMnMn2, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // over keys
                 umma_bf16(tmem + kCQK, at(dK, kOffC + (kk >> 2) * kBlkC + (kk & 3) * 32),
                           at(dK, kOffC + 8192 + (kk >> 2) * kBlkC + (kk & 3) * 32), kIdKK, kk > 0);
 #pragma unroll
-            for (int t3 = 0; t3 < 3; ++t3) {  // dV' hi T hi, dV' hi T lo, dV' lo T hi
-                const uint32_t oa = kOffF + (t3 == 2 ? kFdvLo : kFdvHi);
-                const uint32_t ob = kOffF + (t3 == 1 ? kFtLo : kFtHi);
+            for (int kk = 0; kk < 4; ++kk)  // over tokens i: dV' hi [T hi | T lo]
+                umma_bf16(tmem + kCDvb, at(dK, kOffF + kFdvHi + kk * 32),
+                          at(dM8, kOffF + kFtHi + kk * 2048), kIdKMn2, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // over tokens i
-                    umma_bf16(tmem + kCDvb, at(dK, oa + kk * 32), at(dM8, ob + kk * 2048), kIdKMn,
-                              (t3 | kk) != 0);
-            }
+            for (int kk = 0; kk < 4; ++kk)  // dV' lo T hi, into the first half
+                umma_bf16(tmem + kCDvb, at(dK, kOffF + kFdvLo + kk * 32),
+                          at(dM8, kOffF + kFtHi + kk * 2048), kIdKMn, 1u);
             umma_commit(&bars[1]);
         }
         {  // <E, h> over the two images (the same layout), meanwhile
@@ -360,7 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         // hi / lo tiles (group 2's operand), dv, rowdot(dVb, V)
         {
             float f[32], x[32];
-            tmem_load32f(tl + kCDvb + j0, f);  // dVb[j][v = r]
+            tmem_load2(tl + kCDvb + j0, tl + kCDvb + 64 + j0, f, x);  // dVb[j][v = r]
+#pragma unroll
+            for (int u = 0; u < 32; ++u) f[u] += x[u];
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 const int j = j0 + u;
@@ -384,14 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int pz = 0; pz < 2; ++pz)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // over v; V' hi, then lo
-                    umma_bf16(tmem + kCDmY, at(dK, kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32),
-                              at(dM8, kOffD + pz * 16384 + kk * 2048), kIdKMn, (pz | kk) != 0);
+            for (int kk = 0; kk < 8; ++kk)  // over v; B = [V' hi | V' lo]
+                umma_bf16(tmem + kCDmY, at(dK, kOffB + (kk >> 2) * kBlkB + (kk & 3) * 32),
+                          at(dM16, kOffD + kk * 2048), kIdKMn2, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // [dVb hi; dVb lo] V' hi^T: rows 64-127 used
-                umma_bf16(tmem + kCDvb, at(dK, kOffB + 8192 + (kk >> 2) * kBlkB + (kk & 3) * 32),
+                umma_bf16(tmem + kCD2, at(dK, kOffB + 8192 + (kk >> 2) * kBlkB + (kk & 3) * 32),
                           at(dM8, kOffD + kk * 2048), kIdKMn, kk > 0);
 #pragma unroll
             for (int pz = 0; pz < 2; ++pz)
@@ -406,7 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         {
             float f[32], g[32], x[32];
             const uint32_t oq = kOffC + (r >> 6) * kBlkC;
-            tmem_load2(tl + kCP1 + j0, tl + kCP3 + j0, f, g);  // P1, P3 [i][key = r]
+            tmem_load3(tl + kCP1 + j0, tl + kCP3 + j0, tl + kCP3 + 64 + j0, f, g, x);  // P1, P3
+#pragma unroll
+            for (int u = 0; u < 32; ++u) g[u] += x[u];
 #pragma unroll
             for (int u = 0; u < 32; ++u) x[u] = f[u] * bf16_at(sm + oq + sw128_off(j0 + u, r & 63, 64));
             mf[kR1 + 64 * q4 + j0 + lane_id] = warp_colsum32(x, lane_id);
@@ -424,7 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
             float f[32], g[32], srow[32];
             if (q4 < 2) {
                 const int i = r;
-                tmem_load2(tl + kCDmY + j0, tl + kCQK + j0, f, g);  // dm, Q K^T [i][j]
+                float f2[32];
+                tmem_load3(tl + kCDmY + j0, tl + kCDmY + 64 + j0, tl + kCQK + j0, f, f2, g);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) f[u] += f2[u];  // dm[i][j]; g: (Q K^T)[i][j]
                 const float Gi = mf[kVG + i], epi = mf[kVEp + i];
                 float z[32], rowR = 0.f;
 #pragma unroll
@@ -446,9 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
             } else {
                 const int i = r - 64;
                 float y2[32];
-                tmem_load3(tl + kCDmY + j0, tl + kCDvb + j0, tl + kCQK + j0, f, y2, g);
+                tmem_load3(tl + kCDmY + j0, tl + kCDmY + 64 + j0, tl + kCD2 + j0, f, y2, g);
 #pragma unroll
-                for (int u = 0; u < 32; ++u) f[u] += y2[u];  // Y[i][j]: dVb hi + lo parts; g: K K^T
+                for (int u = 0; u < 32; ++u) f[u] += y2[u] + g[u];  // Y[i][j]: its three parts
+                tmem_load32f(tl + kCQK + j0, g);                   // (K K^T)[i][j]
                 const float Gi = mf[kVG + i], bi = mf[kVB + i], epi = mf[kVEp + i];
                 float rdA = 0.f;
 #pragma unroll
@@ -475,30 +486,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // ---- group 3: (Z K)^T, (Z^T Q + S^T K + S K)^T
+        // ---- group 3: (Z K)^T, (Z^T Q + S^T K + S K)^T, each over [hi | lo]
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int pz = 0; pz < 2; ++pz)
+            for (int kk = 0; kk < 4; ++kk)  // over tokens j; B = [Z hi; Z lo] rows
+                umma_bf16(tmem + kCXq, at(dM16, kOffC + 8192 + kk * 2048),
+                          at(dK, kOffF + kFzHi + kk * 32), kIdMnK2, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // over tokens j; Z hi, then lo
-                    umma_bf16(tmem + kCXq, at(dM16, kOffC + 8192 + kk * 2048),
-                              at(dK, kOffF + kFzHi + pz * 8192 + kk * 32), kIdMnK, (pz | kk) != 0);
-#pragma unroll
-            for (int t4 = 0; t4 < 4; ++t4) {  // Q^T Z hi, Q^T Z lo, K^T S hi, K^T S lo
-                const uint32_t oa = kOffC + (t4 < 2 ? 0u : 8192u);
-                const uint32_t ob = kOffF + (t4 < 2 ? kFzHi : kFsHi) + (t4 & 1) * 8192;
+            for (int t3 = 0; t3 < 2; ++t3) {  // Q^T [Z hi | Z lo], K^T [S hi | S lo]
+                const uint32_t oa = kOffC + (t3 ? 8192u : 0u);
+                const uint32_t ob = kOffF + (t3 ? kFsHi : kFzHi);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tmem + kCXk, at(dM16, oa + kk * 2048), at(dM8, ob + kk * 2048), kIdMnMn,
-                              (t4 | kk) != 0);
+                    umma_bf16(tmem + kCXk, at(dM16, oa + kk * 2048), at(dM8, ob + kk * 2048),
+                              kIdMnMn2, (t3 | kk) != 0);
             }
 #pragma unroll
-            for (int pz = 0; pz < 2; ++pz)  // K^T S^T: S hi, then lo as the K-major operand
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(tmem + kCXk, at(dM16, kOffC + 8192 + kk * 2048),
-                              at(dK, kOffF + kFsHi + pz * 8192 + kk * 32), kIdMnK, 1);
+            for (int kk = 0; kk < 4; ++kk)  // K^T S^T: [S hi; S lo] rows as the K-major operand
+                umma_bf16(tmem + kCXk, at(dM16, kOffC + 8192 + kk * 2048),
+                          at(dK, kOffF + kFsHi + kk * 32), kIdMnK2, 1u);
             umma_commit(&bars[3]);
         }
         {  // while group 3 runs: r2 = rowdot(dKb, K), dKb = -dVb h^T
@@ -515,17 +522,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_grad(const __grid_consta
         if (tid == 0 && next < n_items) issue_b(next);
         // ---- epilogue 3: dq, dk (lanes = keys)
         {
-            float f[32], x[32], kb[32];
-            tmem_load2(tl + kCP1 + j0, tl + kCXq + j0, f, x);
+            float f[32], x[32], y[32];
+            tmem_load3(tl + kCP1 + j0, tl + kCXq + j0, tl + kCXq + 64 + j0, f, x, y);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) x[u] = fmaf(scale * mf[kVGam + j0 + u], f[u], x[u]);
+            for (int u = 0; u < 32; ++u) x[u] = fmaf(scale * mf[kVGam + j0 + u], f[u], x[u] + y[u]);
             store_cols(static_cast<__nv_bfloat16 *>(args.a.dq), x, t0, hh, len);
-            tmem_load3(tl + kCP3 + j0, tl + kCXk + j0, tl + kCKb + j0, f, x, kb);
+            tmem_load3(tl + kCP3 + j0, tl + kCP3 + 64 + j0, tl + kCKb + j0, f, y, x);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
+            for (int u = 0; u < 32; ++u) {  // x: -beta gamma dKb + lam P3
                 const int i = j0 + u;
-                x[u] = fmaf(-mf[kVB + i] * mf[kVGam + i], kb[u], fmaf(mf[kVLam + i], f[u], x[u]));
+                x[u] = fmaf(-mf[kVB + i] * mf[kVGam + i], x[u], mf[kVLam + i] * (f[u] + y[u]));
             }
+            tmem_load2(tl + kCXk + j0, tl + kCXk + 64 + j0, f, y);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[u] += f[u] + y[u];
             store_cols(static_cast<__nv_bfloat16 *>(args.a.dk), x, t0, hh, len);
         }
         // ---- dbeta and the gate gradient
