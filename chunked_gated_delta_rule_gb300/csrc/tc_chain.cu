@@ -19,10 +19,15 @@
 // one rounding to BF16) and K~ = diag(e^{G_last - G}) K formed here, in
 // place in the stage.  The formulation is
 // the transposed one (value columns are TMEM lanes), so every MMA has M =
-// 128.  The warps specialise:
+// 128.  The A operands (the BF16 mirror of h^T and v_new^T) live in tensor
+// memory, so an MMA reads only its B tile from shared memory: shared-memory
+// bandwidth, which the stage loads, the K~ pass and the output staging also
+// draw on, bounds a chunk's MMAs when A is read from there as well.  The
+// warps specialise:
 //   warps 0-3  the state path, which is the serial dependency: per chunk the
 //              BF16 mirror of h^T (and h^T scaled by e^{G_last} in place),
-//              then v_new^T once the first product lands;
+//              then v_new^T once the first product lands, both written to
+//              tensor memory;
 //   warps 4-7  the side path: K~ in place once a chunk lands, then the
 //              previous chunk's O, staged and stored (a TMA store for whole
 //              chunks);
@@ -84,9 +89,7 @@ constexpr int kRing = 3;       // decoded chains handed out ahead (bounds the lo
 //                      loaded, scaled in place
 //   scale P 8 KB: B operand of O (K-major, N = 64); U^T 16 KB; vectors.
 constexpr uint32_t kStage = kRecBytes;
-constexpr uint32_t kOffHm = 2 * kStage;        // h^T mirror, K-major, 32 KB
-constexpr uint32_t kOffVn = kOffHm + 32768;    // v_new^T tile, 16 KB
-constexpr uint32_t kOffOs = kOffVn + 16384;    // output staging, 16 KB
+constexpr uint32_t kOffOs = 2 * kStage;        // output staging, 16 KB
 constexpr uint32_t kOffRing = kOffOs + 16384;  // decoded chains
 enum : int {
     kBFull = 0,     // [2] stage landed (bulk-copy and TMA bytes)
@@ -119,6 +122,9 @@ constexpr uint32_t kSmemLaunch = kOffMisc + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0;    // two buffers of [h^T W^T | O], 128 columns each
 constexpr uint32_t kColS = 256;  // FP32 state h^T, 128 columns
+constexpr uint32_t kColM = 384;  // BF16 mirror of h^T, two keys a column, 64 columns
+constexpr uint32_t kColV = 448;  // BF16 v_new^T, two tokens a column, 32 columns
+static_assert(kColV + 32 <= kTmemCols, "TMEM columns");
 
 constexpr uint32_t kIdescW = idesc_bf16(128, 64, 0, 1);   // B = W^T, MN-major
 constexpr uint32_t kIdescQ = idesc_bf16(128, 64, 0, 0);   // B = Q~, K-major
@@ -304,24 +310,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    // h^T W^T, then O = h^T Q~^T while v_new is formed
+                    // h^T W^T, then O = h^T Q~^T while v_new is formed (A = the
+                    // mirror in TMEM)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16(tmem + kColA + 128 * b,
-                                  sdesc_sw128(sb + kOffHm + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
-                                              1024),
-                                  sdesc_sw128(sta + kImgW + kk * 2048, 16384, 1024), kIdescW,
-                                  kk > 0);
+                        umma_bf16_ts(tmem + kColA + 128 * b, tmem + kColM + 8 * kk,
+                                     sdesc_sw128(sta + kImgW + kk * 2048, 16384, 1024), kIdescW,
+                                     kk > 0);
                     umma_commit(&bars[kBAdone]);
                     if (kOut) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
-                            umma_bf16(tmem + kColA + 128 * b + 64,
-                                      sdesc_sw128(sb + kOffHm + (kk >> 2) * 16384 + (kk & 3) * 32,
-                                                  16, 1024),
-                                      sdesc_sw128(sta + kImgQ + (kk >> 2) * 8192 + (kk & 3) * 32,
-                                                  16, 1024),
-                                      kIdescQ, kk > 0);
+                            umma_bf16_ts(tmem + kColA + 128 * b + 64, tmem + kColM + 8 * kk,
+                                         sdesc_sw128(sta + kImgQ + (kk >> 2) * 8192 + (kk & 3) * 32,
+                                                     16, 1024),
+                                         kIdescQ, kk > 0);
                     }
                     if (!wait(kBVready, gk) || !wait(kBKready + b, gk >> 1)) {
                         ok = false;
@@ -330,16 +333,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + kColS, sdesc_sw128(sb + kOffVn + kk * 32, 16, 1024),
-                                  sdesc_sw128(sta + kImgK + kk * 2048, 8192, 1024), kIdescH, 1u);
+                        umma_bf16_ts(tmem + kColS, tmem + kColV + 8 * kk,
+                                     sdesc_sw128(sta + kImgK + kk * 2048, 8192, 1024), kIdescH, 1u);
                     umma_commit(&bars[kBHdone]);
                     if (kOut) {  // O += v_new^T (scale P)^T
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            umma_bf16(tmem + kColA + 128 * b + 64,
-                                      sdesc_sw128(sb + kOffVn + kk * 32, 16, 1024),
-                                      sdesc_sw128(sta + kImgP + kk * 32, 16, 1024), kIdescO2,
-                                      1u);
+                            umma_bf16_ts(tmem + kColA + 128 * b + 64, tmem + kColV + 8 * kk,
+                                         sdesc_sw128(sta + kImgP + kk * 32, 16, 1024), kIdescO2,
+                                         1u);
                         umma_commit(&bars[kBO2 + b]);
                     }
                     umma_commit(&bars[kBFree + b]);
@@ -394,36 +396,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         reg_fence(r1);
                     }
                 };
-                // h_pre -> BF16 mirror (the first product's A operand): the
-                // chain's critical path, so it goes first
-                // the recompute's image of the chunk's h^T mirror, for the
-                // backward's per-chunk gradients
+                // h_pre -> BF16 mirror in TMEM (two keys a column; the first
+                // product's A operand): the chain's critical path, so it goes
+                // first.  The recompute also writes the mirror's byte image
+                // (128-byte swizzled rows) for the backward's per-chunk
+                // gradients.
                 uint8_t *limg = kImages
                                     ? ws.bwd_lkimg + ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes
                                     : nullptr;
 #pragma unroll 1
                 for (int hq = 0; hq < 2; ++hq) {
-                    uint32_t r0[32], r1[32];
+                    uint32_t r0[32], r1[32], m[32];
                     state_half(hq, r0, r1);
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        float x[8], y[8];
+                    for (int i = 0; i < 16; ++i) {
+                        m[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                        m[16 + i] =
+                            pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+                    }
+                    tmem_st32(tmem + lane + kColM + 32 * hq, m);
+                    if (kImages) {
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            x[u] = __uint_as_float(r0[8 * c8 + u]);
-                            y[u] = __uint_as_float(r1[8 * c8 + u]);
-                        }
-                        const uint32_t ox = sw128_off(row, 64 * hq + 8 * c8, 128);
-                        const uint32_t oy = sw128_off(row, 64 * hq + 32 + 8 * c8, 128);
-                        st_bf16x8(sm + kOffHm + ox, x);
-                        st_bf16x8(sm + kOffHm + oy, y);
-                        if (kImages) {
-                            st_bf16x8(limg + kLkImgH + ox, x);
-                            st_bf16x8(limg + kLkImgH + oy, y);
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const uint32_t ox = sw128_off(row, 64 * hq + 8 * c8, 128);
+                            const uint32_t oy = sw128_off(row, 64 * hq + 32 + 8 * c8, 128);
+                            *reinterpret_cast<uint4 *>(limg + kLkImgH + ox) =
+                                make_uint4(m[4 * c8], m[4 * c8 + 1], m[4 * c8 + 2], m[4 * c8 + 3]);
+                            *reinterpret_cast<uint4 *>(limg + kLkImgH + oy) =
+                                make_uint4(m[16 + 4 * c8], m[16 + 4 * c8 + 1], m[16 + 4 * c8 + 2],
+                                           m[16 + 4 * c8 + 3]);
                         }
                     }
                 }
-                fence_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
                 mbar_arrive(&bars[kBMready]);
                 // then the FP32 state scaled by e^{G_last} for the update product,
                 // while the first product runs
@@ -441,8 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 }
                 if (!wait(kBAdone, gk)) { ok = false; break; }
                 tc_fence_after();
-                {  // v_new^T = U^T - h^T W^T
-                    uint32_t w0[32], w1[32];
+                {  // v_new^T = U^T - h^T W^T, to TMEM as BF16 (two tokens a column)
+                    uint32_t w0[32], w1[32], vv[32];
                     tmem_ld32(tmem + lane + kColA + 128 * b, w0);
                     tmem_ld32(tmem + lane + kColA + 128 * b + 32, w1);
 #pragma unroll
@@ -465,20 +471,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
 #pragma unroll
                         for (int i = 0; i < 32; ++i) u[i] -= __uint_as_float(hh ? w1[i] : w0[i]);
 #pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
-                            st_bf16x8(sm + kOffVn + ou, u + 8 * c8);
-                            if (kImages) {  // v_new^T as BF16 hi + lo images
-                                uint8_t *vimg = ws.bwd_lkimg +
-                                                ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes;
+                        for (int i = 0; i < 16; ++i) vv[16 * hh + i] = pack_bf16x2(u[2 * i], u[2 * i + 1]);
+                        if (kImages) {  // v_new^T as BF16 hi + lo images
+                            uint8_t *vimg =
+                                ws.bwd_lkimg + ((int64_t)(C.c_begin + cc) * H + h) * kLkImgBytes;
+#pragma unroll
+                            for (int c8 = 0; c8 < 4; ++c8) {
+                                const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
                                 st_split_bf16x8(vimg + kLkImgVh + ou, vimg + kLkImgVl + ou,
                                                 u + 8 * c8);
                             }
                         }
                     }
+                    tmem_st32(tmem + lane + kColV, vv);
                 }
-                fence_async_smem();
-                tmem_wait_st();  // the scaled state, before the update product
+                tmem_wait_st();  // v_new and the scaled state, before the update product
                 tc_fence_before();
                 mbar_arrive(&bars[kBVready]);
                 if (!wait(kBHdone, gk)) { ok = false; break; }
