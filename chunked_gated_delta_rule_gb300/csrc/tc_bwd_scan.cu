@@ -27,7 +27,10 @@
 // dV'^T is stored as a pair of BF16 images (hi + lo) and the E^T mirror as
 // its byte image, for the per-chunk gradients (tc_bwd_grad.cu); dh0 is E
 // after the sequence's first chunk.  The state stays FP32 in TMEM; its BF16 mirror,
-// dV' and dO are the MMA operands (the route's tolerance covers them).
+// dV' and dO are the MMA operands (the route's tolerance covers them).  The
+// mirror and -dV'^T, the A operands the state path forms, are written to
+// tensor memory, so those products read only their B tiles from shared
+// memory.
 //
 // Warps: 0-3 state path (the serial dependency: E mirror and image, decay,
 // dV'), 4-7 side path (K~ in place; rows past a sequence's end zeroed in
@@ -59,13 +62,10 @@ constexpr int kRing = 3;
 
 // Shared memory: two stages of the record image (layout in tc_chunk.cuh),
 // with the dO tile in the U^T slot (two 64-column blocks, 128-byte
-// swizzled rows of 64 tokens); the BF16 mirror of E^T (K-major, 32 KB); the
-// -dV'^T tile (K-major, 16 KB); chain ring, barriers.
+// swizzled rows of 64 tokens); chain ring, barriers.
 constexpr uint32_t kStage = kRecBytes;
 constexpr uint32_t kImgDo = kImgU;
-constexpr uint32_t kOffEm = 2 * kStage;
-constexpr uint32_t kOffDv = kOffEm + 32768;
-constexpr uint32_t kOffRing = kOffDv + 16384;
+constexpr uint32_t kOffRing = 2 * kStage;
 enum : int {
     kBFull = 0,     // [2] stage landed
     kBMready = 2,   // mirror of E^T written (state path, 128)
@@ -94,6 +94,8 @@ constexpr uint32_t kSmemLaunch = kOffMisc + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;    // two buffers of dV'^T (64 columns), 128 apart
 constexpr uint32_t kColE = 256;  // FP32 E^T, 128 columns
+constexpr uint32_t kColM = 384;  // BF16 mirror of E^T, two keys a column, 64 columns
+constexpr uint32_t kColV = 448;  // BF16 -dV'^T, two tokens a column, 32 columns
 
 constexpr uint32_t kIdescDP = idesc_bf16(128, 64, 1, 1);    // dO^T (scale P)
 constexpr uint32_t kIdescEK = idesc_bf16(128, 64, 0, 0);    // E^T K~^T
@@ -252,12 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                     // D += E^T K~^T
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16(dcol,
-                                  sdesc_sw128(sb + kOffEm + (kk >> 2) * 16384 + (kk & 3) * 32, 16,
-                                              1024),
-                                  sdesc_sw128(sta + kImgK + (kk >> 2) * 8192 + (kk & 3) * 32, 16,
-                                              1024),
-                                  kIdescEK, 1u);
+                        umma_bf16_ts(dcol, tmem + kColM + 8 * kk,
+                                     sdesc_sw128(sta + kImgK + (kk >> 2) * 8192 + (kk & 3) * 32, 16,
+                                                 1024),
+                                     kIdescEK, 1u);
                     umma_commit(&bars[kBAdone]);
                     if (!wait(kBVready, gk)) { ok = false; break; }
                     tc_fence_after();
@@ -268,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                                   sdesc_sw128(sta + kImgQ + kk * 2048, 8192, 1024), kIdescDQ, 1u);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + kColE, sdesc_sw128(sb + kOffDv + kk * 32, 16, 1024),
-                                  sdesc_sw128(sta + kImgW + kk * 32, 16, 1024), kIdescVW, 1u);
+                        umma_bf16_ts(tmem + kColE, tmem + kColV + 8 * kk,
+                                     sdesc_sw128(sta + kImgW + kk * 32, 16, 1024), kIdescVW, 1u);
                     umma_commit(&bars[kBHdone]);
                     umma_commit(&bars[kBFree + b]);
                 }
@@ -330,27 +330,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                 uint8_t *limg = args.lkimg + item * kLkImgBytes;
 #pragma unroll 1
                 for (int hq = 0; hq < 2; ++hq) {
-                    uint32_t r0[32], r1[32];
+                    uint32_t r0[32], r1[32], m[32];
                     state_half(hq, r0, r1);
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        float x[8], y[8];
+                    for (int i = 0; i < 16; ++i) {
+                        m[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                        m[16 + i] =
+                            pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+                    }
+                    tmem_st32(tmem + lane + kColM + 32 * hq, m);
+                    if (kImages) {
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            x[u] = __uint_as_float(r0[8 * c8 + u]);
-                            y[u] = __uint_as_float(r1[8 * c8 + u]);
-                        }
-                        const uint32_t ox = sw128_off(row, 64 * hq + 8 * c8, 128);
-                        const uint32_t oy = sw128_off(row, 64 * hq + 32 + 8 * c8, 128);
-                        st_bf16x8(sm + kOffEm + ox, x);
-                        st_bf16x8(sm + kOffEm + oy, y);
-                        if (kImages) {
-                            st_bf16x8(limg + kLkImgE + ox, x);
-                            st_bf16x8(limg + kLkImgE + oy, y);
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const uint32_t ox = sw128_off(row, 64 * hq + 8 * c8, 128);
+                            const uint32_t oy = sw128_off(row, 64 * hq + 32 + 8 * c8, 128);
+                            *reinterpret_cast<uint4 *>(limg + kLkImgE + ox) =
+                                make_uint4(m[4 * c8], m[4 * c8 + 1], m[4 * c8 + 2], m[4 * c8 + 3]);
+                            *reinterpret_cast<uint4 *>(limg + kLkImgE + oy) =
+                                make_uint4(m[16 + 4 * c8], m[16 + 4 * c8 + 1], m[16 + 4 * c8 + 2],
+                                           m[16 + 4 * c8 + 3]);
                         }
                     }
                 }
-                fence_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
                 mbar_arrive(&bars[kBMready]);
                 // E^T decayed by e^{G_last} in TMEM, while D is formed
 #pragma unroll 1
@@ -375,25 +378,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                     reg_fence(w0);
                     reg_fence(w1);
                     uint8_t *dimg = args.lkimg + item * kLkImgBytes;
+                    uint32_t vv[32];
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8) {
-                            float d[8], u[8];
+                            float d[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
+                            for (int i = 0; i < 8; ++i)
                                 d[i] = __uint_as_float(hh ? w1[8 * c8 + i] : w0[8 * c8 + i]);
-                                u[i] = -d[i];
-                            }
-                            const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
-                            st_bf16x8(sm + kOffDv + ou, u);
-                            if (kImages)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                vv[16 * hh + 4 * c8 + i] = pack_bf16x2(-d[2 * i], -d[2 * i + 1]);
+                            if (kImages) {
+                                const uint32_t ou = sw128_off(row, 32 * hh + 8 * c8, 128);
                                 st_split_bf16x8(dimg + kLkImgDh + ou, dimg + kLkImgDl + ou, d);
+                            }
                         }
                     }
+                    tmem_st32(tmem + lane + kColV, vv);
                 }
-                fence_async_smem();
-                tmem_wait_st();  // the decayed state, before the update products
+                tmem_wait_st();  // -dV'^T and the decayed state, before the update products
                 tc_fence_before();
                 mbar_arrive(&bars[kBVready]);
                 if (!wait(kBHdone, gk)) { ok = false; break; }

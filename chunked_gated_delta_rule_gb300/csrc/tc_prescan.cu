@@ -8,9 +8,10 @@
 // with K~ = diag(e^{G_last - G}) K; the segment's summaries are c_s = h_c and
 // M_s^T = h_t (the K x K transition of cuLA PR #127 "Root cause and
 // implementation", kept in FP32).  The two chains share every load and the
-// K~ pass, and their BF16 mirrors (the first product's A operand) live in
-// tensor memory, so shared memory holds only the two-stage ring of record
-// images and the two v_new tiles.
+// K~ pass, and their BF16 mirrors (the first product's A operand) and v_new
+// tiles (the update's A operand, written over the columns of h^T W^T it was
+// formed from) live in tensor memory, so shared memory holds only the
+// two-stage ring of record images, and an MMA reads only its B tile there.
 //
 // The two recurrences are independent, so each has its own warps and
 // barriers and runs at the latency of one chain: warps 0-3 (local state) and
@@ -42,10 +43,9 @@ constexpr int kThreads = 352;  // warps 0-3, 4-7 state paths; 8, 9 their MMAs; 1
 constexpr int kRing = 3;
 
 // Shared memory (bytes from a 1024-aligned base): two record-image stages
-// (only W, the k tile, U^T and the vectors are loaded), the two v_new tiles.
+// (only W, the k tile, U^T and the vectors are loaded).
 constexpr uint32_t kStage = kRecBytes;
-constexpr uint32_t kOffVn = 2 * kStage;          // [2] v_new^T tiles, 16 KB each
-constexpr uint32_t kOffRing = kOffVn + 2 * 16384;
+constexpr uint32_t kOffRing = 2 * kStage;
 enum : int {
     kPFull = 0,     // [2] stage landed
     kPKready = 2,   // [2] K~ formed in the stage (both paths: 256)
@@ -68,8 +68,9 @@ static_assert(sizeof(PreDesc) == 56, "chain descriptor layout");
 constexpr uint32_t kOffBar = kOffRing + 64 * kRing;
 constexpr uint32_t kSmemLaunch = kOffBar + 8 * kPNumBars + 16 + 1024;
 
-// TMEM (512 columns): h W^T of both states, both FP32 states, both mirrors
-// (two BF16 keys per column).
+// TMEM (512 columns): h W^T of both states (then v_new^T over its first 32
+// columns, two BF16 tokens per column), both FP32 states, both mirrors (two
+// BF16 keys per column).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColA = 0;     // [2] 64 columns each
 constexpr uint32_t kColS = 128;   // [2] 128 columns each
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
         if (lane_id == 0) {
             const int q = warp - 8;
             const uint32_t cA = tmem + kColA + 64 * q, cS = tmem + kColS + 128 * q;
-            const uint32_t cM = tmem + kColM + 64 * q, vn = sb + kOffVn + 16384 * q;
+            const uint32_t cM = tmem + kColM + 64 * q;
             int k = 0, gk = 0;
             bool ok = true;
             while (ok) {
@@ -219,11 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    // h^T += v_new^T K~
+                    // h^T += v_new^T K~ (A = v_new^T in TMEM; the next chunk's h^T W^T,
+                    // issued after this by the same thread, overwrites it only
+                    // once this product has read it)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(cS, sdesc_sw128(vn + kk * 32, 16, 1024),
-                                  sdesc_sw128(sta + kImgK + kk * 2048, 8192, 1024), kIdescH, 1u);
+                        umma_bf16_ts(cS, cA + 8 * kk,
+                                     sdesc_sw128(sta + kImgK + kk * 2048, 8192, 1024), kIdescH, 1u);
                     umma_commit(&bars[kPHdone + q]);
                     umma_commit(&bars[kPFree + b]);
                 }
@@ -238,7 +241,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
         const int path = warp >> 2;  // 0: local state from 0, 1: transition from I
         const int pt = tid & 127;
         const uint32_t cS = kColS + 128 * path, cM = kColM + 64 * path, cA = kColA + 64 * path;
-        uint8_t *vn = sm + kOffVn + 16384 * path;
         int k = 0, gk = 0;
         bool ok = true;
         while (ok) {
@@ -323,8 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                 mbar_arrive(&bars[kPKready + b]);
                 if (!wait(kPAdone + path, gk)) { ok = false; break; }
                 tc_fence_after();
-                {  // v_new^T = U^T - h^T W^T (the transition: U = 0)
-                    uint32_t w0[32], w1[32];
+                {  // v_new^T = U^T - h^T W^T (the transition: U = 0), as BF16 over
+                   // the first 32 columns of h^T W^T once those are read
+                    uint32_t w0[32], w1[32], vv[32];
                     tmem_ld32(tmem + lane + cA, w0);
                     tmem_ld32(tmem + lane + cA + 32, w1);
 #pragma unroll
@@ -347,12 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
 #pragma unroll
                         for (int i = 0; i < 32; ++i) u[i] -= __uint_as_float(hh ? w1[i] : w0[i]);
 #pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8)
-                            st_bf16x8(vn + sw128_off(row, 32 * hh + 8 * c8, 128), u + 8 * c8);
+                        for (int i = 0; i < 16; ++i) vv[16 * hh + i] = pack_bf16x2(u[2 * i], u[2 * i + 1]);
                     }
+                    tmem_st32(tmem + lane + cA, vv);
                 }
-                fence_async_smem();
-                tmem_wait_st();  // the scaled state, before the update product
+                tmem_wait_st();  // v_new and the scaled state, before the update product
                 tc_fence_before();
                 mbar_arrive(&bars[kPVready + path]);
                 if (!wait(kPHdone + path, gk)) { ok = false; break; }
