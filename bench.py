@@ -197,13 +197,18 @@ def counts(x, n_segments=1):
     else:
         lens = [x["T"]] * x["B"]
     chunks = sum((L + 63) // 64 for L in lens)
-    segs = 0
+    segs = groups = 0
+    S = max(1, n_segments)
+    G = 0 if S < 4 else int(S ** 0.5)  # the two-level composition's group size
     for L in lens:  # runs of ceil(chunks / S) whole chunks per sequence
         nc = (L + 63) // 64
-        per = -(-nc // max(1, n_segments)) if nc else 0
-        segs += -(-nc // per) if per else 0
+        per = -(-nc // S) if nc else 0
+        ns = -(-nc // per) if per else 0
+        segs += ns
+        groups += -(-ns // G) if G else 0
     return dict(tokens=sum(lens), token_heads=sum(lens) * H, chunk_heads=chunks * H,
-                seq_heads=len(lens) * H, n_seqs=len(lens), chunks=chunks, segments=segs * H)
+                seq_heads=len(lens) * H, n_seqs=len(lens), chunks=chunks, segments=segs * H,
+                groups=groups * H)
 
 
 REC_BYTES = 57616  # bytes of one record written by tc_prep and read by the scan (k aside)
@@ -227,8 +232,14 @@ def algorithmic_bytes(kernel, x, c):
         return th * ((2 * K + V) * es + 4 + V * es) + c["segments"] * K * V * 4
     if kernel == "compose_scalar":  # c_s, d_s read; h_s written; h0 / ht
         return c["segments"] * (2 * K * V * 4 + 4) + states
-    if kernel == "compose_delta":  # M_s, c_s read; h_s written; h0 / ht
+    if kernel in ("compose_delta", "tc_compose"):  # M_s, c_s read; h_s written; h0 / ht
         return c["segments"] * ((K * K if delta else 1) + 2 * K * V) * 4 + states
+    if kernel == "tc_compose_groups":  # M_s, c_s read; a group's transition and offset written
+        return c["segments"] * (K * K + K * V) * 4 + c["groups"] * (K * K + K * V) * 4
+    if kernel == "tc_compose_top":  # group transitions and offsets read; group states, h0 / ht
+        return c["groups"] * (K * K + 2 * K * V) * 4 + states
+    if kernel == "tc_compose_fill":  # M_s, c_s read; h_s written
+        return c["segments"] * (K * K + 2 * K * V) * 4
     rec = ch * REC_BYTES  # per-chunk records of the tensor-core prep kernel
     if kernel == "tc_prep":  # q, k, v, g, beta read; records written
         return th * ((2 * K + V) * es + 8) + rec
@@ -324,6 +335,7 @@ def bwd_algorithmic(kernel, x, c):
 
 # The translation unit each kernel is compiled from (plus every shared header).
 KERNEL_SOURCES = {"tc_prep": "tc_prep.cu", "tc_chain": "tc_chain.cu", "tc_gla": "tc_gla.cu",
+                  "tc_compose": "tc_compose.cu",
                   "tc_prescan": "tc_prescan.cu", "tc_bwd_scan": "tc_bwd_scan.cu",
                   "tc_bwd_grad": "tc_bwd_grad.cu", "recurrent": "recurrent.cu",
                   "compose": "compose.cu", "simt": "simt_path.cu", "bwd": "simt_bwd.cu"}

@@ -301,6 +301,9 @@ int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
         if (beta_free) pre = t_pre * pass((double)per, segs);
         else if (prescan_split_kinds(segs)) pre = t_pre * (double)per;
         else pre = 2.9 * pass((double)per, segs);
+        // the composition at its CUDA-core cost: a batch of many short
+        // sequences splits each of them too, and the tensor-core pass's
+        // lower cost there does not make up for the extra segment chains
         const double est = pre + t_out * pass((double)per, segs) + t_step * S;
         if (est < best) {
             best = est;
@@ -415,8 +418,45 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     L.off_segH = take(sizeof(float) * segs * K * V);
     L.off_segD = take(delta ? 0 : sizeof(float) * segs);
     L.off_rec = take(simt || !delta ? 0 : (size_t)mc * H * 74752u);  // paths 2 and 3
+    // the tensor-core composition's transition images, and the two-level
+    // form's group transitions and offsets (tensor-core paths, delta rule)
+    const ComposePlan cp = (!simt && delta && S > 1) ? compose_plan(d, S) : ComposePlan{0, 0, 0.0};
+    L.seg_images = cp.kind != 0;
+    L.off_segMimg = take(L.seg_images ? segs * 65536u : 0);
+    L.grp_size = cp.grp_size;
+    const size_t grps = L.grp_size ? (size_t)ns * H * (size_t)((S + L.grp_size - 1) / L.grp_size) : 0;
+    L.off_grpA = take(grps * 65536u);
+    L.off_grpD = take(sizeof(float) * grps * K * V);
     L.total = off;
     return L;
+}
+
+// Fitted to GB300 (microseconds): the CUDA-core composition costs t_step
+// per segment and wave of its CTAs (4, 8 or 16 value columns of one
+// (sequence, head) each); the tensor-core pass about 8 + 2.7 per segment and
+// wave of (sequence, head) runs; its two-level form about 8 per launch and
+// 2.9 per step of each level (G - 1, ceil(S / G), G - 1 steps).  Measured:
+// 64K tokens x 8 heads at S = 19: 51 / 59 / 57 (CUDA cores); 64K x 1 head at
+// S = 54: 92 / 143 / 77 (two levels); 16K x 16 heads at S = 9: 41 / 35
+// (single pass); a 16K-token sequence among 31 short ones x 4 heads at
+// S = 7: 155 / 35 (single pass).
+ComposePlan compose_plan(const gdr_dims &d, int S) {
+    const int64_t heads = n_seqs(d) * d.H, sms = device_sms();
+    auto waves = [&](int64_t n) { return (double)((n + sms - 1) / sms); };
+    const int64_t cc = heads * (d.V / 4) <= sms ? 4 : heads * (d.V / 8) <= sms ? 8 : 16;
+    ComposePlan c{0, 0, (cc == 4 ? 1.8 : cc == 8 ? 2.6 : 4.4) * waves(heads * (d.V / cc)) * S};
+    if (d.K != 128 || d.V != 128) return c;
+    const double one = 8.0 + 2.7 * S * waves(heads);
+    if (one < c.cost_us) c = ComposePlan{1, 0, one};
+    if (S >= 4) {
+        int G = 2;
+        while ((G + 1) * (G + 1) <= S) ++G;  // floor(sqrt(S))
+        const int64_t ng = (S + G - 1) / G;
+        const double two = 24.0 + 2.9 * ((G - 1) * waves(2 * heads * ng) + ng * waves(heads) +
+                                          (G - 1) * waves(heads * ng));
+        if (two < c.cost_us) c = ComposePlan{2, G, two};
+    }
+    return c;
 }
 
 Workspace carve_workspace(void *base, const WorkspaceLayout &L, int S) {
@@ -436,8 +476,12 @@ Workspace carve_workspace(void *base, const WorkspaceLayout &L, int S) {
     w.segH = reinterpret_cast<float *>(b + L.off_segH);
     w.segD = reinterpret_cast<float *>(b + L.off_segD);
     w.rec = reinterpret_cast<uint8_t *>(b + L.off_rec);
+    w.segMimg = L.seg_images ? reinterpret_cast<uint8_t *>(b + L.off_segMimg) : nullptr;
+    w.grpAimg = reinterpret_cast<uint8_t *>(b + L.off_grpA);
+    w.grpD = reinterpret_cast<float *>(b + L.off_grpD);
     w.max_chunks = L.max_chunks;
     w.n_segments = S;
+    w.grp_size = L.grp_size;
     return w;
 }
 
@@ -512,6 +556,22 @@ namespace {
         GDR_TRY((rec).end());                                          \
     } while (0)
 
+// The delta rule's segment composition on the tensor-core paths, as the
+// workspace was planned (compose_plan): on CUDA cores when the pre-scan left
+// no transition images, else the tensor-core pass or its two-level form.
+int run_compose_tc(const Problem &p, const Workspace &ws, cudaStream_t st, LaunchRecorder &rec) {
+    if (!ws.segMimg) {
+        GDR_LAUNCH(rec, kKCompose, compose_mt(p, ws, st));
+    } else if (ws.grp_size == 0) {
+        GDR_LAUNCH(rec, kKTcCompose, compose_tc(p, ws, 0, st));
+    } else {
+        GDR_LAUNCH(rec, kKTcComposeGroups, compose_tc(p, ws, 1, st));
+        GDR_LAUNCH(rec, kKTcComposeTop, compose_tc(p, ws, 2, st));
+        GDR_LAUNCH(rec, kKTcComposeFill, compose_tc(p, ws, 3, st));
+    }
+    return GDR_OK;
+}
+
 int run_simt(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStream_t st,
              LaunchRecorder &rec) {
     GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
@@ -553,7 +613,7 @@ int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStre
             GDR_LAUNCH(rec, kKTcPre, tc_chain(p, ws, 1, st));
         else
             GDR_LAUNCH(rec, kKTcPreDual, tc_prescan(p, ws, st));
-        GDR_LAUNCH(rec, kKCompose, compose_mt(p, ws, st));
+        if (int rc = run_compose_tc(p, ws, st, rec)) return rc;
         GDR_LAUNCH(rec, kKTcSegOut, tc_chain(p, ws, 2, st));
     }
     return GDR_OK;
@@ -584,7 +644,7 @@ int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs
                 GDR_LAUNCH(rec, kKTcPre, tc_chain(pf, ws, 1, st));
             else
                 GDR_LAUNCH(rec, kKTcPreDual, tc_prescan(pf, ws, st));
-            GDR_LAUNCH(rec, kKCompose, compose_mt(pf, ws, st));
+            if (int rc = run_compose_tc(pf, ws, st, rec)) return rc;
             GDR_LAUNCH(rec, kKTcSegRecompute, tc_chain(pf, ws, 4, st));
             GDR_LAUNCH(rec, kKBwdMaps, bwd_maps(p, ws, bw.segMb, st));
             GDR_LAUNCH(rec, kKTcBwdPre, tc_bwd_scan(p, ws, 1, nullptr, nullptr, a.dout, st));
@@ -593,7 +653,8 @@ int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs
             pr.ht = a.dh0;
             Workspace wr = ws;
             wr.segM = bw.segMb;
-            GDR_LAUNCH(rec, kKCompose, compose_mt(pr, wr, st));
+            wr.segMimg = nullptr;  // the reverse maps exist as FP32 rows only: CUDA cores
+            if (int rc = run_compose_tc(pr, wr, st, rec)) return rc;
             GDR_LAUNCH(rec, kKTcBwdSegOut, tc_bwd_scan(p, ws, 2, nullptr, nullptr, a.dout, st));
         }
         GDR_LAUNCH(rec, kKTcBwdGrad, tc_bwd_grad(p, ws, a, st));
@@ -640,6 +701,10 @@ const char *gdr_kernel_name(int id) {
     case kKScanSerial: return "simt_scan_serial";
     case kKScanPre: return "simt_scan_prescan";
     case kKCompose: return "compose_delta";
+    case kKTcCompose: return "tc_compose";
+    case kKTcComposeGroups: return "tc_compose_groups";
+    case kKTcComposeTop: return "tc_compose_top";
+    case kKTcComposeFill: return "tc_compose_fill";
     case kKScanSegOut: return "simt_scan_segment_out";
     case kKOutput: return "simt_output";
     case kKTcSerial: return "tc_chain_serial";

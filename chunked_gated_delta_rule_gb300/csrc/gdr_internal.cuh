@@ -151,13 +151,22 @@ struct Workspace {
     float *hpre;          // [max_chunks][H][K][V]: state before each chunk
     float *vnew;          // [max_chunks][H][64][V]   (delta mode)
     float *segM;          // [N][H][S][K][K] transition per segment (delta), transposed
+                          // (the tensor-core pre-scans write it for the backward only)
     float *segC;          // [N][H][S][K][V] local state per segment
     float *segH;          // [N][H][S][K][V] composed initial state per segment
     float *segD;          // [N][H][S] scalar transition (beta-free)
     uint8_t *rec;         // [max_chunks][H] per-chunk records of the
                           // tensor-core path (tc_chunk.cuh)
+    // Transitions as the tensor-core composition's B operands: per
+    // transition 64 KB, the BF16 hi image then the lo image (x = hi + lo) of
+    // its transposed FP32 rows [m][r], each row m 128-byte swizzled in two
+    // 64-column blocks of 16 KB (sw128_off(m, r, 128)).
+    uint8_t *segMimg;     // [N][H][S] the segment transitions (tensor-core pre-scans)
+    uint8_t *grpAimg;     // [N][H][ceil(S/G)] the group transitions (two-level composition)
+    float *grpD;          // [N][H][ceil(S/G)][K][V] group offsets
     int64_t max_chunks;
     int n_segments;       // S (1 = serial)
+    int grp_size;         // G, segments a group of the two-level composition (0: one level)
     int bwd_tc;           // the tensor-core backward's forward recompute: tc_prep
                           // also stores the T images, G and beta, the chain
                           // the h mirror and v_new images (bwd_lkimg)

@@ -12,9 +12,23 @@ namespace gdr {
 // Byte layout of the workspace for one problem.
 struct WorkspaceLayout {
     size_t off_tab, off_seq0, off_nchunks, off_order, off_G, off_W, off_U, off_hpre,
-        off_vnew, off_segM, off_segC, off_segH, off_segD, off_rec, total;
+        off_vnew, off_segM, off_segC, off_segH, off_segD, off_rec, off_segMimg, off_grpA, off_grpD,
+        total;
     int64_t max_chunks;
+    int grp_size;     // G of the two-level tensor-core composition (0: one level)
+    bool seg_images;  // transition images: the composition runs on the tensor cores
 };
+
+// How the delta rule's segment composition runs on the tensor-core paths:
+// kind 0 on CUDA cores (compose_mt), 1 the single ordered tensor-core pass,
+// 2 its two-level form with groups of grp_size segments; cost_us the
+// estimate of the cheapest (a model of GB300 timings, from the shape and
+// the device's SM count, never from a launch's grid).
+struct ComposePlan {
+    int kind, grp_size;
+    double cost_us;
+};
+ComposePlan compose_plan(const gdr_dims &d, int S);
 
 // path 1: CUDA-core path (chunk table, G, W, U, h_pre, v_new, segments);
 // path 2: tensor-core path (chunk table, records and segment summaries);
@@ -63,6 +77,10 @@ enum KernelId {
     kKTcSegRecompute = 28,
     kKTcBwdPre = 29,
     kKTcBwdSegOut = 30,
+    kKTcCompose = 31,
+    kKTcComposeGroups = 32,
+    kKTcComposeTop = 33,
+    kKTcComposeFill = 34,
     kKNumIds
 };
 
@@ -127,6 +145,12 @@ cudaError_t tc_bwd_grad(const Problem &p, const Workspace &ws, const BwdArgs &a,
 // bulk-copied transposed transitions, 32 value columns per CTA.
 bool compose_mt_supported(const Problem &p);
 cudaError_t compose_mt(const Problem &p, const Workspace &ws, cudaStream_t st);
+// Composition for the delta rule at K = V = 128 on the tensor cores
+// (tc_compose.cu): level 0 the single ordered pass over every segment; with
+// ws.grp_size = G > 0, level 1 the group transitions and offsets, level 2
+// the pass over the groups, level 3 the states inside every group.
+bool compose_tc_supported(const Problem &p);
+cudaError_t compose_tc(const Problem &p, const Workspace &ws, int level, cudaStream_t st);
 // A9 for the beta-free form (scalar transitions d_s).
 cudaError_t compose_scalar(const Problem &p, const Workspace &ws, cudaStream_t st);
 

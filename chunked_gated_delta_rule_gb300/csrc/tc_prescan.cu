@@ -365,13 +365,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
             for (int q = 0; q < 4; ++q) {
                 float hv[32];
                 tmem_load32f(tmem + lane + cS + 32 * q, hv);
-                if (path == 1) {  // M_s stored transposed: row `row`
-                    float4 *dst = reinterpret_cast<float4 *>(ws.segM + (seg_base * kD + row) * kD +
-                                                             32 * q);
+                if (path == 1) {  // M_s stored transposed: row `row`, as the
+                    // tensor-core composition's B images when it runs, FP32 rows for
+                    // the CUDA-core composition and the backward's maps
+                    if (ws.segMimg) {
+                        uint8_t *img = ws.segMimg + seg_base * 65536;
 #pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4)
-                        dst[k4] = make_float4(hv[4 * k4], hv[4 * k4 + 1], hv[4 * k4 + 2],
-                                              hv[4 * k4 + 3]);
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const uint32_t o = sw128_off(row, 32 * q + 8 * c8, 128);
+                            st_split_bf16x8(img + o, img + 32768 + o, hv + 8 * c8);
+                        }
+                    }
+                    if (ws.bwd_tc || !ws.segMimg) {
+                        float4 *dst = reinterpret_cast<float4 *>(ws.segM + (seg_base * kD + row) * kD +
+                                                                 32 * q);
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; ++k4)
+                            dst[k4] = make_float4(hv[4 * k4], hv[4 * k4 + 1], hv[4 * k4 + 2],
+                                                  hv[4 * k4 + 3]);
+                    }
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < 32; ++kk)
