@@ -182,15 +182,47 @@ def test_bit_identical_across_plans_and_repeats(S):
         assert torch.equal(_bits(ht), _bits(tc_h))
 
 
+@pytest.mark.parametrize("case", ["two_level_h0", "two_level_no_ht", "two_level_varlen",
+                                  "single_many_heads"])
+def test_tensor_core_composition(case):
+    """The segment composition on the tensor cores (FP32 operands carried as
+    BF16 hi + lo pairs): its two-level form (one head, 64 one-chunk segments
+    in groups of 8) from h0, the same without the final state (the last
+    group step is skipped), over sequences with different segment counts
+    (empty, one chunk, ragged, a partial last group); its single ordered pass
+    at 16 heads.  Element by element against the FP64 oracle."""
+    if case == "single_many_heads":
+        w = synthetic.small(W["long_16k_bf16"], T=1024, H=16, with_h0=True)
+        x, S = synthetic.make_inputs(w), 9
+    elif case == "two_level_varlen":
+        w = synthetic.small(W["wide_varlen_bf16"], H=1, with_h0=True)
+        x, S = synthetic.make_inputs(w, lengths=[4096, 0, 64, 1000, 3000]), 64
+    else:
+        w = synthetic.small(W["long_16k_bf16"], T=4096, H=1, with_h0=True)
+        x, S = synthetic.make_inputs(w), 64
+    if case != "two_level_no_ht":
+        check(x, n_segments=S, force_path=2)
+        return
+    o0, _ = poisoned_outputs(x)
+    o, ht = run_gpu(x, o=o0, n_segments=S, force_path=2, output_final_state=False)
+    assert ht is None and torch.isfinite(o.float()).all()
+    ro, _ = run_oracle(x)
+    assert rel_l2_masked(o, ro) <= tol_of(x)
+
+
 @pytest.mark.parametrize("case", ["delta_serial", "delta_split_chains", "delta_split_dual",
-                                  "beta_free_split", "beta_free_k256"])
+                                  "delta_two_level", "beta_free_split", "beta_free_k256"])
 def test_tensor_core_bits_identical_across_grids(case):
     """Bit-identical across launch configurations: the persistent
-    tensor-core kernels (preparation, scan, both pre-scans, the beta-free
-    scan) with 1, 5 and 37 CTAs give the bits of their one-CTA-per-SM grids
+    tensor-core kernels (preparation, scan, both pre-scans, the composition
+    in one and two levels, the beta-free scan) with 1, 5 and 37 CTAs give the
+    bits of their one-CTA-per-SM grids
     (every chain and chunk is computed by one CTA in a fixed order whichever
     CTA pulls it)."""
-    if case.startswith("delta"):
+    if case == "delta_two_level":  # the two-level tensor-core composition
+        w = synthetic.small(W["long_16k_bf16"], T=4096, H=1, with_h0=True)
+        lens, S = None, 64
+    elif case.startswith("delta"):
         w = synthetic.small(W["wide_varlen_bf16"], H=4)
         lens = [1000, 700, 64, 0, 333] if case != "delta_serial" else RAGGED
         S = {"delta_serial": 1, "delta_split_chains": 2, "delta_split_dual": 8}[case]
