@@ -433,27 +433,27 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
 
 // Fitted to GB300 (microseconds): the CUDA-core composition costs t_step
 // per segment and wave of its CTAs (4, 8 or 16 value columns of one
-// (sequence, head) each); the tensor-core pass about 8 + 2.7 per segment and
-// wave of (sequence, head) runs; its two-level form about 8 per launch and
-// 2.9 per step of each level (G - 1, ceil(S / G), G - 1 steps).  Measured:
-// 64K tokens x 8 heads at S = 19: 51 / 59 / 57 (CUDA cores); 64K x 1 head at
-// S = 54: 92 / 143 / 77 (two levels); 16K x 16 heads at S = 9: 41 / 35
-// (single pass); a 16K-token sequence among 31 short ones x 4 heads at
-// S = 7: 155 / 35 (single pass).
+// (sequence, head) each); the tensor-core pass about 11.6 + 1.87 per segment
+// and wave of (sequence, head) runs; its two-level form about 33.5 for its
+// three launches and 1.59 per step of each level (G - 1, ceil(S / G),
+// G - 1 steps, in waves of their runs).  Measured, CUDA cores / single pass
+// / two levels: 64K tokens x 8 heads at S = 19: 51 / 47 / 51; 64K x 1 head
+// at S = 54: 92 / 113 / 65; 16K x 16 heads at S = 9: 41 / 29 / 45; a
+// 16K-token sequence among 31 short ones x 4 heads at S = 7: 154 / 33 / 107.
 ComposePlan compose_plan(const gdr_dims &d, int S) {
     const int64_t heads = n_seqs(d) * d.H, sms = device_sms();
     auto waves = [&](int64_t n) { return (double)((n + sms - 1) / sms); };
     const int64_t cc = heads * (d.V / 4) <= sms ? 4 : heads * (d.V / 8) <= sms ? 8 : 16;
     ComposePlan c{0, 0, (cc == 4 ? 1.8 : cc == 8 ? 2.6 : 4.4) * waves(heads * (d.V / cc)) * S};
     if (d.K != 128 || d.V != 128) return c;
-    const double one = 8.0 + 2.7 * S * waves(heads);
+    const double one = 11.6 + 1.87 * S * waves(heads);
     if (one < c.cost_us) c = ComposePlan{1, 0, one};
     if (S >= 4) {
         int G = 2;
         while ((G + 1) * (G + 1) <= S) ++G;  // floor(sqrt(S))
         const int64_t ng = (S + G - 1) / G;
-        const double two = 24.0 + 2.9 * ((G - 1) * waves(2 * heads * ng) + ng * waves(heads) +
-                                          (G - 1) * waves(heads * ng));
+        const double two = 33.5 + 1.59 * ((G - 1) * waves(2 * heads * ng) + ng * waves(heads) +
+                                           (G - 1) * waves(heads * ng));
         if (two < c.cost_us) c = ComposePlan{2, G, two};
     }
     return c;

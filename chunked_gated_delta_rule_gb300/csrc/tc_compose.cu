@@ -16,7 +16,8 @@
 // relative 2^-16 of the product) dropped.  X^T's hi and lo parts are the A
 // operands, in TMEM; M_s's B images (hi and lo, MN-major, 128-byte swizzled:
 // the pre-scan writes them beside its FP32 summaries) are bulk-copied into
-// shared memory one step ahead, and c_s is staged there by bulk copy.
+// shared memory one step ahead, and c_s is read into the next-but-one D
+// buffer (three of them) while a step runs.
 //
 // Two-level form (a composition of S segments in about 2 sqrt(S) ordered
 // steps): level 1 forms, for every group of G consecutive segments in
@@ -27,10 +28,11 @@
 // 0 is the single ordered pass over all segments.  Every product has one
 // fixed order, whatever the grid.
 //
-// Warps: 0 issues the MMAs; 1 bulk-loads the B images and c_s; 2-9 (twice
-// the four TMEM lane quarters, half the keys each) read D, write the states
-// and form the next X^T hi / lo; 10-13 preload the next D buffer with c_s^T
-// (or zeros).
+// Warps: 0 issues the MMAs; 1 bulk-loads the B images; 2-9 (twice the four
+// TMEM lane quarters, half the keys each) read D, form the next X^T hi / lo
+// (keys 0-63 first: the next step's first four K-steps start on them while
+// keys 64-127 are formed) and write the states; 10-17 (likewise) preload the
+// D buffer two steps ahead with c_s^T (or zeros), from memory.
 // Each CTA walks runs blockIdx.x, blockIdx.x + gridDim.x, ...; every role
 // counts the same steps, so buffers and barrier phases follow one global
 // step counter.  Every wait is time-bounded: on expiry the CTA records
@@ -43,34 +45,32 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 576;
 constexpr int kCD = 128;  // K = V
+constexpr int kND = 3;    // D buffers: the offsets are read two steps ahead
 
-// Shared memory (1024-aligned base): the staging of c_s (64 KB), two
-// buffers of the hi and lo B images, barriers.
-constexpr uint32_t kOffMf = 0;                     // 64 KB
-constexpr uint32_t kOffImg = 65536;                // [2] x (hi 32 KB, lo 32 KB)
+// Shared memory (1024-aligned base): two buffers of the hi and lo B images,
+// barriers.
+constexpr uint32_t kOffImg = 0;                    // [2] x (hi 32 KB, lo 32 KB)
 constexpr uint32_t kImgLo = 32768;
 constexpr uint32_t kOffBar = kOffImg + 2 * 65536;
 enum : int {
-    kBMfull = 0,    // c_s staged (bulk-copy bytes)
-    kBMfree = 1,    // staging read (D-preload warps, 128)
-    kBIready = 2,   // [2] B images landed (bulk-copy bytes)
-    kBIfree = 4,    // [2] B images read (commit)
-    kBCready = 6,   // [2] D preloaded (c warps, 128)
-    kBDdone = 8,    // [2] step's products done (commit)
-    kBDfree = 10,   // [2] D read (state warps, 128)
-    kBXready = 12,  // X^T hi / lo written (state warps, 128)
-    kBDrain = 13,   // every issued MMA done (commit, at the end)
-    kNumBars = 14
+    kBIready = 0,   // [2] B images landed (bulk-copy bytes)
+    kBIfree = 2,    // [2] B images read (commit)
+    kBCready = 4,   // [3] D preloaded with c_s^T (c warps, 256)
+    kBDdone = 7,    // [3] step's products done (commit)
+    kBDfree = 10,   // [3] D read (state warps, 256)
+    kBXready = 13,  // [2] X^T hi / lo of keys 0-63, then 64-127, written (state warps, 256)
+    kBDrain = 15,   // every issued MMA done (commit, at the end)
+    kNumBars = 16
 };
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;  // TMEM base, abort flag
 constexpr uint32_t kSmemLaunch = kOffMisc + 16 + 1024;
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD = 0;     // [2] D, FP32, 128 columns each
-constexpr uint32_t kColXh = 256;  // X^T hi, two BF16 a column
-constexpr uint32_t kColXl = 320;  // X^T lo
+constexpr uint32_t kColD = 0;     // [3] D, FP32, 128 columns each
+constexpr uint32_t kColXh = 384;  // X^T hi, two BF16 a column
+constexpr uint32_t kColXl = 448;  // X^T lo
 // D[c][r] += sum_m A[c][m] B[r][m]: A = X^T (K-major, TMEM), B = M with
 // B[r][m] at row m of the image (MN-major: r contiguous)
 constexpr uint32_t kIdesc = idesc_bf16(128, 128, 0, 1);
@@ -232,11 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
     }
     if (tid == 0) {
         for (int b = 0; b < kNumBars; ++b) {
-            uint32_t cnt = 128;
-            if (b == kBMfull || b == kBIready || b == kBIready + 1 || b == kBIfree ||
-                b == kBIfree + 1 || b == kBDdone || b == kBDdone + 1 || b == kBDrain)
-                cnt = 1;
-            if (b == kBDfree || b == kBDfree + 1 || b == kBXready) cnt = 256;
+            // bulk-copy bytes and commits: one arrival; warp groups: 256
+            const bool one = (b >= kBIready && b < kBCready) || (b >= kBDdone && b < kBDfree) ||
+                              b == kBDrain;
+            const uint32_t cnt = one ? 1u : 256u;
             mbar_init(&bars[b], cnt);
         }
         *s_abort = 0;
@@ -252,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
     if (warp == 1) {
         // ------------------------------------------------------------ loads
         if (lane_id == 0) {
-            uint32_t g = 0, gc = 0;  // steps; steps with an offset (staged c_s)
+            uint32_t g = 0;
             bool ok = true;
             for (int64_t r = blockIdx.x; ok && r < runs; r += gridDim.x) {
                 const Run u = decode(p, ws, level, r);
@@ -266,16 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
                     for (int i = 0; i < 8; ++i)
                         bulk_load(sm + kOffImg + 65536 * b + 8192 * i, src + 8192 * i, 8192u,
                                   &bars[kBIready + b]);
-                    // then c_s into the staging, once the previous one is read
-                    const uint8_t *c = reinterpret_cast<const uint8_t *>(offset_of(ws, level, u, j));
-                    if (c) {
-                        if (gc >= 1 && !wait_ahead(kBMfree, gc - 1)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&bars[kBMfull], 65536u);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            bulk_load(sm + kOffMf + 8192 * i, c + 8192 * i, 8192u, &bars[kBMfull]);
-                        ++gc;
-                    }
                 }
             }
         }
@@ -288,26 +277,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
             for (int64_t r = blockIdx.x; ok && r < runs; r += gridDim.x) {
                 const Run u = decode(p, ws, level, r);
                 for (int j = 0; j < u.nsteps; ++j, ++g) {
-                    const uint32_t b = g & 1;
-                    if (!wait(kBIready + b, g >> 1) || !wait(kBCready + b, g >> 1) ||
-                        !wait(kBXready, g)) {
+                    const uint32_t b = g & 1, bd = g % kND;
+                    if (!wait(kBIready + b, g >> 1) || !wait(kBCready + bd, g / kND)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t d = tmem + kColD + 128 * b;
+                    const uint32_t d = tmem + kColD + 128 * bd;
                     const uint32_t img = sb + kOffImg + 65536 * b;
-                    // small terms first: Xl Mh^T, Xh Ml^T, then Xh Mh^T
+                    // keys 0-63 as soon as X's first half is written, while the
+                    // state warps form the second; per half, the small terms
+                    // first: Xl Mh^T, Xh Ml^T, then Xh Mh^T
 #pragma unroll
-                    for (int t = 0; t < 3; ++t) {
-                        const uint32_t a = tmem + (t == 0 ? kColXl : kColXh);
-                        const uint32_t bi = img + (t == 1 ? kImgLo : 0u);
+                    for (int hk = 0; hk < 2; ++hk) {
+                        if (!wait(kBXready + hk, g)) break;
+                        tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            umma_bf16_ts(d, a + 8 * kk, sdesc_sw128(bi + kk * 2048, 16384, 1024),
-                                         kIdesc, 1u);
+                        for (int t = 0; t < 3; ++t) {
+                            const uint32_t a = tmem + (t == 0 ? kColXl : kColXh);
+                            const uint32_t bi = img + (t == 1 ? kImgLo : 0u);
+#pragma unroll
+                            for (int kk = 4 * hk; kk < 4 * hk + 4; ++kk)
+                                umma_bf16_ts(d, a + 8 * kk, sdesc_sw128(bi + kk * 2048, 16384, 1024),
+                                             kIdesc, 1u);
+                        }
                     }
-                    umma_commit(&bars[kBDdone + b]);
+                    if (*s_abort) {
+                        ok = false;
+                        break;
+                    }
+                    umma_commit(&bars[kBDdone + bd]);
                     umma_commit(&bars[kBIfree + b]);
                 }
             }
@@ -318,54 +316,49 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
         __syncwarp();
     } else if (warp >= 10) {
         // ------------------------------------------------------------ D preload
-        uint32_t g = 0, gc = 0;
+        // Warps 10-17: D^T row `row` = column `row` of c_s, keys [64 ch,
+        // 64 ch + 64), read from memory (coalesced: a warp's loads of one key
+        // cover 32 consecutive columns) into D two steps ahead.
+        const int ch = (warp - 10) >> 2;
+        uint32_t g = 0;
         bool ok = true;
         for (int64_t r = blockIdx.x; ok && r < runs; r += gridDim.x) {
             const Run u = decode(p, ws, level, r);
             for (int j = 0; j < u.nsteps; ++j, ++g) {
-                const uint32_t b = g & 1;
-                const bool got = g < 2 || wait_ahead(kBDfree + b, (g >> 1) - 1);
+                const uint32_t bd = g % kND;
+                const bool got = g < (uint32_t)kND || wait_ahead(kBDfree + bd, g / kND - 1);
                 if (!__all_sync(0xffffffffu, got ? 1 : 0)) {
                     ok = false;
                     break;
                 }
                 const float *c = offset_of(ws, level, u, j);
-                // c_s from the staging
-                const bool staged = c != nullptr;
-                if (staged && !__all_sync(0xffffffffu, wait_ahead(kBMfull, gc) ? 1 : 0)) {
-                    ok = false;
-                    break;
-                }
-                // D^T row `row` = column `row` of c_s, 32 rows r at a time
 #pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
+                    const int r0 = 64 * ch + 32 * q;
                     uint32_t v[32];
-                    if (staged) {
-                        const float *src = reinterpret_cast<const float *>(sm + kOffMf) + 32 * q * kCD + row;
+                    if (c) {
+                        const float *src = c + (int64_t)r0 * kCD + row;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(src[i * kCD]);
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__ldg(src + i * kCD));
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0u;
                     }
-                    tmem_st32(tmem + lane + kColD + 128 * b + 32 * q, v);
-                }
-                if (staged) {  // the staging is read (its values are in registers)
-                    mbar_arrive(&bars[kBMfree]);
-                    ++gc;
+                    tmem_st32(tmem + lane + kColD + 128 * bd + r0, v);
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&bars[kBCready + b]);
+                mbar_arrive(&bars[kBCready + bd]);
             }
         }
     } else {
         // ------------------------------------------------------------ states
         // Warps 2-9: thread `row` of a lane quarter holds column c = row of
-        // X, keys r in [64 eh, 64 eh + 64).
+        // X, keys r in [32 eh, 32 eh + 32) and [64 + 32 eh, 96 + 32 eh): the
+        // two groups of four warps together write keys 0-63 first.
         const int c = row;
         const int eh = (warp - 2) >> 2;
-        const int rb = 64 * eh;
+        auto rq = [&](int q) { return 64 * q + 32 * eh; };
         uint32_t g = 0;
         bool ok = true;
         // X^T row c (32 keys r0 .. r0 + 31) into the A operands
@@ -420,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
             // first transition or offset (1)
 #pragma unroll 1
             for (int q = 0; q < 2; ++q) {
-                const int r0 = rb + 32 * q;
+                const int r0 = rq(q);
                 float x[32];
                 if (level == 0 || level == 2) {
 #pragma unroll
@@ -449,15 +442,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
                 // segH of the first segment (levels 0, 2), ht of a sequence
                 // without tokens, a one-segment group's result (level 1)
                 put_out(-1, r0, x);
-                if (u.nsteps > 0) put_x(r0, x);
+                if (u.nsteps > 0) {
+                    put_x(r0, x);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bars[kBXready + q]);
+                }
             }
             if (u.nsteps == 0) continue;
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bars[kBXready]);
             for (int j = 0; j < u.nsteps; ++j, ++g) {
-                const uint32_t b = g & 1;
-                if (!__all_sync(0xffffffffu, wait(kBDdone + b, g >> 1) ? 1 : 0)) {
+                const uint32_t bd = g % kND;
+                if (!__all_sync(0xffffffffu, wait(kBDdone + bd, g / kND) ? 1 : 0)) {
                     ok = false;
                     break;
                 }
@@ -467,23 +462,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
                 // next step's products run
                 if (j + 1 < u.nsteps) {
 #pragma unroll 1
-                    for (int q = 0; q < 2; ++q) {
+                    for (int q = 0; q < 2; ++q) {  // keys 0-63, then 64-127
                         float x[32];
-                        tmem_load32f(tmem + lane + kColD + 128 * b + rb + 32 * q, x);
-                        put_x(rb + 32 * q, x);
+                        tmem_load32f(tmem + lane + kColD + 128 * bd + rq(q), x);
+                        put_x(rq(q), x);
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(&bars[kBXready + q]);
                     }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(&bars[kBXready]);
                 }
 #pragma unroll 1
                 for (int q = 0; q < 2; ++q) {
                     float x[32];
-                    tmem_load32f(tmem + lane + kColD + 128 * b + rb + 32 * q, x);
-                    put_out(j, rb + 32 * q, x);
+                    tmem_load32f(tmem + lane + kColD + 128 * bd + rq(q), x);
+                    put_out(j, rq(q), x);
                 }
                 tc_fence_before();
-                mbar_arrive(&bars[kBDfree + b]);
+                mbar_arrive(&bars[kBDfree + bd]);
             }
         }
     }
