@@ -480,10 +480,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                         tmem_load32f(tmem + lane + L::kColD + 32 * hh, f);
                         const int j0 = 32 * hh;
                         if (fact) {
+                            // the 32 column factors as eight 16-byte shared-memory reads
                             const float ri = sEP[i];
+                            float dj[32];
+#pragma unroll
+                            for (int v4 = 0; v4 < 8; ++v4) {
+                                const float4 t4 = *reinterpret_cast<const float4 *>(sDec + j0 + 4 * v4);
+                                dj[4 * v4] = t4.x;
+                                dj[4 * v4 + 1] = t4.y;
+                                dj[4 * v4 + 2] = t4.z;
+                                dj[4 * v4 + 3] = t4.w;
+                            }
 #pragma unroll
                             for (int u = 0; u < 32; ++u)
-                                f[u] = (j0 + u <= i && j0 + u < len) ? f[u] * (ri * sDec[j0 + u]) : 0.f;
+                                f[u] = (j0 + u <= i && j0 + u < len) ? f[u] * (ri * dj[u]) : 0.f;
                         } else {
                             const float gi = sG[i];
 #pragma unroll
