@@ -31,7 +31,7 @@ class gdr_dims(ctypes.Structure):
 
 class gdr_plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("bv", ctypes.c_int32),
-                ("n_segments", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("n_segments", ctypes.c_int32), ("compose", ctypes.c_int32)]
 
 
 class gdr_options(ctypes.Structure):
@@ -490,7 +490,7 @@ def gdr_plan_query(B, T, H, K, V, N=0, dtype=GDR_BF16, beta_free=False, n_segmen
                                        int(bool(beta_free)), int(n_segments), ctypes.byref(plan))
     if rc != 0:
         raise GdrError(rc)
-    return dict(path=plan.path, bv=plan.bv, n_segments=plan.n_segments)
+    return dict(path=plan.path, bv=plan.bv, n_segments=plan.n_segments, compose=plan.compose)
 
 
 def gdr_selftest_umma(A, B, a_mn, b_mn, status=None):

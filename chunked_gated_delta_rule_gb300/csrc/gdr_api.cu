@@ -325,6 +325,14 @@ bool tc_shape(const gdr_dims &d, bool beta_free) {
     return d.dtype == GDR_BF16 && tc_shape_any_dtype(d, beta_free);
 }
 
+// gdr_plan::compose: 0 for the CUDA-core composition (or none), 1 for the
+// tensor-core pass, G >= 2 for its two-level form in groups of G segments.
+int compose_of(const gdr_dims &d, bool beta_free, int path, int S) {
+    if (path != 2 || beta_free || S <= 1) return 0;
+    const ComposePlan c = compose_plan(d, S);
+    return c.kind == 0 ? 0 : c.kind == 1 ? 1 : c.grp_size;
+}
+
 int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_options *opt,
               gdr_plan *plan) {
     gdr_plan p{};
@@ -350,6 +358,7 @@ int make_plan(const gdr_dims &d, bool beta_free, int n_segments, const gdr_optio
     if (n_segments > (beta_free ? kMaxSegmentsBetaFree : kMaxSegments))
         return GDR_ERR_UNSUPPORTED;
     p.n_segments = n_segments == 0 ? auto_segments(d, beta_free, p.path, p.bv) : n_segments;
+    p.compose = compose_of(d, beta_free, p.path, p.n_segments);
     *plan = p;
     return GDR_OK;
 }
@@ -383,6 +392,7 @@ int plan_for_call(const gdr_dims &d, bool beta_free, int n_segments, const gdr_o
         p.path = 1;
         p.bv = pick_bv(d);
         if (n_segments == 0) p.n_segments = auto_segments(d, beta_free, 1, p.bv);
+        p.compose = 0;
     }
     *plan = p;
     if (ws_bytes) *ws_bytes = workspace_layout(d, beta_free, p.n_segments, p.path).total;

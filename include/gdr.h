@@ -135,7 +135,10 @@ typedef struct gdr_plan {
     int32_t path;       /* 1 = CUDA-core FP32 path, 2 = tensor-core path    */
     int32_t bv;         /* value columns per scan CTA                      */
     int32_t n_segments; /* 1 = serial scan, S > 1 = segment split           */
-    int32_t reserved;
+    int32_t compose;    /* the split's ordered composition (delta rule):
+                           0 on CUDA cores (or no split), 1 one pass on the
+                           tensor cores, G >= 2 the tensor cores' two-level
+                           form in groups of G segments                     */
 } gdr_plan;
 
 /* Options of gdr_chunk_fwd_ex.  Zero-initialise, then set what you need. */

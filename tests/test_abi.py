@@ -181,6 +181,23 @@ def test_plan_query_is_deterministic_and_valid():
         assert pkg.gdr_plan_query(B, T, H, K, V, beta_free=bf)["n_segments"] == s
 
 
+def test_plan_reports_the_composition():
+    """The segment split's ordered composition as the plan reports it (the
+    cost model of GB300 timings, 152 SMs): the tensor cores' single pass for
+    the 64K x 8-head and 16K x 16-head splits, their two-level form in groups
+    of 7 for one 64K-token head at 54 segments, the CUDA-core pass for one
+    head at 4 segments; none without a split, on the CUDA-core path, or in
+    the beta-free mode (its composition is element-wise)."""
+    q = pkg.gdr_plan_query
+    assert q(1, 65536, 8, 128, 128)["compose"] == 1
+    assert q(1, 65536, 1, 128, 128)["compose"] == 7
+    assert q(1, 16384, 16, 128, 128)["compose"] == 1
+    assert q(1, 16384, 1, 128, 128, n_segments=4)["compose"] == 0
+    assert q(1, 10456, 16, 128, 128, N=32)["compose"] == 0
+    assert q(2, 8192, 4, 256, 512, beta_free=True)["compose"] == 0
+    assert q(1, 4096, 2, 64, 64, dtype=0, n_segments=4)["compose"] == 0
+
+
 def test_plan_keys_on_the_longest_sequence():
     """Varlen plans read the longest sequence from the max_len hint
     (cu_seqlens is device data): at 4 heads one 16K-token sequence among 31
@@ -212,11 +229,11 @@ def test_cuda_core_plan_rules():
     measurements behind each rule are stated beside pick_bv and
     auto_segments)."""
     q = lambda *a, **k: pkg.gdr_plan_query(*a, dtype=0, **k)
-    assert q(1, 256, 2, 64, 64) == {"path": 1, "bv": 16, "n_segments": 1}
-    assert q(1, 10456, 16, 128, 128, N=32) == {"path": 1, "bv": 32, "n_segments": 1}
-    assert q(1, 16384, 16, 128, 128) == {"path": 1, "bv": 32, "n_segments": 8}
-    assert q(1, 65536, 1, 128, 128) == {"path": 1, "bv": 32, "n_segments": 64}
-    assert q(2, 8192, 4, 256, 512, beta_free=True) == {"path": 1, "bv": 32, "n_segments": 4}
+    assert q(1, 256, 2, 64, 64) == {"path": 1, "bv": 16, "n_segments": 1, "compose": 0}
+    assert q(1, 10456, 16, 128, 128, N=32) == {"path": 1, "bv": 32, "n_segments": 1, "compose": 0}
+    assert q(1, 16384, 16, 128, 128) == {"path": 1, "bv": 32, "n_segments": 8, "compose": 0}
+    assert q(1, 65536, 1, 128, 128) == {"path": 1, "bv": 32, "n_segments": 64, "compose": 0}
+    assert q(2, 8192, 4, 256, 512, beta_free=True) == {"path": 1, "bv": 32, "n_segments": 4, "compose": 0}
 
 
 def test_fp16_inputs_plan_the_cuda_core_path():
