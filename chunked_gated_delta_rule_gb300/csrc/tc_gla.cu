@@ -442,7 +442,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                 const int len = rem < kChunk ? (int)rem : kChunk;
                 if (!wait(kGFull + b, gk >> 1)) { ok = false; break; }
                 // (e^{G_last - G} V) in V's layout; rows past the sequence end
-                // (they belong to the next one) become zero
+                // (they belong to the next one) become zero.  Every read is
+                // issued before the first write (the compiler cannot reorder
+                // shared-memory reads past writes it cannot tell apart).
+                uint4 raw[8];
+                float dv[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int idx = tb + 128 * r;
+                    const int t = (idx >> 3) & 63;
+                    const uint32_t off = (idx >> 9) * 8192 + t * 128 + (idx & 7) * 16;
+                    raw[r] = *reinterpret_cast<const uint4 *>(st + L::kStV + off);
+                    dv[r] = t < len ? sDec[t] : 0.f;
+                }
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int idx = tb + 128 * r;
@@ -450,10 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                     const uint32_t off = (idx >> 9) * 8192 + t * 128 + (idx & 7) * 16;
                     if (t < len) {
                         float x[8];
-                        ld_bf16x8(st + L::kStV + off, x);
-                        const float d = sDec[t];
+                        ld_bf16x8(&raw[r], x);
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) x[u] *= d;
+                        for (int u = 0; u < 8; ++u) x[u] *= dv[r];
                         st_bf16x8(sm + L::kOffVd + off, x);
                     } else {
                         st_shared_v4(sm + L::kOffVd + off, 0u, 0u, 0u, 0u);
@@ -474,10 +485,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                 if (q4 >= 2) {
                     const int i = row - 64;
                     const bool fact = vec[386] != 0.f;
+                    // row i of Q K^T (both halves) in one TMEM wait
+                    uint32_t d0[32], d1[32];
+                    tmem_ld32(tmem + lane + L::kColD, d0);
+                    tmem_ld32(tmem + lane + L::kColD + 32, d1);
+                    tmem_wait_ld();
+                    reg_fence(d0);
+                    reg_fence(d1);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         float f[32];
-                        tmem_load32f(tmem + lane + L::kColD + 32 * hh, f);
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) f[u] = __uint_as_float(hh ? d1[u] : d0[u]);
                         const int j0 = 32 * hh;
                         if (fact) {
                             // the 32 column factors as eight 16-byte shared-memory reads
