@@ -190,25 +190,43 @@ def gpu_index_for_smi():
 # algorithmic bytes per kernel launch (units: token-heads, chunk-heads,
 # sequence-heads, segment summaries)
 # ----------------------------------------------------------------------------
-def counts(x, n_segments=1):
+def counts(x, n_segments=1, common=False):
+    """Units of one call.  common: one segment length for every sequence,
+    ceil(longest / S) chunks (the tensor-core delta forward), a sequence no
+    longer than it left whole; else ceil(own chunks / S) per sequence."""
     H = x["H"]
     if x["cu_seqlens"] is not None:
         lens = (x["cu_seqlens"][1:] - x["cu_seqlens"][:-1]).tolist()
     else:
         lens = [x["T"]] * x["B"]
     chunks = sum((L + 63) // 64 for L in lens)
-    segs = groups = 0
+    segs = groups = split_tokens = split_chunks = 0
     S = max(1, n_segments)
     G = 0 if S < 4 else int(S ** 0.5)  # the two-level composition's group size
-    for L in lens:  # runs of ceil(chunks / S) whole chunks per sequence
+    longest = max([(L + 63) // 64 for L in lens] + [0])
+    for L in lens:  # runs of whole chunks per sequence
         nc = (L + 63) // 64
-        per = -(-nc // S) if nc else 0
-        ns = -(-nc // per) if per else 0
+        if common:
+            per = -(-longest // S)
+            ns = 0 if S == 1 or nc <= per else -(-nc // per)
+        else:
+            per = -(-nc // S) if nc else 0
+            ns = -(-nc // per) if per else 0
         segs += ns
         groups += -(-ns // G) if G else 0
+        if ns:
+            split_tokens += L
+            split_chunks += nc
     return dict(tokens=sum(lens), token_heads=sum(lens) * H, chunk_heads=chunks * H,
                 seq_heads=len(lens) * H, n_seqs=len(lens), chunks=chunks, segments=segs * H,
-                groups=groups * H)
+                groups=groups * H, split_token_heads=split_tokens * H,
+                split_chunk_heads=split_chunks * H)
+
+
+def common_segments(x, plan):
+    """The plan cuts sequences at one common segment length (the tensor-core
+    delta forward)."""
+    return plan.get("path") == 2 and x["beta"] is not None
 
 
 REC_BYTES = 57616  # bytes of one record written by tc_prep and read by the scan (k aside)
@@ -244,8 +262,9 @@ def algorithmic_bytes(kernel, x, c):
     if kernel == "tc_prep":  # q, k, v, g, beta read; records written
         return th * ((2 * K + V) * es + 8) + rec
     if kernel in ("tc_chain_prescan", "tc_prescan_dual"):
-        # W, U^T, decay of the records and k (once); c_s, M_s
-        return th * K * es + ch * (2 * 16384 + 272) + c["segments"] * K * (K + V) * 4
+        # W, U^T, decay of the split sequences' records and k (once); c_s, M_s
+        return (c["split_token_heads"] * K * es + c["split_chunk_heads"] * (2 * 16384 + 272)
+                + c["segments"] * K * (K + V) * 4)
     if kernel == "tc_chain_segment_out":  # records and k read, o written, h_s read
         return th * (K + V) * es + rec + c["segments"] * K * V * 4
     if kernel == "simt_prep":
@@ -700,7 +719,7 @@ def config_record(pkg, name, dev, steps, flush, hbm):
     from chunked_gated_delta_rule_gb300 import synthetic
     x = synthetic.make_inputs(synthetic.WORKLOADS[name])
     plan = plan_of(pkg, x)
-    c = counts(x, plan["n_segments"])
+    c = counts(x, plan["n_segments"], common_segments(x, plan))
     m = Measured(pkg, x, dev, steps, 3, flush)
     rec = {"plan": plan, "tokens": c["tokens"], "ms_per_call": m.ms,
            "tokens_per_s": c["tokens"] / (m.ms * 1e-3),
@@ -817,7 +836,7 @@ def run_gdr(args):
         seg_count = args.segments or 1
         plan = {"path": args.force_path, "bv": "per the forced path's rule",
                 "n_segments": args.segments or "per the forced path's rule"}
-    c = counts(x, seg_count)
+    c = counts(x, seg_count, common_segments(x, plan))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     peaks = load_peaks()

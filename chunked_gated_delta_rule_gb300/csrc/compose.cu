@@ -11,6 +11,7 @@
 // partial sums are added in a fixed order, so every output element has one
 // fixed summation order.
 #include "gdr_internal.cuh"
+#include "gdr_segments.cuh"
 #include "tc_common.cuh"
 
 namespace gdr {
@@ -45,8 +46,11 @@ __global__ void __launch_bounds__(kComposeThreads, 1) k_compose_mt(Problem p, Wo
     pdl_wait();
 
     const int nc = ws.seq_chunk0[n + 1] - ws.seq_chunk0[n];
-    const int per = (nc + S - 1) / S;
+    const int per = seg_per(ws, nc);
     const int nseg = per ? (nc + per - 1) / per : 0;
+    // at most one segment under the common length: the output pass runs it
+    // whole, from h0 to ht
+    if (seg_len(ws) && nseg <= 1) return;
     const int64_t sbase = (n * H + h) * (int64_t)S;
     for (int idx = tid; idx < K * CC; idx += kComposeThreads) {
         const int key = idx / CC, c = idx - key * CC;

@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "gdr_internal.cuh"
+#include "gdr_segments.cuh"
 #include "gdr_launch.cuh"
 
 namespace gdr {
@@ -257,6 +258,19 @@ int pick_bv(const gdr_dims &d) {
 // their two summaries as its own chain while all of them fit one wave.
 bool prescan_split_kinds(int64_t segs) { return 2 * segs <= device_sms(); }
 
+}  // namespace
+
+int64_t split_seqs(const gdr_dims &d, int S) {
+    const int64_t nseq = n_seqs(d);
+    if (S <= 1 || nseq <= 1) return S <= 1 ? 0 : nseq;
+    const ChunkStats cs = chunk_stats(d);
+    const int64_t per = (cs.longest + S - 1) / S;
+    const int64_t rest = (cs.total - cs.longest) / (nseq - 1);  // the others' mean, in chunks
+    return rest > per ? nseq : 1;
+}
+
+namespace {
+
 int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     const int64_t nseq = n_seqs(d);
     const ChunkStats cs = chunk_stats(d);
@@ -294,6 +308,27 @@ int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     for (int S = 2; S <= kMaxSegments && S <= cps; ++S) {
         const int64_t per = (cps + S - 1) / S;
         if (S > 2 && (cps + S - 2) / (S - 1) == per) continue;  // same runs as S - 1
+        // the delta rule's forward keeps one segment length for all sequences:
+        // when the others fit one segment, only the longest is pre-scanned and
+        // composed, and the output pass runs the others whole
+        if (!beta_free && split_seqs(d, S) < nseq) {
+            // the pre-scan: the long sequence's H x S chains, in waves when
+            // both summaries share a CTA; the output pass: the longest chain,
+            // or the spread of all chunk steps plus one whole short chain at
+            // its tail (measured, 16K + 31 short x 4 heads, S = 12 / 16 / 24
+            // / 32: output pass 53 / 43 / 45 / 53 us)
+            const int64_t segs = d.H * (int64_t)S;
+            const double pre = prescan_split_kinds(segs) ? t_pre * (double)per
+                                                         : 8.0 + t_pre * (double)per * waves(segs);
+            const double rest = (double)(cs.total - cps) / (double)(nseq - 1);
+            const double out = t_out * std::max((double)per, steps / (double)sms + rest);
+            const double est = pre + out + compose_plan(d, S, true).cost_us;
+            if (est < best) {
+                best = est;
+                best_s = S;
+            }
+            continue;
+        }
         // segment chains: the longest sequence's S, the mean one's as many
         // as its chunks allow
         const int64_t segs = nseq * d.H * tiles * std::min<int64_t>(S, std::max<int64_t>(cs.mean, 1));
@@ -329,7 +364,7 @@ bool tc_shape(const gdr_dims &d, bool beta_free) {
 // tensor-core pass, G >= 2 for its two-level form in groups of G segments.
 int compose_of(const gdr_dims &d, bool beta_free, int path, int S) {
     if (path != 2 || beta_free || S <= 1) return 0;
-    const ComposePlan c = compose_plan(d, S);
+    const ComposePlan c = compose_plan(d, S, true);
     return c.kind == 0 ? 0 : c.kind == 1 ? 1 : c.grp_size;
 }
 
@@ -415,7 +450,7 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     };
     L.off_tab = take(sizeof(int32_t) * 4 * (size_t)mc);
     L.off_seq0 = take(sizeof(int32_t) * (size_t)(ns + 1));
-    L.off_nchunks = take(sizeof(int32_t) * kNumCtr);
+    L.off_nchunks = take(sizeof(int32_t) * kNumCtrSlots);
     L.off_order = take(sizeof(int32_t) * (size_t)ns);
     L.off_G = take(simt ? sizeof(float) * (size_t)mc * H * kChunk : 0);
     L.off_W = take(simt && delta ? sizeof(float) * (size_t)mc * H * kChunk * K : 0);
@@ -430,7 +465,8 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
     L.off_rec = take(simt || !delta ? 0 : (size_t)mc * H * 74752u);  // paths 2 and 3
     // the tensor-core composition's transition images, and the two-level
     // form's group transitions and offsets (tensor-core paths, delta rule)
-    const ComposePlan cp = (!simt && delta && S > 1) ? compose_plan(d, S) : ComposePlan{0, 0, 0.0};
+    const ComposePlan cp =
+        (!simt && delta && S > 1) ? compose_plan(d, S, path == 2) : ComposePlan{0, 0, 0.0};
     L.seg_images = cp.kind != 0;
     L.off_segMimg = take(L.seg_images ? segs * 65536u : 0);
     L.grp_size = cp.grp_size;
@@ -450,11 +486,14 @@ WorkspaceLayout workspace_layout(const gdr_dims &d, bool beta_free, int S, int p
 // / two levels: 64K tokens x 8 heads at S = 19: 51 / 47 / 51; 64K x 1 head
 // at S = 54: 92 / 113 / 65; 16K x 16 heads at S = 9: 41 / 29 / 45; a
 // 16K-token sequence among 31 short ones x 4 heads at S = 7: 154 / 33 / 107.
-ComposePlan compose_plan(const gdr_dims &d, int S) {
-    const int64_t heads = n_seqs(d) * d.H, sms = device_sms();
+// With one common segment length the tensor-core passes' runs of unsplit
+// sequences end at once: their waves count the split sequences' heads.
+ComposePlan compose_plan(const gdr_dims &d, int S, bool common) {
+    const int64_t all = n_seqs(d) * d.H, sms = device_sms();
+    const int64_t heads = common ? split_seqs(d, S) * d.H : all;
     auto waves = [&](int64_t n) { return (double)((n + sms - 1) / sms); };
-    const int64_t cc = heads * (d.V / 4) <= sms ? 4 : heads * (d.V / 8) <= sms ? 8 : 16;
-    ComposePlan c{0, 0, (cc == 4 ? 1.8 : cc == 8 ? 2.6 : 4.4) * waves(heads * (d.V / cc)) * S};
+    const int64_t cc = all * (d.V / 4) <= sms ? 4 : all * (d.V / 8) <= sms ? 8 : 16;
+    ComposePlan c{0, 0, (cc == 4 ? 1.8 : cc == 8 ? 2.6 : 4.4) * waves(all * (d.V / cc)) * S};
     if (d.K != 128 || d.V != 128) return c;
     const double one = 11.6 + 1.87 * S * waves(heads);
     if (one < c.cost_us) c = ComposePlan{1, 0, one};
@@ -584,7 +623,7 @@ int run_compose_tc(const Problem &p, const Workspace &ws, cudaStream_t st, Launc
 
 int run_simt(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStream_t st,
              LaunchRecorder &rec) {
-    GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
+    GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, false, st));
     GDR_LAUNCH(rec, kKPrep, simt_prep(p, ws, st));
     if (plan.n_segments <= 1) {
         GDR_LAUNCH(rec, kKScanSerial, simt_scan(p, ws, 0, plan.bv, st));
@@ -602,9 +641,13 @@ int run_simt(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaSt
     return GDR_OK;
 }
 
-int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStream_t st,
-           LaunchRecorder &rec) {
-    GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
+// The delta rule cuts every sequence into runs of one common length (the
+// chunk table fixes it), so shorter sequences run whole in the output pass;
+// split: the sequences that rule cuts (split_seqs), for the pre-scan's form.
+int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, int64_t split,
+           cudaStream_t st, LaunchRecorder &rec) {
+    GDR_LAUNCH(rec, kKChunkTable,
+               simt_chunk_table(p, ws, p.beta != nullptr && plan.n_segments > 1, st));
     if (p.beta == nullptr) {
         if (plan.n_segments <= 1) {
             GDR_LAUNCH(rec, kKTcGlaSerial, tc_gla(p, ws, 0, st));
@@ -619,7 +662,7 @@ int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStre
     if (plan.n_segments <= 1) {
         GDR_LAUNCH(rec, kKTcSerial, tc_chain(p, ws, 0, st));
     } else {
-        if (prescan_split_kinds(p.N * plan.n_segments * p.H))
+        if (prescan_split_kinds(split * plan.n_segments * p.H))
             GDR_LAUNCH(rec, kKTcPre, tc_chain(p, ws, 1, st));
         else
             GDR_LAUNCH(rec, kKTcPreDual, tc_prescan(p, ws, st));
@@ -637,7 +680,7 @@ int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaStre
 // and backward kernels.
 int run_bwd(const Problem &p, const Workspace &ws, const BwdArgs &a, const BwdWs &bw, int bv,
             int route, cudaStream_t st, LaunchRecorder &rec) {
-    GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, true, st));
+    GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, false, st));
     if (route == 2) {
         GDR_LAUNCH(rec, kKTcPrep, tc_prep(p, ws, st));
         if (ws.n_segments <= 1) {
@@ -890,7 +933,8 @@ int gdr_chunk_fwd_ex(const gdr_dims *dims, const void *q, const void *k, const v
         owned = true;
     }
     const Workspace ws = carve_workspace(base, L, plan.n_segments);
-    rc = plan.path == 2 ? run_tc(p, ws, plan, st, rec) : run_simt(p, ws, plan, st, rec);
+    rc = plan.path == 2 ? run_tc(p, ws, plan, split_seqs(*dims, plan.n_segments), st, rec)
+                        : run_simt(p, ws, plan, st, rec);
     if (conv) {
         if (rc == GDR_OK && (rec.begin(kKConvertOut) != cudaSuccess ||
                              convert_bf16_to_f16(p.o, o_f16, nvo, st) != cudaSuccess ||

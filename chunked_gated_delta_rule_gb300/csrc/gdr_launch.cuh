@@ -28,7 +28,13 @@ struct ComposePlan {
     int kind, grp_size;
     double cost_us;
 };
-ComposePlan compose_plan(const gdr_dims &d, int S);
+// common: one segment length for every sequence (the tensor-core forward),
+// so only the sequences longer than it take part (split_seqs).
+ComposePlan compose_plan(const gdr_dims &d, int S, bool common);
+// Sequences a split into S segments of one common length (ceil(longest / S)
+// chunks) cuts, from the host's length statistics: the longest alone when
+// the others' mean fits one segment, else all of them.
+int64_t split_seqs(const gdr_dims &d, int S);
 
 // path 1: CUDA-core path (chunk table, G, W, U, h_pre, v_new, segments);
 // path 2: tensor-core path (chunk table, records and segment summaries);
@@ -105,7 +111,9 @@ struct LaunchRecorder {
 };
 
 // ---- CUDA-core FP32 path (any supported shape; arithmetic in FP32) --------
-cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool check,
+// common: fix one segment length for the call, ceil(longest / S) chunks
+// (gdr_segments.cuh), else every sequence is cut by its own length.
+cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool common,
                              cudaStream_t st);
 cudaError_t simt_prep(const Problem &p, const Workspace &ws, cudaStream_t st);
 // mode 0: serial scan (h0 -> ht), stores hpre / vnew

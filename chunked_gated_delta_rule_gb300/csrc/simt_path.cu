@@ -19,6 +19,7 @@
 // a local state c_s (scan from 0) and a K x K transition M_s (the same scan
 // on identity columns with U = 0), then h_{s+1} = M_s h_s + c_s.
 #include "gdr_internal.cuh"
+#include "gdr_segments.cuh"
 #include "simt_tile.cuh"
 
 namespace gdr {
@@ -55,7 +56,7 @@ __device__ __forceinline__ void report(int32_t *status, int code) {
 // chunk offsets come from a block-wide scan.  Up to kSmemSeqs sequences the
 // counts and offsets live in shared memory; beyond that in global memory.
 constexpr int kSmemSeqs = 8192;
-constexpr int kBuckets = 128;
+constexpr int kBuckets = kOrderBuckets;
 
 __device__ __forceinline__ int chunk_bucket(int c) { return c < kBuckets - 1 ? c : kBuckets - 1; }
 
@@ -65,8 +66,8 @@ __global__ void __launch_bounds__(kThreads) k_chunk_table(const Problem p, int64
                                                           int32_t *__restrict__ seq_chunk0,
                                                           int32_t *__restrict__ n_chunks,
                                                           int32_t *__restrict__ seq_order,
-                                                          int32_t *status) {
-    __shared__ int s_bad;
+                                                          int common_S, int32_t *status) {
+    __shared__ int s_bad, s_longest;
     __shared__ int s_hist[kBuckets];
     __shared__ long long s_part[kThreads / 32];
     __shared__ int s_c0[kSmemSeqs + 1];
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(kThreads) k_chunk_table(const Problem p, int64
     pdl_trigger();  // the first kernel of a call: launched in stream order, it waits for nothing
     for (int b = tid; b < kBuckets; b += kThreads) s_hist[b] = 0;
     if (tid < kNumCtr - 1) n_chunks[1 + tid] = 0;
+    if (tid == 0) s_longest = 0;
     if (tid == 0) s_bad = (is_varlen_p(p) && (seq_bound(p, 0) != 0 || seq_bound(p, N) != T)) ? 1 : 0;
     __syncthreads();
     // this thread's run of sequences, their chunk counts and the histogram
@@ -91,6 +93,7 @@ __global__ void __launch_bounds__(kThreads) k_chunk_table(const Problem p, int64
         c0[n] = cc;
         local += cc;
         atomicAdd(&s_hist[chunk_bucket(cc)], 1);
+        atomicMax(&s_longest, cc);
     }
     // block-wide exclusive scan of the runs' chunk totals
     long long incl = local;
@@ -118,6 +121,9 @@ __global__ void __launch_bounds__(kThreads) k_chunk_table(const Problem p, int64
     }
     if (tid == 0) {
         *n_chunks = bad ? 0 : (int32_t)total;
+        // the common segment length (at least 1), or 0 for the own-length rule
+        n_chunks[kCtrSegLen] =
+            bad || !common_S ? 0 : max(1, (s_longest + common_S - 1) / common_S);
         if (bad) report(status, GDR_ERR_SEQLENS);
     }
     if (bad) {
@@ -677,10 +683,11 @@ cudaError_t set_smem(F *f, size_t bytes) {
 
 }  // namespace
 
-cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool /*check*/,
+cudaError_t simt_chunk_table(const Problem &p, const Workspace &ws, bool common,
                              cudaStream_t st) {
     k_chunk_table<<<1, kThreads, 0, st>>>(p, p.N, p.T, ws.max_chunks, ws.chunk_tab,
-                                          ws.seq_chunk0, ws.n_chunks, ws.seq_order, p.status);
+                                          ws.seq_chunk0, ws.n_chunks, ws.seq_order,
+                                          common ? ws.n_segments : 0, p.status);
     return cudaGetLastError();
 }
 

@@ -191,6 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd_scan(const __grid_consta
                         c.valid = 1;
                         break;
                     }
+                    // the sequence's later ids are empty too: skip them for all
+                    atomicMax(counter, (id / H / S + 1) * S * H);
                 }
                 const int slot = posted % kRing;
                 if (posted >= kRing && !wait(kBCempty + slot, (uint32_t)(posted / kRing - 1)))

@@ -49,6 +49,7 @@
 // the segment pre-scan with a K x K transition (cuLA PR #127 "Summary",
 // "Root cause and implementation").
 #include "gdr_internal.cuh"
+#include "gdr_segments.cuh"
 #include "tc_chunk.cuh"
 #include "tma_host.cuh"
 
@@ -108,10 +109,11 @@ enum : int {
 };
 
 // One chain of the work list, decoded: (sequence n, segment s, head h[,
-// transition]); valid == 0 ends the list.
+// transition]); valid == 0 ends the list; whole: an output-pass chain over
+// a whole unsplit sequence (common segment length), from h0 to ht.
 struct ChainDesc {
     int64_t n, tstart, tlen;  // the sequence's first token row and length
-    int h, s, trans, c_begin, s0, s1, valid, pad;
+    int h, s, trans, c_begin, s0, s1, valid, whole;
 };
 static_assert(sizeof(ChainDesc) == 56, "chain descriptor layout");
 constexpr uint32_t kOffBar = kOffRing + 64 * kRing;
@@ -238,19 +240,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                     const int nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
                     c.s0 = 0;
                     c.s1 = nc;
+                    c.whole = 0;
                     if (!kFromH0) {
-                        const int per = (nc + S - 1) / S;
+                        const int per = seg_per(ws, nc);
                         c.s0 = c.s * per;
                         c.s1 = min(nc, c.s0 + per);
+                        // with one segment length, a sequence no longer than it
+                        // has no pre-scan chain; its output chain runs it whole
+                        if (seg_len(ws) && nc <= per) {
+                            if (MODE == kModePre) {
+                                // and so do all after it in the exact order
+                                if (whole_from_here(ws, nc, per)) {
+                                    atomicMax(counter, total);
+                                    break;
+                                }
+                                c.s1 = c.s0;
+                            } else {
+                                c.whole = 1;
+                            }
+                        }
                     }
                     // the serial scan also takes a sequence without tokens
-                    // (its final state is its initial one)
-                    if (c.s0 < c.s1 || MODE == kModeSerial) {
+                    // (its final state is its initial one), and so does the
+                    // output chain of a whole one
+                    if (c.s0 < c.s1 || MODE == kModeSerial || (c.whole && c.s == 0)) {
                         c.tstart = seq_start(p, c.n);
                         c.tlen = seq_end(p, c.n) - c.tstart;
                         c.valid = 1;
                         break;
                     }
+                    // the sequence's later ids are empty too: skip them for all
+                    atomicMax(counter, (r + 1) * S * kinds * H);
                 }
                 const int slot = posted % kRing;
                 if (posted >= kRing && !wait(kBCempty + slot, (uint32_t)(posted / kRing - 1)))
@@ -378,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                         for (int kk = 0; kk < 64; ++kk) {
                             const int key = 64 * hq + kk;
                             float v = 0.f;
-                            if (kFromH0) {
+                            if (kFromH0 || C.whole) {
                                 if (p.h0) v = p.h0[st_base + (p.state_vk ? key : key * kD)];
                             } else if (kFromSeg) {
                                 v = ws.segH[(seg_base * kD + key) * kD + row];
@@ -491,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 if (!wait(kBHdone, gk)) { ok = false; break; }
             }
             if (!ok) break;
-            if (MODE == kModeSerial && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
+            if ((MODE == kModeSerial || C.whole) && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
                 if (p.ht) {
                     for (int key = 0; key < kD; ++key) {
                         const int64_t idx = st_base + (p.state_vk ? key : key * kD);
@@ -500,13 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_chain(const __grid_constant_
                 }
                 continue;
             }
-            if (MODE == kModePre || (MODE == kModeSerial && p.ht)) {
+            const bool to_ht = (MODE == kModeSerial || (MODE == kModeSegOut && C.whole)) && p.ht;
+            if (MODE == kModePre || to_ht) {
                 tc_fence_after();
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float hv[32];
                     tmem_load32f(tmem + lane + kColS + 32 * q, hv);
-                    if (MODE == kModeSerial) {  // compile-time strides in either layout
+                    if (to_ht) {  // compile-time strides in either layout
                         float *dst = p.ht + st_base + (p.state_vk ? 32 * q : 32 * q * kD);
                         if (p.state_vk) {
 #pragma unroll

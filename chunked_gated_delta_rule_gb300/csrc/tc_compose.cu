@@ -38,6 +38,7 @@
 // step counter.  Every wait is time-bounded: on expiry the CTA records
 // GDR_ERR_TIMEOUT in the status word and every role leaves.
 #include "gdr_internal.cuh"
+#include "gdr_segments.cuh"
 #include "tc_chunk.cuh"
 
 namespace gdr {
@@ -89,14 +90,8 @@ struct Run {
     int kind;     // level 1: 0 the group's transition, 1 its offset
     int b0, e;    // the group's segments [b0, e) (levels 1 and 3)
     int nsteps;   // -1: nothing to do
+    int stop;     // nothing to do for this run and every later one
 };
-
-__device__ __forceinline__ int seq_nseg(const Workspace &ws, int64_t n) {
-    const int S = ws.n_segments;
-    const int nc = ws.seq_chunk0[n + 1] - ws.seq_chunk0[n];
-    const int per = (nc + S - 1) / S;
-    return per ? (nc + per - 1) / per : 0;
-}
 
 __device__ __forceinline__ int64_t n_runs(const Problem &p, const Workspace &ws, int level) {
     const int64_t heads = p.N * p.H;
@@ -120,8 +115,17 @@ __device__ Run decode(const Problem &p, const Workspace &ws, int level, int64_t 
     const int h = (int)(r % H);
     const int64_t n = ws.seq_order[r / H];
     u.nh = n * H + h;
-    u.nseg = seq_nseg(ws, n);
+    const int nc = ws.seq_chunk0[n + 1] - ws.seq_chunk0[n];
+    const int per = seg_per(ws, nc);
+    u.nseg = per ? (nc + per - 1) / per : 0;
     const bool ht = p.ht != nullptr;
+    // at most one segment under the common length: the output pass runs the
+    // sequence whole, from h0 to ht (and, in the exact order, every later one)
+    if (seg_len(ws) && u.nseg <= 1) {
+        u.nsteps = -1;
+        u.stop = whole_from_here(ws, nc, per) ? 1 : 0;
+        return u;
+    }
     if (level == 0) {
         u.nsteps = u.nseg == 0 ? 0 : u.nseg - 1 + (ht ? 1 : 0);
     } else {
@@ -255,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
             bool ok = true;
             for (int64_t r = blockIdx.x; ok && r < runs; r += gridDim.x) {
                 const Run u = decode(p, ws, level, r);
+                if (u.stop) break;
                 for (int j = 0; j < u.nsteps; ++j, ++g) {
                     // the images, straight into a buffer once it is free
                     const uint32_t b = g & 1;
@@ -276,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
             bool ok = true;
             for (int64_t r = blockIdx.x; ok && r < runs; r += gridDim.x) {
                 const Run u = decode(p, ws, level, r);
+                if (u.stop) break;
                 for (int j = 0; j < u.nsteps; ++j, ++g) {
                     const uint32_t b = g & 1, bd = g % kND;
                     if (!wait(kBIready + b, g >> 1) || !wait(kBCready + bd, g / kND)) {
@@ -324,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
         bool ok = true;
         for (int64_t r = blockIdx.x; ok && r < runs; r += gridDim.x) {
             const Run u = decode(p, ws, level, r);
+            if (u.stop) break;
             for (int j = 0; j < u.nsteps; ++j, ++g) {
                 const uint32_t bd = g % kND;
                 const bool got = g < (uint32_t)kND || wait_ahead(kBDfree + bd, g / kND - 1);
@@ -371,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_compose(const __grid_constan
         };
         for (int64_t r = blockIdx.x; ok && r < runs; r += gridDim.x) {
             const Run u = decode(p, ws, level, r);
+            if (u.stop) break;
             if (u.nsteps < 0) continue;
             const int64_t slot = u.nh * ngm + u.grp;  // level 1: the group's result
             // Where X (element (rr, c) at dst[rr * rstride]) goes after step j

@@ -197,6 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                         c.valid = 1;
                         break;
                     }
+                    // the sequence's later ids are empty too: skip them for all
+                    atomicMax(counter, (r + 1) * S * H * VT);
                 }
                 const int slot = posted % kRing;
                 if (posted >= kRing && !wait(kGCempty + slot, (uint32_t)(posted / kRing - 1))) {

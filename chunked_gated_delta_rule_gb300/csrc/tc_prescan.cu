@@ -25,6 +25,7 @@
 // GDR_ERR_TIMEOUT in the status word, the other roles leave too, and the
 // CTA exits.
 #include "gdr_internal.cuh"
+#include "gdr_segments.cuh"
 #include "tc_chunk.cuh"
 #include "tma_host.cuh"
 
@@ -151,15 +152,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prescan(const __grid_constan
                     c.n = ws.seq_order[r];
                     c.c_begin = ws.seq_chunk0[c.n];
                     const int nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
-                    const int per = (nc + S - 1) / S;
+                    const int per = seg_per(ws, nc);
                     c.s0 = c.s * per;
                     c.s1 = min(nc, c.s0 + per);
+                    // a sequence within the common segment length runs whole in
+                    // the output pass, and so do all after it in the exact order
+                    if (whole_from_here(ws, nc, per)) {
+                        atomicMax(counter, total);
+                        break;
+                    }
+                    if (seg_len(ws) && nc <= per) c.s1 = c.s0;
                     if (c.s0 < c.s1) {
                         c.tstart = seq_start(p, c.n);
                         c.tlen = seq_end(p, c.n) - c.tstart;
                         c.valid = 1;
                         break;
                     }
+                    // the sequence's later ids are empty too: skip them for all
+                    atomicMax(counter, (r + 1) * S * H);
                 }
                 const int slot = posted % kRing;
                 if (posted >= kRing && !wait(kPCempty + slot, (uint32_t)(posted / kRing - 1)))

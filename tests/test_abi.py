@@ -206,9 +206,11 @@ def test_plan_keys_on_the_longest_sequence():
     skew = (1, 26304, 4, 128, 128)  # one 16K-token sequence and 31 of 320 tokens
     assert pkg.gdr_plan_query(*skew, N=32)["n_segments"] == 1
     assert pkg.gdr_plan_query(*skew, N=32, max_len=16384)["n_segments"] > 1
-    # with 16 heads and 100 short sequences the composition would run in 85
-    # waves (1.1 ms measured at 3 segments against 0.88 ms serial): serial
-    assert pkg.gdr_plan_query(1, 50360, 16, 128, 128, N=101, max_len=16384)["n_segments"] == 1
+    # with 16 heads and 100 short sequences too: one segment length for all
+    # sequences leaves the short ones whole, so only the long one's 16 heads
+    # are pre-scanned and composed
+    skew16 = pkg.gdr_plan_query(1, 50360, 16, 128, 128, N=101, max_len=16384)
+    assert skew16["n_segments"] > 1 and skew16["compose"] == 1
     assert pkg.gdr_plan_query(1, 10456, 16, 128, 128, N=32, max_len=512)["n_segments"] == 1
     # a hint longer than the batch is clamped to it: one sequence of T tokens
     assert (pkg.gdr_plan_query(1, 16384, 16, 128, 128, N=1, max_len=1 << 40)

@@ -116,7 +116,7 @@ def test_measured_traffic_stays_near_the_algorithmic_bytes():
                                       N=x["N"] if x["cu_seqlens"] is not None else 0,
                                       dtype={"f32": 0, "bf16": 1, "f16": 2}[x["dtype"]],
                                       beta_free=x["beta"] is None)
-            cache[w] = (x, b.counts(x, plan["n_segments"]))
+            cache[w] = (x, b.counts(x, plan["n_segments"], b.common_segments(x, plan)))
         x, c = cache[w]
         if backward:
             a = b.bwd_algorithmic(k, x, c)[0]

@@ -123,6 +123,39 @@ def test_many_short_sequences_delta(S):
           force_path=2)
 
 
+@pytest.mark.parametrize("S", [8, 16])
+def test_common_segment_length(S):
+    """One segment length for every sequence, ceil(longest / S) chunks: the
+    long sequence is split; sequences of exactly that length or shorter
+    (empty, one token, ragged) run whole in the output pass from h0 to ht;
+    one a token longer is split into a full segment and a one-token one."""
+    w = synthetic.small(W["wide_varlen_bf16"], H=2, with_h0=True)
+    per = -(-47 // S)  # 3000 tokens: 47 chunks
+    lens = [3000, 64 * per, 64 * per + 1, 0, 1, 200]
+    check(synthetic.make_inputs(w, lengths=lens), n_segments=S, force_path=2)
+
+
+@pytest.mark.parametrize("case", ["two_long", "default_plan"])
+def test_common_segment_length_long_sequences(case):
+    """Two sequences of 127 chunks or more (the sequence order's top bucket,
+    where it does not rank them): the segment length follows the longer one
+    (201 chunks, 26 a segment at S = 8), the other splits into 5; a
+    sequence of exactly 26 chunks runs whole.  Then a skewed batch at the
+    default plan, which splits the long sequence only."""
+    w = synthetic.small(W["wide_varlen_bf16"], H=1, with_h0=True)
+    if case == "two_long":
+        lens = [130 * 64 - 5, 200 * 64 + 7, 300, 0, 64 * 26]
+        check(synthetic.make_inputs(w, lengths=lens), n_segments=8, force_path=2)
+    else:
+        w = synthetic.small(W["skewed_varlen_h4_bf16"], H=2, with_h0=True)
+        lens = [8192] + [128 + 37 * i for i in range(12)]
+        x = synthetic.make_inputs(w, lengths=lens)
+        import chunked_gated_delta_rule_gb300 as pkg
+        assert pkg.gdr_plan_query(1, sum(lens), 2, 128, 128, N=len(lens), dtype=1,
+                                  max_len=8192)["n_segments"] > 1
+        check(x)
+
+
 @pytest.mark.parametrize("S", [2, 8])
 def test_segment_prescan_both_kernels(S):
     """Multi-chunk ragged segments, an empty sequence: at 4 heads, S = 2 runs
