@@ -112,10 +112,13 @@ def test_measured_traffic_stays_near_the_algorithmic_bytes():
         backward = w.startswith("bwd_")  # a backward-pass kernel, on workload w[4:]
         if w not in cache:
             x = synthetic.make_inputs(synthetic.WORKLOADS[w[4:] if backward else w])
+            cu = x["cu_seqlens"]
             plan = pkg.gdr_plan_query(x["B"], x["T"], x["H"], x["K"], x["V"],
-                                      N=x["N"] if x["cu_seqlens"] is not None else 0,
+                                      N=x["N"] if cu is not None else 0,
                                       dtype={"f32": 0, "bf16": 1, "f16": 2}[x["dtype"]],
-                                      beta_free=x["beta"] is None)
+                                      beta_free=x["beta"] is None,
+                                      max_len=int((cu[1:] - cu[:-1]).max()) if cu is not None
+                                      else 0)
             cache[w] = (x, b.counts(x, plan["n_segments"], b.common_segments(x, plan)))
         x, c = cache[w]
         if backward:
