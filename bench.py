@@ -225,8 +225,8 @@ def counts(x, n_segments=1, common=False):
 
 def common_segments(x, plan):
     """The plan cuts sequences at one common segment length (the tensor-core
-    delta forward)."""
-    return plan.get("path") == 2 and x["beta"] is not None
+    forward, either mode)."""
+    return plan.get("path") == 2
 
 
 REC_BYTES = 57616  # bytes of one record written by tc_prep and read by the scan (k aside)
@@ -244,8 +244,8 @@ def algorithmic_bytes(kernel, x, c):
         return th * ((2 * K + V) * es + 4 + (4 if delta else 0) + V * es) + states
     if kernel == "tc_chain_serial":  # the records and k read, o written, states
         return th * (K + V) * es + ch * REC_BYTES + states
-    if kernel == "tc_gla_prescan":  # k, v, g read; c_s written
-        return th * ((K + V) * es + 4) + c["segments"] * K * V * 4
+    if kernel == "tc_gla_prescan":  # k, v, g of the split sequences read; c_s written
+        return c["split_token_heads"] * ((K + V) * es + 4) + c["segments"] * K * V * 4
     if kernel == "tc_gla_segment_out":  # q, k, v, g read, o written, h_s read
         return th * ((2 * K + V) * es + 4 + V * es) + c["segments"] * K * V * 4
     if kernel == "compose_scalar":  # c_s, d_s read; h_s written; h0 / ht

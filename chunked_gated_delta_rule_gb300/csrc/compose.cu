@@ -190,8 +190,11 @@ __global__ void __launch_bounds__(256) k_compose_scalar(Problem p, Workspace ws)
     const int64_t n = nh / p.H;
     const int S = ws.n_segments;
     const int nc = ws.seq_chunk0[n + 1] - ws.seq_chunk0[n];
-    const int per = (nc + S - 1) / S;
+    const int per = seg_per(ws, nc);
     const int nseg = per ? (nc + per - 1) / per : 0;
+    // at most one segment under the common length: the output pass runs it
+    // whole, from h0 to ht
+    if (seg_len(ws) && nseg <= 1) return;
     const float *__restrict__ C = ws.segC + nh * S * kv + e;
     float *__restrict__ Hs = ws.segH + nh * S * kv + e;
     const float *__restrict__ D = ws.segD + nh * S;

@@ -308,21 +308,27 @@ int auto_segments(const gdr_dims &d, bool beta_free, int path, int bv) {
     for (int S = 2; S <= kMaxSegments && S <= cps; ++S) {
         const int64_t per = (cps + S - 1) / S;
         if (S > 2 && (cps + S - 2) / (S - 1) == per) continue;  // same runs as S - 1
-        // the delta rule's forward keeps one segment length for all sequences:
+        // the tensor-core forward keeps one segment length for all sequences:
         // when the others fit one segment, only the longest is pre-scanned and
         // composed, and the output pass runs the others whole
-        if (!beta_free && split_seqs(d, S) < nseq) {
+        if (split_seqs(d, S) < nseq) {
             // the pre-scan: the long sequence's H x S chains, in waves when
             // both summaries share a CTA; the output pass: the longest chain,
             // or the spread of all chunk steps plus one whole short chain at
             // its tail (measured, 16K + 31 short x 4 heads, S = 12 / 16 / 24
             // / 32: output pass 53 / 43 / 45 / 53 us)
-            const int64_t segs = d.H * (int64_t)S;
-            const double pre = prescan_split_kinds(segs) ? t_pre * (double)per
-                                                         : 8.0 + t_pre * (double)per * waves(segs);
+            const int64_t segs = d.H * tiles * (int64_t)S;
+            const double pre = beta_free                  ? t_pre * (double)per * waves(segs)
+                               : prescan_split_kinds(segs) ? t_pre * (double)per
+                                                           : 8.0 + t_pre * (double)per * waves(segs);
             const double rest = (double)(cs.total - cps) / (double)(nseq - 1);
             const double out = t_out * std::max((double)per, steps / (double)sms + rest);
-            const double est = pre + out + compose_plan(d, S, true).cost_us;
+            // the beta-free composition walks the split sequences' states only
+            // (the others' threads leave at once)
+            const double split_mb = state_mb * (double)split_seqs(d, S) / (double)nseq;
+            const double comp = beta_free ? std::max(0.5, 0.65 * split_mb) * S
+                                          : compose_plan(d, S, true).cost_us;
+            const double est = pre + out + comp;
             if (est < best) {
                 best = est;
                 best_s = S;
@@ -641,13 +647,12 @@ int run_simt(const Problem &p, const Workspace &ws, const gdr_plan &plan, cudaSt
     return GDR_OK;
 }
 
-// The delta rule cuts every sequence into runs of one common length (the
-// chunk table fixes it), so shorter sequences run whole in the output pass;
+// A split cuts every sequence into runs of one common length (the chunk
+// table fixes it), so shorter sequences run whole in the output pass;
 // split: the sequences that rule cuts (split_seqs), for the pre-scan's form.
 int run_tc(const Problem &p, const Workspace &ws, const gdr_plan &plan, int64_t split,
            cudaStream_t st, LaunchRecorder &rec) {
-    GDR_LAUNCH(rec, kKChunkTable,
-               simt_chunk_table(p, ws, p.beta != nullptr && plan.n_segments > 1, st));
+    GDR_LAUNCH(rec, kKChunkTable, simt_chunk_table(p, ws, plan.n_segments > 1, st));
     if (p.beta == nullptr) {
         if (plan.n_segments <= 1) {
             GDR_LAUNCH(rec, kKTcGlaSerial, tc_gla(p, ws, 0, st));

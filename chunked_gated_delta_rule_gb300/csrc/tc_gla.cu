@@ -29,6 +29,7 @@
 // Every wait is time-bounded: on expiry the CTA records GDR_ERR_TIMEOUT in
 // the status word, the other roles leave too, and the CTA exits.
 #include "gdr_internal.cuh"
+#include "gdr_segments.cuh"
 #include "tc_chunk.cuh"
 #include "tma_host.cuh"
 
@@ -48,10 +49,12 @@ struct GlaArgs {
 constexpr int kThreads = 320;  // warps 0-3 state, 4-7 side, 8 control, 9 producer
 constexpr int kRing = 3;       // decoded chains handed out ahead
 
-// One chain of the work list, decoded; valid == 0 ends the list.
+// One chain of the work list, decoded; valid == 0 ends the list; whole: an
+// output-pass chain over a whole unsplit sequence (common segment length),
+// from h0 to ht.
 struct GlaDesc {
     int64_t n, tstart, tlen;  // the sequence's first token row and length
-    int h, s, vt, c_begin, s0, s1, valid, pad;
+    int h, s, vt, c_begin, s0, s1, valid, whole;
 };
 static_assert(sizeof(GlaDesc) == 56, "chain descriptor layout");
 
@@ -184,14 +187,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                     const int nc = ws.seq_chunk0[c.n + 1] - c.c_begin;
                     c.s0 = 0;
                     c.s1 = nc;
+                    c.whole = 0;
                     if (MODE != kModeSerial) {
-                        const int per = (nc + S - 1) / S;
+                        const int per = seg_per(ws, nc);
                         c.s0 = c.s * per;
                         c.s1 = min(nc, c.s0 + per);
+                        // with one segment length, a sequence no longer than it
+                        // has no pre-scan chain; its output chain runs it whole
+                        if (seg_len(ws) && nc <= per) {
+                            if (MODE == kModePre) {
+                                // and so do all after it in the exact order
+                                if (whole_from_here(ws, nc, per)) {
+                                    atomicMax(counter, total);
+                                    break;
+                                }
+                                c.s1 = c.s0;
+                            } else {
+                                c.whole = 1;
+                            }
+                        }
                     }
                     // the serial scan also takes a sequence without tokens
-                    // (its final state is its initial one)
-                    if (c.s0 < c.s1 || MODE == kModeSerial) {
+                    // (its final state is its initial one), and so does the
+                    // output chain of a whole one
+                    if (c.s0 < c.s1 || MODE == kModeSerial || (c.whole && c.s == 0)) {
                         c.tstart = seq_start(p, c.n);
                         c.tlen = seq_end(p, c.n) - c.tstart;
                         c.valid = 1;
@@ -357,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                         for (int kk = 0; kk < 64; ++kk) {
                             const int key = 64 * q + kk;
                             float x = 0.f;
-                            if (MODE == kModeSerial) {
+                            if (MODE == kModeSerial || C.whole) {
                                 if (p.h0) x = p.h0[st_base + key * st_step];
                             } else if (MODE == kModeSegOut) {
                                 x = ws.segH[(seg_base * KD + key) * V + v0 + row];
@@ -396,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                 if (!wait(kGHdone, gk)) { ok = false; break; }
             }
             if (!ok) break;
-            if (MODE == kModeSerial && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
+            if ((MODE == kModeSerial || C.whole) && C.s0 == C.s1) {  // no tokens: ht = h0 (or 0)
                 if (p.ht) {
                     for (int key = 0; key < KD; ++key) {
                         const int64_t idx = st_base + key * st_step;
@@ -405,7 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
                 }
                 continue;
             }
-            if (MODE != kModeSegOut && (MODE != kModeSerial || p.ht)) {
+            const bool to_ht = (MODE == kModeSerial || C.whole) && p.ht;
+            if (MODE == kModePre || to_ht) {
                 tc_fence_after();
 #pragma unroll 1
                 for (int q = 0; q < KD / 32; ++q) {
@@ -414,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gla(const __grid_constant__ 
 #pragma unroll
                     for (int kk = 0; kk < 32; ++kk) {
                         const int key = 32 * q + kk;
-                        if (MODE == kModeSerial)
+                        if (to_ht)
                             p.ht[st_base + key * st_step] = hv[kk];
                         else
                             ws.segC[(seg_base * KD + key) * V + v0 + row] = hv[kk];

@@ -211,6 +211,11 @@ def test_plan_keys_on_the_longest_sequence():
     # are pre-scanned and composed
     skew16 = pkg.gdr_plan_query(1, 50360, 16, 128, 128, N=101, max_len=16384)
     assert skew16["n_segments"] > 1 and skew16["compose"] == 1
+    # the beta-free mode alike (K = 256, V = 512, 4 heads): its composition
+    # walks the long sequence's states only
+    gla = (1, 26005, 4, 256, 512)
+    assert pkg.gdr_plan_query(*gla, N=32, beta_free=True, max_len=16384)["n_segments"] > 1
+    assert pkg.gdr_plan_query(*gla, N=32, beta_free=True)["n_segments"] == 1
     assert pkg.gdr_plan_query(1, 10456, 16, 128, 128, N=32, max_len=512)["n_segments"] == 1
     # a hint longer than the batch is clamped to it: one sequence of T tokens
     assert (pkg.gdr_plan_query(1, 16384, 16, 128, 128, N=1, max_len=1 << 40)

@@ -135,6 +135,18 @@ def test_common_segment_length(S):
     check(synthetic.make_inputs(w, lengths=lens), n_segments=S, force_path=2)
 
 
+@pytest.mark.parametrize("S", [4, 16])
+def test_common_segment_length_beta_free(S):
+    """The beta-free mode at one segment length for every sequence: the long
+    sequence is split into ceil(40 / S)-chunk runs (two 128-column value
+    tiles, K = 128); shorter ones, an empty one and one of exactly that
+    length run whole in the output pass from h0 to ht."""
+    w = synthetic.small(W["gla_k256_v512_bf16"], K=128, V=256, H=2, with_h0=True)
+    per = -(-40 // S)  # 2540 tokens: 40 chunks
+    lens = [2540, 64 * per, 64 * per + 1, 0, 1, 90]
+    check(synthetic.make_inputs(w, lengths=lens), n_segments=S, force_path=2)
+
+
 @pytest.mark.parametrize("case", ["two_long", "default_plan"])
 def test_common_segment_length_long_sequences(case):
     """Two sequences of 127 chunks or more (the sequence order's top bucket,
