@@ -132,3 +132,24 @@ def test_measured_traffic_stays_near_the_algorithmic_bytes():
         assert t <= 1.25 * a, (k, w, t / a)
         checked += 1
     assert checked >= 25
+
+
+def test_segment_counts_under_both_cutting_rules():
+    """The units the roofline numerators count, for a varlen batch cut into
+    S = 8 runs: each sequence's own length (ceil(chunks / 8) chunks a run)
+    against one common length (ceil(47 / 8) = 6 chunks a run, the tensor-core
+    forward), under which sequences of at most 6 chunks stay whole and only
+    the 47- and 7-chunk sequences are split (8 + 2 runs)."""
+    import torch
+    b = _bench()
+    lens = [3000, 384, 385, 0, 1, 200]  # 47, 6, 7, 0, 1, 4 chunks
+    cu = torch.tensor([0] + list(torch.tensor(lens).cumsum(0).tolist()), dtype=torch.int32)
+    x = {"H": 2, "cu_seqlens": cu, "T": sum(lens), "B": 1}
+    own = b.counts(x, 8)
+    common = b.counts(x, 8, common=True)
+    assert own["segments"] == 2 * (8 + 6 + 7 + 0 + 1 + 4)
+    assert common["segments"] == 2 * (8 + 2)
+    assert common["split_chunk_heads"] == 2 * (47 + 7)
+    assert common["split_token_heads"] == 2 * (3000 + 385)
+    assert own["split_chunk_heads"] == own["chunk_heads"] == 2 * 65
+    assert b.counts(x, 1, common=True)["segments"] == 0
