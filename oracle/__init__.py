@@ -216,15 +216,17 @@ def affine(k, v, g, beta=None, lib=None):
     return M, c
 
 
-def segment_bounds(n_tokens: int, n_segments: int, chunk: int = CHUNK):
+def segment_bounds(n_tokens: int, n_segments: int, chunk: int = CHUNK, per=None):
     """Token ranges of the segments of one sequence: runs of
     ceil(n_chunks / S) whole 64-token chunks; a sequence with fewer chunks
     than S uses fewer segments (the reading taken where the pages leave the
-    split rule open)."""
+    split rule open).  ``per`` fixes the run length in chunks instead (one
+    common length for a whole batch, the other reading of that rule)."""
     n_chunks = -(-n_tokens // chunk)
     if n_chunks == 0:
         return []
-    per = -(-n_chunks // max(1, n_segments))
+    if per is None:
+        per = -(-n_chunks // max(1, n_segments))
     out = []
     c0 = 0
     while c0 < n_chunks:
@@ -235,11 +237,13 @@ def segment_bounds(n_tokens: int, n_segments: int, chunk: int = CHUNK):
 
 
 def forward_segmented(q, k, v, g, beta=None, cu_seqlens=None, h0=None,
-                      n_segments=2, scale=None, lib=None):
+                      n_segments=2, scale=None, lib=None, common=False):
     """Serial result rebuilt through the segment split: per (sequence, head)
     each segment's affine summary (M_s, c_s) from :func:`affine`, the ordered
     composition h_{s+1} = M_s h_s + c_s, then each segment's outputs from its
-    composed initial state by :func:`forward`.  Returns (o, ht)."""
+    composed initial state by :func:`forward`.  ``common``: every sequence
+    cut into runs of ceil(longest sequence's chunks / S) chunks, a shorter
+    sequence left as one run.  Returns (o, ht)."""
     q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(g)
     beta, h0 = _f64(beta), _f64(h0)
     B, T, H, K = q.shape
@@ -253,10 +257,14 @@ def forward_segmented(q, k, v, g, beta=None, cu_seqlens=None, h0=None,
     N = len(spans)
     o = np.full((B, T, H, V), np.nan)
     ht = np.zeros((N, H, K, V))
+    per = None
+    if common:
+        longest = max([-(-(t1 - t0) // CHUNK) for (_, t0, t1) in spans] + [0])
+        per = max(1, -(-longest // max(1, n_segments)))
     for n, (row, t0, t1) in enumerate(spans):
         for hh in range(H):
             h = h0[n, hh].copy() if h0 is not None else np.zeros((K, V))
-            for (s0, s1) in segment_bounds(t1 - t0, n_segments):
+            for (s0, s1) in segment_bounds(t1 - t0, n_segments, per=per):
                 a, b = t0 + s0, t0 + s1
                 sl = (slice(row, row + 1), slice(a, b), slice(hh, hh + 1))
                 bo, _, _ = forward(q[sl], k[sl], v[sl], g[sl],

@@ -247,6 +247,23 @@ def test_segment_split_composition(S, delta):
     assert pf.rel(sht, ht) < 1e-10
 
 
+@pytest.mark.parametrize("S", [2, 4, 16])
+@pytest.mark.parametrize("delta", [True, False])
+def test_segment_split_common_length(S, delta):
+    """One run length for the whole batch (ceil(longest / S) chunks): the
+    short sequences stay one run, the long one is cut; the composition still
+    rebuilds the serial result."""
+    rng = np.random.default_rng(100 + S)
+    lengths = [64 * 9 + 5, 64, 0, 70, 130]
+    c = rand_case(rng, H=2, K=6, V=5, lengths=lengths, delta=delta)
+    o, ht = run_oracle(c)
+    so, sht = oracle.forward_segmented(c["q"], c["k"], c["v"], c["g"], c["beta"],
+                                       cu_seqlens=c["cu"], h0=c["h0"], n_segments=S,
+                                       common=True)
+    assert pf.rel(so, o) < 1e-10
+    assert pf.rel(sht, ht) < 1e-10
+
+
 def test_affine_map_matches_recurrence():
     """M h_in + c equals the recurrence run from h_in, for random h_in."""
     rng = np.random.default_rng(21)
@@ -264,6 +281,9 @@ def test_segment_bounds():
     assert oracle.segment_bounds(65, 4) == [(0, 64), (64, 65)]
     assert oracle.segment_bounds(64 * 16, 16) == [(64 * i, 64 * (i + 1)) for i in range(16)]
     assert oracle.segment_bounds(64 * 10, 4) == [(0, 192), (192, 384), (384, 576), (576, 640)]
+    # a common run length: 3 chunks a run whatever the sequence's own length
+    assert oracle.segment_bounds(64 * 2 + 1, 4, per=3) == [(0, 129)]
+    assert oracle.segment_bounds(64 * 7, 4, per=3) == [(0, 192), (192, 384), (384, 448)]
 
 
 def test_pair_mask_limits_work():
