@@ -179,6 +179,11 @@ def test_plan_query_is_deterministic_and_valid():
             (1, 65536, 1, 128, 128, False): 54, (2, 8192, 4, 256, 512, True): 4}
     for (B, T, H, K, V, bf), s in best.items():
         assert pkg.gdr_plan_query(B, T, H, K, V, beta_free=bf)["n_segments"] == s
+    # and for the two skewed batches (one 16K-token sequence among short
+    # ones, the max_len hint given) at the common segment length: 9 of
+    # 6 / 8 / 9 / 12 / 16 at 16 heads, 16 of 12 / 16 / 24 / 32 at 4 heads
+    assert pkg.gdr_plan_query(1, 50360, 16, 128, 128, N=101, max_len=16384)["n_segments"] == 9
+    assert pkg.gdr_plan_query(1, 26421, 4, 128, 128, N=32, max_len=16384)["n_segments"] == 16
 
 
 def test_plan_reports_the_composition():
