@@ -179,7 +179,10 @@ typedef struct gdr_options {
  *   cu_seqlens  NULL selects the dense layout.
  *   h0          NULL: zero initial state.   ht  NULL: final state not written.
  *   n_segments  0: plan chooses; 1: serial scan; S > 1: split every sequence
- *               into runs of ceil(chunks / S) whole chunks.  At most 64 for
+ *               into runs of whole chunks: ceil(longest sequence's chunks /
+ *               S) a run on the tensor-core path (a sequence no longer than
+ *               that stays one run, taken whole from h0 to ht), ceil(own
+ *               chunks / S) on the CUDA-core path.  At most 64 for
  *               the delta rule; at most 4096 in the beta-free mode, where a
  *               count at or above the chunk count gives every chunk its own
  *               segment: the chunk-parallel producer dataflow of
