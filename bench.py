@@ -200,7 +200,7 @@ def counts(x, n_segments=1, common=False):
     else:
         lens = [x["T"]] * x["B"]
     chunks = sum((L + 63) // 64 for L in lens)
-    segs = groups = split_tokens = split_chunks = 0
+    segs = groups = split_tokens = split_chunks = split_seqs = 0
     S = max(1, n_segments)
     G = 0 if S < 4 else int(S ** 0.5)  # the two-level composition's group size
     longest = max([(L + 63) // 64 for L in lens] + [0])
@@ -217,10 +217,11 @@ def counts(x, n_segments=1, common=False):
         if ns:
             split_tokens += L
             split_chunks += nc
+            split_seqs += 1
     return dict(tokens=sum(lens), token_heads=sum(lens) * H, chunk_heads=chunks * H,
                 seq_heads=len(lens) * H, n_seqs=len(lens), chunks=chunks, segments=segs * H,
                 groups=groups * H, split_token_heads=split_tokens * H,
-                split_chunk_heads=split_chunks * H)
+                split_chunk_heads=split_chunks * H, split_seq_heads=split_seqs * H)
 
 
 def common_segments(x, plan):
@@ -238,6 +239,10 @@ def algorithmic_bytes(kernel, x, c):
     delta = x["beta"] is not None
     th, ch, sh = c["token_heads"], c["chunk_heads"], c["seq_heads"]
     states = sh * K * V * 4 * ((1 if x["h0"] is not None else 0) + 1)
+    # h0 / ht of the sequences a split composes (all of them but the empty
+    # ones under each sequence's own run length; the split ones under a
+    # common length, whose output pass takes the others whole)
+    cstates = c["split_seq_heads"] * K * V * 4 * ((1 if x["h0"] is not None else 0) + 1)
     if kernel in ("call", "tc_gla_serial"):
         # whole forward pass: q, k, v, g, beta read once, o written once,
         # h0 / ht once
@@ -249,13 +254,13 @@ def algorithmic_bytes(kernel, x, c):
     if kernel == "tc_gla_segment_out":  # q, k, v, g read, o written, h_s read
         return th * ((2 * K + V) * es + 4 + V * es) + c["segments"] * K * V * 4
     if kernel == "compose_scalar":  # c_s, d_s read; h_s written; h0 / ht
-        return c["segments"] * (2 * K * V * 4 + 4) + states
+        return c["segments"] * (2 * K * V * 4 + 4) + cstates
     if kernel in ("compose_delta", "tc_compose"):  # M_s, c_s read; h_s written; h0 / ht
-        return c["segments"] * ((K * K if delta else 1) + 2 * K * V) * 4 + states
+        return c["segments"] * ((K * K if delta else 1) + 2 * K * V) * 4 + cstates
     if kernel == "tc_compose_groups":  # M_s, c_s read; a group's transition and offset written
         return c["segments"] * (K * K + K * V) * 4 + c["groups"] * (K * K + K * V) * 4
     if kernel == "tc_compose_top":  # group transitions and offsets read; group states, h0 / ht
-        return c["groups"] * (K * K + 2 * K * V) * 4 + states
+        return c["groups"] * (K * K + 2 * K * V) * 4 + cstates
     if kernel == "tc_compose_fill":  # M_s, c_s read; h_s written
         return c["segments"] * (K * K + 2 * K * V) * 4
     rec = ch * REC_BYTES  # per-chunk records of the tensor-core prep kernel
@@ -712,7 +717,7 @@ def rooflines(x, c, m, hbm, workload):
 # statement (64K at 8 and 1 heads) and a batch with one long sequence.
 CONFIG_WORKLOADS = ("tiny_dense_f32", "wide_varlen_bf16", "long_16k_bf16", "stress_64k_h8_bf16",
                     "stress_64k_h1_bf16", "gla_k256_v512_bf16", "skewed_varlen_bf16",
-                    "skewed_varlen_h4_bf16")
+                    "skewed_varlen_h4_bf16", "skewed_gla_h4_bf16")
 
 
 def config_record(pkg, name, dev, steps, flush, hbm):

@@ -77,6 +77,10 @@ WORKLOADS = {
     # the long sequence's, so splitting it pays.
     "skewed_varlen_h4_bf16": Workload("skewed_varlen_h4_bf16", 1, 0, 4, 128, 128, "bf16",
                                       n_seqs=32, len_lo=128, len_hi=512, long_len=16384),
+    # The same skew in the beta-free geometry (K = 256, V = 512, h0 in).
+    "skewed_gla_h4_bf16": Workload("skewed_gla_h4_bf16", 1, 0, 4, 256, 512, "bf16",
+                                   n_seqs=32, len_lo=128, len_hi=512, long_len=16384,
+                                   delta=False, with_h0=True),
     # The wide varlen batch with FP16 q / k / v.
     "wide_varlen_f16": Workload("wide_varlen_f16", 1, 0, 16, 128, 128,
                                 "f16", n_seqs=32, len_lo=128, len_hi=512),

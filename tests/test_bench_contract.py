@@ -153,3 +153,7 @@ def test_segment_counts_under_both_cutting_rules():
     assert common["split_token_heads"] == 2 * (3000 + 385)
     assert own["split_chunk_heads"] == own["chunk_heads"] == 2 * 65
     assert b.counts(x, 1, common=True)["segments"] == 0
+    # the states a composition touches: the split sequences' (common length)
+    # or every non-empty one's (own length)
+    assert common["split_seq_heads"] == 2 * 2
+    assert own["split_seq_heads"] == 2 * 5

@@ -67,3 +67,12 @@ def test_skewed_varlen_h4(S):
     """One 16K-token sequence (number 16) among 31 short ones at 4 heads: the
     longest-sequence hint makes the plan split (S = 0)."""
     check("skewed_varlen_h4_bf16", pairs=[(16, 0), (16, 3), (0, 1), (31, 2)], n_segments=S)
+
+
+@pytest.mark.parametrize("S", [0, 1])
+def test_skewed_gla_h4(S):
+    """The beta-free mode (K = 256, V = 512, h0 in) on one 16K-token sequence
+    (number 16) among 31 short ones: the plan splits the long sequence alone
+    at the common segment length (S = 0); pairs on the long sequence and on
+    short ones."""
+    check("skewed_gla_h4_bf16", pairs=[(16, 0), (16, 3), (0, 1), (31, 2)], n_segments=S)
